@@ -1,0 +1,161 @@
+"""fp64 CPU oracle of the NAtS-L hybrid attention layer forward.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package; the library product
+never does.  It wraps ``nats_oracle.cpp`` (plain C++17, float64, one thread per
+(batch, head)) through ctypes.  It shares no code with the CUDA path.
+
+Every function follows "Neural Attention Search Linear (NAtS-L)", technical
+summary, section "Kernmechanismen", items 1, 3 and 4; the readings taken where
+the page is silent are listed in ``oracle/README.md``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "nats_oracle.cpp")
+_LIB = os.path.join(_HERE, "libnats_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class _Dims(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("L", ctypes.c_int32),
+        ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("chunk", ctypes.c_int32),
+        ("scale", ctypes.c_double), ("eps", ctypes.c_double),
+    ]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with g++ (no GPU needed).  Returns the library path."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["g++", "-O2", "-std=c++17", "-shared", "-fPIC", "-pthread", _SRC, "-o", tmp]
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            lib.nats_oracle_select.argtypes = [ctypes.POINTER(_Dims), P, P, P, P, P, P, ctypes.c_int32]
+            lib.nats_oracle_select.restype = ctypes.c_int
+            lib.nats_oracle_forward.argtypes = [ctypes.POINTER(_Dims)] + [P] * 13 + [
+                ctypes.c_int32, P, P, P, P, P, P, P, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]
+            lib.nats_oracle_forward.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f32(x):
+    if x is None:
+        return None
+    return np.ascontiguousarray(x, dtype=np.float32)
+
+
+def _ptr(x):
+    return None if x is None else ctypes.c_void_p(x.ctypes.data)
+
+
+def _dims(B, H, L, dk, dv, chunk, scale, eps):
+    return _Dims(B, H, L, dk, dv, chunk, float(scale), float(eps))
+
+
+def select(q, k, w_s, b_s=None, chunk: int = 64, threads: int = 0):
+    """Score-layer selection for every (b, h).
+
+    q, k: [B, H, L, dk]; w_s: [H, 2, 2dk]; b_s: [H, 2] or None.
+    Returns (sel uint8 [B, H, N] with 0 = softmax, 1 = Gated DeltaNet,
+    scores float64 [B, H, N, 2]).
+    """
+    lib = _load()
+    q, k, w_s, b_s = _f32(q), _f32(k), _f32(w_s), _f32(b_s)
+    B, H, L, dk = q.shape
+    N = (L + chunk - 1) // chunk
+    sel = np.zeros((B, H, N), np.uint8)
+    scores = np.zeros((B, H, N, 2), np.float64)
+    d = _dims(B, H, L, dk, dk, chunk, 0.0, 1e-6)
+    rc = lib.nats_oracle_select(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(w_s), _ptr(b_s),
+                                _ptr(sel), _ptr(scores), int(threads))
+    if rc != 0:
+        raise RuntimeError(f"nats_oracle_select failed ({rc})")
+    return sel, scores
+
+
+def forward(q, k, v, g, beta, w_s, b_s, w_g, b_g=None, *, chunk: int = 64, scale: float = 0.0,
+            eps: float = 1e-6, norm_w_soft=None, norm_w_lin=None, sel_in=None, heads=None,
+            rows=None, outputs=("sel", "scores", "o_s", "o_l", "out", "state"), threads: int = 0):
+    """Layer forward in float64.
+
+    Shapes: q, k [B, H, L, dk]; v [B, H, L, dv]; g, beta [B, H, L]; w_s [H, 2, 2dk];
+    b_s [H, 2]; w_g [H, dk]; b_g [H]; norm weights [dv]; sel_in [B, H, N] uint8.
+    heads: iterable of (b, h) pairs or flat indices (default: all, in order).
+    rows: optional [L] bool mask of the rows whose softmax output and merged
+    output are computed (others are NaN).
+    Returns a dict with the requested outputs, each packed over the listed
+    heads: sel [n, N], scores [n, N, 2], o_s / o_l / out [n, L, dv], state
+    [n, dv, dk]; plus "threads" (threads used).
+    """
+    lib = _load()
+    q, k, v, g, beta = _f32(q), _f32(k), _f32(v), _f32(g), _f32(beta)
+    w_s, b_s, w_g, b_g = _f32(w_s), _f32(b_s), _f32(w_g), _f32(b_g)
+    nws, nwl = _f32(norm_w_soft), _f32(norm_w_lin)
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    N = (L + chunk - 1) // chunk
+    if heads is None:
+        flat = np.arange(B * H, dtype=np.int32)
+    else:
+        flat = np.array([h if np.isscalar(h) else h[0] * H + h[1] for h in heads], dtype=np.int32)
+    n = len(flat)
+    res = {}
+    want = set(outputs)
+    res_sel = np.zeros((n, N), np.uint8) if "sel" in want else None
+    res_scores = np.zeros((n, N, 2), np.float64) if "scores" in want else None
+    fill = np.nan if rows is not None else 0.0
+    res_os = np.full((n, L, dv), fill) if "o_s" in want else None
+    res_ol = np.zeros((n, L, dv)) if "o_l" in want else None
+    res_out = np.full((n, L, dv), fill) if "out" in want else None
+    res_state = np.zeros((n, dv, dk)) if "state" in want else None
+    sel_arr = None if sel_in is None else np.ascontiguousarray(sel_in, np.uint8).reshape(B * H, N)
+    rows_arr = None if rows is None else np.ascontiguousarray(rows, np.uint8).reshape(L)
+    used = ctypes.c_int32(0)
+    d = _dims(B, H, L, dk, dv, chunk, scale, eps)
+    rc = lib.nats_oracle_forward(
+        ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(w_s), _ptr(b_s),
+        _ptr(w_g), _ptr(b_g), _ptr(nws), _ptr(nwl), _ptr(sel_arr), _ptr(flat), n, _ptr(rows_arr),
+        _ptr(res_sel), _ptr(res_scores), _ptr(res_os), _ptr(res_ol), _ptr(res_out),
+        _ptr(res_state), int(threads), ctypes.byref(used))
+    if rc != 0:
+        raise RuntimeError(f"nats_oracle_forward failed ({rc})")
+    for name, arr in (("sel", res_sel), ("scores", res_scores), ("o_s", res_os), ("o_l", res_ol),
+                      ("out", res_out), ("state", res_state)):
+        if arr is not None:
+            res[name] = arr
+    res["threads"] = used.value
+    return res
+
+
+def forward_inputs(inp, **kw):
+    """forward() on a gen.NatsInputs workload."""
+    return forward(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.w_s, inp.b_s, inp.w_g, inp.b_g,
+                   chunk=inp.chunk, **kw)
+
+
+def select_inputs(inp, threads: int = 0):
+    """select() on a gen.NatsInputs workload."""
+    return select(inp.q, inp.k, inp.w_s, inp.b_s, chunk=inp.chunk, threads=threads)
