@@ -1,0 +1,408 @@
+#!/usr/bin/env python
+"""Throughput of the NAtS-L hybrid attention layer forward on GB300.
+
+One step = one full layer forward (score + select, compaction, softmax
+branch, Gated DeltaNet prep + scan with commit / rollback, RMSNorm + gated
+merge) over one batch of the 1.3B-scale workload: B=4, H=16, L=8192,
+d_k=d_v=128, chunk 64, bf16, 25 % softmax chunks chosen by the score layer.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+With N > 1 it runs under torchrun, one rank per GPU: every rank processes its
+own batch (independent (b, h) units, no collective on the data path; weak
+scaling) and rank 0 prints one JSON line with the max-over-ranks time.
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload on the host cores (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "hybrid-attn fwd tokens/s on 1 GB300 and % of tensor-core roofline (L=8192)"
+WORKLOAD = "l8192"
+WORKLOAD_DESC = ("NAtS-L layer forward, 1.3B-scale: B=4 H=16 L=8192 d_k=d_v=128 chunk=64, bf16 Q/K/V "
+                 "~N(0,1) with unit keys, fp32 g/beta, 25% softmax chunks chosen by the score layer")
+C = 64
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("native", "reference"), default="native")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- peaks ----
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ------------------------------------------------------- algorithmic work ----
+
+def algorithmic_work(sel, B, H, L, d, in_bytes):
+    """FLOPs of the dense contractions the method computes, from the actual selection.
+
+    softmax: 4 d per (query, visible key) pair; pairs of chunk c =
+      C^2 * nprev[c] + C (C + 1) / 2.
+    Gated DeltaNet per chunk: 5 C^2 d (QK^T, KK^T, T.bV, T.bgK, P.Delta with
+      triangular halves) + 6 C d^2 (W S^T, Q S^T, Delta^T K).
+    """
+    import numpy as np
+
+    soft = (sel == 0).astype(np.int64)
+    nprev = np.cumsum(soft, axis=-1) - soft
+    N = sel.shape[-1]
+    pairs = C * C * int(nprev.sum()) + B * H * N * C * (C + 1) // 2
+    f_soft = 4 * d * pairs
+    f_gdn = B * H * N * (5 * C * C * d + 6 * C * d * d)
+    return {"flops_softmax": float(f_soft), "flops_gdn": float(f_gdn),
+            "flops_total": float(f_soft + f_gdn), "bytes_io": float(in_bytes),
+            "softmax_fraction": float(soft.mean())}
+
+
+# --------------------------------------------------------------- clocks ----
+
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index, enabled=True):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"nats_clocks_{os.getpid()}.csv")
+        if not enabled:
+            return
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(gpu_index)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------ traffic ----
+
+def recorded_traffic(kernel_src):
+    """DRAM bytes per launch of the softmax kernel from the committed ncu summary,
+    valid only while the kernel source is unchanged (hash match)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        kv = dict(x.split("=", 1) for x in line.split() if "=" in x)
+        if kv.get("src") == os.path.basename(kernel_src) and kv.get("sha") == h and kv.get("workload") == WORKLOAD:
+            return float(kv["dram_bytes_per_launch"])
+    return None
+
+
+# ------------------------------------------------------------- oracle ----
+
+def oracle_sample(inp, n_heads, threads):
+    """Wall time of the oracle on the first n_heads (b, h) heads, all rows."""
+    import oracle
+
+    oracle.build()
+    heads = list(range(n_heads))
+    t0 = time.perf_counter()
+    r = oracle.forward_inputs(inp, heads=heads, outputs=("out",), threads=threads)
+    dt = time.perf_counter() - t0
+    return dt, r["threads"]
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# -------------------------------------------------------------- arms ----
+
+def run_reference(args, rank):
+    """The oracle on the host cores: each step is n heads (one per core) of the workload."""
+    if rank != 0:
+        return None
+    import gen
+
+    inp = gen.config_inputs(WORKLOAD)
+    cores = cpu_cores()
+    n = min(cores, inp.B * inp.H)
+    for _ in range(args.warmup):
+        oracle_sample(inp, n, cores)
+    times = []
+    used = cores
+    for _ in range(args.steps):
+        dt, used = oracle_sample(inp, n, cores)
+        times.append(dt)
+    total = sum(times)
+    tokens_per_step = n * inp.L / inp.H  # n of the B*H (b, h) head-rows of L tokens
+    value = tokens_per_step * args.steps / total
+    sample = f"{n} of {inp.B * inp.H} (b,h) heads, all {inp.L} rows, per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_native(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import gen
+    import linear_attention_nats_gb300 as nats
+    from linear_attention_nats_gb300 import _native
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    cfg = dict(gen.CONFIGS[WORKLOAD])
+    cfg["seed"] = cfg["seed"] + 1000 * rank  # every rank its own batch
+    inp = gen.make_inputs(name=WORKLOAD, **cfg)
+    B, H, L, d = inp.B, inp.H, inp.L, inp.d
+    N = L // C
+
+    host = {}
+    for n in ("q", "k", "v"):
+        host[n] = torch.from_numpy(getattr(inp, n)).to(torch.bfloat16)  # exact: values are bf16
+    for n in ("g", "beta", "w_s", "b_s", "w_g", "b_g"):
+        host[n] = torch.from_numpy(np.ascontiguousarray(getattr(inp, n)))
+    dv = {n: t.to(dev) for n, t in host.items()}
+    out = torch.empty_like(dv["q"])
+    sel = torch.empty((B, H, N), dtype=torch.uint8, device=dev)
+    dm = nats.dims(B, H, L, d, nats.NATS_BF16)
+    ws_bytes = int(_native.lib.nats_workspace_size(ctypes.byref(dm)))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+    def call(tensors, prof=None):
+        code = _native.lib.nats_hybrid_fwd_profiled(
+            ctypes.byref(dm), P(tensors["q"]), P(tensors["k"]), P(tensors["v"]), P(tensors["g"]),
+            P(tensors["beta"]), P(tensors["w_s"]), P(tensors["b_s"]), P(tensors["w_g"]), P(tensors["b_g"]),
+            None, None, None, P(out), P(sel), None, None, None, P(ws), ctypes.c_size_t(ws_bytes),
+            ctypes.c_void_p(stream.cuda_stream), ctypes.byref(prof) if prof is not None else None)
+        if code != 0:
+            raise _native.NatsError(code, "nats_hybrid_fwd_profiled")
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 0)):
+        call(dv)
+    torch.cuda.synchronize()
+    sel_h = sel.cpu().numpy()
+    in_bytes = sum(t.numel() * t.element_size() for n, t in dv.items() if n in ("q", "k", "v", "g", "beta")) \
+        + out.numel() * out.element_size()
+    work = algorithmic_work(sel_h, B, H, L, d, in_bytes)
+
+    # ---- device-resident timed region: K back-to-back steps ----
+    stage_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in _native.STAGES] for _ in range(args.steps)]
+    for row in stage_ev:  # materialise the event handles
+        for a, b in row:
+            a.record(stream)
+            b.record(stream)
+    profs = []
+    for row in stage_ev:
+        p = _native.Profile()
+        for i, (a, b) in enumerate(row):
+            p.start[i] = a.cuda_event
+            p.stop[i] = b.cuda_event
+        profs.append(p)
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    clocks = Clocks(local_rank, enabled=not args.no_clocks and rank == 0)
+    barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        call(dv, profs[i])
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_stop)
+    launches = sum(p.launches for p in profs)
+    stage_ms = {}
+    for si, name in enumerate(_native.STAGES):
+        vals = [row[si][0].elapsed_time(row[si][1]) for row in stage_ev]
+        stage_ms[name] = sum(vals) / len(vals)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    tokens = B * L * world
+    value = tokens / (ms_step / 1e3)
+
+    # ---- end to end: pinned host buffers in, result out, copies timed ----
+    e2e = None
+    if not args.no_e2e:
+        pin = {n: t.pin_memory() for n, t in host.items()}
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = out_h.numel() * out_h.element_size()
+        staged = {n: torch.empty_like(t) for n, t in dv.items()}
+
+        def e2e_step():
+            for n in pin:
+                staged[n].copy_(pin[n], non_blocking=True)
+            call(staged)
+            out_h.copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ems = e0.elapsed_time(e1)
+        if dist is not None:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": tokens / (ems / args.steps / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+        launches_e2e = None  # noqa: F841 (counted in gpu_launches only for the device-timed region)
+
+    pk = peaks()
+    soft_ms = stage_ms["softmax"]
+    achieved = work["flops_softmax"] / (soft_ms / 1e3) / 1e12
+    peak_tc = pk["bf16_tflops_sustained"]
+    roofline = {"kernel": "softmax branch (NATS_STAGE_SOFTMAX)", "bound": "tensor",
+                "achieved": achieved, "peak": peak_tc, "unit": "TFLOP/s", "frac": achieved / peak_tc,
+                "peak_source": f"{pk['source']} bf16 sustained",
+                "traffic": recorded_traffic(os.path.join(ROOT, "linear_attention_nats_gb300", "csrc",
+                                                         "softmax_simt.cu")),
+                "flops_per_launch": work["flops_softmax"], "ms_per_launch": soft_ms}
+    layer_tflops = work["flops_total"] / (ms_step / 1e3) / 1e12 / world
+    res = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "global_batch": B * world, "seq_len": L,
+                   "parallelism": f"replicas x{world} ((b,h) units per rank, no collective)",
+                   "l2": "inputs larger than L2: Q/K/V 384 MiB + workspace per step, no explicit flush",
+                   "softmax_fraction": work["softmax_fraction"]},
+        "roofline": roofline,
+        "layer_roofline": {"bound": "tensor", "achieved": layer_tflops, "peak": peak_tc,
+                           "unit": "TFLOP/s", "frac": layer_tflops / peak_tc,
+                           "flops_per_step": work["flops_total"]},
+        "stages_ms": stage_ms,
+        "gpu_launches": launches,
+        "e2e": e2e,
+        "clocks": clk,
+    }
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
+    if not args.no_cpu_baseline and world == 1 and rank == 0:
+        cores = cpu_cores()
+        n = min(2 * cores, B * H)
+        dt, used = oracle_sample(inp, n, cores)
+        res["cpu_baseline"] = {"value": n * L / H / dt, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                               "sample": f"{n} of {B * H} (b,h) heads of the workload, all {L} rows "
+                                         f"({dt:.1f} s wall)"}
+    return res
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        res = run_reference(args, rank)
+        print(json.dumps(res), flush=True)
+        return 0
+    import __graft_entry__
+
+    __graft_entry__.build()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_native(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -82,21 +82,26 @@ class NatsInputs:
 
 
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
-    """Round float32 values to the nearest bfloat16 (ties to even), kept as float32."""
+    """Round float32 values to the nearest bfloat16 (ties to even), kept as float32.
+
+    Works in place on a contiguous float32 array (a copy is made otherwise)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     b = x.view(np.uint32)
-    lsb = (b >> np.uint32(16)) & np.uint32(1)
-    r = (b + np.uint32(0x7FFF) + lsb) & np.uint32(0xFFFF0000)
-    return r.view(np.float32)
+    lsb = b >> np.uint32(16)
+    lsb &= np.uint32(1)
+    lsb += np.uint32(0x7FFF)
+    b += lsb
+    b &= np.uint32(0xFFFF0000)
+    return x
 
 
 def bf16_bits(x: np.ndarray) -> np.ndarray:
     """uint16 bit patterns of float32 values that are exactly bf16-representable."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    b = x.view(np.uint32)
-    if np.any(b & np.uint32(0xFFFF)):
+    halves = x.view(np.uint16)  # little-endian: [low, high] per element
+    if np.any(halves[..., 0::2]):
         raise ValueError("values are not bf16-representable; round them first")
-    return (b >> np.uint32(16)).astype(np.uint16)
+    return np.ascontiguousarray(halves[..., 1::2])
 
 
 def _rng(seed: int, stream: int) -> np.random.Generator:
@@ -111,10 +116,11 @@ def _normal(rng, shape, scale=1.0):
 
 
 def _unit_rows(x: np.ndarray) -> np.ndarray:
-    """Scale every vector along the last axis to unit L2 norm (float64 norm)."""
+    """Scale every vector along the last axis to unit L2 norm (in place)."""
     n = np.sqrt(np.einsum("...i,...i->...", x, x, dtype=np.float64))
-    n = np.maximum(n, 1e-30)
-    return (x / n[..., None]).astype(np.float32)
+    inv = (1.0 / np.maximum(n, 1e-30)).astype(np.float32)
+    x *= inv[..., None]
+    return x
 
 
 def _softplus(z: np.ndarray) -> np.ndarray:
@@ -228,7 +234,10 @@ def make_inputs(
         else:
             planted = _pattern_mask(prng, B, H, N, pattern, frac, bursts)
         tok = np.repeat(planted, chunk, axis=2)[:, :, :L]  # [B, H, L]
-        q = q + np.float32(PLANT_ALPHA) * tok[..., None].astype(np.float32) * u[None, :, None, :]
+        shift = np.float32(PLANT_ALPHA) * u  # [H, d]
+        for b in range(B):
+            for h in range(H):
+                q[b, h, tok[b, h]] += shift[h]
         w_s[:, 1] = w1
         w_s[:, 0] = w1 + noise
         w_s[:, 0, :d] += np.float32(PLANT_GAMMA) * u

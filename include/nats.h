@@ -1,0 +1,159 @@
+/*
+ * nats.h - C ABI of libnats, the NAtS-L token-level hybrid attention layer
+ * forward (prefill) for NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("Neural Attention Search Linear (NAtS-L)", technical
+ * summary, section "Kernmechanismen"):
+ *   item 1  The sequence is cut into 64-token chunks.  An Attention Score
+ *           Layer (mean pooling, then a linear layer) gives each chunk one
+ *           score per operation; the highest score picks softmax attention
+ *           (0) or Gated DeltaNet (1) for that chunk.
+ *   item 3  Both branches run over every chunk.  The softmax branch of a
+ *           token attends to the tokens of earlier softmax-selected chunks
+ *           plus its own chunk causally.  The Gated DeltaNet state
+ *           S_t = a_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *           (a_t = exp(g_t), read out as o_t = S_t (scale q_t)) is
+ *           pseudo-updated through every chunk and rolled back to the chunk
+ *           start when the chunk chose softmax.
+ *   item 4  Each branch output is RMS-normalised on its own; the output is
+ *           w N_soft + (1 - w) N_lin with w = sigmoid(q . W_g[h] + b_g[h]).
+ *
+ * Conventions common to every entry point:
+ *   - Layout: Q, K [B, H, L, dk], V and the output [B, H, L, dv], all
+ *     contiguous, row-major, element type `dtype` (bf16 or fp32).  g and
+ *     beta are fp32 [B, H, L].  Selection codes are uint8 [B, H, N] with
+ *     N = L / 64.
+ *   - Every data pointer is a DEVICE pointer owned by the caller; `dims` is
+ *     a host pointer.  The library allocates no device memory, keeps no
+ *     global state and never synchronises the host: all work is enqueued on
+ *     `stream` (0 = the legacy default stream).
+ *   - Arguments are validated on the host before anything is launched; a
+ *     violation returns its status and leaves every output untouched.
+ *   - Launch failures return NATS_ERR_CUDA (from cudaGetLastError).  Errors
+ *     that happen while the kernels run surface, as usual for CUDA, on the
+ *     caller's next synchronising call.
+ *   - No C++ exception crosses this interface.  Distinct calls are
+ *     thread-safe (no shared state); calls that share a workspace must be
+ *     ordered by the caller.
+ *   - Supported shapes: chunk = 64, L % 64 == 0, dk == dv in {64, 128},
+ *     B, H, L >= 0 (any zero extent makes the call a no-op that returns
+ *     NATS_OK).  Q, K, V, the output and the workspace must be 16-byte
+ *     aligned.
+ */
+#ifndef NATS_H_
+#define NATS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st* nats_stream_t;
+
+typedef enum {
+  NATS_OK = 0,
+  NATS_ERR_NULL = 1,        /* a required pointer is NULL */
+  NATS_ERR_SHAPE = 2,       /* negative extent, L % chunk != 0, chunk != 64, dk != dv */
+  NATS_ERR_DTYPE = 3,       /* dtype is not NATS_BF16 / NATS_F32 */
+  NATS_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned */
+  NATS_ERR_WORKSPACE = 5,   /* workspace smaller than nats_workspace_size() */
+  NATS_ERR_UNSUPPORTED = 6, /* head size other than 64 / 128, or a size beyond int32 tiling */
+  NATS_ERR_CUDA = 7,        /* a CUDA runtime call or kernel launch failed */
+  NATS_ERR_INTERNAL = 8,
+  NATS_ERR_VALUE = 9        /* scale or eps negative or not finite */
+} nats_status;
+
+typedef enum { NATS_BF16 = 0, NATS_F32 = 1 } nats_dtype;
+
+typedef struct {
+  int32_t B, H, L; /* batch, heads, tokens per sequence */
+  int32_t dk, dv;  /* key / value head size (equal) */
+  int32_t chunk;   /* must be 64 */
+  int32_t dtype;   /* nats_dtype of Q, K, V and the output */
+  float scale;     /* softmax logit and linear readout scale; 0 => 1/sqrt(dk) */
+  float eps;       /* RMSNorm epsilon (1e-6 in the reference workloads) */
+} nats_dims;
+
+/* Human-readable name of a status code (static storage). */
+const char* nats_status_string(nats_status s);
+
+/* Bytes of device workspace nats_hybrid_fwd needs for `dims` (0 for an
+ * invalid `dims`).  The workspace holds the selection, the compacted
+ * softmax-chunk lists, the per-chunk Gated DeltaNet factors and both branch
+ * outputs; its contents are scratch between calls. */
+size_t nats_workspace_size(const nats_dims* dims);
+
+/* Attention Score Layer + argmax alone ("Kernmechanismen" item 1).
+ *   q, k    [B, H, L, dk] dtype
+ *   w_s     fp32 [H, 2, 2*dk]: row 0 scores softmax, row 1 Gated DeltaNet,
+ *           applied to the chunk mean of [q_t ; k_t] (unscaled q)
+ *   b_s     fp32 [H, 2] or NULL (zero bias)
+ *   sel     uint8 [B, H, N] out: 0 = softmax, 1 = Gated DeltaNet; ties -> 0
+ *   scores  fp32 [B, H, N, 2] out, or NULL */
+nats_status nats_select(const nats_dims* dims, const void* q, const void* k, const float* w_s,
+                        const float* b_s, uint8_t* sel, float* scores, nats_stream_t stream);
+
+/* The whole layer forward ("Kernmechanismen" items 1, 3, 4).
+ *   q, k, v      dtype [B, H, L, d]
+ *   g, beta      fp32 [B, H, L]: log-decay (a_t = exp(g_t)) and write strength
+ *   w_s, b_s     score layer as in nats_select (w_s may be NULL when sel_in is given)
+ *   w_g          fp32 [H, dk] merge-gate projection; b_g fp32 [H] or NULL
+ *   norm_w_soft, norm_w_lin   fp32 [dv] RMSNorm weights, or NULL (unit)
+ *   sel_in       uint8 [B, H, N] or NULL: when given, replaces the score
+ *                layer's choice (values must be 0 or 1)
+ *   out          dtype [B, H, L, dv] out
+ *   sel_out      uint8 [B, H, N] out, or NULL
+ *   state_out    fp32 [B, H, dv, dk] out, or NULL: the Gated DeltaNet state
+ *                after the last chunk (after its commit or rollback)
+ *   o_soft_out, o_lin_out   fp32 [B, H, L, dv] out, or NULL: the branch
+ *                outputs before normalisation (diagnostics)
+ *   workspace    device scratch of at least nats_workspace_size(dims) bytes */
+nats_status nats_hybrid_fwd(const nats_dims* dims, const void* q, const void* k, const void* v,
+                            const float* g, const float* beta, const float* w_s, const float* b_s,
+                            const float* w_g, const float* b_g, const float* norm_w_soft,
+                            const float* norm_w_lin, const uint8_t* sel_in, void* out,
+                            uint8_t* sel_out, float* state_out, float* o_soft_out,
+                            float* o_lin_out, void* workspace, size_t workspace_bytes,
+                            nats_stream_t stream);
+
+/* Stages of nats_hybrid_fwd, for per-stage timing. */
+typedef enum {
+  NATS_STAGE_SCORE = 0,    /* Attention Score Layer + argmax (skipped with sel_in) */
+  NATS_STAGE_COMPACT = 1,  /* prefix counts / compacted softmax-chunk lists */
+  NATS_STAGE_SOFTMAX = 2,  /* softmax branch */
+  NATS_STAGE_GDN_PREP = 3, /* Gated DeltaNet per-chunk factors (parallel over chunks) */
+  NATS_STAGE_GDN_SCAN = 4, /* Gated DeltaNet chunk scan with commit / rollback */
+  NATS_STAGE_MERGE = 5,    /* RMSNorm per branch + gated merge */
+  NATS_NUM_STAGES = 8
+} nats_stage;
+
+/* Caller-owned timing hooks.  start[s] / stop[s] are cudaEvent_t handles
+ * (or NULL); the library records them on `stream` right before the first
+ * and right after the last kernel of stage s.  `launches` is set to the
+ * number of kernels the call launched. */
+typedef struct {
+  void* start[NATS_NUM_STAGES];
+  void* stop[NATS_NUM_STAGES];
+  int32_t launches;
+} nats_profile;
+
+/* nats_hybrid_fwd plus per-stage event records (prof may be NULL, which
+ * makes it identical to nats_hybrid_fwd).  Same arguments, errors and
+ * results; recording an event that fails returns NATS_ERR_CUDA. */
+nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const void* k,
+                                     const void* v, const float* g, const float* beta,
+                                     const float* w_s, const float* b_s, const float* w_g,
+                                     const float* b_g, const float* norm_w_soft,
+                                     const float* norm_w_lin, const uint8_t* sel_in, void* out,
+                                     uint8_t* sel_out, float* state_out, float* o_soft_out,
+                                     float* o_lin_out, void* workspace, size_t workspace_bytes,
+                                     nats_stream_t stream, nats_profile* prof);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NATS_H_ */

@@ -1,0 +1,130 @@
+"""libnats: NAtS-L token-level hybrid attention layer forward on GB300 (sm_103a).
+
+Thin torch-facing binding of the C ABI in include/nats.h.  Tensors must be
+CUDA tensors; work is enqueued on the current torch CUDA stream (or the one
+given).  The functions here only marshal arguments: selection, both branches
+and the merge all run in libnats' CUDA kernels.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _native
+from ._native import NATS_BF16, NATS_F32, NatsError, check, dims  # noqa: F401
+
+__all__ = ["select", "hybrid_fwd", "workspace_size", "NatsError", "dims", "NATS_BF16", "NATS_F32"]
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return NATS_BF16
+    if t.dtype == torch.float32:
+        return NATS_F32
+    raise TypeError(f"unsupported dtype {t.dtype}; use bfloat16 or float32")
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _req(t: Optional[torch.Tensor], name: str, dtype=None, shape=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def workspace_size(B: int, H: int, L: int, d: int, dtype=NATS_BF16) -> int:
+    """Bytes of workspace hybrid_fwd needs (0 for unsupported sizes)."""
+    dm = dims(B, H, L, d, dtype)
+    return int(_native.lib.nats_workspace_size(ctypes.byref(dm)))
+
+
+def select(q, k, w_s, b_s=None, *, scores: bool = False, stream=None):
+    """Chunk selection: uint8 [B, H, L/64] (0 softmax, 1 Gated DeltaNet)."""
+    _req(q, "q")
+    B, H, L, d = q.shape
+    _req(k, "k", q.dtype, q.shape)
+    _req(w_s, "w_s", torch.float32, (H, 2, 2 * d))
+    _req(b_s, "b_s", torch.float32, (H, 2))
+    N = L // 64
+    sel = torch.empty((B, H, N), dtype=torch.uint8, device=q.device)
+    sc = torch.empty((B, H, N, 2), dtype=torch.float32, device=q.device) if scores else None
+    dm = dims(B, H, L, d, _dtype_code(q))
+    check(_native.lib.nats_select(ctypes.byref(dm), _p(q), _p(k), _p(w_s), _p(b_s), _p(sel), _p(sc),
+                                  _stream(stream)), "nats_select")
+    return (sel, sc) if scores else sel
+
+
+def hybrid_fwd(q, k, v, g, beta, w_s, b_s, w_g, b_g=None, *, norm_w_soft=None, norm_w_lin=None,
+               sel_in=None, scale: float = 0.0, eps: float = 1e-6, out=None, workspace=None,
+               return_sel: bool = False, return_state: bool = False,
+               return_branches: bool = False, stream=None):
+    """NAtS-L hybrid attention layer forward.
+
+    q, k, v: [B, H, L, d] bf16 or fp32 (same dtype); g, beta: fp32 [B, H, L];
+    w_s: fp32 [H, 2, 2d]; b_s: fp32 [H, 2] or None; w_g: fp32 [H, d];
+    b_g: fp32 [H] or None; norm weights fp32 [d] or None; sel_in: uint8
+    [B, H, L/64] or None.  Returns `out` alone, or a dict with "out" and the
+    requested "sel", "state" ([B, H, d, d] fp32), "o_soft", "o_lin".
+    """
+    _req(q, "q")
+    B, H, L, d = q.shape
+    N = L // 64
+    for name, t in (("k", k), ("v", v)):
+        _req(t, name, q.dtype, q.shape)
+    _req(g, "g", torch.float32, (B, H, L))
+    _req(beta, "beta", torch.float32, (B, H, L))
+    _req(w_s, "w_s", torch.float32, (H, 2, 2 * d))
+    _req(b_s, "b_s", torch.float32, (H, 2))
+    _req(w_g, "w_g", torch.float32, (H, d))
+    _req(b_g, "b_g", torch.float32, (H,))
+    _req(norm_w_soft, "norm_w_soft", torch.float32, (d,))
+    _req(norm_w_lin, "norm_w_lin", torch.float32, (d,))
+    _req(sel_in, "sel_in", torch.uint8, (B, H, N))
+    dt = _dtype_code(q)
+    dm = dims(B, H, L, d, dt, scale, eps)
+    if out is None:
+        out = torch.empty_like(q)
+    _req(out, "out", q.dtype, q.shape)
+    need = int(_native.lib.nats_workspace_size(ctypes.byref(dm)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _req(workspace, "workspace", torch.uint8)
+    dev = q.device
+    sel = torch.empty((B, H, N), dtype=torch.uint8, device=dev) if return_sel else None
+    state = torch.empty((B, H, d, d), dtype=torch.float32, device=dev) if return_state else None
+    o_soft = torch.empty((B, H, L, d), dtype=torch.float32, device=dev) if return_branches else None
+    o_lin = torch.empty((B, H, L, d), dtype=torch.float32, device=dev) if return_branches else None
+    check(_native.lib.nats_hybrid_fwd(
+        ctypes.byref(dm), _p(q), _p(k), _p(v), _p(g), _p(beta), _p(w_s), _p(b_s), _p(w_g), _p(b_g),
+        _p(norm_w_soft), _p(norm_w_lin), _p(sel_in), _p(out), _p(sel), _p(state), _p(o_soft),
+        _p(o_lin), _p(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream)),
+        "nats_hybrid_fwd")
+    if not (return_sel or return_state or return_branches):
+        return out
+    res = {"out": out}
+    if return_sel:
+        res["sel"] = sel
+    if return_state:
+        res["state"] = state
+    if return_branches:
+        res["o_soft"] = o_soft
+        res["o_lin"] = o_lin
+    return res

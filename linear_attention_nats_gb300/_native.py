@@ -1,0 +1,81 @@
+"""ctypes view of libnats.so (the C ABI declared in include/nats.h).
+
+Argument marshalling only: every step of the layer runs in the CUDA kernels
+behind this library.  There is no fallback: if the library is missing the
+import fails.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libnats.so")
+
+NATS_BF16 = 0
+NATS_F32 = 1
+
+STATUS = {
+    0: "NATS_OK", 1: "NATS_ERR_NULL", 2: "NATS_ERR_SHAPE", 3: "NATS_ERR_DTYPE",
+    4: "NATS_ERR_ALIGN", 5: "NATS_ERR_WORKSPACE", 6: "NATS_ERR_UNSUPPORTED", 7: "NATS_ERR_CUDA",
+    8: "NATS_ERR_INTERNAL", 9: "NATS_ERR_VALUE",
+}
+
+# Every symbol include/nats.h declares.
+EXPORTS = ("nats_status_string", "nats_workspace_size", "nats_select", "nats_hybrid_fwd",
+           "nats_hybrid_fwd_profiled")
+
+NUM_STAGES = 8
+STAGES = ("score", "compact", "softmax", "gdn_prep", "gdn_scan", "merge")
+
+
+class Profile(ctypes.Structure):
+    _fields_ = [("start", ctypes.c_void_p * NUM_STAGES), ("stop", ctypes.c_void_p * NUM_STAGES),
+                ("launches", ctypes.c_int32)]
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("L", ctypes.c_int32),
+        ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("chunk", ctypes.c_int32),
+        ("dtype", ctypes.c_int32), ("scale", ctypes.c_float), ("eps", ctypes.c_float),
+    ]
+
+
+class NatsError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)}")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libnats.so is not built ({LIB_PATH}); run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.c_void_p
+    lib.nats_status_string.argtypes = [ctypes.c_int]
+    lib.nats_status_string.restype = ctypes.c_char_p
+    lib.nats_workspace_size.argtypes = [ctypes.POINTER(Dims)]
+    lib.nats_workspace_size.restype = ctypes.c_size_t
+    lib.nats_select.argtypes = [ctypes.POINTER(Dims), P, P, P, P, P, P, P]
+    lib.nats_select.restype = ctypes.c_int
+    lib.nats_hybrid_fwd.argtypes = [ctypes.POINTER(Dims)] + [P] * 18 + [ctypes.c_size_t, P]
+    lib.nats_hybrid_fwd.restype = ctypes.c_int
+    lib.nats_hybrid_fwd_profiled.argtypes = [ctypes.POINTER(Dims)] + [P] * 18 + [
+        ctypes.c_size_t, P, ctypes.POINTER(Profile)]
+    lib.nats_hybrid_fwd_profiled.restype = ctypes.c_int
+    return lib
+
+
+lib = _load()
+
+
+def dims(B, H, L, d, dtype=NATS_BF16, scale=0.0, eps=1e-6, chunk=64) -> Dims:
+    return Dims(int(B), int(H), int(L), int(d), int(d), int(chunk), int(dtype), float(scale), float(eps))
+
+
+def check(code: int, where: str) -> None:
+    if code != 0:
+        raise NatsError(code, where)

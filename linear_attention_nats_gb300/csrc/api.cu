@@ -1,0 +1,194 @@
+// api.cu - the C ABI of libnats: argument validation, workspace layout and
+// the launch sequence of the NAtS-L hybrid attention layer forward.
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/nats.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace nats {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape / dtype / value checks shared by every entry point.
+nats_status check_dims(const nats_dims* d) {
+  if (!d) return NATS_ERR_NULL;
+  if (d->dtype != NATS_BF16 && d->dtype != NATS_F32) return NATS_ERR_DTYPE;
+  if (d->B < 0 || d->H < 0 || d->L < 0 || d->dk <= 0 || d->dv <= 0) return NATS_ERR_SHAPE;
+  if (d->chunk != kChunk || d->L % kChunk != 0 || d->dk != d->dv) return NATS_ERR_SHAPE;
+  if (d->dk != 64 && d->dk != 128) return NATS_ERR_UNSUPPORTED;
+  if (!std::isfinite(d->scale) || d->scale < 0.f || !std::isfinite(d->eps) || d->eps < 0.f)
+    return NATS_ERR_VALUE;
+  // every flat element offset must fit the int64 / int32 grid arithmetic used below
+  const long long BH = (long long)d->B * d->H;
+  if (BH > (1LL << 31) - 1 || BH * (d->L / kChunk) > (1LL << 31) - 1) return NATS_ERR_UNSUPPORTED;
+  return NATS_OK;
+}
+
+Problem problem_of(const nats_dims* d) {
+  Problem p;
+  p.B = d->B;
+  p.H = d->H;
+  p.L = d->L;
+  p.d = d->dk;
+  p.N = d->L / kChunk;
+  p.BH = (long long)d->B * d->H;
+  p.scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt((float)d->dk);
+  p.eps = d->eps;
+  return p;
+}
+
+// Carves the workspace; returns the bytes needed.  `base` may be null
+// (size query only).
+size_t layout(const Problem& p, char* base, Workspace* ws) {
+  const size_t BH = (size_t)p.BH, N = (size_t)p.N, L = (size_t)p.L, D = (size_t)p.d;
+  const size_t C = kChunk;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    char* ptr = base ? base + off : nullptr;
+    off += align_up(bytes);
+    return ptr;
+  };
+  Workspace w;
+  w.sel = (uint8_t*)take(BH * N);
+  w.nprev = (int32_t*)take(4 * BH * N);
+  w.sel_idx = (int32_t*)take(4 * BH * N);
+  w.G = (float*)take(4 * BH * L);
+  w.W = (float*)take(4 * BH * L * D);
+  w.U = (float*)take(4 * BH * L * D);
+  w.P = (float*)take(4 * BH * N * C * C);
+  w.o_s = (float*)take(4 * BH * L * D);
+  w.o_l = (float*)take(4 * BH * L * D);
+  if (ws) *ws = w;
+  return off;
+}
+
+nats_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NATS_OK : NATS_ERR_CUDA; }
+
+// Optional per-stage event records around each launch group.
+struct Stages {
+  nats_profile* prof;
+  cudaStream_t st;
+  cudaError_t mark(void* const* ev, int s) const {
+    if (!prof || !ev[s]) return cudaSuccess;
+    return cudaEventRecord((cudaEvent_t)ev[s], st);
+  }
+};
+
+#define NATS_STAGE(stg, id, n_launch, expr)                                           \
+  do {                                                                                \
+    if ((stg).prof && (stg).mark((stg).prof->start, id) != cudaSuccess) return NATS_ERR_CUDA; \
+    if (cuda_status(expr) != NATS_OK) return NATS_ERR_CUDA;                           \
+    if ((stg).prof) {                                                                 \
+      (stg).prof->launches += (n_launch);                                             \
+      if ((stg).mark((stg).prof->stop, id) != cudaSuccess) return NATS_ERR_CUDA;      \
+    }                                                                                 \
+  } while (0)
+
+}  // namespace
+}  // namespace nats
+
+using namespace nats;
+
+extern "C" {
+
+const char* nats_status_string(nats_status s) {
+  switch (s) {
+    case NATS_OK: return "NATS_OK";
+    case NATS_ERR_NULL: return "NATS_ERR_NULL: a required pointer is NULL";
+    case NATS_ERR_SHAPE: return "NATS_ERR_SHAPE: bad extent (chunk must be 64, L % 64 == 0, dk == dv)";
+    case NATS_ERR_DTYPE: return "NATS_ERR_DTYPE: dtype must be NATS_BF16 or NATS_F32";
+    case NATS_ERR_ALIGN: return "NATS_ERR_ALIGN: a pointer is not 16-byte aligned";
+    case NATS_ERR_WORKSPACE: return "NATS_ERR_WORKSPACE: workspace too small";
+    case NATS_ERR_UNSUPPORTED: return "NATS_ERR_UNSUPPORTED: head size must be 64 or 128";
+    case NATS_ERR_CUDA: return "NATS_ERR_CUDA: a CUDA call or kernel launch failed";
+    case NATS_ERR_INTERNAL: return "NATS_ERR_INTERNAL";
+    case NATS_ERR_VALUE: return "NATS_ERR_VALUE: scale / eps must be finite and >= 0";
+  }
+  return "unknown nats_status";
+}
+
+size_t nats_workspace_size(const nats_dims* dims) {
+  if (check_dims(dims) != NATS_OK) return 0;
+  return layout(problem_of(dims), nullptr, nullptr);
+}
+
+nats_status nats_select(const nats_dims* dims, const void* q, const void* k, const float* w_s,
+                        const float* b_s, uint8_t* sel, float* scores, nats_stream_t stream) {
+  nats_status s = check_dims(dims);
+  if (s != NATS_OK) return s;
+  const Problem p = problem_of(dims);
+  if (p.BH == 0 || p.L == 0) return NATS_OK;
+  if (!q || !k || !w_s || !sel) return NATS_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k)) return NATS_ERR_ALIGN;
+  return cuda_status(launch_score(p, dims->dtype, q, k, w_s, b_s, sel, scores, (cudaStream_t)stream));
+}
+
+nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const void* k,
+                                     const void* v, const float* g, const float* beta,
+                                     const float* w_s, const float* b_s, const float* w_g,
+                                     const float* b_g, const float* norm_w_soft,
+                                     const float* norm_w_lin, const uint8_t* sel_in, void* out,
+                                     uint8_t* sel_out, float* state_out, float* o_soft_out,
+                                     float* o_lin_out, void* workspace, size_t workspace_bytes,
+                                     nats_stream_t stream, nats_profile* prof) {
+  nats_status s = check_dims(dims);
+  if (s != NATS_OK) return s;
+  const Problem p = problem_of(dims);
+  if (prof) prof->launches = 0;
+  if (p.BH == 0 || p.L == 0) return NATS_OK;
+  if (!q || !k || !v || !g || !beta || !w_g || !out || !workspace) return NATS_ERR_NULL;
+  if (!sel_in && !w_s) return NATS_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(workspace))
+    return NATS_ERR_ALIGN;
+  Workspace ws;
+  const size_t need = layout(p, (char*)workspace, &ws);
+  if (workspace_bytes < need) return NATS_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int dt = dims->dtype;
+  Stages stg{prof, st};
+
+  // 1. selection (score layer, or the caller's override)
+  const uint8_t* sel = sel_in;
+  if (!sel) {
+    uint8_t* dst = sel_out ? sel_out : ws.sel;
+    NATS_STAGE(stg, NATS_STAGE_SCORE, 1, launch_score(p, dt, q, k, w_s, b_s, dst, nullptr, st));
+    sel = dst;
+  }
+  // 2. compacted softmax-chunk lists (mirrors an overridden selection to sel_out)
+  NATS_STAGE(stg, NATS_STAGE_COMPACT, 1,
+             launch_compact(p, sel, ws.nprev, ws.sel_idx, (sel_in && sel_out) ? sel_out : nullptr, st));
+  // 3. softmax branch
+  float* o_s = o_soft_out ? o_soft_out : ws.o_s;
+  NATS_STAGE(stg, NATS_STAGE_SOFTMAX, 1,
+             launch_softmax_simt(p, dt, q, k, v, ws.nprev, ws.sel_idx, o_s, st));
+  // 4. Gated DeltaNet branch (prep + scan with commit / rollback)
+  float* o_l = o_lin_out ? o_lin_out : ws.o_l;
+  NATS_STAGE(stg, NATS_STAGE_GDN_PREP, 1, launch_gdn_prep_simt(p, dt, q, k, v, g, beta, ws, st));
+  NATS_STAGE(stg, NATS_STAGE_GDN_SCAN, 1,
+             launch_gdn_scan_simt(p, dt, q, k, sel, ws, o_l, state_out, st));
+  // 5. RMSNorm per branch + gated merge
+  NATS_STAGE(stg, NATS_STAGE_MERGE, 1,
+             launch_norm_merge(p, dt, o_s, o_l, q, w_g, b_g, norm_w_soft, norm_w_lin, out, st));
+  return NATS_OK;
+}
+
+nats_status nats_hybrid_fwd(const nats_dims* dims, const void* q, const void* k, const void* v,
+                            const float* g, const float* beta, const float* w_s, const float* b_s,
+                            const float* w_g, const float* b_g, const float* norm_w_soft,
+                            const float* norm_w_lin, const uint8_t* sel_in, void* out,
+                            uint8_t* sel_out, float* state_out, float* o_soft_out,
+                            float* o_lin_out, void* workspace, size_t workspace_bytes,
+                            nats_stream_t stream) {
+  return nats_hybrid_fwd_profiled(dims, q, k, v, g, beta, w_s, b_s, w_g, b_g, norm_w_soft,
+                                  norm_w_lin, sel_in, out, sel_out, state_out, o_soft_out,
+                                  o_lin_out, workspace, workspace_bytes, stream, nullptr);
+}
+
+}  // extern "C"

@@ -1,0 +1,32 @@
+// kernels.h - host-side launchers of the libnats kernels (internal).
+#pragma once
+
+#include "common.cuh"
+
+namespace nats {
+
+// dtype: 0 = bf16, 1 = fp32 (nats_dtype).
+
+cudaError_t launch_score(const Problem& p, int dtype, const void* q, const void* k, const float* w_s,
+                         const float* b_s, uint8_t* sel, float* scores, cudaStream_t st);
+
+cudaError_t launch_compact(const Problem& p, const uint8_t* sel, int32_t* nprev, int32_t* sel_idx,
+                           uint8_t* sel_copy, cudaStream_t st);
+
+cudaError_t launch_softmax_simt(const Problem& p, int dtype, const void* q, const void* k,
+                                const void* v, const int32_t* nprev, const int32_t* sel_idx,
+                                float* o_s, cudaStream_t st);
+
+cudaError_t launch_gdn_prep_simt(const Problem& p, int dtype, const void* q, const void* k,
+                                 const void* v, const float* g, const float* beta,
+                                 const Workspace& ws, cudaStream_t st);
+
+cudaError_t launch_gdn_scan_simt(const Problem& p, int dtype, const void* q, const void* k,
+                                 const uint8_t* sel, const Workspace& ws, float* o_l,
+                                 float* state_out, cudaStream_t st);
+
+cudaError_t launch_norm_merge(const Problem& p, int dtype, const float* o_s, const float* o_l,
+                              const void* q, const float* w_g, const float* b_g, const float* nw_s,
+                              const float* nw_l, void* out, cudaStream_t st);
+
+}  // namespace nats

@@ -1,0 +1,122 @@
+"""The C ABI: the library loads, exports what include/nats.h declares, and
+rejects bad arguments on the host before any launch (no GPU needed)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def nat():
+    from linear_attention_nats_gb300 import build as b
+
+    b.build()
+    from linear_attention_nats_gb300 import _native
+
+    return _native
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(nats_\w+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_symbol(nat):
+    declared = _declared()
+    assert {"nats_select", "nats_hybrid_fwd", "nats_workspace_size", "nats_status_string"} <= declared
+    assert declared == set(nat.EXPORTS)
+    for name in sorted(declared):
+        assert hasattr(nat.lib, name), name
+
+
+def test_status_strings(nat):
+    for code, name in nat.STATUS.items():
+        s = nat.lib.nats_status_string(code).decode()
+        assert s.startswith(name), (code, s)
+
+
+def test_workspace_size(nat):
+    ws = lambda *a, **k: nat.lib.nats_workspace_size(ctypes.byref(nat.dims(*a, **k)))
+    assert ws(4, 16, 8192, 128) > 4 * 16 * 8192 * 128 * 4 * 2
+    assert ws(1, 1, 64, 64) > 0
+    assert ws(1, 1, 100, 64) == 0  # L % 64 != 0
+    assert ws(1, 1, 64, 96) == 0  # unsupported head size
+    assert ws(0, 4, 256, 64) >= 0
+    small, big = ws(1, 2, 256, 64), ws(2, 2, 256, 64)
+    assert big > small
+
+
+def _fwd(nat, dm, **ptrs):
+    names = ["q", "k", "v", "g", "beta", "w_s", "b_s", "w_g", "b_g", "nws", "nwl", "sel_in", "out",
+             "sel_out", "state", "o_soft", "o_lin", "ws"]
+    args = [ptrs.get(n) for n in names]
+    args = [None if a is None else ctypes.c_void_p(a) for a in args]
+    return nat.lib.nats_hybrid_fwd(ctypes.byref(dm), *args[:17], args[17],
+                                   ctypes.c_size_t(ptrs.get("ws_bytes", 1 << 40)), None)
+
+
+# Fake but 256-aligned addresses: validation must reject before touching them.
+A = 0x10000000
+FULL = dict(q=A, k=A + 0x1000, v=A + 0x2000, g=A + 0x3000, beta=A + 0x4000, w_s=A + 0x5000,
+            w_g=A + 0x6000, out=A + 0x7000, ws=A + 0x8000)
+
+
+@pytest.mark.parametrize("case,code", [
+    (dict(B=-1), 2), (dict(L=100), 2), (dict(d=96), 6), (dict(dtype=7), 3), (dict(chunk=32), 2),
+    (dict(scale=float("nan")), 9), (dict(eps=-1.0), 9),
+])
+def test_shape_errors(nat, case, code):
+    kw = dict(B=1, H=2, L=256, d=64, dtype=0, scale=0.0, eps=1e-6, chunk=64)
+    kw.update(case)
+    dm = nat.dims(kw["B"], kw["H"], kw["L"], kw["d"], kw["dtype"], kw["scale"], kw["eps"], kw["chunk"])
+    assert _fwd(nat, dm, **FULL) == code
+    assert nat.lib.nats_select(ctypes.byref(dm), *[ctypes.c_void_p(A)] * 3, None,
+                               ctypes.c_void_p(A), None, None) == code
+
+
+def test_dk_ne_dv(nat):
+    dm = nat.Dims(1, 2, 256, 64, 128, 64, 0, 0.0, 1e-6)
+    assert _fwd(nat, dm, **FULL) == 2
+
+
+@pytest.mark.parametrize("missing", ["q", "k", "v", "g", "beta", "w_g", "out", "ws"])
+def test_null_errors(nat, missing):
+    dm = nat.dims(1, 2, 256, 64)
+    p = dict(FULL)
+    p[missing] = None
+    assert _fwd(nat, dm, **p) == 1
+
+
+def test_w_s_optional_only_with_override(nat):
+    dm = nat.dims(1, 2, 256, 64)
+    p = dict(FULL)
+    p["w_s"] = None
+    assert _fwd(nat, dm, **p) == 1
+
+
+def test_alignment_error(nat):
+    dm = nat.dims(1, 2, 256, 64)
+    p = dict(FULL)
+    p["v"] = A + 0x2008
+    assert _fwd(nat, dm, **p) == 4
+
+
+def test_workspace_too_small(nat):
+    dm = nat.dims(1, 2, 256, 64)
+    need = nat.lib.nats_workspace_size(ctypes.byref(dm))
+    assert _fwd(nat, dm, ws_bytes=need - 1, **FULL) == 5
+
+
+def test_empty_is_a_no_op(nat):
+    # zero extents return NATS_OK without touching any pointer (all NULL here)
+    for B, H, L in ((0, 2, 256), (1, 0, 256), (1, 2, 0)):
+        assert _fwd(nat, nat.dims(B, H, L, 64)) == 0
