@@ -69,7 +69,18 @@ def _load() -> ctypes.CDLL:
     return lib
 
 
-lib = _load()
+_lib = None
+
+
+def __getattr__(name):
+    # `lib` loads on first use, so that the build helper in this package can
+    # be imported before the library exists.
+    global _lib
+    if name == "lib":
+        if _lib is None:
+            _lib = _load()
+        return _lib
+    raise AttributeError(name)
 
 
 def dims(B, H, L, d, dtype=NATS_BF16, scale=0.0, eps=1e-6, chunk=64) -> Dims:
