@@ -86,6 +86,12 @@ const char* nats_status_string(nats_status s);
  * outputs; its contents are scratch between calls. */
 size_t nats_workspace_size(const nats_dims* dims);
 
+/* Synchronises `stream`, then reports whether a kernel of the last
+ * nats_hybrid_fwd call that used `workspace` gave up on a bounded internal
+ * wait (NATS_ERR_INTERNAL; its outputs are then invalid) or NATS_OK.  The
+ * tensor-core kernels bound every spin-wait (about 2 s) instead of hanging. */
+nats_status nats_workspace_check(const nats_dims* dims, const void* workspace, nats_stream_t stream);
+
 /* Attention Score Layer + argmax alone ("Kernmechanismen" item 1).
  *   q, k    [B, H, L, dk] dtype
  *   w_s     fp32 [H, 2, 2*dk]: row 0 scores softmax, row 1 Gated DeltaNet,

@@ -50,6 +50,12 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def check_workspace(dm, workspace, stream=None) -> None:
+    """Synchronise and raise NatsError if a kernel of the last call gave up."""
+    check(_native.lib.nats_workspace_check(ctypes.byref(dm), _p(workspace), _stream(stream)),
+          "nats_workspace_check")
+
+
 def workspace_size(B: int, H: int, L: int, d: int, dtype=NATS_BF16) -> int:
     """Bytes of workspace hybrid_fwd needs (0 for unsupported sizes)."""
     dm = dims(B, H, L, d, dtype)
@@ -75,7 +81,7 @@ def select(q, k, w_s, b_s=None, *, scores: bool = False, stream=None):
 def hybrid_fwd(q, k, v, g, beta, w_s, b_s, w_g, b_g=None, *, norm_w_soft=None, norm_w_lin=None,
                sel_in=None, scale: float = 0.0, eps: float = 1e-6, out=None, workspace=None,
                return_sel: bool = False, return_state: bool = False,
-               return_branches: bool = False, stream=None):
+               return_branches: bool = False, check_errors: bool = False, stream=None):
     """NAtS-L hybrid attention layer forward.
 
     q, k, v: [B, H, L, d] bf16 or fp32 (same dtype); g, beta: fp32 [B, H, L];
@@ -83,6 +89,7 @@ def hybrid_fwd(q, k, v, g, beta, w_s, b_s, w_g, b_g=None, *, norm_w_soft=None, n
     b_g: fp32 [H] or None; norm weights fp32 [d] or None; sel_in: uint8
     [B, H, L/64] or None.  Returns `out` alone, or a dict with "out" and the
     requested "sel", "state" ([B, H, d, d] fp32), "o_soft", "o_lin".
+    check_errors=True synchronises and raises if a kernel gave up on a bounded wait.
     """
     _req(q, "q")
     B, H, L, d = q.shape
@@ -117,6 +124,8 @@ def hybrid_fwd(q, k, v, g, beta, w_s, b_s, w_g, b_g=None, *, norm_w_soft=None, n
         _p(norm_w_soft), _p(norm_w_lin), _p(sel_in), _p(out), _p(sel), _p(state), _p(o_soft),
         _p(o_lin), _p(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream)),
         "nats_hybrid_fwd")
+    if check_errors:
+        check_workspace(dm, workspace, stream)
     if not (return_sel or return_state or return_branches):
         return out
     res = {"out": out}

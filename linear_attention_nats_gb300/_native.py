@@ -23,8 +23,8 @@ STATUS = {
 }
 
 # Every symbol include/nats.h declares.
-EXPORTS = ("nats_status_string", "nats_workspace_size", "nats_select", "nats_hybrid_fwd",
-           "nats_hybrid_fwd_profiled")
+EXPORTS = ("nats_status_string", "nats_workspace_size", "nats_workspace_check", "nats_select",
+           "nats_hybrid_fwd", "nats_hybrid_fwd_profiled")
 
 NUM_STAGES = 8
 STAGES = ("score", "compact", "softmax", "gdn_prep", "gdn_scan", "merge")
@@ -59,6 +59,8 @@ def _load() -> ctypes.CDLL:
     lib.nats_status_string.restype = ctypes.c_char_p
     lib.nats_workspace_size.argtypes = [ctypes.POINTER(Dims)]
     lib.nats_workspace_size.restype = ctypes.c_size_t
+    lib.nats_workspace_check.argtypes = [ctypes.POINTER(Dims), P, P]
+    lib.nats_workspace_check.restype = ctypes.c_int
     lib.nats_select.argtypes = [ctypes.POINTER(Dims), P, P, P, P, P, P, P]
     lib.nats_select.restype = ctypes.c_int
     lib.nats_hybrid_fwd.argtypes = [ctypes.POINTER(Dims)] + [P] * 18 + [ctypes.c_size_t, P]

@@ -65,6 +65,7 @@ size_t layout(const Problem& p, char* base, Workspace* ws) {
   w.P = (float*)take(4 * BH * N * C * C);
   w.o_s = (float*)take(4 * BH * L * D);
   w.o_l = (float*)take(4 * BH * L * D);
+  w.err = (int*)take(16);
   if (ws) *ws = w;
   return off;
 }
@@ -119,6 +120,22 @@ size_t nats_workspace_size(const nats_dims* dims) {
   return layout(problem_of(dims), nullptr, nullptr);
 }
 
+nats_status nats_workspace_check(const nats_dims* dims, const void* workspace, nats_stream_t stream) {
+  nats_status s = check_dims(dims);
+  if (s != NATS_OK) return s;
+  const Problem p = problem_of(dims);
+  if (p.BH == 0 || p.L == 0) return NATS_OK;
+  if (!workspace) return NATS_ERR_NULL;
+  Workspace ws;
+  layout(p, (char*)workspace, &ws);
+  int flag = 0;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&flag, ws.err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return NATS_ERR_CUDA;
+  return flag ? NATS_ERR_INTERNAL : NATS_OK;
+}
+
 nats_status nats_select(const nats_dims* dims, const void* q, const void* k, const float* w_s,
                         const float* b_s, uint8_t* sel, float* scores, nats_stream_t stream) {
   nats_status s = check_dims(dims);
@@ -163,11 +180,16 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
   }
   // 2. compacted softmax-chunk lists (mirrors an overridden selection to sel_out)
   NATS_STAGE(stg, NATS_STAGE_COMPACT, 1,
-             launch_compact(p, sel, ws.nprev, ws.sel_idx, (sel_in && sel_out) ? sel_out : nullptr, st));
+             launch_compact(p, sel, ws.nprev, ws.sel_idx, (sel_in && sel_out) ? sel_out : nullptr, ws.err, st));
   // 3. softmax branch
   float* o_s = o_soft_out ? o_soft_out : ws.o_s;
-  NATS_STAGE(stg, NATS_STAGE_SOFTMAX, 1,
-             launch_softmax_simt(p, dt, q, k, v, ws.nprev, ws.sel_idx, o_s, st));
+  if (dt == NATS_BF16) {
+    NATS_STAGE(stg, NATS_STAGE_SOFTMAX, 1,
+               launch_softmax_tc(p, q, k, v, ws.nprev, ws.sel_idx, sel, o_s, ws.err, st));
+  } else {
+    NATS_STAGE(stg, NATS_STAGE_SOFTMAX, 1,
+               launch_softmax_simt(p, dt, q, k, v, ws.nprev, ws.sel_idx, o_s, st));
+  }
   // 4. Gated DeltaNet branch (prep + scan with commit / rollback)
   float* o_l = o_lin_out ? o_lin_out : ws.o_l;
   NATS_STAGE(stg, NATS_STAGE_GDN_PREP, 1, launch_gdn_prep_simt(p, dt, q, k, v, g, beta, ws, st));

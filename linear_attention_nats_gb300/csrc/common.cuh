@@ -55,6 +55,7 @@ struct Workspace {
   float* P;          // [BH, N, C, C]   lower(e^{G_t - G_i} scale q_t . k_i)
   float* o_s;        // [BH, L, dv] softmax branch output (before norm)
   float* o_l;        // [BH, L, dv] Gated DeltaNet branch output (before norm)
+  int* err;          // [1] set by a kernel whose bounded wait expired (zeroed per call)
 };
 
 }  // namespace nats

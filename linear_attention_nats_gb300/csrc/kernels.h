@@ -11,7 +11,11 @@ cudaError_t launch_score(const Problem& p, int dtype, const void* q, const void*
                          const float* b_s, uint8_t* sel, float* scores, cudaStream_t st);
 
 cudaError_t launch_compact(const Problem& p, const uint8_t* sel, int32_t* nprev, int32_t* sel_idx,
-                           uint8_t* sel_copy, cudaStream_t st);
+                           uint8_t* sel_copy, int* err, cudaStream_t st);
+
+cudaError_t launch_softmax_tc(const Problem& p, const void* q, const void* k, const void* v,
+                              const int32_t* nprev, const int32_t* sel_idx, const uint8_t* sel, float* o_s,
+                              int* err, cudaStream_t st);
 
 cudaError_t launch_softmax_simt(const Problem& p, int dtype, const void* q, const void* k,
                                 const void* v, const int32_t* nprev, const int32_t* sel_idx,

@@ -31,7 +31,7 @@ def run_cuda(inp: gen.NatsInputs, sel_in=None, **kw):
     if sel_in is not None:
         kw["sel_in"] = torch.from_numpy(np.ascontiguousarray(sel_in, np.uint8)).cuda()
     r = nats.hybrid_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_s"], t["b_s"], t["w_g"],
-                        t["b_g"], return_sel=True, return_state=True, return_branches=True, **kw)
+                        t["b_g"], return_sel=True, return_state=True, return_branches=True, check_errors=True, **kw)
     torch.cuda.synchronize()
     return {k: v.float().cpu().numpy() if v.dtype != torch.uint8 else v.cpu().numpy() for k, v in r.items()}
 
