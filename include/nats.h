@@ -125,6 +125,34 @@ nats_status nats_hybrid_fwd(const nats_dims* dims, const void* q, const void* k,
                             float* o_lin_out, void* workspace, size_t workspace_bytes,
                             nats_stream_t stream);
 
+/* nats_hybrid_fwd for callers that cannot allocate device memory (the
+ * pages describe no such variant; it exists for deployment).  Some callers
+ * have no way to hand over a workspace: a plugin whose host application owns
+ * all device memory through its own pool (a direct cudaMalloc would bypass
+ * the pool and may synchronise the device), a latency-critical loop that must
+ * never block on an allocation, or a plain C caller without an allocator.
+ * This entry point takes the same inputs and outputs as nats_hybrid_fwd but
+ * no workspace, and allocates nothing: its scratch is a 64 MiB device array
+ * built into the library, held on every GPU that loads the library until
+ * the process exits.
+ *   - Problems whose nats_workspace_size() exceeds 64 MiB (67108864 bytes)
+ *     are rejected with NATS_ERR_WORKSPACE before any launch.
+ *   - The first call on a device looks up the array's device address on the
+ *     current device (cudaGetSymbolAddress); make that first call before any
+ *     stream capture.
+ *   - All calls on a device share the one array, which keeps the last call's
+ *     contents; calls that can overlap on the GPU (different streams without
+ *     ordering, or several host threads) race on it and must be serialised
+ *     by the caller.  Nothing in it needs to start zeroed.
+ * Other arguments, results and errors are those of nats_hybrid_fwd. */
+nats_status nats_hybrid_fwd_noalloc(const nats_dims* dims, const void* q, const void* k,
+                                    const void* v, const float* g, const float* beta,
+                                    const float* w_s, const float* b_s, const float* w_g,
+                                    const float* b_g, const float* norm_w_soft,
+                                    const float* norm_w_lin, const uint8_t* sel_in, void* out,
+                                    uint8_t* sel_out, float* state_out, float* o_soft_out,
+                                    float* o_lin_out, nats_stream_t stream);
+
 /* Stages of nats_hybrid_fwd, for per-stage timing. */
 typedef enum {
   NATS_STAGE_SCORE = 0,    /* Attention Score Layer + argmax (skipped with sel_in) */

@@ -24,7 +24,9 @@ STATUS = {
 
 # Every symbol include/nats.h declares.
 EXPORTS = ("nats_status_string", "nats_workspace_size", "nats_workspace_check", "nats_select",
-           "nats_hybrid_fwd", "nats_hybrid_fwd_profiled")
+           "nats_hybrid_fwd", "nats_hybrid_fwd_profiled", "nats_hybrid_fwd_noalloc")
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 NUM_STAGES = 8
 STAGES = ("score", "compact", "softmax", "gdn_prep", "gdn_scan", "merge")
@@ -68,6 +70,8 @@ def _load() -> ctypes.CDLL:
     lib.nats_hybrid_fwd_profiled.argtypes = [ctypes.POINTER(Dims)] + [P] * 18 + [
         ctypes.c_size_t, P, ctypes.POINTER(Profile)]
     lib.nats_hybrid_fwd_profiled.restype = ctypes.c_int
+    lib.nats_hybrid_fwd_noalloc.argtypes = [ctypes.POINTER(Dims)] + [P] * 17 + [P]
+    lib.nats_hybrid_fwd_noalloc.restype = ctypes.c_int
     return lib
 
 
