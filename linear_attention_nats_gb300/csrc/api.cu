@@ -192,9 +192,17 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
   }
   // 4. Gated DeltaNet branch (prep + scan with commit / rollback)
   float* o_l = o_lin_out ? o_lin_out : ws.o_l;
-  NATS_STAGE(stg, NATS_STAGE_GDN_PREP, 1, launch_gdn_prep_simt(p, dt, q, k, v, g, beta, ws, st));
-  NATS_STAGE(stg, NATS_STAGE_GDN_SCAN, 1,
-             launch_gdn_scan_simt(p, dt, q, k, sel, ws, o_l, state_out, st));
+  if (dt == NATS_BF16) {
+    // bf16 factors W, U, P reuse the fp32 factor buffers of the workspace
+    NATS_STAGE(stg, NATS_STAGE_GDN_PREP, 1,
+               launch_gdn_prep_mma(p, q, k, v, g, beta, ws.G, ws.W, ws.U, ws.P, st));
+    NATS_STAGE(stg, NATS_STAGE_GDN_SCAN, 1,
+               launch_gdn_scan_tc(p, q, k, sel, ws.G, ws.W, ws.U, ws.P, o_l, state_out, ws.err, st));
+  } else {
+    NATS_STAGE(stg, NATS_STAGE_GDN_PREP, 1, launch_gdn_prep_simt(p, dt, q, k, v, g, beta, ws, st));
+    NATS_STAGE(stg, NATS_STAGE_GDN_SCAN, 1,
+               launch_gdn_scan_simt(p, dt, q, k, sel, ws, o_l, state_out, st));
+  }
   // 5. RMSNorm per branch + gated merge
   NATS_STAGE(stg, NATS_STAGE_MERGE, 1,
              launch_norm_merge(p, dt, o_s, o_l, q, w_g, b_g, norm_w_soft, norm_w_lin, out, st));

@@ -1,0 +1,251 @@
+// gdn_prep_mma.cu - Gated DeltaNet phase 1 on tensor cores (bf16 inputs):
+// the per-chunk factors of the chunkwise WY/UT form, parallel over chunks.
+//
+// "Neural Attention Search Linear (NAtS-L)", technical summary,
+// "Kernmechanismen" item 3 (both states are pseudo-updated for every chunk);
+// Gated DeltaNet S_t = a_t S_{t-1}(I - beta_t k_t k_t^T) + beta_t v_t k_t^T.
+// For one chunk (G = in-chunk cumulative sum of g):
+//   A = strict_lower(beta_t e^{G_t - G_i} k_t . k_i),  T = (I + A)^{-1}
+//   U = T diag(beta) V,  W = T diag(beta e^G) K,  P = lower_incl(scale e^{G_t - G_i} q_t . k_i)
+// KK^T / QK^T and T.(beta V) / T.(beta e^G K) are warp-level bf16 MMAs
+// (fp32 accumulate); the unit-lower-triangular inverse is fp32 forward
+// substitution.  Outputs: W, U as bf16 [chunk][64][D], P as bf16 [chunk][64][64]
+// (the operands of the chunk scan), G as fp32.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace nats {
+namespace {
+
+constexpr int C = kChunk;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D(16x8 fp32) += A(16x16 bf16, row) * B(16x8 bf16, col)
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+template <int D>
+struct PrepSmem {
+  static constexpr int RS = D + 8;  // bf16 row stride (16-byte skew: conflict-free ldmatrix)
+  static constexpr int TS = C + 8;  // bf16 row stride of T
+  static constexpr int offK = 0;
+  static constexpr int offQ = offK + C * RS * 2;
+  static constexpr int offV = offQ + C * RS * 2;
+  static constexpr int offA = offV + C * RS * 2;     // fp32 [C][C+1]
+  static constexpr int offT = offA + C * (C + 1) * 4;  // fp32 [C][C+1]
+  static constexpr int offTb = offT + C * (C + 1) * 4; // bf16 [C][TS]
+  static constexpr int offG = offTb + C * TS * 2;    // fp32 [C]
+  static constexpr int offB = offG + C * 4;          // fp32 [C] beta
+  static constexpr int kBytes = offB + C * 4;
+};
+
+// One CTA (4 warps) per (b, h, chunk).  Warp w owns rows 16w .. 16w+15 of
+// every 64-row product.
+template <int D>
+__global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
+    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+    const __nv_bfloat16* __restrict__ v, const float* __restrict__ g, const float* __restrict__ beta, int L,
+    int N, float scale, float* __restrict__ Gout, __nv_bfloat16* __restrict__ Wout,
+    __nv_bfloat16* __restrict__ Uout, __nv_bfloat16* __restrict__ Pout) {
+  using S = PrepSmem<D>;
+  constexpr int RS = S::RS, TS = S::TS;
+  extern __shared__ __align__(16) uint8_t smem[];
+  __nv_bfloat16* Ks = (__nv_bfloat16*)(smem + S::offK);
+  __nv_bfloat16* Qs = (__nv_bfloat16*)(smem + S::offQ);
+  __nv_bfloat16* Vs = (__nv_bfloat16*)(smem + S::offV);
+  float* As = (float*)(smem + S::offA);
+  float* Ts = (float*)(smem + S::offT);
+  __nv_bfloat16* Tb = (__nv_bfloat16*)(smem + S::offTb);
+  float* Gs = (float*)(smem + S::offG);
+  float* Bs = (float*)(smem + S::offB);
+
+  const long long blk = blockIdx.x;
+  const int c = (int)(blk % N);
+  const long long bh = blk / N;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gq = lane >> 2, cq = lane & 3;  // fragment row / column-pair
+  const size_t tok0 = (size_t)bh * L + (size_t)c * C;
+
+  // ---- stage K, Q, V (16-byte async copies) and the gates
+  constexpr int VPR = D / 8;  // 16-byte vectors per row
+  for (int e = tid; e < C * VPR; e += 128) {
+    const int t = e / VPR, x = e % VPR;
+    cp_async16(Ks + t * RS + x * 8, k + (tok0 + t) * D + x * 8);
+    cp_async16(Qs + t * RS + x * 8, q + (tok0 + t) * D + x * 8);
+    cp_async16(Vs + t * RS + x * 8, v + (tok0 + t) * D + x * 8);
+  }
+  if (warp == 0) {
+    const float g0 = g[tok0 + 2 * lane], g1 = g[tok0 + 2 * lane + 1];
+    float x = g0 + g1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    const float excl = x - (g0 + g1);
+    Gs[2 * lane] = excl + g0;
+    Gs[2 * lane + 1] = excl + g0 + g1;
+    Gout[tok0 + 2 * lane] = excl + g0;
+    Gout[tok0 + 2 * lane + 1] = excl + g0 + g1;
+  } else if (warp == 1) {
+    Bs[2 * lane] = beta[tok0 + 2 * lane];
+    Bs[2 * lane + 1] = beta[tok0 + 2 * lane + 1];
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  // ---- KK^T and QK^T for rows 16w .. 16w+15, all 64 columns
+  const int m0 = 16 * warp;
+  {
+    float kk[8][4], qk[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int x = 0; x < 4; ++x) kk[j][x] = qk[j][x] = 0.f;
+    const int arow = m0 + (lane & 7) + 8 * ((lane >> 3) & 1);
+    const int acol = 8 * (lane >> 4);
+    const int brow = (lane & 7) + 8 * (lane >> 4);
+    const int bcol = 8 * ((lane >> 3) & 1);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t ka[4], qa[4];
+      ldsm_x4(smem_addr(Ks + arow * RS + 16 * ks + acol), ka[0], ka[1], ka[2], ka[3]);
+      ldsm_x4(smem_addr(Qs + arow * RS + 16 * ks + acol), qa[0], qa[1], qa[2], qa[3]);
+#pragma unroll
+      for (int jp = 0; jp < 4; ++jp) {  // key rows 16jp .. 16jp+15 = two n-tiles
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(smem_addr(Ks + (16 * jp + brow) * RS + 16 * ks + bcol), b0, b1, b2, b3);
+        mma16816(kk[2 * jp], ka[0], ka[1], ka[2], ka[3], b0, b1);
+        mma16816(kk[2 * jp + 1], ka[0], ka[1], ka[2], ka[3], b2, b3);
+        mma16816(qk[2 * jp], qa[0], qa[1], qa[2], qa[3], b0, b1);
+        mma16816(qk[2 * jp + 1], qa[0], qa[1], qa[2], qa[3], b2, b3);
+      }
+    }
+    // decay, masks; A -> shared fp32, P -> global bf16
+    __nv_bfloat16* P = Pout + (size_t)blk * C * C;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int t = m0 + gq + 8 * hh;
+        const int i0 = 8 * j + 2 * cq;
+        float av[2], pv[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int i = i0 + u;
+          const float dec = __expf(Gs[t] - Gs[i]);
+          av[u] = (i < t) ? Bs[t] * dec * kk[j][2 * hh + u] : 0.f;
+          pv[u] = (i <= t) ? scale * dec * qk[j][2 * hh + u] : 0.f;
+        }
+        As[t * (C + 1) + i0] = av[0];
+        As[t * (C + 1) + i0 + 1] = av[1];
+        *(uint32_t*)(P + t * C + i0) = pack2(pv[0], pv[1]);
+      }
+    }
+  }
+  __syncthreads();
+  // ---- T = (I + A)^{-1} (threads 0-63, one column each) while the other
+  // threads scale V by beta and K by beta e^G in place (bf16)
+  if (tid < C) {
+    const int j = tid;
+    for (int t = 0; t < C; ++t) {
+      float x = (j == t) ? 1.f : 0.f;
+      for (int i = j; i < t; ++i) x = fmaf(-As[t * (C + 1) + i], Ts[i * (C + 1) + j], x);
+      if (j <= t) Ts[t * (C + 1) + j] = x;
+      asm volatile("bar.sync 1, 64;" ::: "memory");
+    }
+    for (int t = 0; t < C; ++t) Tb[t * TS + j] = __float2bfloat16_rn(j <= t ? Ts[t * (C + 1) + j] : 0.f);
+  } else {
+    for (int e = tid - C; e < C * D; e += 128 - C) {
+      const int t = e / D, f = e % D;
+      const float b = Bs[t];
+      Vs[t * RS + f] = __float2bfloat16_rn(b * __bfloat162float(Vs[t * RS + f]));
+      Ks[t * RS + f] = __float2bfloat16_rn(b * __expf(Gs[t]) * __bfloat162float(Ks[t * RS + f]));
+    }
+  }
+  __syncthreads();
+  // ---- U = T (beta V), W = T (beta e^G K): rows 16w.., k-steps up to the diagonal
+  {
+    const int arow = m0 + (lane & 7) + 8 * ((lane >> 3) & 1);
+    const int acol = 8 * (lane >> 4);
+    const int trow = (lane & 7) + 8 * ((lane >> 3) & 1);  // k row within the 16-row step
+    const int tcol = 8 * (lane >> 4);                     // n column offset
+    __nv_bfloat16* Ug = Uout + (size_t)blk * C * D;
+    __nv_bfloat16* Wg = Wout + (size_t)blk * C * D;
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const __nv_bfloat16* Bsrc = which == 0 ? Vs : Ks;
+      __nv_bfloat16* dst = which == 0 ? Ug : Wg;
+      float acc[D / 8][4];
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) acc[n][x] = 0.f;
+      for (int ks = 0; ks <= warp; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(smem_addr(Tb + arow * TS + 16 * ks + acol), a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int np = 0; np < D / 16; ++np) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(smem_addr(Bsrc + (16 * ks + trow) * RS + 16 * np + tcol), b0, b1, b2, b3);
+          mma16816(acc[2 * np], a[0], a[1], a[2], a[3], b0, b1);
+          mma16816(acc[2 * np + 1], a[0], a[1], a[2], a[3], b2, b3);
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) {
+        const int col = 8 * n + 2 * cq;
+        *(uint32_t*)(dst + (m0 + gq) * D + col) = pack2(acc[n][0], acc[n][1]);
+        *(uint32_t*)(dst + (m0 + gq + 8) * D + col) = pack2(acc[n][2], acc[n][3]);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gdn_prep_mma(const Problem& p, const void* q, const void* k, const void* v, const float* g,
+                                const float* beta, float* G, void* W16, void* U16, void* P16, cudaStream_t st) {
+  if (p.BH == 0 || p.N == 0) return cudaSuccess;
+  auto run = [&](auto kern, int smem) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)(p.BH * p.N), 128, smem, st>>>(
+        (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, g, beta, p.L, p.N, p.scale,
+        G, (__nv_bfloat16*)W16, (__nv_bfloat16*)U16, (__nv_bfloat16*)P16);
+    return cudaGetLastError();
+  };
+  return p.d == 64 ? run(gdn_prep_mma_kernel<64>, PrepSmem<64>::kBytes)
+                   : run(gdn_prep_mma_kernel<128>, PrepSmem<128>::kBytes);
+}
+
+}  // namespace nats

@@ -38,6 +38,7 @@ def _compare(inp, got, ref, rows=None, tag=""):
         "out": rel_err(got["out"][:, r], ref["out"][:, r]),
         "state": rel_err(got["state"], ref["state"]),
     }
+    print(f"[parity] {tag}: " + " ".join(f"{k}={v:.2e}" for k, v in errs.items()))
     bad = {k: v for k, v in errs.items() if not v <= tol}
     assert not bad, f"{tag} {bad} > {tol} (all: {errs})"
     return errs
