@@ -65,7 +65,9 @@ struct PrepSmem {
   static constexpr int offTb = offT + C * (C + 1) * 4; // bf16 [C][TS]
   static constexpr int offG = offTb + C * TS * 2;    // fp32 [C]
   static constexpr int offB = offG + C * 4;          // fp32 [C] beta
-  static constexpr int kBytes = offB + C * 4;
+  static constexpr int offBg = offB + C * 4;         // fp32 [C] beta e^G
+  static constexpr int offX = offBg + C * 4;         // fp32 [C][C+1] scratch of the blocked inverse
+  static constexpr int kBytes = offX + C * (C + 1) * 4;
 };
 
 // One CTA (4 warps) per (b, h, chunk).  Warp w owns rows 16w .. 16w+15 of
@@ -87,6 +89,7 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
   __nv_bfloat16* Tb = (__nv_bfloat16*)(smem + S::offTb);
   float* Gs = (float*)(smem + S::offG);
   float* Bs = (float*)(smem + S::offB);
+  float* Bg = (float*)(smem + S::offBg);
 
   const long long blk = blockIdx.x;
   const int c = (int)(blk % N);
@@ -173,24 +176,63 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
     }
   }
   __syncthreads();
-  // ---- T = (I + A)^{-1} (threads 0-63, one column each) while the other
-  // threads scale V by beta and K by beta e^G in place (bf16)
+  // ---- T = (I + A)^{-1}, unit lower triangular, blocked in 16 x 16 tiles:
+  //   T_bb = (I + A_bb)^{-1}                          (forward substitution)
+  //   T_ij = -T_ii sum_{j <= k < i} A_ik T_kj  (i > j, by distance i - j)
+  // Meanwhile nothing else touches As / Ts.  Scale factors for the second
+  // product: V rows by beta, K rows by beta e^G.
+  float* Xs = (float*)(smem + S::offX);
   if (tid < C) {
-    const int j = tid;
-    for (int t = 0; t < C; ++t) {
-      float x = (j == t) ? 1.f : 0.f;
-      for (int i = j; i < t; ++i) x = fmaf(-As[t * (C + 1) + i], Ts[i * (C + 1) + j], x);
-      if (j <= t) Ts[t * (C + 1) + j] = x;
-      asm volatile("bar.sync 1, 64;" ::: "memory");
+    // diagonal tile b, column jj: a 16-long dependency chain in registers
+    const int b = tid >> 4, jj = tid & 15, j = 16 * b + jj;
+    float x[16];
+#pragma unroll
+    for (int tt = 0; tt < 16; ++tt) {
+      const int t = 16 * b + tt;
+      float acc = (tt == jj) ? 1.f : 0.f;
+#pragma unroll
+      for (int ii = 0; ii < tt; ++ii)
+        if (ii >= jj) acc = fmaf(-As[t * (C + 1) + 16 * b + ii], x[ii], acc);
+      x[tt] = (tt >= jj) ? acc : 0.f;
     }
-    for (int t = 0; t < C; ++t) Tb[t * TS + j] = __float2bfloat16_rn(j <= t ? Ts[t * (C + 1) + j] : 0.f);
+#pragma unroll
+    for (int tt = 0; tt < 16; ++tt) Ts[(16 * b + tt) * (C + 1) + j] = x[tt];
   } else {
-    for (int e = tid - C; e < C * D; e += 128 - C) {
-      const int t = e / D, f = e % D;
-      const float b = Bs[t];
-      Vs[t * RS + f] = __float2bfloat16_rn(b * __bfloat162float(Vs[t * RS + f]));
-      Ks[t * RS + f] = __float2bfloat16_rn(b * __expf(Gs[t]) * __bfloat162float(Ks[t * RS + f]));
+    const int u = tid - C;
+    Bg[u] = Bs[u] * __expf(Gs[u]);
+  }
+  __syncthreads();
+  for (int lv = 1; lv < 4; ++lv) {
+    const int nblk = 4 - lv;
+    // X_ij = sum_{j <= k < i} A_ik T_kj for the tiles (i, j) = (b + lv, b)
+    for (int e = tid; e < nblk * 256; e += 128) {
+      const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+      const int i = b + lv, j = b;
+      const int row = 16 * i + r, col = 16 * j + cc;
+      float acc = 0.f;
+      for (int kk = 16 * j; kk < 16 * i; ++kk) acc = fmaf(As[row * (C + 1) + kk], Ts[kk * (C + 1) + col], acc);
+      Xs[row * (C + 1) + col] = acc;
     }
+    __syncthreads();
+    // T_ij = -T_ii X_ij
+    for (int e = tid; e < nblk * 256; e += 128) {
+      const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+      const int i = b + lv, j = b;
+      const int row = 16 * i + r, col = 16 * j + cc;
+      float acc = 0.f;
+      for (int kk = 16 * i; kk <= row; ++kk) acc = fmaf(Ts[row * (C + 1) + kk], Xs[kk * (C + 1) + col], acc);
+      Ts[row * (C + 1) + col] = -acc;
+    }
+    __syncthreads();
+  }
+  for (int e = tid; e < C * C; e += 128) {
+    const int t = e >> 6, j = e & 63;
+    Tb[t * TS + j] = __float2bfloat16_rn(j <= t ? Ts[t * (C + 1) + j] : 0.f);
+  }
+  for (int e = tid; e < C * D; e += 128) {
+    const int t = e / D, f = e % D;
+    Vs[t * RS + f] = __float2bfloat16_rn(Bs[t] * __bfloat162float(Vs[t * RS + f]));
+    Ks[t * RS + f] = __float2bfloat16_rn(Bg[t] * __bfloat162float(Ks[t * RS + f]));
   }
   __syncthreads();
   // ---- U = T (beta V), W = T (beta e^G K): rows 16w.., k-steps up to the diagonal
