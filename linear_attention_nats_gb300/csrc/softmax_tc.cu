@@ -7,23 +7,29 @@
 // computed, so every query of chunk c attends to the retained chunks before
 // c plus its own chunk causally (diagonal included).
 //
-// Tiling.  A CTA owns one 128-row query tile = the two chunks c0 = 2p and
-// c1 = 2p + 1 of one (b, h).  Its key/value blocks are 128 keys = two 64-token
-// chunk slots: first the softmax chunks before c0 (sel_idx[0 .. nprev[c0]),
-// in pairs), then the diagonal block (c0, c1).  Rows of c1 also see c0 when c0
+// Tiling.  A query tile is 128 rows = the two chunks c0 = 2p and c1 = 2p + 1
+// of one (b, h).  Its key/value blocks are 128 keys = two 64-token chunk
+// slots: first the softmax chunks before c0 (sel_idx[0 .. nprev[c0]), in
+// pairs), then the diagonal block (c0, c1).  Rows of c1 also see c0 when c0
 // chose softmax; both diagonal slots are causal for their own rows.  Slots
 // without a chunk are loaded with c0 (finite data) and masked.
 //
+// Persistent CTAs walk a static list of tiles ordered heaviest first (nprev
+// grows with c); every role of a CTA walks the same list.
 // Roles (256 threads):
-//   warp 0     TMA producer: Q tile once, then K/V blocks into two stages
-//   warp 1     TMEM owner + MMA issuer: S_j = Q K_j^T (TMEM), O += P_j V_j (TMEM)
-//   warps 4-7  softmax: thread r owns query row r (its TMEM lane); online
-//              softmax in the exp2 domain, P_j written to shared memory as the
-//              bf16 A operand of the next MMA.  The running max used for the
-//              exponent is raised (and O, l rescaled in place) only when a
-//              row's max grows by more than 2^8, so P stays <= 256 and the
-//              rescale (which waits for the previous P V product) is rare.
-// TMEM: two S buffers (2 x 128 columns) + the O accumulator (D columns).
+//   warp 0     TMA producer: Q of each tile, then K and V blocks into a
+//              3-deep ring (K and V with separate barriers)
+//   warp 1     TMEM owner + MMA issuer: S_j = Q K_j^T into one of two TMEM S
+//              buffers; O += P_j V_j with P_j read from TMEM (it overwrites
+//              S_j in place) into one of two TMEM O buffers (one per tile,
+//              alternating, so a tile's epilogue overlaps the next tile)
+//   warps 4-7  softmax: thread r owns query row r (its TMEM lane); one pass
+//              over the row in the exp2 domain; P_j packed to bf16 in TMEM.
+//              The running max used for the exponent is raised (and O, l
+//              rescaled in place) only when a row max grows by more than 2^8,
+//              so P <= 256 and the rescale, which waits for the previous
+//              P V product, is rare.
+// TMEM: S0, S1 (128 columns each), O0, O1 (D columns each).
 // Every wait is bounded (tc::kWaitLimitNs); on expiry the kernel records an
 // error, drains what it issued and exits.
 #include <mutex>
@@ -36,27 +42,60 @@ namespace nats {
 namespace {
 
 enum { kFull = 0, kCausal = 1, kNone = 2 };
+constexpr float kRescaleLog2 = 8.f;  // lazy-rescale threshold (log2 units)
+constexpr int KS = 3;                // K/V ring depth
 
 template <int D>
 struct SoftmaxSmem {
-  static constexpr int kHalf = 128 * 128;           // bytes of one 128-row x 64-col bf16 block
+  static constexpr int kHalf = 128 * 128;  // bytes of one 128-line x 64-col bf16 block
   static constexpr int kQ = 128 * D * 2;
   static constexpr int kKV = 128 * D * 2;
-  static constexpr int kP = 128 * 128 * 2;
   static constexpr int offQ = 0;
-  static constexpr int offK = offQ + kQ;           // 2 stages
-  static constexpr int offV = offK + 2 * kKV;      // 2 stages
-  static constexpr int offP = offV + 2 * kKV;      // 2 buffers
-  static constexpr int offBar = offP + 2 * kP;
-  static constexpr int kNumBars = 12;
+  static constexpr int offK = offQ + kQ;
+  static constexpr int offV = offK + KS * kKV;
+  static constexpr int offBar = offV + KS * kKV;
+  static constexpr int kNumBars = 2 + 4 * KS + 10;
   static constexpr int offTmem = offBar + kNumBars * 8;
   static constexpr int kBytes = offTmem + 16 + 1024;  // + alignment slack
 };
 
 // barrier slots
-enum { B_Q = 0, B_KVF = 1, B_KVE = 3, B_SF = 5, B_PF = 7, B_OF = 9, B_DONE = 11 };
+enum {
+  B_QF = 0, B_QE = 1, B_KF = 2, B_KE = B_KF + KS, B_VF = B_KE + KS, B_VE = B_VF + KS,
+  B_SF = B_VE + KS, B_PF = B_SF + 2, B_PV = B_PF + 2, B_OF = B_PV + 2, B_OE = B_OF + 2
+};
 
-constexpr float kRescaleLog2 = 8.f;  // lazy-rescale threshold (log2 units)
+// Masked keys of a 32-column chunk become -inf.  key0 = index of v[0] within
+// its 64-token chunk slot; rr = this row's index within its own chunk.
+__device__ __forceinline__ void mask_chunk(float (&v)[32], int mode, int key0, int rr) {
+  if (mode == kNone) {
+#pragma unroll
+    for (int x = 0; x < 32; ++x) v[x] = -INFINITY;
+  } else if (mode == kCausal) {
+#pragma unroll
+    for (int x = 0; x < 32; ++x) v[x] = (key0 + x <= rr) ? v[x] : -INFINITY;
+  }
+}
+
+struct TileInfo {
+  int p, c0, n0, nbp, nb;
+  long long bh;
+  bool has_c1, c0_soft;
+};
+
+__device__ __forceinline__ TileInfo tile_info(int i, long long BH, int T, int N, const int32_t* nprev,
+                                              const uint8_t* sel) {
+  TileInfo t;
+  t.p = T - 1 - (int)(i / BH);
+  t.bh = i % BH;
+  t.c0 = 2 * t.p;
+  t.has_c1 = t.c0 + 1 < N;
+  t.n0 = nprev[t.bh * N + t.c0];
+  t.nbp = (t.n0 + 1) >> 1;
+  t.nb = t.nbp + 1;
+  t.c0_soft = sel[t.bh * N + t.c0] == 0;
+  return t;
+}
 
 template <int D>
 __global__ void __launch_bounds__(256, 1)
@@ -70,29 +109,25 @@ __global__ void __launch_bounds__(256, 1)
   uint8_t* Qs = smem + S::offQ;
   uint64_t* bars = (uint64_t*)(smem + S::offBar);
   uint32_t* tmem_slot = (uint32_t*)(smem + S::offTmem);
-
-  const long long bid = blockIdx.x;
-  const int p = T - 1 - (int)(bid / BH);  // heaviest tiles first
-  const long long bh = bid % BH;
-  const int c0 = 2 * p, c1 = 2 * p + 1;
-  const bool has_c1 = c1 < N;
-  const int n0 = nprev[bh * N + c0];
-  const int nbp = (n0 + 1) >> 1;  // prefix blocks
-  const int nb = nbp + 1;         // + diagonal block
-  const bool c0_soft = sel[bh * N + c0] == 0;
+  const int n_tiles = (int)(BH * T);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long row0 = bh * (long long)L;
 
   if (threadIdx.x == 0) {
-    tc::mbar_init(&bars[B_Q], 1);
-    for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(&bars[B_KVF + s], 1);
-      tc::mbar_init(&bars[B_KVE + s], 1);
-      tc::mbar_init(&bars[B_SF + s], 1);
-      tc::mbar_init(&bars[B_PF + s], 128);
-      tc::mbar_init(&bars[B_OF + s], 1);
+    tc::mbar_init(&bars[B_QF], 1);
+    tc::mbar_init(&bars[B_QE], 1);
+    for (int s = 0; s < KS; ++s) {
+      tc::mbar_init(&bars[B_KF + s], 1);
+      tc::mbar_init(&bars[B_KE + s], 1);
+      tc::mbar_init(&bars[B_VF + s], 1);
+      tc::mbar_init(&bars[B_VE + s], 1);
     }
-    tc::mbar_init(&bars[B_DONE], 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&bars[B_SF + b], 1);
+      tc::mbar_init(&bars[B_PF + b], 128);
+      tc::mbar_init(&bars[B_PV + b], 1);
+      tc::mbar_init(&bars[B_OF + b], 1);
+      tc::mbar_init(&bars[B_OE + b], 128);
+    }
     tc::fence_barrier_init();
   }
   if (warp == 1) {
@@ -110,48 +145,58 @@ __global__ void __launch_bounds__(256, 1)
       tc::prefetch_tensormap(&tm_q);
       tc::prefetch_tensormap(&tm_k);
       tc::prefetch_tensormap(&tm_v);
-      tc::mbar_arrive_expect_tx(&bars[B_Q], S::kQ);
-      for (int h = 0; h < D / 64; ++h)
-        for (int rc = 0; rc < 2; ++rc)
-          tc::tma_load_2d(Qs + h * S::kHalf + rc * (S::kHalf / 2), &tm_q, 64 * h,
-                          (int)(row0 + 128LL * p + 64 * rc), &bars[B_Q]);
-      int issued[2] = {0, 0};
+      int gj = 0, tn = 0;
       bool ok = true;
-      for (int j = 0; j < nb && ok; ++j) {
-        const int s = j & 1;
-        if (!tc::mbar_wait(&bars[B_KVE + s], ((j >> 1) & 1) ^ 1, err)) {
-          ok = false;
-          break;
+      for (int i = blockIdx.x; i < n_tiles && ok; i += gridDim.x, ++tn) {
+        const TileInfo ti = tile_info(i, BH, T, N, nprev, sel);
+        const long long row0 = ti.bh * (long long)L;
+        if (!(ok = tc::mbar_wait(&bars[B_QE], (tn & 1) ^ 1, err))) break;
+        tc::mbar_arrive_expect_tx(&bars[B_QF], S::kQ);
+        for (int h = 0; h < D / 64; ++h)
+          for (int rc = 0; rc < 2; ++rc)
+            tc::tma_load_2d(Qs + h * S::kHalf + rc * (S::kHalf / 2), &tm_q, 64 * h,
+                            (int)(row0 + 128LL * ti.p + 64 * rc), &bars[B_QF]);
+        for (int j = 0; j < ti.nb; ++j, ++gj) {
+          const int ks = gj % KS, par = ((gj / KS) & 1) ^ 1;
+          int ch[2];
+          if (j < ti.nbp) {
+            ch[0] = sel_idx[ti.bh * N + 2 * j];
+            ch[1] = (2 * j + 1 < ti.n0) ? sel_idx[ti.bh * N + 2 * j + 1] : ti.c0;
+          } else {
+            ch[0] = ti.c0;
+            ch[1] = ti.has_c1 ? ti.c0 + 1 : ti.c0;
+          }
+          uint8_t* Kb = smem + S::offK + ks * S::kKV;
+          uint8_t* Vb = smem + S::offV + ks * S::kKV;
+          if (!(ok = tc::mbar_wait(&bars[B_KE + ks], par, err))) break;
+          tc::mbar_arrive_expect_tx(&bars[B_KF + ks], S::kKV);
+          for (int slot = 0; slot < 2; ++slot)
+            for (int h = 0; h < D / 64; ++h)
+              tc::tma_load_2d(Kb + h * S::kHalf + slot * (S::kHalf / 2), &tm_k, 64 * h,
+                              (int)(row0 + 64LL * ch[slot]), &bars[B_KF + ks]);
+          if (!(ok = tc::mbar_wait(&bars[B_VE + ks], par, err))) break;
+          tc::mbar_arrive_expect_tx(&bars[B_VF + ks], S::kKV);
+          for (int slot = 0; slot < 2; ++slot)
+            for (int h = 0; h < D / 64; ++h)
+              tc::tma_load_2d(Vb + h * S::kHalf + slot * (S::kHalf / 2), &tm_v, 64 * h,
+                              (int)(row0 + 64LL * ch[slot]), &bars[B_VF + ks]);
         }
-        int ch[2];
-        if (j < nbp) {
-          ch[0] = sel_idx[bh * N + 2 * j];
-          ch[1] = (2 * j + 1 < n0) ? sel_idx[bh * N + 2 * j + 1] : c0;
-        } else {
-          ch[0] = c0;
-          ch[1] = has_c1 ? c1 : c0;
-        }
-        uint8_t* Ks = smem + S::offK + s * S::kKV;
-        uint8_t* Vs = smem + S::offV + s * S::kKV;
-        tc::mbar_arrive_expect_tx(&bars[B_KVF + s], 2 * S::kKV);
-        for (int slot = 0; slot < 2; ++slot) {
-          const int y = (int)(row0 + 64LL * ch[slot]);
-          for (int h = 0; h < D / 64; ++h) {
-            tc::tma_load_2d(Ks + h * S::kHalf + slot * (S::kHalf / 2), &tm_k, 64 * h, y, &bars[B_KVF + s]);
-            tc::tma_load_2d(Vs + h * S::kHalf + slot * (S::kHalf / 2), &tm_v, 64 * h, y, &bars[B_KVF + s]);
+      }
+      // make sure every load completed and every release commit landed
+      for (int s = 0; s < KS; ++s) {
+        const int uses = gj > s ? (gj - 1 - s) / KS + 1 : 0;
+        if (uses > 0) {
+          tc::mbar_wait(&bars[B_KF + s], (uses - 1) & 1, nullptr);
+          tc::mbar_wait(&bars[B_VF + s], (uses - 1) & 1, nullptr);
+          if (ok) {
+            tc::mbar_wait(&bars[B_KE + s], (uses - 1) & 1, err);
+            tc::mbar_wait(&bars[B_VE + s], (uses - 1) & 1, err);
           }
         }
-        issued[s]++;
       }
-      if (ok) {
-        // the last commits on the "empty" barriers must land before exit
-        for (int s = 0; s < 2; ++s)
-          if (issued[s] > 0) tc::mbar_wait(&bars[B_KVE + s], (issued[s] - 1) & 1, err);
-      } else {
-        // drain loads still in flight
-        tc::mbar_wait(&bars[B_Q], 0, nullptr);
-        for (int s = 0; s < 2; ++s)
-          if (issued[s] > 0) tc::mbar_wait(&bars[B_KVF + s], (issued[s] - 1) & 1, nullptr);
+      if (tn > 0) {
+        tc::mbar_wait(&bars[B_QF], (tn - 1) & 1, nullptr);
+        if (ok) tc::mbar_wait(&bars[B_QE], (tn - 1) & 1, err);
       }
     }
   } else if (warp == 1) {
@@ -160,162 +205,179 @@ __global__ void __launch_bounds__(256, 1)
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, D, false, true);
       const uint32_t q_base = tc::smem_u32(Qs);
-      bool ok = tc::mbar_wait(&bars[B_Q], 0, err);
-      auto issue_s = [&](int j) -> bool {
-        const int s = j & 1;
-        if (!tc::mbar_wait(&bars[B_KVF + s], (j >> 1) & 1, err)) return false;
+      int gj = 0, tn = 0;
+      bool ok = true;
+      auto issue_s = [&](int g) -> bool {
+        const int ks = g % KS;
+        if (!tc::mbar_wait(&bars[B_KF + ks], (g / KS) & 1, err)) return false;
         tc::fence_after();
-        const uint32_t k_base = tc::smem_u32(smem + S::offK + s * S::kKV);
+        const uint32_t k_base = tc::smem_u32(smem + S::offK + ks * S::kKV);
+        const uint32_t tS = tmem + (g & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * S::kHalf + (kk & 3) * 32;
-          tc::mma_bf16(tmem + s * 128, tc::smem_desc_sw128(q_base + off, 16, 1024),
-                       tc::smem_desc_sw128(k_base + off, 16, 1024), idesc_qk, kk > 0);
+          tc::mma_bf16(tS, tc::smem_desc_sw128(q_base + off, 16, 1024), tc::smem_desc_sw128(k_base + off, 16, 1024),
+                       idesc_qk, kk > 0);
         }
-        tc::mma_commit(&bars[B_SF + s]);
+        tc::mma_commit(&bars[B_SF + (g & 1)]);
+        tc::mma_commit(&bars[B_KE + ks]);
         return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; j < nb && ok; ++j) {
-        if (j + 1 < nb && !(ok = issue_s(j + 1))) break;
-        const int b = j & 1;
-        if (!(ok = tc::mbar_wait(&bars[B_PF + b], (j >> 1) & 1, err))) break;
+      for (int i = blockIdx.x; i < n_tiles && ok; i += gridDim.x, ++tn) {
+        const TileInfo ti = tile_info(i, BH, T, N, nprev, sel);
+        const int ob = tn & 1;
+        const uint32_t tO = tmem + 256 + ob * 128;
+        if (!(ok = tc::mbar_wait(&bars[B_QF], tn & 1, err))) break;
+        if (!(ok = tc::mbar_wait(&bars[B_OE + ob], ((tn >> 1) & 1) ^ 1, err))) break;
         tc::fence_after();
-        const uint32_t p_base = tc::smem_u32(smem + S::offP + b * S::kP);
-        const uint32_t v_base = tc::smem_u32(smem + S::offV + b * S::kKV);
+        const int g0 = gj;
+        if (!(ok = issue_s(g0))) break;
+        if (ti.nb == 1) tc::mma_commit(&bars[B_QE]);
+        for (int j = 0; j < ti.nb; ++j) {
+          const int g = g0 + j;
+          if (j + 1 < ti.nb) {
+            if (!(ok = issue_s(g + 1))) break;
+            if (j + 2 == ti.nb) tc::mma_commit(&bars[B_QE]);
+          }
+          const int b = g & 1, ks = g % KS;
+          if (!(ok = tc::mbar_wait(&bars[B_PF + b], (g >> 1) & 1, err))) break;
+          if (!(ok = tc::mbar_wait(&bars[B_VF + ks], (g / KS) & 1, err))) break;
+          tc::fence_after();
+          const uint32_t v_base = tc::smem_u32(smem + S::offV + ks * S::kKV);
+          const uint32_t tP = tmem + b * 128;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          tc::mma_bf16(tmem + 256,
-                       tc::smem_desc_sw128(p_base + (kk >> 2) * S::kHalf + (kk & 3) * 32, 16, 1024),
-                       tc::smem_desc_sw128(v_base + kk * 2048, S::kHalf, 1024), idesc_pv, (j > 0) || (kk > 0));
+          for (int kk = 0; kk < 8; ++kk)
+            tc::mma_bf16_ts(tO, tP + kk * 8, tc::smem_desc_sw128(v_base + kk * 2048, S::kHalf, 1024), idesc_pv,
+                            (j > 0) || (kk > 0));
+          tc::mma_commit(&bars[B_PV + b]);
+          tc::mma_commit(&bars[B_VE + ks]);
         }
-        tc::mma_commit(&bars[B_OF + b]);
-        tc::mma_commit(&bars[B_KVE + b]);
+        if (!ok) break;
+        gj = g0 + ti.nb;
+        tc::mma_commit(&bars[B_OF + ob]);
       }
-      tc::mma_commit(&bars[B_DONE]);
-      tc::mbar_wait(&bars[B_DONE], 0, err);
+      // drain: every MMA issued so far completes before the commits land
+      tc::mma_commit(&bars[B_PV + 0]);
+      tc::mma_commit(&bars[B_PV + 1]);
+      const int lastpv0 = gj / 2 + (gj & 1);  // uses of B_PV[0] before the drain commit (blocks with g even)
+      const int lastpv1 = gj / 2;
+      tc::mbar_wait(&bars[B_PV + 0], lastpv0 & 1, nullptr);
+      tc::mbar_wait(&bars[B_PV + 1], lastpv1 & 1, nullptr);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------- softmax
     const int r = threadIdx.x - 128;
     const int half = r >> 6, rr = r & 63;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-    const uint32_t o_addr = tmem + 256 + lane_off;
-    float m_used = -INFINITY, l = 0.f;
+    int gj = 0, tn = 0;
     bool ok = true;
-    for (int j = 0; j < nb; ++j) {
-      const int b = j & 1;
-      if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_SF + b], (j >> 1) & 1, err)))) break;
-      tc::fence_after();
-      int mode[2];
-      if (j < nbp) {
-        mode[0] = kFull;
-        mode[1] = (2 * j + 1 < n0) ? kFull : kNone;
-      } else if (half == 0) {
-        mode[0] = kCausal;
-        mode[1] = kNone;
-      } else {
-        mode[0] = has_c1 ? (c0_soft ? kFull : kNone) : kFull;
-        mode[1] = has_c1 ? kCausal : kNone;
-      }
-      const uint32_t s_addr = tmem + b * 128 + lane_off;
-      float mx = -INFINITY;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        float v[32];
-        tc::tmem_ld32(s_addr + ch * 32, v);
-        tc::tmem_ld_wait();
-        const int md = mode[ch >> 1];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = (ch & 1) * 32 + i;
-          const bool keep = (md == kFull) || (md == kCausal && key <= rr);
-          mx = keep ? fmaxf(mx, v[i]) : mx;
+    for (int i = blockIdx.x; i < n_tiles && ok; i += gridDim.x, ++tn) {
+      const TileInfo ti = tile_info(i, BH, T, N, nprev, sel);
+      const int ob = tn & 1;
+      const uint32_t o_addr = tmem + 256 + ob * 128 + lane_off;
+      float m_used = -INFINITY, l = 0.f;
+      for (int j = 0; j < ti.nb; ++j, ++gj) {
+        const int b = gj & 1;
+        if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_SF + b], (gj >> 1) & 1, err)))) break;
+        tc::fence_after();
+        int mode0, mode1;
+        if (j < ti.nbp) {
+          mode0 = kFull;
+          mode1 = (2 * j + 1 < ti.n0) ? kFull : kNone;
+        } else if (half == 0) {
+          mode0 = kCausal;
+          mode1 = kNone;
+        } else {
+          mode0 = ti.has_c1 ? (ti.c0_soft ? kFull : kNone) : kFull;
+          mode1 = ti.has_c1 ? kCausal : kNone;
         }
-      }
-      const float m_cand = mx * sl2;  // every row sees >= 1 key of every block
-      // P[b] is free once P_{j-2} V_{j-2} is done
-      if (j >= 2 && !(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_OF + b], ((j - 2) >> 1) & 1, err))))
-        break;
-      if (j == 0) {
-        m_used = m_cand;
-      } else {
-        const bool need = m_cand > m_used + kRescaleLog2;
+        const uint32_t s_addr = tmem + b * 128 + lane_off;
+        // pass 1: row max over the visible keys, 32 columns at a time, with
+        // eight independent partial maxima (short dependency chains).  The
+        // mask pattern is uniform across a warp (a warp's rows share a half).
+        const bool masked = (mode0 != kFull) || (mode1 != kFull);
+        float mxa[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) mxa[x] = -INFINITY;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          float v[32];
+          tc::tmem_ld32(s_addr + ch * 32, v);
+          tc::tmem_ld_wait();
+          if (masked) mask_chunk(v, ch < 2 ? mode0 : mode1, (ch & 1) * 32, rr);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) mxa[x & 7] = fmaxf(mxa[x & 7], v[x]);
+        }
+        const float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+                               fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
+        const float m_cand = mx * sl2;  // every row sees >= 1 key of every block
+        const bool need = (j > 0) && (m_cand > m_used + kRescaleLog2);
+        const float alpha = need ? tc::fast_exp2(m_used - m_cand) : 1.f;
+        if (j == 0 || need) m_used = m_cand;
+        // pass 2: P = exp2(S scale - m) (masked keys -> exp2(-inf) = 0), packed
+        // to bf16 over S in place (P column c holds keys 2c, 2c+1)
+        float sa[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) sa[x] = 0.f;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          float v[32];
+          tc::tmem_ld32(s_addr + ch * 32, v);
+          tc::tmem_ld_wait();
+          if (masked) mask_chunk(v, ch < 2 ? mode0 : mode1, (ch & 1) * 32, rr);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            v[x] = tc::fast_exp2(fmaf(v[x], sl2, -m_used));
+            sa[x & 7] += v[x];
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) pk[x] = tc::pack_bf16x2(v[2 * x], v[2 * x + 1]);
+          tc::tmem_st16u(s_addr + ch * 16, pk);
+        }
+        const float sum = ((sa[0] + sa[1]) + (sa[2] + sa[3])) + ((sa[4] + sa[5]) + (sa[6] + sa[7]));
+        tc::tmem_st_wait();
         if (__any_sync(0xffffffffu, need)) {
           // O must hold every product so far before it is rescaled in place
-          const int jp = j - 1;
-          if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_OF + (jp & 1)], (jp >> 1) & 1, err)))) break;
+          const int gp = gj - 1;
+          if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_PV + (gp & 1)], (gp >> 1) & 1, err)))) break;
           tc::fence_after();
-          const float alpha = need ? tc::fast_exp2(m_used - m_cand) : 1.f;
 #pragma unroll 1
           for (int ch = 0; ch < D / 32; ++ch) {
-            float v[32];
-            tc::tmem_ld32(o_addr + ch * 32, v);
+            float o[32];
+            tc::tmem_ld32(o_addr + ch * 32, o);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= alpha;
-            tc::tmem_st32(o_addr + ch * 32, v);
+            for (int x = 0; x < 32; ++x) o[x] *= alpha;
+            tc::tmem_st32(o_addr + ch * 32, o);
           }
           tc::tmem_st_wait();
-          if (need) {
-            l *= alpha;
-            m_used = m_cand;
-          }
         }
+        l = l * alpha + sum;
+        tc::fence_before();
+        tc::mbar_arrive(&bars[B_PF + b]);
       }
-      float sum = 0.f;
-      uint8_t* Pb = smem + S::offP + b * S::kP;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        float v[32];
-        tc::tmem_ld32(s_addr + ch * 32, v);
-        tc::tmem_ld_wait();
-        const int md = mode[ch >> 1];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = (ch & 1) * 32 + i;
-          const bool keep = (md == kFull) || (md == kCausal && key <= rr);
-          v[i] = keep ? tc::fast_exp2(fmaf(v[i], sl2, -m_used)) : 0.f;
-          sum += v[i];
-        }
-        uint8_t* row = Pb + (ch >> 1) * S::kHalf + r * 128;
-#pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4) {
-          const int g = (ch & 1) * 4 + g4;
-          uint4 pk;
-          pk.x = tc::pack_bf16x2(v[g4 * 8 + 0], v[g4 * 8 + 1]);
-          pk.y = tc::pack_bf16x2(v[g4 * 8 + 2], v[g4 * 8 + 3]);
-          pk.z = tc::pack_bf16x2(v[g4 * 8 + 4], v[g4 * 8 + 5]);
-          pk.w = tc::pack_bf16x2(v[g4 * 8 + 6], v[g4 * 8 + 7]);
-          *(uint4*)(row + ((g ^ (r & 7)) << 4)) = pk;
-        }
-      }
-      l += sum;
-      tc::fence_proxy_async_smem();
-      tc::fence_before();
-      tc::mbar_arrive(&bars[B_PF + b]);
-    }
-    if (ok) {
-      const int jl = nb - 1;
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_OF + (jl & 1)], (jl >> 1) & 1, err));
-    }
-    if (ok) {
+      if (!ok) break;
+      // epilogue: O / l -> o_s
+      if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_OF + ob], (tn >> 1) & 1, err)))) break;
       tc::fence_after();
       const float inv = 1.f / l;
-      const bool valid = (half == 0 || has_c1);
-      float* dst = o_s + (size_t)(row0 + 128LL * p + r) * D;
+      const bool valid = (half == 0 || ti.has_c1);
+      float* dst = o_s + (size_t)(ti.bh * (long long)L + 128LL * ti.p + r) * D;
 #pragma unroll 1
       for (int ch = 0; ch < D / 32; ++ch) {
-        float v[32];
-        tc::tmem_ld32(o_addr + ch * 32, v);
+        float o[32];
+        tc::tmem_ld32(o_addr + ch * 32, o);
         tc::tmem_ld_wait();
         if (valid) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            ((float4*)(dst + ch * 32))[i] =
-                make_float4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+          for (int x = 0; x < 8; ++x)
+            ((float4*)(dst + ch * 32))[x] = make_float4(o[4 * x] * inv, o[4 * x + 1] * inv, o[4 * x + 2] * inv,
+                                                       o[4 * x + 3] * inv);
         }
       }
+      tc::fence_before();
+      tc::mbar_arrive(&bars[B_OE + ob]);
     }
   }
   tc::fence_before();
@@ -372,9 +434,13 @@ static cudaError_t launch_tc_t(const Problem& p, const void* q, const void* k, c
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int T = (p.N + 1) / 2;
-  const long long blocks = p.BH * T;
-  kern<<<(unsigned)blocks, 256, smem, st>>>(mq, mk, mv, nprev, sel_idx, sel, p.L, p.N, T, p.BH,
-                                            p.scale * 1.4426950408889634f, o_s, err);
+  const long long tiles = p.BH * T;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
+  kern<<<grid, 256, smem, st>>>(mq, mk, mv, nprev, sel_idx, sel, p.L, p.N, T, p.BH,
+                                p.scale * 1.4426950408889634f, o_s, err);
   return cudaGetLastError();
 }
 
