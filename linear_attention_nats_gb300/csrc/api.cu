@@ -65,6 +65,8 @@ size_t layout(const Problem& p, char* base, Workspace* ws) {
   w.P = (float*)take(4 * BH * N * C * C);
   w.o_s = (float*)take(4 * BH * L * D);
   w.o_l = (float*)take(4 * BH * L * D);
+  w.Qt = (void*)take(2 * BH * L * D);
+  w.Kt = (void*)take(2 * BH * L * D);
   w.err = (int*)take(16);
   if (ws) *ws = w;
   return off;
@@ -195,9 +197,9 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
   if (dt == NATS_BF16) {
     // bf16 factors W, U, P reuse the fp32 factor buffers of the workspace
     NATS_STAGE(stg, NATS_STAGE_GDN_PREP, 1,
-               launch_gdn_prep_mma(p, q, k, v, g, beta, ws.G, ws.W, ws.U, ws.P, st));
+               launch_gdn_prep_mma(p, q, k, v, g, beta, ws.G, ws.W, ws.U, ws.P, ws.Qt, ws.Kt, st));
     NATS_STAGE(stg, NATS_STAGE_GDN_SCAN, 1,
-               launch_gdn_scan_tc(p, q, k, sel, ws.G, ws.W, ws.U, ws.P, o_l, state_out, ws.err, st));
+               launch_gdn_scan_tc(p, ws.Kt, sel, ws.G, ws.W, ws.U, ws.P, ws.Qt, o_l, state_out, ws.err, st));
   } else {
     NATS_STAGE(stg, NATS_STAGE_GDN_PREP, 1, launch_gdn_prep_simt(p, dt, q, k, v, g, beta, ws, st));
     NATS_STAGE(stg, NATS_STAGE_GDN_SCAN, 1,

@@ -50,11 +50,13 @@ struct Workspace {
   int32_t* nprev;    // [BH, N]   softmax chunks before chunk c
   int32_t* sel_idx;  // [BH, N]   compacted list of softmax chunks, in order
   float* G;          // [BH, L]   in-chunk cumulative log-decay
-  float* W;          // [BH, N, C, dk]  T diag(beta e^G) K
-  float* U;          // [BH, N, C, dv]  T diag(beta) V
+  float* W;          // [BH, N, C, dk]  T diag(beta e^G) K  (bf16 path: bf16)
+  float* U;          // [BH, N, C, dv]  T diag(beta) V      (bf16 path: bf16, transposed [dv][C])
   float* P;          // [BH, N, C, C]   lower(e^{G_t - G_i} scale q_t . k_i)
   float* o_s;        // [BH, L, dv] softmax branch output (before norm)
   float* o_l;        // [BH, L, dv] Gated DeltaNet branch output (before norm)
+  void* Qt;          // [BH, L, dk] bf16 diag(scale e^G) Q, per chunk (bf16 path)
+  void* Kt;          // [BH, L, dk] bf16 diag(e^{G_C - G}) K, per chunk (bf16 path)
   int* err;          // [1] set by a kernel whose bounded wait expired (zeroed per call)
 };
 

@@ -8,9 +8,12 @@
 //   A = strict_lower(beta_t e^{G_t - G_i} k_t . k_i),  T = (I + A)^{-1}
 //   U = T diag(beta) V,  W = T diag(beta e^G) K,  P = lower_incl(scale e^{G_t - G_i} q_t . k_i)
 // KK^T / QK^T and T.(beta V) / T.(beta e^G K) are warp-level bf16 MMAs
-// (fp32 accumulate); the unit-lower-triangular inverse is fp32 forward
-// substitution.  Outputs: W, U as bf16 [chunk][64][D], P as bf16 [chunk][64][64]
-// (the operands of the chunk scan), G as fp32.
+// (fp32 accumulate); the unit-lower-triangular inverse is fp32, blocked in
+// 16 x 16 tiles.  Outputs (the operands of the chunk scan): W bf16
+// [chunk][64][D]; U transposed, bf16 [chunk][D][64]; P bf16 [chunk][64][64];
+// Q~ = diag(scale e^G) Q, bf16 [chunk][64][D] (the query with its readout
+// decay and scale folded in); K~ = diag(e^{G_C - G}) K, bf16 [chunk][64][D]
+// (the key with the decay to the chunk end folded in); G fp32.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -77,7 +80,8 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
     const __nv_bfloat16* __restrict__ v, const float* __restrict__ g, const float* __restrict__ beta, int L,
     int N, float scale, float* __restrict__ Gout, __nv_bfloat16* __restrict__ Wout,
-    __nv_bfloat16* __restrict__ Uout, __nv_bfloat16* __restrict__ Pout) {
+    __nv_bfloat16* __restrict__ Uout, __nv_bfloat16* __restrict__ Pout, __nv_bfloat16* __restrict__ Qtout,
+    __nv_bfloat16* __restrict__ Ktout) {
   using S = PrepSmem<D>;
   constexpr int RS = S::RS, TS = S::TS;
   extern __shared__ __align__(16) uint8_t smem[];
@@ -90,6 +94,9 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
   float* Gs = (float*)(smem + S::offG);
   float* Bs = (float*)(smem + S::offB);
   float* Bg = (float*)(smem + S::offBg);
+  constexpr int UTS = C + 8;  // bf16 line stride of the staged U^T
+  __nv_bfloat16* UTs = (__nv_bfloat16*)(smem + S::offA);  // reuses A and T once T is in Tb
+  static_assert(D * UTS * 2 <= 2 * C * (C + 1) * 4, "U^T staging must fit the A / T scratch");
 
   const long long blk = blockIdx.x;
   const int c = (int)(blk % N);
@@ -176,6 +183,33 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
     }
   }
   __syncthreads();
+  // ---- Q~ = diag(scale e^G) Q and K~ = diag(e^{G_C - G}) K -> global (16-byte stores)
+  {
+    __nv_bfloat16* Qt = Qtout + tok0 * D;
+    __nv_bfloat16* Kt = Ktout + tok0 * D;
+    const float GC = Gs[C - 1];
+    for (int e = tid; e < C * VPR; e += 128) {
+      const int t = e / VPR, x = e % VPR;
+      const float fq = scale * __expf(Gs[t]);
+      const float fk = __expf(GC - Gs[t]);
+      const uint4 inq = *(const uint4*)(Qs + t * RS + x * 8);
+      const uint4 ink = *(const uint4*)(Ks + t * RS + x * 8);
+      const __nv_bfloat162* hq = (const __nv_bfloat162*)&inq;
+      const __nv_bfloat162* hk = (const __nv_bfloat162*)&ink;
+      uint4 oq, ok;
+      uint32_t* q32 = (uint32_t*)&oq;
+      uint32_t* k32 = (uint32_t*)&ok;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 vq = __bfloat1622float2(hq[i]);
+        const float2 vk = __bfloat1622float2(hk[i]);
+        q32[i] = pack2(vq.x * fq, vq.y * fq);
+        k32[i] = pack2(vk.x * fk, vk.y * fk);
+      }
+      *(uint4*)(Qt + t * D + x * 8) = oq;
+      *(uint4*)(Kt + t * D + x * 8) = ok;
+    }
+  }
   // ---- T = (I + A)^{-1}, unit lower triangular, blocked in 16 x 16 tiles:
   //   T_bb = (I + A_bb)^{-1}                          (forward substitution)
   //   T_ij = -T_ii sum_{j <= k < i} A_ik T_kj  (i > j, by distance i - j)
@@ -241,12 +275,11 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
     const int acol = 8 * (lane >> 4);
     const int trow = (lane & 7) + 8 * ((lane >> 3) & 1);  // k row within the 16-row step
     const int tcol = 8 * (lane >> 4);                     // n column offset
-    __nv_bfloat16* Ug = Uout + (size_t)blk * C * D;
     __nv_bfloat16* Wg = Wout + (size_t)blk * C * D;
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
       const __nv_bfloat16* Bsrc = which == 0 ? Vs : Ks;
-      __nv_bfloat16* dst = which == 0 ? Ug : Wg;
+      __nv_bfloat16* dst = Wg;
       float acc[D / 8][4];
 #pragma unroll
       for (int n = 0; n < D / 8; ++n)
@@ -263,12 +296,32 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
           mma16816(acc[2 * np + 1], a[0], a[1], a[2], a[3], b2, b3);
         }
       }
+      if (which == 0) {
+        // U^T staged in the (now dead) A / T scratch: line e, column t
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        const int col = 8 * n + 2 * cq;
-        *(uint32_t*)(dst + (m0 + gq) * D + col) = pack2(acc[n][0], acc[n][1]);
-        *(uint32_t*)(dst + (m0 + gq + 8) * D + col) = pack2(acc[n][2], acc[n][3]);
+        for (int n = 0; n < D / 8; ++n) {
+          const int e = 8 * n + 2 * cq;
+          UTs[e * UTS + m0 + gq] = __float2bfloat16_rn(acc[n][0]);
+          UTs[(e + 1) * UTS + m0 + gq] = __float2bfloat16_rn(acc[n][1]);
+          UTs[e * UTS + m0 + gq + 8] = __float2bfloat16_rn(acc[n][2]);
+          UTs[(e + 1) * UTS + m0 + gq + 8] = __float2bfloat16_rn(acc[n][3]);
+        }
+      } else {
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) {
+          const int col = 8 * n + 2 * cq;
+          *(uint32_t*)(dst + (m0 + gq) * D + col) = pack2(acc[n][0], acc[n][1]);
+          *(uint32_t*)(dst + (m0 + gq + 8) * D + col) = pack2(acc[n][2], acc[n][3]);
+        }
       }
+    }
+  }
+  __syncthreads();
+  {
+    __nv_bfloat16* Ug = Uout + (size_t)blk * C * D;  // [D][64]
+    for (int e8 = tid; e8 < D * 8; e8 += 128) {
+      const int e = e8 >> 3, x = e8 & 7;
+      *(uint4*)(Ug + e * C + x * 8) = *(const uint4*)(UTs + e * UTS + x * 8);
     }
   }
 }
@@ -276,14 +329,16 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
 }  // namespace
 
 cudaError_t launch_gdn_prep_mma(const Problem& p, const void* q, const void* k, const void* v, const float* g,
-                                const float* beta, float* G, void* W16, void* U16, void* P16, cudaStream_t st) {
+                                const float* beta, float* G, void* W16, void* U16, void* P16, void* Qt16,
+                                void* Kt16, cudaStream_t st) {
   if (p.BH == 0 || p.N == 0) return cudaSuccess;
   auto run = [&](auto kern, int smem) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)(p.BH * p.N), 128, smem, st>>>(
         (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, g, beta, p.L, p.N, p.scale,
-        G, (__nv_bfloat16*)W16, (__nv_bfloat16*)U16, (__nv_bfloat16*)P16);
+        G, (__nv_bfloat16*)W16, (__nv_bfloat16*)U16, (__nv_bfloat16*)P16, (__nv_bfloat16*)Qt16,
+        (__nv_bfloat16*)Kt16);
     return cudaGetLastError();
   };
   return p.d == 64 ? run(gdn_prep_mma_kernel<64>, PrepSmem<64>::kBytes)

@@ -4,23 +4,29 @@
 // "Neural Attention Search Linear (NAtS-L)", technical summary,
 // "Kernmechanismen" item 3: the linear state is pseudo-updated for every
 // chunk; for a chunk that chose softmax it is rolled back to the chunk start.
-// With the phase-1 factors W, U, P of a chunk (S0 = state at its start,
-// G = in-chunk cumulative log-decay, gamma = e^G):
-//   Delta = U - W S0^T
-//   O     = gamma * (scale Q S0^T) + P Delta
-//   S_C   = gamma_C S0 + Delta^T diag(gamma_C / gamma) K     (linear chunks only)
+// With the phase-1 factors of a chunk (S0 = state at its start, dv x dk;
+// G = in-chunk cumulative log-decay, gamma = e^G; Q~ = diag(scale gamma) Q;
+// K~ = diag(gamma_C / gamma) K):
+//   Delta^T = U^T - S0 W^T                    (dv x 64)
+//   O^T     = S0 Q~^T + Delta^T P^T           (dv x 64)
+//   S_C     = gamma_C S0 + Delta^T K~         (linear chunks only)
+// Everything is computed transposed, so the state row dv is the TMEM lane:
+// the per-chunk elementwise work spreads over all 128 lanes (all four SM
+// sub-partitions), and S0 and Delta^T stay in TMEM as MMA A operands.
 //
-// One CTA per (b, h) walks the N chunks in order; the fp32 state S (dv x dk)
-// stays in TMEM for the whole sequence and a bf16 copy in shared memory feeds
-// the next chunk's MMA.  Per chunk:
-//   MMA1  X = [W; Q] S0^T          (M=128 = 64 W rows + 64 Q rows, N=dv, K=dk)
-//   thr   Delta, Delta~ = diag(gamma_C/gamma) Delta -> smem (bf16); S *= gamma_C
-//   MMA2  Y = [. ; P] Delta        (rows 64..127 = P Delta, aligned with Q S0^T)
-//   MMA3  S += Delta~^T K          (linear chunks only; M = dv, N = dk, K = 64)
-//   thr   O = gamma scale (Q S0^T) + P Delta -> o_l;  S -> bf16 copy
-// Roles: warps 0-3 elementwise (thread r <-> TMEM lane r), warp 4 TMA
-// producer (W, Q, K, U, P of the next chunk, double-buffered), warp 5 TMEM
-// owner and MMA issuer.  Every wait is bounded (tc::kWaitLimitNs).
+// One CTA per (b, h) walks the N chunks in order; the fp32 state S stays in
+// TMEM for the whole sequence, next to its bf16 copy S0.  Per chunk c:
+//   MMA1  Z[c&1] = S0 [W; Q~]^T          (M = 128 lanes >= dv, N = 64 + 64, K = dk)
+//   all   Delta^T = U^T - Z[:, 0:64] -> TMEM (bf16)
+//   MMA2  Z[:, 64:128] += Delta^T P^T    (= O^T)
+//   MMA3  S += Delta^T K~                (linear chunks only)
+//   all   S -> bf16 S0; S *= gamma_C of the next chunk when it is linear
+//   all   O^T -> o_l (after the state work, off the critical path; Z is
+//         double-buffered)
+// Roles (320 threads): warps 0-7 elementwise, warp w owning TMEM lanes
+// 32 (w % 4) .. +31 and half (w / 4) of the columns; warp 8 TMA producer
+// (W, Q~, K~, U^T, P of coming chunks, double-buffered); warp 9 TMEM owner and
+// MMA issuer.  Every wait is bounded (tc::kWaitLimitNs).
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -33,23 +39,27 @@ namespace {
 
 template <int D>
 struct ScanSmem {
-  static constexpr int kWQ = 128 * D * 2;  // [W; Q] tile, D/64 halves of 128 lines
-  static constexpr int kK = 64 * D * 2;    // K chunk, D/64 halves of 64 lines
-  static constexpr int kU = 64 * D * 2;    // U chunk
-  static constexpr int kP = 128 * 128;     // 128 lines x 64 cols (P in lines 64..127)
+  static constexpr int kWQ = 128 * D * 2;  // [W; Q~] tile: 128 lines (t), D/64 halves of 16 KiB
+  static constexpr int kK = 64 * D * 2;    // K chunk: 64 lines (t), D/64 halves of 8 KiB
+  static constexpr int kU = D * 64 * 2;    // U^T chunk: D lines (dv) x 64 cols (t), 8 KiB per 64 lines
+  static constexpr int kP = 64 * 64 * 2;   // P chunk: 64 lines (t) x 64 cols (i)
   static constexpr int kStage = kWQ + kK + kU + kP;
   static constexpr int offStage = 0;
-  static constexpr int offS0 = 2 * kStage;         // bf16 S0, K-major (lines dv, cols dk)
-  static constexpr int kS0 = D * D * 2;
-  static constexpr int offDelta = offS0 + kS0;     // Delta  [t][dv], MN-major B operand
-  static constexpr int offDeltaT = offDelta + 64 * D * 2;  // Delta~ [t][dv], MN-major A (2 halves)
-  static constexpr int offBar = offDeltaT + 64 * 128 * 2;
-  static constexpr int kNumBars = 10;
+  static constexpr int offBar = 2 * kStage;
+  static constexpr int kNumBars = 11;
   static constexpr int offTmem = offBar + kNumBars * 8;
   static constexpr int kBytes = offTmem + 16 + 1024;
 };
 
-enum { SB_FULL = 0, SB_EMPTY = 2, SB_S0 = 4, SB_X = 5, SB_DELTA = 6, SB_Y = 7, SB_SDONE = 8, SB_DONE = 9 };
+// SB_OFREE + b: O^T of the chunks using Z buffer b has been read (one barrier per
+// buffer, so a waiter is never two phases behind)
+enum { SB_FULL = 0, SB_EMPTY = 2, SB_S0 = 4, SB_Z = 5, SB_DELTA = 6, SB_OFREE = 7, SB_SDONE = 9, SB_DONE = 10 };
+
+// TMEM columns
+constexpr uint32_t kColZ = 0;      // two Z buffers of 128 columns
+constexpr uint32_t kColS = 256;    // state, D columns (fp32)
+constexpr uint32_t kColS0 = 384;   // state bf16, D / 2 columns (two dk per column)
+constexpr uint32_t kColDT = 448;   // Delta^T bf16, 32 columns (64 t)
 
 // byte offset of element (line, col) in a 128-byte-swizzled tile whose
 // 64-column halves are `half_bytes` apart
@@ -57,21 +67,26 @@ __device__ __forceinline__ uint32_t sw_off(int line, int col, int half_bytes) {
   return (uint32_t)((col >> 6) * half_bytes + line * 128 + ((((col & 63) >> 3) ^ (line & 7)) << 4) + (col & 7) * 2);
 }
 
+// bf16x2 with round-to-nearest-even in integer arithmetic (finite inputs)
+__device__ __forceinline__ uint32_t pack_rne(float lo, float hi) {
+  uint32_t a = __float_as_uint(lo), b = __float_as_uint(hi);
+  a += 0x7FFFu + ((a >> 16) & 1u);
+  b += 0x7FFFu + ((b >> 16) & 1u);
+  return __byte_perm(a, b, 0x7632);
+}
+
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     gdn_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_u,
                        const __grid_constant__ CUtensorMap tm_p, const uint8_t* __restrict__ sel,
-                       const float* __restrict__ G, int L, int N, float scale, float* __restrict__ o_l,
+                       const float* __restrict__ G, int L, int N, float* __restrict__ o_l,
                        float* __restrict__ state_out, int* __restrict__ err) {
   using S = ScanSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + S::offBar);
   uint32_t* tmem_slot = (uint32_t*)(smem + S::offTmem);
-  uint8_t* S0s = smem + S::offS0;
-  uint8_t* Ds = smem + S::offDelta;
-  uint8_t* Dts = smem + S::offDeltaT;
 
   const long long bh = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -81,15 +96,16 @@ __global__ void __launch_bounds__(192, 1)
       tc::mbar_init(&bars[SB_FULL + s], 1);
       tc::mbar_init(&bars[SB_EMPTY + s], 1);
     }
-    tc::mbar_init(&bars[SB_S0], 128);
-    tc::mbar_init(&bars[SB_X], 1);
-    tc::mbar_init(&bars[SB_DELTA], 128);
-    tc::mbar_init(&bars[SB_Y], 1);
+    tc::mbar_init(&bars[SB_S0], 256);
+    tc::mbar_init(&bars[SB_Z], 1);
+    tc::mbar_init(&bars[SB_DELTA], 256);
+    tc::mbar_init(&bars[SB_OFREE], 256);
+    tc::mbar_init(&bars[SB_OFREE + 1], 256);
     tc::mbar_init(&bars[SB_SDONE], 1);
     tc::mbar_init(&bars[SB_DONE], 1);
     tc::fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tc::tmem_alloc(tmem_slot, 512);
     tc::tmem_relinquish();
   }
@@ -97,9 +113,8 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tX = tmem, tY = tmem + 128, tS = tmem + 256;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tc::prefetch_tensormap(&tm_w);
@@ -112,66 +127,61 @@ __global__ void __launch_bounds__(192, 1)
       for (int c = 0; c < N; ++c) {
         const int s = c & 1;
         if (!(ok = tc::mbar_wait(&bars[SB_EMPTY + s], ((c >> 1) & 1) ^ 1, err))) break;
-        uint8_t* st = smem + S::offStage + s * S::kStage;
-        uint8_t* WQ = st;
+        uint8_t* WQ = smem + S::offStage + s * S::kStage;
         uint8_t* Kb = WQ + S::kWQ;
         uint8_t* Ub = Kb + S::kK;
         uint8_t* Pb = Ub + S::kU;
-        const int yc = (int)((bh * N + c) * 64);   // row of this chunk in W / U / P
-        const int yt = (int)(bh * L + 64LL * c);   // row of this chunk in Q / K
-        tc::mbar_arrive_expect_tx(&bars[SB_FULL + s], 4 * 64 * D * 2 + 64 * 64 * 2);
+        const int yc = (int)((bh * N + c) * 64);   // row of this chunk in W / P / Q~ / K / ...
+        const int yt = (int)(bh * L + 64LL * c);   // row of this chunk in Q~ / K
+        const int yu = (int)((bh * N + c) * D);    // first line of this chunk in U^T
+        tc::mbar_arrive_expect_tx(&bars[SB_FULL + s], S::kStage);
         for (int h = 0; h < D / 64; ++h) {
           tc::tma_load_2d(WQ + h * 16384, &tm_w, 64 * h, yc, &bars[SB_FULL + s]);
           tc::tma_load_2d(WQ + h * 16384 + 8192, &tm_q, 64 * h, yt, &bars[SB_FULL + s]);
           tc::tma_load_2d(Kb + h * 8192, &tm_k, 64 * h, yt, &bars[SB_FULL + s]);
-          tc::tma_load_2d(Ub + h * 8192, &tm_u, 64 * h, yc, &bars[SB_FULL + s]);
+          tc::tma_load_2d(Ub + h * 8192, &tm_u, 0, yu + 64 * h, &bars[SB_FULL + s]);
         }
-        tc::tma_load_2d(Pb + 8192, &tm_p, 0, yc, &bars[SB_FULL + s]);
+        tc::tma_load_2d(Pb, &tm_p, 0, yc, &bars[SB_FULL + s]);
         issued[s]++;
       }
-      if (ok) {
-        for (int s = 0; s < 2; ++s)
-          if (issued[s] > 0) tc::mbar_wait(&bars[SB_EMPTY + s], (issued[s] - 1) & 1, err);
-      } else {
-        for (int s = 0; s < 2; ++s)
-          if (issued[s] > 0) tc::mbar_wait(&bars[SB_FULL + s], (issued[s] - 1) & 1, nullptr);
+      for (int s = 0; s < 2; ++s) {
+        if (issued[s] == 0) continue;
+        tc::mbar_wait(&bars[SB_FULL + s], (issued[s] - 1) & 1, nullptr);
+        if (ok) tc::mbar_wait(&bars[SB_EMPTY + s], (issued[s] - 1) & 1, err);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t id1 = tc::idesc_bf16_f32(128, D, false, false);
-      constexpr uint32_t id2 = tc::idesc_bf16_f32(128, D, false, true);
-      constexpr uint32_t id3 = tc::idesc_bf16_f32(128, D, true, true);
-      const uint32_t s0 = tc::smem_u32(S0s), dsa = tc::smem_u32(Ds), dta = tc::smem_u32(Dts);
+      constexpr uint32_t id1 = tc::idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t id2 = tc::idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t id3 = tc::idesc_bf16_f32(128, D, false, true);
       bool ok = true;
       for (int c = 0; c < N && ok; ++c) {
         const int s = c & 1;
-        const uint32_t st = tc::smem_u32(smem + S::offStage + s * S::kStage);
-        const uint32_t wq = st, kb = st + S::kWQ, pb = st + S::kWQ + S::kK + S::kU;
+        const uint32_t wq = tc::smem_u32(smem + S::offStage + s * S::kStage);
+        const uint32_t kb = wq + S::kWQ, pb = wq + S::kWQ + S::kK + S::kU;
+        const uint32_t tZ = tmem + kColZ + (c & 1) * 128;
         if (!(ok = tc::mbar_wait(&bars[SB_FULL + s], (c >> 1) & 1, err))) break;
         if (!(ok = tc::mbar_wait(&bars[SB_S0], c & 1, err))) break;
+        if (c >= 2 && !(ok = tc::mbar_wait(&bars[SB_OFREE + (c & 1)], ((c - 2) >> 1) & 1, err))) break;
         tc::fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint32_t offb = (kk >> 2) * (D * 128) + (kk & 3) * 32;
-          tc::mma_bf16(tX, tc::smem_desc_sw128(wq + off, 16, 1024), tc::smem_desc_sw128(s0 + offb, 16, 1024), id1,
-                       kk > 0);
+          const uint32_t offb = (kk >> 2) * 16384 + (kk & 3) * 32;  // [W; Q~]: 128 lines per 64-col half
+          tc::mma_bf16_ts(tZ, tmem + kColS0 + kk * 8, tc::smem_desc_sw128(wq + offb, 16, 1024), id1, kk > 0);
         }
-        tc::mma_commit(&bars[SB_X]);
+        tc::mma_commit(&bars[SB_Z]);
         if (!(ok = tc::mbar_wait(&bars[SB_DELTA], c & 1, err))) break;
         tc::fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc::mma_bf16(tY, tc::smem_desc_sw128(pb + kk * 32, 16, 1024),
-                       tc::smem_desc_sw128(dsa + kk * 2048, 8192, 1024), id2, kk > 0);
-        tc::mma_commit(&bars[SB_Y]);
+          tc::mma_bf16_ts(tZ + 64, tmem + kColDT + kk * 8, tc::smem_desc_sw128(pb + kk * 32, 16, 1024), id2, 1);
         if (sel[bh * N + c] != 0) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc::mma_bf16(tS, tc::smem_desc_sw128(dta + kk * 2048, 8192, 1024),
-                         tc::smem_desc_sw128(kb + kk * 2048, 8192, 1024), id3, 1);
+            tc::mma_bf16_ts(tmem + kColS, tmem + kColDT + kk * 8, tc::smem_desc_sw128(kb + kk * 2048, 8192, 1024),
+                            id3, 1);
         }
         tc::mma_commit(&bars[SB_SDONE]);
         tc::mma_commit(&bars[SB_EMPTY + s]);
@@ -180,150 +190,127 @@ __global__ void __launch_bounds__(192, 1)
       tc::mbar_wait(&bars[SB_DONE], 0, err);
     }
   } else {
-    // ------------------------------------------------- elementwise (warps 0-3)
-    const int r = threadIdx.x;  // TMEM lane
-    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-    // S = 0 in TMEM and in the bf16 copy
+    // ------------------------------------------------- elementwise (warps 0-7)
+    const int q4 = warp & 3;        // TMEM lane quarter
+    const int r = 32 * q4 + lane;   // TMEM lane = state row (dv)
+    const int hf = warp >> 2;       // column half
+    const bool has_row = r < D;     // warp-uniform (lanes come in 32s, D is 64 or 128)
+    const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+    constexpr int SC = D / 2;       // state columns per thread
+    // S = 0 in TMEM, fp32 and bf16
     {
       float z[32];
+      uint32_t zu[16];
 #pragma unroll
       for (int i = 0; i < 32; ++i) z[i] = 0.f;
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) tc::tmem_st32(tS + lane_off + ch * 32, z);
+      for (int i = 0; i < 16; ++i) zu[i] = 0u;
+#pragma unroll
+      for (int ch = 0; ch < SC / 32; ++ch) tc::tmem_st32(tmem + kColS + lane_off + hf * SC + ch * 32, z);
+#pragma unroll
+      for (int ch = 0; ch < SC / 32; ++ch) tc::tmem_st16u(tmem + kColS0 + lane_off + hf * (SC / 2) + ch * 16, zu);
       tc::tmem_st_wait();
-      for (int e = r; e < D * D / 8; e += 128) ((uint4*)S0s)[e] = make_uint4(0, 0, 0, 0);
-      tc::fence_proxy_async_smem();
       tc::fence_before();
       tc::mbar_arrive(&bars[SB_S0]);
     }
     bool ok = true;
     for (int c = 0; c < N; ++c) {
-      const int s = c & 1;
-      const uint8_t* Ub = smem + S::offStage + s * S::kStage + S::kWQ + S::kK;
+      // per-chunk constants, loaded ahead of the waits
       const bool lin = sel[bh * N + c] != 0;
-      const float* Gc = G + bh * (long long)L + 64LL * c;
-      const float GC = Gc[63];
-      if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_X], c & 1, err)))) break;
-      tc::fence_after();
-      if (r < 64) {
-        // Delta[t] = U[t] - (W S0^T)[t];  Delta~[t] = Delta[t] * e^{G_C - G_t}
-        const int t = r;
-        const float dec = __expf(GC - Gc[t]);
-#pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-          float x[32];
-          tc::tmem_ld32(tX + lane_off + ch * 32, x);
-          tc::tmem_ld_wait();
+      const bool lin_next = (c + 1 < N) && (sel[bh * N + c + 1] != 0);
+      const float gnext = lin_next ? __expf(G[bh * (long long)L + 64LL * c + 64 + 63]) : 1.f;
+      const uint32_t tZ = tmem + kColZ + (c & 1) * 128 + lane_off;
+      // ---- Delta^T (columns t = 32 hf .. 32 hf + 31 of this row)
+      {
+        const uint8_t* Ub = smem + S::offStage + (c & 1) * S::kStage + S::kWQ + S::kK;
+        float x[32];
+        if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_Z], c & 1, err)))) break;
+        tc::fence_after();
+        tc::tmem_ld32(tZ + 32 * hf, x);
+        uint32_t pd[16];
+        uint4 uv[4];
+        if (has_row) {
+#pragma unroll
+          for (int g8 = 0; g8 < 4; ++g8)
+            uv[g8] = *(const uint4*)(Ub + sw_off(r & 63, 32 * hf + 8 * g8, 0) + (r >> 6) * 8192);
+        }
+        tc::tmem_ld_wait();
+        if (has_row) {
 #pragma unroll
           for (int g8 = 0; g8 < 4; ++g8) {
-            const int col = ch * 32 + g8 * 8;
-            const uint32_t off = sw_off(t, col, 8192);
-            const uint4 uv = *(const uint4*)(Ub + off);
-            const __nv_bfloat162* u2 = (const __nv_bfloat162*)&uv;
-            float d[8];
+            const __nv_bfloat162* u2 = (const __nv_bfloat162*)&uv[g8];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const float2 uf = __bfloat1622float2(u2[i]);
-              d[2 * i] = uf.x - x[g8 * 8 + 2 * i];
-              d[2 * i + 1] = uf.y - x[g8 * 8 + 2 * i + 1];
+              pd[4 * g8 + i] = pack_rne(uf.x - x[8 * g8 + 2 * i], uf.y - x[8 * g8 + 2 * i + 1]);
             }
-            uint4 pk, pt;
-            pk.x = tc::pack_bf16x2(d[0], d[1]);
-            pk.y = tc::pack_bf16x2(d[2], d[3]);
-            pk.z = tc::pack_bf16x2(d[4], d[5]);
-            pk.w = tc::pack_bf16x2(d[6], d[7]);
-            pt.x = tc::pack_bf16x2(d[0] * dec, d[1] * dec);
-            pt.y = tc::pack_bf16x2(d[2] * dec, d[3] * dec);
-            pt.z = tc::pack_bf16x2(d[4] * dec, d[5] * dec);
-            pt.w = tc::pack_bf16x2(d[6] * dec, d[7] * dec);
-            *(uint4*)(Ds + off) = pk;
-            *(uint4*)(Dts + off) = pt;
           }
-        }
-      }
-      if (lin) {
-        // S *= gamma_C before the rank-64 update is accumulated onto it
-        const float gC = __expf(GC);
-#pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-          float v[32];
-          tc::tmem_ld32(tS + lane_off + ch * 32, v);
-          tc::tmem_ld_wait();
+        } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= gC;
-          tc::tmem_st32(tS + lane_off + ch * 32, v);
+          for (int i = 0; i < 16; ++i) pd[i] = 0u;
+        }
+        tc::tmem_st16u(tmem + kColDT + lane_off + 16 * hf, pd);
+        tc::tmem_st_wait();
+        tc::fence_before();
+        tc::mbar_arrive(&bars[SB_DELTA]);
+      }
+      // ---- state: bf16 copy after this chunk's update, and the decay of the
+      // next linear chunk applied ahead of its MMA3
+      if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_SDONE], c & 1, err)))) break;
+      tc::fence_after();
+      if ((lin || lin_next) && has_row) {
+#pragma unroll
+        for (int ch = 0; ch < SC / 32; ++ch) {
+          const int col0 = hf * SC + ch * 32;
+          float v[32];
+          tc::tmem_ld32(tmem + kColS + lane_off + col0, v);
+          tc::tmem_ld_wait();
+          if (lin) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pack_rne(v[2 * i], v[2 * i + 1]);
+            tc::tmem_st16u(tmem + kColS0 + lane_off + col0 / 2, pk);
+          }
+          if (lin_next) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= gnext;
+            tc::tmem_st32(tmem + kColS + lane_off + col0, v);
+          }
         }
         tc::tmem_st_wait();
       }
-      tc::fence_proxy_async_smem();
-      tc::fence_before();
-      tc::mbar_arrive(&bars[SB_DELTA]);
-      if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_Y], c & 1, err)))) break;
-      tc::fence_after();
-      if (r >= 64) {
-        // O[t] = e^{G_t} scale (Q S0^T)[t] + (P Delta)[t]
-        const int t = r - 64;
-        const float gq = __expf(Gc[t]) * scale;
-        float* dst = o_l + (bh * (long long)L + 64LL * c + t) * D;
-#pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-          float x[32], y[32];
-          tc::tmem_ld32(tX + lane_off + ch * 32, x);
-          tc::tmem_ld32(tY + lane_off + ch * 32, y);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            ((float4*)(dst + ch * 32))[i] = make_float4(fmaf(gq, x[4 * i], y[4 * i]), fmaf(gq, x[4 * i + 1], y[4 * i + 1]),
-                                                        fmaf(gq, x[4 * i + 2], y[4 * i + 2]),
-                                                        fmaf(gq, x[4 * i + 3], y[4 * i + 3]));
-        }
-      }
-      if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_SDONE], c & 1, err)))) break;
-      tc::fence_after();
-      if (lin && r < D) {
-        // bf16 copy of the new state for the next chunk's MMA1 (lines dv, cols dk)
-#pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-          float v[32];
-          tc::tmem_ld32(tS + lane_off + ch * 32, v);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int g8 = 0; g8 < 4; ++g8) {
-            uint4 pk;
-            pk.x = tc::pack_bf16x2(v[g8 * 8 + 0], v[g8 * 8 + 1]);
-            pk.y = tc::pack_bf16x2(v[g8 * 8 + 2], v[g8 * 8 + 3]);
-            pk.z = tc::pack_bf16x2(v[g8 * 8 + 4], v[g8 * 8 + 5]);
-            pk.w = tc::pack_bf16x2(v[g8 * 8 + 6], v[g8 * 8 + 7]);
-            *(uint4*)(S0s + sw_off(r, ch * 32 + g8 * 8, D * 128)) = pk;
-          }
-        }
-      } else if (lin) {
-        float v[32];  // lanes >= D hold no state, but the load is warp-collective
-        tc::tmem_ld32(tS + lane_off, v);
-        tc::tmem_ld_wait();
-      }
-      tc::fence_proxy_async_smem();
       tc::fence_before();
       tc::mbar_arrive(&bars[SB_S0]);
+      // ---- O^T -> o_l[t][dv]: 32 lanes of a warp write 128 contiguous bytes per t
+      {
+        float o[32];  // warp-collective load (lanes >= D hold no state row)
+        tc::tmem_ld32(tZ + 64 + 32 * hf, o);
+        tc::tmem_ld_wait();
+        if (has_row) {
+          float* dst = o_l + (bh * (long long)L + 64LL * c + 32 * hf) * D + r;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) dst[(size_t)i * D] = o[i];
+        }
+      }
+      tc::fence_before();
+      tc::mbar_arrive(&bars[SB_OFREE + (c & 1)]);
     }
-    if (ok && state_out) {
+    if (ok && state_out && has_row) {
       tc::fence_after();
 #pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
+      for (int ch = 0; ch < SC / 32; ++ch) {
         float v[32];
-        tc::tmem_ld32(tS + lane_off + ch * 32, v);
+        tc::tmem_ld32(tmem + kColS + lane_off + hf * SC + ch * 32, v);
         tc::tmem_ld_wait();
-        if (r < D) {
-          float* dst = state_out + (bh * D + r) * (long long)D + ch * 32;
+        float* dst = state_out + (bh * D + r) * (long long)D + hf * SC + ch * 32;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) ((float4*)dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-        }
+        for (int i = 0; i < 8; ++i) ((float4*)dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
       }
     }
   }
   tc::fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc::fence_after();
     tc::tmem_dealloc(tmem, 512);
   }
@@ -332,28 +319,28 @@ __global__ void __launch_bounds__(192, 1)
 }  // namespace
 
 template <int D>
-static cudaError_t launch_scan_tc_t(const Problem& p, const void* q, const void* k, const uint8_t* sel,
-                                    const float* G, const void* W16, const void* U16, const void* P16,
+static cudaError_t launch_scan_tc_t(const Problem& p, const void* Kt16, const uint8_t* sel, const float* G,
+                                    const void* W16, const void* UT16, const void* P16, const void* Qt16,
                                     float* o_l, float* state_out, int* err, cudaStream_t st) {
   CUtensorMap mw, mq, mk, mu, mp;
   const long long rows = p.BH * p.L;  // = BH * N * 64
-  if (!make_tile_map(&mw, W16, rows, D) || !make_tile_map(&mq, q, rows, D) || !make_tile_map(&mk, k, rows, D) ||
-      !make_tile_map(&mu, U16, rows, D) || !make_tile_map(&mp, P16, rows, 64))
+  if (!make_tile_map(&mw, W16, rows, D) || !make_tile_map(&mq, Qt16, rows, D) || !make_tile_map(&mk, Kt16, rows, D) ||
+      !make_tile_map(&mu, UT16, p.BH * (long long)p.N * D, 64) || !make_tile_map(&mp, P16, rows, 64))
     return cudaErrorInvalidValue;
   auto kern = gdn_scan_tc_kernel<D>;
   const int smem = ScanSmem<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)p.BH, 192, smem, st>>>(mw, mq, mk, mu, mp, sel, G, p.L, p.N, p.scale, o_l, state_out, err);
+  kern<<<(unsigned)p.BH, 320, smem, st>>>(mw, mq, mk, mu, mp, sel, G, p.L, p.N, o_l, state_out, err);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gdn_scan_tc(const Problem& p, const void* q, const void* k, const uint8_t* sel, const float* G,
-                               const void* W16, const void* U16, const void* P16, float* o_l, float* state_out,
-                               int* err, cudaStream_t st) {
+cudaError_t launch_gdn_scan_tc(const Problem& p, const void* Kt16, const uint8_t* sel, const float* G,
+                               const void* W16, const void* UT16, const void* P16, const void* Qt16, float* o_l,
+                               float* state_out, int* err, cudaStream_t st) {
   if (p.BH == 0 || p.N == 0) return cudaSuccess;
-  return p.d == 64 ? launch_scan_tc_t<64>(p, q, k, sel, G, W16, U16, P16, o_l, state_out, err, st)
-                   : launch_scan_tc_t<128>(p, q, k, sel, G, W16, U16, P16, o_l, state_out, err, st);
+  return p.d == 64 ? launch_scan_tc_t<64>(p, Kt16, sel, G, W16, UT16, P16, Qt16, o_l, state_out, err, st)
+                   : launch_scan_tc_t<128>(p, Kt16, sel, G, W16, UT16, P16, Qt16, o_l, state_out, err, st);
 }
 
 }  // namespace nats

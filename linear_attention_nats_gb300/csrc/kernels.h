@@ -30,11 +30,12 @@ cudaError_t launch_gdn_scan_simt(const Problem& p, int dtype, const void* q, con
                                  float* state_out, cudaStream_t st);
 
 cudaError_t launch_gdn_prep_mma(const Problem& p, const void* q, const void* k, const void* v, const float* g,
-                                const float* beta, float* G, void* W16, void* U16, void* P16, cudaStream_t st);
+                                const float* beta, float* G, void* W16, void* U16, void* P16, void* Qt16,
+                                void* Kt16, cudaStream_t st);
 
-cudaError_t launch_gdn_scan_tc(const Problem& p, const void* q, const void* k, const uint8_t* sel, const float* G,
-                               const void* W16, const void* U16, const void* P16, float* o_l, float* state_out,
-                               int* err, cudaStream_t st);
+cudaError_t launch_gdn_scan_tc(const Problem& p, const void* Kt16, const uint8_t* sel, const float* G,
+                               const void* W16, const void* UT16, const void* P16, const void* Qt16, float* o_l,
+                               float* state_out, int* err, cudaStream_t st);
 
 cudaError_t launch_norm_merge(const Problem& p, int dtype, const float* o_s, const float* o_l,
                               const void* q, const float* w_g, const float* b_g, const float* nw_s,
