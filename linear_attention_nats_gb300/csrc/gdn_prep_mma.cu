@@ -63,14 +63,15 @@ struct PrepSmem {
   static constexpr int offK = 0;
   static constexpr int offQ = offK + C * RS * 2;
   static constexpr int offV = offQ + C * RS * 2;
-  static constexpr int offA = offV + C * RS * 2;     // fp32 [C][C+1]
-  static constexpr int offT = offA + C * (C + 1) * 4;  // fp32 [C][C+1]
-  static constexpr int offTb = offT + C * (C + 1) * 4; // bf16 [C][TS]
+  static constexpr int FS = C + 4;  // fp32 row stride (16-byte aligned rows)
+  static constexpr int offA = offV + C * RS * 2;     // fp32 [C][FS]
+  static constexpr int offT = offA + C * FS * 4;     // fp32 [C][FS]
+  static constexpr int offTb = offT + C * FS * 4;    // bf16 [C][TS]
   static constexpr int offG = offTb + C * TS * 2;    // fp32 [C]
   static constexpr int offB = offG + C * 4;          // fp32 [C] beta
   static constexpr int offBg = offB + C * 4;         // fp32 [C] beta e^G
-  static constexpr int offX = offBg + C * 4;         // fp32 [C][C+1] scratch of the blocked inverse
-  static constexpr int kBytes = offX + C * (C + 1) * 4;
+  static constexpr int offX = offBg + C * 4;         // fp32 [C][FS] scratch of the blocked inverse
+  static constexpr int kBytes = offX + C * FS * 4;
 };
 
 // One CTA (4 warps) per (b, h, chunk).  Warp w owns rows 16w .. 16w+15 of
@@ -83,7 +84,7 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
     __nv_bfloat16* __restrict__ Uout, __nv_bfloat16* __restrict__ Pout, __nv_bfloat16* __restrict__ Qtout,
     __nv_bfloat16* __restrict__ Ktout) {
   using S = PrepSmem<D>;
-  constexpr int RS = S::RS, TS = S::TS;
+  constexpr int RS = S::RS, TS = S::TS, FS = S::FS;
   extern __shared__ __align__(16) uint8_t smem[];
   __nv_bfloat16* Ks = (__nv_bfloat16*)(smem + S::offK);
   __nv_bfloat16* Qs = (__nv_bfloat16*)(smem + S::offQ);
@@ -96,7 +97,7 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
   float* Bg = (float*)(smem + S::offBg);
   constexpr int UTS = C + 8;  // bf16 line stride of the staged U^T
   __nv_bfloat16* UTs = (__nv_bfloat16*)(smem + S::offA);  // reuses A and T once T is in Tb
-  static_assert(D * UTS * 2 <= 2 * C * (C + 1) * 4, "U^T staging must fit the A / T scratch");
+  static_assert(D * UTS * 2 <= 2 * C * S::FS * 4, "U^T staging must fit the A / T scratch");
 
   const long long blk = blockIdx.x;
   const int c = (int)(blk % N);
@@ -176,8 +177,8 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
           av[u] = (i < t) ? Bs[t] * dec * kk[j][2 * hh + u] : 0.f;
           pv[u] = (i <= t) ? scale * dec * qk[j][2 * hh + u] : 0.f;
         }
-        As[t * (C + 1) + i0] = av[0];
-        As[t * (C + 1) + i0 + 1] = av[1];
+        As[t * FS + i0] = av[0];
+        As[t * FS + i0 + 1] = av[1];
         *(uint32_t*)(P + t * C + i0) = pack2(pv[0], pv[1]);
       }
     }
@@ -226,47 +227,90 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
       float acc = (tt == jj) ? 1.f : 0.f;
 #pragma unroll
       for (int ii = 0; ii < tt; ++ii)
-        if (ii >= jj) acc = fmaf(-As[t * (C + 1) + 16 * b + ii], x[ii], acc);
+        if (ii >= jj) acc = fmaf(-As[t * FS + 16 * b + ii], x[ii], acc);
       x[tt] = (tt >= jj) ? acc : 0.f;
     }
 #pragma unroll
-    for (int tt = 0; tt < 16; ++tt) Ts[(16 * b + tt) * (C + 1) + j] = x[tt];
+    for (int tt = 0; tt < 16; ++tt) Ts[(16 * b + tt) * FS + j] = x[tt];
   } else {
     const int u = tid - C;
     Bg[u] = Bs[u] * __expf(Gs[u]);
   }
   __syncthreads();
+  // off-diagonal tiles by distance: a thread owns one row and 8 columns of a tile
   for (int lv = 1; lv < 4; ++lv) {
     const int nblk = 4 - lv;
-    // X_ij = sum_{j <= k < i} A_ik T_kj for the tiles (i, j) = (b + lv, b)
-    for (int e = tid; e < nblk * 256; e += 128) {
-      const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-      const int i = b + lv, j = b;
-      const int row = 16 * i + r, col = 16 * j + cc;
-      float acc = 0.f;
-      for (int kk = 16 * j; kk < 16 * i; ++kk) acc = fmaf(As[row * (C + 1) + kk], Ts[kk * (C + 1) + col], acc);
-      Xs[row * (C + 1) + col] = acc;
+    const bool active = tid < nblk * 32;
+    const int b = tid >> 5, r = (tid >> 1) & 15, c8 = (tid & 1) * 8;
+    const int i = b + lv, j = b;
+    const int row = 16 * i + r, col = 16 * j + c8;
+    if (active) {
+      // X_ij = sum_{j <= k < i} A_ik T_kj
+      float acc[8];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) acc[x] = 0.f;
+      for (int kk = 16 * j; kk < 16 * i; ++kk) {
+        const float a = As[row * FS + kk];
+        const float4 t0 = *(const float4*)(Ts + kk * FS + col);
+        const float4 t1 = *(const float4*)(Ts + kk * FS + col + 4);
+        acc[0] = fmaf(a, t0.x, acc[0]); acc[1] = fmaf(a, t0.y, acc[1]);
+        acc[2] = fmaf(a, t0.z, acc[2]); acc[3] = fmaf(a, t0.w, acc[3]);
+        acc[4] = fmaf(a, t1.x, acc[4]); acc[5] = fmaf(a, t1.y, acc[5]);
+        acc[6] = fmaf(a, t1.z, acc[6]); acc[7] = fmaf(a, t1.w, acc[7]);
+      }
+      *(float4*)(Xs + row * FS + col) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      *(float4*)(Xs + row * FS + col + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
     __syncthreads();
-    // T_ij = -T_ii X_ij
-    for (int e = tid; e < nblk * 256; e += 128) {
-      const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-      const int i = b + lv, j = b;
-      const int row = 16 * i + r, col = 16 * j + cc;
-      float acc = 0.f;
-      for (int kk = 16 * i; kk <= row; ++kk) acc = fmaf(Ts[row * (C + 1) + kk], Xs[kk * (C + 1) + col], acc);
-      Ts[row * (C + 1) + col] = -acc;
+    if (active) {
+      // T_ij = -T_ii X_ij
+      float acc[8];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) acc[x] = 0.f;
+      for (int kk = 16 * i; kk <= row; ++kk) {
+        const float a = Ts[row * FS + kk];
+        const float4 t0 = *(const float4*)(Xs + kk * FS + col);
+        const float4 t1 = *(const float4*)(Xs + kk * FS + col + 4);
+        acc[0] = fmaf(a, t0.x, acc[0]); acc[1] = fmaf(a, t0.y, acc[1]);
+        acc[2] = fmaf(a, t0.z, acc[2]); acc[3] = fmaf(a, t0.w, acc[3]);
+        acc[4] = fmaf(a, t1.x, acc[4]); acc[5] = fmaf(a, t1.y, acc[5]);
+        acc[6] = fmaf(a, t1.z, acc[6]); acc[7] = fmaf(a, t1.w, acc[7]);
+      }
+      *(float4*)(Ts + row * FS + col) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+      *(float4*)(Ts + row * FS + col + 4) = make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
     }
     __syncthreads();
   }
-  for (int e = tid; e < C * C; e += 128) {
-    const int t = e >> 6, j = e & 63;
-    Tb[t * TS + j] = __float2bfloat16_rn(j <= t ? Ts[t * (C + 1) + j] : 0.f);
+  // T -> bf16 (zero above the diagonal), 8 columns per step
+  for (int e = tid; e < C * C / 8; e += 128) {
+    const int t = e >> 3, j0 = (e & 7) * 8;
+    const float4 a0 = *(const float4*)(Ts + t * FS + j0);
+    const float4 a1 = *(const float4*)(Ts + t * FS + j0 + 4);
+    const float v8[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    uint4 o;
+    uint32_t* o32 = (uint32_t*)&o;
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+      o32[x] = pack2(j0 + 2 * x <= t ? v8[2 * x] : 0.f, j0 + 2 * x + 1 <= t ? v8[2 * x + 1] : 0.f);
+    *(uint4*)(Tb + t * TS + j0) = o;
   }
-  for (int e = tid; e < C * D; e += 128) {
-    const int t = e / D, f = e % D;
-    Vs[t * RS + f] = __float2bfloat16_rn(Bs[t] * __bfloat162float(Vs[t * RS + f]));
-    Ks[t * RS + f] = __float2bfloat16_rn(Bg[t] * __bfloat162float(Ks[t * RS + f]));
+  // V rows *= beta, K rows *= beta e^G (in place, 8 columns per step)
+  for (int e = tid; e < C * VPR; e += 128) {
+    const int t = e / VPR, x8 = (e % VPR) * 8;
+    const float fb = Bs[t], fg = Bg[t];
+    uint4 vv = *(uint4*)(Vs + t * RS + x8);
+    uint4 kv = *(uint4*)(Ks + t * RS + x8);
+    __nv_bfloat162* v2 = (__nv_bfloat162*)&vv;
+    __nv_bfloat162* k2 = (__nv_bfloat162*)&kv;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const float2 a = __bfloat1622float2(v2[x]);
+      const float2 c2 = __bfloat1622float2(k2[x]);
+      v2[x] = __floats2bfloat162_rn(a.x * fb, a.y * fb);
+      k2[x] = __floats2bfloat162_rn(c2.x * fg, c2.y * fg);
+    }
+    *(uint4*)(Vs + t * RS + x8) = vv;
+    *(uint4*)(Ks + t * RS + x8) = kv;
   }
   __syncthreads();
   // ---- U = T (beta V), W = T (beta e^G K): rows 16w.., k-steps up to the diagonal
@@ -275,11 +319,9 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
     const int acol = 8 * (lane >> 4);
     const int trow = (lane & 7) + 8 * ((lane >> 3) & 1);  // k row within the 16-row step
     const int tcol = 8 * (lane >> 4);                     // n column offset
-    __nv_bfloat16* Wg = Wout + (size_t)blk * C * D;
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
       const __nv_bfloat16* Bsrc = which == 0 ? Vs : Ks;
-      __nv_bfloat16* dst = Wg;
       float acc[D / 8][4];
 #pragma unroll
       for (int n = 0; n < D / 8; ++n)
@@ -307,13 +349,15 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
           UTs[(e + 1) * UTS + m0 + gq + 8] = __float2bfloat16_rn(acc[n][3]);
         }
       } else {
+        // W staged in the V tile (dead once every warp finished U)
 #pragma unroll
         for (int n = 0; n < D / 8; ++n) {
           const int col = 8 * n + 2 * cq;
-          *(uint32_t*)(dst + (m0 + gq) * D + col) = pack2(acc[n][0], acc[n][1]);
-          *(uint32_t*)(dst + (m0 + gq + 8) * D + col) = pack2(acc[n][2], acc[n][3]);
+          *(uint32_t*)(Vs + (m0 + gq) * RS + col) = pack2(acc[n][0], acc[n][1]);
+          *(uint32_t*)(Vs + (m0 + gq + 8) * RS + col) = pack2(acc[n][2], acc[n][3]);
         }
       }
+      if (which == 0) __syncthreads();  // every warp is done reading V
     }
   }
   __syncthreads();
@@ -322,6 +366,11 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
     for (int e8 = tid; e8 < D * 8; e8 += 128) {
       const int e = e8 >> 3, x = e8 & 7;
       *(uint4*)(Ug + e * C + x * 8) = *(const uint4*)(UTs + e * UTS + x * 8);
+    }
+    __nv_bfloat16* Wg = Wout + (size_t)blk * C * D;  // [64][D]
+    for (int e = tid; e < C * VPR; e += 128) {
+      const int t = e / VPR, x = e % VPR;
+      *(uint4*)(Wg + t * D + x * 8) = *(const uint4*)(Vs + t * RS + x * 8);
     }
   }
 }

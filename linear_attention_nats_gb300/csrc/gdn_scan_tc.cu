@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 9) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t id1 = tc::idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t id1 = tc::idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t id2 = tc::idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t id3 = tc::idesc_bf16_f32(128, D, false, true);
       bool ok = true;
@@ -166,12 +166,18 @@ __global__ void __launch_bounds__(320, 1)
         if (!(ok = tc::mbar_wait(&bars[SB_S0], c & 1, err))) break;
         if (c >= 2 && !(ok = tc::mbar_wait(&bars[SB_OFREE + (c & 1)], ((c - 2) >> 1) & 1, err))) break;
         tc::fence_after();
+        // S0 W^T first (Delta waits on it), then S0 Q~^T (O only)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t offb = (kk >> 2) * 16384 + (kk & 3) * 32;  // [W; Q~]: 128 lines per 64-col half
           tc::mma_bf16_ts(tZ, tmem + kColS0 + kk * 8, tc::smem_desc_sw128(wq + offb, 16, 1024), id1, kk > 0);
         }
         tc::mma_commit(&bars[SB_Z]);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t offb = (kk >> 2) * 16384 + (kk & 3) * 32 + 8192;
+          tc::mma_bf16_ts(tZ + 64, tmem + kColS0 + kk * 8, tc::smem_desc_sw128(wq + offb, 16, 1024), id1, kk > 0);
+        }
         if (!(ok = tc::mbar_wait(&bars[SB_DELTA], c & 1, err))) break;
         tc::fence_after();
 #pragma unroll
@@ -224,16 +230,18 @@ __global__ void __launch_bounds__(320, 1)
       {
         const uint8_t* Ub = smem + S::offStage + (c & 1) * S::kStage + S::kWQ + S::kK;
         float x[32];
-        if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_Z], c & 1, err)))) break;
-        tc::fence_after();
-        tc::tmem_ld32(tZ + 32 * hf, x);
         uint32_t pd[16];
         uint4 uv[4];
+        // U^T of this chunk is in shared memory once its stage is full
+        if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_FULL + (c & 1)], (c >> 1) & 1, err)))) break;
         if (has_row) {
 #pragma unroll
           for (int g8 = 0; g8 < 4; ++g8)
             uv[g8] = *(const uint4*)(Ub + sw_off(r & 63, 32 * hf + 8 * g8, 0) + (r >> 6) * 8192);
         }
+        if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_Z], c & 1, err)))) break;
+        tc::fence_after();
+        tc::tmem_ld32(tZ + 32 * hf, x);
         tc::tmem_ld_wait();
         if (has_row) {
 #pragma unroll
@@ -258,29 +266,33 @@ __global__ void __launch_bounds__(320, 1)
       // next linear chunk applied ahead of its MMA3
       if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_SDONE], c & 1, err)))) break;
       tc::fence_after();
+      float v[SC];
       if ((lin || lin_next) && has_row) {
+        tc::tmem_ld32_at<0>(tmem + kColS + lane_off + hf * SC, v);
+        if (SC > 32) tc::tmem_ld32_at<(SC > 32 ? 32 : 0)>(tmem + kColS + lane_off + hf * SC + 32, v);
+        tc::tmem_ld_wait();
+      }
+      if (lin && has_row) {
 #pragma unroll
         for (int ch = 0; ch < SC / 32; ++ch) {
-          const int col0 = hf * SC + ch * 32;
-          float v[32];
-          tc::tmem_ld32(tmem + kColS + lane_off + col0, v);
-          tc::tmem_ld_wait();
-          if (lin) {
-            uint32_t pk[16];
+          uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = pack_rne(v[2 * i], v[2 * i + 1]);
-            tc::tmem_st16u(tmem + kColS0 + lane_off + col0 / 2, pk);
-          }
-          if (lin_next) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= gnext;
-            tc::tmem_st32(tmem + kColS + lane_off + col0, v);
-          }
+          for (int i = 0; i < 16; ++i) pk[i] = pack_rne(v[ch * 32 + 2 * i], v[ch * 32 + 2 * i + 1]);
+          tc::tmem_st16u(tmem + kColS0 + lane_off + (hf * SC + ch * 32) / 2, pk);
         }
         tc::tmem_st_wait();
       }
       tc::fence_before();
       tc::mbar_arrive(&bars[SB_S0]);
+      // the next chunk's MMA3 accumulates onto gamma_C S: scale now, off the
+      // critical path (that MMA3 also waits for this thread's next Delta)
+      if (lin_next && has_row) {
+#pragma unroll
+        for (int i = 0; i < SC; ++i) v[i] *= gnext;
+        tc::tmem_st32(tmem + kColS + lane_off + hf * SC, *reinterpret_cast<float(*)[32]>(&v[0]));
+        if (SC > 32) tc::tmem_st32(tmem + kColS + lane_off + hf * SC + 32, *reinterpret_cast<float(*)[32]>(&v[SC > 32 ? 32 : 0]));
+        tc::tmem_st_wait();
+      }
       // ---- O^T -> o_l[t][dv]: 32 lanes of a warp write 128 contiguous bytes per t
       {
         float o[32];  // warp-collective load (lanes >= D hold no state row)
