@@ -67,6 +67,7 @@ size_t layout(const Problem& p, char* base, Workspace* ws) {
   w.o_l = (float*)take(4 * BH * L * D);
   w.Qt = (void*)take(2 * BH * L * D);
   w.Kt = (void*)take(2 * BH * L * D);
+  w.gate = (float*)take(4 * BH * L);
   w.err = (int*)take(16);
   if (ws) *ws = w;
   return off;
@@ -183,31 +184,33 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
   // 2. compacted softmax-chunk lists (mirrors an overridden selection to sel_out)
   NATS_STAGE(stg, NATS_STAGE_COMPACT, 1,
              launch_compact(p, sel, ws.nprev, ws.sel_idx, (sel_in && sel_out) ? sel_out : nullptr, ws.err, st));
-  // 3. softmax branch
-  float* o_s = o_soft_out ? o_soft_out : ws.o_s;
   if (dt == NATS_BF16) {
-    NATS_STAGE(stg, NATS_STAGE_SOFTMAX, 1,
-               launch_softmax_tc(p, q, k, v, ws.nprev, ws.sel_idx, sel, o_s, ws.err, st));
-  } else {
-    NATS_STAGE(stg, NATS_STAGE_SOFTMAX, 1,
-               launch_softmax_simt(p, dt, q, k, v, ws.nprev, ws.sel_idx, o_s, st));
-  }
-  // 4. Gated DeltaNet branch (prep + scan with commit / rollback)
-  float* o_l = o_lin_out ? o_lin_out : ws.o_l;
-  if (dt == NATS_BF16) {
-    // bf16 factors W, U, P reuse the fp32 factor buffers of the workspace
+    // 3. Gated DeltaNet chunk factors and the per-token merge gate
     NATS_STAGE(stg, NATS_STAGE_GDN_PREP, 1,
-               launch_gdn_prep_mma(p, q, k, v, g, beta, ws.G, ws.W, ws.U, ws.P, ws.Qt, ws.Kt, st));
+               launch_gdn_prep_mma(p, q, k, v, g, beta, w_g, b_g, ws.G, ws.W, ws.U, ws.P, ws.Qt, ws.Kt,
+                                   ws.gate, st));
+    // 4. softmax branch; its epilogue writes out = w RMSNorm(o_s)
+    NATS_STAGE(stg, NATS_STAGE_SOFTMAX, 1,
+               launch_softmax_tc(p, q, k, v, ws.nprev, ws.sel_idx, sel, ws.gate, norm_w_soft, out, o_soft_out,
+                                 ws.err, st));
+    // 5. Gated DeltaNet chunk scan with commit / rollback
+    float* o_l = o_lin_out ? o_lin_out : ws.o_l;
     NATS_STAGE(stg, NATS_STAGE_GDN_SCAN, 1,
                launch_gdn_scan_tc(p, ws.Kt, sel, ws.G, ws.W, ws.U, ws.P, ws.Qt, o_l, state_out, ws.err, st));
+    // 6. out += (1 - w) RMSNorm(o_l)
+    NATS_STAGE(stg, NATS_STAGE_MERGE, 1, launch_merge_lin(p, o_l, ws.gate, norm_w_lin, out, st));
   } else {
+    // fp32 inputs: softmax branch, Gated DeltaNet branch, then RMSNorm + merge
+    float* o_s = o_soft_out ? o_soft_out : ws.o_s;
+    NATS_STAGE(stg, NATS_STAGE_SOFTMAX, 1,
+               launch_softmax_simt(p, dt, q, k, v, ws.nprev, ws.sel_idx, o_s, st));
+    float* o_l = o_lin_out ? o_lin_out : ws.o_l;
     NATS_STAGE(stg, NATS_STAGE_GDN_PREP, 1, launch_gdn_prep_simt(p, dt, q, k, v, g, beta, ws, st));
     NATS_STAGE(stg, NATS_STAGE_GDN_SCAN, 1,
                launch_gdn_scan_simt(p, dt, q, k, sel, ws, o_l, state_out, st));
+    NATS_STAGE(stg, NATS_STAGE_MERGE, 1,
+               launch_norm_merge(p, dt, o_s, o_l, q, w_g, b_g, norm_w_soft, norm_w_lin, out, st));
   }
-  // 5. RMSNorm per branch + gated merge
-  NATS_STAGE(stg, NATS_STAGE_MERGE, 1,
-             launch_norm_merge(p, dt, o_s, o_l, q, w_g, b_g, norm_w_soft, norm_w_lin, out, st));
   return NATS_OK;
 }
 

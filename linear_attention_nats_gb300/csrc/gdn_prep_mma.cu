@@ -13,7 +13,9 @@
 // [chunk][64][D]; U transposed, bf16 [chunk][D][64]; P bf16 [chunk][64][64];
 // Q~ = diag(scale e^G) Q, bf16 [chunk][64][D] (the query with its readout
 // decay and scale folded in); K~ = diag(e^{G_C - G}) K, bf16 [chunk][64][D]
-// (the key with the decay to the chunk end folded in); G fp32.
+// (the key with the decay to the chunk end folded in); G fp32; and the merge
+// gate of each token, w = sigmoid(q . W_g[h] + b_g[h]) ("Kernmechanismen"
+// item 4: weights generated from the query), fp32.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -82,7 +84,8 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
     const __nv_bfloat16* __restrict__ v, const float* __restrict__ g, const float* __restrict__ beta, int L,
     int N, float scale, float* __restrict__ Gout, __nv_bfloat16* __restrict__ Wout,
     __nv_bfloat16* __restrict__ Uout, __nv_bfloat16* __restrict__ Pout, __nv_bfloat16* __restrict__ Qtout,
-    __nv_bfloat16* __restrict__ Ktout) {
+    __nv_bfloat16* __restrict__ Ktout, const float* __restrict__ w_g, const float* __restrict__ b_g, int H,
+    float* __restrict__ gate_out) {
   using S = PrepSmem<D>;
   constexpr int RS = S::RS, TS = S::TS, FS = S::FS;
   extern __shared__ __align__(16) uint8_t smem[];
@@ -184,6 +187,26 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
     }
   }
   __syncthreads();
+  // ---- merge gate: two threads per token, D/2 features each
+  {
+    const int h = (int)(bh % H);
+    const int t = tid >> 1, hh = tid & 1;
+    const float* wg = w_g + (size_t)h * D + hh * (D / 2);
+    const __nv_bfloat16* qr = Qs + t * RS + hh * (D / 2);
+    float z = 0.f;
+#pragma unroll
+    for (int x8 = 0; x8 < D / 16; ++x8) {
+      const uint4 qv = *(const uint4*)(qr + 8 * x8);
+      const __nv_bfloat162* q2 = (const __nv_bfloat162*)&qv;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(q2[i]);
+        z = fmaf(f.x, wg[8 * x8 + 2 * i], fmaf(f.y, wg[8 * x8 + 2 * i + 1], z));
+      }
+    }
+    z += __shfl_xor_sync(0xffffffffu, z, 1);
+    if (hh == 0) gate_out[tok0 + t] = 1.f / (1.f + __expf(-(z + (b_g ? b_g[h] : 0.f))));
+  }
   // ---- Q~ = diag(scale e^G) Q and K~ = diag(e^{G_C - G}) K -> global (16-byte stores)
   {
     __nv_bfloat16* Qt = Qtout + tok0 * D;
@@ -378,8 +401,8 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
 }  // namespace
 
 cudaError_t launch_gdn_prep_mma(const Problem& p, const void* q, const void* k, const void* v, const float* g,
-                                const float* beta, float* G, void* W16, void* U16, void* P16, void* Qt16,
-                                void* Kt16, cudaStream_t st) {
+                                const float* beta, const float* w_g, const float* b_g, float* G, void* W16,
+                                void* U16, void* P16, void* Qt16, void* Kt16, float* gate, cudaStream_t st) {
   if (p.BH == 0 || p.N == 0) return cudaSuccess;
   auto run = [&](auto kern, int smem) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -387,7 +410,7 @@ cudaError_t launch_gdn_prep_mma(const Problem& p, const void* q, const void* k, 
     kern<<<(unsigned)(p.BH * p.N), 128, smem, st>>>(
         (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, g, beta, p.L, p.N, p.scale,
         G, (__nv_bfloat16*)W16, (__nv_bfloat16*)U16, (__nv_bfloat16*)P16, (__nv_bfloat16*)Qt16,
-        (__nv_bfloat16*)Kt16);
+        (__nv_bfloat16*)Kt16, w_g, b_g, p.H, gate);
     return cudaGetLastError();
   };
   return p.d == 64 ? run(gdn_prep_mma_kernel<64>, PrepSmem<64>::kBytes)

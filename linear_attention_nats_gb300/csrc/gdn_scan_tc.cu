@@ -16,13 +16,13 @@
 //
 // One CTA per (b, h) walks the N chunks in order; the fp32 state S stays in
 // TMEM for the whole sequence, next to its bf16 copy S0.  Per chunk c:
-//   MMA1  Z[c&1] = S0 [W; Q~]^T          (M = 128 lanes >= dv, N = 64 + 64, K = dk)
-//   all   Delta^T = U^T - Z[:, 0:64] -> TMEM (bf16)
-//   MMA2  Z[:, 64:128] += Delta^T P^T    (= O^T)
+//   MMA1  X = S0 W^T, O[c%3] = S0 Q~^T    (M = 128 lanes >= dv, N = 64 each, K = dk)
+//   all   Delta^T = U^T - X -> TMEM (bf16)
+//   MMA2  O[c%3] += Delta^T P^T
 //   MMA3  S += Delta^T K~                (linear chunks only)
 //   all   S -> bf16 S0; S *= gamma_C of the next chunk when it is linear
-//   all   O^T -> o_l (after the state work, off the critical path; Z is
-//         double-buffered)
+//   all   O^T -> o_l; the O work of chunk c runs after the state work of
+//         chunk c + 1, overlapping the next MMAs (O is triple-buffered).
 // Roles (320 threads): warps 0-7 elementwise, warp w owning TMEM lanes
 // 32 (w % 4) .. +31 and half (w / 4) of the columns; warp 8 TMA producer
 // (W, Q~, K~, U^T, P of coming chunks, double-buffered); warp 9 TMEM owner and
@@ -46,17 +46,18 @@ struct ScanSmem {
   static constexpr int kStage = kWQ + kK + kU + kP;
   static constexpr int offStage = 0;
   static constexpr int offBar = 2 * kStage;
-  static constexpr int kNumBars = 11;
+  static constexpr int kNumBars = 12;
   static constexpr int offTmem = offBar + kNumBars * 8;
   static constexpr int kBytes = offTmem + 16 + 1024;
 };
 
-// SB_OFREE + b: O^T of the chunks using Z buffer b has been read (one barrier per
-// buffer, so a waiter is never two phases behind)
-enum { SB_FULL = 0, SB_EMPTY = 2, SB_S0 = 4, SB_Z = 5, SB_DELTA = 6, SB_OFREE = 7, SB_SDONE = 9, SB_DONE = 10 };
+// SB_OFREE + b: O^T of the chunks using O buffer b has been read (one barrier
+// per buffer, so a waiter is never two phases behind)
+enum { SB_FULL = 0, SB_EMPTY = 2, SB_S0 = 4, SB_Z = 5, SB_DELTA = 6, SB_OFREE = 7, SB_SDONE = 10, SB_DONE = 11 };
 
 // TMEM columns
-constexpr uint32_t kColZ = 0;      // two Z buffers of 128 columns
+constexpr uint32_t kColX = 0;      // S0 W^T, 64 columns (consumed at once by Delta)
+constexpr uint32_t kColO = 64;     // three O^T buffers of 64 columns
 constexpr uint32_t kColS = 256;    // state, D columns (fp32)
 constexpr uint32_t kColS0 = 384;   // state bf16, D / 2 columns (two dk per column)
 constexpr uint32_t kColDT = 448;   // Delta^T bf16, 32 columns (64 t)
@@ -99,8 +100,7 @@ __global__ void __launch_bounds__(320, 1)
     tc::mbar_init(&bars[SB_S0], 256);
     tc::mbar_init(&bars[SB_Z], 1);
     tc::mbar_init(&bars[SB_DELTA], 256);
-    tc::mbar_init(&bars[SB_OFREE], 256);
-    tc::mbar_init(&bars[SB_OFREE + 1], 256);
+    for (int b = 0; b < 3; ++b) tc::mbar_init(&bars[SB_OFREE + b], 256);
     tc::mbar_init(&bars[SB_SDONE], 1);
     tc::mbar_init(&bars[SB_DONE], 1);
     tc::fence_barrier_init();
@@ -157,33 +157,35 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t id2 = tc::idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t id3 = tc::idesc_bf16_f32(128, D, false, true);
       bool ok = true;
+      uint8_t sel_c = sel[bh * N];  // selections are read one chunk ahead (global latency)
       for (int c = 0; c < N && ok; ++c) {
         const int s = c & 1;
+        const uint8_t sel_n = (c + 1 < N) ? sel[bh * N + c + 1] : 0;
         const uint32_t wq = tc::smem_u32(smem + S::offStage + s * S::kStage);
         const uint32_t kb = wq + S::kWQ, pb = wq + S::kWQ + S::kK + S::kU;
-        const uint32_t tZ = tmem + kColZ + (c & 1) * 128;
+        const uint32_t tX = tmem + kColX, tO = tmem + kColO + (c % 3) * 64;
         if (!(ok = tc::mbar_wait(&bars[SB_FULL + s], (c >> 1) & 1, err))) break;
         if (!(ok = tc::mbar_wait(&bars[SB_S0], c & 1, err))) break;
-        if (c >= 2 && !(ok = tc::mbar_wait(&bars[SB_OFREE + (c & 1)], ((c - 2) >> 1) & 1, err))) break;
+        if (c >= 3 && !(ok = tc::mbar_wait(&bars[SB_OFREE + (c % 3)], ((c - 3) / 3) & 1, err))) break;
         tc::fence_after();
         // S0 W^T first (Delta waits on it), then S0 Q~^T (O only)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t offb = (kk >> 2) * 16384 + (kk & 3) * 32;  // [W; Q~]: 128 lines per 64-col half
-          tc::mma_bf16_ts(tZ, tmem + kColS0 + kk * 8, tc::smem_desc_sw128(wq + offb, 16, 1024), id1, kk > 0);
+          tc::mma_bf16_ts(tX, tmem + kColS0 + kk * 8, tc::smem_desc_sw128(wq + offb, 16, 1024), id1, kk > 0);
         }
         tc::mma_commit(&bars[SB_Z]);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t offb = (kk >> 2) * 16384 + (kk & 3) * 32 + 8192;
-          tc::mma_bf16_ts(tZ + 64, tmem + kColS0 + kk * 8, tc::smem_desc_sw128(wq + offb, 16, 1024), id1, kk > 0);
+          tc::mma_bf16_ts(tO, tmem + kColS0 + kk * 8, tc::smem_desc_sw128(wq + offb, 16, 1024), id1, kk > 0);
         }
         if (!(ok = tc::mbar_wait(&bars[SB_DELTA], c & 1, err))) break;
         tc::fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc::mma_bf16_ts(tZ + 64, tmem + kColDT + kk * 8, tc::smem_desc_sw128(pb + kk * 32, 16, 1024), id2, 1);
-        if (sel[bh * N + c] != 0) {
+          tc::mma_bf16_ts(tO, tmem + kColDT + kk * 8, tc::smem_desc_sw128(pb + kk * 32, 16, 1024), id2, 1);
+        if (sel_c != 0) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             tc::mma_bf16_ts(tmem + kColS, tmem + kColDT + kk * 8, tc::smem_desc_sw128(kb + kk * 2048, 8192, 1024),
@@ -191,6 +193,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         tc::mma_commit(&bars[SB_SDONE]);
         tc::mma_commit(&bars[SB_EMPTY + s]);
+        sel_c = sel_n;
       }
       tc::mma_commit(&bars[SB_DONE]);
       tc::mbar_wait(&bars[SB_DONE], 0, err);
@@ -219,13 +222,38 @@ __global__ void __launch_bounds__(320, 1)
       tc::fence_before();
       tc::mbar_arrive(&bars[SB_S0]);
     }
+    // O work of chunk cc: o_l[t][dv] for t = 32 hf .. +31; a warp's 32 lanes
+    // write 128 contiguous bytes per t
+    auto o_phase = [&](int cc) {
+      float o[32];  // warp-collective load (lanes >= D hold no state row)
+      tc::tmem_ld32(tmem + kColO + (cc % 3) * 64 + lane_off + 32 * hf, o);
+      tc::tmem_ld_wait();
+      if (has_row) {
+        float* dst = o_l + (bh * (long long)L + 64LL * cc + 32 * hf) * D + r;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) dst[(size_t)i * D] = o[i];
+      }
+      tc::fence_before();
+      tc::mbar_arrive(&bars[SB_OFREE + (cc % 3)]);
+    };
     bool ok = true;
+    // per-chunk selections and end-of-chunk log-decays, read two chunks ahead
+    // (a global load on the critical path costs more than a chunk's MMAs)
+    const uint8_t* selh = sel + bh * N;
+    const float* Gh = G + bh * (long long)L;
+    bool lin_c = selh[0] != 0;
+    bool lin_n = N > 1 && selh[1] != 0;
+    float gC_n = N > 1 ? Gh[64 + 63] : 0.f;
     for (int c = 0; c < N; ++c) {
-      // per-chunk constants, loaded ahead of the waits
-      const bool lin = sel[bh * N + c] != 0;
-      const bool lin_next = (c + 1 < N) && (sel[bh * N + c + 1] != 0);
-      const float gnext = lin_next ? __expf(G[bh * (long long)L + 64LL * c + 64 + 63]) : 1.f;
-      const uint32_t tZ = tmem + kColZ + (c & 1) * 128 + lane_off;
+      const bool has_nn = c + 2 < N;
+      const uint8_t sel_nn = has_nn ? selh[c + 2] : 0;
+      const float gC_nn = has_nn ? Gh[64LL * (c + 2) + 63] : 0.f;
+      const bool lin = lin_c, lin_next = lin_n;
+      const float gnext = lin_next ? __expf(gC_n) : 1.f;
+      lin_c = lin_n;
+      lin_n = sel_nn != 0;
+      gC_n = gC_nn;
+      const uint32_t tX = tmem + kColX + lane_off;
       // ---- Delta^T (columns t = 32 hf .. 32 hf + 31 of this row)
       {
         const uint8_t* Ub = smem + S::offStage + (c & 1) * S::kStage + S::kWQ + S::kK;
@@ -241,7 +269,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_Z], c & 1, err)))) break;
         tc::fence_after();
-        tc::tmem_ld32(tZ + 32 * hf, x);
+        tc::tmem_ld32(tX + 32 * hf, x);
         tc::tmem_ld_wait();
         if (has_row) {
 #pragma unroll
@@ -293,20 +321,9 @@ __global__ void __launch_bounds__(320, 1)
         if (SC > 32) tc::tmem_st32(tmem + kColS + lane_off + hf * SC + 32, *reinterpret_cast<float(*)[32]>(&v[SC > 32 ? 32 : 0]));
         tc::tmem_st_wait();
       }
-      // ---- O^T -> o_l[t][dv]: 32 lanes of a warp write 128 contiguous bytes per t
-      {
-        float o[32];  // warp-collective load (lanes >= D hold no state row)
-        tc::tmem_ld32(tZ + 64 + 32 * hf, o);
-        tc::tmem_ld_wait();
-        if (has_row) {
-          float* dst = o_l + (bh * (long long)L + 64LL * c + 32 * hf) * D + r;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) dst[(size_t)i * D] = o[i];
-        }
-      }
-      tc::fence_before();
-      tc::mbar_arrive(&bars[SB_OFREE + (c & 1)]);
+      if (c > 0) o_phase(c - 1);
     }
+    if (ok && N > 0) o_phase(N - 1);  // the last chunk's O work (its SDONE was waited)
     if (ok && state_out && has_row) {
       tc::fence_after();
 #pragma unroll 1

@@ -13,9 +13,12 @@ cudaError_t launch_score(const Problem& p, int dtype, const void* q, const void*
 cudaError_t launch_compact(const Problem& p, const uint8_t* sel, int32_t* nprev, int32_t* sel_idx,
                            uint8_t* sel_copy, int* err, cudaStream_t st);
 
+// bf16 softmax branch; its epilogue writes out = w RMSNorm(o_s) (bf16) with
+// the per-token gate w; o_s (fp32 diagnostics) may be null.
 cudaError_t launch_softmax_tc(const Problem& p, const void* q, const void* k, const void* v,
-                              const int32_t* nprev, const int32_t* sel_idx, const uint8_t* sel, float* o_s,
-                              int* err, cudaStream_t st);
+                              const int32_t* nprev, const int32_t* sel_idx, const uint8_t* sel,
+                              const float* gate, const float* nw_s, void* out, float* o_s, int* err,
+                              cudaStream_t st);
 
 cudaError_t launch_softmax_simt(const Problem& p, int dtype, const void* q, const void* k,
                                 const void* v, const int32_t* nprev, const int32_t* sel_idx,
@@ -29,13 +32,19 @@ cudaError_t launch_gdn_scan_simt(const Problem& p, int dtype, const void* q, con
                                  const uint8_t* sel, const Workspace& ws, float* o_l,
                                  float* state_out, cudaStream_t st);
 
+// bf16 chunk factors of the Gated DeltaNet branch plus the per-token merge gate.
 cudaError_t launch_gdn_prep_mma(const Problem& p, const void* q, const void* k, const void* v, const float* g,
-                                const float* beta, float* G, void* W16, void* U16, void* P16, void* Qt16,
-                                void* Kt16, cudaStream_t st);
+                                const float* beta, const float* w_g, const float* b_g, float* G, void* W16,
+                                void* U16, void* P16, void* Qt16, void* Kt16, float* gate, cudaStream_t st);
 
+// bf16 chunk scan: o_l (fp32 [BH, L, dv]); state_out may be null.
 cudaError_t launch_gdn_scan_tc(const Problem& p, const void* Kt16, const uint8_t* sel, const float* G,
                                const void* W16, const void* UT16, const void* P16, const void* Qt16, float* o_l,
                                float* state_out, int* err, cudaStream_t st);
+
+// bf16 path: out (holding w RMSNorm(o_s)) += (1 - w) RMSNorm(o_l).
+cudaError_t launch_merge_lin(const Problem& p, const float* o_l, const float* gate, const float* nw_l, void* out,
+                             cudaStream_t st);
 
 cudaError_t launch_norm_merge(const Problem& p, int dtype, const float* o_s, const float* o_l,
                               const void* q, const float* w_g, const float* b_g, const float* nw_s,

@@ -48,6 +48,35 @@ __global__ void __launch_bounds__(256) norm_merge_kernel(
   }
 }
 
+// bf16 path, second half of the merge: out already holds w RMSNorm(o_s)
+// (written by the softmax kernel's epilogue); add (1 - w) RMSNorm(o_l).  One
+// warp per token row, coalesced; HBM-bound.
+template <int D>
+__global__ void __launch_bounds__(256) merge_lin_kernel(const float* __restrict__ o_l,
+                                                        const float* __restrict__ gate,
+                                                        const float* __restrict__ nw_l, long long rows,
+                                                        float eps, __nv_bfloat16* __restrict__ out) {
+  constexpr int NC = D / 32;
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int lane = threadIdx.x & 31;
+  const size_t base = (size_t)row * D;
+  float xl[NC], sl = 0.f;
+#pragma unroll
+  for (int i = 0; i < NC; ++i) {
+    xl[i] = o_l[base + lane + 32 * i];
+    sl = fmaf(xl[i], xl[i], sl);
+  }
+  sl = warp_sum(sl);
+  const float f = (1.f - gate[row]) * rsqrtf(sl * (1.f / D) + eps);
+#pragma unroll
+  for (int i = 0; i < NC; ++i) {
+    const int col = lane + 32 * i;
+    const float nl = f * xl[i] * (nw_l ? nw_l[col] : 1.f);
+    out[base + col] = __float2bfloat16_rn(__bfloat162float(out[base + col]) + nl);
+  }
+}
+
 template <class T, int D>
 static cudaError_t launch_t(const Problem& p, const float* o_s, const float* o_l, const void* q,
                             const float* w_g, const float* b_g, const float* nw_s,
@@ -68,6 +97,18 @@ cudaError_t launch_norm_merge(const Problem& p, int dtype, const float* o_s, con
                      : launch_t<__nv_bfloat16, 128>(p, o_s, o_l, q, w_g, b_g, nw_s, nw_l, out, st);
   return p.d == 64 ? launch_t<float, 64>(p, o_s, o_l, q, w_g, b_g, nw_s, nw_l, out, st)
                    : launch_t<float, 128>(p, o_s, o_l, q, w_g, b_g, nw_s, nw_l, out, st);
+}
+
+cudaError_t launch_merge_lin(const Problem& p, const float* o_l, const float* gate, const float* nw_l, void* out,
+                             cudaStream_t st) {
+  const long long rows = p.BH * p.L;
+  if (rows == 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((rows + 7) / 8);
+  if (p.d == 64)
+    merge_lin_kernel<64><<<blocks, 256, 0, st>>>(o_l, gate, nw_l, rows, p.eps, (__nv_bfloat16*)out);
+  else
+    merge_lin_kernel<128><<<blocks, 256, 0, st>>>(o_l, gate, nw_l, rows, p.eps, (__nv_bfloat16*)out);
+  return cudaGetLastError();
 }
 
 }  // namespace nats

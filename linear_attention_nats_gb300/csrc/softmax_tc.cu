@@ -29,6 +29,9 @@
 //              rescaled in place) only when a row max grows by more than 2^8,
 //              so P <= 256 and the rescale, which waits for the previous
 //              P V product, is rare.
+//              The tile epilogue writes the softmax half of the layer output
+//              ("Kernmechanismen" item 4): w RMSNorm(O / l) in bf16, w the
+//              query gate; the Gated DeltaNet scan adds its half afterwards.
 // TMEM: S0, S1 (128 columns each), O0, O1 (D columns each).
 // Every wait is bounded (tc::kWaitLimitNs); on expiry the kernel records an
 // error, drains what it issued and exits.
@@ -102,7 +105,9 @@ __global__ void __launch_bounds__(256, 1)
     softmax_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ nprev,
                       const int32_t* __restrict__ sel_idx, const uint8_t* __restrict__ sel, int L, int N,
-                      int T, long long BH, float sl2, float* __restrict__ o_s, int* __restrict__ err) {
+                      int T, long long BH, float sl2, const float* __restrict__ gate,
+                      const float* __restrict__ nw_s, float eps, __nv_bfloat16* __restrict__ out,
+                      float* __restrict__ o_s, int* __restrict__ err) {
   using S = SoftmaxSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -358,22 +363,48 @@ __global__ void __launch_bounds__(256, 1)
         tc::mbar_arrive(&bars[B_PF + b]);
       }
       if (!ok) break;
-      // epilogue: O / l -> o_s
+      // epilogue: out = w RMSNorm(O / l)   (validity is warp-uniform: a warp's rows share a half)
       if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_OF + ob], (tn >> 1) & 1, err)))) break;
       tc::fence_after();
-      const float inv = 1.f / l;
-      const bool valid = (half == 0 || ti.has_c1);
-      float* dst = o_s + (size_t)(ti.bh * (long long)L + 128LL * ti.p + r) * D;
-#pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        float o[32];
-        tc::tmem_ld32(o_addr + ch * 32, o);
-        tc::tmem_ld_wait();
-        if (valid) {
+      if (half == 0 || ti.has_c1) {
+        const float inv = 1.f / l;
+        const size_t row = (size_t)(ti.bh * (long long)L + 128LL * ti.p + r);
+        const float w = gate[row];
+        float ssa[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int x = 0; x < 8; ++x)
-            ((float4*)(dst + ch * 32))[x] = make_float4(o[4 * x] * inv, o[4 * x + 1] * inv, o[4 * x + 2] * inv,
-                                                       o[4 * x + 3] * inv);
+        for (int ch = 0; ch < D / 32; ++ch) {
+          float o[32];
+          tc::tmem_ld32(o_addr + ch * 32, o);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int x = 0; x < 32; ++x) ssa[x & 3] = fmaf(o[x], o[x], ssa[x & 3]);
+        }
+        const float ms = ((ssa[0] + ssa[1]) + (ssa[2] + ssa[3])) * inv * inv * (1.f / D);
+        const float cs = w * inv * rsqrtf(ms + eps);
+        __nv_bfloat16* orow = out + row * D;
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+          float o[32];
+          tc::tmem_ld32(o_addr + ch * 32, o);
+          tc::tmem_ld_wait();
+          if (o_s) {
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+              ((float4*)(o_s + row * D + ch * 32))[x] =
+                  make_float4(o[4 * x] * inv, o[4 * x + 1] * inv, o[4 * x + 2] * inv, o[4 * x + 3] * inv);
+          }
+#pragma unroll
+          for (int g8 = 0; g8 < 4; ++g8) {
+            uint4 pk;
+            uint32_t* p32 = (uint32_t*)&pk;
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              const int cc = ch * 32 + g8 * 8 + 2 * x;
+              const float f0 = nw_s ? cs * nw_s[cc] : cs, f1 = nw_s ? cs * nw_s[cc + 1] : cs;
+              p32[x] = tc::pack_bf16x2(f0 * o[g8 * 8 + 2 * x], f1 * o[g8 * 8 + 2 * x + 1]);
+            }
+            *(uint4*)(orow + ch * 32 + g8 * 8) = pk;
+          }
         }
       }
       tc::fence_before();
@@ -423,8 +454,9 @@ bool make_tile_map(CUtensorMap* map, const void* base, long long rows, int D) {
 
 template <int D>
 static cudaError_t launch_tc_t(const Problem& p, const void* q, const void* k, const void* v,
-                               const int32_t* nprev, const int32_t* sel_idx, const uint8_t* sel, float* o_s,
-                               int* err, cudaStream_t st) {
+                               const int32_t* nprev, const int32_t* sel_idx, const uint8_t* sel,
+                               const float* gate, const float* nw_s, void* out, float* o_s, int* err,
+                               cudaStream_t st) {
   CUtensorMap mq, mk, mv;
   const long long rows = p.BH * p.L;
   if (!make_tile_map(&mq, q, rows, D) || !make_tile_map(&mk, k, rows, D) || !make_tile_map(&mv, v, rows, D))
@@ -440,16 +472,18 @@ static cudaError_t launch_tc_t(const Problem& p, const void* q, const void* k, c
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
   kern<<<grid, 256, smem, st>>>(mq, mk, mv, nprev, sel_idx, sel, p.L, p.N, T, p.BH,
-                                p.scale * 1.4426950408889634f, o_s, err);
+                                p.scale * 1.4426950408889634f, gate, nw_s, p.eps, (__nv_bfloat16*)out, o_s,
+                                err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_softmax_tc(const Problem& p, const void* q, const void* k, const void* v,
-                              const int32_t* nprev, const int32_t* sel_idx, const uint8_t* sel, float* o_s,
-                              int* err, cudaStream_t st) {
+                              const int32_t* nprev, const int32_t* sel_idx, const uint8_t* sel,
+                              const float* gate, const float* nw_s, void* out, float* o_s, int* err,
+                              cudaStream_t st) {
   if (p.BH == 0 || p.N == 0) return cudaSuccess;
-  return p.d == 64 ? launch_tc_t<64>(p, q, k, v, nprev, sel_idx, sel, o_s, err, st)
-                   : launch_tc_t<128>(p, q, k, v, nprev, sel_idx, sel, o_s, err, st);
+  return p.d == 64 ? launch_tc_t<64>(p, q, k, v, nprev, sel_idx, sel, gate, nw_s, out, o_s, err, st)
+                   : launch_tc_t<128>(p, q, k, v, nprev, sel_idx, sel, gate, nw_s, out, o_s, err, st);
 }
 
 }  // namespace nats
