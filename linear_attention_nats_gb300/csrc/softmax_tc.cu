@@ -297,47 +297,46 @@ __global__ void __launch_bounds__(256, 1)
           mode1 = ti.has_c1 ? kCausal : kNone;
         }
         const uint32_t s_addr = tmem + b * 128 + lane_off;
-        // pass 1: row max over the visible keys, 32 columns at a time, with
-        // eight independent partial maxima (short dependency chains).  The
-        // mask pattern is uniform across a warp (a warp's rows share a half).
+        // The whole 128-column block of the row is read from TMEM once (one
+        // wait), masked in registers, reduced to its max with eight partial
+        // maxima (short dependency chains), then exponentiated in place.
         const bool masked = (mode0 != kFull) || (mode1 != kFull);
+        float v[128];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) tc::tmem_ld32(s_addr + ch * 32, *reinterpret_cast<float(*)[32]>(&v[32 * ch]));
+        tc::tmem_ld_wait();
+        if (masked) {
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch)
+            mask_chunk(*reinterpret_cast<float(*)[32]>(&v[32 * ch]), ch < 2 ? mode0 : mode1, (ch & 1) * 32, rr);
+        }
         float mxa[8];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) mxa[x] = -INFINITY;
+        for (int x = 0; x < 8; ++x) mxa[x] = v[x];
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          float v[32];
-          tc::tmem_ld32(s_addr + ch * 32, v);
-          tc::tmem_ld_wait();
-          if (masked) mask_chunk(v, ch < 2 ? mode0 : mode1, (ch & 1) * 32, rr);
-#pragma unroll
-          for (int x = 0; x < 32; ++x) mxa[x & 7] = fmaxf(mxa[x & 7], v[x]);
-        }
+        for (int x = 8; x < 128; ++x) mxa[x & 7] = fmaxf(mxa[x & 7], v[x]);
         const float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
                                fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
         const float m_cand = mx * sl2;  // every row sees >= 1 key of every block
         const bool need = (j > 0) && (m_cand > m_used + kRescaleLog2);
         const float alpha = need ? tc::fast_exp2(m_used - m_cand) : 1.f;
         if (j == 0 || need) m_used = m_cand;
-        // pass 2: P = exp2(S scale - m) (masked keys -> exp2(-inf) = 0), packed
-        // to bf16 over S in place (P column c holds keys 2c, 2c+1)
+        // P = exp2(S scale - m) (masked keys -> exp2(-inf) = 0), packed to
+        // bf16 over S in place (P column c holds keys 2c, 2c+1)
         float sa[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) sa[x] = 0.f;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
-          float v[32];
-          tc::tmem_ld32(s_addr + ch * 32, v);
-          tc::tmem_ld_wait();
-          if (masked) mask_chunk(v, ch < 2 ? mode0 : mode1, (ch & 1) * 32, rr);
-#pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            v[x] = tc::fast_exp2(fmaf(v[x], sl2, -m_used));
-            sa[x & 7] += v[x];
-          }
           uint32_t pk[16];
 #pragma unroll
-          for (int x = 0; x < 16; ++x) pk[x] = tc::pack_bf16x2(v[2 * x], v[2 * x + 1]);
+          for (int x = 0; x < 16; ++x) {
+            const float e0 = tc::fast_exp2(fmaf(v[32 * ch + 2 * x], sl2, -m_used));
+            const float e1 = tc::fast_exp2(fmaf(v[32 * ch + 2 * x + 1], sl2, -m_used));
+            sa[(2 * x) & 7] += e0;
+            sa[(2 * x + 1) & 7] += e1;
+            pk[x] = tc::pack_bf16x2(e0, e1);
+          }
           tc::tmem_st16u(s_addr + ch * 16, pk);
         }
         const float sum = ((sa[0] + sa[1]) + (sa[2] + sa[3])) + ((sa[4] + sa[5]) + (sa[6] + sa[7]));
