@@ -19,20 +19,25 @@
 // Roles (256 threads):
 //   warp 0     TMA producer: Q of each tile, then K and V blocks into a
 //              3-deep ring (K and V with separate barriers)
-//   warp 1     TMEM owner + MMA issuer: S_j = Q K_j^T into one of two TMEM S
-//              buffers; O += P_j V_j with P_j read from TMEM (it overwrites
-//              S_j in place) into one of two TMEM O buffers (one per tile,
-//              alternating, so a tile's epilogue overlaps the next tile)
-//   warps 4-7  softmax: thread r owns query row r (its TMEM lane); one pass
-//              over the row in the exp2 domain; P_j packed to bf16 in TMEM.
-//              The running max used for the exponent is raised (and O, l
-//              rescaled in place) only when a row max grows by more than 2^8,
-//              so P <= 256 and the rescale, which waits for the previous
+//   warp 1     TMEM owner + MMA issuer: S_j = Q K_j^T into one of three TMEM
+//              S buffers, up to two blocks ahead of O += P_j V_j, with P_j
+//              read from TMEM (it overwrites S_j in place).  Three buffers
+//              put three blocks of softmax work between a P V product and
+//              the S product that must wait for it, which hides the MMA and
+//              barrier latencies of that round trip.
+//   warps 4-7  softmax: thread r owns query row r (its TMEM lane); the row's
+//              128 scores of a block are read from TMEM once, their max taken
+//              in registers, and P_j packed to bf16 in TMEM, in the exp2
+//              domain.  The running max used for the exponent is raised (and
+//              O, l rescaled in place) only when a row max grows by more than
+//              2^8, so P <= 256 and the rescale, which waits for the previous
 //              P V product, is rare.
 //              The tile epilogue writes the softmax half of the layer output
 //              ("Kernmechanismen" item 4): w RMSNorm(O / l) in bf16, w the
-//              query gate; the Gated DeltaNet scan adds its half afterwards.
-// TMEM: S0, S1 (128 columns each), O0, O1 (D columns each).
+//              query gate; the Gated DeltaNet side adds its half afterwards.
+//              It reads O before the warps release the next tile's first P,
+//              so one O accumulator serves every tile.
+// TMEM: S0, S1, S2 (128 columns each), O (D columns).
 // Every wait is bounded (tc::kWaitLimitNs); on expiry the kernel records an
 // error, drains what it issued and exits.
 #include <mutex>
@@ -47,6 +52,7 @@ namespace {
 enum { kFull = 0, kCausal = 1, kNone = 2 };
 constexpr float kRescaleLog2 = 8.f;  // lazy-rescale threshold (log2 units)
 constexpr int KS = 3;                // K/V ring depth
+constexpr int NS = 3;                // S/P buffers in TMEM
 
 template <int D>
 struct SoftmaxSmem {
@@ -57,7 +63,7 @@ struct SoftmaxSmem {
   static constexpr int offK = offQ + kQ;
   static constexpr int offV = offK + KS * kKV;
   static constexpr int offBar = offV + KS * kKV;
-  static constexpr int kNumBars = 2 + 4 * KS + 10;
+  static constexpr int kNumBars = 2 + 4 * KS + 3 * NS + 1;
   static constexpr int offTmem = offBar + kNumBars * 8;
   static constexpr int kBytes = offTmem + 16 + 1024;  // + alignment slack
 };
@@ -65,7 +71,7 @@ struct SoftmaxSmem {
 // barrier slots
 enum {
   B_QF = 0, B_QE = 1, B_KF = 2, B_KE = B_KF + KS, B_VF = B_KE + KS, B_VE = B_VF + KS,
-  B_SF = B_VE + KS, B_PF = B_SF + 2, B_PV = B_PF + 2, B_OF = B_PV + 2, B_OE = B_OF + 2
+  B_SF = B_VE + KS, B_PF = B_SF + NS, B_PV = B_PF + NS, B_OF = B_PV + NS
 };
 
 // Masked keys of a 32-column chunk become -inf.  key0 = index of v[0] within
@@ -126,13 +132,12 @@ __global__ void __launch_bounds__(256, 1)
       tc::mbar_init(&bars[B_VF + s], 1);
       tc::mbar_init(&bars[B_VE + s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NS; ++b) {
       tc::mbar_init(&bars[B_SF + b], 1);
       tc::mbar_init(&bars[B_PF + b], 128);
       tc::mbar_init(&bars[B_PV + b], 1);
-      tc::mbar_init(&bars[B_OF + b], 1);
-      tc::mbar_init(&bars[B_OE + b], 128);
     }
+    tc::mbar_init(&bars[B_OF], 1);
     tc::fence_barrier_init();
   }
   if (warp == 1) {
@@ -212,40 +217,39 @@ __global__ void __launch_bounds__(256, 1)
       const uint32_t q_base = tc::smem_u32(Qs);
       int gj = 0, tn = 0;
       bool ok = true;
-      auto issue_s = [&](int g) -> bool {
+      auto issue_s = [&](int g, bool last_of_tile) -> bool {
         const int ks = g % KS;
         if (!tc::mbar_wait(&bars[B_KF + ks], (g / KS) & 1, err)) return false;
         tc::fence_after();
         const uint32_t k_base = tc::smem_u32(smem + S::offK + ks * S::kKV);
-        const uint32_t tS = tmem + (g & 1) * 128;
+        const uint32_t tS = tmem + (g % NS) * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * S::kHalf + (kk & 3) * 32;
           tc::mma_bf16(tS, tc::smem_desc_sw128(q_base + off, 16, 1024), tc::smem_desc_sw128(k_base + off, 16, 1024),
                        idesc_qk, kk > 0);
         }
-        tc::mma_commit(&bars[B_SF + (g & 1)]);
+        tc::mma_commit(&bars[B_SF + g % NS]);
         tc::mma_commit(&bars[B_KE + ks]);
+        if (last_of_tile) tc::mma_commit(&bars[B_QE]);  // Q may be replaced once these S are done
         return true;
       };
       for (int i = blockIdx.x; i < n_tiles && ok; i += gridDim.x, ++tn) {
         const TileInfo ti = tile_info(i, BH, T, N, nprev, sel);
-        const int ob = tn & 1;
-        const uint32_t tO = tmem + 256 + ob * 128;
+        const uint32_t tO = tmem + NS * 128;
         if (!(ok = tc::mbar_wait(&bars[B_QF], tn & 1, err))) break;
-        if (!(ok = tc::mbar_wait(&bars[B_OE + ob], ((tn >> 1) & 1) ^ 1, err))) break;
         tc::fence_after();
+        // S runs up to two blocks ahead of P V.  The previous tile's O was
+        // read out by the softmax warps before they released this tile's
+        // first P, so the first P V below may overwrite it.
         const int g0 = gj;
-        if (!(ok = issue_s(g0))) break;
-        if (ti.nb == 1) tc::mma_commit(&bars[B_QE]);
+        if (!(ok = issue_s(g0, ti.nb == 1))) break;
+        if (ti.nb > 1 && !(ok = issue_s(g0 + 1, ti.nb == 2))) break;
         for (int j = 0; j < ti.nb; ++j) {
           const int g = g0 + j;
-          if (j + 1 < ti.nb) {
-            if (!(ok = issue_s(g + 1))) break;
-            if (j + 2 == ti.nb) tc::mma_commit(&bars[B_QE]);
-          }
-          const int b = g & 1, ks = g % KS;
-          if (!(ok = tc::mbar_wait(&bars[B_PF + b], (g >> 1) & 1, err))) break;
+          if (j + 2 < ti.nb && !(ok = issue_s(g + 2, j + 3 == ti.nb))) break;
+          const int b = g % NS, ks = g % KS;
+          if (!(ok = tc::mbar_wait(&bars[B_PF + b], (g / NS) & 1, err))) break;
           if (!(ok = tc::mbar_wait(&bars[B_VF + ks], (g / KS) & 1, err))) break;
           tc::fence_after();
           const uint32_t v_base = tc::smem_u32(smem + S::offV + ks * S::kKV);
@@ -259,15 +263,14 @@ __global__ void __launch_bounds__(256, 1)
         }
         if (!ok) break;
         gj = g0 + ti.nb;
-        tc::mma_commit(&bars[B_OF + ob]);
+        tc::mma_commit(&bars[B_OF]);
       }
       // drain: every MMA issued so far completes before the commits land
-      tc::mma_commit(&bars[B_PV + 0]);
-      tc::mma_commit(&bars[B_PV + 1]);
-      const int lastpv0 = gj / 2 + (gj & 1);  // uses of B_PV[0] before the drain commit (blocks with g even)
-      const int lastpv1 = gj / 2;
-      tc::mbar_wait(&bars[B_PV + 0], lastpv0 & 1, nullptr);
-      tc::mbar_wait(&bars[B_PV + 1], lastpv1 & 1, nullptr);
+      for (int b = 0; b < NS; ++b) tc::mma_commit(&bars[B_PV + b]);
+      for (int b = 0; b < NS; ++b) {
+        const int uses = gj > b ? (gj - 1 - b) / NS + 1 : 0;  // earlier commits to B_PV[b]
+        tc::mbar_wait(&bars[B_PV + b], uses & 1, nullptr);
+      }
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------- softmax
@@ -278,12 +281,11 @@ __global__ void __launch_bounds__(256, 1)
     bool ok = true;
     for (int i = blockIdx.x; i < n_tiles && ok; i += gridDim.x, ++tn) {
       const TileInfo ti = tile_info(i, BH, T, N, nprev, sel);
-      const int ob = tn & 1;
-      const uint32_t o_addr = tmem + 256 + ob * 128 + lane_off;
+      const uint32_t o_addr = tmem + NS * 128 + lane_off;
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < ti.nb; ++j, ++gj) {
-        const int b = gj & 1;
-        if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_SF + b], (gj >> 1) & 1, err)))) break;
+        const int b = gj % NS;
+        if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_SF + b], (gj / NS) & 1, err)))) break;
         tc::fence_after();
         int mode0, mode1;
         if (j < ti.nbp) {
@@ -344,7 +346,7 @@ __global__ void __launch_bounds__(256, 1)
         if (__any_sync(0xffffffffu, need)) {
           // O must hold every product so far before it is rescaled in place
           const int gp = gj - 1;
-          if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_PV + (gp & 1)], (gp >> 1) & 1, err)))) break;
+          if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_PV + gp % NS], (gp / NS) & 1, err)))) break;
           tc::fence_after();
 #pragma unroll 1
           for (int ch = 0; ch < D / 32; ++ch) {
@@ -363,7 +365,7 @@ __global__ void __launch_bounds__(256, 1)
       }
       if (!ok) break;
       // epilogue: out = w RMSNorm(O / l)   (validity is warp-uniform: a warp's rows share a half)
-      if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_OF + ob], (tn >> 1) & 1, err)))) break;
+      if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_OF], tn & 1, err)))) break;
       tc::fence_after();
       if (half == 0 || ti.has_c1) {
         const float inv = 1.f / l;
@@ -406,8 +408,6 @@ __global__ void __launch_bounds__(256, 1)
           }
         }
       }
-      tc::fence_before();
-      tc::mbar_arrive(&bars[B_OE + ob]);
     }
   }
   tc::fence_before();
