@@ -156,14 +156,19 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t id1 = tc::idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t id2 = tc::idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t id3 = tc::idesc_bf16_f32(128, D, false, true);
+      // descriptors are built once per stage; each MMA only offsets them
+      const uint32_t w0 = tc::smem_u32(smem + S::offStage);
+      const uint64_t wd0 = tc::smem_desc_sw128(w0, 16, 1024);
+      const uint64_t kd0 = tc::smem_desc_sw128(w0 + S::kWQ, 8192, 1024);
+      const uint64_t pd0 = tc::smem_desc_sw128(w0 + S::kWQ + S::kK + S::kU, 16, 1024);
       bool ok = true;
       uint8_t sel_c = sel[bh * N];  // selections are read one chunk ahead (global latency)
       for (int c = 0; c < N && ok; ++c) {
         const int s = c & 1;
         const uint8_t sel_n = (c + 1 < N) ? sel[bh * N + c + 1] : 0;
-        const uint32_t wq = tc::smem_u32(smem + S::offStage + s * S::kStage);
-        const uint32_t kb = wq + S::kWQ, pb = wq + S::kWQ + S::kK + S::kU;
         const uint32_t tX = tmem + kColX, tO = tmem + kColO + (c % 3) * 64;
+        const uint32_t sb = s * S::kStage;
+        const uint64_t wd = tc::desc_add(wd0, sb), kd = tc::desc_add(kd0, sb), pd = tc::desc_add(pd0, sb);
         if (!(ok = tc::mbar_wait(&bars[SB_FULL + s], (c >> 1) & 1, err))) break;
         if (!(ok = tc::mbar_wait(&bars[SB_S0], c & 1, err))) break;
         if (c >= 3 && !(ok = tc::mbar_wait(&bars[SB_OFREE + (c % 3)], ((c - 3) / 3) & 1, err))) break;
@@ -172,24 +177,23 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t offb = (kk >> 2) * 16384 + (kk & 3) * 32;  // [W; Q~]: 128 lines per 64-col half
-          tc::mma_bf16_ts(tX, tmem + kColS0 + kk * 8, tc::smem_desc_sw128(wq + offb, 16, 1024), id1, kk > 0);
+          tc::mma_bf16_ts(tX, tmem + kColS0 + kk * 8, tc::desc_add(wd, offb), id1, kk > 0);
         }
         tc::mma_commit(&bars[SB_Z]);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t offb = (kk >> 2) * 16384 + (kk & 3) * 32 + 8192;
-          tc::mma_bf16_ts(tO, tmem + kColS0 + kk * 8, tc::smem_desc_sw128(wq + offb, 16, 1024), id1, kk > 0);
+          tc::mma_bf16_ts(tO, tmem + kColS0 + kk * 8, tc::desc_add(wd, offb), id1, kk > 0);
         }
         if (!(ok = tc::mbar_wait(&bars[SB_DELTA], c & 1, err))) break;
         tc::fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc::mma_bf16_ts(tO, tmem + kColDT + kk * 8, tc::smem_desc_sw128(pb + kk * 32, 16, 1024), id2, 1);
+          tc::mma_bf16_ts(tO, tmem + kColDT + kk * 8, tc::desc_add(pd, kk * 32), id2, 1);
         if (sel_c != 0) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc::mma_bf16_ts(tmem + kColS, tmem + kColDT + kk * 8, tc::smem_desc_sw128(kb + kk * 2048, 8192, 1024),
-                            id3, 1);
+            tc::mma_bf16_ts(tmem + kColS, tmem + kColDT + kk * 8, tc::desc_add(kd, kk * 2048), id3, 1);
         }
         tc::mma_commit(&bars[SB_SDONE]);
         tc::mma_commit(&bars[SB_EMPTY + s]);

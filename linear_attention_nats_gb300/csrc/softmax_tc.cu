@@ -214,20 +214,24 @@ __global__ void __launch_bounds__(256, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, D, false, true);
-      const uint32_t q_base = tc::smem_u32(Qs);
+      // descriptors are built once; each MMA only offsets the address field
+      // (the MMA warp shares its SM sub-partition with a busy softmax warp,
+      // so every instruction it needs to issue an MMA counts)
+      const uint64_t qd0 = tc::smem_desc_sw128(tc::smem_u32(Qs), 16, 1024);
+      const uint64_t kd0 = tc::smem_desc_sw128(tc::smem_u32(smem + S::offK), 16, 1024);
+      const uint64_t vd0 = tc::smem_desc_sw128(tc::smem_u32(smem + S::offV), S::kHalf, 1024);
       int gj = 0, tn = 0;
       bool ok = true;
       auto issue_s = [&](int g, bool last_of_tile) -> bool {
         const int ks = g % KS;
         if (!tc::mbar_wait(&bars[B_KF + ks], (g / KS) & 1, err)) return false;
         tc::fence_after();
-        const uint32_t k_base = tc::smem_u32(smem + S::offK + ks * S::kKV);
+        const uint64_t kd = tc::desc_add(kd0, ks * S::kKV);
         const uint32_t tS = tmem + (g % NS) * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * S::kHalf + (kk & 3) * 32;
-          tc::mma_bf16(tS, tc::smem_desc_sw128(q_base + off, 16, 1024), tc::smem_desc_sw128(k_base + off, 16, 1024),
-                       idesc_qk, kk > 0);
+          tc::mma_bf16(tS, tc::desc_add(qd0, off), tc::desc_add(kd, off), idesc_qk, kk > 0);
         }
         tc::mma_commit(&bars[B_SF + g % NS]);
         tc::mma_commit(&bars[B_KE + ks]);
@@ -252,12 +256,11 @@ __global__ void __launch_bounds__(256, 1)
           if (!(ok = tc::mbar_wait(&bars[B_PF + b], (g / NS) & 1, err))) break;
           if (!(ok = tc::mbar_wait(&bars[B_VF + ks], (g / KS) & 1, err))) break;
           tc::fence_after();
-          const uint32_t v_base = tc::smem_u32(smem + S::offV + ks * S::kKV);
+          const uint64_t vd = tc::desc_add(vd0, ks * S::kKV);
           const uint32_t tP = tmem + b * 128;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            tc::mma_bf16_ts(tO, tP + kk * 8, tc::smem_desc_sw128(v_base + kk * 2048, S::kHalf, 1024), idesc_pv,
-                            (j > 0) || (kk > 0));
+            tc::mma_bf16_ts(tO, tP + kk * 8, tc::desc_add(vd, kk * 2048), idesc_pv, (j > 0) || (kk > 0));
           tc::mma_commit(&bars[B_PV + b]);
           tc::mma_commit(&bars[B_VE + ks]);
         }
@@ -316,31 +319,34 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int x = 0; x < 8; ++x) mxa[x] = v[x];
 #pragma unroll
-        for (int x = 8; x < 128; ++x) mxa[x & 7] = fmaxf(mxa[x & 7], v[x]);
-        const float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
-                               fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
+        for (int x = 8; x < 128; x += 2) mxa[(x >> 1) & 7] = tc::max3(mxa[(x >> 1) & 7], v[x], v[x + 1]);
+        const float mx = fmaxf(tc::max3(mxa[0], mxa[1], mxa[2]), fmaxf(tc::max3(mxa[3], mxa[4], mxa[5]),
+                                                                          fmaxf(mxa[6], mxa[7])));
         const float m_cand = mx * sl2;  // every row sees >= 1 key of every block
         const bool need = (j > 0) && (m_cand > m_used + kRescaleLog2);
         const float alpha = need ? tc::fast_exp2(m_used - m_cand) : 1.f;
         if (j == 0 || need) m_used = m_cand;
         // P = exp2(S scale - m) (masked keys -> exp2(-inf) = 0), packed to
-        // bf16 over S in place (P column c holds keys 2c, 2c+1)
-        float sa[8];
-#pragma unroll
-        for (int x = 0; x < 8; ++x) sa[x] = 0.f;
+        // bf16 over S in place (P column c holds keys 2c, 2c+1); the scaling
+        // and the row sum run on fp32 pairs
+        const uint64_t sc2 = tc::f2_pack(sl2, sl2), nm2 = tc::f2_pack(-m_used, -m_used);
+        uint64_t sa2[4] = {0, 0, 0, 0};  // four pairs of partial sums (+0.0f bits)
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t pk[16];
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
-            const float e0 = tc::fast_exp2(fmaf(v[32 * ch + 2 * x], sl2, -m_used));
-            const float e1 = tc::fast_exp2(fmaf(v[32 * ch + 2 * x + 1], sl2, -m_used));
-            sa[(2 * x) & 7] += e0;
-            sa[(2 * x + 1) & 7] += e1;
+            float t0, t1;
+            tc::f2_unpack(tc::f2_fma(tc::f2_pack(v[32 * ch + 2 * x], v[32 * ch + 2 * x + 1]), sc2, nm2), t0, t1);
+            const float e0 = tc::fast_exp2(t0), e1 = tc::fast_exp2(t1);
+            sa2[x & 3] = tc::f2_add(sa2[x & 3], tc::f2_pack(e0, e1));
             pk[x] = tc::pack_bf16x2(e0, e1);
           }
           tc::tmem_st16u(s_addr + ch * 16, pk);
         }
+        float sa[8];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) tc::f2_unpack(sa2[x], sa[2 * x], sa[2 * x + 1]);
         const float sum = ((sa[0] + sa[1]) + (sa[2] + sa[3])) + ((sa[4] + sa[5]) + (sa[6] + sa[7]));
         tc::tmem_st_wait();
         if (__any_sync(0xffffffffu, need)) {
