@@ -17,8 +17,8 @@
 // Persistent CTAs walk a static list of tiles ordered heaviest first (nprev
 // grows with c); every role of a CTA walks the same list.
 // Roles (256 threads):
-//   warp 0     TMA producer: Q of each tile, then K and V blocks into a
-//              3-deep ring (K and V with separate barriers)
+//   warp 0     TMA producer of Q (one per tile) and of the K blocks (3-deep
+//              ring); warp 2 the producer of the V blocks (3-deep ring)
 //   warp 1     TMEM owner + MMA issuer: S_j = Q K_j^T into one of three TMEM
 //              S buffers, up to two blocks ahead of O += P_j V_j, with P_j
 //              read from TMEM (it overwrites S_j in place).  Three buffers
@@ -149,62 +149,69 @@ __global__ void __launch_bounds__(256, 1)
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == 2) {
+    // ----------------------------------------------------------- producers
+    // warp 0 loads Q and K, warp 2 loads V: separate streams, so that a K
+    // block is never queued behind a V block whose ring slot is still held
+    // by an earlier P V product
     if (lane == 0) {
-      tc::prefetch_tensormap(&tm_q);
-      tc::prefetch_tensormap(&tm_k);
-      tc::prefetch_tensormap(&tm_v);
+      const bool kq = (warp == 0);
+      if (kq) tc::prefetch_tensormap(&tm_q);
+      tc::prefetch_tensormap(kq ? &tm_k : &tm_v);
+      const CUtensorMap* tm = kq ? &tm_k : &tm_v;
+      uint8_t* ring = smem + (kq ? S::offK : S::offV);
+      uint64_t* full = &bars[kq ? B_KF : B_VF];
+      uint64_t* empty = &bars[kq ? B_KE : B_VE];
       int gj = 0, tn = 0;
       bool ok = true;
       for (int i = blockIdx.x; i < n_tiles && ok; i += gridDim.x, ++tn) {
         const TileInfo ti = tile_info(i, BH, T, N, nprev, sel);
         const long long row0 = ti.bh * (long long)L;
-        if (!(ok = tc::mbar_wait(&bars[B_QE], (tn & 1) ^ 1, err))) break;
-        tc::mbar_arrive_expect_tx(&bars[B_QF], S::kQ);
-        for (int h = 0; h < D / 64; ++h)
-          for (int rc = 0; rc < 2; ++rc)
-            tc::tma_load_2d(Qs + h * S::kHalf + rc * (S::kHalf / 2), &tm_q, 64 * h,
-                            (int)(row0 + 128LL * ti.p + 64 * rc), &bars[B_QF]);
-        for (int j = 0; j < ti.nb; ++j, ++gj) {
-          const int ks = gj % KS, par = ((gj / KS) & 1) ^ 1;
-          int ch[2];
+        if (kq) {
+          if (!(ok = tc::mbar_wait(&bars[B_QE], (tn & 1) ^ 1, err))) break;
+          tc::mbar_arrive_expect_tx(&bars[B_QF], S::kQ);
+          for (int h = 0; h < D / 64; ++h)
+            for (int rc = 0; rc < 2; ++rc)
+              tc::tma_load_2d(Qs + h * S::kHalf + rc * (S::kHalf / 2), &tm_q, 64 * h,
+                              (int)(row0 + 128LL * ti.p + 64 * rc), &bars[B_QF]);
+        }
+        // chunk pair of block j (the softmax chunks before c0, in pairs, then
+        // the diagonal pair), read one block ahead to hide the global latency
+        auto pair = [&](int j, int& c0, int& c1) {
           if (j < ti.nbp) {
-            ch[0] = sel_idx[ti.bh * N + 2 * j];
-            ch[1] = (2 * j + 1 < ti.n0) ? sel_idx[ti.bh * N + 2 * j + 1] : ti.c0;
+            c0 = sel_idx[ti.bh * N + 2 * j];
+            c1 = (2 * j + 1 < ti.n0) ? sel_idx[ti.bh * N + 2 * j + 1] : ti.c0;
           } else {
-            ch[0] = ti.c0;
-            ch[1] = ti.has_c1 ? ti.c0 + 1 : ti.c0;
+            c0 = ti.c0;
+            c1 = ti.has_c1 ? ti.c0 + 1 : ti.c0;
           }
-          uint8_t* Kb = smem + S::offK + ks * S::kKV;
-          uint8_t* Vb = smem + S::offV + ks * S::kKV;
-          if (!(ok = tc::mbar_wait(&bars[B_KE + ks], par, err))) break;
-          tc::mbar_arrive_expect_tx(&bars[B_KF + ks], S::kKV);
+        };
+        int ch0, ch1;
+        pair(0, ch0, ch1);
+        for (int j = 0; j < ti.nb; ++j, ++gj) {
+          int nx0 = 0, nx1 = 0;
+          if (j + 1 < ti.nb) pair(j + 1, nx0, nx1);
+          const int ks = gj % KS, par = ((gj / KS) & 1) ^ 1;
+          uint8_t* buf = ring + ks * S::kKV;
+          if (!(ok = tc::mbar_wait(&empty[ks], par, err))) break;
+          tc::mbar_arrive_expect_tx(&full[ks], S::kKV);
           for (int slot = 0; slot < 2; ++slot)
             for (int h = 0; h < D / 64; ++h)
-              tc::tma_load_2d(Kb + h * S::kHalf + slot * (S::kHalf / 2), &tm_k, 64 * h,
-                              (int)(row0 + 64LL * ch[slot]), &bars[B_KF + ks]);
-          if (!(ok = tc::mbar_wait(&bars[B_VE + ks], par, err))) break;
-          tc::mbar_arrive_expect_tx(&bars[B_VF + ks], S::kKV);
-          for (int slot = 0; slot < 2; ++slot)
-            for (int h = 0; h < D / 64; ++h)
-              tc::tma_load_2d(Vb + h * S::kHalf + slot * (S::kHalf / 2), &tm_v, 64 * h,
-                              (int)(row0 + 64LL * ch[slot]), &bars[B_VF + ks]);
+              tc::tma_load_2d(buf + h * S::kHalf + slot * (S::kHalf / 2), tm, 64 * h,
+                              (int)(row0 + 64LL * (slot ? ch1 : ch0)), &full[ks]);
+          ch0 = nx0;
+          ch1 = nx1;
         }
       }
       // make sure every load completed and every release commit landed
       for (int s = 0; s < KS; ++s) {
         const int uses = gj > s ? (gj - 1 - s) / KS + 1 : 0;
         if (uses > 0) {
-          tc::mbar_wait(&bars[B_KF + s], (uses - 1) & 1, nullptr);
-          tc::mbar_wait(&bars[B_VF + s], (uses - 1) & 1, nullptr);
-          if (ok) {
-            tc::mbar_wait(&bars[B_KE + s], (uses - 1) & 1, err);
-            tc::mbar_wait(&bars[B_VE + s], (uses - 1) & 1, err);
-          }
+          tc::mbar_wait(&full[s], (uses - 1) & 1, nullptr);
+          if (ok) tc::mbar_wait(&empty[s], (uses - 1) & 1, err);
         }
       }
-      if (tn > 0) {
+      if (kq && tn > 0) {
         tc::mbar_wait(&bars[B_QF], (tn - 1) & 1, nullptr);
         if (ok) tc::mbar_wait(&bars[B_QE], (tn - 1) & 1, err);
       }
