@@ -65,7 +65,8 @@ struct SoftmaxSmem {
   static constexpr int offBar = offV + KS * kKV;
   static constexpr int kNumBars = 2 + 4 * KS + 3 * NS + 1;
   static constexpr int offTmem = offBar + kNumBars * 8;
-  static constexpr int kBytes = offTmem + 16 + 1024;  // + alignment slack
+  static constexpr int offNw = offTmem + 16;  // RMSNorm weights of the softmax branch, D floats
+  static constexpr int kBytes = offNw + D * 4 + 1024;  // + alignment slack
 };
 
 // barrier slots
@@ -122,6 +123,8 @@ __global__ void __launch_bounds__(256, 1)
   uint32_t* tmem_slot = (uint32_t*)(smem + S::offTmem);
   const int n_tiles = (int)(BH * T);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* nw_sm = (float*)(smem + S::offNw);
+  for (int c = threadIdx.x; c < D; c += blockDim.x) nw_sm[c] = nw_s ? nw_s[c] : 1.f;
 
   if (threadIdx.x == 0) {
     tc::mbar_init(&bars[B_QF], 1);
@@ -164,8 +167,11 @@ __global__ void __launch_bounds__(256, 1)
       uint64_t* empty = &bars[kq ? B_KE : B_VE];
       int gj = 0, tn = 0;
       bool ok = true;
+      // each tile's descriptor is read one tile ahead (global latency)
+      TileInfo tnx = tile_info(blockIdx.x < n_tiles ? blockIdx.x : 0, BH, T, N, nprev, sel);
       for (int i = blockIdx.x; i < n_tiles && ok; i += gridDim.x, ++tn) {
-        const TileInfo ti = tile_info(i, BH, T, N, nprev, sel);
+        const TileInfo ti = tnx;
+        if (i + (int)gridDim.x < n_tiles) tnx = tile_info(i + gridDim.x, BH, T, N, nprev, sel);
         const long long row0 = ti.bh * (long long)L;
         if (kq) {
           if (!(ok = tc::mbar_wait(&bars[B_QE], (tn & 1) ^ 1, err))) break;
@@ -245,8 +251,11 @@ __global__ void __launch_bounds__(256, 1)
         if (last_of_tile) tc::mma_commit(&bars[B_QE]);  // Q may be replaced once these S are done
         return true;
       };
+      // each tile's descriptor is read one tile ahead (global latency)
+      TileInfo tnx = tile_info(blockIdx.x < n_tiles ? blockIdx.x : 0, BH, T, N, nprev, sel);
       for (int i = blockIdx.x; i < n_tiles && ok; i += gridDim.x, ++tn) {
-        const TileInfo ti = tile_info(i, BH, T, N, nprev, sel);
+        const TileInfo ti = tnx;
+        if (i + (int)gridDim.x < n_tiles) tnx = tile_info(i + gridDim.x, BH, T, N, nprev, sel);
         const uint32_t tO = tmem + NS * 128;
         if (!(ok = tc::mbar_wait(&bars[B_QF], tn & 1, err))) break;
         tc::fence_after();
@@ -289,8 +298,19 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     int gj = 0, tn = 0;
     bool ok = true;
+    // tile descriptor and the rows' query gate are read one tile ahead
+    auto gate_of = [&](const TileInfo& t) -> float {
+      return (half == 0 || t.has_c1) ? gate[t.bh * (long long)L + 128LL * t.p + r] : 0.f;
+    };
+    TileInfo tnx = tile_info(blockIdx.x < n_tiles ? blockIdx.x : 0, BH, T, N, nprev, sel);
+    float wnx = gate_of(tnx);
     for (int i = blockIdx.x; i < n_tiles && ok; i += gridDim.x, ++tn) {
-      const TileInfo ti = tile_info(i, BH, T, N, nprev, sel);
+      const TileInfo ti = tnx;
+      const float w = wnx;
+      if (i + (int)gridDim.x < n_tiles) {
+        tnx = tile_info(i + gridDim.x, BH, T, N, nprev, sel);
+        wnx = gate_of(tnx);
+      }
       const uint32_t o_addr = tmem + NS * 128 + lane_off;
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < ti.nb; ++j, ++gj) {
@@ -381,44 +401,39 @@ __global__ void __launch_bounds__(256, 1)
       if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_OF], tn & 1, err)))) break;
       tc::fence_after();
       if (half == 0 || ti.has_c1) {
+        // one TMEM pass: the row of O in registers, its mean square, then
+        // the scaled row packed to bf16
         const float inv = 1.f / l;
         const size_t row = (size_t)(ti.bh * (long long)L + 128LL * ti.p + r);
-        const float w = gate[row];
-        float ssa[4] = {0.f, 0.f, 0.f, 0.f};
+        float o[D];
 #pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          float o[32];
-          tc::tmem_ld32(o_addr + ch * 32, o);
-          tc::tmem_ld_wait();
+        for (int ch = 0; ch < D / 32; ++ch) tc::tmem_ld32(o_addr + ch * 32, *reinterpret_cast<float(*)[32]>(&o[32 * ch]));
+        tc::tmem_ld_wait();
+        float ssa[8];
 #pragma unroll
-          for (int x = 0; x < 32; ++x) ssa[x & 3] = fmaf(o[x], o[x], ssa[x & 3]);
-        }
-        const float ms = ((ssa[0] + ssa[1]) + (ssa[2] + ssa[3])) * inv * inv * (1.f / D);
+        for (int x = 0; x < 8; ++x) ssa[x] = 0.f;
+#pragma unroll
+        for (int x = 0; x < D; ++x) ssa[x & 7] = fmaf(o[x], o[x], ssa[x & 7]);
+        const float ss = ((ssa[0] + ssa[1]) + (ssa[2] + ssa[3])) + ((ssa[4] + ssa[5]) + (ssa[6] + ssa[7]));
+        const float ms = ss * inv * inv * (1.f / D);
         const float cs = w * inv * rsqrtf(ms + eps);
+        if (o_s) {
+#pragma unroll
+          for (int x = 0; x < D / 4; ++x)
+            ((float4*)(o_s + row * D))[x] =
+                make_float4(o[4 * x] * inv, o[4 * x + 1] * inv, o[4 * x + 2] * inv, o[4 * x + 3] * inv);
+        }
         __nv_bfloat16* orow = out + row * D;
-#pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-          float o[32];
-          tc::tmem_ld32(o_addr + ch * 32, o);
-          tc::tmem_ld_wait();
-          if (o_s) {
 #pragma unroll
-            for (int x = 0; x < 8; ++x)
-              ((float4*)(o_s + row * D + ch * 32))[x] =
-                  make_float4(o[4 * x] * inv, o[4 * x + 1] * inv, o[4 * x + 2] * inv, o[4 * x + 3] * inv);
+        for (int g8 = 0; g8 < D / 8; ++g8) {
+          uint4 pk;
+          uint32_t* p32 = (uint32_t*)&pk;
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const int cc = g8 * 8 + 2 * x;
+            p32[x] = tc::pack_bf16x2(cs * nw_sm[cc] * o[cc], cs * nw_sm[cc + 1] * o[cc + 1]);
           }
-#pragma unroll
-          for (int g8 = 0; g8 < 4; ++g8) {
-            uint4 pk;
-            uint32_t* p32 = (uint32_t*)&pk;
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              const int cc = ch * 32 + g8 * 8 + 2 * x;
-              const float f0 = nw_s ? cs * nw_s[cc] : cs, f1 = nw_s ? cs * nw_s[cc + 1] : cs;
-              p32[x] = tc::pack_bf16x2(f0 * o[g8 * 8 + 2 * x], f1 * o[g8 * 8 + 2 * x + 1]);
-            }
-            *(uint4*)(orow + ch * 32 + g8 * 8) = pk;
-          }
+          *(uint4*)(orow + g8 * 8) = pk;
         }
       }
     }
