@@ -171,6 +171,30 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+# ------------------------------------------------------------- ranks ----
+
+def rank_seed(seed, rank):
+    """Every rank draws its own batch: the (b, h) units are independent, so the
+    ranks share nothing on the data path (weak scaling)."""
+    return seed + 1000 * rank
+
+
+def max_over_ranks(x, dist, device):
+    """The slowest rank's value (the job ends when its last rank does)."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank, world, ms_per_step):
+    """Whole-job tokens/s: every rank's tokens over the max-over-ranks step time."""
+    return tokens_per_rank * world / (ms_per_step / 1e3)
+
+
 # -------------------------------------------------------------- arms ----
 
 def run_reference(args, rank):
@@ -215,7 +239,7 @@ def run_native(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     cfg = dict(gen.CONFIGS[WORKLOAD])
-    cfg["seed"] = cfg["seed"] + 1000 * rank  # every rank its own batch
+    cfg["seed"] = rank_seed(cfg["seed"], rank)
     inp = gen.make_inputs(name=WORKLOAD, **cfg)
     B, H, L, d = inp.B, inp.H, inp.L, inp.d
     N = L // C
@@ -292,13 +316,10 @@ def run_native(args, rank, world, local_rank):
         vals = [row[si][0].elapsed_time(row[si][1]) for row in stage_ev]
         if max(vals) > 2e-3:  # stages the path does not run keep their back-to-back records
             stage_ms[name] = sum(vals) / len(vals)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     ms_step = ms / args.steps
     tokens = B * L * world
-    value = tokens / (ms_step / 1e3)
+    value = job_throughput(B * L, world, ms_step)
 
     # ---- end to end: pinned host buffers in, result out, copies timed ----
     e2e = None
@@ -328,10 +349,7 @@ def run_native(args, rank, world, local_rank):
         torch.cuda.synchronize()
         barrier()
         ems = e0.elapsed_time(e1)
-        if dist is not None:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = max_over_ranks(ems, dist, dev)
         e2e = {"value": tokens / (ems / args.steps / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
         launches_e2e = None  # noqa: F841 (counted in gpu_launches only for the device-timed region)
