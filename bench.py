@@ -87,6 +87,50 @@ def algorithmic_work(sel, B, H, L, d, in_bytes):
             "softmax_fraction": float(soft.mean())}
 
 
+def kernel_work(B, H, L, d, flops_softmax):
+    """Algorithmic work per launch of each stage, with the bound it is held to.
+
+    softmax: 4 d FLOP per visible (query, key) pair (tensor-bound).  The
+    others are HBM-bound; their bytes are the unique I/O the stage has to
+    move (bf16 activations, fp32 g, beta, G, gate, o_l):
+      gdn_prep per chunk: read Q, K, V, g, beta; write W, U^T, Q~, K~ (bf16
+        C x d each), P (bf16 C x C), gate and G;
+      gdn_scan per chunk: read W, U^T, Q~, K~, P, G; write o_l (fp32 C x d);
+      merge per row: read o_l (fp32), gate, out (bf16); write out;
+      score per chunk: read Q, K."""
+    N = L // C
+    chunks, rows = B * H * N, B * H * L
+    prep = 3 * C * d * 2 + 2 * C * 4 + 4 * C * d * 2 + C * C * 2 + 2 * C * 4
+    scan = 4 * C * d * 2 + C * C * 2 + C * 4 + C * d * 4
+    return {
+        "softmax": ("tensor", float(flops_softmax), "softmax_tc.cu"),
+        "gdn_prep": ("hbm", float(chunks * prep), "gdn_prep_mma.cu"),
+        "gdn_scan": ("hbm", float(chunks * scan), "gdn_scan_tc.cu"),
+        "merge": ("hbm", float(rows * (d * 4 + 4 + 2 * d * 2)), "merge.cu"),
+        "score": ("hbm", float(chunks * 2 * C * d * 2), "select.cu"),
+    }
+
+
+def rooflines(work, stage_ms, pk):
+    """Per-stage roofline objects (achieved = algorithmic work / CUDA-event time)."""
+    out = {}
+    for name, (bound, amount, src) in work.items():
+        if name not in stage_ms:
+            continue
+        ms = stage_ms[name]
+        if bound == "tensor":
+            achieved, peak, unit = amount / (ms / 1e3) / 1e12, pk["bf16_tflops_sustained"], "TFLOP/s"
+            peak_src, per = f"{pk['source']} bf16 sustained", {"flops_per_launch": amount}
+        else:
+            achieved, peak, unit = amount / (ms / 1e3) / 1e9, pk["hbm_gbs"], "GB/s"
+            peak_src, per = f"{pk['source']} HBM copy", {"bytes_per_launch": amount}
+        out[name] = {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "peak_source": peak_src,
+                     "traffic": recorded_traffic(os.path.join(ROOT, "linear_attention_nats_gb300", "csrc", src)),
+                     "ms_per_launch": ms, **per}
+    return out
+
+
 # --------------------------------------------------------------- clocks ----
 
 class Clocks:
@@ -137,8 +181,8 @@ class Clocks:
 # ------------------------------------------------------------ traffic ----
 
 def recorded_traffic(kernel_src):
-    """DRAM bytes per launch of the softmax kernel from the committed ncu summary,
-    valid only while the kernel source is unchanged (hash match)."""
+    """DRAM bytes per launch of a kernel from the committed ncu summaries, valid
+    only while the kernel's source file is unchanged (hash match)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
@@ -355,15 +399,10 @@ def run_native(args, rank, world, local_rank):
         launches_e2e = None  # noqa: F841 (counted in gpu_launches only for the device-timed region)
 
     pk = peaks()
-    soft_ms = stage_ms["softmax"]
-    achieved = work["flops_softmax"] / (soft_ms / 1e3) / 1e12
     peak_tc = pk["bf16_tflops_sustained"]
-    roofline = {"kernel": "softmax branch incl. its w*RMSNorm epilogue (NATS_STAGE_SOFTMAX)", "bound": "tensor",
-                "achieved": achieved, "peak": peak_tc, "unit": "TFLOP/s", "frac": achieved / peak_tc,
-                "peak_source": f"{pk['source']} bf16 sustained",
-                "traffic": recorded_traffic(os.path.join(ROOT, "linear_attention_nats_gb300", "csrc",
-                                                         "softmax_simt.cu")),
-                "flops_per_launch": work["flops_softmax"], "ms_per_launch": soft_ms}
+    per_kernel = rooflines(kernel_work(B, H, L, d, work["flops_softmax"]), stage_ms, pk)
+    dominant = max(per_kernel, key=lambda k: per_kernel[k]["ms_per_launch"])
+    roofline = per_kernel[dominant]
     layer_tflops = work["flops_total"] / (ms_step / 1e3) / 1e12 / world
     res = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -374,6 +413,7 @@ def run_native(args, rank, world, local_rank):
                    "l2": "inputs larger than L2: Q/K/V 384 MiB + workspace per step, no explicit flush",
                    "softmax_fraction": work["softmax_fraction"]},
         "roofline": roofline,
+        "kernel_rooflines": per_kernel,
         "layer_roofline": {"bound": "tensor", "achieved": layer_tflops, "peak": peak_tc,
                            "unit": "TFLOP/s", "frac": layer_tflops / peak_tc,
                            "flops_per_step": work["flops_total"]},
