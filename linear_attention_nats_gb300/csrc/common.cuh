@@ -58,7 +58,8 @@ struct Workspace {
   void* Qt;          // [BH, L, dk] bf16 diag(scale e^G) Q, per chunk (bf16 path)
   void* Kt;          // [BH, L, dk] bf16 diag(e^{G_C - G}) K, per chunk (bf16 path)
   float* gate;       // [BH, L] merge weight w = sigmoid(q . W_g + b_g) (bf16 path)
-  int* err;          // [1] set by a kernel whose bounded wait expired (zeroed per call)
+  int* err;          // [0] set by a kernel whose bounded wait expired; [1] softmax tile counter
+                     // (both zeroed per call by the compaction kernel)
 };
 
 }  // namespace nats

@@ -81,7 +81,10 @@ __global__ void __launch_bounds__(256) compact_kernel(const uint8_t* __restrict_
                                                       uint8_t* __restrict__ sel_copy,
                                                       int* __restrict__ err) {
   const long long bh = blockIdx.x;
-  if (bh == 0 && threadIdx.x == 0 && err) *err = 0;
+  if (bh == 0 && threadIdx.x == 0 && err) {
+    err[0] = 0;  // bounded-wait flag
+    err[1] = 0;  // tile counter of the softmax kernel's dynamic schedule
+  }
   const uint8_t* s = sel + bh * N;
   int32_t* np = nprev + bh * N;
   int32_t* si = sel_idx + bh * N;

@@ -14,8 +14,10 @@
 // chose softmax; both diagonal slots are causal for their own rows.  Slots
 // without a chunk are loaded with c0 (finite data) and masked.
 //
-// Persistent CTAs walk a static list of tiles ordered heaviest first (nprev
-// grows with c); every role of a CTA walks the same list.
+// Persistent CTAs take tiles from a list ordered heaviest first (nprev grows
+// with c) through a global counter, so CTAs that start late (the SMs may be
+// shared with a concurrent kernel) or draw short tiles just take more; inside
+// a CTA the K producer takes the tile and hands it to the other roles.
 // Roles (256 threads):
 //   warp 0     TMA producer of Q (one per tile) and of the K blocks (3-deep
 //              ring); warp 2 the producer of the V blocks (3-deep ring)
@@ -53,6 +55,7 @@ enum { kFull = 0, kCausal = 1, kNone = 2 };
 constexpr float kRescaleLog2 = 8.f;  // lazy-rescale threshold (log2 units)
 constexpr int KS = 3;                // K/V ring depth
 constexpr int NS = 3;                // S/P buffers in TMEM
+constexpr int kTileTakers = 6;       // arrivals that free a tile-queue slot: MMA, V producer, 4 softmax warps
 
 template <int D>
 struct SoftmaxSmem {
@@ -63,16 +66,17 @@ struct SoftmaxSmem {
   static constexpr int offK = offQ + kQ;
   static constexpr int offV = offK + KS * kKV;
   static constexpr int offBar = offV + KS * kKV;
-  static constexpr int kNumBars = 2 + 4 * KS + 3 * NS + 1;
+  static constexpr int kNumBars = 2 + 4 * KS + 3 * NS + 1 + 4;
   static constexpr int offTmem = offBar + kNumBars * 8;
   static constexpr int offNw = offTmem + 16;  // RMSNorm weights of the softmax branch, D floats
-  static constexpr int kBytes = offNw + D * 4 + 1024;  // + alignment slack
+  static constexpr int offTq = offNw + D * 4;  // two-slot tile queue (ints)
+  static constexpr int kBytes = offTq + 16 + 1024;  // + alignment slack
 };
 
 // barrier slots
 enum {
   B_QF = 0, B_QE = 1, B_KF = 2, B_KE = B_KF + KS, B_VF = B_KE + KS, B_VE = B_VF + KS,
-  B_SF = B_VE + KS, B_PF = B_SF + NS, B_PV = B_PF + NS, B_OF = B_PV + NS
+  B_SF = B_VE + KS, B_PF = B_SF + NS, B_PV = B_PF + NS, B_OF = B_PV + NS, B_TF = B_OF + 1, B_TE = B_TF + 2
 };
 
 // Masked keys of a 32-column chunk become -inf.  key0 = index of v[0] within
@@ -114,7 +118,7 @@ __global__ void __launch_bounds__(256, 1)
                       const int32_t* __restrict__ sel_idx, const uint8_t* __restrict__ sel, int L, int N,
                       int T, long long BH, float sl2, const float* __restrict__ gate,
                       const float* __restrict__ nw_s, float eps, __nv_bfloat16* __restrict__ out,
-                      float* __restrict__ o_s, int* __restrict__ err) {
+                      float* __restrict__ o_s, int* __restrict__ err, int* __restrict__ tile_ctr) {
   using S = SoftmaxSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -141,6 +145,10 @@ __global__ void __launch_bounds__(256, 1)
       tc::mbar_init(&bars[B_PV + b], 1);
     }
     tc::mbar_init(&bars[B_OF], 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&bars[B_TF + s], 1);
+      tc::mbar_init(&bars[B_TE + s], kTileTakers);
+    }
     tc::fence_barrier_init();
   }
   if (warp == 1) {
@@ -151,6 +159,28 @@ __global__ void __launch_bounds__(256, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
+
+  // ---- dynamic tile schedule.  Tiles are numbered heaviest first; the K
+  // producer takes the next one from a global counter and publishes it in a
+  // two-slot queue in shared memory; every other role reads each entry once.
+  // -1 ends the list, -2 means a wait expired.
+  volatile int* tileq = (volatile int*)(smem + S::offTq);
+  auto publish = [&](int n) -> int {  // K producer: tile of sequence number n
+    const int s = n & 1;
+    if (!tc::mbar_wait(&bars[B_TE + s], ((n >> 1) & 1) ^ 1, err)) return -2;
+    const int a = atomicAdd(tile_ctr, 1);
+    const int t = a < n_tiles ? a : -1;
+    tileq[s] = t;
+    tc::mbar_arrive(&bars[B_TF + s]);  // release: the entry is visible to whoever sees the phase
+    return t;
+  };
+  auto take = [&](int n, bool release) -> int {  // every other role
+    const int s = n & 1;
+    if (!tc::mbar_wait(&bars[B_TF + s], (n >> 1) & 1, err)) return -2;
+    const int t = tileq[s];
+    if (release) tc::mbar_arrive(&bars[B_TE + s]);
+    return t;
+  };
 
   if (warp == 0 || warp == 2) {
     // ----------------------------------------------------------- producers
@@ -167,11 +197,14 @@ __global__ void __launch_bounds__(256, 1)
       uint64_t* empty = &bars[kq ? B_KE : B_VE];
       int gj = 0, tn = 0;
       bool ok = true;
+      auto next = [&](int n) { return kq ? publish(n) : take(n, true); };
+      int cur = next(0);
+      int nxt = cur >= 0 ? next(1) : -1;
       // each tile's descriptor is read one tile ahead (global latency)
-      TileInfo tnx = tile_info(blockIdx.x < n_tiles ? blockIdx.x : 0, BH, T, N, nprev, sel);
-      for (int i = blockIdx.x; i < n_tiles && ok; i += gridDim.x, ++tn) {
+      TileInfo tnx = tile_info(cur >= 0 ? cur : 0, BH, T, N, nprev, sel);
+      for (; cur >= 0 && ok; ++tn) {
         const TileInfo ti = tnx;
-        if (i + (int)gridDim.x < n_tiles) tnx = tile_info(i + gridDim.x, BH, T, N, nprev, sel);
+        if (nxt >= 0) tnx = tile_info(nxt, BH, T, N, nprev, sel);
         const long long row0 = ti.bh * (long long)L;
         if (kq) {
           if (!(ok = tc::mbar_wait(&bars[B_QE], (tn & 1) ^ 1, err))) break;
@@ -208,7 +241,11 @@ __global__ void __launch_bounds__(256, 1)
           ch0 = nx0;
           ch1 = nx1;
         }
+        if (!ok) break;
+        cur = nxt;
+        nxt = cur >= 0 ? next(tn + 2) : -1;
       }
+      if (cur == -2 || nxt == -2) ok = false;
       // make sure every load completed and every release commit landed
       for (int s = 0; s < KS; ++s) {
         const int uses = gj > s ? (gj - 1 - s) / KS + 1 : 0;
@@ -251,11 +288,13 @@ __global__ void __launch_bounds__(256, 1)
         if (last_of_tile) tc::mma_commit(&bars[B_QE]);  // Q may be replaced once these S are done
         return true;
       };
+      int cur = take(0, true);
+      int nxt = cur >= 0 ? take(1, true) : -1;
       // each tile's descriptor is read one tile ahead (global latency)
-      TileInfo tnx = tile_info(blockIdx.x < n_tiles ? blockIdx.x : 0, BH, T, N, nprev, sel);
-      for (int i = blockIdx.x; i < n_tiles && ok; i += gridDim.x, ++tn) {
+      TileInfo tnx = tile_info(cur >= 0 ? cur : 0, BH, T, N, nprev, sel);
+      for (; cur >= 0 && ok; ++tn) {
         const TileInfo ti = tnx;
-        if (i + (int)gridDim.x < n_tiles) tnx = tile_info(i + gridDim.x, BH, T, N, nprev, sel);
+        if (nxt >= 0) tnx = tile_info(nxt, BH, T, N, nprev, sel);
         const uint32_t tO = tmem + NS * 128;
         if (!(ok = tc::mbar_wait(&bars[B_QF], tn & 1, err))) break;
         tc::fence_after();
@@ -283,6 +322,8 @@ __global__ void __launch_bounds__(256, 1)
         if (!ok) break;
         gj = g0 + ti.nb;
         tc::mma_commit(&bars[B_OF]);
+        cur = nxt;
+        nxt = cur >= 0 ? take(tn + 2, true) : -1;
       }
       // drain: every MMA issued so far completes before the commits land
       for (int b = 0; b < NS; ++b) tc::mma_commit(&bars[B_PV + b]);
@@ -302,13 +343,21 @@ __global__ void __launch_bounds__(256, 1)
     auto gate_of = [&](const TileInfo& t) -> float {
       return (half == 0 || t.has_c1) ? gate[t.bh * (long long)L + 128LL * t.p + r] : 0.f;
     };
-    TileInfo tnx = tile_info(blockIdx.x < n_tiles ? blockIdx.x : 0, BH, T, N, nprev, sel);
-    float wnx = gate_of(tnx);
-    for (int i = blockIdx.x; i < n_tiles && ok; i += gridDim.x, ++tn) {
+    auto take_w = [&](int n) -> int {  // one read per warp of a tile-queue entry
+      const int t = __shfl_sync(0xffffffffu, take(n, false), 0);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bars[B_TE + (n & 1)]);
+      return t;
+    };
+    int cur = take_w(0);
+    int nxt = cur >= 0 ? take_w(1) : -1;
+    TileInfo tnx = tile_info(cur >= 0 ? cur : 0, BH, T, N, nprev, sel);
+    float wnx = cur >= 0 ? gate_of(tnx) : 0.f;
+    for (; cur >= 0 && ok; ++tn) {
       const TileInfo ti = tnx;
       const float w = wnx;
-      if (i + (int)gridDim.x < n_tiles) {
-        tnx = tile_info(i + gridDim.x, BH, T, N, nprev, sel);
+      if (nxt >= 0) {
+        tnx = tile_info(nxt, BH, T, N, nprev, sel);
         wnx = gate_of(tnx);
       }
       const uint32_t o_addr = tmem + NS * 128 + lane_off;
@@ -436,6 +485,8 @@ __global__ void __launch_bounds__(256, 1)
           *(uint4*)(orow + g8 * 8) = pk;
         }
       }
+      cur = nxt;
+      nxt = cur >= 0 ? take_w(tn + 2) : -1;
     }
   }
   tc::fence_before();
@@ -500,7 +551,7 @@ static cudaError_t launch_tc_t(const Problem& p, const void* q, const void* k, c
   const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
   kern<<<grid, 256, smem, st>>>(mq, mk, mv, nprev, sel_idx, sel, p.L, p.N, T, p.BH,
                                 p.scale * 1.4426950408889634f, gate, nw_s, p.eps, (__nv_bfloat16*)out, o_s,
-                                err);
+                                err, err + 1);
   return cudaGetLastError();
 }
 
