@@ -2,6 +2,7 @@
 // the launch sequence of the NAtS-L hybrid attention layer forward.
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/nats.h"
 #include "common.cuh"
@@ -94,6 +95,40 @@ struct Stages {
       if ((stg).mark((stg).prof->stop, id) != cudaSuccess) return NATS_ERR_CUDA;      \
     }                                                                                 \
   } while (0)
+
+// The Gated DeltaNet scan is sequential in the chunks of a head: one CTA per
+// (b, h), so it occupies at most B*H SMs.  The softmax kernel runs
+// concurrently on a second stream: the scan is launched on the caller's
+// stream right behind the chunk factors, so its CTAs are placed first, and
+// the softmax kernel's persistent CTAs, which take tiles dynamically, fill
+// the remaining SMs and then the ones the scan releases.  One stream and two
+// events per device, created on first use; the fork / join is enqueued under
+// a lock so that calls from several host threads do not interleave.
+struct Side {
+  std::mutex mu;
+  bool tried = false;
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+Side* side_of_current_device() {
+  static std::mutex mu;
+  static Side sides[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  Side& sd = sides[dev];
+  if (!sd.tried) {
+    sd.tried = true;
+    if (cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess) {
+      sd.s = nullptr;
+      cudaGetLastError();
+    }
+  }
+  return sd.s ? &sd : nullptr;
+}
 
 }  // namespace
 }  // namespace nats
@@ -189,14 +224,30 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
     NATS_STAGE(stg, NATS_STAGE_GDN_PREP, 1,
                launch_gdn_prep_mma(p, q, k, v, g, beta, w_g, b_g, ws.G, ws.W, ws.U, ws.P, ws.Qt, ws.Kt,
                                    ws.gate, st));
-    // 4. softmax branch; its epilogue writes out = w RMSNorm(o_s)
-    NATS_STAGE(stg, NATS_STAGE_SOFTMAX, 1,
-               launch_softmax_tc(p, q, k, v, ws.nprev, ws.sel_idx, sel, ws.gate, norm_w_soft, out, o_soft_out,
-                                 ws.err, st));
-    // 5. Gated DeltaNet chunk scan with commit / rollback
+    // 4. Gated DeltaNet chunk scan with commit / rollback (caller's stream)
+    // 5. softmax branch, concurrently on the side stream (in order on the
+    //    caller's stream if that stream could not be made); its epilogue
+    //    writes out = w RMSNorm(o_s)
     float* o_l = o_lin_out ? o_lin_out : ws.o_l;
-    NATS_STAGE(stg, NATS_STAGE_GDN_SCAN, 1,
-               launch_gdn_scan_tc(p, ws.Kt, sel, ws.G, ws.W, ws.U, ws.P, ws.Qt, o_l, state_out, ws.err, st));
+    Side* sd = side_of_current_device();
+    {
+      std::unique_lock<std::mutex> lk;
+      cudaStream_t ss = st;
+      if (sd) {
+        lk = std::unique_lock<std::mutex>(sd->mu);
+        if (cudaEventRecord(sd->fork, st) != cudaSuccess || cudaStreamWaitEvent(sd->s, sd->fork, 0) != cudaSuccess)
+          return NATS_ERR_CUDA;
+        ss = sd->s;
+      }
+      NATS_STAGE(stg, NATS_STAGE_GDN_SCAN, 1,
+                 launch_gdn_scan_tc(p, ws.Kt, sel, ws.G, ws.W, ws.U, ws.P, ws.Qt, o_l, state_out, ws.err, st));
+      Stages stg_side{prof, ss};
+      NATS_STAGE(stg_side, NATS_STAGE_SOFTMAX, 1,
+                 launch_softmax_tc(p, q, k, v, ws.nprev, ws.sel_idx, sel, ws.gate, norm_w_soft, out, o_soft_out,
+                                   ws.err, ss));
+      if (sd && (cudaEventRecord(sd->join, sd->s) != cudaSuccess || cudaStreamWaitEvent(st, sd->join, 0) != cudaSuccess))
+        return NATS_ERR_CUDA;
+    }
     // 6. out += (1 - w) RMSNorm(o_l)
     NATS_STAGE(stg, NATS_STAGE_MERGE, 1, launch_merge_lin(p, o_l, ws.gate, norm_w_lin, out, st));
   } else {
