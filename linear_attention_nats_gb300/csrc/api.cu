@@ -209,21 +209,26 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
   const int dt = dims->dtype;
   Stages stg{prof, st};
 
-  // 1. selection (score layer, or the caller's override)
+  // 1. selection (score layer, or the caller's override).  With bf16 inputs
+  //    the chunk-factor kernel scores the chunks from the Q and K it stages.
   const uint8_t* sel = sel_in;
+  uint8_t* score_dst = nullptr;
   if (!sel) {
-    uint8_t* dst = sel_out ? sel_out : ws.sel;
-    NATS_STAGE(stg, NATS_STAGE_SCORE, 1, launch_score(p, dt, q, k, w_s, b_s, dst, nullptr, st));
-    sel = dst;
+    score_dst = sel_out ? sel_out : ws.sel;
+    if (dt != NATS_BF16)
+      NATS_STAGE(stg, NATS_STAGE_SCORE, 1, launch_score(p, dt, q, k, w_s, b_s, score_dst, nullptr, st));
+    sel = score_dst;
   }
-  // 2. compacted softmax-chunk lists (mirrors an overridden selection to sel_out)
+  if (dt == NATS_BF16) {
+    // 2. Gated DeltaNet chunk factors, the per-token merge gate (and the selection)
+    NATS_STAGE(stg, NATS_STAGE_GDN_PREP, 1,
+               launch_gdn_prep_mma(p, q, k, v, g, beta, w_g, b_g, ws.G, ws.W, ws.U, ws.P, ws.Qt, ws.Kt,
+                                   ws.gate, w_s, b_s, score_dst, st));
+  }
+  // 3. compacted softmax-chunk lists (mirrors an overridden selection to sel_out)
   NATS_STAGE(stg, NATS_STAGE_COMPACT, 1,
              launch_compact(p, sel, ws.nprev, ws.sel_idx, (sel_in && sel_out) ? sel_out : nullptr, ws.err, st));
   if (dt == NATS_BF16) {
-    // 3. Gated DeltaNet chunk factors and the per-token merge gate
-    NATS_STAGE(stg, NATS_STAGE_GDN_PREP, 1,
-               launch_gdn_prep_mma(p, q, k, v, g, beta, w_g, b_g, ws.G, ws.W, ws.U, ws.P, ws.Qt, ws.Kt,
-                                   ws.gate, st));
     // 4. Gated DeltaNet chunk scan with commit / rollback (caller's stream)
     // 5. softmax branch, concurrently on the side stream (in order on the
     //    caller's stream if that stream could not be made); its epilogue

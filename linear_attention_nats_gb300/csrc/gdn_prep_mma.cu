@@ -16,6 +16,10 @@
 // (the key with the decay to the chunk end folded in); G fp32; and the merge
 // gate of each token, w = sigmoid(q . W_g[h] + b_g[h]) ("Kernmechanismen"
 // item 4: weights generated from the query), fp32.
+// Optionally it also scores the chunk ("Kernmechanismen" item 1: mean pool of
+// [q ; k] over the chunk, one linear score per operation, the higher score
+// wins, ties to softmax), from the Q and K it has staged anyway, so the
+// layer forward needs no separate pass over Q and K for the selection.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -73,7 +77,8 @@ struct PrepSmem {
   static constexpr int offB = offG + C * 4;          // fp32 [C] beta
   static constexpr int offBg = offB + C * 4;         // fp32 [C] beta e^G
   static constexpr int offX = offBg + C * 4;         // fp32 [C][FS] scratch of the blocked inverse
-  static constexpr int kBytes = offX + C * FS * 4;
+  static constexpr int offRed = offX + C * FS * 4;   // fp32 [2][4] per-warp partial chunk scores
+  static constexpr int kBytes = offRed + 32;
 };
 
 // One CTA (4 warps) per (b, h, chunk).  Warp w owns rows 16w .. 16w+15 of
@@ -85,7 +90,8 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
     int N, float scale, float* __restrict__ Gout, __nv_bfloat16* __restrict__ Wout,
     __nv_bfloat16* __restrict__ Uout, __nv_bfloat16* __restrict__ Pout, __nv_bfloat16* __restrict__ Qtout,
     __nv_bfloat16* __restrict__ Ktout, const float* __restrict__ w_g, const float* __restrict__ b_g, int H,
-    float* __restrict__ gate_out) {
+    float* __restrict__ gate_out, const float* __restrict__ w_s, const float* __restrict__ b_s,
+    uint8_t* __restrict__ sel_out) {
   using S = PrepSmem<D>;
   constexpr int RS = S::RS, TS = S::TS, FS = S::FS;
   extern __shared__ __align__(16) uint8_t smem[];
@@ -207,11 +213,19 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
     z += __shfl_xor_sync(0xffffffffu, z, 1);
     if (hh == 0) gate_out[tok0 + t] = 1.f / (1.f + __expf(-(z + (b_g ? b_g[h] : 0.f))));
   }
-  // ---- Q~ = diag(scale e^G) Q and K~ = diag(e^{G_C - G}) K -> global (16-byte stores)
+  // ---- Q~ = diag(scale e^G) Q and K~ = diag(e^{G_C - G}) K -> global (16-byte stores);
+  // the same pass sums the columns of Q and K for the chunk score (a thread
+  // keeps one 8-column group x = tid % VPR fixed over its rows)
+  float* colsum = (float*)(smem + S::offX);  // [4 warps][VPR][16]: rows 0-15 of the inverse scratch,
+                                             // which the off-diagonal tiles of the inverse never write
+  static_assert(4 * (D / 8) * 16 * 4 <= 16 * S::FS * 4, "column partials must fit rows 0-15 of X");
   {
     __nv_bfloat16* Qt = Qtout + tok0 * D;
     __nv_bfloat16* Kt = Ktout + tok0 * D;
     const float GC = Gs[C - 1];
+    float cs[16];
+#pragma unroll
+    for (int x = 0; x < 16; ++x) cs[x] = 0.f;
     for (int e = tid; e < C * VPR; e += 128) {
       const int t = e / VPR, x = e % VPR;
       const float fq = scale * __expf(Gs[t]);
@@ -229,9 +243,25 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
         const float2 vk = __bfloat1622float2(hk[i]);
         q32[i] = pack2(vq.x * fq, vq.y * fq);
         k32[i] = pack2(vk.x * fk, vk.y * fk);
+        cs[2 * i] += vq.x;
+        cs[2 * i + 1] += vq.y;
+        cs[8 + 2 * i] += vk.x;
+        cs[8 + 2 * i + 1] += vk.y;
       }
       *(uint4*)(Qt + t * D + x * 8) = oq;
       *(uint4*)(Kt + t * D + x * 8) = ok;
+    }
+    if (sel_out) {
+      // 128 / VPR threads share each x; combine them within the warp, then
+      // leave one partial per (warp, x) in shared memory
+#pragma unroll
+      for (int o = VPR; o < 32; o <<= 1)
+#pragma unroll
+        for (int x = 0; x < 16; ++x) cs[x] += __shfl_xor_sync(0xffffffffu, cs[x], o);
+      if (lane < VPR) {
+#pragma unroll
+        for (int x = 0; x < 16; ++x) colsum[(warp * VPR + lane) * 16 + x] = cs[x];
+      }
     }
   }
   // ---- T = (I + A)^{-1}, unit lower triangular, blocked in 16 x 16 tiles:
@@ -260,6 +290,34 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
     Bg[u] = Bs[u] * __expf(Gs[u]);
   }
   __syncthreads();
+  if (sel_out) {
+    // chunk score: thread tid owns pooled features tid and tid + 128 of [q ; k]
+    const int h = (int)(bh % H);
+    const float* W = w_s + (size_t)h * 4 * D;
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int f = tid + 128 * u;
+      if (f < 2 * D) {
+        const int fk = f < D ? 0 : 1, fd = f - fk * D, x = fd >> 3, col = (fd & 7) + 8 * fk;
+        float m = 0.f;
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) m += colsum[(w4 * VPR + x) * 16 + col];
+        m *= 1.0f / C;
+        s0 = fmaf(W[f], m, s0);
+        s1 = fmaf(W[2 * D + f], m, s1);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+    }
+    if (lane == 0) {
+      ((float*)(smem + S::offRed))[warp] = s0;
+      ((float*)(smem + S::offRed))[4 + warp] = s1;
+    }
+  }
   // off-diagonal tiles by distance: a thread owns one row and 8 columns of a tile
   for (int lv = 1; lv < 4; ++lv) {
     const int nblk = 4 - lv;
@@ -285,6 +343,17 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
       *(float4*)(Xs + row * FS + col + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
     __syncthreads();
+    if (lv == 1 && sel_out && tid == 0) {
+      const float* red = (const float*)(smem + S::offRed);
+      const int h = (int)(bh % H);
+      float a = (red[0] + red[1]) + (red[2] + red[3]);
+      float b = (red[4] + red[5]) + (red[6] + red[7]);
+      if (b_s) {
+        a += b_s[2 * h];
+        b += b_s[2 * h + 1];
+      }
+      sel_out[blk] = (a >= b) ? 0 : 1;  // ties go to softmax
+    }
     if (active) {
       // T_ij = -T_ii X_ij
       float acc[8];
@@ -402,7 +471,8 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
 
 cudaError_t launch_gdn_prep_mma(const Problem& p, const void* q, const void* k, const void* v, const float* g,
                                 const float* beta, const float* w_g, const float* b_g, float* G, void* W16,
-                                void* U16, void* P16, void* Qt16, void* Kt16, float* gate, cudaStream_t st) {
+                                void* U16, void* P16, void* Qt16, void* Kt16, float* gate, const float* w_s,
+                                const float* b_s, uint8_t* sel_out, cudaStream_t st) {
   if (p.BH == 0 || p.N == 0) return cudaSuccess;
   auto run = [&](auto kern, int smem) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -410,7 +480,7 @@ cudaError_t launch_gdn_prep_mma(const Problem& p, const void* q, const void* k, 
     kern<<<(unsigned)(p.BH * p.N), 128, smem, st>>>(
         (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, g, beta, p.L, p.N, p.scale,
         G, (__nv_bfloat16*)W16, (__nv_bfloat16*)U16, (__nv_bfloat16*)P16, (__nv_bfloat16*)Qt16,
-        (__nv_bfloat16*)Kt16, w_g, b_g, p.H, gate);
+        (__nv_bfloat16*)Kt16, w_g, b_g, p.H, gate, w_s, b_s, sel_out);
     return cudaGetLastError();
   };
   return p.d == 64 ? run(gdn_prep_mma_kernel<64>, PrepSmem<64>::kBytes)

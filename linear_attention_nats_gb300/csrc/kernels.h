@@ -35,7 +35,8 @@ cudaError_t launch_gdn_scan_simt(const Problem& p, int dtype, const void* q, con
 // bf16 chunk factors of the Gated DeltaNet branch plus the per-token merge gate.
 cudaError_t launch_gdn_prep_mma(const Problem& p, const void* q, const void* k, const void* v, const float* g,
                                 const float* beta, const float* w_g, const float* b_g, float* G, void* W16,
-                                void* U16, void* P16, void* Qt16, void* Kt16, float* gate, cudaStream_t st);
+                                void* U16, void* P16, void* Qt16, void* Kt16, float* gate, const float* w_s,
+                                const float* b_s, uint8_t* sel_out, cudaStream_t st);
 
 // bf16 chunk scan: o_l (fp32 [BH, L, dv]); state_out may be null.
 cudaError_t launch_gdn_scan_tc(const Problem& p, const void* Kt16, const uint8_t* sel, const float* G,
