@@ -77,14 +77,16 @@ struct PrepSmem {
   static constexpr int offB = offG + C * 4;          // fp32 [C] beta
   static constexpr int offBg = offB + C * 4;         // fp32 [C] beta e^G
   static constexpr int offX = offBg + C * 4;         // fp32 [C][FS] scratch of the blocked inverse
-  static constexpr int offRed = offX + C * FS * 4;   // fp32 [2][4] per-warp partial chunk scores
-  static constexpr int kBytes = offRed + 32;
+  static constexpr int offRed = offX + C * FS * 4;   // fp32 [2][8] per-warp partial chunk scores
+  static constexpr int kBytes = offRed + 64;
 };
 
-// One CTA (4 warps) per (b, h, chunk).  Warp w owns rows 16w .. 16w+15 of
-// every 64-row product.
+// One CTA (8 warps) per (b, h, chunk).  Warp w = (wr, wh), wr = w % 4 owns
+// rows 16 wr .. 16 wr + 15 of the 64-row products; wh = w / 4 picks the
+// column half of K K^T / Q K^T, and U (wh = 0) or W (wh = 1) in the last
+// product, so the two run side by side.
 template <int D>
-__global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
+__global__ void __launch_bounds__(256, 2) gdn_prep_mma_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
     const __nv_bfloat16* __restrict__ v, const float* __restrict__ g, const float* __restrict__ beta, int L,
     int N, float scale, float* __restrict__ Gout, __nv_bfloat16* __restrict__ Wout,
@@ -94,6 +96,7 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
     uint8_t* __restrict__ sel_out) {
   using S = PrepSmem<D>;
   constexpr int RS = S::RS, TS = S::TS, FS = S::FS;
+  constexpr int NT = 256;
   extern __shared__ __align__(16) uint8_t smem[];
   __nv_bfloat16* Ks = (__nv_bfloat16*)(smem + S::offK);
   __nv_bfloat16* Qs = (__nv_bfloat16*)(smem + S::offQ);
@@ -104,20 +107,26 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
   float* Gs = (float*)(smem + S::offG);
   float* Bs = (float*)(smem + S::offB);
   float* Bg = (float*)(smem + S::offBg);
+  float* Xs = (float*)(smem + S::offX);
+  float* red = (float*)(smem + S::offRed);
   constexpr int UTS = C + 8;  // bf16 line stride of the staged U^T
   __nv_bfloat16* UTs = (__nv_bfloat16*)(smem + S::offA);  // reuses A and T once T is in Tb
   static_assert(D * UTS * 2 <= 2 * C * S::FS * 4, "U^T staging must fit the A / T scratch");
+  __nv_bfloat16* Wst = (__nv_bfloat16*)(smem + S::offX);  // W staged in the inverse scratch
+  static_assert(C * RS * 2 <= C * S::FS * 4, "W staging must fit the inverse scratch");
 
   const long long blk = blockIdx.x;
   const int c = (int)(blk % N);
   const long long bh = blk / N;
+  const int h = (int)(bh % H);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int wr = warp & 3, wh = warp >> 2;
   const int gq = lane >> 2, cq = lane & 3;  // fragment row / column-pair
   const size_t tok0 = (size_t)bh * L + (size_t)c * C;
 
   // ---- stage K, Q, V (16-byte async copies) and the gates
   constexpr int VPR = D / 8;  // 16-byte vectors per row
-  for (int e = tid; e < C * VPR; e += 128) {
+  for (int e = tid; e < C * VPR; e += NT) {
     const int t = e / VPR, x = e % VPR;
     cp_async16(Ks + t * RS + x * 8, k + (tok0 + t) * D + x * 8);
     cp_async16(Qs + t * RS + x * 8, q + (tok0 + t) * D + x * 8);
@@ -143,12 +152,12 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
   cp_async_wait_all();
   __syncthreads();
 
-  // ---- KK^T and QK^T for rows 16w .. 16w+15, all 64 columns
-  const int m0 = 16 * warp;
+  // ---- KK^T and QK^T for rows 16 wr .. 16 wr + 15, columns 32 wh .. 32 wh + 31
+  const int m0 = 16 * wr;
   {
-    float kk[8][4], qk[8][4];
+    float kk[4][4], qk[4][4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int j = 0; j < 4; ++j)
 #pragma unroll
       for (int x = 0; x < 4; ++x) kk[j][x] = qk[j][x] = 0.f;
     const int arow = m0 + (lane & 7) + 8 * ((lane >> 3) & 1);
@@ -161,30 +170,31 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
       ldsm_x4(smem_addr(Ks + arow * RS + 16 * ks + acol), ka[0], ka[1], ka[2], ka[3]);
       ldsm_x4(smem_addr(Qs + arow * RS + 16 * ks + acol), qa[0], qa[1], qa[2], qa[3]);
 #pragma unroll
-      for (int jp = 0; jp < 4; ++jp) {  // key rows 16jp .. 16jp+15 = two n-tiles
+      for (int jq = 0; jq < 2; ++jq) {  // key rows 16 jp .. 16 jp + 15 = two n-tiles
+        const int jp = 2 * wh + jq;
         uint32_t b0, b1, b2, b3;
         ldsm_x4(smem_addr(Ks + (16 * jp + brow) * RS + 16 * ks + bcol), b0, b1, b2, b3);
-        mma16816(kk[2 * jp], ka[0], ka[1], ka[2], ka[3], b0, b1);
-        mma16816(kk[2 * jp + 1], ka[0], ka[1], ka[2], ka[3], b2, b3);
-        mma16816(qk[2 * jp], qa[0], qa[1], qa[2], qa[3], b0, b1);
-        mma16816(qk[2 * jp + 1], qa[0], qa[1], qa[2], qa[3], b2, b3);
+        mma16816(kk[2 * jq], ka[0], ka[1], ka[2], ka[3], b0, b1);
+        mma16816(kk[2 * jq + 1], ka[0], ka[1], ka[2], ka[3], b2, b3);
+        mma16816(qk[2 * jq], qa[0], qa[1], qa[2], qa[3], b0, b1);
+        mma16816(qk[2 * jq + 1], qa[0], qa[1], qa[2], qa[3], b2, b3);
       }
     }
     // decay, masks; A -> shared fp32, P -> global bf16
     __nv_bfloat16* P = Pout + (size_t)blk * C * C;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int jl = 0; jl < 4; ++jl) {
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int t = m0 + gq + 8 * hh;
-        const int i0 = 8 * j + 2 * cq;
+        const int i0 = 8 * (4 * wh + jl) + 2 * cq;
         float av[2], pv[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int i = i0 + u;
           const float dec = __expf(Gs[t] - Gs[i]);
-          av[u] = (i < t) ? Bs[t] * dec * kk[j][2 * hh + u] : 0.f;
-          pv[u] = (i <= t) ? scale * dec * qk[j][2 * hh + u] : 0.f;
+          av[u] = (i < t) ? Bs[t] * dec * kk[jl][2 * hh + u] : 0.f;
+          pv[u] = (i <= t) ? scale * dec * qk[jl][2 * hh + u] : 0.f;
         }
         As[t * FS + i0] = av[0];
         As[t * FS + i0 + 1] = av[1];
@@ -193,15 +203,14 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
     }
   }
   __syncthreads();
-  // ---- merge gate: two threads per token, D/2 features each
+  // ---- merge gate: four threads per token, D/4 features each
   {
-    const int h = (int)(bh % H);
-    const int t = tid >> 1, hh = tid & 1;
-    const float* wg = w_g + (size_t)h * D + hh * (D / 2);
-    const __nv_bfloat16* qr = Qs + t * RS + hh * (D / 2);
+    const int t = tid >> 2, qq = tid & 3;
+    const float* wg = w_g + (size_t)h * D + qq * (D / 4);
+    const __nv_bfloat16* qr = Qs + t * RS + qq * (D / 4);
     float z = 0.f;
 #pragma unroll
-    for (int x8 = 0; x8 < D / 16; ++x8) {
+    for (int x8 = 0; x8 < D / 32; ++x8) {
       const uint4 qv = *(const uint4*)(qr + 8 * x8);
       const __nv_bfloat162* q2 = (const __nv_bfloat162*)&qv;
 #pragma unroll
@@ -211,14 +220,14 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
       }
     }
     z += __shfl_xor_sync(0xffffffffu, z, 1);
-    if (hh == 0) gate_out[tok0 + t] = 1.f / (1.f + __expf(-(z + (b_g ? b_g[h] : 0.f))));
+    z += __shfl_xor_sync(0xffffffffu, z, 2);
+    if (qq == 0) gate_out[tok0 + t] = 1.f / (1.f + __expf(-(z + (b_g ? b_g[h] : 0.f))));
   }
   // ---- Q~ = diag(scale e^G) Q and K~ = diag(e^{G_C - G}) K -> global (16-byte stores);
   // the same pass sums the columns of Q and K for the chunk score (a thread
   // keeps one 8-column group x = tid % VPR fixed over its rows)
-  float* colsum = (float*)(smem + S::offX);  // [4 warps][VPR][16]: rows 0-15 of the inverse scratch,
-                                             // which the off-diagonal tiles of the inverse never write
-  static_assert(4 * (D / 8) * 16 * 4 <= 16 * S::FS * 4, "column partials must fit rows 0-15 of X");
+  float* colsum = (float*)(smem + S::offTb);  // [8 warps][VPR][16]; Tb is written only after the inverse
+  static_assert(8 * (D / 8) * 16 * 4 <= C * S::TS * 2, "column partials must fit the Tb tile");
   {
     __nv_bfloat16* Qt = Qtout + tok0 * D;
     __nv_bfloat16* Kt = Ktout + tok0 * D;
@@ -226,7 +235,7 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
     float cs[16];
 #pragma unroll
     for (int x = 0; x < 16; ++x) cs[x] = 0.f;
-    for (int e = tid; e < C * VPR; e += 128) {
+    for (int e = tid; e < C * VPR; e += NT) {
       const int t = e / VPR, x = e % VPR;
       const float fq = scale * __expf(Gs[t]);
       const float fk = __expf(GC - Gs[t]);
@@ -252,8 +261,8 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
       *(uint4*)(Kt + t * D + x * 8) = ok;
     }
     if (sel_out) {
-      // 128 / VPR threads share each x; combine them within the warp, then
-      // leave one partial per (warp, x) in shared memory
+      // the 32 / VPR threads of a warp that share x are combined here, the
+      // warps in the score below
 #pragma unroll
       for (int o = VPR; o < 32; o <<= 1)
 #pragma unroll
@@ -269,7 +278,6 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
   //   T_ij = -T_ii sum_{j <= k < i} A_ik T_kj  (i > j, by distance i - j)
   // Meanwhile nothing else touches As / Ts.  Scale factors for the second
   // product: V rows by beta, K rows by beta e^G.
-  float* Xs = (float*)(smem + S::offX);
   if (tid < C) {
     // diagonal tile b, column jj: a 16-long dependency chain in registers
     const int b = tid >> 4, jj = tid & 15, j = 16 * b + jj;
@@ -285,28 +293,24 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
     }
 #pragma unroll
     for (int tt = 0; tt < 16; ++tt) Ts[(16 * b + tt) * FS + j] = x[tt];
-  } else {
+  } else if (tid < 2 * C) {
     const int u = tid - C;
     Bg[u] = Bs[u] * __expf(Gs[u]);
   }
   __syncthreads();
   if (sel_out) {
-    // chunk score: thread tid owns pooled features tid and tid + 128 of [q ; k]
-    const int h = (int)(bh % H);
+    // chunk score: thread tid owns pooled feature tid of [q ; k]
     const float* W = w_s + (size_t)h * 4 * D;
     float s0 = 0.f, s1 = 0.f;
+    const int f = tid;
+    if (f < 2 * D) {
+      const int fk = f < D ? 0 : 1, fd = f - fk * D, x = fd >> 3, col = (fd & 7) + 8 * fk;
+      float m = 0.f;
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int f = tid + 128 * u;
-      if (f < 2 * D) {
-        const int fk = f < D ? 0 : 1, fd = f - fk * D, x = fd >> 3, col = (fd & 7) + 8 * fk;
-        float m = 0.f;
-#pragma unroll
-        for (int w4 = 0; w4 < 4; ++w4) m += colsum[(w4 * VPR + x) * 16 + col];
-        m *= 1.0f / C;
-        s0 = fmaf(W[f], m, s0);
-        s1 = fmaf(W[2 * D + f], m, s1);
-      }
+      for (int w8 = 0; w8 < 8; ++w8) m += colsum[(w8 * VPR + x) * 16 + col];
+      m *= 1.0f / C;
+      s0 = W[f] * m;
+      s1 = W[2 * D + f] * m;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -314,67 +318,57 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
       s1 += __shfl_xor_sync(0xffffffffu, s1, o);
     }
     if (lane == 0) {
-      ((float*)(smem + S::offRed))[warp] = s0;
-      ((float*)(smem + S::offRed))[4 + warp] = s1;
+      red[warp] = s0;
+      red[8 + warp] = s1;
     }
   }
-  // off-diagonal tiles by distance: a thread owns one row and 8 columns of a tile
+  // off-diagonal tiles by distance: a thread owns one row and 4 columns of a tile
   for (int lv = 1; lv < 4; ++lv) {
     const int nblk = 4 - lv;
-    const bool active = tid < nblk * 32;
-    const int b = tid >> 5, r = (tid >> 1) & 15, c8 = (tid & 1) * 8;
+    const bool active = tid < nblk * 64;
+    const int b = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
     const int i = b + lv, j = b;
-    const int row = 16 * i + r, col = 16 * j + c8;
+    const int row = 16 * i + r, col = 16 * j + c4;
     if (active) {
       // X_ij = sum_{j <= k < i} A_ik T_kj
-      float acc[8];
-#pragma unroll
-      for (int x = 0; x < 8; ++x) acc[x] = 0.f;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
       for (int kk = 16 * j; kk < 16 * i; ++kk) {
         const float a = As[row * FS + kk];
         const float4 t0 = *(const float4*)(Ts + kk * FS + col);
-        const float4 t1 = *(const float4*)(Ts + kk * FS + col + 4);
         acc[0] = fmaf(a, t0.x, acc[0]); acc[1] = fmaf(a, t0.y, acc[1]);
         acc[2] = fmaf(a, t0.z, acc[2]); acc[3] = fmaf(a, t0.w, acc[3]);
-        acc[4] = fmaf(a, t1.x, acc[4]); acc[5] = fmaf(a, t1.y, acc[5]);
-        acc[6] = fmaf(a, t1.z, acc[6]); acc[7] = fmaf(a, t1.w, acc[7]);
       }
       *(float4*)(Xs + row * FS + col) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      *(float4*)(Xs + row * FS + col + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
     __syncthreads();
     if (lv == 1 && sel_out && tid == 0) {
-      const float* red = (const float*)(smem + S::offRed);
-      const int h = (int)(bh % H);
-      float a = (red[0] + red[1]) + (red[2] + red[3]);
-      float b = (red[4] + red[5]) + (red[6] + red[7]);
+      float a = 0.f, bb = 0.f;
+#pragma unroll
+      for (int w8 = 0; w8 < 8; ++w8) {
+        a += red[w8];
+        bb += red[8 + w8];
+      }
       if (b_s) {
         a += b_s[2 * h];
-        b += b_s[2 * h + 1];
+        bb += b_s[2 * h + 1];
       }
-      sel_out[blk] = (a >= b) ? 0 : 1;  // ties go to softmax
+      sel_out[blk] = (a >= bb) ? 0 : 1;  // ties go to softmax
     }
     if (active) {
       // T_ij = -T_ii X_ij
-      float acc[8];
-#pragma unroll
-      for (int x = 0; x < 8; ++x) acc[x] = 0.f;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
       for (int kk = 16 * i; kk <= row; ++kk) {
         const float a = Ts[row * FS + kk];
         const float4 t0 = *(const float4*)(Xs + kk * FS + col);
-        const float4 t1 = *(const float4*)(Xs + kk * FS + col + 4);
         acc[0] = fmaf(a, t0.x, acc[0]); acc[1] = fmaf(a, t0.y, acc[1]);
         acc[2] = fmaf(a, t0.z, acc[2]); acc[3] = fmaf(a, t0.w, acc[3]);
-        acc[4] = fmaf(a, t1.x, acc[4]); acc[5] = fmaf(a, t1.y, acc[5]);
-        acc[6] = fmaf(a, t1.z, acc[6]); acc[7] = fmaf(a, t1.w, acc[7]);
       }
       *(float4*)(Ts + row * FS + col) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
-      *(float4*)(Ts + row * FS + col + 4) = make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
     }
     __syncthreads();
   }
   // T -> bf16 (zero above the diagonal), 8 columns per step
-  for (int e = tid; e < C * C / 8; e += 128) {
+  for (int e = tid; e < C * C / 8; e += NT) {
     const int t = e >> 3, j0 = (e & 7) * 8;
     const float4 a0 = *(const float4*)(Ts + t * FS + j0);
     const float4 a1 = *(const float4*)(Ts + t * FS + j0 + 4);
@@ -387,7 +381,7 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
     *(uint4*)(Tb + t * TS + j0) = o;
   }
   // V rows *= beta, K rows *= beta e^G (in place, 8 columns per step)
-  for (int e = tid; e < C * VPR; e += 128) {
+  for (int e = tid; e < C * VPR; e += NT) {
     const int t = e / VPR, x8 = (e % VPR) * 8;
     const float fb = Bs[t], fg = Bg[t];
     uint4 vv = *(uint4*)(Vs + t * RS + x8);
@@ -405,64 +399,61 @@ __global__ void __launch_bounds__(128) gdn_prep_mma_kernel(
     *(uint4*)(Ks + t * RS + x8) = kv;
   }
   __syncthreads();
-  // ---- U = T (beta V), W = T (beta e^G K): rows 16w.., k-steps up to the diagonal
+  // ---- U = T (beta V) on warps wh = 0, W = T (beta e^G K) on warps wh = 1:
+  // rows 16 wr .., k-steps up to the diagonal
   {
     const int arow = m0 + (lane & 7) + 8 * ((lane >> 3) & 1);
     const int acol = 8 * (lane >> 4);
     const int trow = (lane & 7) + 8 * ((lane >> 3) & 1);  // k row within the 16-row step
     const int tcol = 8 * (lane >> 4);                     // n column offset
+    const __nv_bfloat16* Bsrc = wh == 0 ? Vs : Ks;
+    float acc[D / 8][4];
 #pragma unroll
-    for (int which = 0; which < 2; ++which) {
-      const __nv_bfloat16* Bsrc = which == 0 ? Vs : Ks;
-      float acc[D / 8][4];
+    for (int n = 0; n < D / 8; ++n)
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n)
+      for (int x = 0; x < 4; ++x) acc[n][x] = 0.f;
+    for (int ks = 0; ks <= wr; ++ks) {
+      uint32_t a[4];
+      ldsm_x4(smem_addr(Tb + arow * TS + 16 * ks + acol), a[0], a[1], a[2], a[3]);
 #pragma unroll
-        for (int x = 0; x < 4; ++x) acc[n][x] = 0.f;
-      for (int ks = 0; ks <= warp; ++ks) {
-        uint32_t a[4];
-        ldsm_x4(smem_addr(Tb + arow * TS + 16 * ks + acol), a[0], a[1], a[2], a[3]);
-#pragma unroll
-        for (int np = 0; np < D / 16; ++np) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(smem_addr(Bsrc + (16 * ks + trow) * RS + 16 * np + tcol), b0, b1, b2, b3);
-          mma16816(acc[2 * np], a[0], a[1], a[2], a[3], b0, b1);
-          mma16816(acc[2 * np + 1], a[0], a[1], a[2], a[3], b2, b3);
-        }
+      for (int np = 0; np < D / 16; ++np) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(smem_addr(Bsrc + (16 * ks + trow) * RS + 16 * np + tcol), b0, b1, b2, b3);
+        mma16816(acc[2 * np], a[0], a[1], a[2], a[3], b0, b1);
+        mma16816(acc[2 * np + 1], a[0], a[1], a[2], a[3], b2, b3);
       }
-      if (which == 0) {
-        // U^T staged in the (now dead) A / T scratch: line e, column t
+    }
+    if (wh == 0) {
+      // U^T staged in the (now dead) A / T scratch: line e, column t
 #pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-          const int e = 8 * n + 2 * cq;
-          UTs[e * UTS + m0 + gq] = __float2bfloat16_rn(acc[n][0]);
-          UTs[(e + 1) * UTS + m0 + gq] = __float2bfloat16_rn(acc[n][1]);
-          UTs[e * UTS + m0 + gq + 8] = __float2bfloat16_rn(acc[n][2]);
-          UTs[(e + 1) * UTS + m0 + gq + 8] = __float2bfloat16_rn(acc[n][3]);
-        }
-      } else {
-        // W staged in the V tile (dead once every warp finished U)
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-          const int col = 8 * n + 2 * cq;
-          *(uint32_t*)(Vs + (m0 + gq) * RS + col) = pack2(acc[n][0], acc[n][1]);
-          *(uint32_t*)(Vs + (m0 + gq + 8) * RS + col) = pack2(acc[n][2], acc[n][3]);
-        }
+      for (int n = 0; n < D / 8; ++n) {
+        const int e = 8 * n + 2 * cq;
+        UTs[e * UTS + m0 + gq] = __float2bfloat16_rn(acc[n][0]);
+        UTs[(e + 1) * UTS + m0 + gq] = __float2bfloat16_rn(acc[n][1]);
+        UTs[e * UTS + m0 + gq + 8] = __float2bfloat16_rn(acc[n][2]);
+        UTs[(e + 1) * UTS + m0 + gq + 8] = __float2bfloat16_rn(acc[n][3]);
       }
-      if (which == 0) __syncthreads();  // every warp is done reading V
+    } else {
+      // W staged in the (now dead) inverse scratch
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) {
+        const int col = 8 * n + 2 * cq;
+        *(uint32_t*)(Wst + (m0 + gq) * RS + col) = pack2(acc[n][0], acc[n][1]);
+        *(uint32_t*)(Wst + (m0 + gq + 8) * RS + col) = pack2(acc[n][2], acc[n][3]);
+      }
     }
   }
   __syncthreads();
   {
     __nv_bfloat16* Ug = Uout + (size_t)blk * C * D;  // [D][64]
-    for (int e8 = tid; e8 < D * 8; e8 += 128) {
+    for (int e8 = tid; e8 < D * 8; e8 += NT) {
       const int e = e8 >> 3, x = e8 & 7;
       *(uint4*)(Ug + e * C + x * 8) = *(const uint4*)(UTs + e * UTS + x * 8);
     }
     __nv_bfloat16* Wg = Wout + (size_t)blk * C * D;  // [64][D]
-    for (int e = tid; e < C * VPR; e += 128) {
+    for (int e = tid; e < C * VPR; e += NT) {
       const int t = e / VPR, x = e % VPR;
-      *(uint4*)(Wg + t * D + x * 8) = *(const uint4*)(Vs + t * RS + x * 8);
+      *(uint4*)(Wg + t * D + x * 8) = *(const uint4*)(Wst + t * RS + x * 8);
     }
   }
 }
@@ -477,7 +468,7 @@ cudaError_t launch_gdn_prep_mma(const Problem& p, const void* q, const void* k, 
   auto run = [&](auto kern, int smem) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)(p.BH * p.N), 128, smem, st>>>(
+    kern<<<(unsigned)(p.BH * p.N), 256, smem, st>>>(
         (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, g, beta, p.L, p.N, p.scale,
         G, (__nv_bfloat16*)W16, (__nv_bfloat16*)U16, (__nv_bfloat16*)P16, (__nv_bfloat16*)Qt16,
         (__nv_bfloat16*)Kt16, w_g, b_g, p.H, gate, w_s, b_s, sel_out);
