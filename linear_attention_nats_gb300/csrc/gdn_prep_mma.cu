@@ -330,13 +330,17 @@ __global__ void __launch_bounds__(256, 2) gdn_prep_mma_kernel(
     const int i = b + lv, j = b;
     const int row = 16 * i + r, col = 16 * j + c4;
     if (active) {
-      // X_ij = sum_{j <= k < i} A_ik T_kj
+      // X_ij = sum_{j <= k < i} A_ik T_kj, in whole 16-row blocks of k so the
+      // loads of a block are issued together
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int kk = 16 * j; kk < 16 * i; ++kk) {
-        const float a = As[row * FS + kk];
-        const float4 t0 = *(const float4*)(Ts + kk * FS + col);
-        acc[0] = fmaf(a, t0.x, acc[0]); acc[1] = fmaf(a, t0.y, acc[1]);
-        acc[2] = fmaf(a, t0.z, acc[2]); acc[3] = fmaf(a, t0.w, acc[3]);
+      for (int kb = 16 * j; kb < 16 * i; kb += 16) {
+#pragma unroll
+        for (int kk = kb; kk < kb + 16; ++kk) {
+          const float a = As[row * FS + kk];
+          const float4 t0 = *(const float4*)(Ts + kk * FS + col);
+          acc[0] = fmaf(a, t0.x, acc[0]); acc[1] = fmaf(a, t0.y, acc[1]);
+          acc[2] = fmaf(a, t0.z, acc[2]); acc[3] = fmaf(a, t0.w, acc[3]);
+        }
       }
       *(float4*)(Xs + row * FS + col) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     }
@@ -355,9 +359,11 @@ __global__ void __launch_bounds__(256, 2) gdn_prep_mma_kernel(
       sel_out[blk] = (a >= bb) ? 0 : 1;  // ties go to softmax
     }
     if (active) {
-      // T_ij = -T_ii X_ij
+      // T_ij = -T_ii X_ij over the whole 16-row block (T_ii is zero above its
+      // diagonal, so the terms past this row vanish)
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int kk = 16 * i; kk <= row; ++kk) {
+#pragma unroll
+      for (int kk = 16 * i; kk < 16 * i + 16; ++kk) {
         const float a = Ts[row * FS + kk];
         const float4 t0 = *(const float4*)(Xs + kk * FS + col);
         acc[0] = fmaf(a, t0.x, acc[0]); acc[1] = fmaf(a, t0.y, acc[1]);
