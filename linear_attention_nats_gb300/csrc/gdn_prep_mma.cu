@@ -52,6 +52,22 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D(16x8 fp32) += A(16x8 tf32, row) * B(8x8 tf32, col)
+__device__ __forceinline__ void mma1688_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -322,27 +338,61 @@ __global__ void __launch_bounds__(256, 2) gdn_prep_mma_kernel(
       red[8 + warp] = s1;
     }
   }
-  // off-diagonal tiles by distance: a thread owns one row and 4 columns of a tile
+  // off-diagonal tiles by distance, one warp per tile, on tf32 MMAs (fp32
+  // accumulate; T is rounded to bf16 for the U / W products right after, far
+  // coarser than the tf32 operands):
+  //   X_ij = A_{i, j..i-1} T_{j..i-1, j}   then   T_ij = -T_ii X_ij
   for (int lv = 1; lv < 4; ++lv) {
     const int nblk = 4 - lv;
-    const bool active = tid < nblk * 64;
-    const int b = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-    const int i = b + lv, j = b;
-    const int row = 16 * i + r, col = 16 * j + c4;
-    if (active) {
-      // X_ij = sum_{j <= k < i} A_ik T_kj, in whole 16-row blocks of k so the
-      // loads of a block are issued together
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int kb = 16 * j; kb < 16 * i; kb += 16) {
+    if (warp < nblk) {
+      const int i = warp + lv, j = warp;
+      float x[2][4];
 #pragma unroll
-        for (int kk = kb; kk < kb + 16; ++kk) {
-          const float a = As[row * FS + kk];
-          const float4 t0 = *(const float4*)(Ts + kk * FS + col);
-          acc[0] = fmaf(a, t0.x, acc[0]); acc[1] = fmaf(a, t0.y, acc[1]);
-          acc[2] = fmaf(a, t0.z, acc[2]); acc[3] = fmaf(a, t0.w, acc[3]);
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[nt][e] = 0.f;
+      for (int k0 = 16 * j; k0 < 16 * i; k0 += 8) {
+        const float* ar = As + (16 * i + gq) * FS + k0 + cq;
+        const uint32_t a0 = tf32(ar[0]), a1 = tf32(ar[8 * FS]), a2 = tf32(ar[4]), a3 = tf32(ar[8 * FS + 4]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const float* br = Ts + (k0 + cq) * FS + 16 * j + 8 * nt + gq;
+          mma1688_tf32(x[nt], a0, a1, a2, a3, tf32(br[0]), tf32(br[4 * FS]));
         }
       }
-      *(float4*)(Xs + row * FS + col) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      // X_ij -> shared memory (the B operand of the second product)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        float* xr = Xs + (16 * i + gq) * FS + 16 * j + 8 * nt + 2 * cq;
+        xr[0] = x[nt][0];
+        xr[1] = x[nt][1];
+        xr[8 * FS] = x[nt][2];
+        xr[8 * FS + 1] = x[nt][3];
+      }
+      __syncwarp();
+      float y[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) y[nt][e] = 0.f;
+#pragma unroll
+      for (int k0 = 0; k0 < 16; k0 += 8) {
+        const float* ar = Ts + (16 * i + gq) * FS + 16 * i + k0 + cq;
+        const uint32_t a0 = tf32(ar[0]), a1 = tf32(ar[8 * FS]), a2 = tf32(ar[4]), a3 = tf32(ar[8 * FS + 4]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const float* br = Xs + (16 * i + k0 + cq) * FS + 16 * j + 8 * nt + gq;
+          mma1688_tf32(y[nt], a0, a1, a2, a3, tf32(br[0]), tf32(br[4 * FS]));
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        float* tr = Ts + (16 * i + gq) * FS + 16 * j + 8 * nt + 2 * cq;
+        tr[0] = -y[nt][0];
+        tr[1] = -y[nt][1];
+        tr[8 * FS] = -y[nt][2];
+        tr[8 * FS + 1] = -y[nt][3];
+      }
     }
     __syncthreads();
     if (lv == 1 && sel_out && tid == 0) {
@@ -358,20 +408,6 @@ __global__ void __launch_bounds__(256, 2) gdn_prep_mma_kernel(
       }
       sel_out[blk] = (a >= bb) ? 0 : 1;  // ties go to softmax
     }
-    if (active) {
-      // T_ij = -T_ii X_ij over the whole 16-row block (T_ii is zero above its
-      // diagonal, so the terms past this row vanish)
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int kk = 16 * i; kk < 16 * i + 16; ++kk) {
-        const float a = Ts[row * FS + kk];
-        const float4 t0 = *(const float4*)(Xs + kk * FS + col);
-        acc[0] = fmaf(a, t0.x, acc[0]); acc[1] = fmaf(a, t0.y, acc[1]);
-        acc[2] = fmaf(a, t0.z, acc[2]); acc[3] = fmaf(a, t0.w, acc[3]);
-      }
-      *(float4*)(Ts + row * FS + col) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
-    }
-    __syncthreads();
   }
   // T -> bf16 (zero above the diagonal), 8 columns per step
   for (int e = tid; e < C * C / 8; e += NT) {
