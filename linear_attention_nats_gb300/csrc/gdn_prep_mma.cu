@@ -68,6 +68,11 @@ __device__ __forceinline__ uint32_t tf32(float x) {
   return r;
 }
 
+// hardware barrier of `count` threads (whole warps) under barrier id `id`
+__device__ __forceinline__ void named_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -93,7 +98,7 @@ struct PrepSmem {
   static constexpr int offB = offG + C * 4;          // fp32 [C] beta
   static constexpr int offBg = offB + C * 4;         // fp32 [C] beta e^G
   static constexpr int offX = offBg + C * 4;         // fp32 [C][FS] scratch of the blocked inverse
-  static constexpr int offRed = offX + C * FS * 4;   // fp32 [2][8] per-warp partial chunk scores
+  static constexpr int offRed = offX + C * FS * 4;   // fp32 [2][4] per-warp partial chunk scores
   static constexpr int kBytes = offRed + 64;
 };
 
@@ -219,228 +224,218 @@ __global__ void __launch_bounds__(256, 2) gdn_prep_mma_kernel(
     }
   }
   __syncthreads();
-  // ---- merge gate: four threads per token, D/4 features each
-  {
-    const int t = tid >> 2, qq = tid & 3;
-    const float* wg = w_g + (size_t)h * D + qq * (D / 4);
-    const __nv_bfloat16* qr = Qs + t * RS + qq * (D / 4);
-    float z = 0.f;
+  // ---- two warp groups side by side: both depend only on the products
+  // above, and each synchronises on its own named barrier (every thread of a
+  // group reaches every barrier of its group)
+  if (warp >= 4) {
+    // warps 4-7: merge gate, Q~ / K~ with the column sums of Q and K for the
+    // chunk score, then V rows *= beta and K rows *= beta e^G
+    const int t4 = tid - 128;
+    {
+      // merge gate: two threads per token, D/2 features each
+      const int t = t4 >> 1, hh = t4 & 1;
+      const float* wg = w_g + (size_t)h * D + hh * (D / 2);
+      const __nv_bfloat16* qr = Qs + t * RS + hh * (D / 2);
+      float z = 0.f;
 #pragma unroll
-    for (int x8 = 0; x8 < D / 32; ++x8) {
-      const uint4 qv = *(const uint4*)(qr + 8 * x8);
-      const __nv_bfloat162* q2 = (const __nv_bfloat162*)&qv;
+      for (int x8 = 0; x8 < D / 16; ++x8) {
+        const uint4 qv = *(const uint4*)(qr + 8 * x8);
+        const __nv_bfloat162* q2 = (const __nv_bfloat162*)&qv;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(q2[i]);
-        z = fmaf(f.x, wg[8 * x8 + 2 * i], fmaf(f.y, wg[8 * x8 + 2 * i + 1], z));
-      }
-    }
-    z += __shfl_xor_sync(0xffffffffu, z, 1);
-    z += __shfl_xor_sync(0xffffffffu, z, 2);
-    if (qq == 0) gate_out[tok0 + t] = 1.f / (1.f + __expf(-(z + (b_g ? b_g[h] : 0.f))));
-  }
-  // ---- Q~ = diag(scale e^G) Q and K~ = diag(e^{G_C - G}) K -> global (16-byte stores);
-  // the same pass sums the columns of Q and K for the chunk score (a thread
-  // keeps one 8-column group x = tid % VPR fixed over its rows)
-  float* colsum = (float*)(smem + S::offTb);  // [8 warps][VPR][16]; Tb is written only after the inverse
-  static_assert(8 * (D / 8) * 16 * 4 <= C * S::TS * 2, "column partials must fit the Tb tile");
-  {
-    __nv_bfloat16* Qt = Qtout + tok0 * D;
-    __nv_bfloat16* Kt = Ktout + tok0 * D;
-    const float GC = Gs[C - 1];
-    float cs[16];
-#pragma unroll
-    for (int x = 0; x < 16; ++x) cs[x] = 0.f;
-    for (int e = tid; e < C * VPR; e += NT) {
-      const int t = e / VPR, x = e % VPR;
-      const float fq = scale * __expf(Gs[t]);
-      const float fk = __expf(GC - Gs[t]);
-      const uint4 inq = *(const uint4*)(Qs + t * RS + x * 8);
-      const uint4 ink = *(const uint4*)(Ks + t * RS + x * 8);
-      const __nv_bfloat162* hq = (const __nv_bfloat162*)&inq;
-      const __nv_bfloat162* hk = (const __nv_bfloat162*)&ink;
-      uint4 oq, ok;
-      uint32_t* q32 = (uint32_t*)&oq;
-      uint32_t* k32 = (uint32_t*)&ok;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 vq = __bfloat1622float2(hq[i]);
-        const float2 vk = __bfloat1622float2(hk[i]);
-        q32[i] = pack2(vq.x * fq, vq.y * fq);
-        k32[i] = pack2(vk.x * fk, vk.y * fk);
-        cs[2 * i] += vq.x;
-        cs[2 * i + 1] += vq.y;
-        cs[8 + 2 * i] += vk.x;
-        cs[8 + 2 * i + 1] += vk.y;
-      }
-      *(uint4*)(Qt + t * D + x * 8) = oq;
-      *(uint4*)(Kt + t * D + x * 8) = ok;
-    }
-    if (sel_out) {
-      // the 32 / VPR threads of a warp that share x are combined here, the
-      // warps in the score below
-#pragma unroll
-      for (int o = VPR; o < 32; o <<= 1)
-#pragma unroll
-        for (int x = 0; x < 16; ++x) cs[x] += __shfl_xor_sync(0xffffffffu, cs[x], o);
-      if (lane < VPR) {
-#pragma unroll
-        for (int x = 0; x < 16; ++x) colsum[(warp * VPR + lane) * 16 + x] = cs[x];
-      }
-    }
-  }
-  // ---- T = (I + A)^{-1}, unit lower triangular, blocked in 16 x 16 tiles:
-  //   T_bb = (I + A_bb)^{-1}                          (forward substitution)
-  //   T_ij = -T_ii sum_{j <= k < i} A_ik T_kj  (i > j, by distance i - j)
-  // Meanwhile nothing else touches As / Ts.  Scale factors for the second
-  // product: V rows by beta, K rows by beta e^G.
-  if (tid < C) {
-    // diagonal tile b, column jj: a 16-long dependency chain in registers
-    const int b = tid >> 4, jj = tid & 15, j = 16 * b + jj;
-    float x[16];
-#pragma unroll
-    for (int tt = 0; tt < 16; ++tt) {
-      const int t = 16 * b + tt;
-      float acc = (tt == jj) ? 1.f : 0.f;
-#pragma unroll
-      for (int ii = 0; ii < tt; ++ii)
-        if (ii >= jj) acc = fmaf(-As[t * FS + 16 * b + ii], x[ii], acc);
-      x[tt] = (tt >= jj) ? acc : 0.f;
-    }
-#pragma unroll
-    for (int tt = 0; tt < 16; ++tt) Ts[(16 * b + tt) * FS + j] = x[tt];
-  } else if (tid < 2 * C) {
-    const int u = tid - C;
-    Bg[u] = Bs[u] * __expf(Gs[u]);
-  }
-  __syncthreads();
-  if (sel_out) {
-    // chunk score: thread tid owns pooled feature tid of [q ; k]
-    const float* W = w_s + (size_t)h * 4 * D;
-    float s0 = 0.f, s1 = 0.f;
-    const int f = tid;
-    if (f < 2 * D) {
-      const int fk = f < D ? 0 : 1, fd = f - fk * D, x = fd >> 3, col = (fd & 7) + 8 * fk;
-      float m = 0.f;
-#pragma unroll
-      for (int w8 = 0; w8 < 8; ++w8) m += colsum[(w8 * VPR + x) * 16 + col];
-      m *= 1.0f / C;
-      s0 = W[f] * m;
-      s1 = W[2 * D + f] * m;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      s0 += __shfl_xor_sync(0xffffffffu, s0, o);
-      s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-    }
-    if (lane == 0) {
-      red[warp] = s0;
-      red[8 + warp] = s1;
-    }
-  }
-  // off-diagonal tiles by distance, one warp per tile, on tf32 MMAs (fp32
-  // accumulate; T is rounded to bf16 for the U / W products right after, far
-  // coarser than the tf32 operands):
-  //   X_ij = A_{i, j..i-1} T_{j..i-1, j}   then   T_ij = -T_ii X_ij
-  for (int lv = 1; lv < 4; ++lv) {
-    const int nblk = 4 - lv;
-    if (warp < nblk) {
-      const int i = warp + lv, j = warp;
-      float x[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) x[nt][e] = 0.f;
-      for (int k0 = 16 * j; k0 < 16 * i; k0 += 8) {
-        const float* ar = As + (16 * i + gq) * FS + k0 + cq;
-        const uint32_t a0 = tf32(ar[0]), a1 = tf32(ar[8 * FS]), a2 = tf32(ar[4]), a3 = tf32(ar[8 * FS + 4]);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const float* br = Ts + (k0 + cq) * FS + 16 * j + 8 * nt + gq;
-          mma1688_tf32(x[nt], a0, a1, a2, a3, tf32(br[0]), tf32(br[4 * FS]));
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(q2[i]);
+          z = fmaf(f.x, wg[8 * x8 + 2 * i], fmaf(f.y, wg[8 * x8 + 2 * i + 1], z));
         }
       }
-      // X_ij -> shared memory (the B operand of the second product)
+      z += __shfl_xor_sync(0xffffffffu, z, 1);
+      if (hh == 0) gate_out[tok0 + t] = 1.f / (1.f + __expf(-(z + (b_g ? b_g[h] : 0.f))));
+    }
+    {
+      // Q~ = diag(scale e^G) Q and K~ = diag(e^{G_C - G}) K -> global (16-byte
+      // stores); a thread keeps one 8-column group x = t4 % VPR over its rows
+      __nv_bfloat16* Qt = Qtout + tok0 * D;
+      __nv_bfloat16* Kt = Ktout + tok0 * D;
+      const float GC = Gs[C - 1];
+      float cs[16];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        float* xr = Xs + (16 * i + gq) * FS + 16 * j + 8 * nt + 2 * cq;
-        xr[0] = x[nt][0];
-        xr[1] = x[nt][1];
-        xr[8 * FS] = x[nt][2];
-        xr[8 * FS + 1] = x[nt][3];
+      for (int x = 0; x < 16; ++x) cs[x] = 0.f;
+      for (int e = t4; e < C * VPR; e += 128) {
+        const int t = e / VPR, x = e % VPR;
+        const float fq = scale * __expf(Gs[t]);
+        const float fk = __expf(GC - Gs[t]);
+        const uint4 inq = *(const uint4*)(Qs + t * RS + x * 8);
+        const uint4 ink = *(const uint4*)(Ks + t * RS + x * 8);
+        const __nv_bfloat162* hq = (const __nv_bfloat162*)&inq;
+        const __nv_bfloat162* hk = (const __nv_bfloat162*)&ink;
+        uint4 oq, ok;
+        uint32_t* q32 = (uint32_t*)&oq;
+        uint32_t* k32 = (uint32_t*)&ok;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 vq = __bfloat1622float2(hq[i]);
+          const float2 vk = __bfloat1622float2(hk[i]);
+          q32[i] = pack2(vq.x * fq, vq.y * fq);
+          k32[i] = pack2(vk.x * fk, vk.y * fk);
+          cs[2 * i] += vq.x;
+          cs[2 * i + 1] += vq.y;
+          cs[8 + 2 * i] += vk.x;
+          cs[8 + 2 * i + 1] += vk.y;
+        }
+        *(uint4*)(Qt + t * D + x * 8) = oq;
+        *(uint4*)(Kt + t * D + x * 8) = ok;
       }
-      __syncwarp();
-      float y[2][4];
+      if (sel_out) {
+        // chunk score, linear in the column sums: combine the threads of the
+        // warp that share x, dot each group with the score weights, reduce
+        // over the warp; the four warps' partials are added after the join
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+        for (int o = VPR; o < 32; o <<= 1)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) y[nt][e] = 0.f;
+          for (int x = 0; x < 16; ++x) cs[x] += __shfl_xor_sync(0xffffffffu, cs[x], o);
+        float s0 = 0.f, s1 = 0.f;
+        if (lane < VPR) {
+          const float* W = w_s + (size_t)h * 4 * D + 8 * lane;
 #pragma unroll
-      for (int k0 = 0; k0 < 16; k0 += 8) {
-        const float* ar = Ts + (16 * i + gq) * FS + 16 * i + k0 + cq;
-        const uint32_t a0 = tf32(ar[0]), a1 = tf32(ar[8 * FS]), a2 = tf32(ar[4]), a3 = tf32(ar[8 * FS + 4]);
+          for (int cc = 0; cc < 8; ++cc) {
+            s0 = fmaf(W[cc], cs[cc], fmaf(W[D + cc], cs[8 + cc], s0));
+            s1 = fmaf(W[2 * D + cc], cs[cc], fmaf(W[3 * D + cc], cs[8 + cc], s1));
+          }
+        }
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const float* br = Xs + (16 * i + k0 + cq) * FS + 16 * j + 8 * nt + gq;
-          mma1688_tf32(y[nt], a0, a1, a2, a3, tf32(br[0]), tf32(br[4 * FS]));
+        for (int o = 16; o > 0; o >>= 1) {
+          s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+          s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        }
+        if (lane == 0) {
+          red[warp - 4] = s0;
+          red[warp] = s1;  // 4 + (warp - 4)
         }
       }
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        float* tr = Ts + (16 * i + gq) * FS + 16 * j + 8 * nt + 2 * cq;
-        tr[0] = -y[nt][0];
-        tr[1] = -y[nt][1];
-        tr[8 * FS] = -y[nt][2];
-        tr[8 * FS + 1] = -y[nt][3];
-      }
     }
-    __syncthreads();
-    if (lv == 1 && sel_out && tid == 0) {
-      float a = 0.f, bb = 0.f;
+    if (t4 < C) Bg[t4] = Bs[t4] * __expf(Gs[t4]);
+    named_barrier(2, 128);
+    // V rows *= beta, K rows *= beta e^G (in place, 8 columns per step; K~ is out)
+    for (int e = t4; e < C * VPR; e += 128) {
+      const int t = e / VPR, x8 = (e % VPR) * 8;
+      const float fb = Bs[t], fg = Bg[t];
+      uint4 vv = *(uint4*)(Vs + t * RS + x8);
+      uint4 kv = *(uint4*)(Ks + t * RS + x8);
+      __nv_bfloat162* v2 = (__nv_bfloat162*)&vv;
+      __nv_bfloat162* k2 = (__nv_bfloat162*)&kv;
 #pragma unroll
-      for (int w8 = 0; w8 < 8; ++w8) {
-        a += red[w8];
-        bb += red[8 + w8];
+      for (int x = 0; x < 4; ++x) {
+        const float2 a2 = __bfloat1622float2(v2[x]);
+        const float2 c2 = __bfloat1622float2(k2[x]);
+        v2[x] = __floats2bfloat162_rn(a2.x * fb, a2.y * fb);
+        k2[x] = __floats2bfloat162_rn(c2.x * fg, c2.y * fg);
       }
-      if (b_s) {
-        a += b_s[2 * h];
-        bb += b_s[2 * h + 1];
+      *(uint4*)(Vs + t * RS + x8) = vv;
+      *(uint4*)(Ks + t * RS + x8) = kv;
+    }
+  } else {
+    // warps 0-3: T = (I + A)^{-1}, unit lower triangular, blocked in 16 x 16 tiles:
+    //   T_bb = (I + A_bb)^{-1}                          (forward substitution, fp32)
+    //   T_ij = -T_ii sum_{j <= k < i} A_ik T_kj  (i > j, by distance i - j)
+    if (tid < C) {
+      // diagonal tile b, column jj: a 16-long dependency chain in registers
+      const int b = tid >> 4, jj = tid & 15, j = 16 * b + jj;
+      float x[16];
+#pragma unroll
+      for (int tt = 0; tt < 16; ++tt) {
+        const int t = 16 * b + tt;
+        float acc = (tt == jj) ? 1.f : 0.f;
+#pragma unroll
+        for (int ii = 0; ii < tt; ++ii)
+          if (ii >= jj) acc = fmaf(-As[t * FS + 16 * b + ii], x[ii], acc);
+        x[tt] = (tt >= jj) ? acc : 0.f;
       }
-      sel_out[blk] = (a >= bb) ? 0 : 1;  // ties go to softmax
-    }
-  }
-  // T -> bf16 (zero above the diagonal), 8 columns per step
-  for (int e = tid; e < C * C / 8; e += NT) {
-    const int t = e >> 3, j0 = (e & 7) * 8;
-    const float4 a0 = *(const float4*)(Ts + t * FS + j0);
-    const float4 a1 = *(const float4*)(Ts + t * FS + j0 + 4);
-    const float v8[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-    uint4 o;
-    uint32_t* o32 = (uint32_t*)&o;
 #pragma unroll
-    for (int x = 0; x < 4; ++x)
-      o32[x] = pack2(j0 + 2 * x <= t ? v8[2 * x] : 0.f, j0 + 2 * x + 1 <= t ? v8[2 * x + 1] : 0.f);
-    *(uint4*)(Tb + t * TS + j0) = o;
-  }
-  // V rows *= beta, K rows *= beta e^G (in place, 8 columns per step)
-  for (int e = tid; e < C * VPR; e += NT) {
-    const int t = e / VPR, x8 = (e % VPR) * 8;
-    const float fb = Bs[t], fg = Bg[t];
-    uint4 vv = *(uint4*)(Vs + t * RS + x8);
-    uint4 kv = *(uint4*)(Ks + t * RS + x8);
-    __nv_bfloat162* v2 = (__nv_bfloat162*)&vv;
-    __nv_bfloat162* k2 = (__nv_bfloat162*)&kv;
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const float2 a = __bfloat1622float2(v2[x]);
-      const float2 c2 = __bfloat1622float2(k2[x]);
-      v2[x] = __floats2bfloat162_rn(a.x * fb, a.y * fb);
-      k2[x] = __floats2bfloat162_rn(c2.x * fg, c2.y * fg);
+      for (int tt = 0; tt < 16; ++tt) Ts[(16 * b + tt) * FS + j] = x[tt];
     }
-    *(uint4*)(Vs + t * RS + x8) = vv;
-    *(uint4*)(Ks + t * RS + x8) = kv;
+    named_barrier(1, 128);
+    // off-diagonal tiles by distance, one warp per tile, on tf32 MMAs (fp32
+    // accumulate; T is rounded to bf16 for the U / W products right after,
+    // far coarser than the tf32 operands):
+    //   X_ij = A_{i, j..i-1} T_{j..i-1, j}   then   T_ij = -T_ii X_ij
+    for (int lv = 1; lv < 4; ++lv) {
+      const int nblk = 4 - lv;
+      if (warp < nblk) {
+        const int i = warp + lv, j = warp;
+        float x[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[nt][e] = 0.f;
+        for (int k0 = 16 * j; k0 < 16 * i; k0 += 8) {
+          const float* ar = As + (16 * i + gq) * FS + k0 + cq;
+          const uint32_t a0 = tf32(ar[0]), a1 = tf32(ar[8 * FS]), a2 = tf32(ar[4]), a3 = tf32(ar[8 * FS + 4]);
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            const float* br = Ts + (k0 + cq) * FS + 16 * j + 8 * nt + gq;
+            mma1688_tf32(x[nt], a0, a1, a2, a3, tf32(br[0]), tf32(br[4 * FS]));
+          }
+        }
+        // X_ij -> shared memory (the B operand of the second product)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          float* xr = Xs + (16 * i + gq) * FS + 16 * j + 8 * nt + 2 * cq;
+          xr[0] = x[nt][0];
+          xr[1] = x[nt][1];
+          xr[8 * FS] = x[nt][2];
+          xr[8 * FS + 1] = x[nt][3];
+        }
+        __syncwarp();
+        float y[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) y[nt][e] = 0.f;
+#pragma unroll
+        for (int k0 = 0; k0 < 16; k0 += 8) {
+          const float* ar = Ts + (16 * i + gq) * FS + 16 * i + k0 + cq;
+          const uint32_t a0 = tf32(ar[0]), a1 = tf32(ar[8 * FS]), a2 = tf32(ar[4]), a3 = tf32(ar[8 * FS + 4]);
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            const float* br = Xs + (16 * i + k0 + cq) * FS + 16 * j + 8 * nt + gq;
+            mma1688_tf32(y[nt], a0, a1, a2, a3, tf32(br[0]), tf32(br[4 * FS]));
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          float* tr = Ts + (16 * i + gq) * FS + 16 * j + 8 * nt + 2 * cq;
+          tr[0] = -y[nt][0];
+          tr[1] = -y[nt][1];
+          tr[8 * FS] = -y[nt][2];
+          tr[8 * FS + 1] = -y[nt][3];
+        }
+      }
+      named_barrier(1, 128);
+    }
+    // T -> bf16 (zero above the diagonal), 8 columns per step
+    for (int e = tid; e < C * C / 8; e += 128) {
+      const int t = e >> 3, j0 = (e & 7) * 8;
+      const float4 a0 = *(const float4*)(Ts + t * FS + j0);
+      const float4 a1 = *(const float4*)(Ts + t * FS + j0 + 4);
+      const float v8[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      uint4 o;
+      uint32_t* o32 = (uint32_t*)&o;
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+        o32[x] = pack2(j0 + 2 * x <= t ? v8[2 * x] : 0.f, j0 + 2 * x + 1 <= t ? v8[2 * x + 1] : 0.f);
+      *(uint4*)(Tb + t * TS + j0) = o;
+    }
   }
   __syncthreads();
+  if (sel_out && tid == 0) {
+    // chunk score = (1/C) w_s . (column sums of [Q ; K]) + b_s; ties to softmax
+    float a = ((red[0] + red[1]) + (red[2] + red[3])) * (1.0f / C);
+    float bb = ((red[4] + red[5]) + (red[6] + red[7])) * (1.0f / C);
+    if (b_s) {
+      a += b_s[2 * h];
+      bb += b_s[2 * h + 1];
+    }
+    sel_out[blk] = (a >= bb) ? 0 : 1;
+  }
   // ---- U = T (beta V) on warps wh = 0, W = T (beta e^G K) on warps wh = 1:
   // rows 16 wr .., k-steps up to the diagonal
   {
