@@ -233,7 +233,10 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
     // 5. softmax branch, concurrently on the side stream (in order on the
     //    caller's stream if that stream could not be made); its epilogue
     //    writes out = w RMSNorm(o_s)
-    float* o_l = o_lin_out ? o_lin_out : ws.o_l;
+    // o_l goes to the caller's fp32 buffer if asked for, else as bf16 into the
+    // workspace (the merge reads half the bytes)
+    float* o_l = o_lin_out;
+    void* o_l16 = o_lin_out ? nullptr : (void*)ws.o_l;
     Side* sd = side_of_current_device();
     {
       std::unique_lock<std::mutex> lk;
@@ -245,7 +248,8 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
         ss = sd->s;
       }
       NATS_STAGE(stg, NATS_STAGE_GDN_SCAN, 1,
-                 launch_gdn_scan_tc(p, ws.Kt, sel, ws.G, ws.W, ws.U, ws.P, ws.Qt, o_l, state_out, ws.err, st));
+                 launch_gdn_scan_tc(p, ws.Kt, sel, ws.G, ws.W, ws.U, ws.P, ws.Qt, o_l, o_l16, state_out, ws.err,
+                                    st));
       Stages stg_side{prof, ss};
       NATS_STAGE(stg_side, NATS_STAGE_SOFTMAX, 1,
                  launch_softmax_tc(p, q, k, v, ws.nprev, ws.sel_idx, sel, ws.gate, norm_w_soft, out, o_soft_out,
@@ -254,7 +258,7 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
         return NATS_ERR_CUDA;
     }
     // 6. out += (1 - w) RMSNorm(o_l)
-    NATS_STAGE(stg, NATS_STAGE_MERGE, 1, launch_merge_lin(p, o_l, ws.gate, norm_w_lin, out, st));
+    NATS_STAGE(stg, NATS_STAGE_MERGE, 1, launch_merge_lin(p, o_l, o_l16, ws.gate, norm_w_lin, out, st));
   } else {
     // fp32 inputs: softmax branch, Gated DeltaNet branch, then RMSNorm + merge
     float* o_s = o_soft_out ? o_soft_out : ws.o_s;

@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(320, 1)
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_u,
                        const __grid_constant__ CUtensorMap tm_p, const uint8_t* __restrict__ sel,
                        const float* __restrict__ G, int L, int N, float* __restrict__ o_l,
+                       __nv_bfloat16* __restrict__ o_l16,
                        float* __restrict__ state_out, int* __restrict__ err) {
   using S = ScanSmem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -233,9 +234,14 @@ __global__ void __launch_bounds__(320, 1)
       tc::tmem_ld32(tmem + kColO + (cc % 3) * 64 + lane_off + 32 * hf, o);
       tc::tmem_ld_wait();
       if (has_row) {
-        float* dst = o_l + (bh * (long long)L + 64LL * cc + 32 * hf) * D + r;
+        const size_t off = (bh * (long long)L + 64LL * cc + 32 * hf) * D + r;
+        if (o_l16) {  // bf16 copy for the merge (the caller did not ask for o_l)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) dst[(size_t)i * D] = o[i];
+          for (int i = 0; i < 32; ++i) o_l16[off + (size_t)i * D] = __float2bfloat16_rn(o[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o_l[off + (size_t)i * D] = o[i];
+        }
       }
       tc::fence_before();
       tc::mbar_arrive(&bars[SB_OFREE + (cc % 3)]);
@@ -354,7 +360,8 @@ __global__ void __launch_bounds__(320, 1)
 template <int D>
 static cudaError_t launch_scan_tc_t(const Problem& p, const void* Kt16, const uint8_t* sel, const float* G,
                                     const void* W16, const void* UT16, const void* P16, const void* Qt16,
-                                    float* o_l, float* state_out, int* err, cudaStream_t st) {
+                                    float* o_l, __nv_bfloat16* o_l16, float* state_out, int* err,
+                                    cudaStream_t st) {
   CUtensorMap mw, mq, mk, mu, mp;
   const long long rows = p.BH * p.L;  // = BH * N * 64
   if (!make_tile_map(&mw, W16, rows, D) || !make_tile_map(&mq, Qt16, rows, D) || !make_tile_map(&mk, Kt16, rows, D) ||
@@ -364,16 +371,17 @@ static cudaError_t launch_scan_tc_t(const Problem& p, const void* Kt16, const ui
   const int smem = ScanSmem<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)p.BH, 320, smem, st>>>(mw, mq, mk, mu, mp, sel, G, p.L, p.N, o_l, state_out, err);
+  kern<<<(unsigned)p.BH, 320, smem, st>>>(mw, mq, mk, mu, mp, sel, G, p.L, p.N, o_l, o_l16, state_out, err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gdn_scan_tc(const Problem& p, const void* Kt16, const uint8_t* sel, const float* G,
                                const void* W16, const void* UT16, const void* P16, const void* Qt16, float* o_l,
-                               float* state_out, int* err, cudaStream_t st) {
+                               void* o_l16, float* state_out, int* err, cudaStream_t st) {
   if (p.BH == 0 || p.N == 0) return cudaSuccess;
-  return p.d == 64 ? launch_scan_tc_t<64>(p, Kt16, sel, G, W16, UT16, P16, Qt16, o_l, state_out, err, st)
-                   : launch_scan_tc_t<128>(p, Kt16, sel, G, W16, UT16, P16, Qt16, o_l, state_out, err, st);
+  __nv_bfloat16* ol16 = (__nv_bfloat16*)o_l16;
+  return p.d == 64 ? launch_scan_tc_t<64>(p, Kt16, sel, G, W16, UT16, P16, Qt16, o_l, ol16, state_out, err, st)
+                   : launch_scan_tc_t<128>(p, Kt16, sel, G, W16, UT16, P16, Qt16, o_l, ol16, state_out, err, st);
 }
 
 }  // namespace nats

@@ -41,11 +41,11 @@ cudaError_t launch_gdn_prep_mma(const Problem& p, const void* q, const void* k, 
 // bf16 chunk scan: o_l (fp32 [BH, L, dv]); state_out may be null.
 cudaError_t launch_gdn_scan_tc(const Problem& p, const void* Kt16, const uint8_t* sel, const float* G,
                                const void* W16, const void* UT16, const void* P16, const void* Qt16, float* o_l,
-                               float* state_out, int* err, cudaStream_t st);
+                               void* o_l16, float* state_out, int* err, cudaStream_t st);
 
 // bf16 path: out (holding w RMSNorm(o_s)) += (1 - w) RMSNorm(o_l).
-cudaError_t launch_merge_lin(const Problem& p, const float* o_l, const float* gate, const float* nw_l, void* out,
-                             cudaStream_t st);
+cudaError_t launch_merge_lin(const Problem& p, const float* o_l, const void* o_l16, const float* gate,
+                             const float* nw_l, void* out, cudaStream_t st);
 
 cudaError_t launch_norm_merge(const Problem& p, int dtype, const float* o_s, const float* o_l,
                               const void* q, const float* w_g, const float* b_g, const float* nw_s,

@@ -50,9 +50,10 @@ __global__ void __launch_bounds__(256) norm_merge_kernel(
 
 // bf16 path, second half of the merge: out already holds w RMSNorm(o_s)
 // (written by the softmax kernel's epilogue); add (1 - w) RMSNorm(o_l).  One
-// warp per token row, coalesced; HBM-bound.
-template <int D>
-__global__ void __launch_bounds__(256) merge_lin_kernel(const float* __restrict__ o_l,
+// warp per token row, coalesced; HBM-bound.  o_l is fp32, or the bf16 copy the
+// scan writes when the caller does not ask for o_l (half the bytes to read).
+template <int D, class TL>
+__global__ void __launch_bounds__(256) merge_lin_kernel(const TL* __restrict__ o_l,
                                                         const float* __restrict__ gate,
                                                         const float* __restrict__ nw_l, long long rows,
                                                         float eps, __nv_bfloat16* __restrict__ out) {
@@ -64,7 +65,7 @@ __global__ void __launch_bounds__(256) merge_lin_kernel(const float* __restrict_
   float xl[NC], sl = 0.f;
 #pragma unroll
   for (int i = 0; i < NC; ++i) {
-    xl[i] = o_l[base + lane + 32 * i];
+    xl[i] = to_f32(o_l[base + lane + 32 * i]);
     sl = fmaf(xl[i], xl[i], sl);
   }
   sl = warp_sum(sl);
@@ -99,15 +100,19 @@ cudaError_t launch_norm_merge(const Problem& p, int dtype, const float* o_s, con
                    : launch_t<float, 128>(p, o_s, o_l, q, w_g, b_g, nw_s, nw_l, out, st);
 }
 
-cudaError_t launch_merge_lin(const Problem& p, const float* o_l, const float* gate, const float* nw_l, void* out,
-                             cudaStream_t st) {
+cudaError_t launch_merge_lin(const Problem& p, const float* o_l, const void* o_l16, const float* gate,
+                             const float* nw_l, void* out, cudaStream_t st) {
   const long long rows = p.BH * p.L;
   if (rows == 0) return cudaSuccess;
   const unsigned blocks = (unsigned)((rows + 7) / 8);
-  if (p.d == 64)
-    merge_lin_kernel<64><<<blocks, 256, 0, st>>>(o_l, gate, nw_l, rows, p.eps, (__nv_bfloat16*)out);
+  __nv_bfloat16* o = (__nv_bfloat16*)out;
+  const __nv_bfloat16* l16 = (const __nv_bfloat16*)o_l16;
+  if (l16)
+    p.d == 64 ? merge_lin_kernel<64><<<blocks, 256, 0, st>>>(l16, gate, nw_l, rows, p.eps, o)
+              : merge_lin_kernel<128><<<blocks, 256, 0, st>>>(l16, gate, nw_l, rows, p.eps, o);
   else
-    merge_lin_kernel<128><<<blocks, 256, 0, st>>>(o_l, gate, nw_l, rows, p.eps, (__nv_bfloat16*)out);
+    p.d == 64 ? merge_lin_kernel<64><<<blocks, 256, 0, st>>>(o_l, gate, nw_l, rows, p.eps, o)
+              : merge_lin_kernel<128><<<blocks, 256, 0, st>>>(o_l, gate, nw_l, rows, p.eps, o);
   return cudaGetLastError();
 }
 

@@ -161,3 +161,30 @@ def test_full_size_sampled(name):
     ref = oracle.forward_inputs(inp, heads=heads, rows=rows)
     sub = {k: _flat(v, inp)[heads] for k, v in got.items()}
     _compare(inp, sub, ref, rows=rows, tag=name)
+
+
+@pytest.mark.parametrize("name", ["small", "l8192"])
+def test_out_without_branch_outputs(name):
+    """The call as the bench makes it: no branch outputs requested, so the
+    Gated DeltaNet output stays in the workspace (bf16) until the merge."""
+    import linear_attention_nats_gb300 as nats
+
+    inp = gen.config_inputs(name)
+    t = to_device(inp)
+    r = nats.hybrid_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_s"], t["b_s"], t["w_g"], t["b_g"],
+                        return_sel=True, check_errors=True)
+    torch.cuda.synchronize()
+    out = _flat(r["out"].float().cpu().numpy(), inp)
+    ref_sel, _ = oracle.select_inputs(inp)
+    assert np.array_equal(r["sel"].cpu().numpy(), ref_sel)
+    if name == "small":
+        ref = oracle.forward_inputs(inp, outputs=("out",))
+        err = rel_err(out, ref["out"])
+    else:
+        rng = np.random.default_rng(23)
+        heads = sorted(rng.choice(inp.B * inp.H, size=2, replace=False).tolist())
+        rows = _sample_rows(inp.L, 96, 7)
+        ref = oracle.forward_inputs(inp, heads=heads, rows=rows, outputs=("out",))
+        err = rel_err(out[heads][:, rows], ref["out"][:, rows])
+    print(f"[parity] {name} out only: out={err:.2e}")
+    assert err <= TOL[inp.dtype]
