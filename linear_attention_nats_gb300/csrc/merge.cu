@@ -57,24 +57,38 @@ __global__ void __launch_bounds__(256) merge_lin_kernel(const TL* __restrict__ o
                                                         const float* __restrict__ gate,
                                                         const float* __restrict__ nw_l, long long rows,
                                                         float eps, __nv_bfloat16* __restrict__ out) {
-  constexpr int NC = D / 32;
+  constexpr int E = D / 32;  // contiguous elements per lane (vector loads / stores)
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= rows) return;
   const int lane = threadIdx.x & 31;
-  const size_t base = (size_t)row * D;
-  float xl[NC], sl = 0.f;
+  const size_t base = (size_t)row * D + E * lane;
+  float xl[E], sl = 0.f;
+  if constexpr (sizeof(TL) == 2) {
+    // bf16: E = 4 -> one 8-byte load, E = 2 -> one 4-byte load
+    if constexpr (E == 4) {
+      const uint2 u = *(const uint2*)(o_l + base);
+      const float2 a = __bfloat1622float2(*(const __nv_bfloat162*)&u.x);
+      const float2 b = __bfloat1622float2(*(const __nv_bfloat162*)&u.y);
+      xl[0] = a.x; xl[1] = a.y; xl[2] = b.x; xl[3] = b.y;
+    } else {
+      const float2 a = __bfloat1622float2(*(const __nv_bfloat162*)(o_l + base));
+      xl[0] = a.x; xl[1] = a.y;
+    }
+  } else {
 #pragma unroll
-  for (int i = 0; i < NC; ++i) {
-    xl[i] = to_f32(o_l[base + lane + 32 * i]);
-    sl = fmaf(xl[i], xl[i], sl);
+    for (int i = 0; i < E; ++i) xl[i] = to_f32(o_l[base + i]);
   }
+#pragma unroll
+  for (int i = 0; i < E; ++i) sl = fmaf(xl[i], xl[i], sl);
   sl = warp_sum(sl);
   const float f = (1.f - gate[row]) * rsqrtf(sl * (1.f / D) + eps);
+  __nv_bfloat162* o2 = (__nv_bfloat162*)(out + base);
 #pragma unroll
-  for (int i = 0; i < NC; ++i) {
-    const int col = lane + 32 * i;
-    const float nl = f * xl[i] * (nw_l ? nw_l[col] : 1.f);
-    out[base + col] = __float2bfloat16_rn(__bfloat162float(out[base + col]) + nl);
+  for (int i = 0; i < E / 2; ++i) {
+    const float2 prev = __bfloat1622float2(o2[i]);
+    const int col = E * lane + 2 * i;
+    const float w0 = nw_l ? nw_l[col] : 1.f, w1 = nw_l ? nw_l[col + 1] : 1.f;
+    o2[i] = __floats2bfloat162_rn(prev.x + f * xl[2 * i] * w0, prev.y + f * xl[2 * i + 1] * w1);
   }
 }
 
