@@ -53,7 +53,8 @@ namespace {
 
 enum { kFull = 0, kCausal = 1, kNone = 2 };
 constexpr float kRescaleLog2 = 8.f;  // lazy-rescale threshold (log2 units)
-constexpr int KS = 3;                // K/V ring depth
+constexpr int KS = 3;                // K ring depth
+constexpr int VS = 2;                // V ring depth (the V producer runs far ahead of P V)
 constexpr int NS = 3;                // S/P buffers in TMEM
 constexpr int kTileTakers = 6;       // arrivals that free a tile-queue slot: MMA, V producer, 4 softmax warps
 
@@ -65,8 +66,9 @@ struct SoftmaxSmem {
   static constexpr int offQ = 0;
   static constexpr int offK = offQ + kQ;
   static constexpr int offV = offK + KS * kKV;
-  static constexpr int offBar = offV + KS * kKV;
-  static constexpr int kNumBars = 2 + 4 * KS + 3 * NS + 1 + 4;
+  static constexpr int offOst = offV + VS * kKV;  // bf16 output tile of the epilogue (TMA store source)
+  static constexpr int offBar = offOst + kQ;
+  static constexpr int kNumBars = 2 + 2 * KS + 2 * VS + 3 * NS + 1 + 4 + 2;
   static constexpr int offTmem = offBar + kNumBars * 8;
   static constexpr int offNw = offTmem + 16;  // RMSNorm weights of the softmax branch, D floats
   static constexpr int offTq = offNw + D * 4;  // two-slot tile queue (ints)
@@ -75,8 +77,9 @@ struct SoftmaxSmem {
 
 // barrier slots
 enum {
-  B_QF = 0, B_QE = 1, B_KF = 2, B_KE = B_KF + KS, B_VF = B_KE + KS, B_VE = B_VF + KS,
-  B_SF = B_VE + KS, B_PF = B_SF + NS, B_PV = B_PF + NS, B_OF = B_PV + NS, B_TF = B_OF + 1, B_TE = B_TF + 2
+  B_QF = 0, B_QE = 1, B_KF = 2, B_KE = B_KF + KS, B_VF = B_KE + KS, B_VE = B_VF + VS,
+  B_SF = B_VE + VS, B_PF = B_SF + NS, B_PV = B_PF + NS, B_OF = B_PV + NS, B_TF = B_OF + 1, B_TE = B_TF + 2,
+  B_OSF = B_TE + 2, B_OSE = B_OSF + 1
 };
 
 // Masked keys of a 32-column chunk become -inf.  key0 = index of v[0] within
@@ -114,7 +117,7 @@ __device__ __forceinline__ TileInfo tile_info(int i, long long BH, int T, int N,
 template <int D>
 __global__ void __launch_bounds__(256, 1)
     softmax_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ nprev,
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, const int32_t* __restrict__ nprev,
                       const int32_t* __restrict__ sel_idx, const uint8_t* __restrict__ sel, int L, int N,
                       int T, long long BH, float sl2, const float* __restrict__ gate,
                       const float* __restrict__ nw_s, float eps, __nv_bfloat16* __restrict__ out,
@@ -136,9 +139,13 @@ __global__ void __launch_bounds__(256, 1)
     for (int s = 0; s < KS; ++s) {
       tc::mbar_init(&bars[B_KF + s], 1);
       tc::mbar_init(&bars[B_KE + s], 1);
+    }
+    for (int s = 0; s < VS; ++s) {
       tc::mbar_init(&bars[B_VF + s], 1);
       tc::mbar_init(&bars[B_VE + s], 1);
     }
+    tc::mbar_init(&bars[B_OSF], 128);  // output tile written by the 128 softmax threads
+    tc::mbar_init(&bars[B_OSE], 1);    // previous tile's TMA store has read the tile
     for (int b = 0; b < NS; ++b) {
       tc::mbar_init(&bars[B_SF + b], 1);
       tc::mbar_init(&bars[B_PF + b], 128);
@@ -195,6 +202,7 @@ __global__ void __launch_bounds__(256, 1)
       uint8_t* ring = smem + (kq ? S::offK : S::offV);
       uint64_t* full = &bars[kq ? B_KF : B_VF];
       uint64_t* empty = &bars[kq ? B_KE : B_VE];
+      const int RD = kq ? KS : VS;  // ring depth
       int gj = 0, tn = 0;
       bool ok = true;
       auto next = [&](int n) { return kq ? publish(n) : take(n, true); };
@@ -230,7 +238,7 @@ __global__ void __launch_bounds__(256, 1)
         for (int j = 0; j < ti.nb; ++j, ++gj) {
           int nx0 = 0, nx1 = 0;
           if (j + 1 < ti.nb) pair(j + 1, nx0, nx1);
-          const int ks = gj % KS, par = ((gj / KS) & 1) ^ 1;
+          const int ks = gj % RD, par = ((gj / RD) & 1) ^ 1;
           uint8_t* buf = ring + ks * S::kKV;
           if (!(ok = tc::mbar_wait(&empty[ks], par, err))) break;
           tc::mbar_arrive_expect_tx(&full[ks], S::kKV);
@@ -247,8 +255,8 @@ __global__ void __launch_bounds__(256, 1)
       }
       if (cur == -2 || nxt == -2) ok = false;
       // make sure every load completed and every release commit landed
-      for (int s = 0; s < KS; ++s) {
-        const int uses = gj > s ? (gj - 1 - s) / KS + 1 : 0;
+      for (int s = 0; s < RD; ++s) {
+        const int uses = gj > s ? (gj - 1 - s) / RD + 1 : 0;
         if (uses > 0) {
           tc::mbar_wait(&full[s], (uses - 1) & 1, nullptr);
           if (ok) tc::mbar_wait(&empty[s], (uses - 1) & 1, err);
@@ -307,17 +315,17 @@ __global__ void __launch_bounds__(256, 1)
         for (int j = 0; j < ti.nb; ++j) {
           const int g = g0 + j;
           if (j + 2 < ti.nb && !(ok = issue_s(g + 2, j + 3 == ti.nb))) break;
-          const int b = g % NS, ks = g % KS;
+          const int b = g % NS, vs = g % VS;
           if (!(ok = tc::mbar_wait(&bars[B_PF + b], (g / NS) & 1, err))) break;
-          if (!(ok = tc::mbar_wait(&bars[B_VF + ks], (g / KS) & 1, err))) break;
+          if (!(ok = tc::mbar_wait(&bars[B_VF + vs], (g / VS) & 1, err))) break;
           tc::fence_after();
-          const uint64_t vd = tc::desc_add(vd0, ks * S::kKV);
+          const uint64_t vd = tc::desc_add(vd0, vs * S::kKV);
           const uint32_t tP = tmem + b * 128;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             tc::mma_bf16_ts(tO, tP + kk * 8, tc::desc_add(vd, kk * 2048), idesc_pv, (j > 0) || (kk > 0));
           tc::mma_commit(&bars[B_PV + b]);
-          tc::mma_commit(&bars[B_VE + ks]);
+          tc::mma_commit(&bars[B_VE + vs]);
         }
         if (!ok) break;
         gj = g0 + ti.nb;
@@ -449,6 +457,16 @@ __global__ void __launch_bounds__(256, 1)
       // epilogue: out = w RMSNorm(O / l)   (validity is warp-uniform: a warp's rows share a half)
       if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_OF], tn & 1, err)))) break;
       tc::fence_after();
+      // the rows go through a swizzled bf16 tile in shared memory and leave
+      // with TMA stores (coalesced lines, not one 256-byte row per thread);
+      // the previous tile's stores must have read the tile first
+      if (tn > 0) {
+        if (warp == 4 && lane == 0) {
+          tc::bulk_wait_read_all();
+          tc::mbar_arrive(&bars[B_OSE]);
+        }
+        if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_OSE], (tn - 1) & 1, err)))) break;
+      }
       if (half == 0 || ti.has_c1) {
         // one TMEM pass: the row of O in registers, its mean square, then
         // the scaled row packed to bf16
@@ -472,7 +490,7 @@ __global__ void __launch_bounds__(256, 1)
             ((float4*)(o_s + row * D))[x] =
                 make_float4(o[4 * x] * inv, o[4 * x + 1] * inv, o[4 * x + 2] * inv, o[4 * x + 3] * inv);
         }
-        __nv_bfloat16* orow = out + row * D;
+        uint8_t* ost = smem + S::offOst + r * 128;
 #pragma unroll
         for (int g8 = 0; g8 < D / 8; ++g8) {
           uint4 pk;
@@ -482,12 +500,24 @@ __global__ void __launch_bounds__(256, 1)
             const int cc = g8 * 8 + 2 * x;
             p32[x] = tc::pack_bf16x2(cs * nw_sm[cc] * o[cc], cs * nw_sm[cc + 1] * o[cc + 1]);
           }
-          *(uint4*)(orow + g8 * 8) = pk;
+          // 16-byte granule (g8 & 7) of row r in half (g8 >> 3), 128-byte swizzle
+          *(uint4*)(ost + (g8 >> 3) * S::kHalf + (((g8 & 7) ^ (r & 7)) << 4)) = pk;
         }
       }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&bars[B_OSF]);
+      if (warp == 4 && lane == 0 && (ok = tc::mbar_wait(&bars[B_OSF], tn & 1, err))) {
+        const int orow0 = (int)(ti.bh * (long long)L + 128LL * ti.p);
+        for (int hh = 0; hh < D / 64; ++hh)
+          for (int rc = 0; rc < (ti.has_c1 ? 2 : 1); ++rc)
+            tc::tma_store_2d(&tm_o, smem + S::offOst + hh * S::kHalf + rc * (S::kHalf / 2), 64 * hh, orow0 + 64 * rc);
+        tc::bulk_commit();
+      }
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
       cur = nxt;
       nxt = cur >= 0 ? take_w(tn + 2) : -1;
     }
+    if (warp == 4 && lane == 0) tc::bulk_wait_all();  // the output tiles are written before exit
   }
   tc::fence_before();
   __syncthreads();
@@ -535,9 +565,10 @@ static cudaError_t launch_tc_t(const Problem& p, const void* q, const void* k, c
                                const int32_t* nprev, const int32_t* sel_idx, const uint8_t* sel,
                                const float* gate, const float* nw_s, void* out, float* o_s, int* err,
                                cudaStream_t st) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   const long long rows = p.BH * p.L;
-  if (!make_tile_map(&mq, q, rows, D) || !make_tile_map(&mk, k, rows, D) || !make_tile_map(&mv, v, rows, D))
+  if (!make_tile_map(&mq, q, rows, D) || !make_tile_map(&mk, k, rows, D) || !make_tile_map(&mv, v, rows, D) ||
+      !make_tile_map(&mo, out, rows, D))
     return cudaErrorInvalidValue;
   auto kern = softmax_tc_kernel<D>;
   const int smem = SoftmaxSmem<D>::kBytes;
@@ -549,7 +580,7 @@ static cudaError_t launch_tc_t(const Problem& p, const void* q, const void* k, c
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
-  kern<<<grid, 256, smem, st>>>(mq, mk, mv, nprev, sel_idx, sel, p.L, p.N, T, p.BH,
+  kern<<<grid, 256, smem, st>>>(mq, mk, mv, mo, nprev, sel_idx, sel, p.L, p.N, T, p.BH,
                                 p.scale * 1.4426950408889634f, gate, nw_s, p.eps, (__nv_bfloat16*)out, o_s,
                                 err, err + 1);
   return cudaGetLastError();
