@@ -68,14 +68,6 @@ __device__ __forceinline__ uint32_t sw_off(int line, int col, int half_bytes) {
   return (uint32_t)((col >> 6) * half_bytes + line * 128 + ((((col & 63) >> 3) ^ (line & 7)) << 4) + (col & 7) * 2);
 }
 
-// bf16x2 with round-to-nearest-even in integer arithmetic (finite inputs)
-__device__ __forceinline__ uint32_t pack_rne(float lo, float hi) {
-  uint32_t a = __float_as_uint(lo), b = __float_as_uint(hi);
-  a += 0x7FFFu + ((a >> 16) & 1u);
-  b += 0x7FFFu + ((b >> 16) & 1u);
-  return __byte_perm(a, b, 0x7632);
-}
-
 template <int D>
 __global__ void __launch_bounds__(320, 1)
     gdn_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
@@ -288,7 +280,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const float2 uf = __bfloat1622float2(u2[i]);
-              pd[4 * g8 + i] = pack_rne(uf.x - x[8 * g8 + 2 * i], uf.y - x[8 * g8 + 2 * i + 1]);
+              pd[4 * g8 + i] = tc::pack_bf16x2(uf.x - x[8 * g8 + 2 * i], uf.y - x[8 * g8 + 2 * i + 1]);
             }
           }
         } else {
@@ -315,7 +307,7 @@ __global__ void __launch_bounds__(320, 1)
         for (int ch = 0; ch < SC / 32; ++ch) {
           uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_rne(v[ch * 32 + 2 * i], v[ch * 32 + 2 * i + 1]);
+          for (int i = 0; i < 16; ++i) pk[i] = tc::pack_bf16x2(v[ch * 32 + 2 * i], v[ch * 32 + 2 * i + 1]);
           tc::tmem_st16u(tmem + kColS0 + lane_off + (hf * SC + ch * 32) / 2, pk);
         }
         tc::tmem_st_wait();
