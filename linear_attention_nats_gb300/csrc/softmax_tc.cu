@@ -21,12 +21,13 @@
 // Roles (256 threads):
 //   warp 0     TMA producer of Q (one per tile) and of the K blocks (3-deep
 //              ring); warp 2 the producer of the V blocks (3-deep ring)
-//   warp 1     TMEM owner + MMA issuer: S_j = Q K_j^T into one of three TMEM
-//              S buffers, up to two blocks ahead of O += P_j V_j, with P_j
-//              read from TMEM (it overwrites S_j in place).  Three buffers
-//              put three blocks of softmax work between a P V product and
-//              the S product that must wait for it, which hides the MMA and
-//              barrier latencies of that round trip.
+//   warp 1     TMEM owner; lane 0 issues S_j = Q K_j^T into one of three
+//              TMEM S buffers, up to three blocks ahead (a buffer is reused
+//              once the P V product that read its P has completed)
+//   warp 3     lane 0 issues O += P_j V_j, P_j read from TMEM (it overwrites
+//              S_j in place).  Two issuing threads on two SM sub-partitions:
+//              an MMA goes out only when its thread is scheduled, and each
+//              shares its sub-partition with a busy softmax warp.
 //   warps 4-7  softmax: thread r owns query row r (its TMEM lane); the row's
 //              128 scores of a block are read from TMEM once, their max taken
 //              in registers, and P_j packed to bf16 in TMEM, in the exp2
@@ -56,7 +57,7 @@ constexpr float kRescaleLog2 = 8.f;  // lazy-rescale threshold (log2 units)
 constexpr int KS = 3;                // K ring depth
 constexpr int VS = 2;                // V ring depth (the V producer runs far ahead of P V)
 constexpr int NS = 3;                // S/P buffers in TMEM
-constexpr int kTileTakers = 6;       // arrivals that free a tile-queue slot: MMA, V producer, 4 softmax warps
+constexpr int kTileTakers = 7;       // arrivals that free a tile-queue slot: 2 MMA issuers, V producer, 4 softmax warps
 
 template <int D>
 struct SoftmaxSmem {
@@ -68,7 +69,7 @@ struct SoftmaxSmem {
   static constexpr int offV = offK + KS * kKV;
   static constexpr int offOst = offV + VS * kKV;  // bf16 output tile of the epilogue (TMA store source)
   static constexpr int offBar = offOst + kQ;
-  static constexpr int kNumBars = 2 + 2 * KS + 2 * VS + 3 * NS + 1 + 4 + 2;
+  static constexpr int kNumBars = 2 + 2 * KS + 2 * VS + 3 * NS + 1 + 4 + 2 + 2;
   static constexpr int offTmem = offBar + kNumBars * 8;
   static constexpr int offNw = offTmem + 16;  // RMSNorm weights of the softmax branch, D floats
   static constexpr int offTq = offNw + D * 4;  // two-slot tile queue (ints)
@@ -79,7 +80,7 @@ struct SoftmaxSmem {
 enum {
   B_QF = 0, B_QE = 1, B_KF = 2, B_KE = B_KF + KS, B_VF = B_KE + KS, B_VE = B_VF + VS,
   B_SF = B_VE + VS, B_PF = B_SF + NS, B_PV = B_PF + NS, B_OF = B_PV + NS, B_TF = B_OF + 1, B_TE = B_TF + 2,
-  B_OSF = B_TE + 2, B_OSE = B_OSF + 1
+  B_OSF = B_TE + 2, B_OSE = B_OSF + 1, B_SDR = B_OSE + 1, B_PDR = B_SDR + 1
 };
 
 // Masked keys of a 32-column chunk become -inf.  key0 = index of v[0] within
@@ -146,6 +147,8 @@ __global__ void __launch_bounds__(256, 1)
     }
     tc::mbar_init(&bars[B_OSF], 128);  // output tile written by the 128 softmax threads
     tc::mbar_init(&bars[B_OSE], 1);    // previous tile's TMA store has read the tile
+    tc::mbar_init(&bars[B_SDR], 1);    // drains of the two MMA-issuing threads
+    tc::mbar_init(&bars[B_PDR], 1);
     for (int b = 0; b < NS; ++b) {
       tc::mbar_init(&bars[B_SF + b], 1);
       tc::mbar_init(&bars[B_PF + b], 128);
@@ -267,35 +270,26 @@ __global__ void __launch_bounds__(256, 1)
         if (ok) tc::mbar_wait(&bars[B_QE], (tn - 1) & 1, err);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 3) {
     // ----------------------------------------------------------------- MMA
+    // Two issuing threads on different SM sub-partitions: warp 1 issues
+    // S_j = Q K_j^T, warp 3 issues O += P_j V_j.  An MMA goes out only when
+    // its thread is scheduled, and each of these threads shares its
+    // sub-partition with a softmax warp that keeps the issue port busy;
+    // split, each has half the MMAs to issue.  S_j reuses the TMEM buffer of
+    // P_{j-3}, so warp 1 waits for that product first (B_PV); every P V comes
+    // from warp 3, so O accumulates them in order.
     if (lane == 0) {
+      const bool s_role = (warp == 1);
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, D, false, true);
       // descriptors are built once; each MMA only offsets the address field
-      // (the MMA warp shares its SM sub-partition with a busy softmax warp,
-      // so every instruction it needs to issue an MMA counts)
       const uint64_t qd0 = tc::smem_desc_sw128(tc::smem_u32(Qs), 16, 1024);
       const uint64_t kd0 = tc::smem_desc_sw128(tc::smem_u32(smem + S::offK), 16, 1024);
       const uint64_t vd0 = tc::smem_desc_sw128(tc::smem_u32(smem + S::offV), S::kHalf, 1024);
+      const uint32_t tO = tmem + NS * 128;
       int gj = 0, tn = 0;
       bool ok = true;
-      auto issue_s = [&](int g, bool last_of_tile) -> bool {
-        const int ks = g % KS;
-        if (!tc::mbar_wait(&bars[B_KF + ks], (g / KS) & 1, err)) return false;
-        tc::fence_after();
-        const uint64_t kd = tc::desc_add(kd0, ks * S::kKV);
-        const uint32_t tS = tmem + (g % NS) * 128;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * S::kHalf + (kk & 3) * 32;
-          tc::mma_bf16(tS, tc::desc_add(qd0, off), tc::desc_add(kd, off), idesc_qk, kk > 0);
-        }
-        tc::mma_commit(&bars[B_SF + g % NS]);
-        tc::mma_commit(&bars[B_KE + ks]);
-        if (last_of_tile) tc::mma_commit(&bars[B_QE]);  // Q may be replaced once these S are done
-        return true;
-      };
       int cur = take(0, true);
       int nxt = cur >= 0 ? take(1, true) : -1;
       // each tile's descriptor is read one tile ahead (global latency)
@@ -303,42 +297,52 @@ __global__ void __launch_bounds__(256, 1)
       for (; cur >= 0 && ok; ++tn) {
         const TileInfo ti = tnx;
         if (nxt >= 0) tnx = tile_info(nxt, BH, T, N, nprev, sel);
-        const uint32_t tO = tmem + NS * 128;
-        if (!(ok = tc::mbar_wait(&bars[B_QF], tn & 1, err))) break;
-        tc::fence_after();
-        // S runs up to two blocks ahead of P V.  The previous tile's O was
-        // read out by the softmax warps before they released this tile's
-        // first P, so the first P V below may overwrite it.
-        const int g0 = gj;
-        if (!(ok = issue_s(g0, ti.nb == 1))) break;
-        if (ti.nb > 1 && !(ok = issue_s(g0 + 1, ti.nb == 2))) break;
-        for (int j = 0; j < ti.nb; ++j) {
-          const int g = g0 + j;
-          if (j + 2 < ti.nb && !(ok = issue_s(g + 2, j + 3 == ti.nb))) break;
-          const int b = g % NS, vs = g % VS;
-          if (!(ok = tc::mbar_wait(&bars[B_PF + b], (g / NS) & 1, err))) break;
-          if (!(ok = tc::mbar_wait(&bars[B_VF + vs], (g / VS) & 1, err))) break;
-          tc::fence_after();
-          const uint64_t vd = tc::desc_add(vd0, vs * S::kKV);
-          const uint32_t tP = tmem + b * 128;
+        if (s_role) {
+          if (!(ok = tc::mbar_wait(&bars[B_QF], tn & 1, err))) break;
+          for (int j = 0; j < ti.nb; ++j) {
+            const int g = gj + j, b = g % NS, ks = g % KS;
+            // the buffer's previous P has been read by its P V product
+            if (g >= NS && !(ok = tc::mbar_wait(&bars[B_PV + b], ((g - NS) / NS) & 1, err))) break;
+            if (!(ok = tc::mbar_wait(&bars[B_KF + ks], (g / KS) & 1, err))) break;
+            tc::fence_after();
+            const uint64_t kd = tc::desc_add(kd0, ks * S::kKV);
+            const uint32_t tS = tmem + b * 128;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            tc::mma_bf16_ts(tO, tP + kk * 8, tc::desc_add(vd, kk * 2048), idesc_pv, (j > 0) || (kk > 0));
-          tc::mma_commit(&bars[B_PV + b]);
-          tc::mma_commit(&bars[B_VE + vs]);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * S::kHalf + (kk & 3) * 32;
+              tc::mma_bf16(tS, tc::desc_add(qd0, off), tc::desc_add(kd, off), idesc_qk, kk > 0);
+            }
+            tc::mma_commit(&bars[B_SF + b]);
+            tc::mma_commit(&bars[B_KE + ks]);
+            if (j + 1 == ti.nb) tc::mma_commit(&bars[B_QE]);  // Q may be replaced once these S are done
+          }
+        } else {
+          // The previous tile's O was read out by the softmax warps before
+          // they released this tile's first P, so its P V may overwrite O.
+          for (int j = 0; j < ti.nb; ++j) {
+            const int g = gj + j, b = g % NS, vs = g % VS;
+            if (!(ok = tc::mbar_wait(&bars[B_PF + b], (g / NS) & 1, err))) break;
+            if (!(ok = tc::mbar_wait(&bars[B_VF + vs], (g / VS) & 1, err))) break;
+            tc::fence_after();
+            const uint64_t vd = tc::desc_add(vd0, vs * S::kKV);
+            const uint32_t tP = tmem + b * 128;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              tc::mma_bf16_ts(tO, tP + kk * 8, tc::desc_add(vd, kk * 2048), idesc_pv, (j > 0) || (kk > 0));
+            tc::mma_commit(&bars[B_PV + b]);
+            tc::mma_commit(&bars[B_VE + vs]);
+          }
+          if (ok) tc::mma_commit(&bars[B_OF]);
         }
         if (!ok) break;
-        gj = g0 + ti.nb;
-        tc::mma_commit(&bars[B_OF]);
+        gj += ti.nb;
         cur = nxt;
         nxt = cur >= 0 ? take(tn + 2, true) : -1;
       }
-      // drain: every MMA issued so far completes before the commits land
-      for (int b = 0; b < NS; ++b) tc::mma_commit(&bars[B_PV + b]);
-      for (int b = 0; b < NS; ++b) {
-        const int uses = gj > b ? (gj - 1 - b) / NS + 1 : 0;  // earlier commits to B_PV[b]
-        tc::mbar_wait(&bars[B_PV + b], uses & 1, nullptr);
-      }
+      // drain: every MMA this thread issued completes before the commit lands
+      uint64_t* dr = &bars[s_role ? B_SDR : B_PDR];
+      tc::mma_commit(dr);
+      tc::mbar_wait(dr, 0, nullptr);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------- softmax
