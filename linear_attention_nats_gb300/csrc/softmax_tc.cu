@@ -20,7 +20,7 @@
 // a CTA the K producer takes the tile and hands it to the other roles.
 // Roles (256 threads):
 //   warp 0     TMA producer of Q (one per tile) and of the K blocks (3-deep
-//              ring); warp 2 the producer of the V blocks (3-deep ring)
+//              ring); warp 2 the producer of the V blocks (2-deep ring)
 //   warp 1     TMEM owner; lane 0 issues S_j = Q K_j^T into one of three
 //              TMEM S buffers, up to three blocks ahead (a buffer is reused
 //              once the P V product that read its P has completed)
@@ -38,6 +38,8 @@
 //              The tile epilogue writes the softmax half of the layer output
 //              ("Kernmechanismen" item 4): w RMSNorm(O / l) in bf16, w the
 //              query gate; the Gated DeltaNet side adds its half afterwards.
+//              The rows go through a swizzled bf16 tile in shared memory and
+//              leave with TMA stores.
 //              It reads O before the warps release the next tile's first P,
 //              so one O accumulator serves every tile.
 // TMEM: S0, S1, S2 (128 columns each), O (D columns).
