@@ -25,7 +25,7 @@
 //         chunk c + 1, overlapping the next MMAs (O is triple-buffered).
 // Roles (320 threads): warps 0-7 elementwise, warp w owning TMEM lanes
 // 32 (w % 4) .. +31 and half (w / 4) of the columns; warp 8 TMA producer
-// (W, Q~, K~, U^T, P of coming chunks, double-buffered); warp 9 TMEM owner and
+// (W, Q~, K~, U^T, P of coming chunks, three stages); warp 9 TMEM owner and
 // MMA issuer.  Every wait is bounded (tc::kWaitLimitNs).
 #include "common.cuh"
 #include "kernels.h"
@@ -44,16 +44,17 @@ struct ScanSmem {
   static constexpr int kU = D * 64 * 2;    // U^T chunk: D lines (dv) x 64 cols (t), 8 KiB per 64 lines
   static constexpr int kP = 64 * 64 * 2;   // P chunk: 64 lines (t) x 64 cols (i)
   static constexpr int kStage = kWQ + kK + kU + kP;
+  static constexpr int kStages = 3;  // chunks in flight: the loads run two chunks ahead
   static constexpr int offStage = 0;
-  static constexpr int offBar = 2 * kStage;
-  static constexpr int kNumBars = 12;
+  static constexpr int offBar = kStages * kStage;
+  static constexpr int kNumBars = 14;
   static constexpr int offTmem = offBar + kNumBars * 8;
   static constexpr int kBytes = offTmem + 16 + 1024;
 };
 
 // SB_OFREE + b: O^T of the chunks using O buffer b has been read (one barrier
 // per buffer, so a waiter is never two phases behind)
-enum { SB_FULL = 0, SB_EMPTY = 2, SB_S0 = 4, SB_Z = 5, SB_DELTA = 6, SB_OFREE = 7, SB_SDONE = 10, SB_DONE = 11 };
+enum { SB_FULL = 0, SB_EMPTY = 3, SB_S0 = 6, SB_Z = 7, SB_DELTA = 8, SB_OFREE = 9, SB_SDONE = 12, SB_DONE = 13 };
 
 // TMEM columns
 constexpr uint32_t kColX = 0;      // S0 W^T, 64 columns (consumed at once by Delta)
@@ -86,7 +87,7 @@ __global__ void __launch_bounds__(320, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < S::kStages; ++s) {
       tc::mbar_init(&bars[SB_FULL + s], 1);
       tc::mbar_init(&bars[SB_EMPTY + s], 1);
     }
@@ -115,11 +116,11 @@ __global__ void __launch_bounds__(320, 1)
       tc::prefetch_tensormap(&tm_k);
       tc::prefetch_tensormap(&tm_u);
       tc::prefetch_tensormap(&tm_p);
-      int issued[2] = {0, 0};
+      int issued[S::kStages] = {};
       bool ok = true;
       for (int c = 0; c < N; ++c) {
-        const int s = c & 1;
-        if (!(ok = tc::mbar_wait(&bars[SB_EMPTY + s], ((c >> 1) & 1) ^ 1, err))) break;
+        const int s = c % S::kStages;
+        if (!(ok = tc::mbar_wait(&bars[SB_EMPTY + s], ((c / S::kStages) & 1) ^ 1, err))) break;
         uint8_t* WQ = smem + S::offStage + s * S::kStage;
         uint8_t* Kb = WQ + S::kWQ;
         uint8_t* Ub = Kb + S::kK;
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(320, 1)
         tc::tma_load_2d(Pb, &tm_p, 0, yc, &bars[SB_FULL + s]);
         issued[s]++;
       }
-      for (int s = 0; s < 2; ++s) {
+      for (int s = 0; s < S::kStages; ++s) {
         if (issued[s] == 0) continue;
         tc::mbar_wait(&bars[SB_FULL + s], (issued[s] - 1) & 1, nullptr);
         if (ok) tc::mbar_wait(&bars[SB_EMPTY + s], (issued[s] - 1) & 1, err);
@@ -157,12 +158,12 @@ __global__ void __launch_bounds__(320, 1)
       bool ok = true;
       uint8_t sel_c = sel[bh * N];  // selections are read one chunk ahead (global latency)
       for (int c = 0; c < N && ok; ++c) {
-        const int s = c & 1;
+        const int s = c % S::kStages;
         const uint8_t sel_n = (c + 1 < N) ? sel[bh * N + c + 1] : 0;
         const uint32_t tX = tmem + kColX, tO = tmem + kColO + (c % 3) * 64;
         const uint32_t sb = s * S::kStage;
         const uint64_t wd = tc::desc_add(wd0, sb), kd = tc::desc_add(kd0, sb), pd = tc::desc_add(pd0, sb);
-        if (!(ok = tc::mbar_wait(&bars[SB_FULL + s], (c >> 1) & 1, err))) break;
+        if (!(ok = tc::mbar_wait(&bars[SB_FULL + s], (c / S::kStages) & 1, err))) break;
         if (!(ok = tc::mbar_wait(&bars[SB_S0], c & 1, err))) break;
         if (c >= 3 && !(ok = tc::mbar_wait(&bars[SB_OFREE + (c % 3)], ((c - 3) / 3) & 1, err))) break;
         tc::fence_after();
@@ -180,15 +181,16 @@ __global__ void __launch_bounds__(320, 1)
         }
         if (!(ok = tc::mbar_wait(&bars[SB_DELTA], c & 1, err))) break;
         tc::fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc::mma_bf16_ts(tO, tmem + kColDT + kk * 8, tc::desc_add(pd, kk * 32), id2, 1);
+        // the state update first (the next chunk waits for it), then O
         if (sel_c != 0) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             tc::mma_bf16_ts(tmem + kColS, tmem + kColDT + kk * 8, tc::desc_add(kd, kk * 2048), id3, 1);
         }
         tc::mma_commit(&bars[SB_SDONE]);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_bf16_ts(tO, tmem + kColDT + kk * 8, tc::desc_add(pd, kk * 32), id2, 1);
         tc::mma_commit(&bars[SB_EMPTY + s]);
         sel_c = sel_n;
       }
@@ -246,7 +248,22 @@ __global__ void __launch_bounds__(320, 1)
     bool lin_c = selh[0] != 0;
     bool lin_n = N > 1 && selh[1] != 0;
     float gC_n = N > 1 ? Gh[64 + 63] : 0.f;
-    for (int c = 0; c < N; ++c) {
+    // U^T of a chunk is read into registers one chunk ahead, while the
+    // previous chunk waits for its state update
+    uint4 uvn[4];
+    auto load_u = [&](int cc) -> bool {
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_FULL + cc % S::kStages], (cc / S::kStages) & 1, err)))
+        return false;
+      if (has_row) {
+        const uint8_t* Ub = smem + S::offStage + (cc % S::kStages) * S::kStage + S::kWQ + S::kK;
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8)
+          uvn[g8] = *(const uint4*)(Ub + sw_off(r & 63, 32 * hf + 8 * g8, 0) + (r >> 6) * 8192);
+      }
+      return true;
+    };
+    if (N > 0) ok = load_u(0);
+    for (int c = 0; c < N && ok; ++c) {
       const bool has_nn = c + 2 < N;
       const uint8_t sel_nn = has_nn ? selh[c + 2] : 0;
       const float gC_nn = has_nn ? Gh[64LL * (c + 2) + 63] : 0.f;
@@ -258,17 +275,11 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t tX = tmem + kColX + lane_off;
       // ---- Delta^T (columns t = 32 hf .. 32 hf + 31 of this row)
       {
-        const uint8_t* Ub = smem + S::offStage + (c & 1) * S::kStage + S::kWQ + S::kK;
         float x[32];
         uint32_t pd[16];
         uint4 uv[4];
-        // U^T of this chunk is in shared memory once its stage is full
-        if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_FULL + (c & 1)], (c >> 1) & 1, err)))) break;
-        if (has_row) {
 #pragma unroll
-          for (int g8 = 0; g8 < 4; ++g8)
-            uv[g8] = *(const uint4*)(Ub + sw_off(r & 63, 32 * hf + 8 * g8, 0) + (r >> 6) * 8192);
-        }
+        for (int g8 = 0; g8 < 4; ++g8) uv[g8] = uvn[g8];
         if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_Z], c & 1, err)))) break;
         tc::fence_after();
         tc::tmem_ld32(tX + 32 * hf, x);
@@ -292,6 +303,7 @@ __global__ void __launch_bounds__(320, 1)
         tc::fence_before();
         tc::mbar_arrive(&bars[SB_DELTA]);
       }
+      if (c + 1 < N && !(ok = load_u(c + 1))) break;
       // ---- state: bf16 copy after this chunk's update, and the decay of the
       // next linear chunk applied ahead of its MMA3
       if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_SDONE], c & 1, err)))) break;
@@ -325,7 +337,11 @@ __global__ void __launch_bounds__(320, 1)
       }
       if (c > 0) o_phase(c - 1);
     }
-    if (ok && N > 0) o_phase(N - 1);  // the last chunk's O work (its SDONE was waited)
+    // the last chunk's O work, once every MMA has completed
+    if (ok && N > 0 && (ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_DONE], 0, err)))) {
+      tc::fence_after();
+      o_phase(N - 1);
+    }
     if (ok && state_out && has_row) {
       tc::fence_after();
 #pragma unroll 1
