@@ -16,13 +16,13 @@
 //
 // One CTA per (b, h) walks the N chunks in order; the fp32 state S stays in
 // TMEM for the whole sequence, next to its bf16 copy S0.  Per chunk c:
-//   MMA1  X = S0 W^T, O[c%3] = S0 Q~^T    (M = 128 lanes >= dv, N = 64 each, K = dk)
+//   MMA1  [X | O] = S0 [W; Q~]^T  into TMEM buffer c % 2 (M = 128 lanes >= dv,
+//         N = 128: X = S0 W^T and the first term of O in one product, K = dk)
 //   all   Delta^T = U^T - X -> TMEM (bf16)
-//   MMA2  O[c%3] += Delta^T P^T
-//   MMA3  S += Delta^T K~                (linear chunks only)
-//   all   S -> bf16 S0; S *= gamma_C of the next chunk when it is linear
-//   all   O^T -> o_l; the O work of chunk c runs after the state work of
-//         chunk c + 1, overlapping the next MMAs (O is triple-buffered).
+//   MMA3  S += Delta^T K~                (linear chunks only), then
+//   MMA2  O += Delta^T P^T
+//   all   O^T of chunk c - 1 -> o_l while MMA3 runs, then S -> bf16 S0 and
+//         S *= gamma_C of the next chunk when it is linear
 // Roles (320 threads): warps 0-7 elementwise, warp w owning TMEM lanes
 // 32 (w % 4) .. +31 and half (w / 4) of the columns; warp 8 TMA producer
 // (W, Q~, K~, U^T, P of coming chunks, three stages); warp 9 TMEM owner and
@@ -47,18 +47,17 @@ struct ScanSmem {
   static constexpr int kStages = 3;  // chunks in flight: the loads run two chunks ahead
   static constexpr int offStage = 0;
   static constexpr int offBar = kStages * kStage;
-  static constexpr int kNumBars = 14;
+  static constexpr int kNumBars = 13;
   static constexpr int offTmem = offBar + kNumBars * 8;
   static constexpr int kBytes = offTmem + 16 + 1024;
 };
 
 // SB_OFREE + b: O^T of the chunks using O buffer b has been read (one barrier
 // per buffer, so a waiter is never two phases behind)
-enum { SB_FULL = 0, SB_EMPTY = 3, SB_S0 = 6, SB_Z = 7, SB_DELTA = 8, SB_OFREE = 9, SB_SDONE = 12, SB_DONE = 13 };
+enum { SB_FULL = 0, SB_EMPTY = 3, SB_S0 = 6, SB_Z = 7, SB_DELTA = 8, SB_OFREE = 9, SB_SDONE = 11, SB_DONE = 12 };
 
 // TMEM columns
-constexpr uint32_t kColX = 0;      // S0 W^T, 64 columns (consumed at once by Delta)
-constexpr uint32_t kColO = 64;     // three O^T buffers of 64 columns
+constexpr uint32_t kColXO = 0;     // two buffers of 128 columns: [S0 W^T | O^T] of chunks c % 2
 constexpr uint32_t kColS = 256;    // state, D columns (fp32)
 constexpr uint32_t kColS0 = 384;   // state bf16, D / 2 columns (two dk per column)
 constexpr uint32_t kColDT = 448;   // Delta^T bf16, 32 columns (64 t)
@@ -94,7 +93,7 @@ __global__ void __launch_bounds__(320, 1)
     tc::mbar_init(&bars[SB_S0], 256);
     tc::mbar_init(&bars[SB_Z], 1);
     tc::mbar_init(&bars[SB_DELTA], 256);
-    for (int b = 0; b < 3; ++b) tc::mbar_init(&bars[SB_OFREE + b], 256);
+    for (int b = 0; b < 2; ++b) tc::mbar_init(&bars[SB_OFREE + b], 256);
     tc::mbar_init(&bars[SB_SDONE], 1);
     tc::mbar_init(&bars[SB_DONE], 1);
     tc::fence_barrier_init();
@@ -147,7 +146,7 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 9) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t id1 = tc::idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t id1 = tc::idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t id2 = tc::idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t id3 = tc::idesc_bf16_f32(128, D, false, true);
       // descriptors are built once per stage; each MMA only offsets them
@@ -160,25 +159,22 @@ __global__ void __launch_bounds__(320, 1)
       for (int c = 0; c < N && ok; ++c) {
         const int s = c % S::kStages;
         const uint8_t sel_n = (c + 1 < N) ? sel[bh * N + c + 1] : 0;
-        const uint32_t tX = tmem + kColX, tO = tmem + kColO + (c % 3) * 64;
+        const uint32_t tX = tmem + kColXO + (c & 1) * 128, tO = tX + 64;
         const uint32_t sb = s * S::kStage;
         const uint64_t wd = tc::desc_add(wd0, sb), kd = tc::desc_add(kd0, sb), pd = tc::desc_add(pd0, sb);
         if (!(ok = tc::mbar_wait(&bars[SB_FULL + s], (c / S::kStages) & 1, err))) break;
         if (!(ok = tc::mbar_wait(&bars[SB_S0], c & 1, err))) break;
-        if (c >= 3 && !(ok = tc::mbar_wait(&bars[SB_OFREE + (c % 3)], ((c - 3) / 3) & 1, err))) break;
+        if (c >= 2 && !(ok = tc::mbar_wait(&bars[SB_OFREE + (c & 1)], ((c - 2) / 2) & 1, err))) break;
         tc::fence_after();
-        // S0 W^T first (Delta waits on it), then S0 Q~^T (O only)
+        // [S0 W^T | S0 Q~^T] in one N = 128 product over the stacked [W; Q~]
+        // tile (128 lines per 64-column half): X for Delta, and the first
+        // term of O, for the cost of one 64-wide product
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t offb = (kk >> 2) * 16384 + (kk & 3) * 32;  // [W; Q~]: 128 lines per 64-col half
+          const uint32_t offb = (kk >> 2) * 16384 + (kk & 3) * 32;
           tc::mma_bf16_ts(tX, tmem + kColS0 + kk * 8, tc::desc_add(wd, offb), id1, kk > 0);
         }
         tc::mma_commit(&bars[SB_Z]);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t offb = (kk >> 2) * 16384 + (kk & 3) * 32 + 8192;
-          tc::mma_bf16_ts(tO, tmem + kColS0 + kk * 8, tc::desc_add(wd, offb), id1, kk > 0);
-        }
         if (!(ok = tc::mbar_wait(&bars[SB_DELTA], c & 1, err))) break;
         tc::fence_after();
         // the state update first (the next chunk waits for it), then O
@@ -225,7 +221,7 @@ __global__ void __launch_bounds__(320, 1)
     // write 128 contiguous bytes per t
     auto o_phase = [&](int cc) {
       float o[32];  // warp-collective load (lanes >= D hold no state row)
-      tc::tmem_ld32(tmem + kColO + (cc % 3) * 64 + lane_off + 32 * hf, o);
+      tc::tmem_ld32(tmem + kColXO + (cc & 1) * 128 + 64 + lane_off + 32 * hf, o);
       tc::tmem_ld_wait();
       if (has_row) {
         const size_t off = (bh * (long long)L + 64LL * cc + 32 * hf) * D + r;
@@ -238,7 +234,7 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       tc::fence_before();
-      tc::mbar_arrive(&bars[SB_OFREE + (cc % 3)]);
+      tc::mbar_arrive(&bars[SB_OFREE + (cc & 1)]);
     };
     bool ok = true;
     // per-chunk selections and end-of-chunk log-decays, read two chunks ahead
@@ -272,7 +268,7 @@ __global__ void __launch_bounds__(320, 1)
       lin_c = lin_n;
       lin_n = sel_nn != 0;
       gC_n = gC_nn;
-      const uint32_t tX = tmem + kColX + lane_off;
+      const uint32_t tX = tmem + kColXO + (c & 1) * 128 + lane_off;
       // ---- Delta^T (columns t = 32 hf .. 32 hf + 31 of this row)
       {
         float x[32];
@@ -304,6 +300,10 @@ __global__ void __launch_bounds__(320, 1)
         tc::mbar_arrive(&bars[SB_DELTA]);
       }
       if (c + 1 < N && !(ok = load_u(c + 1))) break;
+      // O of the previous chunk (complete: its last product was issued
+      // before this chunk's S0 W^T, which Delta waited for), while this
+      // chunk's state update runs
+      if (c > 0) o_phase(c - 1);
       // ---- state: bf16 copy after this chunk's update, and the decay of the
       // next linear chunk applied ahead of its MMA3
       if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_SDONE], c & 1, err)))) break;
@@ -335,7 +335,6 @@ __global__ void __launch_bounds__(320, 1)
         if (SC > 32) tc::tmem_st32(tmem + kColS + lane_off + hf * SC + 32, *reinterpret_cast<float(*)[32]>(&v[SC > 32 ? 32 : 0]));
         tc::tmem_st_wait();
       }
-      if (c > 0) o_phase(c - 1);
     }
     // the last chunk's O work, once every MMA has completed
     if (ok && N > 0 && (ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_DONE], 0, err)))) {
