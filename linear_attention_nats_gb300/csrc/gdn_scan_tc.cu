@@ -265,9 +265,6 @@ __global__ void __launch_bounds__(320, 1)
       const float gC_nn = has_nn ? Gh[64LL * (c + 2) + 63] : 0.f;
       const bool lin = lin_c, lin_next = lin_n;
       const float gnext = lin_next ? __expf(gC_n) : 1.f;
-      lin_c = lin_n;
-      lin_n = sel_nn != 0;
-      gC_n = gC_nn;
       const uint32_t tX = tmem + kColXO + (c & 1) * 128 + lane_off;
       // ---- Delta^T (columns t = 32 hf .. 32 hf + 31 of this row)
       {
@@ -335,6 +332,10 @@ __global__ void __launch_bounds__(320, 1)
         if (SC > 32) tc::tmem_st32(tmem + kColS + lane_off + hf * SC + 32, *reinterpret_cast<float(*)[32]>(&v[SC > 32 ? 32 : 0]));
         tc::tmem_st_wait();
       }
+      // the loads for chunk c + 2 issued at the top are consumed only here
+      lin_c = lin_n;
+      lin_n = sel_nn != 0;
+      gC_n = gC_nn;
     }
     // the last chunk's O work, once every MMA has completed
     if (ok && N > 0 && (ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_DONE], 0, err)))) {
