@@ -360,9 +360,10 @@ def run_native(args, rank, world, local_rank):
     launches = sum(p.launches for p in profs)
     stage_ms = {}
     for si, name in enumerate(_native.STAGES):
+        if profs[0].stage_launches[si] == 0:  # the path does not run this stage
+            continue
         vals = [row[si][0].elapsed_time(row[si][1]) for row in stage_ev]
-        if max(vals) > 2e-3:  # stages the path does not run keep their back-to-back records
-            stage_ms[name] = sum(vals) / len(vals)
+        stage_ms[name] = sum(vals) / len(vals)
     ms = max_over_ranks(ms, dist, dev)
     ms_step = ms / args.steps
     tokens = B * L * world

@@ -165,13 +165,18 @@ typedef enum {
 } nats_stage;
 
 /* Caller-owned timing hooks.  start[s] / stop[s] are cudaEvent_t handles
- * (or NULL); the library records them on `stream` right before the first
- * and right after the last kernel of stage s.  `launches` is set to the
- * number of kernels the call launched. */
+ * (or NULL); the library records them right before the first and right
+ * after the last kernel of stage s, on the stream that stage runs on (the
+ * softmax stage runs on a second stream, concurrently with the Gated
+ * DeltaNet scan, and is joined back before the call's last kernel).
+ * `launches` is set to the number of kernels the call launched and
+ * stage_launches[s] to the number stage s launched (0: the stage did not
+ * run and its events were not recorded). */
 typedef struct {
   void* start[NATS_NUM_STAGES];
   void* stop[NATS_NUM_STAGES];
   int32_t launches;
+  int32_t stage_launches[NATS_NUM_STAGES];
 } nats_profile;
 
 /* nats_hybrid_fwd plus per-stage event records (prof may be NULL, which

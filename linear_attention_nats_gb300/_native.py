@@ -34,7 +34,7 @@ STAGES = ("score", "compact", "softmax", "gdn_prep", "gdn_scan", "merge")
 
 class Profile(ctypes.Structure):
     _fields_ = [("start", ctypes.c_void_p * NUM_STAGES), ("stop", ctypes.c_void_p * NUM_STAGES),
-                ("launches", ctypes.c_int32)]
+                ("launches", ctypes.c_int32), ("stage_launches", ctypes.c_int32 * NUM_STAGES)]
 
 
 class Dims(ctypes.Structure):

@@ -92,6 +92,7 @@ struct Stages {
     if (cuda_status(expr) != NATS_OK) return NATS_ERR_CUDA;                           \
     if ((stg).prof) {                                                                 \
       (stg).prof->launches += (n_launch);                                             \
+      (stg).prof->stage_launches[id] += (n_launch);                                   \
       if ((stg).mark((stg).prof->stop, id) != cudaSuccess) return NATS_ERR_CUDA;      \
     }                                                                                 \
   } while (0)
@@ -196,7 +197,10 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
   nats_status s = check_dims(dims);
   if (s != NATS_OK) return s;
   const Problem p = problem_of(dims);
-  if (prof) prof->launches = 0;
+  if (prof) {
+    prof->launches = 0;
+    for (int i = 0; i < NATS_NUM_STAGES; ++i) prof->stage_launches[i] = 0;
+  }
   if (p.BH == 0 || p.L == 0) return NATS_OK;
   if (!q || !k || !v || !g || !beta || !w_g || !out || !workspace) return NATS_ERR_NULL;
   if (!sel_in && !w_s) return NATS_ERR_NULL;

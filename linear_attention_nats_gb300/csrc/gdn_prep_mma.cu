@@ -98,7 +98,7 @@ struct PrepSmem {
   static constexpr int offB = offG + C * 4;          // fp32 [C] beta
   static constexpr int offBg = offB + C * 4;         // fp32 [C] beta e^G
   static constexpr int offX = offBg + C * 4;         // fp32 [C][FS] scratch of the blocked inverse
-  static constexpr int offRed = offX + C * FS * 4;   // fp32 [2][4] per-warp partial chunk scores
+  static constexpr int offRed = offX + C * FS * 4;   // fp32 [2][4] per-warp partial chunk scores, [2] bias
   static constexpr int kBytes = offRed + 64;
 };
 
@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(256, 2) gdn_prep_mma_kernel(
   } else if (warp == 1) {
     Bs[2 * lane] = beta[tok0 + 2 * lane];
     Bs[2 * lane + 1] = beta[tok0 + 2 * lane + 1];
+    if (lane < 2) red[8 + lane] = (sel_out && b_s) ? b_s[2 * h + lane] : 0.f;  // score bias, for the end
   }
   cp_async_wait_all();
   __syncthreads();
@@ -353,64 +354,63 @@ __global__ void __launch_bounds__(256, 2) gdn_prep_mma_kernel(
       for (int tt = 0; tt < 16; ++tt) Ts[(16 * b + tt) * FS + j] = x[tt];
     }
     named_barrier(1, 128);
-    // off-diagonal tiles by distance, one warp per tile, on tf32 MMAs (fp32
-    // accumulate; T is rounded to bf16 for the U / W products right after,
-    // far coarser than the tf32 operands):
-    //   X_ij = A_{i, j..i-1} T_{j..i-1, j}   then   T_ij = -T_ii X_ij
-    for (int lv = 1; lv < 4; ++lv) {
-      const int nblk = 4 - lv;
-      if (warp < nblk) {
-        const int i = warp + lv, j = warp;
-        float x[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) x[nt][e] = 0.f;
-        for (int k0 = 16 * j; k0 < 16 * i; k0 += 8) {
-          const float* ar = As + (16 * i + gq) * FS + k0 + cq;
-          const uint32_t a0 = tf32(ar[0]), a1 = tf32(ar[8 * FS]), a2 = tf32(ar[4]), a3 = tf32(ar[8 * FS + 4]);
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            const float* br = Ts + (k0 + cq) * FS + 16 * j + 8 * nt + gq;
-            mma1688_tf32(x[nt], a0, a1, a2, a3, tf32(br[0]), tf32(br[4 * FS]));
-          }
-        }
-        // X_ij -> shared memory (the B operand of the second product)
+    // off-diagonal tiles on tf32 MMAs (fp32 accumulate; T is rounded to bf16
+    // for the U / W products right after, far coarser than the tf32
+    // operands), blocked in two levels so that the chain is four products:
+    //   halves a = rows 0-31, b = rows 32-63:  T = [[T_a, 0], [T_ba, T_b]]
+    //   level 1: T_10 = -T_11 (A_10 T_00), T_32 = -T_33 (A_32 T_22)
+    //   level 2: Y = A_ba T_a, then T_ba = -T_b Y (four 16 x 16 tiles each)
+    // acc (16 x 16, two n-tiles) += M1[r0.., c0 .. c0+klen) * M2[c0'.., n0 ..]
+    auto tile_mma = [&](float (&acc)[2][4], const float* M1, int r0, int c0, const float* M2, int k0, int n0,
+                        int klen) {
+      for (int kk = 0; kk < klen; kk += 8) {
+        const float* ar = M1 + (r0 + gq) * FS + c0 + kk + cq;
+        const uint32_t a0 = tf32(ar[0]), a1 = tf32(ar[8 * FS]), a2 = tf32(ar[4]), a3 = tf32(ar[8 * FS + 4]);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          float* xr = Xs + (16 * i + gq) * FS + 16 * j + 8 * nt + 2 * cq;
-          xr[0] = x[nt][0];
-          xr[1] = x[nt][1];
-          xr[8 * FS] = x[nt][2];
-          xr[8 * FS + 1] = x[nt][3];
-        }
-        __syncwarp();
-        float y[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) y[nt][e] = 0.f;
-#pragma unroll
-        for (int k0 = 0; k0 < 16; k0 += 8) {
-          const float* ar = Ts + (16 * i + gq) * FS + 16 * i + k0 + cq;
-          const uint32_t a0 = tf32(ar[0]), a1 = tf32(ar[8 * FS]), a2 = tf32(ar[4]), a3 = tf32(ar[8 * FS + 4]);
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            const float* br = Xs + (16 * i + k0 + cq) * FS + 16 * j + 8 * nt + gq;
-            mma1688_tf32(y[nt], a0, a1, a2, a3, tf32(br[0]), tf32(br[4 * FS]));
-          }
-        }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          float* tr = Ts + (16 * i + gq) * FS + 16 * j + 8 * nt + 2 * cq;
-          tr[0] = -y[nt][0];
-          tr[1] = -y[nt][1];
-          tr[8 * FS] = -y[nt][2];
-          tr[8 * FS + 1] = -y[nt][3];
+          const float* br = M2 + (k0 + kk + cq) * FS + n0 + 8 * nt + gq;
+          mma1688_tf32(acc[nt], a0, a1, a2, a3, tf32(br[0]), tf32(br[4 * FS]));
         }
       }
-      named_barrier(1, 128);
+    };
+    auto tile_store = [&](float* M, int r0, int n0, const float (&acc)[2][4], float sgn) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        float* dr = M + (r0 + gq) * FS + n0 + 8 * nt + 2 * cq;
+        dr[0] = sgn * acc[nt][0];
+        dr[1] = sgn * acc[nt][1];
+        dr[8 * FS] = sgn * acc[nt][2];
+        dr[8 * FS + 1] = sgn * acc[nt][3];
+      }
+    };
+    if (warp < 2) {
+      // level 1: tile (i, j) = (2w + 1, 2w)
+      const int i = 2 * warp + 1, j = 2 * warp;
+      float x[2][4] = {};
+      tile_mma(x, As, 16 * i, 16 * j, Ts, 16 * j, 16 * j, 16);  // A_ij T_jj
+      tile_store(Xs, 16 * i, 16 * j, x, 1.f);
+      __syncwarp();
+      float y[2][4] = {};
+      tile_mma(y, Ts, 16 * i, 16 * i, Xs, 16 * i, 16 * j, 16);  // T_ii X_ij
+      tile_store(Ts, 16 * i, 16 * j, y, -1.f);
     }
+    named_barrier(1, 128);
+    // level 2, warp w owns tile (i, j) = (2 + w / 2, w % 2) of the lower-left block
+    const int li = 2 + (warp >> 1), lj = warp & 1;
+    {
+      // Y_ij = sum_{k = j..1} A_ik T_kj   (T_a is lower triangular)
+      float yv[2][4] = {};
+      tile_mma(yv, As, 16 * li, 16 * lj, Ts, 16 * lj, 16 * lj, 16 * (2 - lj));
+      tile_store(Xs, 16 * li, 16 * lj, yv, 1.f);
+    }
+    named_barrier(1, 128);
+    {
+      // T_ij = -sum_{k = 2..i} T_ik Y_kj   (T_b is lower triangular)
+      float tv[2][4] = {};
+      tile_mma(tv, Ts, 16 * li, 32, Xs, 32, 16 * lj, 16 * (li - 1));
+      tile_store(Ts, 16 * li, 16 * lj, tv, -1.f);
+    }
+    named_barrier(1, 128);
     // T -> bf16 (zero above the diagonal), 8 columns per step
     for (int e = tid; e < C * C / 8; e += 128) {
       const int t = e >> 3, j0 = (e & 7) * 8;
@@ -426,16 +426,6 @@ __global__ void __launch_bounds__(256, 2) gdn_prep_mma_kernel(
     }
   }
   __syncthreads();
-  if (sel_out && tid == 0) {
-    // chunk score = (1/C) w_s . (column sums of [Q ; K]) + b_s; ties to softmax
-    float a = ((red[0] + red[1]) + (red[2] + red[3])) * (1.0f / C);
-    float bb = ((red[4] + red[5]) + (red[6] + red[7])) * (1.0f / C);
-    if (b_s) {
-      a += b_s[2 * h];
-      bb += b_s[2 * h + 1];
-    }
-    sel_out[blk] = (a >= bb) ? 0 : 1;
-  }
   // ---- U = T (beta V) on warps wh = 0, W = T (beta e^G K) on warps wh = 1:
   // rows 16 wr .., k-steps up to the diagonal
   {
@@ -492,6 +482,13 @@ __global__ void __launch_bounds__(256, 2) gdn_prep_mma_kernel(
       const int t = e / VPR, x = e % VPR;
       *(uint4*)(Wg + t * D + x * 8) = *(const uint4*)(Wst + t * RS + x * 8);
     }
+  }
+  if (sel_out && tid == 0) {
+    // chunk score = (1/C) w_s . (column sums of [Q ; K]) + b_s; ties to softmax
+    // (done last: no warp waits for it)
+    const float a = ((red[0] + red[1]) + (red[2] + red[3])) * (1.0f / C) + red[8];
+    const float bb = ((red[4] + red[5]) + (red[6] + red[7])) * (1.0f / C) + red[9];
+    sel_out[blk] = (a >= bb) ? 0 : 1;
   }
 }
 
