@@ -47,6 +47,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-x-path", action="store_true", help="skip the layer-with-projections measurement")
     return ap.parse_args()
 
 
@@ -426,6 +427,10 @@ def run_native(args, rank, world, local_rank):
         "e2e": e2e,
         "clocks": clk,
     }
+    # ---- the layer with its projections (nats_hybrid_fwd_x), same shapes,
+    # hidden = H d = 2048: tokens/s of the whole model layer ----
+    if not args.no_x_path:
+        res["x_path"] = run_x_path(args, rank, dev, stream, dist)
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
     if not args.no_cpu_baseline and world == 1 and rank == 0:
         cores = cpu_cores()
@@ -435,6 +440,66 @@ def run_native(args, rank, world, local_rank):
                                "sample": f"{n} of {B * H} (b,h) heads of the workload, all {L} rows "
                                          f"({dt:.1f} s wall)"}
     return res
+
+
+def run_x_path(args, rank, dev, stream, dist):
+    """Times nats_hybrid_fwd_x: x [B, L, hidden] -> y, through the C ABI, inputs
+    resident in HBM (K steps after warm-up, CUDA events, max over ranks)."""
+    import numpy as np
+    import torch
+
+    import gen
+    import linear_attention_nats_gb300 as nats
+    from linear_attention_nats_gb300 import _native
+
+    cfg = dict(gen.X_CONFIGS["x_l8192"])
+    cfg["seed"] = rank_seed(cfg["seed"], rank)
+    xi = gen.make_x_inputs(name="x_l8192", **cfg)
+
+    def bf(a):
+        return torch.from_numpy(gen.bf16_bits(np.ascontiguousarray(a, np.float32)).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+
+    def f(a):
+        return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+
+    B, H, L, d, hidden = xi.B, xi.H, xi.L, xi.d, xi.hidden
+    t = dict(x=bf(xi.x), w_qkv=bf(xi.w_qkv), w_ab=bf(xi.w_ab), w_o=bf(xi.w_o), b_a=f(xi.b_a),
+             a_scale=f(xi.a_scale), b_b=f(xi.b_b), w_s=f(xi.w_s), b_s=f(xi.b_s), w_g=f(xi.w_g), b_g=f(xi.b_g))
+    y = torch.empty((B, L, hidden), dtype=torch.bfloat16, device=dev)
+    dm = nats.dims(B, H, L, d, nats.NATS_BF16)
+    wsb = int(_native.lib.nats_x_workspace_size(ctypes.byref(dm), hidden))
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    P = lambda v: ctypes.c_void_p(v.data_ptr())
+
+    def call():
+        code = _native.lib.nats_hybrid_fwd_x(
+            ctypes.byref(dm), hidden, P(t["x"]), P(t["w_qkv"]), P(t["w_ab"]), P(t["b_a"]), P(t["a_scale"]),
+            P(t["b_b"]), P(t["w_s"]), P(t["b_s"]), P(t["w_g"]), P(t["b_g"]), P(t["w_o"]), P(y), None, P(ws),
+            ctypes.c_size_t(wsb), ctypes.c_void_p(stream.cuda_stream))
+        if code != 0:
+            raise _native.NatsError(code, "nats_hybrid_fwd_x")
+
+    for _ in range(max(args.warmup, 1)):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
+    world = dist.get_world_size() if dist is not None else 1
+    gemm_flops = 2.0 * B * L * hidden * (3 * H * d + 2 * H) + 2.0 * B * L * H * d * hidden
+    return {"what": "nats_hybrid_fwd_x: x -> [q|k|v], [a|b] (cuBLAS GEMMs), head split + key norm + gates, "
+                    "the layer, output projection (cuBLAS)",
+            "config": {"B": B, "H": H, "L": L, "d": d, "hidden": hidden},
+            "value": job_throughput(B * L, world, ms), "unit": "tokens/s", "ms_per_step": ms,
+            "projection_gemm_flops_per_step": gemm_flops}
 
 
 def main():

@@ -13,4 +13,8 @@ from .synth import (  # noqa: F401
     make_inputs,
     round_to_bf16,
     bf16_bits,
+    NatsXInputs,
+    X_CONFIGS,
+    make_x_inputs,
+    x_config_inputs,
 )

@@ -271,3 +271,59 @@ def config_inputs(name: str) -> NatsInputs:
     """The named workload (see CONFIGS)."""
     cfg = dict(CONFIGS[name])
     return make_inputs(name=name, **cfg)
+
+
+@dataclasses.dataclass
+class NatsXInputs:
+    """Hidden states and projection weights of the layer with its projections
+    (bf16-representable float32 where the layer takes bf16)."""
+
+    name: str
+    B: int
+    H: int
+    L: int
+    d: int
+    hidden: int
+    x: np.ndarray  # [B, L, hidden]
+    w_qkv: np.ndarray  # [hidden, 3 H d]
+    w_ab: np.ndarray  # [hidden, 2 H]
+    b_a: np.ndarray  # [H]
+    a_scale: np.ndarray  # [H]
+    b_b: np.ndarray  # [H]
+    w_s: np.ndarray  # [H, 2, 2d]
+    b_s: np.ndarray  # [H, 2]
+    w_g: np.ndarray  # [H, d]
+    b_g: np.ndarray  # [H]
+    w_o: np.ndarray  # [H d, hidden]
+
+
+def make_x_inputs(B: int, H: int, L: int, d: int, hidden: int, seed: int = 0, name: str = "",
+                  score_scale: float = 0.5) -> NatsXInputs:
+    """x ~ N(0, 1); projection weights ~ N(0, 1 / fan_in) so that q, k', v,
+    a, b come out ~ N(0, 1); a_scale 0.1 (log-decays like the layer's own
+    workloads); score weights ~ N(0, score_scale^2), gate weights
+    ~ N(0, 0.02^2).  bf16 tensors are rounded in place (RNE)."""
+    rng = _rng(seed, 101)
+    x = round_to_bf16(_normal(rng, (B, L, hidden)))
+    w_qkv = round_to_bf16(_normal(rng, (hidden, 3 * H * d), 1.0 / np.sqrt(hidden)))
+    w_ab = round_to_bf16(_normal(rng, (hidden, 2 * H), 1.0 / np.sqrt(hidden)))
+    w_s = _normal(rng, (H, 2, 2 * d), score_scale)
+    w_g = _normal(rng, (H, d), 0.02)
+    w_o = round_to_bf16(_normal(rng, (H * d, hidden), 1.0 / np.sqrt(H * d)))
+    return NatsXInputs(
+        name=name, B=B, H=H, L=L, d=d, hidden=hidden, x=x, w_qkv=w_qkv, w_ab=w_ab,
+        b_a=np.zeros(H, np.float32), a_scale=np.full(H, 0.1, np.float32), b_b=np.zeros(H, np.float32),
+        w_s=w_s, b_s=np.zeros((H, 2), np.float32), w_g=w_g, b_g=np.zeros(H, np.float32), w_o=w_o)
+
+
+X_CONFIGS = {
+    "x_tiny": dict(B=1, H=2, L=256, d=64, hidden=128, seed=11),
+    "x_small": dict(B=2, H=4, L=1024, d=128, hidden=512, seed=12),
+    # the 1.3B-scale layer of the main workload (hidden = H d = 2048)
+    "x_l8192": dict(B=4, H=16, L=8192, d=128, hidden=2048, seed=13),
+}
+
+
+def x_config_inputs(name: str) -> NatsXInputs:
+    cfg = dict(X_CONFIGS[name])
+    return make_x_inputs(name=name, **cfg)

@@ -191,6 +191,45 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
                                      float* o_lin_out, void* workspace, size_t workspace_bytes,
                                      nats_stream_t stream, nats_profile* prof);
 
+/* ---- The projections around the layer ------------------------------------
+ * The layer above takes Q, K, V and the gates; a model layer makes them
+ * from its hidden states x and maps the output back ("Neural Attention
+ * Search Linear (NAtS-L)", technical summary, "Kernmechanismen" item 4:
+ * the merge weights come from Q projections; the projections themselves
+ * are not spelled out, so this follows the plain Gated DeltaNet form and
+ * the definitions below are the reading).  bf16 only (dims->dtype must be
+ * NATS_BF16), d = dims->dk = dims->dv, H = dims->H.  Per token t (row of x):
+ *   [q_t | k'_t | v_t] = bf16(x_t W_qkv), head h at columns h d .. h d + d - 1
+ *                        of each third;
+ *   k_t = bf16(k'_t / |k'_t|) per head (|0| gives k = 0);
+ *   [a_t | b_t] = x_t W_ab (fp32, not rounded);
+ *   g_t,h    = -a_scale[h] softplus(a_t,h + b_a[h])   (log-decay, <= 0)
+ *   beta_t,h = sigmoid(b_t,h + b_b[h]);
+ *   o = the layer (nats_hybrid_fwd with w_s, b_s, w_g, b_g), bf16;
+ *   y_t = bf16(sum_h o_t,h W_o[h d .. h d + d - 1, :]).
+ * The three products are plain GEMMs (cuBLAS, fp32 accumulate); the
+ * head split, the key normalisation and the gates are one kernel.
+ *   hidden       width of x and y (multiple of 8)
+ *   x            [B, L, hidden] bf16
+ *   w_qkv        [hidden, 3 H d] bf16, row-major
+ *   w_ab         [hidden, 2 H] bf16, row-major (column h: a of head h,
+ *                column H + h: b of head h)
+ *   b_a, b_b     [H] fp32 or NULL (zero); a_scale [H] fp32 or NULL (one)
+ *   w_s .. b_g   as for nats_hybrid_fwd
+ *   w_o          [H d, hidden] bf16, row-major
+ *   y            [B, L, hidden] bf16 (output)
+ *   sel_out      [B, H, N] u8 or NULL: the chunk selection
+ *   workspace    device scratch of at least nats_x_workspace_size(dims, hidden)
+ * Errors as nats_hybrid_fwd; NATS_ERR_SHAPE if hidden <= 0 or hidden % 8,
+ * NATS_ERR_CUDA if a cuBLAS call fails.  The library keeps one cuBLAS handle
+ * per device, created on first use; calls are serialised around it. */
+size_t nats_x_workspace_size(const nats_dims* dims, int32_t hidden);
+nats_status nats_hybrid_fwd_x(const nats_dims* dims, int32_t hidden, const void* x, const void* w_qkv,
+                              const void* w_ab, const float* b_a, const float* a_scale, const float* b_b,
+                              const float* w_s, const float* b_s, const float* w_g, const float* b_g,
+                              const void* w_o, void* y, uint8_t* sel_out, void* workspace,
+                              size_t workspace_bytes, nats_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,7 +16,7 @@ import torch
 from . import _native
 from ._native import NATS_BF16, NATS_F32, NatsError, check, dims  # noqa: F401
 
-__all__ = ["select", "hybrid_fwd", "workspace_size", "NatsError", "dims", "NATS_BF16", "NATS_F32"]
+__all__ = ["select", "hybrid_fwd", "hybrid_fwd_x", "workspace_size", "NatsError", "dims", "NATS_BF16", "NATS_F32"]
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -137,3 +137,40 @@ def hybrid_fwd(q, k, v, g, beta, w_s, b_s, w_g, b_g=None, *, norm_w_soft=None, n
         res["o_soft"] = o_soft
         res["o_lin"] = o_lin
     return res
+
+
+def hybrid_fwd_x(x, w_qkv, w_ab, w_s, b_s, w_g, b_g=None, *, heads: int, b_a=None, a_scale=None, b_b=None,
+                 w_o, y=None, workspace=None, return_sel: bool = False, stream=None):
+    """The layer with its projections: x [B, L, hidden] bf16 -> y [B, L, hidden] bf16.
+
+    w_qkv: bf16 [hidden, 3 H d]; w_ab: bf16 [hidden, 2 H]; b_a, a_scale, b_b:
+    fp32 [H] or None; w_s, b_s, w_g, b_g as for hybrid_fwd; w_o: bf16
+    [H d, hidden].  The definitions are those of nats_hybrid_fwd_x in
+    include/nats.h.  Returns y, or {"y": y, "sel": sel} with return_sel."""
+    _req(x, "x", torch.bfloat16)
+    B, L, hidden = x.shape
+    H = int(heads)
+    d = w_qkv.shape[1] // (3 * H)
+    N = L // 64
+    _req(w_qkv, "w_qkv", torch.bfloat16, (hidden, 3 * H * d))
+    _req(w_ab, "w_ab", torch.bfloat16, (hidden, 2 * H))
+    for name, t in (("b_a", b_a), ("a_scale", a_scale), ("b_b", b_b), ("b_g", b_g)):
+        _req(t, name, torch.float32, (H,))
+    _req(w_s, "w_s", torch.float32, (H, 2, 2 * d))
+    _req(b_s, "b_s", torch.float32, (H, 2))
+    _req(w_g, "w_g", torch.float32, (H, d))
+    _req(w_o, "w_o", torch.bfloat16, (H * d, hidden))
+    dm = dims(B, H, L, d, NATS_BF16)
+    if y is None:
+        y = torch.empty((B, L, hidden), dtype=torch.bfloat16, device=x.device)
+    _req(y, "y", torch.bfloat16, (B, L, hidden))
+    need = int(_native.lib.nats_x_workspace_size(ctypes.byref(dm), hidden))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    _req(workspace, "workspace", torch.uint8)
+    sel = torch.empty((B, H, N), dtype=torch.uint8, device=x.device) if return_sel else None
+    check(_native.lib.nats_hybrid_fwd_x(
+        ctypes.byref(dm), hidden, _p(x), _p(w_qkv), _p(w_ab), _p(b_a), _p(a_scale), _p(b_b), _p(w_s), _p(b_s),
+        _p(w_g), _p(b_g), _p(w_o), _p(y), _p(sel), _p(workspace), ctypes.c_size_t(workspace.numel()),
+        _stream(stream)), "nats_hybrid_fwd_x")
+    return {"y": y, "sel": sel} if return_sel else y

@@ -159,3 +159,64 @@ def forward_inputs(inp, **kw):
 def select_inputs(inp, threads: int = 0):
     """select() on a gen.NatsInputs workload."""
     return select(inp.q, inp.k, inp.w_s, inp.b_s, chunk=inp.chunk, threads=threads)
+
+
+def _bf16(a):
+    """Round to the nearest bf16 value (ties to even), returned as float64.
+
+    The value goes through float32 first (round to nearest), then keeps the
+    top 16 bits of its encoding with round-to-nearest-even on the rest."""
+    f = np.ascontiguousarray(np.asarray(a, np.float64).astype(np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def _softplus(z):
+    return np.where(z > 20.0, z, np.log1p(np.exp(np.minimum(z, 20.0))))
+
+
+def project(x, w_qkv, w_ab, heads, *, b_a=None, a_scale=None, b_b=None):
+    """Inputs of the layer from hidden states x [B, L, hidden] (fp64 products).
+
+    The projections are not spelled out by the pages ("Kernmechanismen"
+    item 4 only says the merge weights come from projections of the query);
+    the reading is the plain Gated DeltaNet form:
+      [q | k' | v] = bf16(x W_qkv), head h at columns h d .. h d + d - 1;
+      k = bf16(k' / |k'|) per head (a zero k' stays zero);
+      [a | b] = x W_ab;  g = -a_scale softplus(a + b_a);  beta = sigmoid(b + b_b).
+    Returns q, k, v [B, H, L, d] and g, beta [B, H, L] (float64)."""
+    x = np.asarray(x, np.float64)
+    B, L, hidden = x.shape
+    H = int(heads)
+    P = x.reshape(B * L, hidden) @ np.asarray(w_qkv, np.float64)
+    d = P.shape[1] // (3 * H)
+    P = P.reshape(B, L, 3, H, d).transpose(2, 0, 3, 1, 4)  # part, B, H, L, d
+    q, kr, v = _bf16(P[0]), _bf16(P[1]), _bf16(P[2])
+    nrm = np.sqrt((kr * kr).sum(-1, keepdims=True))
+    k = _bf16(np.where(nrm > 0, kr / np.where(nrm > 0, nrm, 1.0), 0.0))
+    AB = (x.reshape(B * L, hidden) @ np.asarray(w_ab, np.float64)).reshape(B, L, 2, H).transpose(2, 0, 3, 1)
+    zero = np.zeros(H)
+    b_a = zero if b_a is None else np.asarray(b_a, np.float64)
+    b_b = zero if b_b is None else np.asarray(b_b, np.float64)
+    a_scale = np.ones(H) if a_scale is None else np.asarray(a_scale, np.float64)
+    g = -a_scale[None, :, None] * _softplus(AB[0] + b_a[None, :, None])
+    beta = 1.0 / (1.0 + np.exp(-(AB[1] + b_b[None, :, None])))
+    return q, k, v, g, beta
+
+
+def forward_x(x, w_qkv, w_ab, w_s, b_s, w_g, b_g, w_o, heads, *, b_a=None, a_scale=None, b_b=None,
+              threads: int = 0):
+    """The layer with its projections, float64: y = bf16(o_flat W_o) where o is
+    the layer output (rounded to bf16, as the layer emits it) with the heads of
+    a token side by side.  Returns {"y": [B, L, hidden], "sel": [B, H, N],
+    "scores": [B, H, N, 2], "q", "k", "v", "g", "beta", "o"}."""
+    q, k, v, g, beta = project(x, w_qkv, w_ab, heads, b_a=b_a, a_scale=a_scale, b_b=b_b)
+    B, H, L, d = q.shape
+    r = forward(q, k, v, g, beta, w_s, b_s, w_g, b_g, outputs=("sel", "scores", "out"), threads=threads)
+    o = _bf16(r["out"]).reshape(B, H, L, d)
+    of = o.transpose(0, 2, 1, 3).reshape(B * L, H * d)
+    y = _bf16(of @ np.asarray(w_o, np.float64)).reshape(B, L, -1)
+    N = r["sel"].shape[-1]
+    return {"y": y, "sel": r["sel"].reshape(B, H, N), "scores": r["scores"].reshape(B, H, N, 2),
+            "q": q, "k": k, "v": v, "g": g, "beta": beta, "o": o}

@@ -120,3 +120,17 @@ def test_empty_is_a_no_op(nat):
     # zero extents return NATS_OK without touching any pointer (all NULL here)
     for B, H, L in ((0, 2, 256), (1, 0, 256), (1, 2, 0)):
         assert _fwd(nat, nat.dims(B, H, L, 64)) == 0
+
+
+def test_x_path_validation(nat):
+    # the layer with its projections: argument checks before any launch
+    dm = nat.dims(1, 2, 256, 64)
+    assert nat.lib.nats_x_workspace_size(ctypes.byref(dm), 100) == 0  # hidden % 8
+    assert nat.lib.nats_x_workspace_size(ctypes.byref(dm), 128) > nat.lib.nats_workspace_size(ctypes.byref(dm))
+    f32 = nat.dims(1, 2, 256, 64, 1)
+    null = [None] * 14
+    assert nat.lib.nats_hybrid_fwd_x(ctypes.byref(f32), 128, *null, ctypes.c_size_t(0), None) == 3
+    assert nat.lib.nats_hybrid_fwd_x(ctypes.byref(dm), 100, *null, ctypes.c_size_t(0), None) == 2
+    assert nat.lib.nats_hybrid_fwd_x(ctypes.byref(dm), 128, *null, ctypes.c_size_t(0), None) == 1
+    bad = nat.dims(1, 2, 100, 64)  # L % 64
+    assert nat.lib.nats_hybrid_fwd_x(ctypes.byref(bad), 128, *null, ctypes.c_size_t(0), None) == 2
