@@ -94,9 +94,9 @@ def kernel_work(B, H, L, d, flops_softmax):
     softmax: 4 d FLOP per visible (query, key) pair (tensor-bound).  The
     others are HBM-bound; their bytes are the unique I/O the stage has to
     move (bf16 activations, fp32 g, beta, G, gate, o_l):
-      gdn_prep per chunk: read Q, K, V, g, beta; write W, U^T, Q~, K~ (bf16
-        C x d each), P (bf16 C x C), gate and G;
-      gdn_scan per chunk: read W, U^T, Q~, K~, P, G; write o_l (bf16 C x d);
+      gdn_prep per chunk: read Q, K, V, g, beta; write W, U^T (bf16 C x d
+        each), P (bf16 C x C), gate and G;
+      gdn_scan per chunk: read W, U^T, Q, K, P, G; write o_l (bf16 C x d);
       merge per row: read o_l (bf16), gate, out (bf16); write out;
       score per chunk: read Q, K (only when a separate score pass runs).
     The softmax kernel and the scan run concurrently on two streams, so
@@ -104,11 +104,11 @@ def kernel_work(B, H, L, d, flops_softmax):
     the GPU with the other."""
     N = L // C
     chunks, rows = B * H * N, B * H * L
-    prep = 3 * C * d * 2 + 2 * C * 4 + 4 * C * d * 2 + C * C * 2 + 2 * C * 4
+    prep = 3 * C * d * 2 + 2 * C * 4 + 2 * C * d * 2 + C * C * 2 + 2 * C * 4
     scan = 4 * C * d * 2 + C * C * 2 + C * 4 + C * d * 2
     return {
         "softmax": ("tensor", float(flops_softmax), "softmax_tc.cu"),
-        "gdn_prep": ("hbm", float(chunks * prep), "gdn_prep_mma.cu"),
+        "gdn_prep": ("hbm", float(chunks * prep), "gdn_prep_tc.cu" if d == 128 else "gdn_prep_mma.cu"),
         "gdn_scan": ("hbm", float(chunks * scan), "gdn_scan_tc.cu"),
         "merge": ("hbm", float(rows * (d * 2 + 4 + 2 * d * 2)), "merge.cu"),
         "score": ("hbm", float(chunks * 2 * C * d * 2), "select.cu"),

@@ -80,6 +80,11 @@ typedef struct {
 /* Human-readable name of a status code (static storage). */
 const char* nats_status_string(nats_status s);
 
+/* The CUDA runtime's description of the last CUDA error a libnats call on
+ * this host thread met (the cause behind its NATS_ERR_CUDA), or "no error".
+ * Static storage; only the calling thread's own calls update it. */
+const char* nats_last_cuda_error(void);
+
 /* Bytes of device workspace nats_hybrid_fwd needs for `dims` (0 for an
  * invalid `dims`).  The workspace holds the selection, the compacted
  * softmax-chunk lists, the per-chunk Gated DeltaNet factors and both branch

@@ -23,7 +23,7 @@ STATUS = {
 }
 
 # Every symbol include/nats.h declares.
-EXPORTS = ("nats_status_string", "nats_workspace_size", "nats_workspace_check", "nats_select",
+EXPORTS = ("nats_status_string", "nats_last_cuda_error", "nats_workspace_size", "nats_workspace_check", "nats_select",
            "nats_hybrid_fwd", "nats_hybrid_fwd_profiled", "nats_hybrid_fwd_noalloc", "nats_x_workspace_size",
            "nats_hybrid_fwd_x")
 
@@ -49,7 +49,10 @@ class Dims(ctypes.Structure):
 class NatsError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where}: {STATUS.get(code, code)}")
+        msg = f"{where}: {STATUS.get(code, code)}"
+        if code == 7 and _lib is not None:  # NATS_ERR_CUDA: add the CUDA runtime's reason
+            msg += f" ({_lib.nats_last_cuda_error().decode()})"
+        super().__init__(msg)
 
 
 def _load() -> ctypes.CDLL:
@@ -58,6 +61,8 @@ def _load() -> ctypes.CDLL:
             f"libnats.so is not built ({LIB_PATH}); run `python -c 'import __graft_entry__ as g; g.build()'`")
     lib = ctypes.CDLL(LIB_PATH)
     P = ctypes.c_void_p
+    lib.nats_last_cuda_error.argtypes = []
+    lib.nats_last_cuda_error.restype = ctypes.c_char_p
     lib.nats_status_string.argtypes = [ctypes.c_int]
     lib.nats_status_string.restype = ctypes.c_char_p
     lib.nats_workspace_size.argtypes = [ctypes.POINTER(Dims)]

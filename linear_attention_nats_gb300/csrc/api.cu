@@ -66,15 +66,20 @@ size_t layout(const Problem& p, char* base, Workspace* ws) {
   w.P = (float*)take(4 * BH * N * C * C);
   w.o_s = (float*)take(4 * BH * L * D);
   w.o_l = (float*)take(4 * BH * L * D);
-  w.Qt = (void*)take(2 * BH * L * D);
-  w.Kt = (void*)take(2 * BH * L * D);
   w.gate = (float*)take(4 * BH * L);
   w.err = (int*)take(16);
   if (ws) *ws = w;
   return off;
 }
 
-nats_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NATS_OK : NATS_ERR_CUDA; }
+// last CUDA error a libnats call on this host thread met
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+nats_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return NATS_OK;
+  g_last_cuda_error = e;
+  return NATS_ERR_CUDA;
+}
 
 // Optional per-stage event records around each launch group.
 struct Stages {
@@ -154,6 +159,8 @@ const char* nats_status_string(nats_status s) {
   return "unknown nats_status";
 }
 
+const char* nats_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda_error); }
+
 size_t nats_workspace_size(const nats_dims* dims) {
   if (check_dims(dims) != NATS_OK) return 0;
   return layout(problem_of(dims), nullptr, nullptr);
@@ -212,6 +219,9 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
   cudaStream_t st = (cudaStream_t)stream;
   const int dt = dims->dtype;
   Stages stg{prof, st};
+  // err[0]: bounded-wait flag; err[1]: tile counter of the softmax kernel's
+  // dynamic schedule.  Both start at zero before the first kernel runs.
+  if (cudaMemsetAsync(ws.err, 0, 2 * sizeof(int), st) != cudaSuccess) return NATS_ERR_CUDA;
 
   // 1. selection (score layer, or the caller's override).  With bf16 inputs
   //    the chunk-factor kernel scores the chunks from the Q and K it stages.
@@ -225,13 +235,18 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
   }
   if (dt == NATS_BF16) {
     // 2. Gated DeltaNet chunk factors, the per-token merge gate (and the selection)
-    NATS_STAGE(stg, NATS_STAGE_GDN_PREP, 1,
-               launch_gdn_prep_mma(p, q, k, v, g, beta, w_g, b_g, ws.G, ws.W, ws.U, ws.P, ws.Qt, ws.Kt,
-                                   ws.gate, w_s, b_s, score_dst, st));
+    if (p.d == 128)
+      NATS_STAGE(stg, NATS_STAGE_GDN_PREP, 1,
+                 launch_gdn_prep_tc(p, q, k, v, g, beta, w_g, b_g, ws.G, ws.W, ws.U, ws.P, ws.gate, w_s, b_s,
+                                    score_dst, ws.err, st));
+    else
+      NATS_STAGE(stg, NATS_STAGE_GDN_PREP, 1,
+                 launch_gdn_prep_mma(p, q, k, v, g, beta, w_g, b_g, ws.G, ws.W, ws.U, ws.P, ws.gate, w_s, b_s,
+                                     score_dst, st));
   }
   // 3. compacted softmax-chunk lists (mirrors an overridden selection to sel_out)
   NATS_STAGE(stg, NATS_STAGE_COMPACT, 1,
-             launch_compact(p, sel, ws.nprev, ws.sel_idx, (sel_in && sel_out) ? sel_out : nullptr, ws.err, st));
+             launch_compact(p, sel, ws.nprev, ws.sel_idx, (sel_in && sel_out) ? sel_out : nullptr, st));
   if (dt == NATS_BF16) {
     // 4. Gated DeltaNet chunk scan with commit / rollback (caller's stream)
     // 5. softmax branch, concurrently on the side stream (in order on the
@@ -252,8 +267,7 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
         ss = sd->s;
       }
       NATS_STAGE(stg, NATS_STAGE_GDN_SCAN, 1,
-                 launch_gdn_scan_tc(p, ws.Kt, sel, ws.G, ws.W, ws.U, ws.P, ws.Qt, o_l, o_l16, state_out, ws.err,
-                                    st));
+                 launch_gdn_scan_tc(p, q, k, sel, ws.G, ws.W, ws.U, ws.P, o_l, o_l16, state_out, ws.err, st));
       Stages stg_side{prof, ss};
       NATS_STAGE(stg_side, NATS_STAGE_SOFTMAX, 1,
                  launch_softmax_tc(p, q, k, v, ws.nprev, ws.sel_idx, sel, ws.gate, norm_w_soft, out, o_soft_out,

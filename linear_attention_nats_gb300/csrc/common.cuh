@@ -55,11 +55,9 @@ struct Workspace {
   float* P;          // [BH, N, C, C]   lower(e^{G_t - G_i} scale q_t . k_i)
   float* o_s;        // [BH, L, dv] softmax branch output (before norm)
   float* o_l;        // [BH, L, dv] Gated DeltaNet branch output (before norm)
-  void* Qt;          // [BH, L, dk] bf16 diag(scale e^G) Q, per chunk (bf16 path)
-  void* Kt;          // [BH, L, dk] bf16 diag(e^{G_C - G}) K, per chunk (bf16 path)
   float* gate;       // [BH, L] merge weight w = sigmoid(q . W_g + b_g) (bf16 path)
   int* err;          // [0] set by a kernel whose bounded wait expired; [1] softmax tile counter
-                     // (both zeroed per call by the compaction kernel)
+                     // (both zeroed at the start of each call)
 };
 
 }  // namespace nats

@@ -11,11 +11,8 @@
 // (fp32 accumulate); the unit-lower-triangular inverse is fp32, blocked in
 // 16 x 16 tiles.  Outputs (the operands of the chunk scan): W bf16
 // [chunk][64][D]; U transposed, bf16 [chunk][D][64]; P bf16 [chunk][64][64];
-// Q~ = diag(scale e^G) Q, bf16 [chunk][64][D] (the query with its readout
-// decay and scale folded in); K~ = diag(e^{G_C - G}) K, bf16 [chunk][64][D]
-// (the key with the decay to the chunk end folded in); G fp32; and the merge
-// gate of each token, w = sigmoid(q . W_g[h] + b_g[h]) ("Kernmechanismen"
-// item 4: weights generated from the query), fp32.
+// G fp32; and the merge gate of each token, w = sigmoid(q . W_g[h] + b_g[h])
+// ("Kernmechanismen" item 4: weights generated from the query), fp32.
 // Optionally it also scores the chunk ("Kernmechanismen" item 1: mean pool of
 // [q ; k] over the chunk, one linear score per operation, the higher score
 // wins, ties to softmax), from the Q and K it has staged anyway, so the
@@ -111,8 +108,7 @@ __global__ void __launch_bounds__(256, 2) gdn_prep_mma_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
     const __nv_bfloat16* __restrict__ v, const float* __restrict__ g, const float* __restrict__ beta, int L,
     int N, float scale, float* __restrict__ Gout, __nv_bfloat16* __restrict__ Wout,
-    __nv_bfloat16* __restrict__ Uout, __nv_bfloat16* __restrict__ Pout, __nv_bfloat16* __restrict__ Qtout,
-    __nv_bfloat16* __restrict__ Ktout, const float* __restrict__ w_g, const float* __restrict__ b_g, int H,
+    __nv_bfloat16* __restrict__ Uout, __nv_bfloat16* __restrict__ Pout, const float* __restrict__ w_g, const float* __restrict__ b_g, int H,
     float* __restrict__ gate_out, const float* __restrict__ w_s, const float* __restrict__ b_s,
     uint8_t* __restrict__ sel_out) {
   using S = PrepSmem<D>;
@@ -229,8 +225,8 @@ __global__ void __launch_bounds__(256, 2) gdn_prep_mma_kernel(
   // above, and each synchronises on its own named barrier (every thread of a
   // group reaches every barrier of its group)
   if (warp >= 4) {
-    // warps 4-7: merge gate, Q~ / K~ with the column sums of Q and K for the
-    // chunk score, then V rows *= beta and K rows *= beta e^G
+    // warps 4-7: merge gate, the column sums of Q and K for the chunk score,
+    // then V rows *= beta and K rows *= beta e^G
     const int t4 = tid - 128;
     {
       // merge gate: two threads per token, D/2 features each
@@ -252,38 +248,26 @@ __global__ void __launch_bounds__(256, 2) gdn_prep_mma_kernel(
       if (hh == 0) gate_out[tok0 + t] = 1.f / (1.f + __expf(-(z + (b_g ? b_g[h] : 0.f))));
     }
     {
-      // Q~ = diag(scale e^G) Q and K~ = diag(e^{G_C - G}) K -> global (16-byte
-      // stores); a thread keeps one 8-column group x = t4 % VPR over its rows
-      __nv_bfloat16* Qt = Qtout + tok0 * D;
-      __nv_bfloat16* Kt = Ktout + tok0 * D;
-      const float GC = Gs[C - 1];
+      // column sums of Q and K for the chunk score; a thread keeps one
+      // 8-column group x = t4 % VPR over its rows
       float cs[16];
 #pragma unroll
       for (int x = 0; x < 16; ++x) cs[x] = 0.f;
       for (int e = t4; e < C * VPR; e += 128) {
         const int t = e / VPR, x = e % VPR;
-        const float fq = scale * __expf(Gs[t]);
-        const float fk = __expf(GC - Gs[t]);
         const uint4 inq = *(const uint4*)(Qs + t * RS + x * 8);
         const uint4 ink = *(const uint4*)(Ks + t * RS + x * 8);
         const __nv_bfloat162* hq = (const __nv_bfloat162*)&inq;
         const __nv_bfloat162* hk = (const __nv_bfloat162*)&ink;
-        uint4 oq, ok;
-        uint32_t* q32 = (uint32_t*)&oq;
-        uint32_t* k32 = (uint32_t*)&ok;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float2 vq = __bfloat1622float2(hq[i]);
           const float2 vk = __bfloat1622float2(hk[i]);
-          q32[i] = pack2(vq.x * fq, vq.y * fq);
-          k32[i] = pack2(vk.x * fk, vk.y * fk);
           cs[2 * i] += vq.x;
           cs[2 * i + 1] += vq.y;
           cs[8 + 2 * i] += vk.x;
           cs[8 + 2 * i + 1] += vk.y;
         }
-        *(uint4*)(Qt + t * D + x * 8) = oq;
-        *(uint4*)(Kt + t * D + x * 8) = ok;
       }
       if (sel_out) {
         // chunk score, linear in the column sums: combine the threads of the
@@ -315,7 +299,7 @@ __global__ void __launch_bounds__(256, 2) gdn_prep_mma_kernel(
     }
     if (t4 < C) Bg[t4] = Bs[t4] * __expf(Gs[t4]);
     named_barrier(2, 128);
-    // V rows *= beta, K rows *= beta e^G (in place, 8 columns per step; K~ is out)
+    // V rows *= beta, K rows *= beta e^G (in place, 8 columns per step)
     for (int e = t4; e < C * VPR; e += 128) {
       const int t = e / VPR, x8 = (e % VPR) * 8;
       const float fb = Bs[t], fg = Bg[t];
@@ -496,16 +480,16 @@ __global__ void __launch_bounds__(256, 2) gdn_prep_mma_kernel(
 
 cudaError_t launch_gdn_prep_mma(const Problem& p, const void* q, const void* k, const void* v, const float* g,
                                 const float* beta, const float* w_g, const float* b_g, float* G, void* W16,
-                                void* U16, void* P16, void* Qt16, void* Kt16, float* gate, const float* w_s,
-                                const float* b_s, uint8_t* sel_out, cudaStream_t st) {
+                                void* U16, void* P16, float* gate, const float* w_s, const float* b_s,
+                                uint8_t* sel_out, cudaStream_t st) {
   if (p.BH == 0 || p.N == 0) return cudaSuccess;
   auto run = [&](auto kern, int smem) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)(p.BH * p.N), 256, smem, st>>>(
         (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, g, beta, p.L, p.N, p.scale,
-        G, (__nv_bfloat16*)W16, (__nv_bfloat16*)U16, (__nv_bfloat16*)P16, (__nv_bfloat16*)Qt16,
-        (__nv_bfloat16*)Kt16, w_g, b_g, p.H, gate, w_s, b_s, sel_out);
+        G, (__nv_bfloat16*)W16, (__nv_bfloat16*)U16, (__nv_bfloat16*)P16, w_g, b_g, p.H, gate, w_s, b_s,
+        sel_out);
     return cudaGetLastError();
   };
   return p.d == 64 ? run(gdn_prep_mma_kernel<64>, PrepSmem<64>::kBytes)

@@ -6,7 +6,8 @@
 // chunk; for a chunk that chose softmax it is rolled back to the chunk start.
 // With the phase-1 factors of a chunk (S0 = state at its start, dv x dk;
 // G = in-chunk cumulative log-decay, gamma = e^G; Q~ = diag(scale gamma) Q;
-// K~ = diag(gamma_C / gamma) K):
+// K~ = diag(gamma_C / gamma) K, both formed here in shared memory from the
+// chunk's Q and K tiles):
 //   Delta^T = U^T - S0 W^T                    (dv x 64)
 //   O^T     = S0 Q~^T + Delta^T P^T           (dv x 64)
 //   S_C     = gamma_C S0 + Delta^T K~         (linear chunks only)
@@ -23,10 +24,12 @@
 //   MMA2  O += Delta^T P^T
 //   all   O^T of chunk c - 1 -> o_l while MMA3 runs, then S -> bf16 S0 and
 //         S *= gamma_C of the next chunk when it is linear
-// Roles (320 threads): warps 0-7 elementwise, warp w owning TMEM lanes
+// Roles (448 threads): warps 0-7 elementwise, warp w owning TMEM lanes
 // 32 (w % 4) .. +31 and half (w / 4) of the columns; warp 8 TMA producer
-// (W, Q~, K~, U^T, P of coming chunks, three stages); warp 9 TMEM owner and
-// MMA issuer.  Every wait is bounded (tc::kWaitLimitNs).
+// (W, Q, K, U^T, P and G of coming chunks, three stages); warp 9 TMEM owner
+// and MMA issuer; warps 10-13 scale the staged Q and K rows in place into Q~
+// and K~ (two chunks ahead of the products that read them).  Every wait is
+// bounded (tc::kWaitLimitNs).
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -39,22 +42,27 @@ namespace {
 
 template <int D>
 struct ScanSmem {
-  static constexpr int kWQ = 128 * D * 2;  // [W; Q~] tile: 128 lines (t), D/64 halves of 16 KiB
+  static constexpr int kWQ = 128 * D * 2;  // [W; Q] tile: 128 lines (t), D/64 halves of 16 KiB
   static constexpr int kK = 64 * D * 2;    // K chunk: 64 lines (t), D/64 halves of 8 KiB
   static constexpr int kU = D * 64 * 2;    // U^T chunk: D lines (dv) x 64 cols (t), 8 KiB per 64 lines
   static constexpr int kP = 64 * 64 * 2;   // P chunk: 64 lines (t) x 64 cols (i)
   static constexpr int kStage = kWQ + kK + kU + kP;
   static constexpr int kStages = 3;  // chunks in flight: the loads run two chunks ahead
   static constexpr int offStage = 0;
-  static constexpr int offBar = kStages * kStage;
-  static constexpr int kNumBars = 13;
+  static constexpr int offG = kStages * kStage;  // fp32 [kStages][64]: G of the staged chunks
+  static constexpr int offBar = offG + kStages * 64 * 4;
+  static constexpr int kNumBars = 16;
   static constexpr int offTmem = offBar + kNumBars * 8;
   static constexpr int kBytes = offTmem + 16 + 1024;
 };
 
 // SB_OFREE + b: O^T of the chunks using O buffer b has been read (one barrier
 // per buffer, so a waiter is never two phases behind)
-enum { SB_FULL = 0, SB_EMPTY = 3, SB_S0 = 6, SB_Z = 7, SB_DELTA = 8, SB_OFREE = 9, SB_SDONE = 11, SB_DONE = 12 };
+// SB_SCALED + s: Q~ and K~ of stage s are in place
+enum {
+  SB_FULL = 0, SB_EMPTY = 3, SB_S0 = 6, SB_Z = 7, SB_DELTA = 8, SB_OFREE = 9, SB_SDONE = 11, SB_DONE = 12,
+  SB_SCALED = 13
+};
 
 // TMEM columns
 constexpr uint32_t kColXO = 0;     // two buffers of 128 columns: [S0 W^T | O^T] of chunks c % 2
@@ -69,11 +77,11 @@ __device__ __forceinline__ uint32_t sw_off(int line, int col, int half_bytes) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
     gdn_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_u,
                        const __grid_constant__ CUtensorMap tm_p, const uint8_t* __restrict__ sel,
-                       const float* __restrict__ G, int L, int N, float* __restrict__ o_l,
+                       const float* __restrict__ G, int L, int N, float scale, float* __restrict__ o_l,
                        __nv_bfloat16* __restrict__ o_l16,
                        float* __restrict__ state_out, int* __restrict__ err) {
   using S = ScanSmem<D>;
@@ -96,6 +104,7 @@ __global__ void __launch_bounds__(320, 1)
     for (int b = 0; b < 2; ++b) tc::mbar_init(&bars[SB_OFREE + b], 256);
     tc::mbar_init(&bars[SB_SDONE], 1);
     tc::mbar_init(&bars[SB_DONE], 1);
+    for (int s = 0; s < S::kStages; ++s) tc::mbar_init(&bars[SB_SCALED + s], 4);
     tc::fence_barrier_init();
   }
   if (warp == 9) {
@@ -127,7 +136,8 @@ __global__ void __launch_bounds__(320, 1)
         const int yc = (int)((bh * N + c) * 64);   // row of this chunk in W / P / Q~ / K / ...
         const int yt = (int)(bh * L + 64LL * c);   // row of this chunk in Q~ / K
         const int yu = (int)((bh * N + c) * D);    // first line of this chunk in U^T
-        tc::mbar_arrive_expect_tx(&bars[SB_FULL + s], S::kStage);
+        tc::mbar_arrive_expect_tx(&bars[SB_FULL + s], S::kStage + 64 * 4);
+        tc::bulk_load_1d(smem + S::offG + s * 256, G + yt, 256, &bars[SB_FULL + s]);
         for (int h = 0; h < D / 64; ++h) {
           tc::tma_load_2d(WQ + h * 16384, &tm_w, 64 * h, yc, &bars[SB_FULL + s]);
           tc::tma_load_2d(WQ + h * 16384 + 8192, &tm_q, 64 * h, yt, &bars[SB_FULL + s]);
@@ -163,6 +173,7 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t sb = s * S::kStage;
         const uint64_t wd = tc::desc_add(wd0, sb), kd = tc::desc_add(kd0, sb), pd = tc::desc_add(pd0, sb);
         if (!(ok = tc::mbar_wait(&bars[SB_FULL + s], (c / S::kStages) & 1, err))) break;
+        if (!(ok = tc::mbar_wait(&bars[SB_SCALED + s], (c / S::kStages) & 1, err))) break;
         if (!(ok = tc::mbar_wait(&bars[SB_S0], c & 1, err))) break;
         if (c >= 2 && !(ok = tc::mbar_wait(&bars[SB_OFREE + (c & 1)], ((c - 2) / 2) & 1, err))) break;
         tc::fence_after();
@@ -192,6 +203,47 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc::mma_commit(&bars[SB_DONE]);
       tc::mbar_wait(&bars[SB_DONE], 0, err);
+    }
+  } else if (warp >= 10) {
+    // ----------------------------------------- Q~ and K~ in place (warps 10-13)
+    // Q~_t = scale e^{G_t} q_t and K~_t = e^{G_C - G_t} k_t, rounded to bf16;
+    // a thread takes 16-byte granules (8 features of one token) of both tiles
+    constexpr int VPR = D / 8;
+    const int el = threadIdx.x - 320;
+    bool ok = true;
+    for (int c = 0; c < N && ok; ++c) {
+      const int s = c % S::kStages;
+      if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_FULL + s], (c / S::kStages) & 1, err)))) break;
+      uint8_t* Qb = smem + S::offStage + s * S::kStage + 8192;  // Q lines follow the W lines in each half
+      uint8_t* Kb = smem + S::offStage + s * S::kStage + S::kWQ;
+      const float* Gs = (const float*)(smem + S::offG + s * 256);
+      const float GC = Gs[63];
+#pragma unroll 2
+      for (int e = el; e < 64 * VPR; e += 128) {
+        const int t = e / VPR, x = e % VPR;
+        const uint32_t off = (uint32_t)(t * 128 + ((((x & 7) ^ (t & 7))) << 4));
+        const float Gt = Gs[t];
+        const float fq = scale * __expf(Gt), fk = __expf(GC - Gt);
+        uint4* pq = (uint4*)(Qb + (x >> 3) * 16384 + off);
+        uint4* pk = (uint4*)(Kb + (x >> 3) * 8192 + off);
+        const uint4 iq = *pq, ik = *pk;
+        const __nv_bfloat162* hq = (const __nv_bfloat162*)&iq;
+        const __nv_bfloat162* hk = (const __nv_bfloat162*)&ik;
+        uint4 oq, ok4;
+        uint32_t* q32 = (uint32_t*)&oq;
+        uint32_t* k32 = (uint32_t*)&ok4;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float2 a = __bfloat1622float2(hq[u]), b = __bfloat1622float2(hk[u]);
+          q32[u] = tc::pack_bf16x2(a.x * fq, a.y * fq);
+          k32[u] = tc::pack_bf16x2(b.x * fk, b.y * fk);
+        }
+        *pq = oq;
+        *pk = ok4;
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bars[SB_SCALED + s]);
     }
   } else {
     // ------------------------------------------------- elementwise (warps 0-7)
@@ -305,18 +357,17 @@ __global__ void __launch_bounds__(320, 1)
       // next linear chunk applied ahead of its MMA3
       if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[SB_SDONE], c & 1, err)))) break;
       tc::fence_after();
-      float v[SC];
-      if ((lin || lin_next) && has_row) {
-        tc::tmem_ld32_at<0>(tmem + kColS + lane_off + hf * SC, v);
-        if (SC > 32) tc::tmem_ld32_at<(SC > 32 ? 32 : 0)>(tmem + kColS + lane_off + hf * SC + 32, v);
-        tc::tmem_ld_wait();
-      }
+      // 32 state columns at a time (registers): the bf16 copy first, it is
+      // on the critical path
       if (lin && has_row) {
-#pragma unroll
+#pragma unroll 1
         for (int ch = 0; ch < SC / 32; ++ch) {
+          float v[32];
+          tc::tmem_ld32(tmem + kColS + lane_off + hf * SC + ch * 32, v);
+          tc::tmem_ld_wait();
           uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = tc::pack_bf16x2(v[ch * 32 + 2 * i], v[ch * 32 + 2 * i + 1]);
+          for (int i = 0; i < 16; ++i) pk[i] = tc::pack_bf16x2(v[2 * i], v[2 * i + 1]);
           tc::tmem_st16u(tmem + kColS0 + lane_off + (hf * SC + ch * 32) / 2, pk);
         }
         tc::tmem_st_wait();
@@ -326,10 +377,15 @@ __global__ void __launch_bounds__(320, 1)
       // the next chunk's MMA3 accumulates onto gamma_C S: scale now, off the
       // critical path (that MMA3 also waits for this thread's next Delta)
       if (lin_next && has_row) {
+#pragma unroll 1
+        for (int ch = 0; ch < SC / 32; ++ch) {
+          float v[32];
+          tc::tmem_ld32(tmem + kColS + lane_off + hf * SC + ch * 32, v);
+          tc::tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < SC; ++i) v[i] *= gnext;
-        tc::tmem_st32(tmem + kColS + lane_off + hf * SC, *reinterpret_cast<float(*)[32]>(&v[0]));
-        if (SC > 32) tc::tmem_st32(tmem + kColS + lane_off + hf * SC + 32, *reinterpret_cast<float(*)[32]>(&v[SC > 32 ? 32 : 0]));
+          for (int i = 0; i < 32; ++i) v[i] *= gnext;
+          tc::tmem_st32(tmem + kColS + lane_off + hf * SC + ch * 32, v);
+        }
         tc::tmem_st_wait();
       }
       // the loads for chunk c + 2 issued at the top are consumed only here
@@ -366,30 +422,31 @@ __global__ void __launch_bounds__(320, 1)
 }  // namespace
 
 template <int D>
-static cudaError_t launch_scan_tc_t(const Problem& p, const void* Kt16, const uint8_t* sel, const float* G,
-                                    const void* W16, const void* UT16, const void* P16, const void* Qt16,
+static cudaError_t launch_scan_tc_t(const Problem& p, const void* q, const void* k, const uint8_t* sel,
+                                    const float* G, const void* W16, const void* UT16, const void* P16,
                                     float* o_l, __nv_bfloat16* o_l16, float* state_out, int* err,
                                     cudaStream_t st) {
   CUtensorMap mw, mq, mk, mu, mp;
   const long long rows = p.BH * p.L;  // = BH * N * 64
-  if (!make_tile_map(&mw, W16, rows, D) || !make_tile_map(&mq, Qt16, rows, D) || !make_tile_map(&mk, Kt16, rows, D) ||
+  if (!make_tile_map(&mw, W16, rows, D) || !make_tile_map(&mq, q, rows, D) || !make_tile_map(&mk, k, rows, D) ||
       !make_tile_map(&mu, UT16, p.BH * (long long)p.N * D, 64) || !make_tile_map(&mp, P16, rows, 64))
     return cudaErrorInvalidValue;
   auto kern = gdn_scan_tc_kernel<D>;
   const int smem = ScanSmem<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)p.BH, 320, smem, st>>>(mw, mq, mk, mu, mp, sel, G, p.L, p.N, o_l, o_l16, state_out, err);
+  kern<<<(unsigned)p.BH, 448, smem, st>>>(mw, mq, mk, mu, mp, sel, G, p.L, p.N, p.scale, o_l, o_l16, state_out,
+                                          err);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gdn_scan_tc(const Problem& p, const void* Kt16, const uint8_t* sel, const float* G,
-                               const void* W16, const void* UT16, const void* P16, const void* Qt16, float* o_l,
-                               void* o_l16, float* state_out, int* err, cudaStream_t st) {
+cudaError_t launch_gdn_scan_tc(const Problem& p, const void* q, const void* k, const uint8_t* sel, const float* G,
+                               const void* W16, const void* UT16, const void* P16, float* o_l, void* o_l16,
+                               float* state_out, int* err, cudaStream_t st) {
   if (p.BH == 0 || p.N == 0) return cudaSuccess;
   __nv_bfloat16* ol16 = (__nv_bfloat16*)o_l16;
-  return p.d == 64 ? launch_scan_tc_t<64>(p, Kt16, sel, G, W16, UT16, P16, Qt16, o_l, ol16, state_out, err, st)
-                   : launch_scan_tc_t<128>(p, Kt16, sel, G, W16, UT16, P16, Qt16, o_l, ol16, state_out, err, st);
+  return p.d == 64 ? launch_scan_tc_t<64>(p, q, k, sel, G, W16, UT16, P16, o_l, ol16, state_out, err, st)
+                   : launch_scan_tc_t<128>(p, q, k, sel, G, W16, UT16, P16, o_l, ol16, state_out, err, st);
 }
 
 }  // namespace nats

@@ -11,7 +11,7 @@ cudaError_t launch_score(const Problem& p, int dtype, const void* q, const void*
                          const float* b_s, uint8_t* sel, float* scores, cudaStream_t st);
 
 cudaError_t launch_compact(const Problem& p, const uint8_t* sel, int32_t* nprev, int32_t* sel_idx,
-                           uint8_t* sel_copy, int* err, cudaStream_t st);
+                           uint8_t* sel_copy, cudaStream_t st);
 
 // bf16 softmax branch; its epilogue writes out = w RMSNorm(o_s) (bf16) with
 // the per-token gate w; o_s (fp32 diagnostics) may be null.
@@ -35,13 +35,20 @@ cudaError_t launch_gdn_scan_simt(const Problem& p, int dtype, const void* q, con
 // bf16 chunk factors of the Gated DeltaNet branch plus the per-token merge gate.
 cudaError_t launch_gdn_prep_mma(const Problem& p, const void* q, const void* k, const void* v, const float* g,
                                 const float* beta, const float* w_g, const float* b_g, float* G, void* W16,
-                                void* U16, void* P16, void* Qt16, void* Kt16, float* gate, const float* w_s,
-                                const float* b_s, uint8_t* sel_out, cudaStream_t st);
+                                void* U16, void* P16, float* gate, const float* w_s, const float* b_s,
+                                uint8_t* sel_out, cudaStream_t st);
+
+// The same factors (d = 128) from the persistent tcgen05 pipeline; err[0] is
+// set if one of its bounded waits expires.
+cudaError_t launch_gdn_prep_tc(const Problem& p, const void* q, const void* k, const void* v, const float* g,
+                               const float* beta, const float* w_g, const float* b_g, float* G, void* W16,
+                               void* U16, void* P16, float* gate, const float* w_s, const float* b_s,
+                               uint8_t* sel_out, int* err, cudaStream_t st);
 
 // bf16 chunk scan: o_l (fp32 [BH, L, dv]); state_out may be null.
-cudaError_t launch_gdn_scan_tc(const Problem& p, const void* Kt16, const uint8_t* sel, const float* G,
-                               const void* W16, const void* UT16, const void* P16, const void* Qt16, float* o_l,
-                               void* o_l16, float* state_out, int* err, cudaStream_t st);
+cudaError_t launch_gdn_scan_tc(const Problem& p, const void* q, const void* k, const uint8_t* sel, const float* G,
+                               const void* W16, const void* UT16, const void* P16, float* o_l, void* o_l16,
+                               float* state_out, int* err, cudaStream_t st);
 
 // bf16 path: out (holding w RMSNorm(o_s)) += (1 - w) RMSNorm(o_l).
 cudaError_t launch_merge_lin(const Problem& p, const float* o_l, const void* o_l16, const float* gate,

@@ -78,13 +78,8 @@ __global__ void __launch_bounds__(128) score_kernel(const T* __restrict__ q, con
 __global__ void __launch_bounds__(256) compact_kernel(const uint8_t* __restrict__ sel, int N,
                                                       int32_t* __restrict__ nprev,
                                                       int32_t* __restrict__ sel_idx,
-                                                      uint8_t* __restrict__ sel_copy,
-                                                      int* __restrict__ err) {
+                                                      uint8_t* __restrict__ sel_copy) {
   const long long bh = blockIdx.x;
-  if (bh == 0 && threadIdx.x == 0 && err) {
-    err[0] = 0;  // bounded-wait flag
-    err[1] = 0;  // tile counter of the softmax kernel's dynamic schedule
-  }
   const uint8_t* s = sel + bh * N;
   int32_t* np = nprev + bh * N;
   int32_t* si = sel_idx + bh * N;
@@ -133,9 +128,9 @@ cudaError_t launch_score(const Problem& p, int dtype, const void* q, const void*
 }
 
 cudaError_t launch_compact(const Problem& p, const uint8_t* sel, int32_t* nprev, int32_t* sel_idx,
-                           uint8_t* sel_copy, int* err, cudaStream_t st) {
+                           uint8_t* sel_copy, cudaStream_t st) {
   if (p.BH == 0 || p.N == 0) return cudaSuccess;
-  compact_kernel<<<(unsigned)p.BH, 256, 0, st>>>(sel, p.N, nprev, sel_idx, sel_copy, err);
+  compact_kernel<<<(unsigned)p.BH, 256, 0, st>>>(sel, p.N, nprev, sel_idx, sel_copy);
   return cudaGetLastError();
 }
 
