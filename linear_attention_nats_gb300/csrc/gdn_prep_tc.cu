@@ -91,23 +91,8 @@ constexpr int kWarpProd = 0, kWarpMma = 1, kWarpEl = 2, kWarpInv = 6, kWarpUw = 
 // named barriers (0 is __syncthreads)
 constexpr int kBarEl = 1, kBarInv = 2, kBarUw = 3, kBarEpi = 4;
 
-__device__ __forceinline__ void named_barrier(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// barrier of `count` threads that also returns whether `v` held on all of them
-__device__ __forceinline__ bool group_all(int id, int count, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.and.pred p, %2, %3, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
-}
+using tc::group_all;
+using tc::named_barrier;
 
 // D(16x8 fp32) += A(16x8 tf32, row) * B(8x8 tf32, col)
 __device__ __forceinline__ void mma1688_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
