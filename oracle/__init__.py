@@ -220,3 +220,92 @@ def forward_x(x, w_qkv, w_ab, w_s, b_s, w_g, b_g, w_o, heads, *, b_a=None, a_sca
     N = r["sel"].shape[-1]
     return {"y": y, "sel": r["sel"].reshape(B, H, N), "scores": r["scores"].reshape(B, H, N, 2),
             "q": q, "k": k, "v": v, "g": g, "beta": beta, "o": o}
+
+
+class Decoder:
+    """The same layer in decode mode, one token per step, in float64.
+
+    "Neural Attention Search Linear (NAtS-L)", technical summary,
+    "Kernmechanismen" items 1, 3 and 4, read token by token (the readings of
+    the prefill oracle hold, see ``oracle/README.md``, plus DEC-1 there):
+
+    * every new token is appended to the keys / values of its chunk and sees
+      the retained keys / values (those of earlier softmax chunks) plus its
+      own chunk up to itself;
+    * the Gated DeltaNet state takes the token's update at once (the
+      pseudo-update) and the readout uses it;
+    * when a chunk is complete its score (mean of [q; k] over the chunk
+      through the linear score layer, ties to softmax) decides: softmax keeps
+      the chunk's keys / values and returns the state to the chunk start;
+      Gated DeltaNet keeps the state and drops the chunk's keys / values.
+
+    Run from an empty state over a whole sequence, it reproduces ``forward``.
+    """
+
+    def __init__(self, B, H, dk, dv, w_s, b_s, w_g, b_g=None, *, chunk: int = 64, scale: float = 0.0,
+                 eps: float = 1e-6, norm_w_soft=None, norm_w_lin=None):
+        self.B, self.H, self.dk, self.dv, self.C = B, H, dk, dv, chunk
+        self.scale = scale if scale > 0 else 1.0 / np.sqrt(dk)
+        self.eps = eps
+        self.w_s = np.asarray(w_s, np.float64).reshape(H, 2, 2 * dk)
+        self.b_s = np.zeros((H, 2)) if b_s is None else np.asarray(b_s, np.float64).reshape(H, 2)
+        self.w_g = np.asarray(w_g, np.float64).reshape(H, dk)
+        self.b_g = np.zeros(H) if b_g is None else np.asarray(b_g, np.float64).reshape(H)
+        self.nws = np.ones(dv) if norm_w_soft is None else np.asarray(norm_w_soft, np.float64)
+        self.nwl = np.ones(dv) if norm_w_lin is None else np.asarray(norm_w_lin, np.float64)
+        self.S = np.zeros((B, H, dv, dk))   # state after the last token
+        self.S0 = np.zeros((B, H, dv, dk))  # state at the start of the current chunk
+        self.kv_k = [[np.zeros((0, dk)) for _ in range(H)] for _ in range(B)]  # retained
+        self.kv_v = [[np.zeros((0, dv)) for _ in range(H)] for _ in range(B)]
+        self.ck = np.zeros((B, H, chunk, dk))  # current chunk
+        self.cv = np.zeros((B, H, chunk, dv))
+        self.psum = np.zeros((B, H, 2 * dk))  # sum of [q; k] over the current chunk
+        self.t = 0
+        self.sel = [[[] for _ in range(H)] for _ in range(B)]  # selection of each completed chunk
+
+    def _rms(self, o, w):
+        return o / np.sqrt(np.mean(o * o) + self.eps) * w
+
+    def step(self, q, k, v, g, beta):
+        """One token for every (b, h): q, k [B, H, dk], v [B, H, dv], g, beta [B, H].
+        Returns (out, o_s, o_l), each [B, H, dv]; completed chunks append to ``sel``."""
+        q, k, v = (np.asarray(x, np.float64) for x in (q, k, v))
+        g, beta = np.asarray(g, np.float64), np.asarray(beta, np.float64)
+        B, H, C = self.B, self.H, self.C
+        p = self.t % C
+        out = np.zeros((B, H, self.dv))
+        o_s = np.zeros((B, H, self.dv))
+        o_l = np.zeros((B, H, self.dv))
+        for b in range(B):
+            for h in range(H):
+                qt, kt, vt = q[b, h], k[b, h], v[b, h]
+                self.ck[b, h, p], self.cv[b, h, p] = kt, vt
+                # Gated DeltaNet: S <- a S (I - beta k k^T) + beta v k^T, readout with the new S
+                a, bt = np.exp(g[b, h]), beta[b, h]
+                S = self.S[b, h]
+                S = a * S - a * bt * np.outer(S @ kt, kt) + bt * np.outer(vt, kt)
+                self.S[b, h] = S
+                o_l[b, h] = S @ (qt * self.scale)
+                # softmax over the retained keys and this chunk up to the token
+                K = np.concatenate([self.kv_k[b][h], self.ck[b, h, :p + 1]])
+                V = np.concatenate([self.kv_v[b][h], self.cv[b, h, :p + 1]])
+                lg = (K @ qt) * self.scale
+                e = np.exp(lg - lg.max())
+                o_s[b, h] = (e / e.sum()) @ V
+                # per-branch RMSNorm and the query-gated sum
+                w = 1.0 / (1.0 + np.exp(-(qt @ self.w_g[h] + self.b_g[h])))
+                out[b, h] = w * self._rms(o_s[b, h], self.nws) + (1 - w) * self._rms(o_l[b, h], self.nwl)
+                self.psum[b, h] += np.concatenate([qt, kt])
+                if p == C - 1:
+                    s = self.w_s[h] @ (self.psum[b, h] / C) + self.b_s[h]
+                    sel = 0 if s[0] >= s[1] else 1
+                    self.sel[b][h].append(sel)
+                    if sel == 0:  # softmax: keep the chunk's keys / values, roll the state back
+                        self.kv_k[b][h] = np.concatenate([self.kv_k[b][h], self.ck[b, h]])
+                        self.kv_v[b][h] = np.concatenate([self.kv_v[b][h], self.cv[b, h]])
+                        self.S[b, h] = self.S0[b, h]
+                    else:  # Gated DeltaNet: commit the state
+                        self.S0[b, h] = self.S[b, h]
+                    self.psum[b, h] = 0.0
+        self.t += 1
+        return out, o_s, o_l
