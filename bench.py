@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-x-path", action="store_true", help="skip the layer-with-projections measurement")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
     return ap.parse_args()
 
 
@@ -431,6 +432,8 @@ def run_native(args, rank, world, local_rank):
     # hidden = H d = 2048: tokens/s of the whole model layer ----
     if not args.no_x_path:
         res["x_path"] = run_x_path(args, rank, dev, stream, dist)
+    if not args.no_decode:
+        res["decode"] = run_decode(args, rank, dev, stream, dist)
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
     if not args.no_cpu_baseline and world == 1 and rank == 0:
         cores = cpu_cores()
@@ -500,6 +503,89 @@ def run_x_path(args, rank, dev, stream, dist):
             "config": {"B": B, "H": H, "L": L, "d": d, "hidden": hidden},
             "value": job_throughput(B * L, world, ms), "unit": "tokens/s", "ms_per_step": ms,
             "projection_gemm_flops_per_step": gemm_flops}
+
+
+def run_decode(args, rank, dev, stream, dist):
+    """Times nats_decode_step after an 8192-token context (B = 4, H = 16,
+    d = 128, bf16, 25 % of the context's chunks retained: 2048 keys / values
+    per head): K steps at positions following the warm-up steps, captured in
+    a CUDA graph and replayed (device time, CUDA events, max over ranks), as
+    a serving loop would run them; the same steps issued one call at a time
+    from Python are reported beside it (host-bound).  The state and the
+    retained keys / values are seeded synthetic values of the right shapes."""
+    import torch
+
+    import linear_attention_nats_gb300 as nats
+
+    B, H, d, t0, kept = 4, 16, 128, 8192, 2048
+    g_ = torch.Generator(device="cpu").manual_seed(rank_seed(41, rank))
+    steps_all = max(args.warmup, 1) + 2 * args.steps
+    cap = 64 * ((t0 + steps_all) // 64 + 1)
+    st = nats.DecodeState(B, H, d, cap=cap, dtype=torch.bfloat16, device=dev)
+    rn = lambda *shape: torch.randn(*shape, generator=g_)
+    st.S.copy_(0.05 * rn(B, H, d, d))
+    st.S0.copy_(st.S)
+    st.kv_k[:, :, :kept].copy_(torch.nn.functional.normalize(rn(B, H, kept, d), dim=-1).to(torch.bfloat16))
+    st.kv_v[:, :, :kept].copy_(rn(B, H, kept, d).to(torch.bfloat16))
+    st.n_kv.fill_(kept)
+    q = rn(steps_all, B, H, d).to(torch.bfloat16).to(dev)
+    k = torch.nn.functional.normalize(rn(steps_all, B, H, d), dim=-1).to(torch.bfloat16).to(dev)
+    v = rn(steps_all, B, H, d).to(torch.bfloat16).to(dev)
+    g = (-0.1 * torch.nn.functional.softplus(rn(steps_all, B, H))).to(dev)
+    beta = torch.sigmoid(rn(steps_all, B, H)).to(dev)
+    w_s = (0.02 * rn(H, 2, 2 * d)).to(dev)
+    b_s = torch.zeros(H, 2).to(dev)
+    w_g = (0.02 * rn(H, d)).to(dev)
+    b_g = torch.zeros(H).to(dev)
+    out = torch.empty((B, H, d), dtype=torch.bfloat16, device=dev)
+
+    def step(i, s=None):
+        nats.decode_step(st, t0 + i, q[i], k[i], v[i], g[i], beta[i], w_s, b_s, w_g, b_g, out=out, stream=s)
+
+    nw = max(args.warmup, 1)
+    with torch.cuda.stream(stream):
+        for i in range(nw):
+            step(i)
+    torch.cuda.synchronize()
+    # one call at a time from Python (host-bound)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record()
+        for i in range(args.steps):
+            step(nw + i)
+        e1.record()
+    torch.cuda.synchronize()
+    host_ms = e0.elapsed_time(e1) / args.steps
+    # the next K steps as one CUDA graph
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(args.steps):
+            step(nw + args.steps + i)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
+    world = dist.get_world_size() if dist is not None else 1
+    # bytes a step has to move: the state (read + write), the retained and
+    # current-chunk keys / values (read), the token in and out
+    p_mean = (t0 % 64) + nw + args.steps + (args.steps - 1) / 2.0
+    nbytes = B * H * (2 * d * d * 4 + (kept + p_mean + 1) * d * 2 * 2 + 5 * d * 2)
+    pk = peaks()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"what": "nats_decode_step: one token per (b, h) after an 8192-token context, 25 % of its chunks "
+                    "retained (2048 keys / values per head)",
+            "config": {"B": B, "H": H, "d": d, "position": t0, "retained_per_head": kept},
+            "value": job_throughput(B, world, ms), "unit": "tokens/s", "ms_per_step": ms,
+            "host_loop_ms_per_step": host_ms,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"], "bytes_per_step": nbytes}}
 
 
 def main():

@@ -235,6 +235,58 @@ nats_status nats_hybrid_fwd_x(const nats_dims* dims, int32_t hidden, const void*
                               const void* w_o, void* y, uint8_t* sel_out, void* workspace,
                               size_t workspace_bytes, nats_stream_t stream);
 
+/* ------------------------------------------------------------------ decode
+ * The same layer in decode mode: one new token per (b, h) per call, at
+ * position t of the sequence.  "Neural Attention Search Linear (NAtS-L)",
+ * technical summary, "Kernmechanismen" items 1, 3 and 4 read token by token
+ * (the decode reading of the oracle README): the token joins its chunk's keys
+ * and values and attends to the retained ones (those of earlier softmax
+ * chunks) plus its chunk up to itself; the Gated DeltaNet state takes the
+ * token's update at once (the pseudo-update) and the readout uses it; when
+ * the token completes its chunk (t % chunk == chunk - 1) the chunk's score
+ * (mean of [q; k] over the chunk through W_s, b_s; ties to softmax) decides:
+ * softmax appends the chunk's keys and values to the retained ones and puts
+ * the state back to the chunk start; Gated DeltaNet keeps the state (the new
+ * chunk start) and drops them.  Stepped from the empty state over a
+ * sequence, it gives the outputs nats_hybrid_fwd gives for that sequence.
+ *
+ * The state is the caller's device memory, updated in place by each call;
+ * all zeros (S, S0, psum, n_kv) is the empty state (ck, cv need no
+ * initialisation).  Layouts are contiguous, element type fp32 where marked,
+ * else dims->dtype. */
+typedef struct {
+  float* S;       /* [B, H, dv, dk] fp32 state after the last token */
+  float* S0;      /* [B, H, dv, dk] fp32 state at the start of the current chunk */
+  void* ck;       /* [B, H, chunk, dk] keys of the current chunk */
+  void* cv;       /* [B, H, chunk, dv] values of the current chunk */
+  float* psum;    /* [B, H, 2 dk] fp32 sum of [q; k] over the current chunk */
+  void* kv_k;     /* [B, H, cap, dk] keys of the retained chunks, in order */
+  void* kv_v;     /* [B, H, cap, dv] values of the retained chunks */
+  int32_t* n_kv;  /* [B, H] retained tokens per head (a multiple of chunk) */
+  int64_t cap;    /* tokens per head kv_k / kv_v hold */
+} nats_decode_state;
+
+/* One decode step.  dims: B, H, dk = dv (64 or 128), chunk (64), dtype,
+ * scale, eps as for nats_hybrid_fwd; dims->L is not used.  t >= 0 is the
+ * position of this token.  q, k [B, H, dk], v [B, H, dv] (dtype); g, beta
+ * [B, H] fp32 (log-decay and delta-rule strength of this token); w_s, b_s,
+ * w_g, b_g, norm weights as for nats_hybrid_fwd (b_s, b_g, norm weights may
+ * be NULL).  out [B, H, dv] (dtype) = w RMSNorm(o_s) + (1 - w) RMSNorm(o_l).
+ * sel_out [B, H] (or NULL) receives the selection of the completed chunk and
+ * is written only when t % chunk == chunk - 1.  o_soft_out / o_lin_out [B, H,
+ * dv] fp32 (or NULL) receive the two branch outputs.  All pointers device,
+ * 16-byte aligned; asynchronous on `stream`.
+ * Errors before any launch: NATS_ERR_NULL (a required pointer), NATS_ERR_SHAPE
+ * / NATS_ERR_UNSUPPORTED / NATS_ERR_DTYPE / NATS_ERR_VALUE (dims, t < 0),
+ * NATS_ERR_ALIGN, NATS_ERR_WORKSPACE when cap < chunk * (t / chunk + 1) (the
+ * retained tokens could outgrow kv_k / kv_v); NATS_ERR_CUDA on a failed
+ * launch. */
+nats_status nats_decode_step(const nats_dims* dims, int64_t t, const void* q, const void* k, const void* v,
+                             const float* g, const float* beta, const float* w_s, const float* b_s,
+                             const float* w_g, const float* b_g, const float* norm_w_soft,
+                             const float* norm_w_lin, const nats_decode_state* state, void* out,
+                             uint8_t* sel_out, float* o_soft_out, float* o_lin_out, nats_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,7 +16,8 @@ import torch
 from . import _native
 from ._native import NATS_BF16, NATS_F32, NatsError, check, dims  # noqa: F401
 
-__all__ = ["select", "hybrid_fwd", "hybrid_fwd_x", "workspace_size", "NatsError", "dims", "NATS_BF16", "NATS_F32"]
+__all__ = ["select", "hybrid_fwd", "hybrid_fwd_x", "DecodeState", "decode_step", "workspace_size", "NatsError",
+           "dims", "NATS_BF16", "NATS_F32"]
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -174,3 +175,63 @@ def hybrid_fwd_x(x, w_qkv, w_ab, w_s, b_s, w_g, b_g=None, *, heads: int, b_a=Non
         _p(w_g), _p(b_g), _p(w_o), _p(y), _p(sel), _p(workspace), ctypes.c_size_t(workspace.numel()),
         _stream(stream)), "nats_hybrid_fwd_x")
     return {"y": y, "sel": sel} if return_sel else y
+
+
+class DecodeState:
+    """Device state of the layer in decode mode (nats_decode_state): the
+    Gated DeltaNet state S and its chunk-start copy S0 (fp32 [B, H, d, d]), the
+    current chunk's keys / values ck, cv ([B, H, 64, d]), the running sum of
+    [q; k] over the chunk (fp32 [B, H, 2 d]), the retained keys / values kv_k,
+    kv_v ([B, H, cap, d]) and their count n_kv (int32 [B, H]).  New states are
+    empty (zeros)."""
+
+    def __init__(self, B: int, H: int, d: int, cap: int, dtype=torch.bfloat16, device="cuda"):
+        z = dict(device=device)
+        self.B, self.H, self.d, self.cap, self.dtype = B, H, d, int(cap), dtype
+        self.S = torch.zeros((B, H, d, d), dtype=torch.float32, **z)
+        self.S0 = torch.zeros((B, H, d, d), dtype=torch.float32, **z)
+        self.ck = torch.zeros((B, H, 64, d), dtype=dtype, **z)
+        self.cv = torch.zeros((B, H, 64, d), dtype=dtype, **z)
+        self.psum = torch.zeros((B, H, 2 * d), dtype=torch.float32, **z)
+        self.kv_k = torch.zeros((B, H, self.cap, d), dtype=dtype, **z)
+        self.kv_v = torch.zeros((B, H, self.cap, d), dtype=dtype, **z)
+        self.n_kv = torch.zeros((B, H), dtype=torch.int32, **z)
+
+    def c_struct(self) -> _native.DecodeState:
+        return _native.DecodeState(self.S.data_ptr(), self.S0.data_ptr(), self.ck.data_ptr(), self.cv.data_ptr(),
+                                   self.psum.data_ptr(), self.kv_k.data_ptr(), self.kv_v.data_ptr(),
+                                   self.n_kv.data_ptr(), self.cap)
+
+
+def decode_step(state: DecodeState, t: int, q, k, v, g, beta, w_s, b_s, w_g, b_g=None, *, norm_w_soft=None,
+                norm_w_lin=None, out=None, sel_out=None, return_branches: bool = False, scale: float = 0.0,
+                eps: float = 1e-6, stream=None):
+    """One decode step at position t: q, k, v [B, H, d] (the state's dtype), g,
+    beta fp32 [B, H]; weights as for hybrid_fwd.  Updates `state` in place and
+    returns out [B, H, d] (or {"out", "o_s", "o_l"} with return_branches).
+    sel_out (uint8 [B, H]) receives the chunk's selection when t completes a
+    chunk.  The definitions are those of nats_decode_step in include/nats.h."""
+    B, H, d = state.B, state.H, state.d
+    for name, x in (("q", q), ("k", k), ("v", v)):
+        _req(x, name, state.dtype, (B, H, d))
+    _req(g, "g", torch.float32, (B, H))
+    _req(beta, "beta", torch.float32, (B, H))
+    _req(w_s, "w_s", torch.float32, (H, 2, 2 * d))
+    _req(b_s, "b_s", torch.float32, (H, 2))
+    _req(w_g, "w_g", torch.float32, (H, d))
+    _req(b_g, "b_g", torch.float32, (H,))
+    if out is None:
+        out = torch.empty((B, H, d), dtype=state.dtype, device=q.device)
+    _req(out, "out", state.dtype, (B, H, d))
+    _req(sel_out, "sel_out", torch.uint8, (B, H))
+    o_s = o_l = None
+    if return_branches:
+        o_s = torch.empty((B, H, d), dtype=torch.float32, device=q.device)
+        o_l = torch.empty((B, H, d), dtype=torch.float32, device=q.device)
+    dm = dims(B, H, 0, d, _dtype_code(q), scale=scale, eps=eps)
+    st = state.c_struct()
+    check(_native.lib.nats_decode_step(
+        ctypes.byref(dm), int(t), _p(q), _p(k), _p(v), _p(g), _p(beta), _p(w_s), _p(b_s), _p(w_g), _p(b_g),
+        _p(norm_w_soft), _p(norm_w_lin), ctypes.byref(st), _p(out), _p(sel_out), _p(o_s), _p(o_l),
+        _stream(stream)), "nats_decode_step")
+    return {"out": out, "o_s": o_s, "o_l": o_l} if return_branches else out

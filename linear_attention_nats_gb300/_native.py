@@ -25,7 +25,7 @@ STATUS = {
 # Every symbol include/nats.h declares.
 EXPORTS = ("nats_status_string", "nats_last_cuda_error", "nats_workspace_size", "nats_workspace_check", "nats_select",
            "nats_hybrid_fwd", "nats_hybrid_fwd_profiled", "nats_hybrid_fwd_noalloc", "nats_x_workspace_size",
-           "nats_hybrid_fwd_x")
+           "nats_hybrid_fwd_x", "nats_decode_step")
 
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -36,6 +36,12 @@ STAGES = ("score", "compact", "softmax", "gdn_prep", "gdn_scan", "merge")
 class Profile(ctypes.Structure):
     _fields_ = [("start", ctypes.c_void_p * NUM_STAGES), ("stop", ctypes.c_void_p * NUM_STAGES),
                 ("launches", ctypes.c_int32), ("stage_launches", ctypes.c_int32 * NUM_STAGES)]
+
+
+class DecodeState(ctypes.Structure):
+    _fields_ = [("S", ctypes.c_void_p), ("S0", ctypes.c_void_p), ("ck", ctypes.c_void_p), ("cv", ctypes.c_void_p),
+                ("psum", ctypes.c_void_p), ("kv_k", ctypes.c_void_p), ("kv_v", ctypes.c_void_p),
+                ("n_kv", ctypes.c_void_p), ("cap", ctypes.c_int64)]
 
 
 class Dims(ctypes.Structure):
@@ -82,6 +88,9 @@ def _load() -> ctypes.CDLL:
     lib.nats_x_workspace_size.restype = ctypes.c_size_t
     lib.nats_hybrid_fwd_x.argtypes = [ctypes.POINTER(Dims), ctypes.c_int32] + [P] * 14 + [ctypes.c_size_t, P]
     lib.nats_hybrid_fwd_x.restype = ctypes.c_int
+    lib.nats_decode_step.argtypes = [ctypes.POINTER(Dims), ctypes.c_int64] + [P] * 11 + [
+        ctypes.POINTER(DecodeState)] + [P] * 4 + [P]
+    lib.nats_decode_step.restype = ctypes.c_int
     return lib
 
 

@@ -304,4 +304,29 @@ nats_status nats_hybrid_fwd(const nats_dims* dims, const void* q, const void* k,
                                   o_lin_out, workspace, workspace_bytes, stream, nullptr);
 }
 
+nats_status nats_decode_step(const nats_dims* dims, int64_t t, const void* q, const void* k, const void* v,
+                             const float* g, const float* beta, const float* w_s, const float* b_s,
+                             const float* w_g, const float* b_g, const float* norm_w_soft,
+                             const float* norm_w_lin, const nats_decode_state* state, void* out,
+                             uint8_t* sel_out, float* o_soft_out, float* o_lin_out, nats_stream_t stream) {
+  if (!dims) return NATS_ERR_NULL;
+  nats_dims d = *dims;
+  d.L = 0;  // not used in decode mode
+  nats_status s = check_dims(&d);
+  if (s != NATS_OK) return s;
+  if (t < 0) return NATS_ERR_VALUE;
+  const Problem p = problem_of(&d);
+  if (p.BH == 0) return NATS_OK;
+  if (!q || !k || !v || !g || !beta || !w_s || !w_g || !state || !out) return NATS_ERR_NULL;
+  const nats_decode_state& st = *state;
+  if (!st.S || !st.S0 || !st.ck || !st.cv || !st.psum || !st.kv_k || !st.kv_v || !st.n_kv) return NATS_ERR_NULL;
+  const void* ptrs[] = {q, k, v, out, st.S, st.S0, st.ck, st.cv, st.psum, st.kv_k, st.kv_v};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return NATS_ERR_ALIGN;
+  if (st.cap < (long long)kChunk * (t / kChunk + 1)) return NATS_ERR_WORKSPACE;
+  return cuda_status(launch_decode_step(p, d.dtype, t, q, k, v, g, beta, w_s, b_s, w_g, b_g, norm_w_soft,
+                                        norm_w_lin, st.S, st.S0, st.ck, st.cv, st.psum, st.kv_k, st.kv_v, st.n_kv,
+                                        st.cap, out, sel_out, o_soft_out, o_lin_out, (cudaStream_t)stream));
+}
+
 }  // extern "C"

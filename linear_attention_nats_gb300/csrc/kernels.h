@@ -50,6 +50,14 @@ cudaError_t launch_gdn_scan_tc(const Problem& p, const void* q, const void* k, c
                                const void* W16, const void* UT16, const void* P16, float* o_l, void* o_l16,
                                float* state_out, int* err, cudaStream_t st);
 
+// One decode step of the layer (dtype 0 = bf16, 1 = fp32), one CTA per (b, h).
+cudaError_t launch_decode_step(const Problem& p, int dtype, long long t, const void* q, const void* k,
+                               const void* v, const float* g, const float* beta, const float* w_s,
+                               const float* b_s, const float* w_g, const float* b_g, const float* nw_s,
+                               const float* nw_l, float* S, float* S0, void* ck, void* cv, float* psum,
+                               void* kv_k, void* kv_v, int32_t* n_kv, long long cap, void* out,
+                               uint8_t* sel_out, float* o_s_out, float* o_l_out, cudaStream_t st);
+
 // bf16 path: out (holding w RMSNorm(o_s)) += (1 - w) RMSNorm(o_l).
 cudaError_t launch_merge_lin(const Problem& p, const float* o_l, const void* o_l16, const float* gate,
                              const float* nw_l, void* out, cudaStream_t st);

@@ -134,3 +134,27 @@ def test_x_path_validation(nat):
     assert nat.lib.nats_hybrid_fwd_x(ctypes.byref(dm), 128, *null, ctypes.c_size_t(0), None) == 1
     bad = nat.dims(1, 2, 100, 64)  # L % 64
     assert nat.lib.nats_hybrid_fwd_x(ctypes.byref(bad), 128, *null, ctypes.c_size_t(0), None) == 2
+
+
+def test_decode_validation(nat):
+    # the decode step: argument checks before any launch (no device memory is touched)
+    dm = nat.dims(1, 2, 0, 64)
+    fake = ctypes.c_void_p(256)  # 16-byte aligned, never dereferenced on these paths
+    odd = ctypes.c_void_p(264)   # 8-byte aligned only
+    st = nat.DecodeState(fake.value, fake.value, fake.value, fake.value, fake.value, fake.value, fake.value,
+                         fake.value, 64)
+    args = [fake] * 11
+    tail = [fake, None, None, None, None]
+
+    def call(d=dm, t=0, a=args, s=st, tl=tail):
+        return nat.lib.nats_decode_step(ctypes.byref(d), t, *a, ctypes.byref(s) if s is not None else None, *tl)
+
+    assert call(t=-1) == 9                       # NATS_ERR_VALUE
+    assert call(t=64) == 5                       # cap 64 cannot take a second chunk: NATS_ERR_WORKSPACE
+    assert call(a=[None] + args[1:]) == 1        # q NULL
+    assert call(s=None) == 1                     # state NULL
+    assert call(a=[odd] + args[1:]) == 4         # q misaligned: NATS_ERR_ALIGN
+    bad = nat.dims(1, 2, 0, 96)
+    assert call(d=bad) == 6                      # head size: NATS_ERR_UNSUPPORTED
+    empty = nat.dims(0, 2, 0, 64)
+    assert call(d=empty) == 0                    # nothing to do
