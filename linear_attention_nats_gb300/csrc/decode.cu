@@ -11,13 +11,14 @@
 //      row i of S becomes a S_i + beta (v_i - a S_i . k) k^T, and
 //      o_l = S (scale q), 256 / d threads per state row (fp32 state in
 //      global memory);
-//   3. every CTA: softmax over its share of the keys (the retained keys of
-//      earlier softmax chunks, then the chunk's keys up to the token): each
-//      warp takes blocks of 32 keys, a lane scores one key (the whole q . k
-//      dot product), then the warp accumulates P V with each lane holding
-//      d / 32 output columns; the CTA's eight warps are combined, and the
-//      CTA's (max, sum, partial output) goes into CTA 0's shared memory
-//      (distributed shared memory) before a cluster barrier;
+//   3. CTAs 1 .. kSplit - 1: softmax over their share of the keys (the
+//      retained keys of earlier softmax chunks, then the chunk's keys up to
+//      the token): a warp takes its keys in batches of eight, lanes split the
+//      d features (one coalesced 256-byte row per key), the next batch's rows
+//      are loaded while the current one is scored; the eight dot products
+//      are summed over the warp by halving (nine shuffles); the CTA's warps
+//      are combined and its (max, sum, partial output) goes into CTA 0's
+//      shared memory (distributed shared memory) before a cluster barrier;
 //   4. CTA 0: the kSplit partials combined, RMSNorm of both branches and the
 //      query-gated sum;
 //   5. CTA 0: the running [q; k] sum of the chunk; when the token completes
@@ -34,7 +35,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kSplit = 4;  // CTAs per (b, h) (a thread-block cluster)
+constexpr int kSplit = 8;  // CTAs per (b, h) (a thread-block cluster): CTA 0 the state, CTAs 1.. the keys
 
 template <int N>
 __device__ __forceinline__ void load_n(const float* p, float (&o)[N]) {
@@ -69,6 +70,44 @@ __device__ __forceinline__ void load_e(const __nv_bfloat16* p, float (&o)[E]) {
   for (int x = 0; x < E; ++x) o[x] = __bfloat162float(p[x]);
 }
 
+// E consecutive elements kept in their storage form (the rows of a batch in
+// flight), converted when used
+template <typename T, int E>
+struct Raw;
+template <>
+struct Raw<__nv_bfloat16, 4> {
+  uint2 r;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) { r = *(const uint2*)p; }
+  __device__ __forceinline__ void zero() { r = make_uint2(0, 0); }
+  __device__ __forceinline__ void get(float (&o)[4]) const {
+    o[0] = __uint_as_float(r.x << 16), o[1] = __uint_as_float(r.x & 0xffff0000u);
+    o[2] = __uint_as_float(r.y << 16), o[3] = __uint_as_float(r.y & 0xffff0000u);
+  }
+};
+template <>
+struct Raw<__nv_bfloat16, 2> {
+  uint32_t r;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) { r = *(const uint32_t*)p; }
+  __device__ __forceinline__ void zero() { r = 0; }
+  __device__ __forceinline__ void get(float (&o)[2]) const {
+    o[0] = __uint_as_float(r << 16), o[1] = __uint_as_float(r & 0xffff0000u);
+  }
+};
+template <>
+struct Raw<float, 4> {
+  float4 r;
+  __device__ __forceinline__ void load(const float* p) { r = *(const float4*)p; }
+  __device__ __forceinline__ void zero() { r = make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ __forceinline__ void get(float (&o)[4]) const { o[0] = r.x, o[1] = r.y, o[2] = r.z, o[3] = r.w; }
+};
+template <>
+struct Raw<float, 2> {
+  float2 r;
+  __device__ __forceinline__ void load(const float* p) { r = *(const float2*)p; }
+  __device__ __forceinline__ void zero() { r = make_float2(0.f, 0.f); }
+  __device__ __forceinline__ void get(float (&o)[2]) const { o[0] = r.x, o[1] = r.y; }
+};
+
 // sums of three per-thread values over the CTA (every thread gets them)
 __device__ __forceinline__ void block_sum3(float& a, float& b, float& c, float (*red)[3]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -92,10 +131,11 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 1) de
     float* __restrict__ S0, T* __restrict__ ck, T* __restrict__ cv, float* __restrict__ psum,
     T* __restrict__ kv_k, T* __restrict__ kv_v, int32_t* __restrict__ n_kv, long long cap, T* __restrict__ out,
     uint8_t* __restrict__ sel_out, float* __restrict__ o_s_out, float* __restrict__ o_l_out) {
-  static_assert(kThreads % D == 0 && D % 32 == 0, "shape");
-  constexpr int TPR = kThreads / D;  // threads per state row
-  constexpr int CPT = D / TPR;       // state columns per thread
-  constexpr int E = D / 32;          // output columns per lane in the P V sum
+  static_assert(D % 32 == 0 && D <= 128, "shape");
+  constexpr int CPT = 32;              // state columns per thread
+  constexpr int TPR = D / CPT;         // threads per state row
+  constexpr int RPP = kThreads / TPR;  // state rows per pass
+  constexpr int E = D / 32;            // features per lane in the softmax
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -126,95 +166,129 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 1) de
 
   // 2. Gated DeltaNet state update and readout (CTA 0)
   if (rank == 0) {
-    const int row = tid / TPR, part = tid % TPR;
-    float* srow = S + (bh * D + row) * D + part * CPT;
-    float sv[CPT];
-    load_n<CPT>(srow, sv);
-    float u = 0.f;
+#pragma unroll 1
+    for (int row0 = 0; row0 < D; row0 += RPP) {
+      const int row = row0 + tid / TPR, part = tid % TPR;
+      if (RPP > D && row >= D) break;  // (d = 64: half the threads have no row); warp-uniform
+      float* srow = S + (bh * D + row) * D + part * CPT;
+      float sv[CPT];
+      load_n<CPT>(srow, sv);
+      float u = 0.f;
 #pragma unroll
-    for (int j = 0; j < CPT; ++j) u = fmaf(sv[j], ks[part * CPT + j], u);
+      for (int j = 0; j < CPT; ++j) u = fmaf(sv[j], ks[part * CPT + j], u);
 #pragma unroll
-    for (int o = 1; o < TPR; o <<= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
-    const float coef = bt * (vs[row] - a * u);
-    float r = 0.f;
+      for (int o = 1; o < TPR; o <<= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
+      const float coef = bt * (vs[row] - a * u);
+      float r = 0.f;
 #pragma unroll
-    for (int j = 0; j < CPT; ++j) {
-      sv[j] = fmaf(a, sv[j], coef * ks[part * CPT + j]);
-      r = fmaf(sv[j], qs[part * CPT + j], r);
+      for (int j = 0; j < CPT; ++j) {
+        sv[j] = fmaf(a, sv[j], coef * ks[part * CPT + j]);
+        r = fmaf(sv[j], qs[part * CPT + j], r);
+      }
+#pragma unroll
+      for (int o = 1; o < TPR; o <<= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+#pragma unroll
+      for (int j = 0; j < CPT; j += 4)
+        *(float4*)(srow + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
+      if (part == 0) ol[row] = r * scale;
     }
-#pragma unroll
-    for (int o = 1; o < TPR; o <<= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
-#pragma unroll
-    for (int j = 0; j < CPT; j += 4)
-      *(float4*)(srow + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
-    if (part == 0) ol[row] = r * scale;
   }
 
   // 3. softmax over the retained keys and the chunk's keys up to the token
   {
     const int nr = n_kv[bh];
     const int n = nr + p + 1;  // key n - 1 is this token (taken from shared memory)
-    const int lo = (int)((long long)n * rank / kSplit), hi = (int)((long long)n * (rank + 1) / kSplit);
+    // keys [lo, hi) of this CTA (CTA 0 has none), [wlo, whi) of this warp
+    const int nk = kSplit - 1, kr_ = rank - 1;
+    const int lo = rank == 0 ? 0 : (int)((long long)n * kr_ / nk), hi = rank == 0 ? 0 : (int)((long long)n * (kr_ + 1) / nk);
+    const int wlo = lo + (int)((long long)(hi - lo) * warp / kWarps), whi = lo + (int)((long long)(hi - lo) * (warp + 1) / kWarps);
     const T* Kr = kv_k + bh * cap * D;
     const T* Vr = kv_v + bh * cap * D;
     const T* Kc = ck + bh * C * D;
     const T* Vc = cv + bh * C * D;
+    float qv[E];
+#pragma unroll
+    for (int x = 0; x < E; ++x) qv[x] = qs[lane * E + x];
     float m = -INFINITY, l = 0.f, acc[E];
 #pragma unroll
     for (int x = 0; x < E; ++x) acc[x] = 0.f;
-    for (int j0 = lo + 32 * warp; j0 < hi; j0 += 32 * kWarps) {
-      const int j = j0 + lane;
-      float s = -INFINITY;
-      if (j < hi) {
-        float dot = 0.f;
-        if (j == n - 1) {
-#pragma unroll 8
-          for (int c = 0; c < D; ++c) dot = fmaf(ks[c], qs[c], dot);
-        } else {
-          const T* kr = j < nr ? Kr + (long long)j * D : Kc + (long long)(j - nr) * D;
-#pragma unroll 4
-          for (int c = 0; c < D; c += 8) {
-            float kk[8];
-            load_n<8>(kr + c, kk);
-#pragma unroll
-            for (int x = 0; x < 8; ++x) dot = fmaf(kk[x], qs[c + x], dot);
-          }
-        }
-        s = dot * scale;
+    // lane's E features of key / value row j, in storage form (zeros past
+    // the end of the warp's keys; this token's from the inputs)
+    using RV = Raw<T, E>;
+    auto fetch = [&](int j, RV (&kb)[8], RV (&vb)[8], int u) {
+      if (j >= whi) {
+        kb[u].zero();
+        vb[u].zero();
+      } else if (j == n - 1) {
+        kb[u].load(k + bh * D + lane * E);
+        vb[u].load(v + bh * D + lane * E);
+      } else {
+        const long long off = (j < nr ? (long long)j : (long long)(j - nr)) * D + lane * E;
+        kb[u].load((j < nr ? Kr : Kc) + off);
+        vb[u].load((j < nr ? Vr : Vc) + off);
       }
-      const float mb = warp_max(s);
+    };
+    auto fetch8 = [&](int j0, RV (&kb)[8], RV (&vb)[8]) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) fetch(j0 + u, kb, vb, u);
+    };
+    // the 8 keys from j0: scores (partial dot products summed over the warp
+    // by halving: lane (b4 b3 b2 . .) ends with key 4 b4 + 2 b3 + b2), online
+    // softmax, P V
+    auto batch = [&](int j0, const RV (&kb)[8], const RV (&vb)[8]) {
+      float dp[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        float kk[E];
+        kb[u].get(kk);
+        dp[u] = 0.f;
+#pragma unroll
+        for (int x = 0; x < E; ++x) dp[u] = fmaf(qv[x], kk[x], dp[u]);
+      }
+      const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+      float d4[4], d2[2];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) d4[u] = (b4 ? dp[4 + u] : dp[u]) + __shfl_xor_sync(0xffffffffu, b4 ? dp[u] : dp[4 + u], 16);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) d2[u] = (b3 ? d4[2 + u] : d4[u]) + __shfl_xor_sync(0xffffffffu, b3 ? d4[u] : d4[2 + u], 8);
+      float d1 = (b2 ? d2[1] : d2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? d2[0] : d2[1], 4);
+      d1 += __shfl_xor_sync(0xffffffffu, d1, 2);
+      d1 += __shfl_xor_sync(0xffffffffu, d1, 1);
+      const int ku = 4 * (lane >> 4) + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
+      const float sc = (j0 + ku < whi) ? d1 * scale : -INFINITY;
+      float mb = sc;
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
       const float mn = fmaxf(m, mb);
-      const float alpha = __expf(m - mn);  // 0 on the first block (m = -inf)
-      const float pj = (j < hi) ? __expf(s - mn) : 0.f;
-      l = l * alpha + warp_sum(pj);
+      const float alpha = __expf(m - mn);  // 0 on the first batch (m = -inf)
+      const float pu = (j0 + ku < whi) ? __expf(sc - mn) : 0.f;
+      float ps = pu;
+      ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+      ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+      ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+      l = l * alpha + ps;
+      m = mn;
 #pragma unroll
       for (int x = 0; x < E; ++x) acc[x] *= alpha;
-      m = mn;
-      const int nb = min(32, hi - j0);
-      // eight values rows in flight per step
-      for (int jj = 0; jj < nb; jj += 8) {
-        float vv[8][E], pw[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          pw[u] = __shfl_sync(0xffffffffu, pj, (jj + u) & 31);
-          const int jk = j0 + jj + u;
+      for (int u = 0; u < 8; ++u) {
+        const float pw = __shfl_sync(0xffffffffu, pu, ((u >> 2) << 4) | (((u >> 1) & 1) << 3) | ((u & 1) << 2));
+        float vv[E];
+        vb[u].get(vv);
 #pragma unroll
-          for (int x = 0; x < E; ++x) vv[u][x] = 0.f;
-          if (jj + u < nb) {
-            if (jk == n - 1) {
-#pragma unroll
-              for (int x = 0; x < E; ++x) vv[u][x] = vs[lane * E + x];
-            } else {
-              const T* vr = jk < nr ? Vr + (long long)jk * D : Vc + (long long)(jk - nr) * D;
-              load_e<E>(vr + lane * E, vv[u]);
-            }
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-#pragma unroll
-          for (int x = 0; x < E; ++x) acc[x] = fmaf(pw[u], vv[u][x], acc[x]);
+        for (int x = 0; x < E; ++x) acc[x] = fmaf(pw, vv[x], acc[x]);
       }
+    };
+    // two batches of rows in flight: the next one loads while one is scored
+    RV k0[8], v0[8], k1[8], v1[8];
+    if (wlo < whi) fetch8(wlo, k0, v0);
+    for (int j0 = wlo; j0 < whi; j0 += 16) {
+      fetch8(j0 + 8, k1, v1);
+      batch(j0, k0, v0);
+      if (j0 + 8 >= whi) break;
+      fetch8(j0 + 16, k0, v0);
+      batch(j0 + 8, k1, v1);
     }
     if (lane == 0) wm[warp] = m, wl[warp] = l;
 #pragma unroll
