@@ -235,6 +235,21 @@ nats_status nats_hybrid_fwd_x(const nats_dims* dims, int32_t hidden, const void*
                               const void* w_o, void* y, uint8_t* sel_out, void* workspace,
                               size_t workspace_bytes, nats_stream_t stream);
 
+/* --------------------------------------------------------------- test hooks
+ * Failure injection without a GPU fault.
+ * nats_debug_fail_stage: the next layer forward on this host thread
+ * (nats_hybrid_fwd, _profiled, _noalloc, _x) replaces the launch of stage
+ * `stage` (a NATS_STAGE_* id) by a cudaErrorInvalidValue: it returns
+ * NATS_ERR_CUDA there, nats_last_cuda_error() names the error, and the
+ * stages before it have been enqueued.  -1 cancels.
+ * nats_debug_bounded_wait: one device thread waits for an mbarrier phase
+ * that nothing completes, gives up after limit_ns (1 .. 1e9) and sets *flag
+ * (device int) to 1 -- the path every tensor-core kernel takes when one of
+ * its bounded waits expires.  NATS_ERR_NULL / NATS_ERR_VALUE for bad
+ * arguments. */
+void nats_debug_fail_stage(int32_t stage);
+nats_status nats_debug_bounded_wait(int32_t* flag, int64_t limit_ns, nats_stream_t stream);
+
 /* ------------------------------------------------------------------ decode
  * The same layer in decode mode: one new token per (b, h) per call, at
  * position t of the sequence.  "Neural Attention Search Linear (NAtS-L)",

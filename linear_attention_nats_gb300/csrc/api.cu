@@ -74,6 +74,9 @@ size_t layout(const Problem& p, char* base, Workspace* ws) {
 
 // last CUDA error a libnats call on this host thread met
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+// test hook: the launch stage (nats_profile stage id) whose launch the next
+// layer forward on this thread replaces by a cudaErrorInvalidValue; -1 none
+thread_local int g_fail_stage = -1;
 
 nats_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return NATS_OK;
@@ -94,6 +97,10 @@ struct Stages {
 #define NATS_STAGE(stg, id, n_launch, expr)                                           \
   do {                                                                                \
     if ((stg).prof && (stg).mark((stg).prof->start, id) != cudaSuccess) return NATS_ERR_CUDA; \
+    if (g_fail_stage == (id)) {                                                       \
+      g_fail_stage = -1;                                                              \
+      return cuda_status(cudaErrorInvalidValue);                                      \
+    }                                                                                 \
     if (cuda_status(expr) != NATS_OK) return NATS_ERR_CUDA;                           \
     if ((stg).prof) {                                                                 \
       (stg).prof->launches += (n_launch);                                             \
@@ -160,6 +167,14 @@ const char* nats_status_string(nats_status s) {
 }
 
 const char* nats_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda_error); }
+
+void nats_debug_fail_stage(int32_t stage) { g_fail_stage = stage; }
+
+nats_status nats_debug_bounded_wait(int32_t* flag, int64_t limit_ns, nats_stream_t stream) {
+  if (!flag) return NATS_ERR_NULL;
+  if (limit_ns <= 0 || limit_ns > 1000000000LL) return NATS_ERR_VALUE;
+  return cuda_status(launch_bounded_wait(flag, limit_ns, (cudaStream_t)stream));
+}
 
 size_t nats_workspace_size(const nats_dims* dims) {
   if (check_dims(dims) != NATS_OK) return 0;

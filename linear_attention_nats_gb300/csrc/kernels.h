@@ -58,6 +58,9 @@ cudaError_t launch_decode_step(const Problem& p, int dtype, long long t, const v
                                void* kv_k, void* kv_v, int32_t* n_kv, long long cap, void* out,
                                uint8_t* sel_out, float* o_s_out, float* o_l_out, cudaStream_t st);
 
+// Test hook: one bounded wait that runs out after limit_ns and sets *flag.
+cudaError_t launch_bounded_wait(int* flag, long long limit_ns, cudaStream_t st);
+
 // bf16 path: out (holding w RMSNorm(o_s)) += (1 - w) RMSNorm(o_l).
 cudaError_t launch_merge_lin(const Problem& p, const float* o_l, const void* o_l16, const float* gate,
                              const float* nw_l, void* out, cudaStream_t st);

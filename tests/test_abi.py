@@ -158,3 +158,11 @@ def test_decode_validation(nat):
     assert call(d=bad) == 6                      # head size: NATS_ERR_UNSUPPORTED
     empty = nat.dims(0, 2, 0, 64)
     assert call(d=empty) == 0                    # nothing to do
+
+
+def test_debug_hook_validation(nat):
+    # the bounded-wait hook checks its arguments before any launch
+    assert nat.lib.nats_debug_bounded_wait(None, 1000, None) == 1           # NATS_ERR_NULL
+    assert nat.lib.nats_debug_bounded_wait(ctypes.c_void_p(256), 0, None) == 9  # NATS_ERR_VALUE
+    assert nat.lib.nats_debug_bounded_wait(ctypes.c_void_p(256), 2 * 10**9, None) == 9
+    nat.lib.nats_debug_fail_stage(-1)  # cancelling an injection is always allowed
