@@ -16,7 +16,7 @@ from gpu_util import TOL, rel_err, to_device
 pytestmark = pytest.mark.gpu
 
 
-def _decode(t_dev, inp, state, t0, t1):
+def _decode(t_dev, inp, state, t0, t1, nws=None, nwl=None):
     import linear_attention_nats_gb300 as nats
 
     B, H, d = inp.B, inp.H, inp.d
@@ -27,7 +27,7 @@ def _decode(t_dev, inp, state, t0, t1):
         q, k, v = (t_dev[n][:, :, t].contiguous() for n in ("q", "k", "v"))
         g, beta = (t_dev[n][:, :, t].contiguous() for n in ("g", "beta"))
         r = nats.decode_step(state, t, q, k, v, g, beta, t_dev["w_s"], t_dev["b_s"], t_dev["w_g"], t_dev["b_g"],
-                             sel_out=sel_buf, return_branches=True)
+                             norm_w_soft=nws, norm_w_lin=nwl, sel_out=sel_buf, return_branches=True)
         for n in ("out", "o_s", "o_l"):
             outs[n][:, :, t - t0] = r[n].float().cpu().numpy()
         if t % 64 == 63:
@@ -36,8 +36,10 @@ def _decode(t_dev, inp, state, t0, t1):
     return outs, (np.stack(sel, axis=-1) if sel else np.zeros((B, H, 0), np.uint8))
 
 
-@pytest.mark.parametrize("B,H,L,d,dtype,seed", [(1, 2, 256, 64, "f32", 31), (2, 4, 384, 128, "bf16", 32)])
-def test_decode_from_empty_matches_prefill_oracle(B, H, L, d, dtype, seed):
+@pytest.mark.parametrize("B,H,L,d,dtype,seed,norm", [
+    (1, 2, 256, 64, "f32", 31, False), (2, 4, 384, 128, "bf16", 32, False),
+    (1, 2, 256, 64, "bf16", 34, True), (1, 2, 192, 128, "f32", 35, True)])
+def test_decode_from_empty_matches_prefill_oracle(B, H, L, d, dtype, seed, norm):
     import linear_attention_nats_gb300 as nats
     from linear_attention_nats_gb300 import build
 
@@ -46,13 +48,19 @@ def test_decode_from_empty_matches_prefill_oracle(B, H, L, d, dtype, seed):
     t_dev = to_device(inp)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     state = nats.DecodeState(B, H, d, cap=L, dtype=tdt)
-    outs, sel = _decode(t_dev, inp, state, 0, L)
-    ref = oracle.forward_inputs(inp)
+    nw = {}
+    if norm:  # learnable RMSNorm weights of both branches
+        rng = np.random.default_rng(seed + 100)
+        nw = {"norm_w_soft": (1 + 0.2 * rng.standard_normal(d)).astype(np.float32),
+              "norm_w_lin": (1 + 0.2 * rng.standard_normal(d)).astype(np.float32)}
+    dev_nw = {k: torch.from_numpy(v).cuda() for k, v in nw.items()}
+    outs, sel = _decode(t_dev, inp, state, 0, L, dev_nw.get("norm_w_soft"), dev_nw.get("norm_w_lin"))
+    ref = oracle.forward_inputs(inp, **nw)
     assert np.array_equal(sel.reshape(ref["sel"].shape), ref["sel"])
     tol = TOL[dtype]
     errs = {n: rel_err(outs[n].reshape(ref[n].shape), ref[n]) for n in ("o_s", "o_l", "out")}
     errs["state"] = rel_err(state.S.cpu().numpy().reshape(ref["state"].shape), ref["state"])
-    print(f"[parity] decode {dtype}-{d}: " + " ".join(f"{k}={v:.2e}" for k, v in errs.items()))
+    print(f"[parity] decode {dtype}-{d}{' norm' if norm else ''}: " + " ".join(f"{k}={v:.2e}" for k, v in errs.items()))
     for n, e in errs.items():
         assert e <= tol, (n, e)
     # the retained keys are those of the softmax chunks, in order
@@ -60,13 +68,14 @@ def test_decode_from_empty_matches_prefill_oracle(B, H, L, d, dtype, seed):
     assert np.array_equal(n_kv, 64 * (ref["sel"].reshape(B, H, -1) == 0).sum(-1))
 
 
-def test_decode_continues_prefill():
+@pytest.mark.parametrize("B,H,L,L0,seed", [(2, 4, 448, 256, 33), (1, 2, 2112, 2048, 36)])
+def test_decode_continues_prefill(B, H, L, L0, seed):
     import linear_attention_nats_gb300 as nats
     from linear_attention_nats_gb300 import build
 
     build.build()
-    B, H, L, L0, d = 2, 4, 448, 256, 128
-    inp = gen.make_inputs(B, H, L, d, dtype="bf16", seed=33, pattern="random", frac=0.5)
+    d = 128
+    inp = gen.make_inputs(B, H, L, d, dtype="bf16", seed=seed, pattern="random", frac=0.5)
     t_dev = to_device(inp)
     # prefill of the first L0 tokens through the layer forward
     pre = nats.hybrid_fwd(t_dev["q"][:, :, :L0].contiguous(), t_dev["k"][:, :, :L0].contiguous(),
@@ -91,6 +100,6 @@ def test_decode_continues_prefill():
     assert np.array_equal(sel0.reshape(B * H, -1), ref["sel"][:, :N0])
     assert np.array_equal(sel.reshape(B * H, -1), ref["sel"][:, N0:])
     errs = {n: rel_err(outs[n].reshape(B * H, L - L0, d), ref[n][:, L0:]) for n in ("o_s", "o_l", "out")}
-    print("[parity] decode after prefill: " + " ".join(f"{k}={v:.2e}" for k, v in errs.items()))
+    print(f"[parity] decode after a {L0}-token prefill: " + " ".join(f"{k}={v:.2e}" for k, v in errs.items()))
     for n, e in errs.items():
         assert e <= TOL["bf16"], (n, e)
