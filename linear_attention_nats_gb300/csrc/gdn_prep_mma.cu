@@ -1,4 +1,5 @@
-// gdn_prep_mma.cu - Gated DeltaNet phase 1 on tensor cores (bf16 inputs):
+// gdn_prep_mma.cu - Gated DeltaNet phase 1 on warp-level tensor-core MMAs
+// (bf16 inputs, d = 64; d = 128 uses the tcgen05 pipeline of gdn_prep_tc.cu):
 // the per-chunk factors of the chunkwise WY/UT form, parallel over chunks.
 //
 // "Neural Attention Search Linear (NAtS-L)", technical summary,
@@ -492,8 +493,9 @@ cudaError_t launch_gdn_prep_mma(const Problem& p, const void* q, const void* k, 
         sel_out);
     return cudaGetLastError();
   };
-  return p.d == 64 ? run(gdn_prep_mma_kernel<64>, PrepSmem<64>::kBytes)
-                   : run(gdn_prep_mma_kernel<128>, PrepSmem<128>::kBytes);
+  // d = 128 takes the tcgen05 pipeline (gdn_prep_tc.cu)
+  if (p.d != 64) return cudaErrorInvalidValue;
+  return run(gdn_prep_mma_kernel<64>, PrepSmem<64>::kBytes);
 }
 
 }  // namespace nats
