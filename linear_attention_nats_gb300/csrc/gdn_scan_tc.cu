@@ -133,8 +133,8 @@ __global__ void __launch_bounds__(448, 1)
         uint8_t* Kb = WQ + S::kWQ;
         uint8_t* Ub = Kb + S::kK;
         uint8_t* Pb = Ub + S::kU;
-        const int yc = (int)((bh * N + c) * 64);   // row of this chunk in W / P
-        const int yt = (int)(bh * L + 64LL * c);   // row of this chunk in Q / K / G
+        const int yc = (int)((bh * N + c) * 64);   // row of this chunk in W / P / Q~ / K / ...
+        const int yt = (int)(bh * L + 64LL * c);   // row of this chunk in Q~ / K
         const int yu = (int)((bh * N + c) * D);    // first line of this chunk in U^T
         tc::mbar_arrive_expect_tx(&bars[SB_FULL + s], S::kStage + 64 * 4);
         tc::bulk_load_1d(smem + S::offG + s * 256, G + yt, 256, &bars[SB_FULL + s]);
