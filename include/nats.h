@@ -266,7 +266,7 @@ nats_status nats_debug_bounded_wait(int32_t* flag, int64_t limit_ns, nats_stream
  * sequence, it gives the outputs nats_hybrid_fwd gives for that sequence.
  *
  * The state is the caller's device memory, updated in place by each call;
- * all zeros (S, S0, psum, n_kv) is the empty state (ck, cv need no
+ * all zeros (S, S0, psum, n_kv, err) is the empty state (ck, cv need no
  * initialisation).  Layouts are contiguous, element type fp32 where marked,
  * else dims->dtype. */
 typedef struct {
@@ -279,6 +279,9 @@ typedef struct {
   void* kv_v;     /* [B, H, cap, dv] values of the retained chunks */
   int32_t* n_kv;  /* [B, H] retained tokens per head (a multiple of chunk) */
   int64_t cap;    /* tokens per head kv_k / kv_v hold */
+  int32_t* err;   /* [1] set to 1 by a step whose bounded wait for its key /
+                     value copies ran out (that step's outputs and state are
+                     then not valid); never cleared by the library */
 } nats_decode_state;
 
 /* One decode step.  dims: B, H, dk = dv (64 or 128), chunk (64), dtype,

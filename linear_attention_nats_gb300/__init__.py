@@ -182,8 +182,9 @@ class DecodeState:
     Gated DeltaNet state S and its chunk-start copy S0 (fp32 [B, H, d, d]), the
     current chunk's keys / values ck, cv ([B, H, 64, d]), the running sum of
     [q; k] over the chunk (fp32 [B, H, 2 d]), the retained keys / values kv_k,
-    kv_v ([B, H, cap, d]) and their count n_kv (int32 [B, H]).  New states are
-    empty (zeros)."""
+    kv_v ([B, H, cap, d]) and their count n_kv (int32 [B, H]), and the error
+    flag err (int32 [1], set by a step whose bounded wait for its copies ran
+    out; `check()` reads it).  New states are empty (zeros)."""
 
     def __init__(self, B: int, H: int, d: int, cap: int, dtype=torch.bfloat16, device="cuda"):
         z = dict(device=device)
@@ -196,11 +197,18 @@ class DecodeState:
         self.kv_k = torch.zeros((B, H, self.cap, d), dtype=dtype, **z)
         self.kv_v = torch.zeros((B, H, self.cap, d), dtype=dtype, **z)
         self.n_kv = torch.zeros((B, H), dtype=torch.int32, **z)
+        self.err = torch.zeros((1,), dtype=torch.int32, **z)
 
     def c_struct(self) -> _native.DecodeState:
         return _native.DecodeState(self.S.data_ptr(), self.S0.data_ptr(), self.ck.data_ptr(), self.cv.data_ptr(),
                                    self.psum.data_ptr(), self.kv_k.data_ptr(), self.kv_v.data_ptr(),
-                                   self.n_kv.data_ptr(), self.cap)
+                                   self.n_kv.data_ptr(), self.cap, self.err.data_ptr())
+
+    def check(self) -> None:
+        """Raises if a step since the state was made gave up waiting for its
+        key / value copies (synchronises with the device)."""
+        if int(self.err.item()) != 0:
+            raise _native.NatsError(8, "nats_decode_step (a bounded wait ran out)")
 
 
 def decode_step(state: DecodeState, t: int, q, k, v, g, beta, w_s, b_s, w_g, b_g=None, *, norm_w_soft=None,

@@ -41,7 +41,8 @@ class Profile(ctypes.Structure):
 class DecodeState(ctypes.Structure):
     _fields_ = [("S", ctypes.c_void_p), ("S0", ctypes.c_void_p), ("ck", ctypes.c_void_p), ("cv", ctypes.c_void_p),
                 ("psum", ctypes.c_void_p), ("kv_k", ctypes.c_void_p), ("kv_v", ctypes.c_void_p),
-                ("n_kv", ctypes.c_void_p), ("cap", ctypes.c_int64)]
+                ("n_kv", ctypes.c_void_p), ("cap", ctypes.c_int64),
+                ("err", ctypes.c_void_p)]
 
 
 class Dims(ctypes.Structure):

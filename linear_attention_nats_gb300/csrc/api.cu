@@ -334,14 +334,16 @@ nats_status nats_decode_step(const nats_dims* dims, int64_t t, const void* q, co
   if (p.BH == 0) return NATS_OK;
   if (!q || !k || !v || !g || !beta || !w_s || !w_g || !state || !out) return NATS_ERR_NULL;
   const nats_decode_state& st = *state;
-  if (!st.S || !st.S0 || !st.ck || !st.cv || !st.psum || !st.kv_k || !st.kv_v || !st.n_kv) return NATS_ERR_NULL;
+  if (!st.S || !st.S0 || !st.ck || !st.cv || !st.psum || !st.kv_k || !st.kv_v || !st.n_kv || !st.err)
+    return NATS_ERR_NULL;
   const void* ptrs[] = {q, k, v, out, st.S, st.S0, st.ck, st.cv, st.psum, st.kv_k, st.kv_v};
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return NATS_ERR_ALIGN;
   if (st.cap < (long long)kChunk * (t / kChunk + 1)) return NATS_ERR_WORKSPACE;
   return cuda_status(launch_decode_step(p, d.dtype, t, q, k, v, g, beta, w_s, b_s, w_g, b_g, norm_w_soft,
                                         norm_w_lin, st.S, st.S0, st.ck, st.cv, st.psum, st.kv_k, st.kv_v, st.n_kv,
-                                        st.cap, out, sel_out, o_soft_out, o_lin_out, (cudaStream_t)stream));
+                                        st.cap, out, sel_out, o_soft_out, o_lin_out, st.err,
+                                        (cudaStream_t)stream));
 }
 
 }  // extern "C"

@@ -2,40 +2,60 @@
 // launch ("Neural Attention Search Linear (NAtS-L)", technical summary,
 // "Kernmechanismen" items 1, 3 and 4, read token by token).
 //
-// A cluster of kSplit CTAs (256 threads each) per (b, h); the keys are split
-// between the cluster's CTAs, which keeps many more loads in flight than
-// one CTA per head:
+// A cluster of kSplit CTAs of 128 threads per (b, h), each taking an equal
+// share of the head's work, so that a step is one wave of small CTAs over
+// the whole GPU (four per SM):
 //   1. the token's q, k, v to shared memory (every CTA); CTA 0 appends k, v
-//      to the chunk's keys / values at position p = t % chunk;
-//   2. CTA 0: Gated DeltaNet, S <- a S (I - beta k k^T) + beta v k^T, i.e.
-//      row i of S becomes a S_i + beta (v_i - a S_i . k) k^T, and
-//      o_l = S (scale q), 256 / d threads per state row (fp32 state in
-//      global memory);
-//   3. CTAs 1 .. kSplit - 1: softmax over their share of the keys (the
-//      retained keys of earlier softmax chunks, then the chunk's keys up to
-//      the token): a warp takes its keys in batches of eight, lanes split the
-//      d features (one coalesced 256-byte row per key), the next batch's rows
-//      are loaded while the current one is scored; the eight dot products
-//      are summed over the warp by halving (nine shuffles); the CTA's warps
-//      are combined and its (max, sum, partial output) goes into CTA 0's
-//      shared memory (distributed shared memory) before a cluster barrier;
+//      to the chunk's keys / values at position p = t % chunk.  Thread 0
+//      starts the copies of the CTA's keys (below) before anything else;
+//   2. Gated DeltaNet on the CTA's d / kSplit rows of the fp32 state:
+//      S <- a S (I - beta k k^T) + beta v k^T, i.e. row i of S becomes
+//      a S_i + beta (v_i - a S_i . k) k^T, and o_l = S (scale q); the rows of
+//      o_l go to CTA 0's shared memory (distributed shared memory);
+//   3. softmax over the CTA's share of the keys held in memory (the retained
+//      keys of earlier softmax chunks, then the chunk's keys before the
+//      token), 32 keys per stage: one thread copies a stage's key and value
+//      rows (contiguous runs) into a ring of shared-memory stages with bulk
+//      async copies, up to three stages in flight, completing on an
+//      mbarrier; each warp scores eight rows of a stage, lanes over the d
+//      features, the eight dot products summed over the warp by halving
+//      (nine shuffles), online softmax, P V.  The token itself (the last
+//      key) is scored by one warp of the last CTA from shared memory.  The
+//      CTA's (max, sum, partial output) goes to CTA 0's shared memory before
+//      a cluster barrier;
 //   4. CTA 0: the kSplit partials combined, RMSNorm of both branches and the
-//      query-gated sum;
-//   5. CTA 0: the running [q; k] sum of the chunk; when the token completes
-//      the chunk: the chunk score and selection; softmax appends the chunk's
-//      keys and values to the retained ones and restores the state to the
-//      chunk start, Gated DeltaNet keeps the state as the new chunk start.
+//      query-gated sum; the running [q; k] sum of the chunk;
+//   5. when the token completes the chunk: every CTA computes the chunk's
+//      score and selection (the same arithmetic, so the same result) and
+//      applies it to its own state rows and its share of the chunk's keys
+//      and values: softmax appends them to the retained ones and restores
+//      the state to the chunk start, Gated DeltaNet keeps the state as the
+//      new chunk start.
+// Every wait is bounded: a copy that does not land in time sets *err and
+// the step finishes without it.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
 
 namespace nats {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
-constexpr int kSplit = 8;  // CTAs per (b, h) (a thread-block cluster): CTA 0 the state, CTAs 1.. the keys
+constexpr int kSplit = 8;                  // CTAs per (b, h): a thread-block cluster
+constexpr int kKeysPerStage = 8 * kWarps;  // eight rows per warp and stage
+
+// The ring of key / value stages in dynamic shared memory.
+template <typename T, int D>
+struct Ring {
+  static constexpr int kRow = D * (int)sizeof(T);        // bytes of one key (value) row
+  static constexpr int kHalf = kKeysPerStage * kRow;     // the key rows of a stage
+  static constexpr int kStage = 2 * kHalf;               // then its value rows
+  static constexpr int kStages = kStage <= 16384 ? 3 : 2;
+  static constexpr int kBytes = kStages * kStage;
+};
 
 template <int N>
 __device__ __forceinline__ void load_n(const float* p, float (&o)[N]) {
@@ -122,33 +142,86 @@ __device__ __forceinline__ void block_sum3(float& a, float& b, float& c, float (
   __syncthreads();
 }
 
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+// programmatic dependent launch: let the next kernel of the stream be
+// scheduled now; wait for the previous one to complete (its writes visible)
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 template <typename T, int D>
-__global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 1) decode_step_kernel(
+__global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 4) decode_step_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, const float* __restrict__ g,
     const float* __restrict__ beta, const float* __restrict__ w_s, const float* __restrict__ b_s,
     const float* __restrict__ w_g, const float* __restrict__ b_g, const float* __restrict__ nw_s,
     const float* __restrict__ nw_l, int H, int C, int p, float scale, float eps, float* __restrict__ S,
     float* __restrict__ S0, T* __restrict__ ck, T* __restrict__ cv, float* __restrict__ psum,
     T* __restrict__ kv_k, T* __restrict__ kv_v, int32_t* __restrict__ n_kv, long long cap, T* __restrict__ out,
-    uint8_t* __restrict__ sel_out, float* __restrict__ o_s_out, float* __restrict__ o_l_out) {
-  static_assert(D % 32 == 0 && D <= 128, "shape");
-  constexpr int CPT = 32;              // state columns per thread
-  constexpr int TPR = D / CPT;         // threads per state row
-  constexpr int RPP = kThreads / TPR;  // state rows per pass
-  constexpr int E = D / 32;            // features per lane in the softmax
+    uint8_t* __restrict__ sel_out, float* __restrict__ o_s_out, float* __restrict__ o_l_out, int* err) {
+  static_assert(D % 32 == 0 && D <= 128 && D % kSplit == 0, "shape");
+  using R = Ring<T, D>;
+  constexpr int RPC = D / kSplit;       // state rows per CTA
+  constexpr int TPR = kThreads / RPC;   // threads per state row
+  constexpr int CPT = D / TPR;          // state columns per thread
+  constexpr int E = D / 32;             // features per lane in the softmax
+  static_assert(TPR <= 32 && CPT % 4 == 0, "state split");
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const long long bh = blockIdx.x / kSplit;
   const int h = (int)(bh % H);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ uint64_t full[R::kStages];
   __shared__ __align__(16) float qs[D], ks[D], vs[D], os[D], ol[D];
-  __shared__ __align__(16) float wo[kWarps][D];
   __shared__ float wm[kWarps], wl[kWarps];
   __shared__ float red[kWarps][3];
   __shared__ __align__(16) float part_o[kSplit][D];  // CTA 0: the cluster's partial outputs
   __shared__ float part_m[kSplit], part_l[kSplit];
   __shared__ int sel_sh;
+
+  cluster_arrive_relaxed();  // waited for before the first access to CTA 0's shared memory
+  launch_dependents();
+  if (tid == 0)
+    for (int i = 0; i < R::kStages; ++i) tc::mbar_init(&full[i], 1);
+  // nothing before this point reads global memory: every input, the state
+  // included, may be written by the preceding kernel of the stream
+  wait_prerequisites();
+
+  // the keys held in memory, nr retained then p of the chunk; this CTA's [lo, hi)
+  const int nr = n_kv[bh];
+  const int nm = nr + p;
+  const int lo = (int)((long long)nm * rank / kSplit), hi = (int)((long long)nm * (rank + 1) / kSplit);
+  const int nst = (hi - lo + kKeysPerStage - 1) / kKeysPerStage;
+  const T* Kr = kv_k + bh * cap * D;
+  const T* Vr = kv_v + bh * cap * D;
+  const T* Kc = ck + bh * C * D;
+  const T* Vc = cv + bh * C * D;
+  // stage s (keys [lo + 32 s, ...) of the CTA) into slot s % kStages: the
+  // retained rows and the chunk's rows are two contiguous runs
+  auto issue = [&](int s) {
+    uint8_t* kb = ring + (s % R::kStages) * R::kStage;
+    uint8_t* vb = kb + R::kHalf;
+    uint64_t* bar = &full[s % R::kStages];
+    const int a0 = lo + s * kKeysPerStage, a1 = min(a0 + kKeysPerStage, hi);
+    const int m = min(max(nr, a0), a1);  // [a0, m) retained, [m, a1) of the chunk
+    tc::mbar_arrive_expect_tx(bar, (uint32_t)((a1 - a0) * 2 * R::kRow));
+    if (m > a0) {
+      tc::bulk_load_1d(kb, Kr + (long long)a0 * D, (uint32_t)((m - a0) * R::kRow), bar);
+      tc::bulk_load_1d(vb, Vr + (long long)a0 * D, (uint32_t)((m - a0) * R::kRow), bar);
+    }
+    if (a1 > m) {
+      tc::bulk_load_1d(kb + (m - a0) * R::kRow, Kc + (long long)(m - nr) * D, (uint32_t)((a1 - m) * R::kRow), bar);
+      tc::bulk_load_1d(vb + (m - a0) * R::kRow, Vc + (long long)(m - nr) * D, (uint32_t)((a1 - m) * R::kRow), bar);
+    }
+  };
+  int issued = 0;  // (thread 0)
+  if (tid == 0) {
+    tc::fence_barrier_init();
+    for (; issued < min(nst, R::kStages); ++issued) issue(issued);
+  }
 
   // 1. the token
   if (tid < D) {
@@ -162,159 +235,208 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 1) de
     }
   }
   const float a = __expf(g[bh]), bt = beta[bh];
-  __syncthreads();
+  // operands of the epilogue and of the chunk's selection, read now so that
+  // no global load follows the cluster barrier
+  constexpr int PE = (2 * D + kThreads - 1) / kThreads;  // running-sum entries per thread
+  const bool last = p == C - 1;
+  float psv[PE], ws0[PE], ws1[PE];
+#pragma unroll
+  for (int i = 0; i < PE; ++i) {
+    const int e = tid + i * kThreads;
+    psv[i] = ws0[i] = ws1[i] = 0.f;
+    if (e < 2 * D && (rank == 0 || last)) psv[i] = psum[bh * 2 * D + e];
+    if (e < 2 * D && last) {
+      ws0[i] = w_s[((long long)h * 2 + 0) * 2 * D + e];
+      ws1[i] = w_s[((long long)h * 2 + 1) * 2 * D + e];
+    }
+  }
+  float wg = 0.f, nws = 1.f, nwl = 1.f, bg = 0.f;
+  if (rank == 0 && tid < D) {
+    wg = w_g[(long long)h * D + tid];
+    if (nw_s) nws = nw_s[tid];
+    if (nw_l) nwl = nw_l[tid];
+    if (b_g) bg = b_g[h];
+  }
+  __syncthreads();  // also: the barriers are initialised
 
-  // 2. Gated DeltaNet state update and readout (CTA 0)
-  if (rank == 0) {
-#pragma unroll 1
-    for (int row0 = 0; row0 < D; row0 += RPP) {
-      const int row = row0 + tid / TPR, part = tid % TPR;
-      if (RPP > D && row >= D) break;  // (d = 64: half the threads have no row); warp-uniform
-      float* srow = S + (bh * D + row) * D + part * CPT;
-      float sv[CPT];
-      load_n<CPT>(srow, sv);
-      float u = 0.f;
+  // 2. Gated DeltaNet on this CTA's state rows
+  {
+    const int row = rank * RPC + tid / TPR, part = tid % TPR;
+    float* srow = S + (bh * D + row) * D + part * CPT;
+    float sv[CPT];
+    load_n<CPT>(srow, sv);
+    float u = 0.f;
 #pragma unroll
-      for (int j = 0; j < CPT; ++j) u = fmaf(sv[j], ks[part * CPT + j], u);
+    for (int j = 0; j < CPT; ++j) u = fmaf(sv[j], ks[part * CPT + j], u);
 #pragma unroll
-      for (int o = 1; o < TPR; o <<= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
-      const float coef = bt * (vs[row] - a * u);
-      float r = 0.f;
+    for (int o = 1; o < TPR; o <<= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
+    const float coef = bt * (vs[row] - a * u);
+    float r = 0.f;
 #pragma unroll
-      for (int j = 0; j < CPT; ++j) {
-        sv[j] = fmaf(a, sv[j], coef * ks[part * CPT + j]);
-        r = fmaf(sv[j], qs[part * CPT + j], r);
+    for (int j = 0; j < CPT; ++j) {
+      sv[j] = fmaf(a, sv[j], coef * ks[part * CPT + j]);
+      r = fmaf(sv[j], qs[part * CPT + j], r);
+    }
+#pragma unroll
+    for (int o = 1; o < TPR; o <<= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+#pragma unroll
+    for (int j = 0; j < CPT; j += 4) *(float4*)(srow + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
+    cluster_wait();  // every CTA of the cluster is running
+    if (part == 0) *cluster.map_shared_rank(&ol[row], 0) = r * scale;
+  }
+
+  // 3. softmax over the CTA's keys
+  float qv[E];
+#pragma unroll
+  for (int x = 0; x < E; ++x) qv[x] = qs[lane * E + x];
+  float m = -INFINITY, l = 0.f, acc[E];
+#pragma unroll
+  for (int x = 0; x < E; ++x) acc[x] = 0.f;
+  using RV = Raw<T, E>;
+  // the 8 keys from j0 (valid below hi): scores (partial dot products summed
+  // over the warp by halving: lane (b4 b3 b2 . .) ends with key 4 b4 + 2 b3 +
+  // b2), online softmax, P V
+  auto batch = [&](int j0, const RV (&kb)[8], const RV (&vb)[8]) {
+    float dp[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      float kk[E];
+      kb[u].get(kk);
+      dp[u] = 0.f;
+#pragma unroll
+      for (int x = 0; x < E; ++x) dp[u] = fmaf(qv[x], kk[x], dp[u]);
+    }
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float d4[4], d2[2];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) d4[u] = (b4 ? dp[4 + u] : dp[u]) + __shfl_xor_sync(0xffffffffu, b4 ? dp[u] : dp[4 + u], 16);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) d2[u] = (b3 ? d4[2 + u] : d4[u]) + __shfl_xor_sync(0xffffffffu, b3 ? d4[u] : d4[2 + u], 8);
+    float d1 = (b2 ? d2[1] : d2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? d2[0] : d2[1], 4);
+    d1 += __shfl_xor_sync(0xffffffffu, d1, 2);
+    d1 += __shfl_xor_sync(0xffffffffu, d1, 1);
+    const int ku = 4 * (lane >> 4) + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
+    const float sc = (j0 + ku < hi) ? d1 * scale : -INFINITY;
+    float mb = sc;
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
+    const float mn = fmaxf(m, mb);
+    const float alpha = __expf(m - mn);  // 0 on the first batch (m = -inf)
+    const float pu = (j0 + ku < hi) ? __expf(sc - mn) : 0.f;
+    float ps = pu;
+    ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+    ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+    ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+    l = l * alpha + ps;
+    m = mn;
+#pragma unroll
+    for (int x = 0; x < E; ++x) acc[x] *= alpha;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float pw = __shfl_sync(0xffffffffu, pu, ((u >> 2) << 4) | (((u >> 1) & 1) << 3) | ((u & 1) << 2));
+      float vv[E];
+      vb[u].get(vv);
+#pragma unroll
+      for (int x = 0; x < E; ++x) acc[x] = fmaf(pw, vv[x], acc[x]);
+    }
+  };
+  bool ok = true;
+  int s = 0;
+  for (; s < nst; ++s) {
+    const int slot = s % R::kStages;
+    const bool wok = __all_sync(0xffffffffu, tc::mbar_wait(&full[slot], (uint32_t)((s / R::kStages) & 1), err));
+    if (wok && lo + s * kKeysPerStage + 8 * warp < hi) {
+      const uint8_t* kb = ring + slot * R::kStage + 8 * warp * R::kRow;
+      const uint8_t* vb = kb + R::kHalf;
+      const int j0 = lo + s * kKeysPerStage + 8 * warp;
+      RV kr[8], vr[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (j0 + u < hi) {
+          kr[u].load((const T*)(kb + u * R::kRow) + lane * E);
+          vr[u].load((const T*)(vb + u * R::kRow) + lane * E);
+        } else {
+          kr[u].zero();
+          vr[u].zero();
+        }
       }
+      batch(j0, kr, vr);
+    }
+    ok = __syncthreads_and(wok) != 0;  // the slot is read by every warp
+    if (!ok) break;
+    if (tid == 0 && issued < nst) issue(issued++);
+  }
+  if (!ok && tid == 0) {
+    // a copy did not land in time: wait (bounded) for those still in flight
+    // into this CTA's shared memory before it is released
+    for (int i = s; i < issued; ++i)
+      tc::mbar_wait(&full[i % R::kStages], (uint32_t)((i / R::kStages) & 1), err);
+  }
+  // the token (the last key), from shared memory
+  if (rank == kSplit - 1 && warp == 0) {
+    float dp = 0.f;
 #pragma unroll
-      for (int o = 1; o < TPR; o <<= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    for (int x = 0; x < E; ++x) dp = fmaf(qv[x], ks[lane * E + x], dp);
+    const float sc = warp_sum(dp) * scale;
+    const float mn = fmaxf(m, sc);
+    const float alpha = __expf(m - mn), pw = __expf(sc - mn);
+    l = l * alpha + pw;
+    m = mn;
 #pragma unroll
-      for (int j = 0; j < CPT; j += 4)
-        *(float4*)(srow + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
-      if (part == 0) ol[row] = r * scale;
+    for (int x = 0; x < E; ++x) acc[x] = fmaf(pw, vs[lane * E + x], acc[x] * alpha);
+  }
+  __syncthreads();  // the ring is free: the warps' partials go there
+  float* wo = (float*)ring;  // [kWarps][D]
+  if (lane == 0) wm[warp] = m, wl[warp] = l;
+#pragma unroll
+  for (int x = 0; x < E; ++x) wo[warp * D + lane * E + x] = acc[x];
+  __syncthreads();
+  // this CTA's (max, sum, unnormalised output) into CTA 0's shared memory
+  if (tid < D) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w]);
+    float L = 0.f, o = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = wm[w] == -INFINITY ? 0.f : __expf(wm[w] - M);
+      L = fmaf(wl[w], f, L);
+      o = fmaf(wo[w * D + tid], f, o);
+    }
+    *cluster.map_shared_rank(&part_o[rank][tid], 0) = o;
+    if (tid == 0) {
+      *cluster.map_shared_rank(&part_m[rank], 0) = M;
+      *cluster.map_shared_rank(&part_l[rank], 0) = L;
     }
   }
 
-  // 3. softmax over the retained keys and the chunk's keys up to the token
-  {
-    const int nr = n_kv[bh];
-    const int n = nr + p + 1;  // key n - 1 is this token (taken from shared memory)
-    // keys [lo, hi) of this CTA (CTA 0 has none), [wlo, whi) of this warp
-    const int nk = kSplit - 1, kr_ = rank - 1;
-    const int lo = rank == 0 ? 0 : (int)((long long)n * kr_ / nk), hi = rank == 0 ? 0 : (int)((long long)n * (kr_ + 1) / nk);
-    const int wlo = lo + (int)((long long)(hi - lo) * warp / kWarps), whi = lo + (int)((long long)(hi - lo) * (warp + 1) / kWarps);
-    const T* Kr = kv_k + bh * cap * D;
-    const T* Vr = kv_v + bh * cap * D;
-    const T* Kc = ck + bh * C * D;
-    const T* Vc = cv + bh * C * D;
-    float qv[E];
+  // the chunk's score and selection at its last token (every CTA, from the
+  // running sum read before the barrier, after which CTA 0 rewrites it)
 #pragma unroll
-    for (int x = 0; x < E; ++x) qv[x] = qs[lane * E + x];
-    float m = -INFINITY, l = 0.f, acc[E];
+  for (int i = 0; i < PE; ++i) {
+    const int e = tid + i * kThreads;
+    if (e < 2 * D) psv[i] += e < D ? qs[e] : ks[e - D];
+  }
+  if (last) {
+    float s0 = 0.f, s1 = 0.f, unused = 0.f;
 #pragma unroll
-    for (int x = 0; x < E; ++x) acc[x] = 0.f;
-    // lane's E features of key / value row j, in storage form (zeros past
-    // the end of the warp's keys; this token's from the inputs)
-    using RV = Raw<T, E>;
-    auto fetch = [&](int j, RV (&kb)[8], RV (&vb)[8], int u) {
-      if (j >= whi) {
-        kb[u].zero();
-        vb[u].zero();
-      } else if (j == n - 1) {
-        kb[u].load(k + bh * D + lane * E);
-        vb[u].load(v + bh * D + lane * E);
-      } else {
-        const long long off = (j < nr ? (long long)j : (long long)(j - nr)) * D + lane * E;
-        kb[u].load((j < nr ? Kr : Kc) + off);
-        vb[u].load((j < nr ? Vr : Vc) + off);
-      }
-    };
-    auto fetch8 = [&](int j0, RV (&kb)[8], RV (&vb)[8]) {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) fetch(j0 + u, kb, vb, u);
-    };
-    // the 8 keys from j0: scores (partial dot products summed over the warp
-    // by halving: lane (b4 b3 b2 . .) ends with key 4 b4 + 2 b3 + b2), online
-    // softmax, P V
-    auto batch = [&](int j0, const RV (&kb)[8], const RV (&vb)[8]) {
-      float dp[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        float kk[E];
-        kb[u].get(kk);
-        dp[u] = 0.f;
-#pragma unroll
-        for (int x = 0; x < E; ++x) dp[u] = fmaf(qv[x], kk[x], dp[u]);
-      }
-      const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-      float d4[4], d2[2];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) d4[u] = (b4 ? dp[4 + u] : dp[u]) + __shfl_xor_sync(0xffffffffu, b4 ? dp[u] : dp[4 + u], 16);
-#pragma unroll
-      for (int u = 0; u < 2; ++u) d2[u] = (b3 ? d4[2 + u] : d4[u]) + __shfl_xor_sync(0xffffffffu, b3 ? d4[u] : d4[2 + u], 8);
-      float d1 = (b2 ? d2[1] : d2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? d2[0] : d2[1], 4);
-      d1 += __shfl_xor_sync(0xffffffffu, d1, 2);
-      d1 += __shfl_xor_sync(0xffffffffu, d1, 1);
-      const int ku = 4 * (lane >> 4) + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
-      const float sc = (j0 + ku < whi) ? d1 * scale : -INFINITY;
-      float mb = sc;
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
-      const float mn = fmaxf(m, mb);
-      const float alpha = __expf(m - mn);  // 0 on the first batch (m = -inf)
-      const float pu = (j0 + ku < whi) ? __expf(sc - mn) : 0.f;
-      float ps = pu;
-      ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-      ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-      ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-      l = l * alpha + ps;
-      m = mn;
-#pragma unroll
-      for (int x = 0; x < E; ++x) acc[x] *= alpha;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float pw = __shfl_sync(0xffffffffu, pu, ((u >> 2) << 4) | (((u >> 1) & 1) << 3) | ((u & 1) << 2));
-        float vv[E];
-        vb[u].get(vv);
-#pragma unroll
-        for (int x = 0; x < E; ++x) acc[x] = fmaf(pw, vv[x], acc[x]);
-      }
-    };
-    // two batches of rows in flight: the next one loads while one is scored
-    RV k0[8], v0[8], k1[8], v1[8];
-    if (wlo < whi) fetch8(wlo, k0, v0);
-    for (int j0 = wlo; j0 < whi; j0 += 16) {
-      fetch8(j0 + 8, k1, v1);
-      batch(j0, k0, v0);
-      if (j0 + 8 >= whi) break;
-      fetch8(j0 + 16, k0, v0);
-      batch(j0 + 8, k1, v1);
+    for (int i = 0; i < PE; ++i) {
+      s0 = fmaf(ws0[i], psv[i], s0);
+      s1 = fmaf(ws1[i], psv[i], s1);
     }
-    if (lane == 0) wm[warp] = m, wl[warp] = l;
-#pragma unroll
-    for (int x = 0; x < E; ++x) wo[warp][lane * E + x] = acc[x];
-    __syncthreads();
-    // this CTA's (max, sum, unnormalised output) into CTA 0's shared memory
-    float* po = cluster.map_shared_rank(&part_o[rank][0], 0);
-    if (tid < D) {
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w]);
-      float L = 0.f, o = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float f = wm[w] == -INFINITY ? 0.f : __expf(wm[w] - M);
-        L = fmaf(wl[w], f, L);
-        o = fmaf(wo[w][tid], f, o);
-      }
-      po[tid] = o;
-      if (tid == 0) {
-        *cluster.map_shared_rank(&part_m[rank], 0) = M;
-        *cluster.map_shared_rank(&part_l[rank], 0) = L;
-      }
+    block_sum3(s0, s1, unused, red);
+    if (tid == 0) {
+      const float a0 = s0 / C + (b_s ? b_s[2 * h] : 0.f);
+      const float a1 = s1 / C + (b_s ? b_s[2 * h + 1] : 0.f);
+      sel_sh = (a0 >= a1) ? 0 : 1;
     }
-    cluster.sync();
-    if (rank != 0) return;  // only CTA 0's shared memory is read after the barrier
+  }
+  cluster.sync();
+  if (!ok && tid == 0) atomicExch(err, 1);
+
+  if (rank == 0) {
+    // 4. the partials combined; RMSNorm of each branch and the query-gated sum
     if (tid < D) {
       float M = -INFINITY;
 #pragma unroll
@@ -328,74 +450,86 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 1) de
       }
       os[tid] = o / L;
     }
-    __syncthreads();
-  }
-
-  // 4. RMSNorm of each branch and the query-gated sum
-  {
     float ss_s = 0.f, ss_l = 0.f, z = 0.f;
     if (tid < D) {
       ss_s = os[tid] * os[tid];
       ss_l = ol[tid] * ol[tid];
-      z = qs[tid] * w_g[(long long)h * D + tid];
+      z = qs[tid] * wg;
     }
     block_sum3(ss_s, ss_l, z, red);
     if (tid < D) {
-      const float w = 1.f / (1.f + __expf(-(z + (b_g ? b_g[h] : 0.f))));
-      const float ns = os[tid] * rsqrtf(ss_s / D + eps) * (nw_s ? nw_s[tid] : 1.f);
-      const float nl = ol[tid] * rsqrtf(ss_l / D + eps) * (nw_l ? nw_l[tid] : 1.f);
+      const float w = 1.f / (1.f + __expf(-(z + bg)));
+      const float ns = os[tid] * rsqrtf(ss_s / D + eps) * nws;
+      const float nl = ol[tid] * rsqrtf(ss_l / D + eps) * nwl;
       out[bh * D + tid] = from_f32<T>(w * ns + (1.f - w) * nl);
       if (o_s_out) o_s_out[bh * D + tid] = os[tid];
       if (o_l_out) o_l_out[bh * D + tid] = ol[tid];
     }
+    // the chunk's running [q; k] sum (restarted after its last token)
+#pragma unroll
+    for (int i = 0; i < PE; ++i) {
+      const int e = tid + i * kThreads;
+      if (e < 2 * D) psum[bh * 2 * D + e] = last ? 0.f : psv[i];
+    }
   }
+  if (!last) return;
 
-  // 5. the chunk's [q; k] sum; at the chunk's last token the selection,
-  //    then commit or rollback
-  float ps = 0.f;
-  if (tid < 2 * D) {
-    ps = psum[bh * 2 * D + tid] + (tid < D ? qs[tid] : ks[tid - D]);
-    psum[bh * 2 * D + tid] = ps;
-  }
-  if (p != C - 1) return;
-  {
-    float s0 = 0.f, s1 = 0.f, unused = 0.f;
-    if (tid < 2 * D) {
-      s0 = w_s[((long long)h * 2 + 0) * 2 * D + tid] * ps;
-      s1 = w_s[((long long)h * 2 + 1) * 2 * D + tid] * ps;
-    }
-    block_sum3(s0, s1, unused, red);
-    if (tid == 0) {
-      const float a0 = s0 / C + (b_s ? b_s[2 * h] : 0.f);
-      const float a1 = s1 / C + (b_s ? b_s[2 * h + 1] : 0.f);
-      sel_sh = (a0 >= a1) ? 0 : 1;
-    }
-    __syncthreads();  // also: every thread's state row is written
-  }
+  // 5. commit or rollback of this CTA's state rows and its share of the
+  //    chunk's keys / values
   const int sel = sel_sh;
-  if (tid < 2 * D) psum[bh * 2 * D + tid] = 0.f;
-  float* Sh = S + bh * D * D;
-  float* S0h = S0 + bh * D * D;
+  float4* Sh = (float4*)(S + (bh * D + rank * RPC) * D);
+  float4* S0h = (float4*)(S0 + (bh * D + rank * RPC) * D);
   if (sel == 0) {
-    // softmax: the chunk's keys / values join the retained ones; the state
-    // returns to the chunk start
-    const int nr = n_kv[bh];
-    T* dk = kv_k + (bh * cap + nr) * D;
-    T* dv = kv_v + (bh * cap + nr) * D;
-    const T* sk = ck + bh * C * D;
-    const T* sv = cv + bh * C * D;
-    for (int e = tid; e < C * D; e += kThreads) {
-      dk[e] = sk[e];
-      dv[e] = sv[e];
+    // softmax: the chunk's keys / values join the retained ones (the last
+    // one is this token); the state returns to the chunk start
+    constexpr int RC = kChunk / kSplit;  // chunk rows per CTA
+    for (int e = tid; e < RC * D; e += kThreads) {
+      const int j = rank * RC + e / D, c = e % D;
+      const long long dst = (bh * cap + nr + j) * D + c;
+      kv_k[dst] = j == C - 1 ? from_f32<T>(ks[c]) : Kc[(long long)j * D + c];
+      kv_v[dst] = j == C - 1 ? from_f32<T>(vs[c]) : Vc[(long long)j * D + c];
     }
-    for (int e = tid; e < D * D / 4; e += kThreads) ((float4*)Sh)[e] = ((const float4*)S0h)[e];
-    __syncthreads();
-    if (tid == 0) n_kv[bh] = nr + C;
+    for (int e = tid; e < RPC * D / 4; e += kThreads) Sh[e] = S0h[e];
+    if (rank == 0 && tid == 0) n_kv[bh] = nr + C;
   } else {
     // Gated DeltaNet: the state is committed and starts the next chunk
-    for (int e = tid; e < D * D / 4; e += kThreads) ((float4*)S0h)[e] = ((const float4*)Sh)[e];
+    for (int e = tid; e < RPC * D / 4; e += kThreads) S0h[e] = Sh[e];
   }
-  if (tid == 0 && sel_out) sel_out[bh] = (uint8_t)sel;
+  if (rank == 0 && tid == 0 && sel_out) sel_out[bh] = (uint8_t)sel;
+}
+
+// one (dtype, d) instantiation: its ring is dynamic shared memory, and the
+// largest carveout keeps four CTAs per SM (attributes set once per kernel)
+template <typename T, int D>
+cudaError_t launch_one(const Problem& p, int pos, const void* q, const void* k, const void* v, const float* g,
+                       const float* beta, const float* w_s, const float* b_s, const float* w_g, const float* b_g,
+                       const float* nw_s, const float* nw_l, float* S, float* S0, void* ck, void* cv,
+                       float* psum, void* kv_k, void* kv_v, int32_t* n_kv, long long cap, void* out,
+                       uint8_t* sel_out, float* o_s_out, float* o_l_out, int* err, cudaStream_t st) {
+  constexpr int smem = Ring<T, D>::kBytes;
+  static const cudaError_t attr = [] {
+    cudaError_t e = cudaFuncSetAttribute(decode_step_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_step_kernel<T, D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
+    return e;
+  }();
+  if (attr != cudaSuccess) return attr;
+  // programmatic stream serialization: the kernel may start while the
+  // previous one in the stream finishes (it waits for it before reading)
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.BH * kSplit));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_step_kernel<T, D>, (const T*)q, (const T*)k, (const T*)v, g, beta, w_s,
+                            b_s, w_g, b_g, nw_s, nw_l, (int)p.H, (int)kChunk, pos, p.scale, p.eps, S, S0, (T*)ck,
+                            (T*)cv, psum, (T*)kv_k, (T*)kv_v, n_kv, cap, (T*)out, sel_out, o_s_out, o_l_out, err);
 }
 
 }  // namespace
@@ -405,22 +539,14 @@ cudaError_t launch_decode_step(const Problem& p, int dtype, long long t, const v
                                const float* b_s, const float* w_g, const float* b_g, const float* nw_s,
                                const float* nw_l, float* S, float* S0, void* ck, void* cv, float* psum,
                                void* kv_k, void* kv_v, int32_t* n_kv, long long cap, void* out,
-                               uint8_t* sel_out, float* o_s_out, float* o_l_out, cudaStream_t st) {
+                               uint8_t* sel_out, float* o_s_out, float* o_l_out, int* err, cudaStream_t st) {
   if (p.BH == 0) return cudaSuccess;
   const int pos = (int)(t % kChunk);
-  auto run = [&](auto kern, auto tag) -> cudaError_t {
-    using T = decltype(tag);
-    kern<<<(unsigned)(p.BH * kSplit), kThreads, 0, st>>>(
-        (const T*)q, (const T*)k, (const T*)v, g, beta, w_s, b_s, w_g, b_g, nw_s, nw_l, p.H, kChunk, pos,
-        p.scale, p.eps, S, S0, (T*)ck, (T*)cv, psum, (T*)kv_k, (T*)kv_v, n_kv, cap, (T*)out, sel_out, o_s_out,
-        o_l_out);
-    return cudaGetLastError();
-  };
-  if (dtype == 0) {  // NATS_BF16
-    return p.d == 64 ? run(decode_step_kernel<__nv_bfloat16, 64>, __nv_bfloat16())
-                     : run(decode_step_kernel<__nv_bfloat16, 128>, __nv_bfloat16());
-  }
-  return p.d == 64 ? run(decode_step_kernel<float, 64>, 0.f) : run(decode_step_kernel<float, 128>, 0.f);
+  using bf = __nv_bfloat16;
+  auto* fn = dtype == 0 ? (p.d == 64 ? launch_one<bf, 64> : launch_one<bf, 128>)  // NATS_BF16
+                        : (p.d == 64 ? launch_one<float, 64> : launch_one<float, 128>);
+  return fn(p, pos, q, k, v, g, beta, w_s, b_s, w_g, b_g, nw_s, nw_l, S, S0, ck, cv, psum, kv_k, kv_v, n_kv, cap,
+            out, sel_out, o_s_out, o_l_out, err, st);
 }
 
 }  // namespace nats

@@ -56,7 +56,7 @@ cudaError_t launch_decode_step(const Problem& p, int dtype, long long t, const v
                                const float* b_s, const float* w_g, const float* b_g, const float* nw_s,
                                const float* nw_l, float* S, float* S0, void* ck, void* cv, float* psum,
                                void* kv_k, void* kv_v, int32_t* n_kv, long long cap, void* out,
-                               uint8_t* sel_out, float* o_s_out, float* o_l_out, cudaStream_t st);
+                               uint8_t* sel_out, float* o_s_out, float* o_l_out, int* err, cudaStream_t st);
 
 // Test hook: one bounded wait that runs out after limit_ns and sets *flag.
 cudaError_t launch_bounded_wait(int* flag, long long limit_ns, cudaStream_t st);

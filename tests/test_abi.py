@@ -142,7 +142,9 @@ def test_decode_validation(nat):
     fake = ctypes.c_void_p(256)  # 16-byte aligned, never dereferenced on these paths
     odd = ctypes.c_void_p(264)   # 8-byte aligned only
     st = nat.DecodeState(fake.value, fake.value, fake.value, fake.value, fake.value, fake.value, fake.value,
-                         fake.value, 64)
+                         fake.value, 64, fake.value)
+    no_err = nat.DecodeState(fake.value, fake.value, fake.value, fake.value, fake.value, fake.value, fake.value,
+                             fake.value, 64, None)
     args = [fake] * 11
     tail = [fake, None, None, None, None]
 
@@ -153,6 +155,7 @@ def test_decode_validation(nat):
     assert call(t=64) == 5                       # cap 64 cannot take a second chunk: NATS_ERR_WORKSPACE
     assert call(a=[None] + args[1:]) == 1        # q NULL
     assert call(s=None) == 1                     # state NULL
+    assert call(s=no_err) == 1                   # state without its error flag
     assert call(a=[odd] + args[1:]) == 4         # q misaligned: NATS_ERR_ALIGN
     bad = nat.dims(1, 2, 0, 96)
     assert call(d=bad) == 6                      # head size: NATS_ERR_UNSUPPORTED

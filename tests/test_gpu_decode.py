@@ -33,6 +33,7 @@ def _decode(t_dev, inp, state, t0, t1, nws=None, nwl=None):
         if t % 64 == 63:
             sel.append(sel_buf.cpu().numpy().copy())
     torch.cuda.synchronize()
+    state.check()
     return outs, (np.stack(sel, axis=-1) if sel else np.zeros((B, H, 0), np.uint8))
 
 
