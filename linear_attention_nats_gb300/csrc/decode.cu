@@ -2,27 +2,32 @@
 // launch ("Neural Attention Search Linear (NAtS-L)", technical summary,
 // "Kernmechanismen" items 1, 3 and 4, read token by token).
 //
-// A cluster of kSplit CTAs of 128 threads per (b, h), each taking an equal
-// share of the head's work, so that a step is one wave of small CTAs over
-// the whole GPU (four per SM):
+// A cluster of kSplit CTAs of 128 threads per (b, h), sharing the head's
+// work, so that a step is one wave of small CTAs over the whole GPU (four
+// per SM):
 //   1. the token's q, k, v to shared memory (every CTA); CTA 0 appends k, v
-//      to the chunk's keys / values at position p = t % chunk.  Thread 0
-//      starts the copies of the CTA's keys (below) before anything else;
-//   2. Gated DeltaNet on the CTA's d / kSplit rows of the fp32 state:
-//      S <- a S (I - beta k k^T) + beta v k^T, i.e. row i of S becomes
-//      a S_i + beta (v_i - a S_i . k) k^T, and o_l = S (scale q); the rows of
-//      o_l go to CTA 0's shared memory (distributed shared memory);
-//   3. softmax over the CTA's share of the keys held in memory (the retained
-//      keys of earlier softmax chunks, then the chunk's keys before the
-//      token), 32 keys per stage: one thread copies a stage's key and value
-//      rows (contiguous runs) into a ring of shared-memory stages with bulk
-//      async copies, up to three stages in flight, completing on an
-//      mbarrier; each warp scores eight rows of a stage, lanes over the d
+//      to the chunk's keys / values at position p = t % chunk.  The
+//      CTA's state rows are requested first, then thread 0 starts the copies
+//      of the CTA's keys (below);
+//   2. softmax over the keys held in memory (the retained keys of earlier
+//      softmax chunks, then the chunk's keys before the token) in blocks of
+//      32, which the cluster's CTAs claim one at a time from a counter in
+//      CTA 0's shared memory (distributed shared memory atomics), so that a
+//      CTA whose copies land sooner takes more of them: one thread copies a
+//      claimed block's key and value rows (contiguous runs) into a ring of
+//      shared-memory stages with bulk async copies, up to three stages in
+//      flight, completing on an mbarrier; each warp scores eight rows of a
+//      stage, lanes over the d
 //      features, the eight dot products summed over the warp by halving
 //      (nine shuffles), online softmax, P V.  The token itself (the last
-//      key) is scored by one warp of the last CTA from shared memory.  The
-//      CTA's (max, sum, partial output) goes to CTA 0's shared memory before
-//      a cluster barrier;
+//      key) is scored by one warp of the last CTA from shared memory;
+//   3. Gated DeltaNet on the CTA's d / kSplit rows of the fp32 state (read
+//      before the key copies are issued, updated after the keys):
+//      S <- a S (I - beta k k^T) + beta v k^T, i.e. row i of S becomes
+//      a S_i + beta (v_i - a S_i . k) k^T, and o_l = S (scale q); the rows of
+//      o_l go to CTA 0's shared memory (distributed shared memory), and so
+//      does the CTA's softmax (max, sum, partial output), before a cluster
+//      barrier; the new rows are stored after it;
 //   4. CTA 0: the kSplit partials combined, RMSNorm of both branches and the
 //      query-gated sum; the running [q; k] sum of the chunk;
 //   5. when the token completes the chunk: every CTA computes the chunk's
@@ -142,10 +147,6 @@ __device__ __forceinline__ void block_sum3(float& a, float& b, float& c, float (
   __syncthreads();
 }
 
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 // programmatic dependent launch: let the next kernel of the stream be
 // scheduled now; wait for the previous one to complete (its writes visible)
 __device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -181,31 +182,55 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 4) de
   __shared__ __align__(16) float part_o[kSplit][D];  // CTA 0: the cluster's partial outputs
   __shared__ float part_m[kSplit], part_l[kSplit];
   __shared__ int sel_sh;
+  __shared__ int claim;            // CTA 0's: the next block of 32 keys to hand out
+  __shared__ int blk[R::kStages];  // the block in each slot (-1: none was left)
 
-  cluster_arrive_relaxed();  // waited for before the first access to CTA 0's shared memory
-  launch_dependents();
-  if (tid == 0)
+  if (tid == 0) {
     for (int i = 0; i < R::kStages; ++i) tc::mbar_init(&full[i], 1);
+    tc::fence_barrier_init();
+    claim = 0;
+  }
+  launch_dependents();
+  cluster.sync();  // CTA 0's counter is set and every CTA of the cluster runs
   // nothing before this point reads global memory: every input, the state
   // included, may be written by the preceding kernel of the stream
   wait_prerequisites();
 
-  // the keys held in memory, nr retained then p of the chunk; this CTA's [lo, hi)
+  // this CTA's state rows, read first (used after the keys, by which time
+  // they have long arrived; read after the copies they would queue behind
+  // them)
+  const int srow_i = rank * RPC + tid / TPR, spart = tid % TPR;
+  float* srow = S + (bh * D + srow_i) * D + spart * CPT;
+  float sv[CPT];
+  load_n<CPT>(srow, sv);
+
+  // the hi = nr + p keys held in memory, nr retained then p of the chunk,
+  // in blocks of 32 that the cluster's CTAs claim one at a time from CTA 0's
+  // counter (a CTA whose copies land sooner takes more blocks)
   const int nr = n_kv[bh];
-  const int nm = nr + p;
-  const int lo = (int)((long long)nm * rank / kSplit), hi = (int)((long long)nm * (rank + 1) / kSplit);
-  const int nst = (hi - lo + kKeysPerStage - 1) / kKeysPerStage;
+  const int hi = nr + p;
+  const int nblk = (hi + kKeysPerStage - 1) / kKeysPerStage;
+  int* claim0 = cluster.map_shared_rank(&claim, 0);
   const T* Kr = kv_k + bh * cap * D;
   const T* Vr = kv_v + bh * cap * D;
   const T* Kc = ck + bh * C * D;
   const T* Vc = cv + bh * C * D;
-  // stage s (keys [lo + 32 s, ...) of the CTA) into slot s % kStages: the
-  // retained rows and the chunk's rows are two contiguous runs
-  auto issue = [&](int s) {
-    uint8_t* kb = ring + (s % R::kStages) * R::kStage;
+  // stage s: a claimed block into slot s % kStages (the retained rows and the
+  // chunk's rows are two contiguous runs); false when none was left, the
+  // slot then completes with no copy and blk = -1 ends the CTA's loop
+  auto issue = [&](int s) -> bool {
+    const int slot = s % R::kStages;
+    uint8_t* kb = ring + slot * R::kStage;
     uint8_t* vb = kb + R::kHalf;
-    uint64_t* bar = &full[s % R::kStages];
-    const int a0 = lo + s * kKeysPerStage, a1 = min(a0 + kKeysPerStage, hi);
+    uint64_t* bar = &full[slot];
+    const int b = atomicAdd(claim0, 1);
+    if (b >= nblk) {
+      blk[slot] = -1;
+      tc::mbar_arrive(bar);
+      return false;
+    }
+    blk[slot] = b;
+    const int a0 = b * kKeysPerStage, a1 = min(a0 + kKeysPerStage, hi);
     const int m = min(max(nr, a0), a1);  // [a0, m) retained, [m, a1) of the chunk
     tc::mbar_arrive_expect_tx(bar, (uint32_t)((a1 - a0) * 2 * R::kRow));
     if (m > a0) {
@@ -216,12 +241,12 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 4) de
       tc::bulk_load_1d(kb + (m - a0) * R::kRow, Kc + (long long)(m - nr) * D, (uint32_t)((a1 - m) * R::kRow), bar);
       tc::bulk_load_1d(vb + (m - a0) * R::kRow, Vc + (long long)(m - nr) * D, (uint32_t)((a1 - m) * R::kRow), bar);
     }
+    return true;
   };
-  int issued = 0;  // (thread 0)
-  if (tid == 0) {
-    tc::fence_barrier_init();
-    for (; issued < min(nst, R::kStages); ++issued) issue(issued);
-  }
+  int issued = 0;    // stages issued (thread 0)
+  bool more = true;  // blocks may be left (thread 0)
+  if (tid == 0)
+    for (; issued < R::kStages && more; ++issued) more = issue(issued);
 
   // 1. the token
   if (tid < D) {
@@ -259,33 +284,7 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 4) de
   }
   __syncthreads();  // also: the barriers are initialised
 
-  // 2. Gated DeltaNet on this CTA's state rows
-  {
-    const int row = rank * RPC + tid / TPR, part = tid % TPR;
-    float* srow = S + (bh * D + row) * D + part * CPT;
-    float sv[CPT];
-    load_n<CPT>(srow, sv);
-    float u = 0.f;
-#pragma unroll
-    for (int j = 0; j < CPT; ++j) u = fmaf(sv[j], ks[part * CPT + j], u);
-#pragma unroll
-    for (int o = 1; o < TPR; o <<= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
-    const float coef = bt * (vs[row] - a * u);
-    float r = 0.f;
-#pragma unroll
-    for (int j = 0; j < CPT; ++j) {
-      sv[j] = fmaf(a, sv[j], coef * ks[part * CPT + j]);
-      r = fmaf(sv[j], qs[part * CPT + j], r);
-    }
-#pragma unroll
-    for (int o = 1; o < TPR; o <<= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
-#pragma unroll
-    for (int j = 0; j < CPT; j += 4) *(float4*)(srow + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
-    cluster_wait();  // every CTA of the cluster is running
-    if (part == 0) *cluster.map_shared_rank(&ol[row], 0) = r * scale;
-  }
-
-  // 3. softmax over the CTA's keys
+  // 2. softmax over the CTA's keys
   float qv[E];
 #pragma unroll
   for (int x = 0; x < E; ++x) qv[x] = qs[lane * E + x];
@@ -343,13 +342,14 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 4) de
   };
   bool ok = true;
   int s = 0;
-  for (; s < nst; ++s) {
+  for (;; ++s) {
     const int slot = s % R::kStages;
     const bool wok = __all_sync(0xffffffffu, tc::mbar_wait(&full[slot], (uint32_t)((s / R::kStages) & 1), err));
-    if (wok && lo + s * kKeysPerStage + 8 * warp < hi) {
+    const int b = wok ? blk[slot] : -1;  // written by thread 0 before the slot's arrival
+    if (b >= 0 && b * kKeysPerStage + 8 * warp < hi) {
       const uint8_t* kb = ring + slot * R::kStage + 8 * warp * R::kRow;
       const uint8_t* vb = kb + R::kHalf;
-      const int j0 = lo + s * kKeysPerStage + 8 * warp;
+      const int j0 = b * kKeysPerStage + 8 * warp;
       RV kr[8], vr[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -364,8 +364,8 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 4) de
       batch(j0, kr, vr);
     }
     ok = __syncthreads_and(wok) != 0;  // the slot is read by every warp
-    if (!ok) break;
-    if (tid == 0 && issued < nst) issue(issued++);
+    if (!ok || b < 0) break;
+    if (tid == 0 && more) more = issue(issued++);
   }
   if (!ok && tid == 0) {
     // a copy did not land in time: wait (bounded) for those still in flight
@@ -385,6 +385,25 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 4) de
     m = mn;
 #pragma unroll
     for (int x = 0; x < E; ++x) acc[x] = fmaf(pw, vs[lane * E + x], acc[x] * alpha);
+  }
+
+  // 3. Gated DeltaNet on this CTA's state rows
+  {
+    float u = 0.f;
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) u = fmaf(sv[j], ks[spart * CPT + j], u);
+#pragma unroll
+    for (int o = 1; o < TPR; o <<= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
+    const float coef = bt * (vs[srow_i] - a * u);
+    float r = 0.f;
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+      sv[j] = fmaf(a, sv[j], coef * ks[spart * CPT + j]);
+      r = fmaf(sv[j], qs[spart * CPT + j], r);
+    }
+#pragma unroll
+    for (int o = 1; o < TPR; o <<= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    if (spart == 0) *cluster.map_shared_rank(&ol[srow_i], 0) = r * scale;
   }
   __syncthreads();  // the ring is free: the warps' partials go there
   float* wo = (float*)ring;  // [kWarps][D]
@@ -435,6 +454,22 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 4) de
   cluster.sync();
   if (!ok && tid == 0) atomicExch(err, 1);
 
+  // the new state rows, stored after the barrier (whose release would
+  // otherwise wait for them); at the chunk's last token Gated DeltaNet also
+  // makes them the new chunk start, softmax puts the rows back to the chunk
+  // start instead (each thread its own columns)
+  {
+    float* s0row = S0 + (bh * D + srow_i) * D + spart * CPT;
+    const bool rollback = last && sel_sh == 0;
+    if (rollback) load_n<CPT>(s0row, sv);
+#pragma unroll
+    for (int j = 0; j < CPT; j += 4) {
+      const float4 x = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
+      *(float4*)(srow + j) = x;
+      if (last && !rollback) *(float4*)(s0row + j) = x;
+    }
+  }
+
   if (rank == 0) {
     // 4. the partials combined; RMSNorm of each branch and the query-gated sum
     if (tid < D) {
@@ -474,14 +509,10 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 4) de
   }
   if (!last) return;
 
-  // 5. commit or rollback of this CTA's state rows and its share of the
-  //    chunk's keys / values
+  // 5. softmax: this CTA's share of the chunk's keys / values joins the
+  //    retained ones (the last one is this token)
   const int sel = sel_sh;
-  float4* Sh = (float4*)(S + (bh * D + rank * RPC) * D);
-  float4* S0h = (float4*)(S0 + (bh * D + rank * RPC) * D);
   if (sel == 0) {
-    // softmax: the chunk's keys / values join the retained ones (the last
-    // one is this token); the state returns to the chunk start
     constexpr int RC = kChunk / kSplit;  // chunk rows per CTA
     for (int e = tid; e < RC * D; e += kThreads) {
       const int j = rank * RC + e / D, c = e % D;
@@ -489,11 +520,7 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 4) de
       kv_k[dst] = j == C - 1 ? from_f32<T>(ks[c]) : Kc[(long long)j * D + c];
       kv_v[dst] = j == C - 1 ? from_f32<T>(vs[c]) : Vc[(long long)j * D + c];
     }
-    for (int e = tid; e < RPC * D / 4; e += kThreads) Sh[e] = S0h[e];
     if (rank == 0 && tid == 0) n_kv[bh] = nr + C;
-  } else {
-    // Gated DeltaNet: the state is committed and starts the next chunk
-    for (int e = tid; e < RPC * D / 4; e += kThreads) S0h[e] = Sh[e];
   }
   if (rank == 0 && tid == 0 && sel_out) sel_out[bh] = (uint8_t)sel;
 }
