@@ -425,9 +425,34 @@ def run_native(args, rank, world, local_rank):
         barrier()
         ems = e0.elapsed_time(e1)
         ems = max_over_ranks(ems, dist, dev)
-        e2e = {"value": tokens / (ems / args.steps / 1e3), "unit": "tokens/s",
+        # the host link alone: one step's input copies with an output read
+        # back at the same time and nothing else, the floor of an e2e step
+        link_ms = float("inf")
+        for _ in range(3):
+            l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            l0.record(s_in)
+            s_out.wait_event(l0)
+            with torch.cuda.stream(s_in):
+                for n in pin:
+                    staged[0][n].copy_(pin[n], non_blocking=True)
+            with torch.cuda.stream(s_out):
+                out_h[0].copy_(outs[0], non_blocking=True)
+                o_done = ev()
+                o_done.record(s_out)
+            s_in.wait_event(o_done)
+            l1.record(s_in)
+            torch.cuda.synchronize()
+            link_ms = min(link_ms, l0.elapsed_time(l1))
+        link_ms = max_over_ranks(link_ms, dist, dev)
+        e2e_ms = ems / args.steps
+        e2e = {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "pipeline": "step i + 1's input copy and step i - 1's output read overlap step i's layer"}
+               "pipeline": "step i + 1's input copy and step i - 1's output read overlap step i's layer",
+               "host_link": {"ms_per_step": link_ms, "h2d_gbs": h2d / (link_ms / 1e3) / 1e9,
+                             "frac": link_ms / e2e_ms,
+                             "what": "the step's input copies and an output read-back alone (no layer): "
+                                     "the floor of an e2e step on this host link"}}
         launches_e2e = None  # noqa: F841 (counted in gpu_launches only for the device-timed region)
 
     pk = peaks()
