@@ -305,6 +305,37 @@ nats_status nats_decode_step(const nats_dims* dims, int64_t t, const void* q, co
                              const float* norm_w_lin, const nats_decode_state* state, void* out,
                              uint8_t* sel_out, float* o_soft_out, float* o_lin_out, nats_stream_t stream);
 
+/* ---------------------------------------------------------------- backward
+ * The layer's backward pass at a fixed selection: the gradient of
+ * <dout, out> with respect to its continuous inputs ("Neural Attention
+ * Search Linear (NAtS-L)", technical summary, "Kernmechanismen" items 3 and
+ * 4).  Item 5 says the choice of attention type is learned end to end, but
+ * the pages give no estimator for the argmax; W_s and b_s get no gradient
+ * here.  The forward's selection and its two branch outputs are the saved
+ * activations: call nats_hybrid_fwd with sel_out, o_soft_out and o_lin_out.
+ *
+ * dims as for nats_hybrid_fwd.  q, k, v, dout [B, H, L, d] (dtype); g, beta
+ * [B, H, L] fp32; w_g [H, d]; b_g [H] (or NULL: zero); norm weights [d] (or
+ * NULL: unit); sel [B, H, L / chunk] uint8 (0 softmax, 1 Gated DeltaNet);
+ * o_soft, o_lin [B, H, L, d] fp32, the branch outputs before RMSNorm.
+ * Outputs, all fp32 and overwritten: dq, dk, dv [B, H, L, d]; dg, dbeta
+ * [B, H, L]; dw_g [H, d], db_g [H], dnorm_w_soft, dnorm_w_lin [d] (each may
+ * be NULL: not computed).  The workspace (nats_bwd_workspace_size bytes)
+ * holds the per-token branch gradients, the row log-sum-exp of the softmax
+ * branch, the Gated DeltaNet chunk-start states and the states of one chunk
+ * per head (fp32).  All pointers device; q, k, v, o_soft, o_lin, dout, dq,
+ * dk, dv and the workspace 16-byte aligned; asynchronous on `stream`.
+ * Errors before any launch: NATS_ERR_NULL, NATS_ERR_SHAPE /
+ * NATS_ERR_UNSUPPORTED / NATS_ERR_DTYPE / NATS_ERR_VALUE (dims),
+ * NATS_ERR_ALIGN, NATS_ERR_WORKSPACE; NATS_ERR_CUDA on a failed launch. */
+size_t nats_bwd_workspace_size(const nats_dims* dims);
+nats_status nats_hybrid_bwd(const nats_dims* dims, const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, const float* w_g, const float* b_g, const float* norm_w_soft,
+                            const float* norm_w_lin, const uint8_t* sel, const float* o_soft,
+                            const float* o_lin, const void* dout, float* dq, float* dk, float* dv, float* dg,
+                            float* dbeta, float* dw_g, float* db_g, float* dnorm_w_soft, float* dnorm_w_lin,
+                            void* workspace, size_t workspace_bytes, nats_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

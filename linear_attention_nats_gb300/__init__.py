@@ -177,6 +177,52 @@ def hybrid_fwd_x(x, w_qkv, w_ab, w_s, b_s, w_g, b_g=None, *, heads: int, b_a=Non
     return {"y": y, "sel": sel} if return_sel else y
 
 
+def hybrid_bwd(q, k, v, g, beta, w_g, b_g, sel, o_soft, o_lin, dout, *, norm_w_soft=None, norm_w_lin=None,
+               scale: float = 0.0, eps: float = 1e-6, weight_grads: bool = True, workspace=None, stream=None):
+    """Backward pass of the layer at the forward's selection (nats_hybrid_bwd).
+
+    sel, o_soft, o_lin: the forward's selection and branch outputs
+    (hybrid_fwd(..., return_sel=True, return_branches=True)); dout like q.
+    Returns a dict of fp32 gradients: dq, dk, dv [B, H, L, d]; dg, dbeta
+    [B, H, L]; and, with weight_grads, dw_g [H, d], db_g [H], dnorm_w_soft,
+    dnorm_w_lin [d].  The score layer (W_s, b_s) gets none: the selection is
+    an argmax.
+    """
+    _req(q, "q")
+    B, H, L, d = q.shape
+    N = L // 64
+    for name, t in (("k", k), ("v", v), ("dout", dout)):
+        _req(t, name, q.dtype, q.shape)
+    _req(g, "g", torch.float32, (B, H, L))
+    _req(beta, "beta", torch.float32, (B, H, L))
+    _req(w_g, "w_g", torch.float32, (H, d))
+    _req(b_g, "b_g", torch.float32, (H,))
+    _req(norm_w_soft, "norm_w_soft", torch.float32, (d,))
+    _req(norm_w_lin, "norm_w_lin", torch.float32, (d,))
+    _req(sel, "sel", torch.uint8, (B, H, N))
+    _req(o_soft, "o_soft", torch.float32, (B, H, L, d))
+    _req(o_lin, "o_lin", torch.float32, (B, H, L, d))
+    dm = dims(B, H, L, d, _dtype_code(q), scale, eps)
+    need = int(_native.lib.nats_bwd_workspace_size(ctypes.byref(dm)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _req(workspace, "workspace", torch.uint8)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    res = {"dq": torch.empty((B, H, L, d), **f32), "dk": torch.empty((B, H, L, d), **f32),
+           "dv": torch.empty((B, H, L, d), **f32), "dg": torch.empty((B, H, L), **f32),
+           "dbeta": torch.empty((B, H, L), **f32)}
+    if weight_grads:
+        res.update(dw_g=torch.empty((H, d), **f32), db_g=torch.empty((H,), **f32),
+                   dnorm_w_soft=torch.empty((d,), **f32), dnorm_w_lin=torch.empty((d,), **f32))
+    check(_native.lib.nats_hybrid_bwd(
+        ctypes.byref(dm), _p(q), _p(k), _p(v), _p(g), _p(beta), _p(w_g), _p(b_g), _p(norm_w_soft),
+        _p(norm_w_lin), _p(sel), _p(o_soft), _p(o_lin), _p(dout), _p(res["dq"]), _p(res["dk"]), _p(res["dv"]),
+        _p(res["dg"]), _p(res["dbeta"]), _p(res.get("dw_g")), _p(res.get("db_g")), _p(res.get("dnorm_w_soft")),
+        _p(res.get("dnorm_w_lin")), _p(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream)),
+        "nats_hybrid_bwd")
+    return res
+
+
 class DecodeState:
     """Device state of the layer in decode mode (nats_decode_state): the
     Gated DeltaNet state S and its chunk-start copy S0 (fp32 [B, H, d, d]), the

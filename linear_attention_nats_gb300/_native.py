@@ -25,7 +25,8 @@ STATUS = {
 # Every symbol include/nats.h declares.
 EXPORTS = ("nats_status_string", "nats_last_cuda_error", "nats_workspace_size", "nats_workspace_check", "nats_select",
            "nats_hybrid_fwd", "nats_hybrid_fwd_profiled", "nats_hybrid_fwd_noalloc", "nats_x_workspace_size",
-           "nats_hybrid_fwd_x", "nats_debug_fail_stage", "nats_debug_bounded_wait", "nats_decode_step")
+           "nats_hybrid_fwd_x", "nats_debug_fail_stage", "nats_debug_bounded_wait", "nats_decode_step",
+           "nats_bwd_workspace_size", "nats_hybrid_bwd")
 
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -96,6 +97,10 @@ def _load() -> ctypes.CDLL:
     lib.nats_decode_step.argtypes = [ctypes.POINTER(Dims), ctypes.c_int64] + [P] * 11 + [
         ctypes.POINTER(DecodeState)] + [P] * 4 + [P]
     lib.nats_decode_step.restype = ctypes.c_int
+    lib.nats_bwd_workspace_size.argtypes = [ctypes.POINTER(Dims)]
+    lib.nats_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.nats_hybrid_bwd.argtypes = [ctypes.POINTER(Dims)] + [P] * 23 + [ctypes.c_size_t, P]
+    lib.nats_hybrid_bwd.restype = ctypes.c_int
     return lib
 
 

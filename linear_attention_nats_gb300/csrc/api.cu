@@ -319,6 +319,33 @@ nats_status nats_hybrid_fwd(const nats_dims* dims, const void* q, const void* k,
                                   o_lin_out, workspace, workspace_bytes, stream, nullptr);
 }
 
+size_t nats_bwd_workspace_size(const nats_dims* dims) {
+  if (check_dims(dims) != NATS_OK) return 0;
+  return bwd_workspace_bytes(problem_of(dims));
+}
+
+nats_status nats_hybrid_bwd(const nats_dims* dims, const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, const float* w_g, const float* b_g, const float* norm_w_soft,
+                            const float* norm_w_lin, const uint8_t* sel, const float* o_soft,
+                            const float* o_lin, const void* dout, float* dq, float* dk, float* dv, float* dg,
+                            float* dbeta, float* dw_g, float* db_g, float* dnorm_w_soft, float* dnorm_w_lin,
+                            void* workspace, size_t workspace_bytes, nats_stream_t stream) {
+  nats_status s = check_dims(dims);
+  if (s != NATS_OK) return s;
+  const Problem p = problem_of(dims);
+  if (p.BH == 0 || p.L == 0) return NATS_OK;
+  if (!q || !k || !v || !g || !beta || !w_g || !sel || !o_soft || !o_lin || !dout || !dq || !dk || !dv || !dg ||
+      !dbeta || !workspace)
+    return NATS_ERR_NULL;
+  const void* ptrs[] = {q, k, v, o_soft, o_lin, dout, dq, dk, dv, workspace};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return NATS_ERR_ALIGN;
+  if (workspace_bytes < bwd_workspace_bytes(p)) return NATS_ERR_WORKSPACE;
+  return cuda_status(launch_hybrid_bwd(p, dims->dtype, q, k, v, g, beta, w_g, b_g, norm_w_soft, norm_w_lin, sel,
+                                       o_soft, o_lin, dout, dq, dk, dv, dg, dbeta, dw_g, db_g, dnorm_w_soft,
+                                       dnorm_w_lin, workspace, (cudaStream_t)stream));
+}
+
 nats_status nats_decode_step(const nats_dims* dims, int64_t t, const void* q, const void* k, const void* v,
                              const float* g, const float* beta, const float* w_s, const float* b_s,
                              const float* w_g, const float* b_g, const float* norm_w_soft,

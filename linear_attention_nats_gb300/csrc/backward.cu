@@ -1,0 +1,578 @@
+// backward.cu - the layer's backward pass at the forward's selection:
+// the gradient of <dout, out> with respect to q, k, v, g, beta, W_g, b_g and
+// the two RMSNorm weights ("Neural Attention Search Linear (NAtS-L)",
+// technical summary, "Kernmechanismen" items 3 and 4; item 5 says the
+// selection is learned end to end but gives no estimator for the argmax, so
+// the score layer gets no gradient here).
+//
+// Three stages on one stream, every result in fp32:
+//   1. norm + merge, one warp per token: with N_x = o_x r_x w_x,
+//      r_x = (mean(o_x^2) + eps)^(-1/2), out = w N_s + (1 - w) N_l and
+//      w = sigmoid(q . W_g + b_g):
+//        dN_s = w dout, dN_l = (1 - w) dout, dz = w (1 - w) <dout, N_s - N_l>,
+//        do_x = r_x (w_x dN_x) - o_x r_x^3 <w_x dN_x, o_x> / d,
+//      dq = dz W_g (the gate's share), and the weight gradients (dW_g,
+//      db_g, the norm weights) summed per CTA, then atomically;
+//   2. softmax branch, from the row log-sum-exp: P_tj = exp(s_tj - lse_t),
+//      dS_tj = P_tj (do_s,t . v_j - do_s,t . o_s,t); a row pass (one warp
+//      per query) takes lse_t and dq_t += scale sum_j dS_tj k_j, a key pass
+//      (one warp per key) dk_j = scale sum_t dS_tj q_t and
+//      dv_j = sum_t P_tj do_s,t over the queries that see key j (the rest of
+//      its chunk, and every later query when its chunk chose softmax);
+//   3. Gated DeltaNet, one CTA per (b, h): the forward is replayed for the
+//      chunk-start states, then the adjoint runs backwards.  Per token, with
+//      u = S_{t-1} k, e = v - a u, S_t = a S_{t-1} + beta e k^T and
+//      o_t = S_t (scale q):
+//        dS_t += do_t (scale q)^T, dq += scale S_t^T do_t (formed as
+//        a S_{t-1}^T do_t + beta <e, do_t> k, so S_t is not needed),
+//        x = dS_t k, de = beta x, dbeta = <e, x>, dv = de,
+//        dk = beta dS_t^T e - a S_{t-1}^T de,
+//        da = <dS_t, S_{t-1}> - <u, de>, dg = a da,
+//        dS_{t-1} = a dS_t - a de k^T.
+//      A chunk that chose softmax was rolled back: the state after it is its
+//      start state, so the gradient arriving there passes to the start
+//      unchanged and the tokens inside start from zero.  The states inside a
+//      chunk are replayed into scratch before its tokens are reversed.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace nats {
+namespace {
+
+constexpr int kMergeRows = 64;  // token rows per CTA of the merge stage
+
+template <int E>
+__device__ __forceinline__ void row_load(const float* p, float (&o)[E]) {
+#pragma unroll
+  for (int x = 0; x < E; ++x) o[x] = p[x];
+}
+template <int E>
+__device__ __forceinline__ void row_load(const __nv_bfloat16* p, float (&o)[E]) {
+#pragma unroll
+  for (int x = 0; x < E; ++x) o[x] = __bfloat162float(p[x]);
+}
+
+// ------------------------------------------------------------ 1. merge
+template <typename T, int D>
+__global__ void __launch_bounds__(256) merge_bwd_kernel(
+    const T* __restrict__ q, const T* __restrict__ dout, const float* __restrict__ o_s,
+    const float* __restrict__ o_l, const float* __restrict__ w_g, const float* __restrict__ b_g,
+    const float* __restrict__ nws, const float* __restrict__ nwl, int H, int L, float eps,
+    float* __restrict__ d_os, float* __restrict__ d_ol, float* __restrict__ delta, float* __restrict__ dq,
+    float* __restrict__ dw_g, float* __restrict__ db_g, float* __restrict__ dnws, float* __restrict__ dnwl) {
+  constexpr int E = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per_head = L / kMergeRows;
+  const long long bh = blockIdx.x / per_head;
+  const int h = (int)(bh % H);
+  const int row0 = (int)(blockIdx.x % per_head) * kMergeRows;
+  __shared__ float red[8][3][D];
+  __shared__ float red_b[8];
+  float wg[E], ws[E], wl[E];
+#pragma unroll
+  for (int x = 0; x < E; ++x) {
+    const int f = lane * E + x;
+    wg[x] = w_g[(long long)h * D + f];
+    ws[x] = nws ? nws[f] : 1.f;
+    wl[x] = nwl ? nwl[f] : 1.f;
+  }
+  const float bg = b_g ? b_g[h] : 0.f;
+  float a_wg[E], a_ns[E], a_nl[E], a_bg = 0.f;
+#pragma unroll
+  for (int x = 0; x < E; ++x) a_wg[x] = a_ns[x] = a_nl[x] = 0.f;
+  for (int r = warp; r < kMergeRows; r += 8) {
+    const long long t = bh * L + row0 + r;
+    float os[E], ol[E], R[E], qv[E];
+    row_load<E>(o_s + t * D + lane * E, os);
+    row_load<E>(o_l + t * D + lane * E, ol);
+    row_load<E>(dout + t * D + lane * E, R);
+    row_load<E>(q + t * D + lane * E, qv);
+    float ss = 0.f, sl = 0.f, z = 0.f;
+#pragma unroll
+    for (int x = 0; x < E; ++x) {
+      ss = fmaf(os[x], os[x], ss);
+      sl = fmaf(ol[x], ol[x], sl);
+      z = fmaf(qv[x], wg[x], z);
+    }
+    ss = warp_sum(ss);
+    sl = warp_sum(sl);
+    z = warp_sum(z) + bg;
+    const float rs = rsqrtf(ss / D + eps), rl = rsqrtf(sl / D + eps);
+    const float w = 1.f / (1.f + expf(-z));
+    float dw = 0.f, gs = 0.f, gl = 0.f;  // <dout, N_s - N_l>, <w_s dN_s, o_s>, <w_l dN_l, o_l>
+#pragma unroll
+    for (int x = 0; x < E; ++x) {
+      dw = fmaf(R[x], os[x] * rs * ws[x] - ol[x] * rl * wl[x], dw);
+      gs = fmaf(ws[x] * w * R[x], os[x], gs);
+      gl = fmaf(wl[x] * (1.f - w) * R[x], ol[x], gl);
+    }
+    dw = warp_sum(dw);
+    gs = warp_sum(gs);
+    gl = warp_sum(gl);
+    const float dz = dw * w * (1.f - w);
+    float dl = 0.f;
+#pragma unroll
+    for (int x = 0; x < E; ++x) {
+      const float g_s = rs * ws[x] * w * R[x] - os[x] * rs * rs * rs * gs / D;
+      const float g_l = rl * wl[x] * (1.f - w) * R[x] - ol[x] * rl * rl * rl * gl / D;
+      d_os[t * D + lane * E + x] = g_s;
+      d_ol[t * D + lane * E + x] = g_l;
+      dq[t * D + lane * E + x] = dz * wg[x];
+      dl = fmaf(g_s, os[x], dl);
+      a_wg[x] = fmaf(dz, qv[x], a_wg[x]);
+      a_ns[x] = fmaf(w * R[x], os[x] * rs, a_ns[x]);
+      a_nl[x] = fmaf((1.f - w) * R[x], ol[x] * rl, a_nl[x]);
+    }
+    dl = warp_sum(dl);
+    if (lane == 0) delta[t] = dl;
+    a_bg += dz;
+  }
+  // weight gradients: the CTA's warps summed, then one atomic per element
+#pragma unroll
+  for (int x = 0; x < E; ++x) {
+    red[warp][0][lane * E + x] = a_wg[x];
+    red[warp][1][lane * E + x] = a_ns[x];
+    red[warp][2][lane * E + x] = a_nl[x];
+  }
+  if (lane == 0) red_b[warp] = a_bg;
+  __syncthreads();
+  for (int f = threadIdx.x; f < 3 * D; f += blockDim.x) {
+    const int which = f / D, c = f % D;
+    float s = 0.f;
+#pragma unroll
+    for (int w8 = 0; w8 < 8; ++w8) s += red[w8][which][c];
+    float* dst = which == 0 ? (dw_g ? dw_g + (long long)h * D : nullptr) : which == 1 ? dnws : dnwl;
+    if (dst) atomicAdd(dst + c, s);
+  }
+  if (threadIdx.x == 0 && db_g) {
+    float s = 0.f;
+#pragma unroll
+    for (int w8 = 0; w8 < 8; ++w8) s += red_b[w8];
+    atomicAdd(db_g + h, s);
+  }
+}
+
+// ---------------------------------------------------- 2. softmax branch
+// The keys a query row t of chunk c sees: every key of the earlier chunks
+// that chose softmax, then its own chunk up to t.  fn(j) for each, in order.
+template <typename F>
+__device__ __forceinline__ void for_each_key(const uint8_t* sel_h, int t, F&& fn) {
+  const int c = t / kChunk;
+  for (int cj = 0; cj < c; ++cj)
+    if (sel_h[cj] == 0)
+      for (int j = cj * kChunk; j < (cj + 1) * kChunk; ++j) fn(j);
+  for (int j = c * kChunk; j <= t; ++j) fn(j);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) softmax_bwd_rows_kernel(
+    const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, const uint8_t* __restrict__ sel,
+    const float* __restrict__ d_os, const float* __restrict__ delta, long long rows, int L, int N, float scale,
+    float* __restrict__ lse, float* __restrict__ dq) {
+  constexpr int E = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 8 + warp;
+  if (row >= rows) return;  // warp-uniform
+  const long long bh = row / L;
+  const int t = (int)(row % L);
+  const T* kh = k + bh * L * D;
+  const T* vh = v + bh * L * D;
+  const uint8_t* sel_h = sel + bh * N;
+  float qv[E], dov[E];
+  row_load<E>(q + row * D + lane * E, qv);
+  row_load<E>(d_os + row * D + lane * E, dov);
+  // pass 1: log-sum-exp of the row's scores
+  float m = -INFINITY, s = 0.f;
+  for_each_key(sel_h, t, [&](int j) {
+    float kv[E];
+    row_load<E>(kh + (long long)j * D + lane * E, kv);
+    float p = 0.f;
+#pragma unroll
+    for (int x = 0; x < E; ++x) p = fmaf(qv[x], kv[x], p);
+    const float sc = warp_sum(p) * scale;
+    if (sc > m) {
+      s = s * expf(m - sc) + 1.f;
+      m = sc;
+    } else {
+      s += expf(sc - m);
+    }
+  });
+  const float l = m + logf(s);
+  const float dt = delta[row];
+  // pass 2: dq_t = scale sum_j P_tj (do_t . v_j - delta_t) k_j
+  float acc[E];
+#pragma unroll
+  for (int x = 0; x < E; ++x) acc[x] = 0.f;
+  for_each_key(sel_h, t, [&](int j) {
+    float kv[E], vv[E];
+    row_load<E>(kh + (long long)j * D + lane * E, kv);
+    row_load<E>(vh + (long long)j * D + lane * E, vv);
+    float p = 0.f, dp = 0.f;
+#pragma unroll
+    for (int x = 0; x < E; ++x) {
+      p = fmaf(qv[x], kv[x], p);
+      dp = fmaf(dov[x], vv[x], dp);
+    }
+    const float P = expf(warp_sum(p) * scale - l);
+    const float ds = P * (warp_sum(dp) - dt);
+#pragma unroll
+    for (int x = 0; x < E; ++x) acc[x] = fmaf(ds, kv[x], acc[x]);
+  });
+#pragma unroll
+  for (int x = 0; x < E; ++x) dq[row * D + lane * E + x] += scale * acc[x];
+  if (lane == 0) lse[row] = l;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) softmax_bwd_keys_kernel(
+    const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, const uint8_t* __restrict__ sel,
+    const float* __restrict__ d_os, const float* __restrict__ delta, const float* __restrict__ lse,
+    long long rows, int L, int N, float scale, float* __restrict__ dk, float* __restrict__ dv) {
+  constexpr int E = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 8 + warp;
+  if (row >= rows) return;  // warp-uniform
+  const long long bh = row / L;
+  const int j = (int)(row % L), cj = j / kChunk;
+  const long long h0 = bh * L;
+  float kv[E], vv[E];
+  row_load<E>(k + row * D + lane * E, kv);
+  row_load<E>(v + row * D + lane * E, vv);
+  // the queries that see key j: the rest of its chunk, then every later
+  // query if the chunk chose softmax
+  const int t_end = sel[bh * N + cj] == 0 ? L : (cj + 1) * kChunk;
+  float ak[E], av[E];
+#pragma unroll
+  for (int x = 0; x < E; ++x) ak[x] = av[x] = 0.f;
+  for (int t = j; t < t_end; ++t) {
+    float qv[E], dov[E];
+    row_load<E>(q + (h0 + t) * D + lane * E, qv);
+    row_load<E>(d_os + (h0 + t) * D + lane * E, dov);
+    float p = 0.f, dp = 0.f;
+#pragma unroll
+    for (int x = 0; x < E; ++x) {
+      p = fmaf(qv[x], kv[x], p);
+      dp = fmaf(dov[x], vv[x], dp);
+    }
+    const float P = expf(warp_sum(p) * scale - lse[h0 + t]);
+    const float ds = P * (warp_sum(dp) - delta[h0 + t]);
+#pragma unroll
+    for (int x = 0; x < E; ++x) {
+      ak[x] = fmaf(ds, qv[x], ak[x]);
+      av[x] = fmaf(P, dov[x], av[x]);
+    }
+  }
+#pragma unroll
+  for (int x = 0; x < E; ++x) {
+    dk[row * D + lane * E + x] = scale * ak[x];
+    dv[row * D + lane * E + x] = av[x];
+  }
+}
+
+// --------------------------------------------------- 3. Gated DeltaNet
+// One CTA of 512 threads per (b, h).  Thread (warp w, lane l) holds rows
+// [w RW, w RW + RW) x columns [l CW, l CW + CW) of a d x d matrix.
+constexpr int kGdnThreads = 512;
+
+template <int D>
+struct GdnBwd {
+  static constexpr int RW = D / 16;  // rows per warp
+  static constexpr int CW = D / 32;  // columns per lane
+  // shared memory (floats)
+  static constexpr int offTok = 0;                  // [2][6][D]: k, scale q, v, do, then a, beta
+  static constexpr int offU = offTok + 2 * 6 * D;   // [kChunk][D] u_t of the replayed chunk
+  static constexpr int offColA = offU + kChunk * D; // [16][D]
+  static constexpr int offColB = offColA + 16 * D;  // [16][D]
+  static constexpr int offRed = offColB + 16 * D;   // [16][3]
+  static constexpr int kFloats = offRed + 48;
+  static constexpr int kBytes = kFloats * 4;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kGdnThreads, 1) gdn_bwd_kernel(
+    const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, const float* __restrict__ g,
+    const float* __restrict__ beta, const uint8_t* __restrict__ sel, const float* __restrict__ d_ol, int L,
+    int N, float scale, float* __restrict__ Sc, float* __restrict__ Tk, float* __restrict__ dSx,
+    float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv, float* __restrict__ dg,
+    float* __restrict__ dbeta) {
+  using G = GdnBwd<D>;
+  constexpr int RW = G::RW, CW = G::CW;
+  extern __shared__ __align__(16) float sm[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long bh = blockIdx.x;
+  const long long h0 = bh * L;
+  const uint8_t* sel_h = sel + bh * N;
+  float* sc_h = Sc + bh * (long long)N * D * D;  // chunk-start states
+  float* tk_h = Tk + bh * (long long)kChunk * D * D;  // states after each token of one chunk
+  float* dsx_h = dSx + bh * (long long)D * D;
+  const int r0 = warp * RW, c0 = lane * CW;
+  auto el = [&](int i, int j) { return (long long)(r0 + i) * D + c0 + j; };  // offset in a d x d matrix
+  auto ld = [&](const float* M, float (&X)[RW][CW]) {
+#pragma unroll
+    for (int i = 0; i < RW; ++i)
+#pragma unroll
+      for (int j = 0; j < CW; ++j) X[i][j] = M[el(i, j)];
+  };
+  auto st = [&](float* M, const float (&X)[RW][CW]) {
+#pragma unroll
+    for (int i = 0; i < RW; ++i)
+#pragma unroll
+      for (int j = 0; j < CW; ++j) M[el(i, j)] = X[i][j];
+  };
+  // token t's vectors into buffer b (k, scale q, v, d o_l; a, beta)
+  auto load_tok = [&](int t, int b) {
+    float* tb = sm + G::offTok + b * 6 * D;
+    const long long r = h0 + t;
+    if (tid < D) tb[tid] = to_f32(k[r * D + tid]);
+    else if (tid < 2 * D) tb[tid] = scale * to_f32(q[r * D + tid - D]);
+    else if (tid < 3 * D) tb[tid] = to_f32(v[r * D + tid - 2 * D]);
+    else if (tid < 4 * D) tb[tid] = d_ol[r * D + tid - 3 * D];
+    if (tid == 0) {
+      tb[4 * D] = expf(g[r]);
+      tb[4 * D + 1] = beta[r];
+    }
+  };
+  // row sums over the d columns of X (. y), every lane gets its warp's rows
+  auto row_dot = [&](const float (&X)[RW][CW], const float* y, float (&out)[RW]) {
+#pragma unroll
+    for (int i = 0; i < RW; ++i) {
+      float p = 0.f;
+#pragma unroll
+      for (int j = 0; j < CW; ++j) p = fmaf(X[i][j], y[c0 + j], p);
+      out[i] = warp_sum(p);
+    }
+  };
+  // one forward token step on S (u = S k returned)
+  auto fwd_step = [&](float (&S)[RW][CW], const float* tb, float (&u)[RW]) {
+    const float* kt = tb;
+    const float* vt = tb + 2 * D;
+    const float a = tb[4 * D], bt = tb[4 * D + 1];
+    row_dot(S, kt, u);
+#pragma unroll
+    for (int i = 0; i < RW; ++i) {
+      const float coef = bt * (vt[r0 + i] - a * u[i]);
+#pragma unroll
+      for (int j = 0; j < CW; ++j) S[i][j] = fmaf(a, S[i][j], coef * kt[c0 + j]);
+    }
+  };
+
+  // phase A: the chunk-start states
+  {
+    float S[RW][CW];
+#pragma unroll
+    for (int i = 0; i < RW; ++i)
+#pragma unroll
+      for (int j = 0; j < CW; ++j) S[i][j] = 0.f;
+    int tb_i = 0;
+    for (int c = 0; c < N; ++c) {
+      st(sc_h + (long long)c * D * D, S);
+      for (int t = c * kChunk; t < (c + 1) * kChunk; ++t, tb_i ^= 1) {
+        load_tok(t, tb_i);
+        __syncthreads();
+        float u[RW];
+        fwd_step(S, sm + G::offTok + tb_i * 6 * D, u);
+      }
+      if (sel_h[c] == 0) ld(sc_h + (long long)c * D * D, S);  // rollback (this thread's own elements)
+    }
+  }
+
+  // phase B: the adjoint, chunk by chunk from the last
+  float dS[RW][CW];
+#pragma unroll
+  for (int i = 0; i < RW; ++i)
+#pragma unroll
+    for (int j = 0; j < CW; ++j) dS[i][j] = 0.f;
+  int tb_i = 0;
+  for (int c = N - 1; c >= 0; --c) {
+    const int t0 = c * kChunk;
+    const bool rolled_back = sel_h[c] == 0;
+    // replay the chunk: the state after each token (but the last), and u_t
+    {
+      float S[RW][CW];
+      ld(sc_h + (long long)c * D * D, S);
+      for (int i = 0; i < kChunk; ++i, tb_i ^= 1) {
+        load_tok(t0 + i, tb_i);
+        __syncthreads();
+        float u[RW];
+        fwd_step(S, sm + G::offTok + tb_i * 6 * D, u);
+        if (lane == 0)
+#pragma unroll
+          for (int x = 0; x < RW; ++x) sm[G::offU + i * D + r0 + x] = u[x];
+        if (i + 1 < kChunk) st(tk_h + (long long)i * D * D, S);
+      }
+    }
+    // the gradient arriving at the state after the chunk: through the
+    // tokens, or (rolled back) straight to the chunk start
+    if (rolled_back) {
+      st(dsx_h, dS);
+#pragma unroll
+      for (int i = 0; i < RW; ++i)
+#pragma unroll
+        for (int j = 0; j < CW; ++j) dS[i][j] = 0.f;
+    }
+    for (int i = kChunk - 1; i >= 0; --i, tb_i ^= 1) {
+      const int t = t0 + i;
+      load_tok(t, tb_i);
+      float Sb[RW][CW];
+      ld(i > 0 ? tk_h + (long long)(i - 1) * D * D : sc_h + (long long)c * D * D, Sb);
+      __syncthreads();
+      const float* tb = sm + G::offTok + tb_i * 6 * D;
+      const float* kt = tb;
+      const float* qt = tb + D;
+      const float* vt = tb + 2 * D;
+      const float* dot = tb + 3 * D;
+      const float a = tb[4 * D], bt = tb[4 * D + 1];
+      // dS_t += do_t (scale q_t)^T; S_{t-1}^T do_t (column sums)
+      float colA[CW], colB[CW];
+#pragma unroll
+      for (int j = 0; j < CW; ++j) colA[j] = colB[j] = 0.f;
+#pragma unroll
+      for (int x = 0; x < RW; ++x) {
+        const float dor = dot[r0 + x];
+#pragma unroll
+        for (int j = 0; j < CW; ++j) {
+          dS[x][j] = fmaf(dor, qt[c0 + j], dS[x][j]);
+          colA[j] = fmaf(Sb[x][j], dor, colA[j]);
+        }
+      }
+      float xr[RW];
+      row_dot(dS, kt, xr);
+      float p_da = 0.f, p_db = 0.f, p_ed = 0.f;
+#pragma unroll
+      for (int x = 0; x < RW; ++x) {
+        const float u = sm[G::offU + i * D + r0 + x];
+        const float e = vt[r0 + x] - a * u;
+        const float de = bt * xr[x];
+#pragma unroll
+        for (int j = 0; j < CW; ++j) {
+          colB[j] = fmaf(bt * e, dS[x][j], colB[j]);
+          colB[j] = fmaf(-a * de, Sb[x][j], colB[j]);
+          p_da = fmaf(dS[x][j], Sb[x][j], p_da);
+        }
+        if (lane == 0) {
+          p_da -= u * de;
+          p_db = fmaf(e, xr[x], p_db);
+          p_ed = fmaf(e, dot[r0 + x], p_ed);
+          dv[(h0 + t) * D + r0 + x] += de;
+        }
+        // dS_{t-1} = a dS_t - a de k^T
+#pragma unroll
+        for (int j = 0; j < CW; ++j) dS[x][j] = a * fmaf(-de, kt[c0 + j], dS[x][j]);
+      }
+      p_da = warp_sum(p_da);
+#pragma unroll
+      for (int j = 0; j < CW; ++j) {
+        sm[G::offColA + warp * D + c0 + j] = colA[j];
+        sm[G::offColB + warp * D + c0 + j] = colB[j];
+      }
+      if (lane == 0) {
+        sm[G::offRed + 3 * warp] = p_da;
+        sm[G::offRed + 3 * warp + 1] = p_db;
+        sm[G::offRed + 3 * warp + 2] = p_ed;
+      }
+      __syncthreads();
+      if (tid < D) {
+        float sa = 0.f, sb = 0.f, ed = 0.f;
+#pragma unroll
+        for (int w = 0; w < 16; ++w) {
+          sa += sm[G::offColA + w * D + tid];
+          sb += sm[G::offColB + w * D + tid];
+          ed += sm[G::offRed + 3 * w + 2];
+        }
+        // S_t^T do_t = a S_{t-1}^T do_t + beta <e, do_t> k_t
+        dq[(h0 + t) * D + tid] += scale * fmaf(a, sa, bt * ed * kt[tid]);
+        dk[(h0 + t) * D + tid] += sb;
+      } else if (tid == D) {
+        float da = 0.f, db = 0.f;
+#pragma unroll
+        for (int w = 0; w < 16; ++w) {
+          da += sm[G::offRed + 3 * w];
+          db += sm[G::offRed + 3 * w + 1];
+        }
+        dg[h0 + t] = a * da;
+        dbeta[h0 + t] = db;
+      }
+    }
+    if (rolled_back) {
+      float X[RW][CW];
+      ld(dsx_h, X);
+#pragma unroll
+      for (int i = 0; i < RW; ++i)
+#pragma unroll
+        for (int j = 0; j < CW; ++j) dS[i][j] += X[i][j];
+    }
+  }
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(const Problem& p) {
+  auto al = [](size_t b) { return (b + 255) & ~(size_t)255; };
+  const size_t rows = (size_t)p.BH * p.L, dd = (size_t)p.d * p.d;
+  return 2 * al(rows * p.d * 4)            // d o_s, d o_l
+         + 2 * al(rows * 4)                // delta, lse
+         + al((size_t)p.BH * p.N * dd * 4)  // chunk-start states
+         + al((size_t)p.BH * kChunk * dd * 4)  // states inside the chunk being reversed
+         + al((size_t)p.BH * dd * 4);       // gradient held over a rolled-back chunk
+}
+
+cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const void* k, const void* v,
+                              const float* g, const float* beta, const float* w_g, const float* b_g,
+                              const float* nws, const float* nwl, const uint8_t* sel, const float* o_s,
+                              const float* o_l, const void* dout, float* dq, float* dk, float* dv, float* dg,
+                              float* dbeta, float* dw_g, float* db_g, float* dnws, float* dnwl, void* ws,
+                              cudaStream_t st) {
+  if (p.BH == 0 || p.L == 0) return cudaSuccess;
+  auto al = [](size_t b) { return (b + 255) & ~(size_t)255; };
+  const long long rows = (long long)p.BH * p.L;
+  const size_t dd = (size_t)p.d * p.d;
+  uint8_t* w = (uint8_t*)ws;
+  float* d_os = (float*)w;
+  w += al((size_t)rows * p.d * 4);
+  float* d_ol = (float*)w;
+  w += al((size_t)rows * p.d * 4);
+  float* delta = (float*)w;
+  w += al((size_t)rows * 4);
+  float* lse = (float*)w;
+  w += al((size_t)rows * 4);
+  float* Sc = (float*)w;
+  w += al((size_t)p.BH * p.N * dd * 4);
+  float* Tk = (float*)w;
+  w += al((size_t)p.BH * kChunk * dd * 4);
+  float* dSx = (float*)w;
+  // weight gradients are sums over the launch: zeroed first
+  cudaError_t e = cudaSuccess;
+  if (dw_g) e = cudaMemsetAsync(dw_g, 0, (size_t)p.H * p.d * 4, st);
+  if (e == cudaSuccess && db_g) e = cudaMemsetAsync(db_g, 0, (size_t)p.H * 4, st);
+  if (e == cudaSuccess && dnws) e = cudaMemsetAsync(dnws, 0, (size_t)p.d * 4, st);
+  if (e == cudaSuccess && dnwl) e = cudaMemsetAsync(dnwl, 0, (size_t)p.d * 4, st);
+  if (e != cudaSuccess) return e;
+  auto run = [&](auto tag, auto dtag) -> cudaError_t {
+    using T = decltype(tag);
+    constexpr int D = decltype(dtag)::value;
+    const T* qt = (const T*)q;
+    const T* kt = (const T*)k;
+    const T* vt = (const T*)v;
+    merge_bwd_kernel<T, D><<<(unsigned)(rows / kMergeRows), 256, 0, st>>>(
+        qt, (const T*)dout, o_s, o_l, w_g, b_g, nws, nwl, p.H, p.L, p.eps, d_os, d_ol, delta, dq, dw_g, db_g,
+        dnws, dnwl);
+    softmax_bwd_rows_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(qt, kt, vt, sel, d_os, delta, rows,
+                                                                             p.L, p.N, p.scale, lse, dq);
+    softmax_bwd_keys_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
+        qt, kt, vt, sel, d_os, delta, lse, rows, p.L, p.N, p.scale, dk, dv);
+    constexpr int smem = GdnBwd<D>::kBytes;
+    static const cudaError_t attr =
+        cudaFuncSetAttribute(gdn_bwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (attr != cudaSuccess) return attr;
+    gdn_bwd_kernel<T, D><<<(unsigned)p.BH, kGdnThreads, smem, st>>>(qt, kt, vt, g, beta, sel, d_ol, p.L, p.N,
+                                                                    p.scale, Sc, Tk, dSx, dq, dk, dv, dg, dbeta);
+    return cudaGetLastError();
+  };
+  using bf = __nv_bfloat16;
+  using D64 = std::integral_constant<int, 64>;
+  using D128 = std::integral_constant<int, 128>;
+  if (dtype == 0) return p.d == 64 ? run(bf(), D64()) : run(bf(), D128());
+  return p.d == 64 ? run(0.f, D64()) : run(0.f, D128());
+}
+
+}  // namespace nats

@@ -58,6 +58,16 @@ cudaError_t launch_decode_step(const Problem& p, int dtype, long long t, const v
                                void* kv_k, void* kv_v, int32_t* n_kv, long long cap, void* out,
                                uint8_t* sel_out, float* o_s_out, float* o_l_out, int* err, cudaStream_t st);
 
+// Backward pass at a given selection (backward.cu): its scratch bytes, and
+// the launches (norm + merge, softmax rows, softmax keys, Gated DeltaNet).
+size_t bwd_workspace_bytes(const Problem& p);
+cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const void* k, const void* v,
+                              const float* g, const float* beta, const float* w_g, const float* b_g,
+                              const float* nws, const float* nwl, const uint8_t* sel, const float* o_s,
+                              const float* o_l, const void* dout, float* dq, float* dk, float* dv, float* dg,
+                              float* dbeta, float* dw_g, float* db_g, float* dnws, float* dnwl, void* ws,
+                              cudaStream_t st);
+
 // Test hook: one bounded wait that runs out after limit_ns and sets *flag.
 cudaError_t launch_bounded_wait(int* flag, long long limit_ns, cudaStream_t st);
 

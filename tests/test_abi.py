@@ -163,6 +163,35 @@ def test_decode_validation(nat):
     assert call(d=empty) == 0                    # nothing to do
 
 
+def test_backward_validation(nat):
+    # the backward pass: argument checks before any launch
+    dm = nat.dims(1, 2, 128, 64)
+    need = nat.lib.nats_bwd_workspace_size(ctypes.byref(dm))
+    # d o_s, d o_l, delta, lse, 2 chunk-start states, one chunk of states, one held gradient (fp32)
+    rows, dd = 2 * 128, 64 * 64
+    al = lambda b: (b + 255) // 256 * 256
+    assert need == 2 * al(rows * 64 * 4) + 2 * al(rows * 4) + al(2 * 2 * dd * 4) + al(2 * 64 * dd * 4) + al(2 * dd * 4)
+    fake = ctypes.c_void_p(256)
+    odd = ctypes.c_void_p(264)
+    args = [fake] * 23  # q ... dnorm_w_lin, then the workspace
+
+    def call(d=dm, a=args, ws_bytes=need):
+        return nat.lib.nats_hybrid_bwd(ctypes.byref(d), *a, ctypes.c_size_t(ws_bytes), None)
+
+    assert call(ws_bytes=need - 1) == 5           # NATS_ERR_WORKSPACE
+    assert call(a=[None] + args[1:]) == 1         # q NULL
+    assert call(a=args[:9] + [None] + args[10:]) == 1   # sel NULL
+    assert call(a=args[:12] + [odd] + args[13:]) == 4   # dout misaligned
+    assert call(a=args[:22] + [None]) == 1        # workspace NULL
+    for optional in (6, 7, 8, 18, 19, 20, 21):    # b_g, norm weights, weight gradients may be NULL
+        a = list(args)
+        a[optional] = None
+        assert call(a=a, ws_bytes=0) == 5          # passes the NULL checks, stops at the workspace
+    assert call(d=nat.dims(1, 2, 100, 64)) == 2   # L % 64: NATS_ERR_SHAPE
+    assert call(d=nat.dims(0, 2, 128, 64)) == 0   # nothing to do
+    assert nat.lib.nats_bwd_workspace_size(ctypes.byref(nat.dims(1, 2, 100, 64))) == 0
+
+
 def test_debug_hook_validation(nat):
     # the bounded-wait hook checks its arguments before any launch
     assert nat.lib.nats_debug_bounded_wait(None, 1000, None) == 1           # NATS_ERR_NULL

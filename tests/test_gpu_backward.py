@@ -1,0 +1,108 @@
+"""The layer's backward pass (nats_hybrid_bwd) through the C ABI against the
+fp64 backward oracle (oracle/backward.py), at the forward's selection:
+
+* on the oracle's own activations (selection and branch outputs), so that
+  only the backward's arithmetic is compared: every gradient within the
+  fp32 bar;
+* end to end, on the activations the CUDA forward saved (its selection
+  bit-exact with the oracle's), within the bar of the forward's dtype.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+from oracle import backward as ob
+from gpu_util import TOL, rel_err, to_device
+
+pytestmark = pytest.mark.gpu
+
+GRADS = ("dq", "dk", "dv", "dg", "dbeta", "dw_g", "db_g", "dnorm_w_soft", "dnorm_w_lin")
+
+
+def _case(B, H, L, d, dtype, seed):
+    inp = gen.make_inputs(B, H, L, d, dtype=dtype, seed=seed, pattern="random", frac=0.5)
+    rng = np.random.default_rng(seed + 500)
+    nws = (1 + 0.2 * rng.standard_normal(d)).astype(np.float32)
+    nwl = (1 + 0.2 * rng.standard_normal(d)).astype(np.float32)
+    inp.b_g[:] = (0.3 * rng.standard_normal(H)).astype(np.float32)
+    dout = rng.standard_normal((B, H, L, d)).astype(np.float32)
+    if dtype == "bf16":
+        dout = gen.round_to_bf16(dout)  # the values the device holds
+    return inp, nws, nwl, dout
+
+
+def _dev(x, dtype):
+    t = torch.from_numpy(np.ascontiguousarray(x, np.float32)).cuda()
+    return t.bfloat16() if dtype == "bf16" else t
+
+
+def _oracle(inp, nws, nwl, dout, sel):
+    return ob.backward(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.w_g, inp.b_g, sel, dout,
+                       norm_w_soft=nws, norm_w_lin=nwl)
+
+
+def _compare(got, ref, tol, label):
+    errs = {n: rel_err(got[n].cpu().numpy(), ref[n]) for n in GRADS}
+    print(f"[parity] backward {label}: " + " ".join(f"{n}={e:.1e}" for n, e in errs.items()))
+    for n, e in errs.items():
+        assert e <= tol, (n, e)
+
+
+@pytest.mark.parametrize("B,H,L,d,dtype,seed", [
+    (1, 2, 256, 64, "f32", 41), (1, 2, 256, 128, "f32", 42), (2, 2, 384, 128, "bf16", 43), (1, 3, 192, 64, "bf16", 44)])
+def test_backward_on_oracle_activations(B, H, L, d, dtype, seed):
+    import linear_attention_nats_gb300 as nats
+    from linear_attention_nats_gb300 import build
+
+    build.build()
+    inp, nws, nwl, dout = _case(B, H, L, d, dtype, seed)
+    sel = oracle.select_inputs(inp)[0].reshape(B, H, L // 64)
+    ref = _oracle(inp, nws, nwl, dout, sel)
+    t = to_device(inp)
+    got = nats.hybrid_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_g"], t["b_g"],
+                          torch.from_numpy(sel).cuda(), _dev(ref["o_s"], "f32"), _dev(ref["o_l"], "f32"),
+                          _dev(dout, dtype), norm_w_soft=_dev(nws, "f32"), norm_w_lin=_dev(nwl, "f32"))
+    torch.cuda.synchronize()
+    _compare(got, ref, TOL["f32"], f"{dtype}-{d} (oracle activations)")
+
+
+@pytest.mark.parametrize("B,H,L,d,dtype,seed", [(1, 2, 256, 64, "f32", 45), (2, 2, 320, 128, "bf16", 46)])
+def test_backward_after_cuda_forward(B, H, L, d, dtype, seed):
+    import linear_attention_nats_gb300 as nats
+    from linear_attention_nats_gb300 import build
+
+    build.build()
+    inp, nws, nwl, dout = _case(B, H, L, d, dtype, seed)
+    t = to_device(inp)
+    nw = {"norm_w_soft": _dev(nws, "f32"), "norm_w_lin": _dev(nwl, "f32")}
+    fwd = nats.hybrid_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_s"], t["b_s"], t["w_g"], t["b_g"],
+                          return_sel=True, return_branches=True, check_errors=True, **nw)
+    sel_ref = oracle.select_inputs(inp)[0].reshape(B, H, L // 64)
+    assert np.array_equal(fwd["sel"].cpu().numpy(), sel_ref)
+    got = nats.hybrid_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_g"], t["b_g"], fwd["sel"],
+                          fwd["o_soft"], fwd["o_lin"], _dev(dout, dtype), **nw)
+    torch.cuda.synchronize()
+    _compare(got, _oracle(inp, nws, nwl, dout, sel_ref), TOL[dtype], f"{dtype}-{d} (after the CUDA forward)")
+
+
+def test_backward_all_softmax_and_all_linear():
+    # the two degenerate selections: every chunk softmax (no Gated DeltaNet
+    # state survives a chunk), every chunk Gated DeltaNet (only the own chunk
+    # is attended by softmax)
+    import linear_attention_nats_gb300 as nats
+    from linear_attention_nats_gb300 import build
+
+    build.build()
+    inp, nws, nwl, dout = _case(1, 2, 256, 64, "f32", 47)
+    t = to_device(inp)
+    for fill in (0, 1):
+        sel = np.full((1, 2, 4), fill, np.uint8)
+        ref = _oracle(inp, nws, nwl, dout, sel)
+        got = nats.hybrid_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_g"], t["b_g"],
+                              torch.from_numpy(sel).cuda(), _dev(ref["o_s"], "f32"), _dev(ref["o_l"], "f32"),
+                              _dev(dout, "f32"), norm_w_soft=_dev(nws, "f32"), norm_w_lin=_dev(nwl, "f32"))
+        torch.cuda.synchronize()
+        _compare(got, ref, TOL["f32"], f"all {'softmax' if fill == 0 else 'linear'}")
