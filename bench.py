@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-x-path", action="store_true", help="skip the layer-with-projections measurement")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass measurement")
     return ap.parse_args()
 
 
@@ -485,6 +486,8 @@ def run_native(args, rank, world, local_rank):
         res["x_path"] = run_x_path(args, rank, dev, stream, dist)
     if not args.no_decode:
         res["decode"] = run_decode(args, rank, dev, stream, dist)
+    if not args.no_backward:
+        res["backward"] = run_backward(args, dev, stream, dist, dv, B, H, L, d, work)
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
     if not args.no_cpu_baseline and world == 1 and rank == 0:
         cores = cpu_cores()
@@ -554,6 +557,61 @@ def run_x_path(args, rank, dev, stream, dist):
             "config": {"B": B, "H": H, "L": L, "d": d, "hidden": hidden},
             "value": job_throughput(B * L, world, ms), "unit": "tokens/s", "ms_per_step": ms,
             "projection_gemm_flops_per_step": gemm_flops}
+
+
+def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):
+    """Times nats_hybrid_bwd on the layer workload: the gradients of a seeded
+    dout at the forward's selection, from the activations the CUDA forward
+    saved (one forward outside the timed region).  Its contractions run on
+    the CUDA cores in fp32, so the roofline is the fp32 FMA rate: 152 SMs x
+    128 lanes x 2 FLOP x the SM clock.  Algorithmic FLOPs: 10 d per visible
+    (query, key) pair of the softmax branch (recomputed scores, dP, dq, dk,
+    dv) and 14 d^2 per token of Gated DeltaNet (dS += do q^T, S^T do,
+    dS k, the two column sums of dk, <dS, S>, the dS update)."""
+    import torch
+
+    import linear_attention_nats_gb300 as nats
+
+    t = dv
+    fwd = nats.hybrid_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_s"], t["b_s"], t["w_g"], t["b_g"],
+                          return_sel=True, return_branches=True, stream=stream)
+    gen_ = torch.Generator(device="cpu").manual_seed(43)
+    dout = torch.randn((B, H, L, d), generator=gen_).to(t["q"].dtype).to(dev)
+    dm = nats.dims(B, H, L, d, 0 if t["q"].dtype == torch.bfloat16 else 1)
+    ws = torch.empty(int(nats._native.lib.nats_bwd_workspace_size(ctypes.byref(dm))), dtype=torch.uint8, device=dev)
+
+    def step():
+        return nats.hybrid_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_g"], t["b_g"], fwd["sel"],
+                               fwd["o_soft"], fwd["o_lin"], dout, workspace=ws, stream=stream)
+
+    steps = max(1, min(args.steps, 3))
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev) / steps
+    world = dist.get_world_size() if dist is not None else 1
+    pairs = work["flops_softmax"] / (4 * d)
+    flops = 10 * d * pairs + 14 * d * d * B * H * L
+    sm_mhz = 2070.0
+    peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+    achieved = flops / (ms / 1e3) / 1e12
+    return {"what": "nats_hybrid_bwd: gradients of q, k, v, g, beta, W_g, b_g and the RMSNorm weights at the "
+                    "forward's selection, same workload as the forward",
+            "value": job_throughput(B * L, world, ms), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
+            "launches_per_step": 4,
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "flops_per_step": flops,
+                         "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x 2070 MHz"}}
 
 
 def run_decode(args, rank, dev, stream, dist):
