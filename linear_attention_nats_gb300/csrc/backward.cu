@@ -14,11 +14,13 @@
 //      dq = dz W_g (the gate's share), and the weight gradients (dW_g,
 //      db_g, the norm weights) summed per CTA, then atomically;
 //   2. softmax branch, from the row log-sum-exp: P_tj = exp(s_tj - lse_t),
-//      dS_tj = P_tj (do_s,t . v_j - do_s,t . o_s,t); a row pass (one warp
-//      per query) takes lse_t and dq_t += scale sum_j dS_tj k_j, a key pass
-//      (one warp per key) dk_j = scale sum_t dS_tj q_t and
-//      dv_j = sum_t P_tj do_s,t over the queries that see key j (the rest of
-//      its chunk, and every later query when its chunk chose softmax);
+//      dS_tj = P_tj (do_s,t . v_j - do_s,t . o_s,t); bf16 layers take it on
+//      warp-level tensor-core MMAs in 64 x 64 blocks (backward_mma.cu);
+//      fp32 layers here: a row pass (one warp per query) takes lse_t and
+//      dq_t += scale sum_j dS_tj k_j, a key pass (one warp per key)
+//      dk_j = scale sum_t dS_tj q_t and dv_j = sum_t P_tj do_s,t over the
+//      queries that see key j (the rest of its chunk, and every later query
+//      when its chunk chose softmax);
 //   3. Gated DeltaNet, one CTA per (b, h): the forward is replayed for the
 //      chunk-start states, then the adjoint runs backwards.  Per token, with
 //      u = S_{t-1} k, e = v - a u, S_t = a S_{t-1} + beta e k^T and
@@ -33,6 +35,8 @@
 //      start state, so the gradient arriving there passes to the start
 //      unchanged and the tokens inside start from zero.  The states inside a
 //      chunk are replayed into scratch before its tokens are reversed.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -58,8 +62,9 @@ __global__ void __launch_bounds__(256) merge_bwd_kernel(
     const T* __restrict__ q, const T* __restrict__ dout, const float* __restrict__ o_s,
     const float* __restrict__ o_l, const float* __restrict__ w_g, const float* __restrict__ b_g,
     const float* __restrict__ nws, const float* __restrict__ nwl, int H, int L, float eps,
-    float* __restrict__ d_os, float* __restrict__ d_ol, float* __restrict__ delta, float* __restrict__ dq,
-    float* __restrict__ dw_g, float* __restrict__ db_g, float* __restrict__ dnws, float* __restrict__ dnwl) {
+    float* __restrict__ d_os, __nv_bfloat16* __restrict__ d_os16, float* __restrict__ d_ol,
+    float* __restrict__ delta, float* __restrict__ dq, float* __restrict__ dw_g, float* __restrict__ db_g,
+    float* __restrict__ dnws, float* __restrict__ dnwl) {
   constexpr int E = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int per_head = L / kMergeRows;
@@ -116,6 +121,7 @@ __global__ void __launch_bounds__(256) merge_bwd_kernel(
       const float g_s = rs * ws[x] * w * R[x] - os[x] * rs * rs * rs * gs / D;
       const float g_l = rl * wl[x] * (1.f - w) * R[x] - ol[x] * rl * rl * rl * gl / D;
       d_os[t * D + lane * E + x] = g_s;
+      if (d_os16) d_os16[t * D + lane * E + x] = __float2bfloat16_rn(g_s);
       d_ol[t * D + lane * E + x] = g_l;
       dq[t * D + lane * E + x] = dz * wg[x];
       dl = fmaf(g_s, os[x], dl);
@@ -510,6 +516,7 @@ size_t bwd_workspace_bytes(const Problem& p) {
   auto al = [](size_t b) { return (b + 255) & ~(size_t)255; };
   const size_t rows = (size_t)p.BH * p.L, dd = (size_t)p.d * p.d;
   return 2 * al(rows * p.d * 4)            // d o_s, d o_l
+         + al(rows * p.d * 2)              // d o_s in bf16 (the operand of the tensor-core products)
          + 2 * al(rows * 4)                // delta, lse
          + al((size_t)p.BH * p.N * dd * 4)  // chunk-start states
          + al((size_t)p.BH * kChunk * dd * 4)  // states inside the chunk being reversed
@@ -531,6 +538,8 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
   w += al((size_t)rows * p.d * 4);
   float* d_ol = (float*)w;
   w += al((size_t)rows * p.d * 4);
+  __nv_bfloat16* d_os16 = (__nv_bfloat16*)w;
+  w += al((size_t)rows * p.d * 2);
   float* delta = (float*)w;
   w += al((size_t)rows * 4);
   float* lse = (float*)w;
@@ -553,13 +562,19 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
     const T* qt = (const T*)q;
     const T* kt = (const T*)k;
     const T* vt = (const T*)v;
+    constexpr bool tc = std::is_same<T, __nv_bfloat16>::value;  // bf16: the softmax branch on tensor cores
     merge_bwd_kernel<T, D><<<(unsigned)(rows / kMergeRows), 256, 0, st>>>(
-        qt, (const T*)dout, o_s, o_l, w_g, b_g, nws, nwl, p.H, p.L, p.eps, d_os, d_ol, delta, dq, dw_g, db_g,
-        dnws, dnwl);
-    softmax_bwd_rows_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(qt, kt, vt, sel, d_os, delta, rows,
-                                                                             p.L, p.N, p.scale, lse, dq);
-    softmax_bwd_keys_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
-        qt, kt, vt, sel, d_os, delta, lse, rows, p.L, p.N, p.scale, dk, dv);
+        qt, (const T*)dout, o_s, o_l, w_g, b_g, nws, nwl, p.H, p.L, p.eps, d_os, tc ? d_os16 : nullptr, d_ol,
+        delta, dq, dw_g, db_g, dnws, dnwl);
+    if (tc) {
+      const cudaError_t e2 = launch_softmax_bwd_mma(p, q, k, v, d_os16, delta, sel, lse, dq, dk, dv, st);
+      if (e2 != cudaSuccess) return e2;
+    } else {
+      softmax_bwd_rows_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(qt, kt, vt, sel, d_os, delta,
+                                                                               rows, p.L, p.N, p.scale, lse, dq);
+      softmax_bwd_keys_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
+          qt, kt, vt, sel, d_os, delta, lse, rows, p.L, p.N, p.scale, dk, dv);
+    }
     constexpr int smem = GdnBwd<D>::kBytes;
     static const cudaError_t attr =
         cudaFuncSetAttribute(gdn_bwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -68,6 +68,12 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
                               float* dbeta, float* dw_g, float* db_g, float* dnws, float* dnwl, void* ws,
                               cudaStream_t st);
 
+// Softmax branch of the backward pass on warp-level MMAs, bf16 layers
+// (backward_mma.cu): lse and dq (+=), then dk, dv (=).
+cudaError_t launch_softmax_bwd_mma(const Problem& p, const void* q, const void* k, const void* v, const void* dos,
+                                   const float* delta, const uint8_t* sel, float* lse, float* dq, float* dk,
+                                   float* dv, cudaStream_t st);
+
 // Test hook: one bounded wait that runs out after limit_ns and sets *flag.
 cudaError_t launch_bounded_wait(int* flag, long long limit_ns, cudaStream_t st);
 
