@@ -34,7 +34,9 @@
 //      A chunk that chose softmax was rolled back: the state after it is its
 //      start state, so the gradient arriving there passes to the start
 //      unchanged and the tokens inside start from zero.  The states inside a
-//      chunk are replayed into scratch before its tokens are reversed.
+//      chunk are replayed into scratch before its tokens are reversed.  The
+//      state rows are split between two CTAs per head; a last kernel adds
+//      the halves' column sums and scalars per token.
 #include <type_traits>
 
 #include "common.cuh"
@@ -276,43 +278,71 @@ __global__ void __launch_bounds__(256) softmax_bwd_keys_kernel(
 }
 
 // --------------------------------------------------- 3. Gated DeltaNet
-// One CTA of 512 threads per (b, h).  Thread (warp w, lane l) holds rows
-// [w RW, w RW + RW) x columns [l CW, l CW + CW) of a d x d matrix.
+// The rows of the state are independent under the delta rule, so a head's
+// d rows are split between kRowSplit CTAs of 512 threads.  Thread (warp w,
+// lane l) holds rows [w RW, w RW + RW) of its CTA's half x columns
+// [l CW, l CW + CW).  Column sums and scalars are per-half partials, added
+// by gdn_bwd_combine_kernel.  Each token's vectors are read into registers
+// two steps ahead, and in the reverse sweep each thread copies its elements
+// of the state two tokens back into a three-slot shared-memory ring
+// (cp.async), so global latency hides behind the arithmetic of two tokens.
 constexpr int kGdnThreads = 512;
+constexpr int kRowSplit = 2;
 
 template <int D>
 struct GdnBwd {
-  static constexpr int RW = D / 16;  // rows per warp
-  static constexpr int CW = D / 32;  // columns per lane
+  static constexpr int RH = D / kRowSplit;  // rows per CTA
+  static constexpr int RW = RH / 16;        // rows per warp
+  static constexpr int CW = D / 32;         // columns per lane
+  // a token's vectors: k, scale q, v and do of the CTA's rows, a, beta
+  static constexpr int TOK = 2 * D + 2 * RH + 2;
   // shared memory (floats)
-  static constexpr int offTok = 0;                  // [2][6][D]: k, scale q, v, do, then a, beta
-  static constexpr int offU = offTok + 2 * 6 * D;   // [kChunk][D] u_t of the replayed chunk
-  static constexpr int offColA = offU + kChunk * D; // [16][D]
-  static constexpr int offColB = offColA + 16 * D;  // [16][D]
-  static constexpr int offRed = offColB + 16 * D;   // [16][3]
-  static constexpr int kFloats = offRed + 48;
+  static constexpr int offTok = 0;                    // [2][TOK]
+  static constexpr int offU = offTok + 2 * TOK;       // [kChunk][RH] u_t of the replayed chunk
+  static constexpr int offColA = offU + kChunk * RH;  // [16][D]
+  static constexpr int offColB = offColA + 16 * D;    // [16][D]
+  static constexpr int offRed = offColB + 16 * D;     // [16][3]
+  static constexpr int offSt = offRed + 64;            // [3][RH][D] states before the coming tokens
+  static constexpr int kFloats = offSt + 3 * RH * D;
   static constexpr int kBytes = kFloats * 4;
 };
+
+// asynchronous copy of `bytes` (8 or 16) global -> shared by this thread
+template <int BYTES>
+__device__ __forceinline__ void cp_async(float* dst, const float* src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  if constexpr (BYTES == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kGdnThreads, 1) gdn_bwd_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, const float* __restrict__ g,
     const float* __restrict__ beta, const uint8_t* __restrict__ sel, const float* __restrict__ d_ol, int L,
     int N, float scale, float* __restrict__ Sc, float* __restrict__ Tk, float* __restrict__ dSx,
-    float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv, float* __restrict__ dg,
-    float* __restrict__ dbeta) {
+    float* __restrict__ pcol, float* __restrict__ psc, float* __restrict__ dv) {
   using G = GdnBwd<D>;
-  constexpr int RW = G::RW, CW = G::CW;
+  constexpr int RH = G::RH, RW = G::RW, CW = G::CW, TOK = G::TOK;
   extern __shared__ __align__(16) float sm[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const long long bh = blockIdx.x;
+  const long long bh = blockIdx.x / kRowSplit;
+  const int part = (int)(blockIdx.x % kRowSplit);
+  const int row0 = part * RH;  // first state row of this CTA
   const long long h0 = bh * L;
   const uint8_t* sel_h = sel + bh * N;
-  float* sc_h = Sc + bh * (long long)N * D * D;  // chunk-start states
-  float* tk_h = Tk + bh * (long long)kChunk * D * D;  // states after each token of one chunk
+  float* sc_h = Sc + bh * (long long)N * D * D;        // chunk-start states
+  float* tk_h = Tk + bh * (long long)kChunk * D * D;   // states after each token of one chunk
   float* dsx_h = dSx + bh * (long long)D * D;
-  const int r0 = warp * RW, c0 = lane * CW;
-  auto el = [&](int i, int j) { return (long long)(r0 + i) * D + c0 + j; };  // offset in a d x d matrix
+  // this half's partials: column sums [L][2 D] and scalars [L][4]
+  float* pc = pcol + ((long long)part * (long long)(gridDim.x / kRowSplit) + bh) * L * 2 * D;
+  float* ps = psc + ((long long)part * (long long)(gridDim.x / kRowSplit) + bh) * L * 4;
+  const int r0 = warp * RW, c0 = lane * CW;  // within the half / the row
+  auto el = [&](int i, int j) { return (long long)(row0 + r0 + i) * D + c0 + j; };
   auto ld = [&](const float* M, float (&X)[RW][CW]) {
 #pragma unroll
     for (int i = 0; i < RW; ++i)
@@ -325,20 +355,21 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_bwd_kernel(
 #pragma unroll
       for (int j = 0; j < CW; ++j) M[el(i, j)] = X[i][j];
   };
-  // token t's vectors into buffer b (k, scale q, v, d o_l; a, beta)
-  auto load_tok = [&](int t, int b) {
-    float* tb = sm + G::offTok + b * 6 * D;
+  // this thread's element of token t's vectors (threads >= TOK: none)
+  auto fetch = [&](int t) -> float {
     const long long r = h0 + t;
-    if (tid < D) tb[tid] = to_f32(k[r * D + tid]);
-    else if (tid < 2 * D) tb[tid] = scale * to_f32(q[r * D + tid - D]);
-    else if (tid < 3 * D) tb[tid] = to_f32(v[r * D + tid - 2 * D]);
-    else if (tid < 4 * D) tb[tid] = d_ol[r * D + tid - 3 * D];
-    if (tid == 0) {
-      tb[4 * D] = expf(g[r]);
-      tb[4 * D + 1] = beta[r];
-    }
+    if (tid < D) return to_f32(k[r * D + tid]);
+    if (tid < 2 * D) return scale * to_f32(q[r * D + tid - D]);
+    if (tid < 2 * D + RH) return to_f32(v[r * D + row0 + tid - 2 * D]);
+    if (tid < 2 * D + 2 * RH) return d_ol[r * D + row0 + tid - 2 * D - RH];
+    if (tid == 2 * D + 2 * RH) return expf(g[r]);
+    if (tid == 2 * D + 2 * RH + 1) return beta[r];
+    return 0.f;
   };
-  // row sums over the d columns of X (. y), every lane gets its warp's rows
+  auto tbuf = [&](int b) { return sm + G::offTok + b * TOK; };
+  auto put = [&](int b, float x) {
+    if (tid < TOK) tbuf(b)[tid] = x;
+  };
   auto row_dot = [&](const float (&X)[RW][CW], const float* y, float (&out)[RW]) {
 #pragma unroll
     for (int i = 0; i < RW; ++i) {
@@ -348,11 +379,11 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_bwd_kernel(
       out[i] = warp_sum(p);
     }
   };
-  // one forward token step on S (u = S k returned)
+  // one forward token step on this half of S; u = S_{t-1} k of its rows
   auto fwd_step = [&](float (&S)[RW][CW], const float* tb, float (&u)[RW]) {
     const float* kt = tb;
     const float* vt = tb + 2 * D;
-    const float a = tb[4 * D], bt = tb[4 * D + 1];
+    const float a = tb[2 * D + 2 * RH], bt = tb[2 * D + 2 * RH + 1];
     row_dot(S, kt, u);
 #pragma unroll
     for (int i = 0; i < RW; ++i) {
@@ -363,22 +394,27 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_bwd_kernel(
   };
 
   // phase A: the chunk-start states
+  int b = 0;
   {
     float S[RW][CW];
 #pragma unroll
     for (int i = 0; i < RW; ++i)
 #pragma unroll
       for (int j = 0; j < CW; ++j) S[i][j] = 0.f;
-    int tb_i = 0;
-    for (int c = 0; c < N; ++c) {
-      st(sc_h + (long long)c * D * D, S);
-      for (int t = c * kChunk; t < (c + 1) * kChunk; ++t, tb_i ^= 1) {
-        load_tok(t, tb_i);
-        __syncthreads();
-        float u[RW];
-        fwd_step(S, sm + G::offTok + tb_i * 6 * D, u);
-      }
-      if (sel_h[c] == 0) ld(sc_h + (long long)c * D * D, S);  // rollback (this thread's own elements)
+    put(b, fetch(0));
+    float pfa = L > 1 ? fetch(1) : 0.f;  // the next token's element, read a step ago
+    __syncthreads();
+    for (int t = 0; t < L; ++t) {
+      const int c = t / kChunk;
+      if (t % kChunk == 0) st(sc_h + (long long)c * D * D, S);
+      const float pfb = t + 2 < L ? fetch(t + 2) : 0.f;
+      float u[RW];
+      fwd_step(S, tbuf(b), u);
+      if (t % kChunk == kChunk - 1 && sel_h[c] == 0) ld(sc_h + (long long)c * D * D, S);  // rollback
+      put(b ^ 1, pfa);
+      pfa = pfb;
+      __syncthreads();
+      b ^= 1;
     }
   }
 
@@ -388,23 +424,29 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_bwd_kernel(
   for (int i = 0; i < RW; ++i)
 #pragma unroll
     for (int j = 0; j < CW; ++j) dS[i][j] = 0.f;
-  int tb_i = 0;
   for (int c = N - 1; c >= 0; --c) {
     const int t0 = c * kChunk;
     const bool rolled_back = sel_h[c] == 0;
+    float* sc_c = sc_h + (long long)c * D * D;
     // replay the chunk: the state after each token (but the last), and u_t
     {
       float S[RW][CW];
-      ld(sc_h + (long long)c * D * D, S);
-      for (int i = 0; i < kChunk; ++i, tb_i ^= 1) {
-        load_tok(t0 + i, tb_i);
-        __syncthreads();
+      ld(sc_c, S);
+      put(b, fetch(t0));
+      float pfa = fetch(t0 + 1);
+      __syncthreads();
+      for (int i = 0; i < kChunk; ++i) {
+        const float pfb = i + 2 < kChunk ? fetch(t0 + i + 2) : 0.f;
         float u[RW];
-        fwd_step(S, sm + G::offTok + tb_i * 6 * D, u);
+        fwd_step(S, tbuf(b), u);
         if (lane == 0)
 #pragma unroll
-          for (int x = 0; x < RW; ++x) sm[G::offU + i * D + r0 + x] = u[x];
+          for (int x = 0; x < RW; ++x) sm[G::offU + i * RH + r0 + x] = u[x];
         if (i + 1 < kChunk) st(tk_h + (long long)i * D * D, S);
+        put(b ^ 1, pfa);
+        pfa = pfb;
+        __syncthreads();
+        b ^= 1;
       }
     }
     // the gradient arriving at the state after the chunk: through the
@@ -416,18 +458,43 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_bwd_kernel(
 #pragma unroll
         for (int j = 0; j < CW; ++j) dS[i][j] = 0.f;
     }
-    for (int i = kChunk - 1; i >= 0; --i, tb_i ^= 1) {
+    // the state before token i: after token i - 1, or the chunk start
+    auto before = [&](int i) -> const float* { return i > 0 ? tk_h + (long long)(i - 1) * D * D : sc_c; };
+    // this thread's elements of the state before token i, into ring slot i % 3
+    auto stage = [&](int i) {
+      const float* src = before(i);
+      float* dst = sm + G::offSt + (i % 3) * RH * D;
+#pragma unroll
+      for (int x = 0; x < RW; ++x) cp_async<CW * 4>(dst + (r0 + x) * D + c0, src + el(x, 0));
+    };
+    stage(kChunk - 1);
+    cp_async_commit();
+    stage(kChunk - 2);
+    cp_async_commit();
+    put(b, fetch(t0 + kChunk - 1));
+    float pfa = fetch(t0 + kChunk - 2);
+    __syncthreads();
+    for (int i = kChunk - 1; i >= 0; --i) {
       const int t = t0 + i;
-      load_tok(t, tb_i);
+      // two steps ahead: token i - 2's element and the state before it
+      const float pfb = i >= 2 ? fetch(t - 2) : 0.f;
+      if (i >= 2) stage(i - 2);
+      cp_async_commit();
+      cp_async_wait<2>();  // this thread's copy of the state before token i has landed
       float Sb[RW][CW];
-      ld(i > 0 ? tk_h + (long long)(i - 1) * D * D : sc_h + (long long)c * D * D, Sb);
-      __syncthreads();
-      const float* tb = sm + G::offTok + tb_i * 6 * D;
+      {
+        const float* src = sm + G::offSt + (i % 3) * RH * D;
+#pragma unroll
+        for (int x = 0; x < RW; ++x)
+#pragma unroll
+          for (int j = 0; j < CW; ++j) Sb[x][j] = src[(r0 + x) * D + c0 + j];
+      }
+      const float* tb = tbuf(b);
       const float* kt = tb;
       const float* qt = tb + D;
       const float* vt = tb + 2 * D;
-      const float* dot = tb + 3 * D;
-      const float a = tb[4 * D], bt = tb[4 * D + 1];
+      const float* dot = tb + 2 * D + RH;
+      const float a = tb[2 * D + 2 * RH], bt = tb[2 * D + 2 * RH + 1];
       // dS_t += do_t (scale q_t)^T; S_{t-1}^T do_t (column sums)
       float colA[CW], colB[CW];
 #pragma unroll
@@ -446,7 +513,7 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_bwd_kernel(
       float p_da = 0.f, p_db = 0.f, p_ed = 0.f;
 #pragma unroll
       for (int x = 0; x < RW; ++x) {
-        const float u = sm[G::offU + i * D + r0 + x];
+        const float u = sm[G::offU + i * RH + r0 + x];
         const float e = vt[r0 + x] - a * u;
         const float de = bt * xr[x];
 #pragma unroll
@@ -459,7 +526,7 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_bwd_kernel(
           p_da -= u * de;
           p_db = fmaf(e, xr[x], p_db);
           p_ed = fmaf(e, dot[r0 + x], p_ed);
-          dv[(h0 + t) * D + r0 + x] += de;
+          dv[(h0 + t) * D + row0 + r0 + x] += de;
         }
         // dS_{t-1} = a dS_t - a de k^T
 #pragma unroll
@@ -477,27 +544,24 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_bwd_kernel(
         sm[G::offRed + 3 * warp + 2] = p_ed;
       }
       __syncthreads();
-      if (tid < D) {
-        float sa = 0.f, sb = 0.f, ed = 0.f;
+      // this half's partials of token t
+      if (tid < 2 * D) {
+        const int off = tid < D ? G::offColA + tid : G::offColB + tid - D;
+        float sum = 0.f;
 #pragma unroll
-        for (int w = 0; w < 16; ++w) {
-          sa += sm[G::offColA + w * D + tid];
-          sb += sm[G::offColB + w * D + tid];
-          ed += sm[G::offRed + 3 * w + 2];
-        }
-        // S_t^T do_t = a S_{t-1}^T do_t + beta <e, do_t> k_t
-        dq[(h0 + t) * D + tid] += scale * fmaf(a, sa, bt * ed * kt[tid]);
-        dk[(h0 + t) * D + tid] += sb;
-      } else if (tid == D) {
-        float da = 0.f, db = 0.f;
+        for (int w = 0; w < 16; ++w) sum += sm[off + w * D];
+        pc[(long long)t * 2 * D + tid] = sum;
+      } else if (tid < 2 * D + 3) {
+        const int which = tid - 2 * D;
+        float sum = 0.f;
 #pragma unroll
-        for (int w = 0; w < 16; ++w) {
-          da += sm[G::offRed + 3 * w];
-          db += sm[G::offRed + 3 * w + 1];
-        }
-        dg[h0 + t] = a * da;
-        dbeta[h0 + t] = db;
+        for (int w = 0; w < 16; ++w) sum += sm[G::offRed + 3 * w + which];
+        ps[(long long)t * 4 + which] = sum;
       }
+      put(b ^ 1, pfa);
+      pfa = pfb;
+      __syncthreads();
+      b ^= 1;
     }
     if (rolled_back) {
       float X[RW][CW];
@@ -507,6 +571,48 @@ __global__ void __launch_bounds__(kGdnThreads, 1) gdn_bwd_kernel(
 #pragma unroll
         for (int j = 0; j < CW; ++j) dS[i][j] += X[i][j];
     }
+  }
+}
+
+// The halves' partials of each token combined: S_t^T do_t = a S_{t-1}^T do_t
+// + beta <e, do_t> k_t gives dq, the column sums of dk add up, and
+// dg = a da, dbeta.  One warp per token.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) gdn_bwd_combine_kernel(
+    const T* __restrict__ k, const float* __restrict__ g, const float* __restrict__ beta,
+    const float* __restrict__ pcol, const float* __restrict__ psc, long long rows, float scale,
+    float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dg, float* __restrict__ dbeta) {
+  constexpr int E = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long r = (long long)blockIdx.x * 8 + warp;
+  if (r >= rows) return;  // warp-uniform
+  const float a = expf(g[r]), bt = beta[r];
+  float da = 0.f, db = 0.f, ed = 0.f;
+#pragma unroll
+  for (int h = 0; h < kRowSplit; ++h) {
+    const float* s4 = psc + ((long long)h * rows + r) * 4;
+    da += s4[0];
+    db += s4[1];
+    ed += s4[2];
+  }
+  float kv[E];
+  row_load<E>(k + r * D + lane * E, kv);
+#pragma unroll
+  for (int x = 0; x < E; ++x) {
+    const int f = lane * E + x;
+    float ca = 0.f, cb = 0.f;
+#pragma unroll
+    for (int h = 0; h < kRowSplit; ++h) {
+      const float* pr = pcol + ((long long)h * rows + r) * 2 * D;
+      ca += pr[f];
+      cb += pr[D + f];
+    }
+    dq[r * D + f] += scale * fmaf(a, ca, bt * ed * kv[x]);
+    dk[r * D + f] += cb;
+  }
+  if (lane == 0) {
+    dg[r] = a * da;
+    dbeta[r] = db;
   }
 }
 
@@ -520,7 +626,9 @@ size_t bwd_workspace_bytes(const Problem& p) {
          + 2 * al(rows * 4)                // delta, lse
          + al((size_t)p.BH * p.N * dd * 4)  // chunk-start states
          + al((size_t)p.BH * kChunk * dd * 4)  // states inside the chunk being reversed
-         + al((size_t)p.BH * dd * 4);       // gradient held over a rolled-back chunk
+         + al((size_t)p.BH * dd * 4)        // gradient held over a rolled-back chunk
+         + al((size_t)kRowSplit * rows * 2 * p.d * 4)  // the state halves' column sums per token
+         + al((size_t)kRowSplit * rows * 4 * 4);        // and their scalars
 }
 
 cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const void* k, const void* v,
@@ -549,6 +657,10 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
   float* Tk = (float*)w;
   w += al((size_t)p.BH * kChunk * dd * 4);
   float* dSx = (float*)w;
+  w += al((size_t)p.BH * dd * 4);
+  float* pcol = (float*)w;
+  w += al((size_t)kRowSplit * rows * 2 * p.d * 4);
+  float* psc = (float*)w;
   // weight gradients are sums over the launch: zeroed first
   cudaError_t e = cudaSuccess;
   if (dw_g) e = cudaMemsetAsync(dw_g, 0, (size_t)p.H * p.d * 4, st);
@@ -579,8 +691,10 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
     static const cudaError_t attr =
         cudaFuncSetAttribute(gdn_bwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (attr != cudaSuccess) return attr;
-    gdn_bwd_kernel<T, D><<<(unsigned)p.BH, kGdnThreads, smem, st>>>(qt, kt, vt, g, beta, sel, d_ol, p.L, p.N,
-                                                                    p.scale, Sc, Tk, dSx, dq, dk, dv, dg, dbeta);
+    gdn_bwd_kernel<T, D><<<(unsigned)(p.BH * kRowSplit), kGdnThreads, smem, st>>>(
+        qt, kt, vt, g, beta, sel, d_ol, p.L, p.N, p.scale, Sc, Tk, dSx, pcol, psc, dv);
+    gdn_bwd_combine_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(kt, g, beta, pcol, psc, rows, p.scale,
+                                                                            dq, dk, dg, dbeta);
     return cudaGetLastError();
   };
   using bf = __nv_bfloat16;

@@ -167,11 +167,12 @@ def test_backward_validation(nat):
     # the backward pass: argument checks before any launch
     dm = nat.dims(1, 2, 128, 64)
     need = nat.lib.nats_bwd_workspace_size(ctypes.byref(dm))
-    # d o_s, d o_l (fp32), d o_s (bf16), delta, lse, 2 chunk-start states, one chunk of states, one held gradient
+    # d o_s, d o_l (fp32), d o_s (bf16), delta, lse, 2 chunk-start states, one chunk of states, one held
+    # gradient, then the two state halves' per-token column sums and scalars
     rows, dd = 2 * 128, 64 * 64
     al = lambda b: (b + 255) // 256 * 256
     assert need == (2 * al(rows * 64 * 4) + al(rows * 64 * 2) + 2 * al(rows * 4) + al(2 * 2 * dd * 4)
-                    + al(2 * 64 * dd * 4) + al(2 * dd * 4))
+                    + al(2 * 64 * dd * 4) + al(2 * dd * 4) + al(2 * rows * 2 * 64 * 4) + al(2 * rows * 4 * 4))
     fake = ctypes.c_void_p(256)
     odd = ctypes.c_void_p(264)
     args = [fake] * 23  # q ... dnorm_w_lin, then the workspace
