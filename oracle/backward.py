@@ -45,10 +45,15 @@ def _mask(sel_bh, L, chunk):
     return causal & (same | soft[None, :])
 
 
-def forward_torch(x, sel, *, chunk=64, scale=0.0, eps=1e-6):
+def forward_torch(x, sel, *, chunk=64, scale=0.0, eps=1e-6, prefix_k=None, prefix_v=None, state0=None):
     """The layer at selection `sel` [B, H, N] on the float64 tensors of dict
     x (q, k, v [B, H, L, d]; g, beta [B, H, L]; w_g [H, d]; b_g [H]; norm
-    weights [d]).  Returns (out, o_s, o_l), each [B, H, L, d]."""
+    weights [d]).  Returns (out, o_s, o_l), each [B, H, L, d].
+
+    The tokens may continue a longer sequence: prefix_k, prefix_v
+    [B, H, P, d] are the retained keys / values of its earlier softmax
+    chunks (seen by every query here), state0 [B, H, dv, dk] its Gated
+    DeltaNet state at this point (both constants)."""
     q, k, v, g, beta = x["q"], x["k"], x["v"], x["g"], x["beta"]
     B, H, L, dk = q.shape
     dv = v.shape[-1]
@@ -63,9 +68,14 @@ def forward_torch(x, sel, *, chunk=64, scale=0.0, eps=1e-6):
             M = _mask(sel[b, h], L, chunk)
             logits = (qh @ kh.T) * sc
             logits = logits.masked_fill(~M, float("-inf"))
-            o_s = torch.softmax(logits, dim=-1) @ vh
+            if prefix_k is not None:  # the earlier retained keys, seen by every query
+                pk = torch.as_tensor(prefix_k[b, h], dtype=q.dtype)
+                pv = torch.as_tensor(prefix_v[b, h], dtype=q.dtype)
+                o_s = torch.softmax(torch.cat([(qh @ pk.T) * sc, logits], dim=-1), dim=-1) @ torch.cat([pv, vh])
+            else:
+                o_s = torch.softmax(logits, dim=-1) @ vh
             # Gated DeltaNet branch: token recurrence with chunk rollback
-            S = torch.zeros(dv, dk, dtype=q.dtype)
+            S = torch.zeros(dv, dk, dtype=q.dtype) if state0 is None else torch.as_tensor(state0[b, h], dtype=q.dtype)
             rows = []
             for c in range(N):
                 S0 = S
@@ -103,12 +113,14 @@ def inputs64(q, k, v, g, beta, w_g, b_g=None, norm_w_soft=None, norm_w_lin=None)
 
 
 def backward(q, k, v, g, beta, w_g, b_g, sel, dout, *, norm_w_soft=None, norm_w_lin=None, chunk=64,
-             scale=0.0, eps=1e-6):
+             scale=0.0, eps=1e-6, prefix_k=None, prefix_v=None, state0=None):
     """Gradients of <dout, out> at selection `sel`, float64 numpy arrays named
     as the inputs (dq, dk, dv [B, H, L, d]; dg, dbeta [B, H, L]; dw_g [H, d];
-    db_g [H]; dnorm_w_soft, dnorm_w_lin [d]); also the forward's out, o_s, o_l."""
+    db_g [H]; dnorm_w_soft, dnorm_w_lin [d]); also the forward's out, o_s, o_l.
+    prefix_k, prefix_v, state0: as for forward_torch (constants)."""
     x = inputs64(q, k, v, g, beta, w_g, b_g, norm_w_soft, norm_w_lin)
-    out, o_s, o_l = forward_torch(x, np.asarray(sel), chunk=chunk, scale=scale, eps=eps)
+    out, o_s, o_l = forward_torch(x, np.asarray(sel), chunk=chunk, scale=scale, eps=eps, prefix_k=prefix_k,
+                                  prefix_v=prefix_v, state0=state0)
     grads = torch.autograd.grad(out, [x[n] for n in NAMES], torch.as_tensor(np.asarray(dout, np.float64)))
     res = {"d" + n: gr.detach().numpy() for n, gr in zip(NAMES, grads)}
     res.update(out=out.detach().numpy(), o_s=o_s.detach().numpy(), o_l=o_l.detach().numpy())

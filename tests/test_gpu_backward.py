@@ -109,3 +109,43 @@ def test_backward_all_softmax_and_all_linear():
                               _dev(dout, "f32"), norm_w_soft=_dev(nws, "f32"), norm_w_lin=_dev(nwl, "f32"))
         torch.cuda.synchronize()
         _compare(got, ref, TOL["f32"], f"all {'softmax' if fill == 0 else 'linear'}")
+
+
+def test_backward_full_size_last_chunk():
+    # the benchmark's workload (B=4 H=16 L=8192 d=128 bf16, 25 % softmax
+    # chunks) through the CUDA forward and backward as bench.py runs them;
+    # sampled: the last chunk of two heads, whose gradients (dq, dk, dv, dg,
+    # dbeta) the oracle takes exactly from the retained keys / values before
+    # it and the Gated DeltaNet state at its start
+    import linear_attention_nats_gb300 as nats
+    from linear_attention_nats_gb300 import build
+
+    build.build()
+    inp = gen.make_inputs(name="l8192", **gen.CONFIGS["l8192"])
+    B, H, L, d = inp.B, inp.H, inp.L, inp.d
+    N, L0 = L // 64, L - 64
+    t = to_device(inp)
+    fwd = nats.hybrid_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_s"], t["b_s"], t["w_g"], t["b_g"],
+                          return_sel=True, return_branches=True, check_errors=True)
+    dout = gen.round_to_bf16(np.random.default_rng(48).standard_normal((B, H, L, d)).astype(np.float32))
+    got = nats.hybrid_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_g"], t["b_g"], fwd["sel"], fwd["o_soft"],
+                          fwd["o_lin"], _dev(dout, "bf16"))
+    torch.cuda.synchronize()
+    sel = fwd["sel"].cpu().numpy()
+    sl = slice(L0, L)
+    for b, h in ((0, 3), (3, 13)):
+        one = lambda a: np.ascontiguousarray(a[b:b + 1, h:h + 1])
+        q, k, v, g, beta = (one(getattr(inp, n)) for n in ("q", "k", "v", "g", "beta"))
+        assert np.array_equal(oracle.select(q, k, inp.w_s[h:h + 1], inp.b_s[h:h + 1])[0][0, 0], sel[b, h])
+        state0 = oracle.forward(q[:, :, :L0], k[:, :, :L0], v[:, :, :L0], g[:, :, :L0], beta[:, :, :L0],
+                                inp.w_s[h:h + 1], inp.b_s[h:h + 1], inp.w_g[h:h + 1], inp.b_g[h:h + 1],
+                                sel_in=sel[b:b + 1, h:h + 1, :N - 1], outputs=("state",))["state"].reshape(1, 1, d, d)
+        keep = np.flatnonzero(np.repeat(sel[b, h, :N - 1] == 0, 64))
+        ref = ob.backward(q[:, :, sl], k[:, :, sl], v[:, :, sl], g[:, :, sl], beta[:, :, sl], inp.w_g[h:h + 1],
+                          inp.b_g[h:h + 1], sel[b:b + 1, h:h + 1, N - 1:], dout[b:b + 1, h:h + 1, sl],
+                          prefix_k=k[:, :, keep], prefix_v=v[:, :, keep], state0=state0)
+        errs = {n: rel_err(got[n][b, h, sl].cpu().numpy(), ref[n][0, 0]) for n in ("dq", "dk", "dv", "dg", "dbeta")}
+        print(f"[parity] backward l8192 head ({b}, {h}), last chunk, {len(keep)} retained keys: "
+              + " ".join(f"{n}={e:.1e}" for n, e in errs.items()))
+        for n, e in errs.items():
+            assert e <= TOL["bf16"], (n, e)

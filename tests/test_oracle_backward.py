@@ -111,3 +111,29 @@ def test_all_softmax_is_causal_attention_through_the_norm():
     gq, gk, gv = torch.autograd.grad(y, [q, k, v], torch.tensor(dout))
     for name, ref in (("dq", gq), ("dk", gk), ("dv", gv)):
         np.testing.assert_allclose(res[name], ref.numpy(), rtol=1e-9, atol=1e-11, err_msg=name)
+
+
+def test_last_chunk_from_its_prefix_and_state():
+    # the gradients of the last chunk's tokens (dq, dk, dv, dg, dbeta) depend on
+    # the earlier tokens only through the retained keys / values before it and
+    # the Gated DeltaNet state at its start: the backward of the last chunk
+    # alone, given those as constants, equals the whole sequence's there
+    inp, sel, nws, nwl, b_g, dout = _case(306, L=256, d=16)
+    whole = ob.backward(sel=sel, dout=dout, **_args(inp, nws, nwl, b_g))
+    L0, d = 192, 16
+    state0 = oracle.forward(inp.q[:, :, :L0], inp.k[:, :, :L0], inp.v[:, :, :L0], inp.g[:, :, :L0],
+                            inp.beta[:, :, :L0], inp.w_s, inp.b_s, inp.w_g, b_g.astype(np.float32),
+                            sel_in=sel[:, :, :3], outputs=("state",))["state"].reshape(1, 2, d, d)
+    sl = slice(L0, 256)
+    n_prefix = set()
+    for h in range(2):
+        keep = np.flatnonzero(np.repeat(sel[0, h, :3] == 0, 64))  # retained tokens before the last chunk
+        n_prefix.add(len(keep))
+        one = lambda a: a[:, h:h + 1, sl]
+        local = ob.backward(one(inp.q), one(inp.k), one(inp.v), one(inp.g), one(inp.beta), inp.w_g[h:h + 1],
+                            b_g[h:h + 1], sel[:, h:h + 1, 3:], one(dout), norm_w_soft=nws, norm_w_lin=nwl,
+                            prefix_k=inp.k[:, h:h + 1, keep], prefix_v=inp.v[:, h:h + 1, keep],
+                            state0=state0[:, h:h + 1])
+        for n in ("dq", "dk", "dv", "dg", "dbeta"):
+            np.testing.assert_allclose(local[n], whole[n][:, h:h + 1, sl], rtol=1e-9, atol=1e-11, err_msg=n)
+    assert len(n_prefix) == 2  # the heads retain different prefixes
