@@ -139,16 +139,83 @@ def rooflines(work, stage_ms, pk):
 
 # --------------------------------------------------------------- clocks ----
 
+class _NvmlSampler:
+    """SM clock and clock-event reasons of one GPU, read through NVML (the
+    driver's management library, read-only queries) every `period` seconds
+    on a background thread: enough samples inside a timed region of tens of
+    milliseconds.  Raises OSError where NVML cannot be loaded."""
+
+    # clock-event reason bits (nvml.h)
+    BITS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+
+    def __init__(self, dev_index, period=0.002):
+        import threading
+
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        bus = None
+        try:
+            import torch
+
+            pr = torch.cuda.get_device_properties(dev_index)
+            bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+        except Exception:  # noqa: BLE001 (older torch: no PCI ids)
+            bus = None
+        rc = lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(self.h)) if bus else 1
+        if rc != 0 and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(dev_index), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle")
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint(0)
+        lib.nvmlDeviceGetMaxClockInfo(self.h, ctypes.c_int(1), ctypes.byref(mx))  # NVML_CLOCK_SM
+        self.max_mhz = float(mx.value)
+        self.rows = []
+        self.period = period
+        self.stop_ev = threading.Event()
+        self.th = threading.Thread(target=self._run, daemon=True)
+        self.th.start()
+
+    def _run(self):
+        mhz, bits = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        while not self.stop_ev.is_set():
+            if self.lib.nvmlDeviceGetClockInfo(self.h, ctypes.c_int(1), ctypes.byref(mhz)) == 0 and \
+                    self.reasons_fn(self.h, ctypes.byref(bits)) == 0:
+                self.rows.append((float(mhz.value), int(bits.value)))
+            time.sleep(self.period)
+
+    def stop(self):
+        self.stop_ev.set()
+        self.th.join(timeout=5)
+        self.lib.nvmlShutdown()
+        if not self.rows:
+            return None
+        reasons = sorted({name for _, b in self.rows for bit, name in self.BITS.items() if b & bit})
+        return {"sm_mhz": statistics.median(r[0] for r in self.rows), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.rows), "source": "nvml, every 2 ms"}
+
+
 class Clocks:
+    """Clock record of a timed region: NVML sampled on a thread where the
+    library loads, else nvidia-smi every 100 ms."""
+
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index, enabled=True):
         self.proc = None
+        self.nvml = None
         self.path = os.path.join("/tmp", f"nats_clocks_{os.getpid()}.csv")
         if not enabled:
             return
+        try:
+            self.nvml = _NvmlSampler(gpu_index)
+            return
+        except (OSError, AttributeError):
+            self.nvml = None
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
@@ -158,6 +225,8 @@ class Clocks:
             self.proc = None
 
     def stop(self):
+        if self.nvml is not None:
+            return self.nvml.stop()
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -181,7 +250,7 @@ class Clocks:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "source": "nvidia-smi, every 100 ms"}
 
 
 # ------------------------------------------------------------ traffic ----
