@@ -1,6 +1,8 @@
 /*
  * nats.h - C ABI of libnats, the NAtS-L token-level hybrid attention layer
- * forward (prefill) for NVIDIA GB300 (sm_103a).
+ * for NVIDIA GB300 (sm_103a): the forward (prefill), the same layer with its
+ * projections from x, a decode step on a caller-owned state, and the
+ * backward pass at the forward's selection.
  *
  * The operation ("Neural Attention Search Linear (NAtS-L)", technical
  * summary, section "Kernmechanismen"):
@@ -25,8 +27,11 @@
  *     N = L / 64.
  *   - Every data pointer is a DEVICE pointer owned by the caller; `dims` is
  *     a host pointer.  The library allocates no device memory, keeps no
- *     global state and never synchronises the host: all work is enqueued on
- *     `stream` (0 = the legacy default stream).
+ *     data between calls and never synchronises the host: all work is
+ *     enqueued on `stream` (0 = the legacy default stream).  The layer
+ *     forward runs its two branches concurrently on a second stream of the
+ *     library's (one stream and two events per device, created on first
+ *     use), forked from and joined back into `stream`.
  *   - Arguments are validated on the host before anything is launched; a
  *     violation returns its status and leaves every output untouched.
  *   - Launch failures return NATS_ERR_CUDA (from cudaGetLastError).  Errors
