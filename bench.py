@@ -38,6 +38,20 @@ WORKLOAD_DESC = ("NAtS-L layer forward, 1.3B-scale: B=4 H=16 L=8192 d_k=d_v=128 
 C = 64
 
 
+def set_workload(name):
+    """Another bf16 workload of the generator for the device-timed step."""
+    global WORKLOAD, WORKLOAD_DESC
+    import gen
+
+    cfg = gen.CONFIGS[name]
+    if cfg["dtype"] != "bf16":
+        raise SystemExit(f"--workload {name}: the timed step is the bf16 path")
+    WORKLOAD = name
+    WORKLOAD_DESC = (f"NAtS-L layer forward, workload {name}: B={cfg['B']} H={cfg['H']} L={cfg['L']} "
+                     f"d_k=d_v={cfg['d']} chunk=64, bf16 Q/K/V ~N(0,1) with unit keys, fp32 g/beta, "
+                     f"selection pattern {cfg['pattern']!r}")
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -50,6 +64,9 @@ def parse():
     ap.add_argument("--no-x-path", action="store_true", help="skip the layer-with-projections measurement")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass measurement")
+    ap.add_argument("--workload", default="l8192",
+                    help="layer workload of the device-timed step (default: the 8192-token one); others, e.g. "
+                         "'long' (1 x 32 x 65536, 12.5 %% softmax chunks), are extra data points")
     return ap.parse_args()
 
 
@@ -537,7 +554,8 @@ def run_native(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC, "global_batch": B * world, "seq_len": L,
                    "parallelism": f"replicas x{world} ((b,h) units per rank, no collective)",
-                   "l2": "inputs larger than L2: Q/K/V 384 MiB + workspace per step, no explicit flush",
+                   "l2": f"inputs larger than L2: Q/K/V {3 * B * H * L * d * 2 / 2**20:.0f} MiB + workspace per step, "
+                         "no explicit flush",
                    "softmax_fraction": work["softmax_fraction"]},
         "roofline": roofline,
         "kernel_rooflines": per_kernel,
@@ -779,6 +797,8 @@ def run_decode(args, rank, dev, stream, dist):
 
 def main():
     args = parse()
+    if args.workload != WORKLOAD:
+        set_workload(args.workload)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
