@@ -26,19 +26,26 @@
  *     beta are fp32 [B, H, L].  Selection codes are uint8 [B, H, N] with
  *     N = L / 64.
  *   - Every data pointer is a DEVICE pointer owned by the caller; `dims` is
- *     a host pointer.  The library allocates no device memory, keeps no
- *     data between calls and never synchronises the host: all work is
- *     enqueued on `stream` (0 = the legacy default stream).  The layer
- *     forward runs its two branches concurrently on a second stream of the
- *     library's (one stream and two events per device, created on first
- *     use), forked from and joined back into `stream`.
+ *     a host pointer.  The library keeps no data between calls and never
+ *     synchronises the host: all work is enqueued on `stream` (0 = the
+ *     legacy default stream).  It allocates no device memory per call; what
+ *     it does hold is listed here.  Per device, created on first use and
+ *     kept until the process exits: one side stream and two events (the
+ *     layer forward runs its two branches concurrently on that stream,
+ *     forked from and joined back into `stream`) and one cuBLAS handle (the
+ *     projections of nats_hybrid_fwd_x).  Per loaded library, on every GPU:
+ *     the fixed scratch array of nats_hybrid_fwd_noalloc.
  *   - Arguments are validated on the host before anything is launched; a
  *     violation returns its status and leaves every output untouched.
  *   - Launch failures return NATS_ERR_CUDA (from cudaGetLastError).  Errors
  *     that happen while the kernels run surface, as usual for CUDA, on the
  *     caller's next synchronising call.
- *   - No C++ exception crosses this interface.  Distinct calls are
- *     thread-safe (no shared state); calls that share a workspace must be
+ *   - No C++ exception crosses this interface.  Calls from several host
+ *     threads are safe: the per-device side stream, events and cuBLAS
+ *     handle are used under a lock.  Because all forward calls of a device
+ *     share the one side stream, the softmax halves of concurrent calls
+ *     made on different caller streams run one after the other on it
+ *     (correct, but not concurrent).  Calls that share a workspace must be
  *     ordered by the caller.
  *   - Supported shapes: chunk = 64, L % 64 == 0, dk == dv in {64, 128},
  *     B, H, L >= 0 (any zero extent makes the call a no-op that returns
@@ -154,7 +161,16 @@ nats_status nats_hybrid_fwd(const nats_dims* dims, const void* q, const void* k,
  *     contents; calls that can overlap on the GPU (different streams without
  *     ordering, or several host threads) race on it and must be serialised
  *     by the caller.  Nothing in it needs to start zeroed.
- * Other arguments, results and errors are those of nats_hybrid_fwd. */
+ *   - The device address found by the first call on a device is kept for
+ *     later calls.  cudaDeviceReset unloads the array with the rest of the
+ *     library's device code, so that address is stale after a reset: do not
+ *     use this entry point on a device the process has reset since its first
+ *     call there.
+ *   - A bounded internal wait that expired (outputs invalid) is reported by
+ *     nats_noalloc_check, the counterpart of nats_workspace_check for the
+ *     built-in scratch.
+ * Other arguments, results and errors are those of nats_hybrid_fwd, checked
+ * in the same order; the size limit is checked after them. */
 nats_status nats_hybrid_fwd_noalloc(const nats_dims* dims, const void* q, const void* k,
                                     const void* v, const float* g, const float* beta,
                                     const float* w_s, const float* b_s, const float* w_g,
@@ -162,6 +178,12 @@ nats_status nats_hybrid_fwd_noalloc(const nats_dims* dims, const void* q, const 
                                     const float* norm_w_lin, const uint8_t* sel_in, void* out,
                                     uint8_t* sel_out, float* state_out, float* o_soft_out,
                                     float* o_lin_out, nats_stream_t stream);
+
+/* nats_workspace_check for nats_hybrid_fwd_noalloc: synchronises `stream`,
+ * then reports NATS_ERR_INTERNAL if a kernel of the last allocation-free call
+ * on the current device (with these dims) gave up on a bounded internal wait,
+ * else NATS_OK.  NATS_ERR_WORKSPACE for dims beyond the built-in scratch. */
+nats_status nats_noalloc_check(const nats_dims* dims, nats_stream_t stream);
 
 /* Stages of nats_hybrid_fwd, for per-stage timing. */
 typedef enum {
@@ -259,7 +281,7 @@ nats_status nats_debug_bounded_wait(int32_t* flag, int64_t limit_ns, nats_stream
  * The same layer in decode mode: one new token per (b, h) per call, at
  * position t of the sequence.  "Neural Attention Search Linear (NAtS-L)",
  * technical summary, "Kernmechanismen" items 1, 3 and 4 read token by token
- * (the decode reading of the oracle README): the token joins its chunk's keys
+ * (the decode reading DEC-1): the token joins its chunk's keys
  * and values and attends to the retained ones (those of earlier softmax
  * chunks) plus its chunk up to itself; the Gated DeltaNet state takes the
  * token's update at once (the pseudo-update) and the readout uses it; when

@@ -24,7 +24,8 @@ STATUS = {
 
 # Every symbol include/nats.h declares.
 EXPORTS = ("nats_status_string", "nats_last_cuda_error", "nats_workspace_size", "nats_workspace_check", "nats_select",
-           "nats_hybrid_fwd", "nats_hybrid_fwd_profiled", "nats_hybrid_fwd_noalloc", "nats_x_workspace_size",
+           "nats_hybrid_fwd", "nats_hybrid_fwd_profiled", "nats_hybrid_fwd_noalloc", "nats_noalloc_check",
+           "nats_x_workspace_size",
            "nats_hybrid_fwd_x", "nats_debug_fail_stage", "nats_debug_bounded_wait", "nats_decode_step",
            "nats_bwd_workspace_size", "nats_hybrid_bwd")
 
@@ -86,6 +87,8 @@ def _load() -> ctypes.CDLL:
     lib.nats_hybrid_fwd_profiled.restype = ctypes.c_int
     lib.nats_hybrid_fwd_noalloc.argtypes = [ctypes.POINTER(Dims)] + [P] * 17 + [P]
     lib.nats_hybrid_fwd_noalloc.restype = ctypes.c_int
+    lib.nats_noalloc_check.argtypes = [ctypes.POINTER(Dims), P]
+    lib.nats_noalloc_check.restype = ctypes.c_int
     lib.nats_x_workspace_size.argtypes = [ctypes.POINTER(Dims), ctypes.c_int32]
     lib.nats_x_workspace_size.restype = ctypes.c_size_t
     lib.nats_hybrid_fwd_x.argtypes = [ctypes.POINTER(Dims), ctypes.c_int32] + [P] * 14 + [ctypes.c_size_t, P]

@@ -144,6 +144,26 @@ Side* side_of_current_device() {
 }
 
 }  // namespace
+
+// Argument checks of the layer forward other than the workspace (shared with
+// the allocation-free entry point, so both report the same error first).
+// *empty is set when a zero extent makes the call a no-op.
+nats_status check_fwd_args(const nats_dims* dims, const void* q, const void* k, const void* v, const float* g,
+                           const float* beta, const float* w_s, const float* w_g, const uint8_t* sel_in,
+                           const void* out, bool* empty) {
+  *empty = false;
+  nats_status s = check_dims(dims);
+  if (s != NATS_OK) return s;
+  if ((long long)dims->B * dims->H == 0 || dims->L == 0) {
+    *empty = true;
+    return NATS_OK;
+  }
+  if (!q || !k || !v || !g || !beta || !w_g || !out) return NATS_ERR_NULL;
+  if (!sel_in && !w_s) return NATS_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return NATS_ERR_ALIGN;
+  return NATS_OK;
+}
+
 }  // namespace nats
 
 using namespace nats;
@@ -216,18 +236,17 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
                                      uint8_t* sel_out, float* state_out, float* o_soft_out,
                                      float* o_lin_out, void* workspace, size_t workspace_bytes,
                                      nats_stream_t stream, nats_profile* prof) {
-  nats_status s = check_dims(dims);
+  bool empty = false;
+  nats_status s = check_fwd_args(dims, q, k, v, g, beta, w_s, w_g, sel_in, out, &empty);
   if (s != NATS_OK) return s;
   const Problem p = problem_of(dims);
   if (prof) {
     prof->launches = 0;
     for (int i = 0; i < NATS_NUM_STAGES; ++i) prof->stage_launches[i] = 0;
   }
-  if (p.BH == 0 || p.L == 0) return NATS_OK;
-  if (!q || !k || !v || !g || !beta || !w_g || !out || !workspace) return NATS_ERR_NULL;
-  if (!sel_in && !w_s) return NATS_ERR_NULL;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(workspace))
-    return NATS_ERR_ALIGN;
+  if (empty) return NATS_OK;
+  if (!workspace) return NATS_ERR_NULL;
+  if (!aligned16(workspace)) return NATS_ERR_ALIGN;
   Workspace ws;
   const size_t need = layout(p, (char*)workspace, &ws);
   if (workspace_bytes < need) return NATS_ERR_WORKSPACE;

@@ -14,10 +14,19 @@
 // process exits.  Host code cannot pass the array's name to a kernel (in host
 // code it names a host-side stand-in, not device memory), so the first call
 // on each device looks up its device address with cudaGetSymbolAddress, with
-// that device current, and remembers it.
+// that device current, and remembers it.  cudaDeviceReset unloads the
+// library's device code and with it the array, so the remembered address is
+// stale after a reset: the entry point is not for use on a device that the
+// process has reset since its first call there.
 #include <mutex>
 
 #include "../../include/nats.h"
+
+namespace nats {
+nats_status check_fwd_args(const nats_dims* dims, const void* q, const void* k, const void* v, const float* g,
+                           const float* beta, const float* w_s, const float* w_g, const uint8_t* sel_in,
+                           const void* out, bool* empty);
+}  // namespace nats
 
 namespace {
 
@@ -50,12 +59,11 @@ extern "C" nats_status nats_hybrid_fwd_noalloc(
     const float* w_s, const float* b_s, const float* w_g, const float* b_g, const float* norm_w_soft,
     const float* norm_w_lin, const uint8_t* sel_in, void* out, uint8_t* sel_out, float* state_out,
     float* o_soft_out, float* o_lin_out, nats_stream_t stream) {
-  const size_t need = nats_workspace_size(dims);
-  if (need == 0) {  // invalid dims: let the regular entry point name the error
-    return nats_hybrid_fwd(dims, q, k, v, g, beta, w_s, b_s, w_g, b_g, norm_w_soft, norm_w_lin, sel_in,
-                           out, sel_out, state_out, o_soft_out, o_lin_out, nullptr, 0, stream);
-  }
-  if (need > kNoAllocScratchBytes) return NATS_ERR_WORKSPACE;
+  // the checks of nats_hybrid_fwd, in its order, before the size limit
+  bool empty = false;
+  const nats_status s0 = nats::check_fwd_args(dims, q, k, v, g, beta, w_s, w_g, sel_in, out, &empty);
+  if (s0 != NATS_OK || empty) return s0;
+  if (nats_workspace_size(dims) > kNoAllocScratchBytes) return NATS_ERR_WORKSPACE;
   void* scratch = nullptr;
   const nats_status s = scratch_address(&scratch);
   if (s != NATS_OK) return s;
@@ -63,4 +71,12 @@ extern "C" nats_status nats_hybrid_fwd_noalloc(
   // of it before reading it (the error flag is cleared by the call itself).
   return nats_hybrid_fwd(dims, q, k, v, g, beta, w_s, b_s, w_g, b_g, norm_w_soft, norm_w_lin, sel_in, out,
                          sel_out, state_out, o_soft_out, o_lin_out, scratch, kNoAllocScratchBytes, stream);
+}
+
+extern "C" nats_status nats_noalloc_check(const nats_dims* dims, nats_stream_t stream) {
+  if (nats_workspace_size(dims) > kNoAllocScratchBytes) return NATS_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  const nats_status s = scratch_address(&scratch);
+  if (s != NATS_OK) return s;
+  return nats_workspace_check(dims, scratch, stream);
 }

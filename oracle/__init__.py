@@ -7,7 +7,8 @@ never does.  It wraps ``nats_oracle.cpp`` (plain C++17, float64, one thread per
 
 Every function follows "Neural Attention Search Linear (NAtS-L)", technical
 summary, section "Kernmechanismen", items 1, 3 and 4; the readings taken where
-the page is silent are listed in ``oracle/README.md``.
+the page is silent carry the names CONV-1 ... CONV-15, DEC-1 and BWD-1
+(each restated where it is used).
 """
 
 from __future__ import annotations
@@ -226,8 +227,8 @@ class Decoder:
     """The same layer in decode mode, one token per step, in float64.
 
     "Neural Attention Search Linear (NAtS-L)", technical summary,
-    "Kernmechanismen" items 1, 3 and 4, read token by token (the readings of
-    the prefill oracle hold, see ``oracle/README.md``, plus DEC-1 there):
+    "Kernmechanismen" items 1, 3 and 4, read token by token (the prefill
+    oracle's readings CONV-1 ... CONV-12 hold, plus the decode reading DEC-1):
 
     * every new token is appended to the keys / values of its chunk and sees
       the retained keys / values (those of earlier softmax chunks) plus its

@@ -23,7 +23,7 @@ W_g, b_g and the two RMSNorm weights, taken by torch.autograd through that
 forward.  The selection is the forward's argmax (item 1): a discrete choice
 with no derivative; the pages state that the score layer is trained end to
 end but give no estimator for it, so its gradient is not part of this
-backward (the reading BWD-1 of oracle/README.md).
+backward (the reading BWD-1).
 """
 
 from __future__ import annotations

@@ -21,7 +21,7 @@
 //   item 4 (output merging): both branch outputs are RMS-normalised
 //          separately and combined by a weighted sum whose weights come from
 //          the query projections.
-// Readings where the pages are silent (each restated in oracle/README.md):
+// Readings where the pages are silent (named CONV-n):
 //   CONV-1  Gated DeltaNet: S_t = a_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
 //           read out after the update: o_t = S_t (scale * q_t).
 //   CONV-2  score input: mean over the chunk's tokens of [q_t ; k_t] (unscaled q),

@@ -200,3 +200,28 @@ def test_debug_hook_validation(nat):
     assert nat.lib.nats_debug_bounded_wait(ctypes.c_void_p(256), 0, None) == 9  # NATS_ERR_VALUE
     assert nat.lib.nats_debug_bounded_wait(ctypes.c_void_p(256), 2 * 10**9, None) == 9
     nat.lib.nats_debug_fail_stage(-1)  # cancelling an injection is always allowed
+
+
+def test_noalloc_validation_order(nat):
+    """The allocation-free forward checks its arguments like nats_hybrid_fwd,
+    in the same order, and only then its fixed scratch limit; all of it on
+    the host, before any CUDA call."""
+    P = lambda a: ctypes.c_void_p(a)
+    good = [P(0x10000000)] * 5 + [P(0x10001000), None, P(0x10002000), None, None, None, None, P(0x10003000)]
+    tail = [None] * 5 + [None]
+
+    def call(dm, ptrs):
+        return nat.lib.nats_hybrid_fwd_noalloc(ctypes.byref(dm), *ptrs, *tail)
+
+    big = nat.dims(1, 16, 16384, 128)
+    assert nat.lib.nats_workspace_size(ctypes.byref(big)) > nat.NOALLOC_SCRATCH_BYTES
+    assert call(nat.dims(1, 1, 100, 64), good) == 2  # NATS_ERR_SHAPE
+    assert call(nat.dims(0, 4, 256, 64), good) == 0  # empty problem: no-op
+    no_out = list(good)
+    no_out[12] = None
+    assert call(big, no_out) == 1  # NATS_ERR_NULL comes before the size limit
+    odd = list(good)
+    odd[0] = P(0x10000008)
+    assert call(big, odd) == 4  # NATS_ERR_ALIGN comes before the size limit
+    assert call(big, good) == 5  # NATS_ERR_WORKSPACE
+    assert nat.lib.nats_noalloc_check(ctypes.byref(big), None) == 5

@@ -63,13 +63,32 @@ def test_no_alloc_matches_workspace_entry_on_two_calls(nat, dtype):
     for inp in cases:  # two calls in a row, different shapes and selections
         ref_out, ref_sel, ref_state = _run(nat, inp, no_alloc=False)
         out, sel, state = _run(nat, inp, no_alloc=True)
+        # the same kernels on the same inputs: the results agree bit for bit
         assert np.array_equal(sel, ref_sel)
+        assert np.array_equal(out, ref_out)
+        assert np.array_equal(state, ref_state)
         assert rel_err(out, ref_out) <= TOL[dtype]
-        assert rel_err(state, ref_state) <= TOL[dtype]
+        dm = nat.dims(inp.B, inp.H, inp.L, inp.d, nat.NATS_BF16 if dtype == "bf16" else nat.NATS_F32)
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        assert nat.lib.nats_noalloc_check(ctypes.byref(dm), stream) == 0  # no bounded wait expired
 
 
 def test_no_alloc_rejects_problems_beyond_its_scratch(nat):
-    dm = nat.dims(4, 16, 8192, 128)  # needs far more than the built-in scratch
+    B, H, L, d = 1, 16, 16384, 128  # needs more than the built-in scratch
+    dm = nat.dims(B, H, L, d)
     assert nat.lib.nats_workspace_size(ctypes.byref(dm)) > nat.NOALLOC_SCRATCH_BYTES
-    args = [ctypes.byref(dm)] + [ctypes.c_void_p(0x10000000)] * 10 + [None] * 7 + [None]
+    # valid device buffers for every input and the output: only the size is wrong
+    x = torch.zeros((B, H, L, d), dtype=torch.bfloat16, device="cuda")
+    out = torch.full_like(x, 7.0)
+    gb = torch.zeros((B, H, L), dtype=torch.float32, device="cuda")
+    w_s = torch.zeros((H, 2, 2 * d), dtype=torch.float32, device="cuda")
+    w_g = torch.zeros((H, d), dtype=torch.float32, device="cuda")
+    args = [ctypes.byref(dm), _ptr(x), _ptr(x), _ptr(x), _ptr(gb), _ptr(gb), _ptr(w_s), None, _ptr(w_g), None,
+            None, None, None, _ptr(out), None, None, None, None, None]
     assert nat.lib.nats_hybrid_fwd_noalloc(*args) == 5  # NATS_ERR_WORKSPACE, nothing launched
+    torch.cuda.synchronize()
+    assert bool((out.float() == 7.0).all())  # the output was not touched
+    assert nat.lib.nats_noalloc_check(ctypes.byref(dm), None) == 5
+    # the regular checks come first: a NULL output is reported as such
+    args[13] = None
+    assert nat.lib.nats_hybrid_fwd_noalloc(*args) == 1  # NATS_ERR_NULL
