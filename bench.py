@@ -616,34 +616,65 @@ def run_x_path(args, rank, dev, stream, dist):
     ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
     P = lambda v: ctypes.c_void_p(v.data_ptr())
 
-    def call():
-        code = _native.lib.nats_hybrid_fwd_x(
+    def call(prof=None):
+        code = _native.lib.nats_hybrid_fwd_x_profiled(
             ctypes.byref(dm), hidden, P(t["x"]), P(t["w_qkv"]), P(t["w_ab"]), P(t["b_a"]), P(t["a_scale"]),
             P(t["b_b"]), P(t["w_s"]), P(t["b_s"]), P(t["w_g"]), P(t["b_g"]), P(t["w_o"]), P(y), None, P(ws),
-            ctypes.c_size_t(wsb), ctypes.c_void_p(stream.cuda_stream))
+            ctypes.c_size_t(wsb), ctypes.c_void_p(stream.cuda_stream),
+            ctypes.byref(prof) if prof is not None else None)
         if code != 0:
-            raise _native.NatsError(code, "nats_hybrid_fwd_x")
+            raise _native.NatsError(code, "nats_hybrid_fwd_x_profiled")
 
     for _ in range(max(args.warmup, 1)):
         call()
     torch.cuda.synchronize()
+    # per-stage events of every timed step (the two projection GEMMs among them)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in _native.STAGES] for _ in range(args.steps)]
+    profs = []
+    for row in ev:
+        p = _native.Profile()
+        for i, (a0, a1) in enumerate(row):
+            a0.record(stream)
+            a1.record(stream)
+            p.start[i] = a0.cuda_event
+            p.stop[i] = a1.cuda_event
+        profs.append(p)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     e0.record(stream)
-    for _ in range(args.steps):
-        call()
+    for i in range(args.steps):
+        call(profs[i])
     e1.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
     world = dist.get_world_size() if dist is not None else 1
-    gemm_flops = 2.0 * B * L * hidden * (3 * H * d + 2 * H) + 2.0 * B * L * H * d * hidden
-    return {"what": "nats_hybrid_fwd_x: x -> [q|k|v], [a|b] (cuBLAS GEMMs), head split + key norm + gates, "
-                    "the layer, output projection (cuBLAS)",
+    stage_ms = {}
+    for si, name in enumerate(_native.STAGES):
+        if profs[0].stage_launches[si] == 0:
+            continue
+        vals = [row[si][0].elapsed_time(row[si][1]) for row in ev]
+        stage_ms[name] = sum(vals) / len(vals)
+    f_in = 2.0 * B * L * hidden * (3 * H * d + 2 * H)
+    f_out = 2.0 * B * L * H * d * hidden
+    pk = peaks()
+    peak = pk["bf16_tflops_sustained"]
+    gemms = {}
+    for name, fl in (("proj_in", f_in), ("proj_out", f_out)):
+        if name in stage_ms:
+            ach = fl / (stage_ms[name] / 1e3) / 1e12
+            gemms[name] = {"kernel": "gemm_tc_kernel", "bound": "tensor", "achieved": ach, "peak": peak,
+                           "unit": "TFLOP/s", "frac": ach / peak, "peak_source": "measured bf16 sustained",
+                           "ms_per_launch": stage_ms[name], "flops_per_launch": fl}
+    dom = max(gemms, key=lambda k: gemms[k]["ms_per_launch"]) if gemms else None
+    return {"what": "nats_hybrid_fwd_x: x -> q, k, v, g, beta (tcgen05 GEMM, head split + key norm + gates in "
+                    "its epilogue), the layer, output projection (the same GEMM kernel)",
             "config": {"B": B, "H": H, "L": L, "d": d, "hidden": hidden},
             "value": job_throughput(B * L, world, ms), "unit": "tokens/s", "ms_per_step": ms,
-            "projection_gemm_flops_per_step": gemm_flops}
+            "stages_ms": stage_ms, "projection_gemm_flops_per_step": f_in + f_out,
+            "roofline": gemms.get(dom), "gemm_rooflines": gemms}
 
 
 def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):

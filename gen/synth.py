@@ -319,6 +319,13 @@ def make_x_inputs(B: int, H: int, L: int, d: int, hidden: int, seed: int = 0, na
 X_CONFIGS = {
     "x_tiny": dict(B=1, H=2, L=256, d=64, hidden=128, seed=11),
     "x_small": dict(B=2, H=4, L=1024, d=128, hidden=512, seed=12),
+    # the 1.3B-scale projections (hidden = H d = 2048, the bench's GEMM
+    # shapes but for the number of tokens)
+    "x_mid": dict(B=1, H=16, L=512, d=128, hidden=2048, seed=14),
+    # ragged tiles of the projection GEMMs: 192 tokens (1.5 row tiles), 3 heads
+    # of 64 (a column tile across two thirds, 6 gate columns), hidden 200
+    # (a partial K block and a partial output tile)
+    "x_ragged": dict(B=1, H=3, L=192, d=64, hidden=200, seed=15),
     # the 1.3B-scale layer of the main workload (hidden = H d = 2048)
     "x_l8192": dict(B=4, H=16, L=8192, d=128, hidden=2048, seed=13),
 }

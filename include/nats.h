@@ -32,17 +32,16 @@
  *     it does hold is listed here.  Per device, created on first use and
  *     kept until the process exits: one side stream and two events (the
  *     layer forward runs its two branches concurrently on that stream,
- *     forked from and joined back into `stream`) and one cuBLAS handle (the
- *     projections of nats_hybrid_fwd_x).  Per loaded library, on every GPU:
- *     the fixed scratch array of nats_hybrid_fwd_noalloc.
+ *     forked from and joined back into `stream`).  Per loaded library, on
+ *     every GPU: the fixed scratch array of nats_hybrid_fwd_noalloc.
  *   - Arguments are validated on the host before anything is launched; a
  *     violation returns its status and leaves every output untouched.
  *   - Launch failures return NATS_ERR_CUDA (from cudaGetLastError).  Errors
  *     that happen while the kernels run surface, as usual for CUDA, on the
  *     caller's next synchronising call.
  *   - No C++ exception crosses this interface.  Calls from several host
- *     threads are safe: the per-device side stream, events and cuBLAS
- *     handle are used under a lock.  Because all forward calls of a device
+ *     threads are safe: the per-device side stream and events are used
+ *     under a lock.  Because all forward calls of a device
  *     share the one side stream, the softmax halves of concurrent calls
  *     made on different caller streams run one after the other on it
  *     (correct, but not concurrent).  Calls that share a workspace must be
@@ -193,6 +192,8 @@ typedef enum {
   NATS_STAGE_GDN_PREP = 3, /* Gated DeltaNet per-chunk factors (parallel over chunks) */
   NATS_STAGE_GDN_SCAN = 4, /* Gated DeltaNet chunk scan with commit / rollback */
   NATS_STAGE_MERGE = 5,    /* RMSNorm per branch + gated merge */
+  NATS_STAGE_PROJ_IN = 6,  /* nats_hybrid_fwd_x: x -> q, k, v, g, beta */
+  NATS_STAGE_PROJ_OUT = 7, /* nats_hybrid_fwd_x: output projection */
   NATS_NUM_STAGES = 8
 } nats_stage;
 
@@ -239,8 +240,10 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
  *   beta_t,h = sigmoid(b_t,h + b_b[h]);
  *   o = the layer (nats_hybrid_fwd with w_s, b_s, w_g, b_g), bf16;
  *   y_t = bf16(sum_h o_t,h W_o[h d .. h d + d - 1, :]).
- * The three products are plain GEMMs (cuBLAS, fp32 accumulate); the
- * head split, the key normalisation and the gates are one kernel.
+ * The products run on the library's own tcgen05 GEMM (bf16 operands, fp32
+ * accumulate): the first one's epilogue writes q, k (normalised), v in the
+ * layer's layout and forms g and beta; the second reads the layer output in
+ * its [B, H, L, d] layout.
  *   hidden       width of x and y (multiple of 8)
  *   x            [B, L, hidden] bf16
  *   w_qkv        [hidden, 3 H d] bf16, row-major
@@ -252,15 +255,27 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
  *   y            [B, L, hidden] bf16 (output)
  *   sel_out      [B, H, N] u8 or NULL: the chunk selection
  *   workspace    device scratch of at least nats_x_workspace_size(dims, hidden)
- * Errors as nats_hybrid_fwd; NATS_ERR_SHAPE if hidden <= 0 or hidden % 8,
- * NATS_ERR_CUDA if a cuBLAS call fails.  The library keeps one cuBLAS handle
- * per device, created on first use; calls are serialised around it. */
+ * Errors as nats_hybrid_fwd; NATS_ERR_SHAPE if hidden <= 0 or hidden % 8;
+ * NATS_ERR_UNSUPPORTED if B L or 3 H d exceed int32 tiling.
+ * nats_x_workspace_check synchronises `stream` and reports NATS_ERR_INTERNAL
+ * if a kernel of the last call that used `workspace` gave up on a bounded
+ * internal wait (its outputs are then invalid), else NATS_OK. */
 size_t nats_x_workspace_size(const nats_dims* dims, int32_t hidden);
 nats_status nats_hybrid_fwd_x(const nats_dims* dims, int32_t hidden, const void* x, const void* w_qkv,
                               const void* w_ab, const float* b_a, const float* a_scale, const float* b_b,
                               const float* w_s, const float* b_s, const float* w_g, const float* b_g,
                               const void* w_o, void* y, uint8_t* sel_out, void* workspace,
                               size_t workspace_bytes, nats_stream_t stream);
+nats_status nats_x_workspace_check(const nats_dims* dims, int32_t hidden, const void* workspace,
+                                   nats_stream_t stream);
+/* nats_hybrid_fwd_x plus per-stage event records (the layer's stages and
+ * NATS_STAGE_PROJ_IN / NATS_STAGE_PROJ_OUT, all on `stream` but the softmax
+ * stage); prof may be NULL.  Same arguments, errors and results. */
+nats_status nats_hybrid_fwd_x_profiled(const nats_dims* dims, int32_t hidden, const void* x, const void* w_qkv,
+                                       const void* w_ab, const float* b_a, const float* a_scale, const float* b_b,
+                                       const float* w_s, const float* b_s, const float* w_g, const float* b_g,
+                                       const void* w_o, void* y, uint8_t* sel_out, void* workspace,
+                                       size_t workspace_bytes, nats_stream_t stream, nats_profile* prof);
 
 /* --------------------------------------------------------------- test hooks
  * Failure injection without a GPU fault.

@@ -141,13 +141,14 @@ def hybrid_fwd(q, k, v, g, beta, w_s, b_s, w_g, b_g=None, *, norm_w_soft=None, n
 
 
 def hybrid_fwd_x(x, w_qkv, w_ab, w_s, b_s, w_g, b_g=None, *, heads: int, b_a=None, a_scale=None, b_b=None,
-                 w_o, y=None, workspace=None, return_sel: bool = False, stream=None):
+                 w_o, y=None, workspace=None, return_sel: bool = False, check_errors: bool = False, stream=None):
     """The layer with its projections: x [B, L, hidden] bf16 -> y [B, L, hidden] bf16.
 
     w_qkv: bf16 [hidden, 3 H d]; w_ab: bf16 [hidden, 2 H]; b_a, a_scale, b_b:
     fp32 [H] or None; w_s, b_s, w_g, b_g as for hybrid_fwd; w_o: bf16
     [H d, hidden].  The definitions are those of nats_hybrid_fwd_x in
-    include/nats.h.  Returns y, or {"y": y, "sel": sel} with return_sel."""
+    include/nats.h.  Returns y, or {"y": y, "sel": sel} with return_sel.
+    check_errors synchronises and raises if a bounded device wait expired."""
     _req(x, "x", torch.bfloat16)
     B, L, hidden = x.shape
     H = int(heads)
@@ -174,6 +175,9 @@ def hybrid_fwd_x(x, w_qkv, w_ab, w_s, b_s, w_g, b_g=None, *, heads: int, b_a=Non
         ctypes.byref(dm), hidden, _p(x), _p(w_qkv), _p(w_ab), _p(b_a), _p(a_scale), _p(b_b), _p(w_s), _p(b_s),
         _p(w_g), _p(b_g), _p(w_o), _p(y), _p(sel), _p(workspace), ctypes.c_size_t(workspace.numel()),
         _stream(stream)), "nats_hybrid_fwd_x")
+    if check_errors:
+        check(_native.lib.nats_x_workspace_check(ctypes.byref(dm), hidden, _p(workspace), _stream(stream)),
+              "nats_x_workspace_check")
     return {"y": y, "sel": sel} if return_sel else y
 
 

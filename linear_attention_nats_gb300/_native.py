@@ -25,14 +25,15 @@ STATUS = {
 # Every symbol include/nats.h declares.
 EXPORTS = ("nats_status_string", "nats_last_cuda_error", "nats_workspace_size", "nats_workspace_check", "nats_select",
            "nats_hybrid_fwd", "nats_hybrid_fwd_profiled", "nats_hybrid_fwd_noalloc", "nats_noalloc_check",
-           "nats_x_workspace_size",
+           "nats_x_workspace_size", "nats_x_workspace_check",
+           "nats_hybrid_fwd_x_profiled",
            "nats_hybrid_fwd_x", "nats_debug_fail_stage", "nats_debug_bounded_wait", "nats_decode_step",
            "nats_bwd_workspace_size", "nats_hybrid_bwd")
 
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 NUM_STAGES = 8
-STAGES = ("score", "compact", "softmax", "gdn_prep", "gdn_scan", "merge")
+STAGES = ("score", "compact", "softmax", "gdn_prep", "gdn_scan", "merge", "proj_in", "proj_out")
 
 
 class Profile(ctypes.Structure):
@@ -93,6 +94,11 @@ def _load() -> ctypes.CDLL:
     lib.nats_x_workspace_size.restype = ctypes.c_size_t
     lib.nats_hybrid_fwd_x.argtypes = [ctypes.POINTER(Dims), ctypes.c_int32] + [P] * 14 + [ctypes.c_size_t, P]
     lib.nats_hybrid_fwd_x.restype = ctypes.c_int
+    lib.nats_hybrid_fwd_x_profiled.argtypes = [ctypes.POINTER(Dims), ctypes.c_int32] + [P] * 14 + [
+        ctypes.c_size_t, P, ctypes.POINTER(Profile)]
+    lib.nats_hybrid_fwd_x_profiled.restype = ctypes.c_int
+    lib.nats_x_workspace_check.argtypes = [ctypes.POINTER(Dims), ctypes.c_int32, P, P]
+    lib.nats_x_workspace_check.restype = ctypes.c_int
     lib.nats_debug_fail_stage.argtypes = [ctypes.c_int32]
     lib.nats_debug_fail_stage.restype = None
     lib.nats_debug_bounded_wait.argtypes = [P, ctypes.c_int64, P]

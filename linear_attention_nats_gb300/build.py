@@ -86,7 +86,7 @@ def _build_locked(verbose, extra_flags) -> str:
     with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         list(ex.map(compile_one, zip(srcs, objs)))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcublas"]
+    cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

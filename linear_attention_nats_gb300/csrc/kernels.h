@@ -74,6 +74,19 @@ cudaError_t launch_softmax_bwd_mma(const Problem& p, const void* q, const void* 
                                    const float* delta, const uint8_t* sel, float* lse, float* dq, float* dk,
                                    float* dv, cudaStream_t st);
 
+// The projections around the layer on tcgen05 (gemm_tc.cu).  QKV: x W_qkv
+// into the layer's q, k (normalised per head), v [B, H, L, d] and x W_ab into
+// g, beta [B, H, L]; w_ab_pad is scratch of proj_gate_pad_bytes(H, hidden).
+// Out: y = o_flat W_o, o read from its [B, H, L, d] layout.  err[0] is set if
+// a bounded wait expires.
+size_t proj_gate_pad_bytes(int H, int hidden);
+cudaError_t launch_proj_qkv_tc(int B, int H, int L, int d, int hidden, const void* x, const void* w_qkv,
+                               const void* w_ab, void* w_ab_pad, const float* b_a, const float* a_scale,
+                               const float* b_b, void* q, void* k, void* v, float* g, float* beta, int* err,
+                               cudaStream_t st);
+cudaError_t launch_proj_out_tc(int B, int H, int L, int d, int hidden, const void* o, const void* w_o, void* y,
+                               int* err, cudaStream_t st);
+
 // Test hook: one bounded wait that runs out after limit_ns and sets *flag.
 cudaError_t launch_bounded_wait(int* flag, long long limit_ns, cudaStream_t st);
 

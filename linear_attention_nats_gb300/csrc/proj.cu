@@ -1,5 +1,7 @@
-// proj.cu - the projections around the layer: x -> Q, K, V, g, beta (two
-// GEMMs and one split kernel), the layer forward, and the output projection.
+// proj.cu - the layer with its projections: x -> Q, K, V, g, beta (one
+// tcgen05 GEMM whose epilogue splits the heads, normalises the keys and
+// forms the gates), the layer forward, and the output projection (the same
+// GEMM kernel, reading the layer output in its [B, H, L, d] layout).
 //
 // "Neural Attention Search Linear (NAtS-L)", technical summary,
 // "Kernmechanismen" item 4 (the merge weights come from projections of the
@@ -8,16 +10,12 @@
 //   [q | k' | v] = bf16(x W_qkv), k = bf16(k' / |k'|) per head,
 //   [a | b] = x W_ab, g = -a_scale softplus(a + b_a), beta = sigmoid(b + b_b),
 //   y = bf16(o_flat W_o), o_flat[t] = [o_t,0 | o_t,1 | ...] (heads side by side).
-// The GEMMs are cuBLAS (plain dense products, fp32 accumulate); the rest is
-// two memory-bound kernels of this file.
-#include <cublas_v2.h>
-
 #include <cmath>
 #include <cstdint>
-#include <mutex>
 
 #include "../../include/nats.h"
 #include "common.cuh"
+#include "kernels.h"
 
 namespace nats {
 namespace {
@@ -26,19 +24,17 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct XWorkspace {
-  __nv_bfloat16* qkv;  // [B L, 3 H d] GEMM output; reused as o_flat [B L, H d]
-  float* ab;           // [B L, 2 H]
   __nv_bfloat16 *q, *k, *v;  // [B, H, L, d]
   float *g, *beta;           // [B, H, L]
   __nv_bfloat16* o;          // [B, H, L, d] layer output
+  void* w_ab_pad;            // [hidden, 2H rounded up to 64] bf16
+  int* err;                  // [0] set by a projection GEMM whose bounded wait expired
   void* layer;               // nats_hybrid_fwd workspace
   size_t layer_bytes;
 };
 
 size_t x_layout(const nats_dims* d, int hidden, char* base, XWorkspace* w) {
-  (void)hidden;
-  const size_t BL = (size_t)d->B * d->L, H = (size_t)d->H, D = (size_t)d->dk;
-  const size_t BHL = (size_t)d->B * d->H * d->L;
+  const size_t BHL = (size_t)d->B * d->H * d->L, D = (size_t)d->dk;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     char* p = base ? base + off : nullptr;
@@ -46,110 +42,18 @@ size_t x_layout(const nats_dims* d, int hidden, char* base, XWorkspace* w) {
     return p;
   };
   XWorkspace x;
-  x.qkv = (__nv_bfloat16*)take(BL * 3 * H * D * 2);
-  x.ab = (float*)take(BL * 2 * H * 4);
   x.q = (__nv_bfloat16*)take(BHL * D * 2);
   x.k = (__nv_bfloat16*)take(BHL * D * 2);
   x.v = (__nv_bfloat16*)take(BHL * D * 2);
   x.g = (float*)take(BHL * 4);
   x.beta = (float*)take(BHL * 4);
   x.o = (__nv_bfloat16*)take(BHL * D * 2);
+  x.w_ab_pad = take(proj_gate_pad_bytes(d->H, hidden));
+  x.err = (int*)take(16);
   x.layer_bytes = nats_workspace_size(d);
   x.layer = take(x.layer_bytes);
   if (w) *w = x;
   return off;
-}
-
-// One warp per (token, head): splits the projected row into q, k, v in the
-// layer's [B, H, L, d] layout, normalises k, and forms g and beta.
-template <int D>
-__global__ void __launch_bounds__(256) proj_split_kernel(const __nv_bfloat16* __restrict__ qkv,
-                                                         const float* __restrict__ ab, int B, int H, int L,
-                                                         const float* __restrict__ b_a,
-                                                         const float* __restrict__ a_scale,
-                                                         const float* __restrict__ b_b,
-                                                         __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ k,
-                                                         __nv_bfloat16* __restrict__ v, float* __restrict__ g,
-                                                         float* __restrict__ beta) {
-  constexpr int E = D / 32;  // elements per lane
-  const long long item = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);  // (row, h), h fastest
-  const long long rows = (long long)B * L;
-  if (item >= rows * H) return;
-  const int lane = threadIdx.x & 31;
-  const int h = (int)(item % H);
-  const long long row = item / H;  // b L + l
-  const long long b = row / L, l = row - b * L;
-  const size_t src = (size_t)row * 3 * H * D + (size_t)h * D + E * lane;
-  const size_t dst = (((size_t)b * H + h) * L + l) * D + E * lane;
-  float kf[E], ss = 0.f;
-#pragma unroll
-  for (int i = 0; i < E; ++i) {
-    q[dst + i] = qkv[src + i];
-    v[dst + i] = qkv[src + 2 * (size_t)H * D + i];
-    kf[i] = __bfloat162float(qkv[src + (size_t)H * D + i]);
-    ss = fmaf(kf[i], kf[i], ss);
-  }
-  ss = warp_sum(ss);
-  const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
-#pragma unroll
-  for (int i = 0; i < E; ++i) k[dst + i] = __float2bfloat16_rn(kf[i] * inv);
-  if (lane == 0) {
-    const float a = ab[(size_t)row * 2 * H + h] + (b_a ? b_a[h] : 0.f);
-    const float bb = ab[(size_t)row * 2 * H + H + h] + (b_b ? b_b[h] : 0.f);
-    const float sp = a > 20.f ? a : log1pf(__expf(a));  // softplus
-    const size_t gi = ((size_t)b * H + h) * L + l;
-    g[gi] = -(a_scale ? a_scale[h] : 1.f) * sp;
-    beta[gi] = 1.f / (1.f + __expf(-bb));
-  }
-}
-
-// o [B, H, L, d] -> o_flat [B L, H d] (heads side by side), one warp per row
-// of d elements
-template <int D>
-__global__ void __launch_bounds__(256) heads_to_rows_kernel(const __nv_bfloat16* __restrict__ o, int B, int H,
-                                                            int L, __nv_bfloat16* __restrict__ of) {
-  constexpr int E = D / 32;
-  const long long item = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);  // (b, l, h), h fastest
-  if (item >= (long long)B * L * H) return;
-  const int lane = threadIdx.x & 31;
-  const int h = (int)(item % H);
-  const long long row = item / H;
-  const long long b = row / L, l = row - b * L;
-  const size_t src = (((size_t)b * H + h) * L + l) * D + E * lane;
-  const size_t dst = (size_t)row * H * D + (size_t)h * D + E * lane;
-#pragma unroll
-  for (int i = 0; i < E; ++i) of[dst + i] = o[src + i];
-}
-
-// One cuBLAS handle per device; the enqueue of a call's GEMMs holds the
-// device's lock (the handle's stream is per-handle state).
-struct Blas {
-  std::mutex mu;
-  bool tried = false;
-  cublasHandle_t h = nullptr;
-};
-
-Blas* blas_of_current_device() {
-  static std::mutex mu;
-  static Blas all[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lk(mu);
-  Blas& b = all[dev];
-  if (!b.tried) {
-    b.tried = true;
-    if (cublasCreate(&b.h) != CUBLAS_STATUS_SUCCESS) b.h = nullptr;
-  }
-  return b.h ? &b : nullptr;
-}
-
-// Row-major C[M, N] = A[M, K] B[K, N] (bf16 operands, fp32 accumulate), as
-// the column-major product C^T = B^T A^T.
-bool gemm_rm(cublasHandle_t hdl, int M, int N, int K, const void* A, const void* B, void* C,
-             cudaDataType_t ctype) {
-  const float one = 1.f, zero = 0.f;
-  return cublasGemmEx(hdl, CUBLAS_OP_N, CUBLAS_OP_N, N, M, K, &one, B, CUDA_R_16BF, N, A, CUDA_R_16BF, K, &zero,
-                      C, ctype, N, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS;
 }
 
 }  // namespace
@@ -165,11 +69,27 @@ size_t nats_x_workspace_size(const nats_dims* dims, int32_t hidden) {
   return x_layout(dims, hidden, nullptr, nullptr);
 }
 
-nats_status nats_hybrid_fwd_x(const nats_dims* dims, int32_t hidden, const void* x, const void* w_qkv,
-                              const void* w_ab, const float* b_a, const float* a_scale, const float* b_b,
-                              const float* w_s, const float* b_s, const float* w_g, const float* b_g,
-                              const void* w_o, void* y, uint8_t* sel_out, void* workspace,
-                              size_t workspace_bytes, nats_stream_t stream) {
+nats_status nats_x_workspace_check(const nats_dims* dims, int32_t hidden, const void* workspace,
+                                   nats_stream_t stream) {
+  if (nats_x_workspace_size(dims, hidden) == 0) return dims ? NATS_ERR_SHAPE : NATS_ERR_NULL;
+  if ((long long)dims->B * dims->H * dims->L == 0) return NATS_OK;
+  if (!workspace) return NATS_ERR_NULL;
+  XWorkspace xw;
+  x_layout(dims, hidden, (char*)workspace, &xw);
+  int flag = 0;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&flag, xw.err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return NATS_ERR_CUDA;
+  if (flag) return NATS_ERR_INTERNAL;
+  return nats_workspace_check(dims, xw.layer, stream);
+}
+
+nats_status nats_hybrid_fwd_x_profiled(const nats_dims* dims, int32_t hidden, const void* x, const void* w_qkv,
+                                       const void* w_ab, const float* b_a, const float* a_scale, const float* b_b,
+                                       const float* w_s, const float* b_s, const float* w_g, const float* b_g,
+                                       const void* w_o, void* y, uint8_t* sel_out, void* workspace,
+                                       size_t workspace_bytes, nats_stream_t stream, nats_profile* prof) {
   if (!dims) return NATS_ERR_NULL;
   if (dims->dtype != NATS_BF16) return NATS_ERR_DTYPE;
   if (hidden <= 0 || hidden % 8 != 0) return NATS_ERR_SHAPE;
@@ -183,42 +103,46 @@ nats_status nats_hybrid_fwd_x(const nats_dims* dims, int32_t hidden, const void*
   if (!x || !w_qkv || !w_ab || !w_s || !w_g || !w_o || !y || !workspace) return NATS_ERR_NULL;
   if (((uintptr_t)x | (uintptr_t)w_qkv | (uintptr_t)w_ab | (uintptr_t)w_o | (uintptr_t)y | (uintptr_t)workspace) & 15)
     return NATS_ERR_ALIGN;
+  // every flat offset of the projections fits int32 tiling
+  if ((long long)dims->B * dims->L > (1LL << 31) - 1 - 128 ||
+      3LL * dims->H * dims->dk > (1LL << 31) - 1)
+    return NATS_ERR_UNSUPPORTED;
   XWorkspace xw;
   if (workspace_bytes < x_layout(dims, hidden, (char*)workspace, &xw)) return NATS_ERR_WORKSPACE;
   const int B = dims->B, H = dims->H, L = dims->L, D = dims->dk;
-  const int BL = B * L, HD = H * D;
   cudaStream_t st = (cudaStream_t)stream;
-  Blas* bl = blas_of_current_device();
-  if (!bl) return NATS_ERR_CUDA;
-  {
-    std::lock_guard<std::mutex> lk(bl->mu);
-    if (cublasSetStream(bl->h, st) != CUBLAS_STATUS_SUCCESS) return NATS_ERR_CUDA;
-    if (!gemm_rm(bl->h, BL, 3 * HD, hidden, x, w_qkv, xw.qkv, CUDA_R_16BF)) return NATS_ERR_CUDA;
-    if (!gemm_rm(bl->h, BL, 2 * H, hidden, x, w_ab, xw.ab, CUDA_R_32F)) return NATS_ERR_CUDA;
-  }
-  const long long items = (long long)BL * H;
-  const unsigned blocks = (unsigned)((items + 7) / 8);
-  if (D == 64)
-    proj_split_kernel<64><<<blocks, 256, 0, st>>>(xw.qkv, xw.ab, B, H, L, b_a, a_scale, b_b, xw.q, xw.k, xw.v, xw.g,
-                                                  xw.beta);
-  else
-    proj_split_kernel<128><<<blocks, 256, 0, st>>>(xw.qkv, xw.ab, B, H, L, b_a, a_scale, b_b, xw.q, xw.k, xw.v,
-                                                   xw.g, xw.beta);
-  if (cudaGetLastError() != cudaSuccess) return NATS_ERR_CUDA;
-  const nats_status s = nats_hybrid_fwd(dims, xw.q, xw.k, xw.v, xw.g, xw.beta, w_s, b_s, w_g, b_g, nullptr, nullptr,
-                                        nullptr, xw.o, sel_out, nullptr, nullptr, nullptr, xw.layer, xw.layer_bytes,
-                                        stream);
+  auto mark = [&](void* const* ev, int s) -> bool {
+    return !prof || !ev[s] || cudaEventRecord((cudaEvent_t)ev[s], st) == cudaSuccess;
+  };
+  if (cudaMemsetAsync(xw.err, 0, sizeof(int), st) != cudaSuccess) return NATS_ERR_CUDA;
+  if (!mark(prof ? prof->start : nullptr, NATS_STAGE_PROJ_IN)) return NATS_ERR_CUDA;
+  if (launch_proj_qkv_tc(B, H, L, D, hidden, x, w_qkv, w_ab, xw.w_ab_pad, b_a, a_scale, b_b, xw.q, xw.k, xw.v,
+                         xw.g, xw.beta, xw.err, st) != cudaSuccess)
+    return NATS_ERR_CUDA;
+  if (!mark(prof ? prof->stop : nullptr, NATS_STAGE_PROJ_IN)) return NATS_ERR_CUDA;
+  // the layer fills the profile's other stages (and resets its counts)
+  const nats_status s = nats_hybrid_fwd_profiled(dims, xw.q, xw.k, xw.v, xw.g, xw.beta, w_s, b_s, w_g, b_g, nullptr,
+                                                 nullptr, nullptr, xw.o, sel_out, nullptr, nullptr, nullptr, xw.layer,
+                                                 xw.layer_bytes, stream, prof);
   if (s != NATS_OK) return s;
-  __nv_bfloat16* of = xw.qkv;  // the projected rows are dead by now
-  if (D == 64)
-    heads_to_rows_kernel<64><<<blocks, 256, 0, st>>>(xw.o, B, H, L, of);
-  else
-    heads_to_rows_kernel<128><<<blocks, 256, 0, st>>>(xw.o, B, H, L, of);
-  if (cudaGetLastError() != cudaSuccess) return NATS_ERR_CUDA;
-  std::lock_guard<std::mutex> lk(bl->mu);
-  if (cublasSetStream(bl->h, st) != CUBLAS_STATUS_SUCCESS) return NATS_ERR_CUDA;
-  if (!gemm_rm(bl->h, BL, hidden, HD, of, w_o, y, CUDA_R_16BF)) return NATS_ERR_CUDA;
+  if (!mark(prof ? prof->start : nullptr, NATS_STAGE_PROJ_OUT)) return NATS_ERR_CUDA;
+  if (launch_proj_out_tc(B, H, L, D, hidden, xw.o, w_o, y, xw.err, st) != cudaSuccess) return NATS_ERR_CUDA;
+  if (!mark(prof ? prof->stop : nullptr, NATS_STAGE_PROJ_OUT)) return NATS_ERR_CUDA;
+  if (prof) {
+    prof->launches += 3;  // gate-weight copy, the two GEMMs
+    prof->stage_launches[NATS_STAGE_PROJ_IN] = 2;
+    prof->stage_launches[NATS_STAGE_PROJ_OUT] = 1;
+  }
   return NATS_OK;
+}
+
+nats_status nats_hybrid_fwd_x(const nats_dims* dims, int32_t hidden, const void* x, const void* w_qkv,
+                              const void* w_ab, const float* b_a, const float* a_scale, const float* b_b,
+                              const float* w_s, const float* b_s, const float* w_g, const float* b_g,
+                              const void* w_o, void* y, uint8_t* sel_out, void* workspace,
+                              size_t workspace_bytes, nats_stream_t stream) {
+  return nats_hybrid_fwd_x_profiled(dims, hidden, x, w_qkv, w_ab, b_a, a_scale, b_b, w_s, b_s, w_g, b_g, w_o, y,
+                                    sel_out, workspace, workspace_bytes, stream, nullptr);
 }
 
 }  // extern "C"
