@@ -17,4 +17,8 @@ from .synth import (  # noqa: F401
     X_CONFIGS,
     make_x_inputs,
     x_config_inputs,
+    NhaInputs,
+    NHA_CONFIGS,
+    make_nha_inputs,
+    nha_config_inputs,
 )

@@ -334,3 +334,60 @@ X_CONFIGS = {
 def x_config_inputs(name: str) -> NatsXInputs:
     cfg = dict(X_CONFIGS[name])
     return make_x_inputs(name=name, **cfg)
+
+
+# ------------------------------------------------------------------ NHA ----
+# Inputs of the Native Hybrid Attention layer (the "next" workload on the same
+# attention kernels): per-head q, k, v and a per-token, per-slot forget gate
+# of the slot memory, given as its logarithm.  Recipe:
+#   q, k, v ~ N(0, 1) float32 (keys not normalised: the softmax over slots and
+#   window sees logits of order one);
+#   log_alpha = log(sigmoid(z)) / 8 with z ~ N(0, 1), float32 (the gate damping
+#   of Gated Slot Attention, temperature 8: alpha in (0, 1), mostly 0.9-0.99);
+#   q, k, v rounded to bf16 for the bf16 workloads (canonical inputs).
+
+
+@dataclasses.dataclass
+class NhaInputs:
+    B: int
+    H: int
+    L: int
+    d: int
+    m: int  # slots
+    window: int
+    dtype: str
+    q: np.ndarray  # [B, H, L, d]
+    k: np.ndarray
+    v: np.ndarray
+    log_alpha: np.ndarray  # [B, H, L, m]
+    name: str = ""
+
+
+def make_nha_inputs(B: int, H: int, L: int, d: int = 128, m: int = 64, window: int = 512, dtype: str = "bf16",
+                    seed: int = 0, name: str = "") -> NhaInputs:
+    rng = _rng(seed, 201)
+    q = _normal(rng, (B, H, L, d))
+    k = _normal(rng, (B, H, L, d))
+    v = _normal(rng, (B, H, L, d))
+    z = _normal(rng, (B, H, L, m))
+    log_alpha = (np.log(_sigmoid(z).astype(np.float64)) / 8.0).astype(np.float32)
+    if dtype == "bf16":
+        q, k, v = round_to_bf16(q), round_to_bf16(k), round_to_bf16(v)
+    return NhaInputs(B=B, H=H, L=L, d=d, m=m, window=window, dtype=dtype, q=q, k=k, v=v, log_alpha=log_alpha,
+                     name=name)
+
+
+NHA_CONFIGS = {
+    # parity cases: every window regime, ragged chunk counts
+    "nha_tiny": dict(B=1, H=2, L=512, d=128, m=64, window=128, seed=21),
+    "nha_w0": dict(B=1, H=2, L=384, d=128, m=64, window=0, seed=22),
+    "nha_full": dict(B=1, H=2, L=448, d=128, m=64, window=1 << 20, seed=23),
+    "nha_w256": dict(B=2, H=2, L=704, d=128, m=64, window=256, seed=24),
+    "nha_mid": dict(B=1, H=4, L=2048, d=128, m=64, window=512, seed=25),
+    # the measured workload: the 1.3B-scale layer's shape with a 512-token window
+    "nha_l8192": dict(B=4, H=16, L=8192, d=128, m=64, window=512, seed=26),
+}
+
+
+def nha_config_inputs(name: str) -> NhaInputs:
+    return make_nha_inputs(name=name, **NHA_CONFIGS[name])
