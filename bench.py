@@ -64,6 +64,7 @@ def parse():
     ap.add_argument("--no-x-path", action="store_true", help="skip the layer-with-projections measurement")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass measurement")
+    ap.add_argument("--no-nha", action="store_true", help="skip the Native Hybrid Attention measurement")
     ap.add_argument("--workload", default="l8192",
                     help="layer workload of the device-timed step (default: the 8192-token one); others, e.g. "
                          "'long' (1 x 32 x 65536, 12.5 %% softmax chunks), are extra data points")
@@ -575,6 +576,8 @@ def run_native(args, rank, world, local_rank):
         res["decode"] = run_decode(args, rank, dev, stream, dist)
     if not args.no_backward:
         res["backward"] = run_backward(args, dev, stream, dist, dv, B, H, L, d, work)
+    if not args.no_nha:
+        res["nha"] = run_nha(args, rank, dev, stream, dist)
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
     if not args.no_cpu_baseline and world == 1 and rank == 0:
         cores = cpu_cores()
@@ -675,6 +678,106 @@ def run_x_path(args, rank, dev, stream, dist):
             "value": job_throughput(B * L, world, ms), "unit": "tokens/s", "ms_per_step": ms,
             "stages_ms": stage_ms, "projection_gemm_flops_per_step": f_in + f_out,
             "roofline": gemms.get(dom), "gemm_rooflines": gemms}
+
+
+def nha_work(B, H, L, d, m, w):
+    """Algorithmic FLOPs of the NHA layer (tensor-core work of its plain
+    definition): per query 4 d per window key (q.k and p v) and, once a token
+    has left the window, 4 d per slot (q.K~ and p V~); per token written into
+    the slots 4 m d (the gated update of K~ and V~)."""
+    import numpy as np
+
+    t = np.arange(L)
+    pairs = np.minimum(t + 1, max(w, 0)).sum() if w > 0 else 0
+    n_slot = max(L - w, 0)
+    attn = 4.0 * d * (pairs + m * n_slot)
+    state = 4.0 * m * d * n_slot
+    return {"attn": B * H * attn, "state": B * H * state}
+
+
+def run_nha(args, rank, dev, stream, dist):
+    """Times nats_nha_fwd (Native Hybrid Attention: one softmax over 64 slots
+    and a 512-token window) at the 1.3B-scale layer shape (B = 4, H = 16,
+    L = 8192, d = 128), inputs resident in HBM, K steps after warm-up."""
+    import numpy as np
+    import torch
+
+    import gen
+    import linear_attention_nats_gb300 as nats
+    from linear_attention_nats_gb300 import _native
+
+    cfg = dict(gen.NHA_CONFIGS["nha_l8192"])
+    cfg["seed"] = rank_seed(cfg["seed"], rank)
+    inp = gen.make_nha_inputs(name="nha_l8192", **cfg)
+    B, H, L, d, m, w = inp.B, inp.H, inp.L, inp.d, inp.m, inp.window
+
+    def bf(a):
+        return torch.from_numpy(gen.bf16_bits(np.ascontiguousarray(a, np.float32)).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+
+    q, k, v = bf(inp.q), bf(inp.k), bf(inp.v)
+    la = torch.from_numpy(np.ascontiguousarray(inp.log_alpha)).to(dev)
+    out = torch.empty_like(q)
+    dm = _native.nha_dims(B, H, L, d, m, w)
+    wsb = int(_native.lib.nats_nha_workspace_size(ctypes.byref(dm)))
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+
+    def call(prof=None):
+        code = _native.lib.nats_nha_fwd_profiled(ctypes.byref(dm), P(q), P(k), P(v), P(la), P(out), P(ws),
+                                                 ctypes.c_size_t(wsb), ctypes.c_void_p(stream.cuda_stream),
+                                                 ctypes.byref(prof) if prof is not None else None)
+        if code != 0:
+            raise _native.NatsError(code, "nats_nha_fwd_profiled")
+
+    for _ in range(max(args.warmup, 1)):
+        call()
+    torch.cuda.synchronize()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2)]
+          for _ in range(args.steps)]
+    profs = []
+    for row in ev:
+        p = _native.Profile()
+        for i, (a0, a1) in enumerate(row):
+            a0.record(stream)
+            a1.record(stream)
+            p.start[i] = a0.cuda_event
+            p.stop[i] = a1.cuda_event
+        profs.append(p)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(args.steps):
+        call(profs[i])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
+    world = dist.get_world_size() if dist is not None else 1
+    kms = {name: sum(row[i][0].elapsed_time(row[i][1]) for row in ev) / len(ev)
+           for i, name in enumerate(("nha_state", "nha_attn")) if profs[0].stage_launches[i]}
+    fl = nha_work(B, H, L, d, m, w)
+    pk = peaks()
+    peak = pk["bf16_tflops_sustained"]
+    rl = {}
+    for name, f in (("nha_attn", fl["attn"]), ("nha_state", fl["state"])):
+        if name in kms:
+            ach = f / (kms[name] / 1e3) / 1e12
+            rl[name] = {"kernel": name + "_kernel", "bound": "tensor", "achieved": ach, "peak": peak,
+                        "unit": "TFLOP/s", "frac": ach / peak, "peak_source": f"{pk['source']} bf16 sustained",
+                        "ms_per_launch": kms[name], "flops_per_launch": f}
+    tot = fl["attn"] + fl["state"]
+    return {"what": "nats_nha_fwd: Native Hybrid Attention (reading CONV-16), 64 slots + a 512-token window under "
+                    "one softmax; slot-memory scan (tcgen05, one CTA per head) then the attention (tcgen05, "
+                    "persistent)",
+            "config": {"B": B, "H": H, "L": L, "d": d, "slots": m, "window": w},
+            "value": job_throughput(B * L, world, ms), "unit": "tokens/s", "ms_per_step": ms,
+            "kernels_ms": kms, "flops_per_step": tot,
+            "layer_roofline": {"bound": "tensor", "achieved": tot / (ms / 1e3) / 1e12, "peak": peak,
+                               "unit": "TFLOP/s", "frac": tot / (ms / 1e3) / 1e12 / peak},
+            "roofline": rl.get("nha_attn"), "kernel_rooflines": rl,
+            "gpu_launches": sum(p.launches for p in profs)}
 
 
 def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):

@@ -378,6 +378,58 @@ nats_status nats_hybrid_bwd(const nats_dims* dims, const void* q, const void* k,
                             float* dbeta, float* dw_g, float* db_g, float* dnorm_w_soft, float* dnorm_w_lin,
                             void* workspace, size_t workspace_bytes, nats_stream_t stream);
 
+/* -------------------------------------------------------------------- NHA
+ * Native Hybrid Attention, the related layer of "Native Hybrid Attention
+ * for Efficient Sequence Modeling" (section "2. Methodologie",
+ * "Kernprincipes"): long-term slots updated by a linear RNN and a sliding
+ * window of recent tokens form one key / value set under one softmax; the
+ * window size w is the layer's only knob (w = 0: a pure linear RNN; w =
+ * sequence length: full attention).  The page gives no update rule; the
+ * reading (CONV-16) is the Gated Slot Attention slot update:
+ *   a token j, when it leaves the window, writes every slot s:
+ *     K~[s] <- alpha_j[s] K~[s] + (1 - alpha_j[s]) k_j,   V~[s] likewise with v_j,
+ *   K~ = V~ = 0 at the start; the query at t sees the window tokens
+ *   t - w < j <= t and, once t >= w, the m slots after the writes of every
+ *   j <= t - w:
+ *     o_t = softmax(scale q_t . [K~; k_window]) [V~; v_window].
+ * dims: B, H, L (L % 64 == 0), d = 128, slots = 64, window w (0, a multiple
+ * of 128, or >= L: full attention), dtype NATS_BF16, scale (0 =>
+ * 1/sqrt(d)).  q, k, v, out [B, H, L, d] bf16; log_alpha [B, H, L, slots]
+ * fp32 (log of the forget gate, <= 0).  The kernels hold the chunkwise form
+ * to a product of factors e^{|A|} per half chunk, A a 32-token sum of
+ * log_alpha of one slot: keep log_alpha >= -2.5 on average over any 32
+ * tokens (alpha >= 0.08), far beyond the damped gates of Gated Slot
+ * Attention.  All pointers device, 16-byte aligned; asynchronous on
+ * `stream`.  The workspace (nats_nha_workspace_size bytes) holds the
+ * chunk-start slot memories and the per-chunk gate factors.  Errors before
+ * any launch: NATS_ERR_NULL, NATS_ERR_SHAPE, NATS_ERR_DTYPE,
+ * NATS_ERR_UNSUPPORTED (d, slots or w not supported), NATS_ERR_VALUE,
+ * NATS_ERR_ALIGN, NATS_ERR_WORKSPACE; NATS_ERR_CUDA on a failed launch.
+ * nats_nha_workspace_check synchronises `stream` and reports
+ * NATS_ERR_INTERNAL if a bounded internal wait of the last call that used
+ * `workspace` expired. */
+typedef struct {
+  int32_t B, H, L;
+  int32_t d;       /* head size (128) */
+  int32_t slots;   /* m (64) */
+  int32_t window;  /* w */
+  int32_t dtype;   /* NATS_BF16 */
+  float scale;     /* 0 => 1/sqrt(d) */
+} nats_nha_dims;
+
+size_t nats_nha_workspace_size(const nats_nha_dims* dims);
+nats_status nats_nha_fwd(const nats_nha_dims* dims, const void* q, const void* k, const void* v,
+                         const float* log_alpha, void* out, void* workspace, size_t workspace_bytes,
+                         nats_stream_t stream);
+nats_status nats_nha_workspace_check(const nats_nha_dims* dims, const void* workspace, nats_stream_t stream);
+/* nats_nha_fwd with caller-owned CUDA events recorded around its kernels
+ * (prof may be NULL): start[0] / stop[0] around the slot-memory scan (not
+ * launched when w >= L; stage_launches[0] then 0), start[1] / stop[1] around
+ * the attention kernel; `launches` counts the kernels launched. */
+nats_status nats_nha_fwd_profiled(const nats_nha_dims* dims, const void* q, const void* k, const void* v,
+                                  const float* log_alpha, void* out, void* workspace, size_t workspace_bytes,
+                                  nats_stream_t stream, nats_profile* prof);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,7 +16,7 @@ import torch
 from . import _native
 from ._native import NATS_BF16, NATS_F32, NatsError, check, dims  # noqa: F401
 
-__all__ = ["select", "hybrid_fwd", "hybrid_fwd_x", "DecodeState", "decode_step", "workspace_size", "NatsError",
+__all__ = ["select", "hybrid_fwd", "hybrid_fwd_x", "nha_fwd", "DecodeState", "decode_step", "workspace_size", "NatsError",
            "dims", "NATS_BF16", "NATS_F32"]
 
 
@@ -293,3 +293,33 @@ def decode_step(state: DecodeState, t: int, q, k, v, g, beta, w_s, b_s, w_g, b_g
         _p(norm_w_soft), _p(norm_w_lin), ctypes.byref(st), _p(out), _p(sel_out), _p(o_s), _p(o_l),
         _stream(stream)), "nats_decode_step")
     return {"out": out, "o_s": o_s, "o_l": o_l} if return_branches else out
+
+
+def nha_fwd(q, k, v, log_alpha, *, window: int, scale: float = 0.0, out=None, workspace=None,
+            check_errors: bool = False, stream=None):
+    """Native Hybrid Attention forward (nats_nha_fwd): q, k, v [B, H, L, 128]
+    bf16, log_alpha [B, H, L, 64] fp32 (log of the slot forget gate); one
+    softmax over the slot memory and the window of the last `window` tokens.
+    Returns out [B, H, L, 128] bf16.  The definitions are those of
+    nats_nha_fwd in include/nats.h."""
+    _req(q, "q", torch.bfloat16)
+    B, H, L, d = q.shape
+    for name, t in (("k", k), ("v", v)):
+        _req(t, name, torch.bfloat16, q.shape)
+    _req(log_alpha, "log_alpha", torch.float32)
+    if log_alpha.dim() != 4 or tuple(log_alpha.shape[:3]) != (B, H, L):
+        raise ValueError("log_alpha must be [B, H, L, slots]")
+    dm = _native.nha_dims(B, H, L, d, log_alpha.shape[3], window, NATS_BF16, scale)
+    if out is None:
+        out = torch.empty_like(q)
+    _req(out, "out", torch.bfloat16, q.shape)
+    need = int(_native.lib.nats_nha_workspace_size(ctypes.byref(dm)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _req(workspace, "workspace", torch.uint8)
+    check(_native.lib.nats_nha_fwd(ctypes.byref(dm), _p(q), _p(k), _p(v), _p(log_alpha), _p(out), _p(workspace),
+                                   ctypes.c_size_t(workspace.numel()), _stream(stream)), "nats_nha_fwd")
+    if check_errors:
+        check(_native.lib.nats_nha_workspace_check(ctypes.byref(dm), _p(workspace), _stream(stream)),
+              "nats_nha_workspace_check")
+    return out

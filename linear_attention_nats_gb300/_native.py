@@ -28,7 +28,8 @@ EXPORTS = ("nats_status_string", "nats_last_cuda_error", "nats_workspace_size", 
            "nats_x_workspace_size", "nats_x_workspace_check",
            "nats_hybrid_fwd_x_profiled",
            "nats_hybrid_fwd_x", "nats_debug_fail_stage", "nats_debug_bounded_wait", "nats_decode_step",
-           "nats_bwd_workspace_size", "nats_hybrid_bwd")
+           "nats_bwd_workspace_size", "nats_hybrid_bwd", "nats_nha_workspace_size", "nats_nha_fwd",
+           "nats_nha_workspace_check", "nats_nha_fwd_profiled")
 
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -54,6 +55,16 @@ class Dims(ctypes.Structure):
         ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("chunk", ctypes.c_int32),
         ("dtype", ctypes.c_int32), ("scale", ctypes.c_float), ("eps", ctypes.c_float),
     ]
+
+
+class NhaDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("L", ctypes.c_int32), ("d", ctypes.c_int32),
+                ("slots", ctypes.c_int32), ("window", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("scale", ctypes.c_float)]
+
+
+def nha_dims(B, H, L, d=128, slots=64, window=512, dtype=NATS_BF16, scale=0.0) -> NhaDims:
+    return NhaDims(int(B), int(H), int(L), int(d), int(slots), int(window), int(dtype), float(scale))
 
 
 class NatsError(RuntimeError):
@@ -110,6 +121,15 @@ def _load() -> ctypes.CDLL:
     lib.nats_bwd_workspace_size.restype = ctypes.c_size_t
     lib.nats_hybrid_bwd.argtypes = [ctypes.POINTER(Dims)] + [P] * 23 + [ctypes.c_size_t, P]
     lib.nats_hybrid_bwd.restype = ctypes.c_int
+    lib.nats_nha_workspace_size.argtypes = [ctypes.POINTER(NhaDims)]
+    lib.nats_nha_workspace_size.restype = ctypes.c_size_t
+    lib.nats_nha_fwd.argtypes = [ctypes.POINTER(NhaDims)] + [P] * 6 + [ctypes.c_size_t, P]
+    lib.nats_nha_fwd.restype = ctypes.c_int
+    lib.nats_nha_workspace_check.argtypes = [ctypes.POINTER(NhaDims), P, P]
+    lib.nats_nha_workspace_check.restype = ctypes.c_int
+    lib.nats_nha_fwd_profiled.argtypes = [ctypes.POINTER(NhaDims)] + [P] * 6 + [ctypes.c_size_t, P,
+                                                                                ctypes.POINTER(Profile)]
+    lib.nats_nha_fwd_profiled.restype = ctypes.c_int
     return lib
 
 

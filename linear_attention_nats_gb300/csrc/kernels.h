@@ -87,6 +87,16 @@ cudaError_t launch_proj_qkv_tc(int B, int H, int L, int d, int hidden, const voi
 cudaError_t launch_proj_out_tc(int B, int H, int L, int d, int hidden, const void* o, const void* w_o, void* y,
                                int* err, cudaStream_t st);
 
+// Native Hybrid Attention (nha.cu): workspace bytes, the two launches (slot
+// state scan, unless w >= L; the attention), and the bounded-wait flag.
+size_t nha_workspace_bytes(long long BH, int L);
+// ev_start / ev_stop (or null): cudaEvent_t handles recorded around the
+// slot scan [0] and the attention [1]; *launches counts the kernels.
+cudaError_t launch_nha_fwd(long long BH, int L, int window, float scale, const void* q, const void* k, const void* v,
+                           const float* log_alpha, void* out, void* ws, cudaStream_t st, void* const* ev_start,
+                           void* const* ev_stop, int* launches);
+int* nha_err_flag(void* ws, long long BH, int L);
+
 // Test hook: one bounded wait that runs out after limit_ns and sets *flag.
 cudaError_t launch_bounded_wait(int* flag, long long limit_ns, cudaStream_t st);
 

@@ -225,3 +225,26 @@ def test_noalloc_validation_order(nat):
     assert call(big, odd) == 4  # NATS_ERR_ALIGN comes before the size limit
     assert call(big, good) == 5  # NATS_ERR_WORKSPACE
     assert nat.lib.nats_noalloc_check(ctypes.byref(big), None) == 5
+
+
+def test_nha_validation(nat):
+    """nats_nha_fwd rejects bad arguments on the host, before any launch."""
+    P = lambda a: ctypes.c_void_p(a)
+    ok_ptrs = [P(0x10000000)] * 5 + [P(0x20000000)]
+
+    def call(dm, ptrs=ok_ptrs, nbytes=1 << 40):
+        return nat.lib.nats_nha_fwd(ctypes.byref(dm), *ptrs, ctypes.c_size_t(nbytes), None)
+
+    d = nat.nha_dims
+    assert nat.lib.nats_nha_workspace_size(ctypes.byref(d(1, 2, 512))) > 0
+    assert call(d(1, 2, 500)) == 2  # L % 64
+    assert call(d(1, 2, 512, d=64)) == 6  # head size
+    assert call(d(1, 2, 512, slots=32)) == 6  # slot count
+    assert call(d(1, 2, 512, window=64)) == 6  # window not a multiple of 128 (and < L)
+    assert call(d(1, 2, 512, window=-1)) == 2
+    assert call(d(1, 2, 512, dtype=nat.NATS_F32)) == 3
+    assert call(d(1, 2, 512, scale=float("nan"))) == 9
+    assert call(d(0, 2, 512)) == 0  # empty: no-op
+    assert call(d(1, 2, 512), [None] + ok_ptrs[1:]) == 1
+    assert call(d(1, 2, 512), [P(0x10000004)] + ok_ptrs[1:]) == 4
+    assert call(d(1, 2, 512), nbytes=16) == 5
