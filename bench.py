@@ -65,6 +65,7 @@ def parse():
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass measurement")
     ap.add_argument("--no-nha", action="store_true", help="skip the Native Hybrid Attention measurement")
+    ap.add_argument("--no-select", action="store_true", help="skip the score-layer (nats_select) measurement")
     ap.add_argument("--workload", default="l8192",
                     help="layer workload of the device-timed step (default: the 8192-token one); others, e.g. "
                          "'long' (1 x 32 x 65536, 12.5 %% softmax chunks), are extra data points")
@@ -83,6 +84,12 @@ def peaks():
                 "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
             "source": "fallback"}
+
+
+# GB300 nominal dense rates (context for the measured-peak fractions):
+# bf16 tensor 2.25 PFLOP/s, HBM3e 7.9 TB/s.
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_HBM_GBS = 7900.0
 
 
 # ------------------------------------------------------- algorithmic work ----
@@ -148,8 +155,9 @@ def rooflines(work, stage_ms, pk):
         else:
             achieved, peak, unit = amount / (ms / 1e3) / 1e9, pk["hbm_gbs"], "GB/s"
             peak_src, per = f"{pk['source']} HBM copy", {"bytes_per_launch": amount}
+        nominal = NOMINAL_BF16_TFLOPS if bound == "tensor" else NOMINAL_HBM_GBS
         out[name] = {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                     "frac": achieved / peak, "peak_source": peak_src,
+                     "frac": achieved / peak, "peak_source": peak_src, "frac_of_nominal": achieved / nominal,
                      "traffic": recorded_traffic(os.path.join(ROOT, "linear_attention_nats_gb300", "csrc", src)),
                      "ms_per_launch": ms, **per}
     return out
@@ -273,16 +281,17 @@ class Clocks:
 
 # ------------------------------------------------------------ traffic ----
 
-def recorded_traffic(kernel_src):
+def recorded_traffic(kernel_src, workload=None):
     """DRAM bytes per launch of a kernel from the committed ncu summaries, valid
     only while the kernel's source file is unchanged (hash match)."""
+    workload = workload or WORKLOAD
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
     h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
     for line in open(path):
         kv = dict(x.split("=", 1) for x in line.split() if "=" in x)
-        if kv.get("src") == os.path.basename(kernel_src) and kv.get("sha") == h and kv.get("workload") == WORKLOAD:
+        if kv.get("src") == os.path.basename(kernel_src) and kv.get("sha") == h and kv.get("workload") == workload:
             return float(kv["dram_bytes_per_launch"])
     return None
 
@@ -562,6 +571,10 @@ def run_native(args, rank, world, local_rank):
         "kernel_rooflines": per_kernel,
         "layer_roofline": {"bound": "tensor", "achieved": layer_tflops, "peak": peak_tc,
                            "unit": "TFLOP/s", "frac": layer_tflops / peak_tc,
+                           "frac_of_burst": layer_tflops / pk["bf16_tflops"],
+                           "frac_of_nominal": layer_tflops / NOMINAL_BF16_TFLOPS,
+                           "what": "the whole step (all kernels) against the bf16 tensor peak; `roofline` is the "
+                                   "dominant kernel's",
                            "flops_per_step": work["flops_total"]},
         "stages_ms": stage_ms,
         "gpu_launches": launches,
@@ -578,6 +591,8 @@ def run_native(args, rank, world, local_rank):
         res["backward"] = run_backward(args, dev, stream, dist, dv, B, H, L, d, work)
     if not args.no_nha:
         res["nha"] = run_nha(args, rank, dev, stream, dist)
+    if not args.no_select:
+        res["select"] = run_select(args, dev, stream, dist, dv, B, H, L, d)
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
     if not args.no_cpu_baseline and world == 1 and rank == 0:
         cores = cpu_cores()
@@ -669,8 +684,10 @@ def run_x_path(args, rank, dev, stream, dist):
         if name in stage_ms:
             ach = fl / (stage_ms[name] / 1e3) / 1e12
             gemms[name] = {"kernel": "gemm_tc_kernel", "bound": "tensor", "achieved": ach, "peak": peak,
-                           "unit": "TFLOP/s", "frac": ach / peak, "peak_source": "measured bf16 sustained",
-                           "ms_per_launch": stage_ms[name], "flops_per_launch": fl}
+                           "unit": "TFLOP/s", "frac": ach / peak, "peak_source": f"{pk['source']} bf16 sustained",
+                           "ms_per_launch": stage_ms[name], "flops_per_launch": fl,
+                           "traffic": recorded_traffic(os.path.join(ROOT, "linear_attention_nats_gb300", "csrc",
+                                                                    "gemm_tc.cu"), f"x_l8192_{name}")}
     dom = max(gemms, key=lambda k: gemms[k]["ms_per_launch"]) if gemms else None
     return {"what": "nats_hybrid_fwd_x: x -> q, k, v, g, beta (tcgen05 GEMM, head split + key norm + gates in "
                     "its epilogue), the layer, output projection (the same GEMM kernel)",
@@ -678,6 +695,52 @@ def run_x_path(args, rank, dev, stream, dist):
             "value": job_throughput(B * L, world, ms), "unit": "tokens/s", "ms_per_step": ms,
             "stages_ms": stage_ms, "projection_gemm_flops_per_step": f_in + f_out,
             "roofline": gemms.get(dom), "gemm_rooflines": gemms}
+
+
+def run_select(args, dev, stream, dist, dv, B, H, L, d):
+    """Times nats_select (the Attention Score Layer alone: chunk mean pool of
+    [q; k], the linear score, the argmax; score_kernel) on the layer
+    workload's Q and K, inputs resident in HBM.  HBM-bound: it reads Q and K
+    once (the bf16 layer forward takes its selection inside the chunk-factor
+    kernel instead)."""
+    import torch
+
+    from linear_attention_nats_gb300 import _native
+
+    N = L // C
+    dm = _native.dims(B, H, L, d, _native.NATS_BF16)
+    sel = torch.empty((B, H, N), dtype=torch.uint8, device=dev)
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+
+    def call():
+        code = _native.lib.nats_select(ctypes.byref(dm), P(dv["q"]), P(dv["k"]), P(dv["w_s"]), P(dv["b_s"]), P(sel),
+                                       None, ctypes.c_void_p(stream.cuda_stream))
+        if code != 0:
+            raise _native.NatsError(code, "nats_select")
+
+    for _ in range(max(args.warmup, 1)):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
+    nbytes = 2.0 * B * H * L * d * 2 + B * H * N
+    pk = peaks()
+    ach = nbytes / (ms / 1e3) / 1e9
+    return {"what": "nats_select (score_kernel): mean pool + linear score + argmax per 64-token chunk",
+            "ms_per_launch": ms,
+            "roofline": {"kernel": "score_kernel", "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "peak_source": f"{pk['source']} HBM copy",
+                         "bytes_per_launch": nbytes,
+                         "traffic": recorded_traffic(os.path.join(ROOT, "linear_attention_nats_gb300", "csrc",
+                                                                  "select.cu"))}}
 
 
 def nha_work(B, H, L, d, m, w):
@@ -766,7 +829,9 @@ def run_nha(args, rank, dev, stream, dist):
             ach = f / (kms[name] / 1e3) / 1e12
             rl[name] = {"kernel": name + "_kernel", "bound": "tensor", "achieved": ach, "peak": peak,
                         "unit": "TFLOP/s", "frac": ach / peak, "peak_source": f"{pk['source']} bf16 sustained",
-                        "ms_per_launch": kms[name], "flops_per_launch": f}
+                        "ms_per_launch": kms[name], "flops_per_launch": f,
+                        "traffic": recorded_traffic(os.path.join(ROOT, "linear_attention_nats_gb300", "csrc",
+                                                                 "nha.cu"), f"nha_l8192_{name}")}
     tot = fl["attn"] + fl["state"]
     return {"what": "nats_nha_fwd: Native Hybrid Attention (reading CONV-16), 64 slots + a 512-token window under "
                     "one softmax; slot-memory scan (tcgen05, one CTA per head) then the attention (tcgen05, "

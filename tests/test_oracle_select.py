@@ -91,3 +91,21 @@ def test_workload_margins():
         assert np.abs(scores[..., 0] - scores[..., 1]).min() >= 1e-3, name
         if inp.planted is not None:
             assert np.array_equal(sel == 0, inp.planted)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["l8192", "sweep0", "sweep12", "sweep50", "sweep100", "long"])
+def test_large_workload_margins(name):
+    """The full-size workloads too: every argmax margin >= 1e-3 on the rounded
+    inputs (fp64 scores), and the score layer recovers the planted chunks
+    exactly (or the forced all / none pattern)."""
+    inp = gen.config_inputs(name)
+    sel, scores = oracle.select_inputs(inp)
+    margin = np.abs(scores[..., 0] - scores[..., 1]).min()
+    assert margin >= 1e-3, (name, margin)
+    if inp.planted is not None:
+        assert np.array_equal(sel == 0, inp.planted), name
+    if name == "sweep0":
+        assert (sel == 1).all()
+    if name == "sweep100":
+        assert (sel == 0).all()
