@@ -848,15 +848,26 @@ def run_nha(args, rank, dev, stream, dist):
 def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):
     """Times nats_hybrid_bwd on the layer workload: the gradients of a seeded
     dout at the forward's selection, from the activations the CUDA forward
-    saved (one forward outside the timed region).  Its contractions run on
-    the CUDA cores in fp32, so the roofline is the fp32 FMA rate: 152 SMs x
-    128 lanes x 2 FLOP x the SM clock.  Algorithmic FLOPs: 10 d per visible
-    (query, key) pair of the softmax branch (recomputed scores, dP, dq, dk,
-    dv) and 14 d^2 per token of Gated DeltaNet (dS += do q^T, S^T do,
-    dS k, the two column sums of dk, <dS, S>, the dS update)."""
+    saved (one forward outside the timed region).  Each of its four stages
+    is timed with the library's own stage events and set against the
+    roofline of its own kind of work:
+      merge_bwd   HBM: per token it reads q, dout (bf16) and o_soft, o_lin
+                  (fp32) and writes d o_soft (bf16), d o_lin, dq (fp32) and
+                  delta: 22 d + 4 bytes;
+      softmax_bwd bf16 tensor (warp-level MMAs): 10 d FLOP per visible
+                  (query, key) pair (scores recomputed, dP, dq, dk, dv);
+      gdn_bwd     fp32 CUDA cores: 14 d^2 FLOP per token (dS += do q^T,
+                  S^T do, dS k, the two column sums of dk, <dS, S>, the dS
+                  update), against 152 SMs x 128 FMA lanes x 2 FLOP x the SM
+                  clock sampled during the timed region;
+      combine     HBM: per token k (bf16), the two state halves' column sums
+                  and scalars, dq and dk read and written, g, beta, dg,
+                  dbeta: 34 d + 48 bytes.
+    The headline roofline is the stage with the largest share of the time."""
     import torch
 
     import linear_attention_nats_gb300 as nats
+    from linear_attention_nats_gb300 import _native
 
     t = dv
     fwd = nats.hybrid_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_s"], t["b_s"], t["w_g"], t["b_g"],
@@ -865,39 +876,81 @@ def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):
     dout = torch.randn((B, H, L, d), generator=gen_).to(t["q"].dtype).to(dev)
     dm = nats.dims(B, H, L, d, 0 if t["q"].dtype == torch.bfloat16 else 1)
     ws = torch.empty(int(nats._native.lib.nats_bwd_workspace_size(ctypes.byref(dm))), dtype=torch.uint8, device=dev)
+    ns = len(_native.BWD_STAGES)
 
-    def step():
+    def step(prof=None):
         return nats.hybrid_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_g"], t["b_g"], fwd["sel"],
-                               fwd["o_soft"], fwd["o_lin"], dout, workspace=ws, stream=stream)
+                               fwd["o_soft"], fwd["o_lin"], dout, workspace=ws, stream=stream, profile=prof)
 
     steps = max(1, min(args.steps, 3))
     with torch.cuda.stream(stream):
         step()
     torch.cuda.synchronize()
+    stage_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ns)]
+                for _ in range(steps)]
+    for row in stage_ev:  # materialise the event handles
+        for a, b in row:
+            a.record(stream)
+            b.record(stream)
+    profs = []
+    for row in stage_ev:
+        pr = _native.Profile()
+        for i, (a, b) in enumerate(row):
+            pr.start[i] = a.cuda_event
+            pr.stop[i] = b.cuda_event
+        profs.append(pr)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
+    clocks = Clocks(torch.cuda.current_device(), enabled=not args.no_clocks)
     e0.record(stream)
     with torch.cuda.stream(stream):
-        for _ in range(steps):
-            step()
+        for i in range(steps):
+            step(profs[i])
     e1.record(stream)
     torch.cuda.synchronize()
+    clk = clocks.stop()
     ms = max_over_ranks(e0.elapsed_time(e1), dist, dev) / steps
     world = dist.get_world_size() if dist is not None else 1
+    stage_ms = {name: sum(r[i][0].elapsed_time(r[i][1]) for r in stage_ev) / steps
+                for i, name in enumerate(_native.BWD_STAGES)}
+    pk = peaks()
+    tokens = B * H * L
     pairs = work["flops_softmax"] / (4 * d)
-    flops = 10 * d * pairs + 14 * d * d * B * H * L
-    sm_mhz = 2070.0
-    peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
-    achieved = flops / (ms / 1e3) / 1e12
+    if clk and clk.get("sm_mhz"):
+        sm_mhz, clk_src = clk["sm_mhz"], f"median SM clock sampled during the timed region ({clk['source']})"
+    else:
+        sm_mhz = float(torch.cuda.get_device_properties(dev).clock_rate) / 1e3 \
+            if hasattr(torch.cuda.get_device_properties(dev), "clock_rate") else None
+        clk_src = "the device's reported SM clock (no sample)"
+    fp32_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12 if sm_mhz else None
+    amounts = {"merge_bwd": ("hbm", (22 * d + 4) * tokens),
+               "softmax_bwd": ("tensor", 10 * d * pairs),
+               "gdn_bwd": ("alu", 14 * d * d * tokens),
+               "combine": ("hbm", (34 * d + 48) * tokens)}
+    per = {}
+    for name, (bound, amount) in amounts.items():
+        sms = stage_ms[name]
+        if bound == "hbm":
+            ach, peak, unit, src = amount / (sms / 1e3) / 1e9, pk["hbm_gbs"], "GB/s", f"{pk['source']} HBM copy"
+        elif bound == "tensor":
+            ach, peak, unit = amount / (sms / 1e3) / 1e12, pk["bf16_tflops_sustained"], "TFLOP/s"
+            src = f"{pk['source']} bf16 sustained (the kernels use mma.sync, not tcgen05)"
+        else:
+            ach, peak, unit = amount / (sms / 1e3) / 1e12, fp32_peak, "TFLOP/s"
+            src = f"fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x {sm_mhz} MHz, {clk_src}"
+        per[name] = {"bound": bound, "ms": sms, "share": sms / ms if ms else None, "achieved": ach, "peak": peak,
+                     "unit": unit, "frac": (ach / peak) if peak else None, "peak_source": src,
+                     ("bytes_per_step" if bound == "hbm" else "flops_per_step"): amount}
+    top = max(per, key=lambda n: per[n]["ms"])
     return {"what": "nats_hybrid_bwd: gradients of q, k, v, g, beta, W_g, b_g and the RMSNorm weights at the "
                     "forward's selection, same workload as the forward",
             "value": job_throughput(B * L, world, ms), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
-            "launches_per_step": 4,
-            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "flops_per_step": flops,
-                         "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x 2070 MHz"}}
+            "launches_per_step": int(profs[0].launches),
+            "stages": per, "clocks": clk,
+            "roofline": {"kernel": top, **{k: per[top][k] for k in ("bound", "achieved", "peak", "unit", "frac",
+                                                                   "peak_source")}}}
 
 
 def run_decode(args, rank, dev, stream, dist):

@@ -378,6 +378,27 @@ nats_status nats_hybrid_bwd(const nats_dims* dims, const void* q, const void* k,
                             float* dbeta, float* dw_g, float* db_g, float* dnorm_w_soft, float* dnorm_w_lin,
                             void* workspace, size_t workspace_bytes, nats_stream_t stream);
 
+/* Stages of nats_hybrid_bwd, for per-stage timing (indices into the arrays
+ * of nats_profile). */
+typedef enum {
+  NATS_BWD_STAGE_MERGE = 0,   /* RMSNorm + gated merge backward: branch output gradients, dW_g, db_g, dnorm_w */
+  NATS_BWD_STAGE_SOFTMAX = 1, /* softmax branch: dq, then dk / dv (bf16: warp-level tensor MMAs) */
+  NATS_BWD_STAGE_GDN = 2,     /* Gated DeltaNet adjoint scan, reverse over chunks (fp32 CUDA cores) */
+  NATS_BWD_STAGE_COMBINE = 3, /* per-token dq, dk, dg, dbeta from the adjoint's partial sums */
+  NATS_BWD_NUM_STAGES = 4
+} nats_bwd_stage;
+
+/* nats_hybrid_bwd plus per-stage event records, as in
+ * nats_hybrid_fwd_profiled but with NATS_BWD_STAGE_* ids (prof may be NULL,
+ * which makes it identical to nats_hybrid_bwd). */
+nats_status nats_hybrid_bwd_profiled(const nats_dims* dims, const void* q, const void* k, const void* v,
+                                     const float* g, const float* beta, const float* w_g, const float* b_g,
+                                     const float* norm_w_soft, const float* norm_w_lin, const uint8_t* sel,
+                                     const float* o_soft, const float* o_lin, const void* dout, float* dq,
+                                     float* dk, float* dv, float* dg, float* dbeta, float* dw_g, float* db_g,
+                                     float* dnorm_w_soft, float* dnorm_w_lin, void* workspace,
+                                     size_t workspace_bytes, nats_stream_t stream, nats_profile* prof);
+
 /* -------------------------------------------------------------------- NHA
  * Native Hybrid Attention, the related layer of "Native Hybrid Attention
  * for Efficient Sequence Modeling" (section "2. Methodologie",

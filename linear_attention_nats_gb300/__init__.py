@@ -182,8 +182,10 @@ def hybrid_fwd_x(x, w_qkv, w_ab, w_s, b_s, w_g, b_g=None, *, heads: int, b_a=Non
 
 
 def hybrid_bwd(q, k, v, g, beta, w_g, b_g, sel, o_soft, o_lin, dout, *, norm_w_soft=None, norm_w_lin=None,
-               scale: float = 0.0, eps: float = 1e-6, weight_grads: bool = True, workspace=None, stream=None):
-    """Backward pass of the layer at the forward's selection (nats_hybrid_bwd).
+               scale: float = 0.0, eps: float = 1e-6, weight_grads: bool = True, workspace=None, stream=None,
+               profile=None):
+    """Backward pass of the layer at the forward's selection (nats_hybrid_bwd;
+    nats_hybrid_bwd_profiled when `profile`, a _native.Profile, is given).
 
     sel, o_soft, o_lin: the forward's selection and branch outputs
     (hybrid_fwd(..., return_sel=True, return_branches=True)); dout like q.
@@ -218,12 +220,12 @@ def hybrid_bwd(q, k, v, g, beta, w_g, b_g, sel, o_soft, o_lin, dout, *, norm_w_s
     if weight_grads:
         res.update(dw_g=torch.empty((H, d), **f32), db_g=torch.empty((H,), **f32),
                    dnorm_w_soft=torch.empty((d,), **f32), dnorm_w_lin=torch.empty((d,), **f32))
-    check(_native.lib.nats_hybrid_bwd(
+    check(_native.lib.nats_hybrid_bwd_profiled(
         ctypes.byref(dm), _p(q), _p(k), _p(v), _p(g), _p(beta), _p(w_g), _p(b_g), _p(norm_w_soft),
         _p(norm_w_lin), _p(sel), _p(o_soft), _p(o_lin), _p(dout), _p(res["dq"]), _p(res["dk"]), _p(res["dv"]),
         _p(res["dg"]), _p(res["dbeta"]), _p(res.get("dw_g")), _p(res.get("db_g")), _p(res.get("dnorm_w_soft")),
-        _p(res.get("dnorm_w_lin")), _p(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream)),
-        "nats_hybrid_bwd")
+        _p(res.get("dnorm_w_lin")), _p(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream),
+        ctypes.byref(profile) if profile is not None else None), "nats_hybrid_bwd")
     return res
 
 

@@ -349,6 +349,22 @@ nats_status nats_hybrid_bwd(const nats_dims* dims, const void* q, const void* k,
                             const float* o_lin, const void* dout, float* dq, float* dk, float* dv, float* dg,
                             float* dbeta, float* dw_g, float* db_g, float* dnorm_w_soft, float* dnorm_w_lin,
                             void* workspace, size_t workspace_bytes, nats_stream_t stream) {
+  return nats_hybrid_bwd_profiled(dims, q, k, v, g, beta, w_g, b_g, norm_w_soft, norm_w_lin, sel, o_soft, o_lin,
+                                  dout, dq, dk, dv, dg, dbeta, dw_g, db_g, dnorm_w_soft, dnorm_w_lin, workspace,
+                                  workspace_bytes, stream, nullptr);
+}
+
+nats_status nats_hybrid_bwd_profiled(const nats_dims* dims, const void* q, const void* k, const void* v,
+                                     const float* g, const float* beta, const float* w_g, const float* b_g,
+                                     const float* norm_w_soft, const float* norm_w_lin, const uint8_t* sel,
+                                     const float* o_soft, const float* o_lin, const void* dout, float* dq,
+                                     float* dk, float* dv, float* dg, float* dbeta, float* dw_g, float* db_g,
+                                     float* dnorm_w_soft, float* dnorm_w_lin, void* workspace,
+                                     size_t workspace_bytes, nats_stream_t stream, nats_profile* prof) {
+  if (prof) {
+    prof->launches = 0;
+    for (int i = 0; i < NATS_NUM_STAGES; ++i) prof->stage_launches[i] = 0;
+  }
   nats_status s = check_dims(dims);
   if (s != NATS_OK) return s;
   const Problem p = problem_of(dims);
@@ -360,9 +376,13 @@ nats_status nats_hybrid_bwd(const nats_dims* dims, const void* q, const void* k,
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return NATS_ERR_ALIGN;
   if (workspace_bytes < bwd_workspace_bytes(p)) return NATS_ERR_WORKSPACE;
-  return cuda_status(launch_hybrid_bwd(p, dims->dtype, q, k, v, g, beta, w_g, b_g, norm_w_soft, norm_w_lin, sel,
-                                       o_soft, o_lin, dout, dq, dk, dv, dg, dbeta, dw_g, db_g, dnorm_w_soft,
-                                       dnorm_w_lin, workspace, (cudaStream_t)stream));
+  const nats_status r = cuda_status(launch_hybrid_bwd(
+      p, dims->dtype, q, k, v, g, beta, w_g, b_g, norm_w_soft, norm_w_lin, sel, o_soft, o_lin, dout, dq, dk, dv, dg,
+      dbeta, dw_g, db_g, dnorm_w_soft, dnorm_w_lin, workspace, (cudaStream_t)stream, prof ? prof->start : nullptr,
+      prof ? prof->stop : nullptr, prof ? prof->stage_launches : nullptr));
+  if (prof)
+    for (int i = 0; i < NATS_BWD_NUM_STAGES; ++i) prof->launches += prof->stage_launches[i];
+  return r;
 }
 
 nats_status nats_decode_step(const nats_dims* dims, int64_t t, const void* q, const void* k, const void* v,

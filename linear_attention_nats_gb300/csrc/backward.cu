@@ -39,6 +39,7 @@
 //      the halves' column sums and scalars per token.
 #include <type_traits>
 
+#include "../../include/nats.h"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -636,8 +637,14 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
                               const float* nws, const float* nwl, const uint8_t* sel, const float* o_s,
                               const float* o_l, const void* dout, float* dq, float* dk, float* dv, float* dg,
                               float* dbeta, float* dw_g, float* db_g, float* dnws, float* dnwl, void* ws,
-                              cudaStream_t st) {
+                              cudaStream_t st, void* const* ev_start, void* const* ev_stop, int32_t* launches) {
   if (p.BH == 0 || p.L == 0) return cudaSuccess;
+  auto mark = [&](void* const* ev, int s) -> cudaError_t {
+    return (ev && ev[s]) ? cudaEventRecord((cudaEvent_t)ev[s], st) : cudaSuccess;
+  };
+  auto count = [&](int s, int n) {
+    if (launches) launches[s] += n;
+  };
   auto al = [](size_t b) { return (b + 255) & ~(size_t)255; };
   const long long rows = (long long)p.BH * p.L;
   const size_t dd = (size_t)p.d * p.d;
@@ -675,11 +682,16 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
     const T* kt = (const T*)k;
     const T* vt = (const T*)v;
     constexpr bool tc = std::is_same<T, __nv_bfloat16>::value;  // bf16: the softmax branch on tensor cores
+    cudaError_t e2 = mark(ev_start, NATS_BWD_STAGE_MERGE);
+    if (e2 != cudaSuccess) return e2;
     merge_bwd_kernel<T, D><<<(unsigned)(rows / kMergeRows), 256, 0, st>>>(
         qt, (const T*)dout, o_s, o_l, w_g, b_g, nws, nwl, p.H, p.L, p.eps, d_os, tc ? d_os16 : nullptr, d_ol,
         delta, dq, dw_g, db_g, dnws, dnwl);
+    count(NATS_BWD_STAGE_MERGE, 1);
+    if ((e2 = mark(ev_stop, NATS_BWD_STAGE_MERGE)) != cudaSuccess) return e2;
+    if ((e2 = mark(ev_start, NATS_BWD_STAGE_SOFTMAX)) != cudaSuccess) return e2;
     if (tc) {
-      const cudaError_t e2 = launch_softmax_bwd_mma(p, q, k, v, d_os16, delta, sel, lse, dq, dk, dv, st);
+      e2 = launch_softmax_bwd_mma(p, q, k, v, d_os16, delta, sel, lse, dq, dk, dv, st);
       if (e2 != cudaSuccess) return e2;
     } else {
       softmax_bwd_rows_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(qt, kt, vt, sel, d_os, delta,
@@ -687,14 +699,22 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
       softmax_bwd_keys_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
           qt, kt, vt, sel, d_os, delta, lse, rows, p.L, p.N, p.scale, dk, dv);
     }
+    count(NATS_BWD_STAGE_SOFTMAX, 2);
+    if ((e2 = mark(ev_stop, NATS_BWD_STAGE_SOFTMAX)) != cudaSuccess) return e2;
     constexpr int smem = GdnBwd<D>::kBytes;
     static const cudaError_t attr =
         cudaFuncSetAttribute(gdn_bwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (attr != cudaSuccess) return attr;
+    if ((e2 = mark(ev_start, NATS_BWD_STAGE_GDN)) != cudaSuccess) return e2;
     gdn_bwd_kernel<T, D><<<(unsigned)(p.BH * kRowSplit), kGdnThreads, smem, st>>>(
         qt, kt, vt, g, beta, sel, d_ol, p.L, p.N, p.scale, Sc, Tk, dSx, pcol, psc, dv);
+    count(NATS_BWD_STAGE_GDN, 1);
+    if ((e2 = mark(ev_stop, NATS_BWD_STAGE_GDN)) != cudaSuccess) return e2;
+    if ((e2 = mark(ev_start, NATS_BWD_STAGE_COMBINE)) != cudaSuccess) return e2;
     gdn_bwd_combine_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(kt, g, beta, pcol, psc, rows, p.scale,
                                                                             dq, dk, dg, dbeta);
+    count(NATS_BWD_STAGE_COMBINE, 1);
+    if ((e2 = mark(ev_stop, NATS_BWD_STAGE_COMBINE)) != cudaSuccess) return e2;
     return cudaGetLastError();
   };
   using bf = __nv_bfloat16;

@@ -59,14 +59,17 @@ cudaError_t launch_decode_step(const Problem& p, int dtype, long long t, const v
                                uint8_t* sel_out, float* o_s_out, float* o_l_out, int* err, cudaStream_t st);
 
 // Backward pass at a given selection (backward.cu): its scratch bytes, and
-// the launches (norm + merge, softmax rows, softmax keys, Gated DeltaNet).
+// the launches (norm + merge, softmax dq and dk / dv, Gated DeltaNet adjoint,
+// per-token combine).  ev_start / ev_stop (NATS_BWD_STAGE_* ids, entries may
+// be NULL) are recorded around each stage, launches[stage] counts its kernels.
 size_t bwd_workspace_bytes(const Problem& p);
 cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const void* k, const void* v,
                               const float* g, const float* beta, const float* w_g, const float* b_g,
                               const float* nws, const float* nwl, const uint8_t* sel, const float* o_s,
                               const float* o_l, const void* dout, float* dq, float* dk, float* dv, float* dg,
                               float* dbeta, float* dw_g, float* db_g, float* dnws, float* dnwl, void* ws,
-                              cudaStream_t st);
+                              cudaStream_t st, void* const* ev_start = nullptr, void* const* ev_stop = nullptr,
+                              int32_t* launches = nullptr);
 
 // Softmax branch of the backward pass on warp-level MMAs, bf16 layers
 // (backward_mma.cu): lse and dq (+=), then dk, dv (=).

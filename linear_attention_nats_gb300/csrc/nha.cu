@@ -504,6 +504,24 @@ __global__ void __launch_bounds__(256, 1)
             tc::mma_bf16(d_tmem, tc::desc_add(qd, off), tc::desc_add(kd, off), id_k, kk > 0);
           }
         };
+        // scores of regular block r (key block j0r + r, global key block g0r + r)
+        // into its S buffer, issued one block ahead of that block's P V so
+        // that the tensor pipe computes S_{r+1} while the softmax warps turn
+        // S_r into P_r
+        const int j0r = t.slots ? 1 : t.j0, nreg = t.nb - j0r;
+        int g0r = gk + (t.slots ? 1 : 0);
+        auto issue_s = [&](int r) -> bool {
+          const int g = g0r + r, ks = g % S::KS, b = r & 1;
+          // the buffer's previous P has been read by its product
+          if (ub[b] > 0 && !wait_at(bars, T_PVB + b, (ub[b] - 1) & 1, 2, err)) return false;
+          if (!wait_at(bars, T_KF + ks, (g / S::KS) & 1, 2, err)) return false;
+          tc::fence_after();
+          qk(tmem + (b ? kTR : kTZ), ks);
+          tc::mma_commit(&bars[T_SF + b]);
+          tc::mma_commit(&bars[T_KE + ks]);
+          return true;
+        };
+        int next_s = 0;  // regular blocks whose scores are issued
         if (t.slots) {
           const int ks = gk % S::KS;
           if (!(ok = wait_at(bars, T_SUF, sn & 1, 2, err))) break;
@@ -543,6 +561,12 @@ __global__ void __launch_bounds__(256, 1)
           tc::mma_commit(&bars[T_R]);
           tc::mma_commit(&bars[T_UE]);
           tc::mma_commit(&bars[T_GE]);
+          // Z's columns are free once the two products above have read P~
+          // (issue order): the next block's scores go there now
+          if (nreg > 0) {
+            if (!(ok = issue_s(0))) break;
+            next_s = 1;
+          }
           // O += (lower(R) + P_window) V of the first key block
           if (!(ok = wait_at(bars, T_A3, sn & 1, 2, err))) break;
           if (!(ok = wait_at(bars, T_VF + ks, (gk / S::KS) & 1, 2, err))) break;
@@ -555,21 +579,20 @@ __global__ void __launch_bounds__(256, 1)
           ++gk;
           ++sn;
         }
-        int r = 0;
-        for (int j = t.slots ? 1 : t.j0; j < t.nb && ok; ++j, ++r, ++gk) {
+        for (int r = 0; r < nreg && ok; ++r, ++gk) {
           const int ks = gk % S::KS, b = r & 1;
-          const uint32_t tb = tmem + (b ? kTR : kTZ);
-          // the buffer's previous P has been read by its product
-          if (ub[b] > 0 && !(ok = wait_at(bars, T_PVB + b, (ub[b] - 1) & 1, 2, err))) break;
-          if (!(ok = wait_at(bars, T_KF + ks, (gk / S::KS) & 1, 2, err))) break;
-          tc::fence_after();
-          qk(tb, ks);
-          tc::mma_commit(&bars[T_SF + b]);
-          tc::mma_commit(&bars[T_KE + ks]);
+          if (next_s == r) {
+            if (!(ok = issue_s(r))) break;
+            ++next_s;
+          }
+          if (r + 1 < nreg) {
+            if (!(ok = issue_s(r + 1))) break;
+            ++next_s;
+          }
           if (!(ok = wait_at(bars, T_PF + b, ub[b] & 1, 2, err))) break;
           if (!(ok = wait_at(bars, T_VF + ks, (gk / S::KS) & 1, 2, err))) break;
           tc::fence_after();
-          pv(tb, ks);
+          pv(tmem + (b ? kTR : kTZ), ks);
           tc::mma_commit(&bars[T_PVB + b]);
           tc::mma_commit(&bars[T_PV]);
           tc::mma_commit(&bars[T_VE + ks]);

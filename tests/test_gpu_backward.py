@@ -91,6 +91,45 @@ def test_backward_after_cuda_forward(B, H, L, d, dtype, seed):
     _compare(got, _oracle(inp, nws, nwl, dout, sel_ref), TOL[dtype], f"{dtype}-{d} (after the CUDA forward)")
 
 
+def test_backward_profiled_stages():
+    # nats_hybrid_bwd_profiled: the same per-token gradients bit for bit as
+    # without events (the weight gradients are sums taken with atomics, in
+    # no fixed order: equal to rounding), every stage's events recorded in
+    # order, and the launch count (merge, softmax dq, softmax dk / dv,
+    # adjoint scan, combine)
+    import linear_attention_nats_gb300 as nats
+    from linear_attention_nats_gb300 import _native, build
+
+    build.build()
+    inp, nws, nwl, dout = _case(1, 2, 256, 128, "bf16", 48)
+    t = to_device(inp)
+    nw = {"norm_w_soft": _dev(nws, "f32"), "norm_w_lin": _dev(nwl, "f32")}
+    fwd = nats.hybrid_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_s"], t["b_s"], t["w_g"], t["b_g"],
+                          return_sel=True, return_branches=True, **nw)
+    args = (t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_g"], t["b_g"], fwd["sel"], fwd["o_soft"], fwd["o_lin"],
+            _dev(dout, "bf16"))
+    plain = nats.hybrid_bwd(*args, **nw)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in _native.BWD_STAGES]
+    prof = _native.Profile()
+    for i, (a, b) in enumerate(ev):
+        a.record()  # materialise the event handles
+        b.record()
+        prof.start[i], prof.stop[i] = a.cuda_event, b.cuda_event
+    timed = nats.hybrid_bwd(*args, **nw, profile=prof)
+    torch.cuda.synchronize()
+    for n in GRADS[:5]:
+        assert torch.equal(plain[n], timed[n]), n
+    for n in GRADS[5:]:
+        assert torch.allclose(plain[n], timed[n], rtol=1e-5, atol=1e-5 * float(plain[n].abs().max())), n
+    assert list(prof.stage_launches)[:len(_native.BWD_STAGES)] == [1, 2, 1, 1]
+    assert prof.launches == 5
+    ms = [a.elapsed_time(b) for a, b in ev]
+    assert all(m > 0 for m in ms), ms
+    for (_, b), (a, _) in zip(ev, ev[1:]):  # stage i ends before stage i + 1 starts
+        assert b.elapsed_time(a) >= 0
+
+
 def test_backward_all_softmax_and_all_linear():
     # the two degenerate selections: every chunk softmax (no Gated DeltaNet
     # state survives a chunk), every chunk Gated DeltaNet (only the own chunk
