@@ -24,6 +24,14 @@ forward.  The selection is the forward's argmax (item 1): a discrete choice
 with no derivative; the pages state that the score layer is trained end to
 end but give no estimator for it, so its gradient is not part of this
 backward (the reading BWD-1).
+
+Opt-in (the reading BWD-2, `backward(..., w_s=, b_s=)`): a straight-through
+surrogate that lets the score layer learn.  With pi_c = softmax(s_c) over the
+chunk's two scores s_c = W_s[h] p_c + b_s[h] (p_c the chunk mean of [q; k],
+item 1) and sel_c the argmax, every output row of chunk c is multiplied by
+pi_c[sel_c] / pi_c[sel_c] held constant: the value is unchanged, and
+<dout, out> gains a gradient with respect to W_s, b_s and, through p_c, the
+chunk's q and k.
 """
 
 from __future__ import annotations
@@ -100,6 +108,34 @@ def forward_torch(x, sel, *, chunk=64, scale=0.0, eps=1e-6, prefix_k=None, prefi
     return torch.stack(outs), torch.stack(oss), torch.stack(ols)
 
 
+def score_probs(x, chunk=64):
+    """pi [B, H, N, 2]: the softmax over the two operation scores of every
+    chunk, s = W_s[h] p + b_s[h] with p the mean over the chunk's tokens of
+    [q_t ; k_t] (unscaled q; a partial last chunk pools the tokens it has)."""
+    q, k = x["q"], x["k"]
+    L = q.shape[2]
+    N = (L + chunk - 1) // chunk
+    pooled = torch.stack([torch.cat([q[:, :, c * chunk:(c + 1) * chunk].mean(2),
+                                     k[:, :, c * chunk:(c + 1) * chunk].mean(2)], dim=-1) for c in range(N)], dim=2)
+    s = torch.einsum("bhnf,hof->bhno", pooled, x["w_s"]) + x["b_s"][None, :, None, :]
+    return torch.softmax(s, dim=-1)
+
+
+def forward_st(x, sel, *, chunk=64, pi_bar=None, **kw):
+    """The straight-through surrogate of BWD-2: forward_torch's out with every
+    row of chunk c multiplied by pi_c[sel_c] / pi_bar_c, pi_bar the same
+    probability held constant (by default the one at x, so the value is
+    unchanged; a finite-difference check passes the unperturbed one).
+    Returns (out, o_s, o_l) like forward_torch."""
+    out, o_s, o_l = forward_torch(x, sel, chunk=chunk, **kw)
+    L = out.shape[2]
+    pi = score_probs(x, chunk)
+    chosen = pi.gather(-1, torch.as_tensor(np.asarray(sel, np.int64))[..., None])[..., 0]  # [B, H, N]
+    bar = chosen.detach() if pi_bar is None else torch.as_tensor(np.asarray(pi_bar, np.float64))
+    f = (chosen / bar).repeat_interleave(chunk, dim=-1)[..., :L]
+    return out * f[..., None], o_s, o_l
+
+
 def inputs64(q, k, v, g, beta, w_g, b_g=None, norm_w_soft=None, norm_w_lin=None):
     """float64 leaf tensors of the continuous inputs (absent bias / norm
     weights become zeros / ones)."""
@@ -113,15 +149,27 @@ def inputs64(q, k, v, g, beta, w_g, b_g=None, norm_w_soft=None, norm_w_lin=None)
 
 
 def backward(q, k, v, g, beta, w_g, b_g, sel, dout, *, norm_w_soft=None, norm_w_lin=None, chunk=64,
-             scale=0.0, eps=1e-6, prefix_k=None, prefix_v=None, state0=None):
+             scale=0.0, eps=1e-6, prefix_k=None, prefix_v=None, state0=None, w_s=None, b_s=None):
     """Gradients of <dout, out> at selection `sel`, float64 numpy arrays named
     as the inputs (dq, dk, dv [B, H, L, d]; dg, dbeta [B, H, L]; dw_g [H, d];
     db_g [H]; dnorm_w_soft, dnorm_w_lin [d]); also the forward's out, o_s, o_l.
-    prefix_k, prefix_v, state0: as for forward_torch (constants)."""
+    prefix_k, prefix_v, state0: as for forward_torch (constants).
+    With w_s [H, 2, 2d] (and b_s [H, 2], zero if absent): the BWD-2
+    surrogate (forward_st), which adds dw_s, db_s and the score layer's
+    share of dq, dk."""
     x = inputs64(q, k, v, g, beta, w_g, b_g, norm_w_soft, norm_w_lin)
-    out, o_s, o_l = forward_torch(x, np.asarray(sel), chunk=chunk, scale=scale, eps=eps, prefix_k=prefix_k,
-                                  prefix_v=prefix_v, state0=state0)
-    grads = torch.autograd.grad(out, [x[n] for n in NAMES], torch.as_tensor(np.asarray(dout, np.float64)))
-    res = {"d" + n: gr.detach().numpy() for n, gr in zip(NAMES, grads)}
+    kw = dict(chunk=chunk, scale=scale, eps=eps, prefix_k=prefix_k, prefix_v=prefix_v, state0=state0)
+    names = NAMES
+    if w_s is not None:
+        H = np.shape(w_s)[0]
+        x["w_s"] = torch.tensor(np.asarray(w_s, np.float64), requires_grad=True)
+        x["b_s"] = torch.tensor(np.zeros((H, 2)) if b_s is None else np.asarray(b_s, np.float64),
+                                requires_grad=True)
+        names = NAMES + ("w_s", "b_s")
+        out, o_s, o_l = forward_st(x, np.asarray(sel), **kw)
+    else:
+        out, o_s, o_l = forward_torch(x, np.asarray(sel), **kw)
+    grads = torch.autograd.grad(out, [x[n] for n in names], torch.as_tensor(np.asarray(dout, np.float64)))
+    res = {"d" + n: gr.detach().numpy() for n, gr in zip(names, grads)}
     res.update(out=out.detach().numpy(), o_s=o_s.detach().numpy(), o_l=o_l.detach().numpy())
     return res

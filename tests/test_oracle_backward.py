@@ -137,3 +137,105 @@ def test_last_chunk_from_its_prefix_and_state():
         for n in ("dq", "dk", "dv", "dg", "dbeta"):
             np.testing.assert_allclose(local[n], whole[n][:, h:h + 1, sl], rtol=1e-9, atol=1e-11, err_msg=n)
     assert len(n_prefix) == 2  # the heads retain different prefixes
+
+
+# ---- BWD-2: the straight-through surrogate of the score layer (opt-in) ----
+
+def _st_case(seed, L=192, d=16, H=2):
+    inp, sel, nws, nwl, b_g, dout = _case(seed, L=L, d=d, H=H)
+    rng = np.random.default_rng(seed + 2000)
+    w_s = 0.5 * rng.standard_normal((H, 2, 2 * d))
+    b_s = 0.3 * rng.standard_normal((H, 2))
+    return inp, sel, nws, nwl, b_g, dout, w_s, b_s
+
+
+def _pooled(inp, chunk=64):
+    q, k = inp.q.astype(np.float64), inp.k.astype(np.float64)
+    B, H, L, d = q.shape
+    N = L // chunk
+    return np.concatenate([q.reshape(B, H, N, chunk, d).mean(3), k.reshape(B, H, N, chunk, d).mean(3)], axis=-1)
+
+
+def test_st_surrogate_keeps_the_value_and_the_other_gradients():
+    inp, sel, nws, nwl, b_g, dout, w_s, b_s = _st_case(311)
+    args = _args(inp, nws, nwl, b_g)
+    plain = ob.backward(sel=sel, dout=dout, **args)
+    st = ob.backward(sel=sel, dout=dout, w_s=w_s, b_s=b_s, **args)
+    np.testing.assert_array_equal(st["out"], plain["out"])  # the factor is exactly one
+    for n in ("dv", "dg", "dbeta", "dw_g", "db_g", "dnorm_w_soft", "dnorm_w_lin"):
+        np.testing.assert_allclose(st[n], plain[n], rtol=1e-12, atol=1e-14, err_msg=n)
+
+
+def test_st_surrogate_closed_form():
+    # ds_c = G_c (e_sel - pi_c), G_c = sum over the chunk's tokens of <dout_t, out_t>;
+    # dW_s[h] = sum ds_c p_c^T, db_s[h] = sum ds_c; the chunk's tokens gain
+    # W_s[h]^T ds_c / 64 in (dq, dk) (the q half of p, then the k half)
+    inp, sel, nws, nwl, b_g, dout, w_s, b_s = _st_case(312)
+    args = _args(inp, nws, nwl, b_g)
+    plain = ob.backward(sel=sel, dout=dout, **args)
+    st = ob.backward(sel=sel, dout=dout, w_s=w_s, b_s=b_s, **args)
+    B, H, L, d = inp.q.shape
+    N = L // 64
+    p = _pooled(inp)                                                   # [B, H, N, 2d]
+    s = np.einsum("bhnf,hof->bhno", p, w_s) + b_s[None, :, None, :]
+    pi = np.exp(s - s.max(-1, keepdims=True))
+    pi /= pi.sum(-1, keepdims=True)
+    G = (dout * plain["out"]).reshape(B, H, N, 64, d).sum(axis=(3, 4))  # [B, H, N]
+    ds = G[..., None] * (np.eye(2)[sel.astype(np.int64)] - pi)          # [B, H, N, 2]
+    np.testing.assert_allclose(st["db_s"], ds.sum(axis=(0, 2)), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(st["dw_s"], np.einsum("bhno,bhnf->hof", ds, p), rtol=1e-10, atol=1e-12)
+    extra = np.einsum("bhno,hof->bhnf", ds, w_s) / 64                   # [B, H, N, 2d]
+    np.testing.assert_allclose(st["dq"] - plain["dq"], np.repeat(extra[..., :d], 64, axis=2), rtol=1e-8,
+                               atol=1e-10)
+    np.testing.assert_allclose(st["dk"] - plain["dk"], np.repeat(extra[..., d:], 64, axis=2), rtol=1e-8,
+                               atol=1e-10)
+
+
+@pytest.mark.parametrize("name", ("w_s", "b_s", "q", "k"))
+def test_st_gradient_matches_finite_differences(name):
+    # the surrogate's gradient is the derivative of its relaxed forward: out
+    # scaled per chunk by pi_sel(theta) / pi_sel(theta_0), the selection fixed
+    inp, sel, nws, nwl, b_g, dout, w_s, b_s = _st_case(313)
+    args = _args(inp, nws, nwl, b_g)
+    st = ob.backward(sel=sel, dout=dout, w_s=w_s, b_s=b_s, **args)
+    x = ob.inputs64(**args)
+    x["w_s"], x["b_s"] = torch.tensor(w_s), torch.tensor(b_s)
+    with torch.no_grad():
+        pi0 = ob.score_probs(x).gather(-1, torch.as_tensor(sel.astype(np.int64))[..., None])[..., 0].numpy()
+    rng = np.random.default_rng(17)
+    direction = torch.tensor(rng.standard_normal(tuple(x[name].shape)))
+    R = torch.tensor(dout)
+
+    def f(step):
+        y = {n: t.detach().clone() for n, t in x.items()}
+        y[name] = y[name] + step * direction
+        with torch.no_grad():
+            return float((ob.forward_st(y, sel, pi_bar=pi0)[0] * R).sum())
+
+    h = 1e-5
+    fd = (f(h) - f(-h)) / (2 * h)
+    an = float((torch.tensor(st["d" + name]) * direction).sum())
+    assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (name, fd, an)
+
+
+def test_st_planted_sign_error_fails_the_closed_form():
+    # a surrogate with the sign of (e_sel - pi) flipped, planted in the oracle
+    # on the CPU, is caught by the closed form's db_s
+    inp, sel, nws, nwl, b_g, dout, w_s, b_s = _st_case(314)
+    args = _args(inp, nws, nwl, b_g)
+    good = ob.backward(sel=sel, dout=dout, w_s=w_s, b_s=b_s, **args)
+    orig = ob.forward_st
+
+    def flipped(x, sel_, *, chunk=64, pi_bar=None, **kw):
+        out, o_s, o_l = ob.forward_torch(x, sel_, chunk=chunk, **kw)
+        pi = ob.score_probs(x, chunk)
+        chosen = pi.gather(-1, torch.as_tensor(np.asarray(sel_, np.int64))[..., None])[..., 0]
+        f = (chosen.detach() / chosen).repeat_interleave(chunk, dim=-1)  # inverted factor
+        return out * f[..., None], o_s, o_l
+
+    ob.forward_st = flipped
+    try:
+        bad = ob.backward(sel=sel, dout=dout, w_s=w_s, b_s=b_s, **args)
+    finally:
+        ob.forward_st = orig
+    assert not np.allclose(bad["db_s"], good["db_s"], rtol=1e-6)
