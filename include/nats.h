@@ -399,6 +399,31 @@ nats_status nats_hybrid_bwd_profiled(const nats_dims* dims, const void* q, const
                                      float* dnorm_w_soft, float* dnorm_w_lin, void* workspace,
                                      size_t workspace_bytes, nats_stream_t stream, nats_profile* prof);
 
+/* The score layer's gradient, opt-in ("Kernmechanismen" item 5: the score
+ * layer is trained end to end; the pages name no estimator, and
+ * nats_hybrid_bwd gives W_s, b_s none).  This call adds a straight-through
+ * surrogate (the reading BWD-2): every output row of chunk c is read as
+ * scaled by pi_c[sel_c] / (that probability held constant), pi_c the softmax
+ * of the chunk's two scores s_c = W_s[h] p_c + b_s[h] (p_c the chunk mean of
+ * [q ; k], unscaled q) and sel_c the forward's argmax.  The value does not
+ * change; with G_c = sum over the chunk's tokens of <dout_t, out_t> and
+ * ds_c = G_c (e_sel - pi_c) it writes
+ *   dw_s[h] = sum_{b, c} ds_c p_c^T  [H, 2, 2d] fp32,  db_s[h] = sum ds_c  [H, 2] fp32
+ * (overwritten) and ADDS (W_s[h]^T ds_c) / 64 to dq (first d entries) and dk
+ * (last d) of each token of the chunk.  Call it after nats_hybrid_bwd on the
+ * same dq, dk to get the surrogate's full gradient.
+ * q, k, out, dout [B, H, L, d] in the layer dtype (out: the forward's
+ * output); w_s [H, 2, 2d], b_s [H, 2] (or NULL: zero) fp32; sel [B, H,
+ * L / 64] the forward's selection; dq, dk [B, H, L, d] fp32.  All pointers
+ * device, q, k, out, dout, dq, dk 16-byte aligned; asynchronous on
+ * `stream`; dw_s, db_s are sums taken with atomics (their rounding order is
+ * not fixed).  Errors before any launch: NATS_ERR_NULL, NATS_ERR_SHAPE /
+ * NATS_ERR_UNSUPPORTED / NATS_ERR_DTYPE / NATS_ERR_VALUE (dims),
+ * NATS_ERR_ALIGN; NATS_ERR_CUDA on a failed launch. */
+nats_status nats_score_bwd(const nats_dims* dims, const void* q, const void* k, const float* w_s, const float* b_s,
+                           const uint8_t* sel, const void* out, const void* dout, float* dq, float* dk, float* dw_s,
+                           float* db_s, nats_stream_t stream);
+
 /* -------------------------------------------------------------------- NHA
  * Native Hybrid Attention, the related layer of "Native Hybrid Attention
  * for Efficient Sequence Modeling" (section "2. Methodologie",
@@ -444,7 +469,8 @@ nats_status nats_nha_fwd(const nats_nha_dims* dims, const void* q, const void* k
                          nats_stream_t stream);
 nats_status nats_nha_workspace_check(const nats_nha_dims* dims, const void* workspace, nats_stream_t stream);
 /* nats_nha_fwd with caller-owned CUDA events recorded around its kernels
- * (prof may be NULL): start[0] / stop[0] around the slot-memory scan (not
+ * (prof may be NULL): start[0] / stop[0] around the slot-memory stage (the
+ * chunk-parallel gate factors, then the slot-memory scan: two kernels, not
  * launched when w >= L; stage_launches[0] then 0), start[1] / stop[1] around
  * the attention kernel; `launches` counts the kernels launched. */
 nats_status nats_nha_fwd_profiled(const nats_nha_dims* dims, const void* q, const void* k, const void* v,

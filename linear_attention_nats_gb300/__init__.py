@@ -229,6 +229,29 @@ def hybrid_bwd(q, k, v, g, beta, w_g, b_g, sel, o_soft, o_lin, dout, *, norm_w_s
     return res
 
 
+def score_bwd(q, k, w_s, b_s, sel, out, dout, grads, *, stream=None):
+    """The score layer's gradient under the straight-through surrogate
+    (nats_score_bwd, reading BWD-2), after hybrid_bwd: `grads` is
+    hybrid_bwd's dict; its dq, dk gain the score layer's share in place and
+    it gains dw_s [H, 2, 2d] and db_s [H, 2].  out: the forward's output."""
+    _req(q, "q")
+    B, H, L, d = q.shape
+    for name, t in (("k", k), ("out", out), ("dout", dout)):
+        _req(t, name, q.dtype, q.shape)
+    _req(w_s, "w_s", torch.float32, (H, 2, 2 * d))
+    _req(b_s, "b_s", torch.float32, (H, 2))
+    _req(sel, "sel", torch.uint8, (B, H, L // 64))
+    for name in ("dq", "dk"):
+        _req(grads[name], name, torch.float32, (B, H, L, d))
+    f32 = dict(dtype=torch.float32, device=q.device)
+    grads["dw_s"] = torch.empty((H, 2, 2 * d), **f32)
+    grads["db_s"] = torch.empty((H, 2), **f32)
+    check(_native.lib.nats_score_bwd(
+        ctypes.byref(dims(B, H, L, d, _dtype_code(q))), _p(q), _p(k), _p(w_s), _p(b_s), _p(sel), _p(out), _p(dout),
+        _p(grads["dq"]), _p(grads["dk"]), _p(grads["dw_s"]), _p(grads["db_s"]), _stream(stream)), "nats_score_bwd")
+    return grads
+
+
 class DecodeState:
     """Device state of the layer in decode mode (nats_decode_state): the
     Gated DeltaNet state S and its chunk-start copy S0 (fp32 [B, H, d, d]), the

@@ -385,6 +385,20 @@ nats_status nats_hybrid_bwd_profiled(const nats_dims* dims, const void* q, const
   return r;
 }
 
+nats_status nats_score_bwd(const nats_dims* dims, const void* q, const void* k, const float* w_s, const float* b_s,
+                           const uint8_t* sel, const void* out, const void* dout, float* dq, float* dk, float* dw_s,
+                           float* db_s, nats_stream_t stream) {
+  nats_status s = check_dims(dims);
+  if (s != NATS_OK) return s;
+  const Problem p = problem_of(dims);
+  if (!q || !k || !w_s || !sel || !out || !dout || !dq || !dk || !dw_s || !db_s) return NATS_ERR_NULL;
+  const void* ptrs[] = {q, k, out, dout, dq, dk};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return NATS_ERR_ALIGN;
+  return cuda_status(launch_score_bwd(p, dims->dtype, q, k, w_s, b_s, sel, out, dout, dq, dk, dw_s, db_s,
+                                      (cudaStream_t)stream));
+}
+
 nats_status nats_decode_step(const nats_dims* dims, int64_t t, const void* q, const void* k, const void* v,
                              const float* g, const float* beta, const float* w_s, const float* b_s,
                              const float* w_g, const float* b_g, const float* norm_w_soft,

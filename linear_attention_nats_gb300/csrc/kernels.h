@@ -71,6 +71,13 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
                               cudaStream_t st, void* const* ev_start = nullptr, void* const* ev_stop = nullptr,
                               int32_t* launches = nullptr);
 
+// The score layer's gradient under the straight-through surrogate
+// (score_bwd.cu): zeroes dw_s, db_s, then sums into them and adds the score
+// layer's share into dq, dk.
+cudaError_t launch_score_bwd(const Problem& p, int dtype, const void* q, const void* k, const float* w_s,
+                             const float* b_s, const uint8_t* sel, const void* out, const void* dout, float* dq,
+                             float* dk, float* dw_s, float* db_s, cudaStream_t st);
+
 // Softmax branch of the backward pass on warp-level MMAs, bf16 layers
 // (backward_mma.cu): lse and dq (+=), then dk, dv (=).
 cudaError_t launch_softmax_bwd_mma(const Problem& p, const void* q, const void* k, const void* v, const void* dos,

@@ -248,3 +248,19 @@ def test_nha_validation(nat):
     assert call(d(1, 2, 512), [None] + ok_ptrs[1:]) == 1
     assert call(d(1, 2, 512), [P(0x10000004)] + ok_ptrs[1:]) == 4
     assert call(d(1, 2, 512), nbytes=16) == 5
+
+
+def test_score_bwd_validation(nat):
+    """nats_score_bwd rejects bad arguments on the host, before any launch."""
+    P = lambda a: ctypes.c_void_p(a)
+    ok = [P(0x10000000)] * 11  # q, k, w_s, b_s, sel, out, dout, dq, dk, dw_s, db_s
+
+    def call(dm, ptrs=ok):
+        return nat.lib.nats_score_bwd(ctypes.byref(dm), *ptrs, None)
+
+    assert call(nat.dims(1, 2, 500, 128, 0)) == 2  # L % 64
+    assert call(nat.dims(1, 2, 512, 96, 0)) == 6  # head size
+    for i in (0, 1, 2, 4, 5, 6, 7, 8, 9, 10):  # every pointer but b_s is required
+        assert call(nat.dims(1, 2, 512, 128, 0), ok[:i] + [None] + ok[i + 1:]) == 1, i
+    for i in (0, 1, 5, 6, 7, 8):  # q, k, out, dout, dq, dk 16-byte aligned
+        assert call(nat.dims(1, 2, 512, 128, 0), ok[:i] + [P(0x10000004)] + ok[i + 1:]) == 4, i

@@ -188,3 +188,43 @@ def test_backward_full_size_last_chunk():
               + " ".join(f"{n}={e:.1e}" for n, e in errs.items()))
         for n, e in errs.items():
             assert e <= TOL["bf16"], (n, e)
+
+
+@pytest.mark.parametrize("B,H,L,d,dtype,seed", [(1, 2, 256, 64, "f32", 61), (2, 2, 704, 128, "bf16", 62)])
+def test_score_layer_gradient(B, H, L, d, dtype, seed):
+    # nats_score_bwd after nats_hybrid_bwd: the straight-through surrogate's
+    # gradient (reading BWD-2) against the oracle's, on the oracle's
+    # activations, with the selection the score layer's own argmax; 704
+    # tokens leave a partial group of chunks in the last CTA
+    import linear_attention_nats_gb300 as nats
+    from linear_attention_nats_gb300 import build
+
+    build.build()
+    inp, nws, nwl, dout = _case(B, H, L, d, dtype, seed)
+    rng = np.random.default_rng(seed + 700)
+    w_s = (0.5 * rng.standard_normal((H, 2, 2 * d))).astype(np.float32)
+    b_s = (0.1 * rng.standard_normal((H, 2))).astype(np.float32)
+    sel = oracle.select(inp.q, inp.k, w_s, b_s)[0]
+    assert 0 < sel.mean() < 1  # both operations chosen somewhere
+    ref = ob.backward(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.w_g, inp.b_g, sel, dout,
+                      norm_w_soft=nws, norm_w_lin=nwl, w_s=w_s, b_s=b_s)
+    t = to_device(inp)
+    sel_d = torch.from_numpy(sel).cuda()
+    dout_d = _dev(dout, dtype)
+    grads = nats.hybrid_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_g"], t["b_g"], sel_d,
+                            _dev(ref["o_s"], "f32"), _dev(ref["o_l"], "f32"), dout_d,
+                            norm_w_soft=_dev(nws, "f32"), norm_w_lin=_dev(nwl, "f32"))
+    before = {n: grads[n].clone() for n in ("dq", "dk")}
+    nats.score_bwd(t["q"], t["k"], _dev(w_s, "f32"), _dev(b_s, "f32"), sel_d, _dev(ref["out"], dtype), dout_d,
+                   grads)
+    torch.cuda.synchronize()
+    errs = {n: rel_err(grads[n].cpu().numpy(), ref[n]) for n in ("dq", "dk", "dw_s", "db_s")}
+    # the score layer's share alone (what the call added), against the
+    # oracle's surrogate minus its plain backward
+    plain = ob.backward(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.w_g, inp.b_g, sel, dout,
+                        norm_w_soft=nws, norm_w_lin=nwl)
+    for n in ("dq", "dk"):
+        errs[n + "_share"] = rel_err((grads[n] - before[n]).cpu().numpy(), ref[n] - plain[n])
+    print(f"[parity] score-layer surrogate {dtype}-{d}: " + " ".join(f"{n}={e:.1e}" for n, e in errs.items()))
+    for n, e in errs.items():
+        assert e <= TOL[dtype], (n, e)
