@@ -25,10 +25,14 @@
 // chunks S0 <- e^{A_63} (.) S0 + Gamma^T K, Gamma[i, s] = (1 - alpha_i)
 // e^{A_63 - A_i} <= 1.
 //
-// Two kernels.
-//   nha_state_kernel: one CTA per (b, h) walks the chunks in order with the
-//     slot memory transposed in TMEM (lane = feature) and writes, per chunk,
-//     S0''^T, V0''^T (bf16 [d][m]), G' (bf16 [C][m]) and E' (fp32 [C][m]).
+// Three kernels.
+//   nha_gate_kernel: chunk-parallel; from the log-gates of each chunk it
+//     writes G' (bf16 [C][m]), E' (fp32 [C][m]), Gamma (bf16 [C][m]) and the
+//     per-slot e^{A_r}, e^{A_63}.
+//   nha_state_kernel: two CTAs per (b, h), one per memory (K~, V~), walk the
+//     chunks in order with the slot memory in registers (thread = feature);
+//     the tensor cores form each chunk's write X^T Gamma ahead of them; per
+//     chunk they store S0''^T, V0''^T (bf16 [d][m]).
 //   nha_attn_kernel: persistent CTAs over tiles of 128 query rows (two
 //     chunks of one head).  The first key block (the two write chunks) runs
 //     the slot terms and that block's window keys in one online softmax;
@@ -60,47 +64,116 @@ __device__ __forceinline__ uint32_t sw128(int line, int col_bf16) {
   return (uint32_t)(line * 128 + ((((col_bf16 >> 3) ^ (line & 7))) << 4) + (col_bf16 & 7) * 2);
 }
 
+// ============================================================ gate factors
+// Chunk-parallel: one CTA per chunk of the write stream turns its log-gates
+// into the factors the scan and the attention read.  Thread (part, s) forms
+// the running sum of slot s over tokens 16 part .. 16 part + 15, the four
+// parts' totals give each its offset, and every thread then writes four
+// (token, slot-quad) groups of E', G' and Gamma.
+__global__ void __launch_bounds__(256) nha_gate_kernel(const float* __restrict__ log_alpha,
+                                                       __nv_bfloat16* __restrict__ gh_out,
+                                                       float* __restrict__ ep_out,
+                                                       __nv_bfloat16* __restrict__ gam_out,
+                                                       float* __restrict__ er_out) {
+  __shared__ __align__(16) float lam[C * MS];
+  __shared__ __align__(16) float A[C * MS];
+  __shared__ float tot[4][MS];
+  const size_t chunk = blockIdx.x;
+  const int tid = threadIdx.x;
+  const size_t base = chunk * C * MS;
+  {
+    const float4* src = (const float4*)(log_alpha + base);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) ((float4*)lam)[tid + 256 * j] = src[tid + 256 * j];
+  }
+  __syncthreads();
+  const int sl = tid & 63, part = tid >> 6;
+  float acc = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int i = 16 * part + j;
+    acc += lam[i * MS + sl];
+    A[i * MS + sl] = acc;
+  }
+  tot[part][sl] = acc;
+  __syncthreads();
+  float off = 0.f;
+  for (int p2 = 0; p2 < part; ++p2) off += tot[p2][sl];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) A[(16 * part + j) * MS + sl] += off;
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e4 = tid + 256 * j;  // group of four slots
+    const int i = e4 >> 4, s0 = (e4 & 15) * 4;
+    float ep[4], gh[4], gm[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int sx = s0 + x;
+      const float Ai = A[i * MS + sx], Ar = A[31 * MS + sx], A63 = A[63 * MS + sx];
+      const float om = -expm1f(lam[i * MS + sx]);  // 1 - alpha_i, without cancellation
+      ep[x] = __expf(Ai - Ar);
+      gh[x] = om * __expf(Ar - Ai);
+      gm[x] = om * __expf(A63 - Ai);
+      if (i == 0) {
+        er_out[chunk * 2 * MS + sx] = __expf(Ar);
+        er_out[chunk * 2 * MS + MS + sx] = __expf(A63);
+      }
+    }
+    *(float4*)(ep_out + base + 4 * e4) = make_float4(ep[0], ep[1], ep[2], ep[3]);
+    *(uint2*)(gh_out + base + 4 * e4) = make_uint2(tc::pack_bf16x2(gh[0], gh[1]), tc::pack_bf16x2(gh[2], gh[3]));
+    *(uint2*)(gam_out + base + 4 * e4) = make_uint2(tc::pack_bf16x2(gm[0], gm[1]), tc::pack_bf16x2(gm[2], gm[3]));
+  }
+}
+
 // ============================================================ state scan
-// smem: stages (K tile, V tile, lambda) x 2; Gamma x 2; the cumulative sums
-// A; per-slot e^{A_r}, e^{A_63} x 2.
+// One CTA per (b, h, memory): memory 0 is the key slots K~, 1 the value
+// slots V~ (independent recurrences of the same gates).  The slot memory of
+// the CTA, transposed (feature r x 64 slots), lives in the registers of
+// state thread r.  Per chunk the tensor cores form the chunk's write
+// X^T Gamma (M = 128 features, N = 64 slots, K = 64 tokens) into one of two
+// TMEM buffers with no dependence on the state, so they run ahead of the
+// state threads, whose chain per chunk is: store the chunk-start memory
+// scaled by e^{A_r} (bf16), then S <- e^{A_63} S + X^T Gamma.
 struct StSmem {
-  static constexpr int kKV = C * D * 2;                  // 16 KiB (two 8 KiB feature halves)
-  static constexpr int kLam = C * MS * 4;                // 16 KiB
-  static constexpr int kStage = 2 * kKV + kLam;          // 48 KiB
-  static constexpr int offStage = 0;
-  static constexpr int offGam = 2 * kStage;              // 2 x 8 KiB
-  static constexpr int offA = offGam + 2 * C * MS * 2;   // fp32 [C][MS]
-  static constexpr int offE = offA + C * MS * 4;         // fp32 [2][2][MS]: e^{A_r}, e^{A_63}
-  static constexpr int offBar = offE + 2 * 2 * MS * 4;
-  static constexpr int kNumBars = 12;
+  static constexpr int kX = C * D * 2;                  // 16 KiB token tile (two 8 KiB feature halves)
+  static constexpr int kG = C * MS * 2;                 // 8 KiB Gamma (TMA, 128-byte swizzle)
+  static constexpr int kE = 2 * MS * 4;                 // e^{A_r}, e^{A_63}
+  static constexpr int kStage = kX + kG + 1024;         // 1 KiB aligned
+  static constexpr int kStages = 4;
+  static constexpr int offBar = kStages * kStage;
+  static constexpr int kNumBars = 2 * kStages + 5;
   static constexpr int offTmem = offBar + kNumBars * 8;
   static constexpr int kBytes = offTmem + 16 + 1024;
+  static_assert(kX + kG + kE <= kStage, "stage");
 };
-enum { A_FULL = 0, A_EMPTY = 2, A_GATE = 4, A_GEMPTY = 6, A_STATE = 8, A_MMA = 9, A_DONE = 10 };
+enum { B_FULL = 0, B_EMPTY = StSmem::kStages, B_DFULL = 2 * StSmem::kStages, B_DEMPTY = B_DFULL + 2,
+       B_DONE = B_DEMPTY + 2 };
 
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(192, 1)
     nha_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                     const float* __restrict__ log_alpha, int L, int N, __nv_bfloat16* __restrict__ st_out,
-                     __nv_bfloat16* __restrict__ ut_out, __nv_bfloat16* __restrict__ gh_out,
-                     float* __restrict__ ep_out, int* __restrict__ err) {
+                     const __grid_constant__ CUtensorMap tm_gam, const float* __restrict__ er, int L, int N,
+                     __nv_bfloat16* __restrict__ st_out, __nv_bfloat16* __restrict__ ut_out, int* __restrict__ err) {
   using S = StSmem;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + S::offBar);
   uint32_t* tmem_slot = (uint32_t*)(smem + S::offTmem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long bh = blockIdx.x;
+  const long long bh = blockIdx.x >> 1;
+  const int mem = blockIdx.x & 1;  // 0: key slots, 1: value slots
+  const CUtensorMap* tm_x = mem ? &tm_v : &tm_k;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(&bars[A_FULL + s], 1);
-      tc::mbar_init(&bars[A_EMPTY + s], 1 + 4);  // the MMA's commit + the four gate warps
-      tc::mbar_init(&bars[A_GATE + s], 4);
-      tc::mbar_init(&bars[A_GEMPTY + s], 1);
+    for (int s = 0; s < S::kStages; ++s) {
+      tc::mbar_init(&bars[B_FULL + s], 1);
+      tc::mbar_init(&bars[B_EMPTY + s], 1 + 4);  // the MMA's commit + the four state warps (they read E)
     }
-    tc::mbar_init(&bars[A_STATE], 4);
-    tc::mbar_init(&bars[A_MMA], 1);
-    tc::mbar_init(&bars[A_DONE], 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&bars[B_DFULL + b], 1);
+      tc::mbar_init(&bars[B_DEMPTY + b], 4);
+    }
+    tc::mbar_init(&bars[B_DONE], 1);
     tc::fence_barrier_init();
   }
   if (warp == 1) {
@@ -110,155 +183,94 @@ __global__ void __launch_bounds__(384, 1)
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  const uint32_t tmem = *tmem_slot;  // columns 0-63: S^T, 64-127: V~^T (lane = feature)
+  const uint32_t tmem = *tmem_slot;  // columns 64 b .. 64 b + 63: the write of chunks c = b (mod 2)
 
   if (warp == 0) {
     if (lane == 0) {
-      tc::prefetch_tensormap(&tm_k);
-      tc::prefetch_tensormap(&tm_v);
+      tc::prefetch_tensormap(tm_x);
+      tc::prefetch_tensormap(&tm_gam);
       bool ok = true;
       for (int c = 0; c < N && ok; ++c) {
-        const int s = c & 1;
-        if (!(ok = tc::mbar_wait(&bars[A_EMPTY + s], ((c >> 1) & 1) ^ 1, err))) break;
-        uint8_t* st = smem + S::offStage + s * S::kStage;
+        const int s = c % S::kStages;
+        if (!(ok = tc::mbar_wait(&bars[B_EMPTY + s], ((c / S::kStages) & 1) ^ 1, err))) break;
+        uint8_t* st = smem + s * S::kStage;
         const int row = (int)(bh * L + (long long)c * C);
-        tc::mbar_arrive_expect_tx(&bars[A_FULL + s], S::kStage);
-        for (int hh = 0; hh < 2; ++hh) {
-          tc::tma_load_2d(st + hh * 8192, &tm_k, 64 * hh, row, &bars[A_FULL + s]);
-          tc::tma_load_2d(st + S::kKV + hh * 8192, &tm_v, 64 * hh, row, &bars[A_FULL + s]);
-        }
-        tc::bulk_load_1d(st + 2 * S::kKV, log_alpha + (size_t)row * MS, S::kLam, &bars[A_FULL + s]);
+        const long long ch = bh * N + c;
+        tc::mbar_arrive_expect_tx(&bars[B_FULL + s], S::kX + S::kG + S::kE);
+        tc::tma_load_2d(st, tm_x, 0, row, &bars[B_FULL + s]);
+        tc::tma_load_2d(st + 8192, tm_x, 64, row, &bars[B_FULL + s]);
+        tc::tma_load_2d(st + S::kX, &tm_gam, 0, (int)(ch * C), &bars[B_FULL + s]);
+        tc::bulk_load_1d(st + S::kX + S::kG, er + ch * 2 * MS, S::kE, &bars[B_FULL + s]);
       }
-      for (int s = 0; s < 2; ++s) {
-        const int uses = N > s ? (N - 1 - s) / 2 + 1 : 0;
-        if (uses > 0) {
-          tc::mbar_wait(&bars[A_FULL + s], (uses - 1) & 1, nullptr);
-          if (ok) tc::mbar_wait(&bars[A_EMPTY + s], (uses - 1) & 1, err);
-        }
+      // every copy issued has landed before the CTA may exit
+      for (int s = 0; s < S::kStages; ++s) {
+        const int uses = N > s ? (N - 1 - s) / S::kStages + 1 : 0;
+        if (uses > 0) tc::mbar_wait(&bars[B_FULL + s], (uses - 1) & 1, nullptr);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // S^T += K^T Gamma and V~^T += V^T Gamma: M = 128 features (A read
-      // feature-major from the staged token tiles), N = 64 slots, K = 64 tokens
+      // D[feature, slot] = sum_i X[i, feature] Gamma[i, slot]: A = X^T read
+      // feature-major from the token tile, B = Gamma slot-major
       constexpr uint32_t idesc = tc::idesc_bf16_f32(128, MS, true, true);
       const uint32_t s0 = tc::smem_u32(smem);
       bool ok = true;
       for (int c = 0; c < N && ok; ++c) {
-        const int s = c & 1;
-        if (!(ok = tc::mbar_wait(&bars[A_FULL + s], (c >> 1) & 1, err))) break;
-        if (!(ok = tc::mbar_wait(&bars[A_GATE + s], (c >> 1) & 1, err))) break;
-        if (!(ok = tc::mbar_wait(&bars[A_STATE], c & 1, err))) break;
+        const int s = c % S::kStages, b = c & 1;
+        if (!(ok = tc::mbar_wait(&bars[B_FULL + s], (c / S::kStages) & 1, err))) break;
+        if (c >= 2 && !(ok = tc::mbar_wait(&bars[B_DEMPTY + b], ((c - 2) >> 1) & 1, err))) break;
         tc::fence_after();
-        const uint32_t kb = s0 + S::offStage + s * S::kStage;
-        const uint64_t kd = tc::smem_desc_sw128(kb, 8192, 1024);
-        const uint64_t vd = tc::smem_desc_sw128(kb + S::kKV, 8192, 1024);
-        const uint64_t gd = tc::smem_desc_sw128(s0 + S::offGam + s * C * MS * 2, 8192, 1024);
+        const uint32_t xb = s0 + s * S::kStage;
+        const uint64_t xd = tc::smem_desc_sw128(xb, 8192, 1024);
+        const uint64_t gd = tc::smem_desc_sw128(xb + S::kX, 8192, 1024);
 #pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk) {
-          tc::mma_bf16(tmem, tc::desc_add(kd, kk * 2048), tc::desc_add(gd, kk * 2048), idesc, 1);
-          tc::mma_bf16(tmem + MS, tc::desc_add(vd, kk * 2048), tc::desc_add(gd, kk * 2048), idesc, 1);
-        }
-        tc::mma_commit(&bars[A_EMPTY + s]);
-        tc::mma_commit(&bars[A_GEMPTY + s]);
-        tc::mma_commit(&bars[A_MMA]);
+        for (int kk = 0; kk < C / 16; ++kk)
+          tc::mma_bf16(tmem + MS * b, tc::desc_add(xd, kk * 2048), tc::desc_add(gd, kk * 2048), idesc, kk > 0);
+        tc::mma_commit(&bars[B_DFULL + b]);
+        tc::mma_commit(&bars[B_EMPTY + s]);
       }
-      tc::mma_commit(&bars[A_DONE]);
-      tc::mbar_wait(&bars[A_DONE], 0, nullptr);
+      tc::mma_commit(&bars[B_DONE]);
+      tc::mbar_wait(&bars[B_DONE], 0, nullptr);
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ---- state warps: thread r owns feature r (TMEM lane r)
-    const int r = threadIdx.x - 128;
+  } else {
+    // ---- state warps 2..5: thread r owns feature r (TMEM lane r)
+    const int r = 32 * (warp & 3) + lane;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-    const float* ef = (const float*)(smem + S::offE);
-    {
-      float z[32];
+    __nv_bfloat16* outp = mem ? ut_out : st_out;
+    float sm[MS];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) z[i] = 0.f;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) tc::tmem_st32(tmem + lane_off + 32 * ch, z);
-      tc::tmem_st_wait();
-    }
+    for (int x = 0; x < MS; ++x) sm[x] = 0.f;
     bool ok = true;
     for (int c = 0; c < N && ok; ++c) {
-      const int s = c & 1;
-      if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[A_GATE + s], (c >> 1) & 1, err)))) break;
-      if (c > 0 && !(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[A_MMA], (c - 1) & 1, err)))) break;
-      tc::fence_after();
-      const float* er = ef + s * 2 * MS;  // e^{A_r} per slot, then e^{A_63}
-      const size_t orow = ((size_t)bh * N + c) * D + r;
-#pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        __nv_bfloat16* dst = (which == 0 ? st_out : ut_out) + orow * MS;
+      const int s = c % S::kStages, b = c & 1;
+      if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_FULL + s], (c / S::kStages) & 1, err)))) break;
+      const float* ef = (const float*)(smem + s * S::kStage + S::kX + S::kG);  // e^{A_r} [MS], e^{A_63} [MS]
+      // the chunk-start memory, scaled by e^{A_r}: row r of [D][MS]
+      {
+        uint4* dst = (uint4*)(outp + ((size_t)(bh * N + c) * D + r) * MS);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float v[32];
-          const uint32_t ta = tmem + lane_off + which * MS + 32 * half;
-          tc::tmem_ld32(ta, v);
-          tc::tmem_ld_wait();
-          uint4 pk[4];
-          uint32_t* p32 = (uint32_t*)pk;
-#pragma unroll
-          for (int x = 0; x < 16; ++x)
-            p32[x] = tc::pack_bf16x2(v[2 * x] * er[32 * half + 2 * x], v[2 * x + 1] * er[32 * half + 2 * x + 1]);
-#pragma unroll
-          for (int x = 0; x < 4; ++x) ((uint4*)(dst + 32 * half))[x] = pk[x];
-#pragma unroll
-          for (int x = 0; x < 32; ++x) v[x] *= er[MS + 32 * half + x];
-          tc::tmem_st32(ta, v);
+        for (int x8 = 0; x8 < MS / 8; ++x8) {
+          uint4 pk;
+          pk.x = tc::pack_bf16x2(sm[8 * x8] * ef[8 * x8], sm[8 * x8 + 1] * ef[8 * x8 + 1]);
+          pk.y = tc::pack_bf16x2(sm[8 * x8 + 2] * ef[8 * x8 + 2], sm[8 * x8 + 3] * ef[8 * x8 + 3]);
+          pk.z = tc::pack_bf16x2(sm[8 * x8 + 4] * ef[8 * x8 + 4], sm[8 * x8 + 5] * ef[8 * x8 + 5]);
+          pk.w = tc::pack_bf16x2(sm[8 * x8 + 6] * ef[8 * x8 + 6], sm[8 * x8 + 7] * ef[8 * x8 + 7]);
+          dst[x8] = pk;
         }
       }
-      tc::tmem_st_wait();
+      if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[B_DFULL + b], (c >> 1) & 1, err)))) break;
+      tc::fence_after();
+      float w[MS];
+      tc::tmem_ld32(tmem + lane_off + MS * b, *reinterpret_cast<float(*)[32]>(&w[0]));
+      tc::tmem_ld32(tmem + lane_off + MS * b + 32, *reinterpret_cast<float(*)[32]>(&w[32]));
+      tc::tmem_ld_wait();
+#pragma unroll
+      for (int x = 0; x < MS; ++x) sm[x] = fmaf(sm[x], ef[MS + x], w[x]);
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&bars[A_STATE]);
-    }
-    if (ok && N > 0) __all_sync(0xffffffffu, tc::mbar_wait(&bars[A_MMA], (N - 1) & 1, err));
-  } else if (warp >= 8) {
-    // ---- gate warps: cumulative log-gates, E', G' (global) and Gamma (smem)
-    const int gt = threadIdx.x - 256;  // 0..127
-    float* A = (float*)(smem + S::offA);
-    bool ok = true;
-    for (int c = 0; c < N && ok; ++c) {
-      const int s = c & 1;
-      // the four warps decide together (barrier reduction), so that none is
-      // left waiting at a named barrier the others skipped
-      if (!(ok = tc::group_all(1, 128, tc::mbar_wait(&bars[A_FULL + s], (c >> 1) & 1, err)))) break;
-      if (!(ok = tc::group_all(1, 128, tc::mbar_wait(&bars[A_GEMPTY + s], ((c >> 1) & 1) ^ 1, err)))) break;
-      const float* lam = (const float*)(smem + S::offStage + s * S::kStage + 2 * S::kKV);
-      if (gt < MS) {
-        float x[C];
-#pragma unroll
-        for (int i = 0; i < C; ++i) x[i] = lam[i * MS + gt];
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < C; ++i) {
-          acc += x[i];
-          A[i * MS + gt] = acc;
-        }
-      }
-      tc::named_barrier(1, 128);
-      uint8_t* gam = smem + S::offGam + s * C * MS * 2;
-      float* er = (float*)(smem + S::offE) + s * 2 * MS;
-      const size_t cbase = ((size_t)bh * N + c) * C * MS;
-#pragma unroll 4
-      for (int e = gt; e < C * MS; e += 128) {
-        const int i = e >> 6, sl = e & 63;
-        const float Ai = A[e], Ar = A[31 * MS + sl], A63 = A[63 * MS + sl];
-        const float om = -expm1f(lam[e]);  // 1 - alpha_i, without cancellation
-        ep_out[cbase + e] = __expf(Ai - Ar);
-        gh_out[cbase + e] = __float2bfloat16_rn(om * __expf(Ar - Ai));
-        *(__nv_bfloat16*)(gam + sw128(i, sl)) = __float2bfloat16_rn(om * __expf(A63 - Ai));
-        if (i == 0) {
-          er[sl] = __expf(Ar);
-          er[MS + sl] = __expf(A63);
-        }
-      }
-      tc::fence_proxy_async_smem();
-      tc::named_barrier(1, 128);  // A is rewritten by the next chunk only after every thread read it
       if (lane == 0) {
-        tc::mbar_arrive(&bars[A_GATE + s]);
-        tc::mbar_arrive(&bars[A_EMPTY + s]);
+        tc::mbar_arrive(&bars[B_DEMPTY + b]);
+        tc::mbar_arrive(&bars[B_EMPTY + s]);
       }
     }
   }
@@ -854,7 +866,8 @@ __global__ void __launch_bounds__(256, 1)
 size_t nha_workspace_bytes(long long BH, int L) {
   const size_t chunks = (size_t)BH * (L / C);
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
-  return al(chunks * D * MS * 2) * 2 + al(chunks * C * MS * 2) + al(chunks * C * MS * 4) + 256;
+  return al(chunks * D * MS * 2) * 2 + al(chunks * C * MS * 2) * 2 + al(chunks * C * MS * 4) +
+         al(chunks * 2 * MS * 4) + 256;
 }
 
 cudaError_t launch_nha_fwd(long long BH, int L, int window, float scale, const void* q, const void* k, const void* v,
@@ -874,8 +887,12 @@ cudaError_t launch_nha_fwd(long long BH, int L, int window, float scale, const v
   p += al(chunks * D * MS * 2);
   __nv_bfloat16* gh_buf = (__nv_bfloat16*)p;
   p += al(chunks * C * MS * 2);
+  __nv_bfloat16* gam_buf = (__nv_bfloat16*)p;
+  p += al(chunks * C * MS * 2);
   float* ep_buf = (float*)p;
   p += al(chunks * C * MS * 4);
+  float* er_buf = (float*)p;
+  p += al(chunks * 2 * MS * 4);
   int* err = (int*)p;
   cudaError_t e = cudaMemsetAsync(err, 0, 16, st);
   if (e != cudaSuccess) return e;
@@ -884,14 +901,18 @@ cudaError_t launch_nha_fwd(long long BH, int L, int window, float scale, const v
   CUtensorMap mk, mv;
   if (!make_tile_map(&mk, k, rows, D) || !make_tile_map(&mv, v, rows, D)) return cudaErrorInvalidValue;
   if (!full) {
+    CUtensorMap mgam;
+    if (!make_tile_map(&mgam, gam_buf, (long long)chunks * C, MS)) return cudaErrorInvalidValue;
     e = cudaFuncSetAttribute(nha_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, StSmem::kBytes);
     if (e != cudaSuccess) return e;
     if ((e = mark(ev_start, 0)) != cudaSuccess) return e;
-    nha_state_kernel<<<(unsigned)BH, 384, StSmem::kBytes, st>>>(mk, mv, log_alpha, L, N, st_buf, ut_buf, gh_buf,
-                                                                 ep_buf, err);
+    nha_gate_kernel<<<(unsigned)chunks, 256, 0, st>>>(log_alpha, gh_buf, ep_buf, gam_buf, er_buf);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    nha_state_kernel<<<(unsigned)(2 * BH), 192, StSmem::kBytes, st>>>(mk, mv, mgam, er_buf, L, N, st_buf, ut_buf,
+                                                                       err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = mark(ev_stop, 0)) != cudaSuccess) return e;
-    if (launches) ++*launches;
+    if (launches) *launches += 2;
   }
   CUtensorMap mq, mst, mut, mgh;
   if (!make_tile_map(&mq, q, rows, D) || !make_tile_map(&mst, st_buf, (long long)chunks * D, MS) ||
@@ -969,7 +990,7 @@ nats_status nats_nha_fwd_profiled(const nats_nha_dims* dims, const void* q, cons
                                        (cudaStream_t)stream, prof ? prof->start : nullptr,
                                        prof ? prof->stop : nullptr, prof ? &prof->launches : nullptr);
   if (prof) {
-    prof->stage_launches[0] = dims->window < dims->L ? 1 : 0;
+    prof->stage_launches[0] = dims->window < dims->L ? 2 : 0;
     prof->stage_launches[1] = 1;
   }
   return e == cudaSuccess ? NATS_OK : NATS_ERR_CUDA;
