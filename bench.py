@@ -863,21 +863,21 @@ def run_nha(args, rank, dev, stream, dist):
 def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):
     """Times nats_hybrid_bwd on the layer workload: the gradients of a seeded
     dout at the forward's selection, from the activations the CUDA forward
-    saved (one forward outside the timed region).  Each of its four stages
-    is timed with the library's own stage events and set against the
-    roofline of its own kind of work:
-      merge_bwd   HBM: per token it reads q, dout (bf16) and o_soft, o_lin
-                  (fp32) and writes d o_soft (bf16), d o_lin, dq (fp32) and
-                  delta: 22 d + 4 bytes;
-      softmax_bwd bf16 tensor (warp-level MMAs): 10 d FLOP per visible
-                  (query, key) pair (scores recomputed, dP, dq, dk, dv);
-      gdn_bwd     fp32 CUDA cores: 14 d^2 FLOP per token (dS += do q^T,
-                  S^T do, dS k, the two column sums of dk, <dS, S>, the dS
-                  update), against 152 SMs x 128 FMA lanes x 2 FLOP x the SM
-                  clock sampled during the timed region;
-      combine     HBM: per token k (bf16), the two state halves' column sums
-                  and scalars, dq and dk read and written, g, beta, dg,
-                  dbeta: 34 d + 48 bytes.
+    saved (one forward outside the timed region).  Its stages are timed with
+    the library's own stage events and set against the roofline of their
+    own kind of work:
+      merge_bwd    HBM: per token it reads q, dout (bf16) and o_soft, o_lin
+                   (fp32) and writes d o_soft (bf16), d o_lin, dq (fp32) and
+                   delta: 22 d + 4 bytes;
+      softmax_bwd  bf16 tensor (warp-level MMAs): 10 d FLOP per visible
+                   (query, key) pair (scores recomputed, dP, dq, dk, dv);
+      gdn_bwd      the Gated DeltaNet stage and the per-chunk C x C stage
+                   together, tf32 tensor (warp-level MMAs): per chunk the
+                   forward's chunk factors and scan that recompute the chunk
+                   start states (5 C^2 d + 6 C d^2 FLOP, the forward's count)
+                   and the chunkwise adjoint's products, 2 (8 C d^2 + 15 C^2 d)
+                   FLOP (full tiles; rolled-back chunks skip some), against
+                   the bf16 peak x 1.1 / 2.25 (the nominal tf32 : bf16 ratio).
     The headline roofline is the stage with the largest share of the time."""
     import torch
 
@@ -933,28 +933,22 @@ def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):
     pk = peaks()
     tokens = B * H * L
     pairs = work["flops_softmax"] / (4 * d)
-    if clk and clk.get("sm_mhz"):
-        sm_mhz, clk_src = clk["sm_mhz"], f"median SM clock sampled during the timed region ({clk['source']})"
-    else:
-        sm_mhz = float(torch.cuda.get_device_properties(dev).clock_rate) / 1e3 \
-            if hasattr(torch.cuda.get_device_properties(dev), "clock_rate") else None
-        clk_src = "the device's reported SM clock (no sample)"
-    fp32_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12 if sm_mhz else None
-    amounts = {"merge_bwd": ("hbm", (22 * d + 4) * tokens),
-               "softmax_bwd": ("tensor", 10 * d * pairs),
-               "gdn_bwd": ("alu", 14 * d * d * tokens),
-               "combine": ("hbm", (34 * d + 48) * tokens)}
+    Cc = 64
+    chunks = B * H * (L // Cc)
+    amounts = {"merge_bwd": ("hbm", (22 * d + 4) * tokens, stage_ms["merge_bwd"]),
+               "softmax_bwd": ("tensor", 10 * d * pairs, stage_ms["softmax_bwd"]),
+               "gdn_bwd": ("tf32", chunks * (5 * Cc * Cc * d + 6 * Cc * d * d + 2 * (8 * Cc * d * d + 15 * Cc * Cc * d)),
+                           stage_ms["gdn_bwd"] + stage_ms["combine"])}
     per = {}
-    for name, (bound, amount) in amounts.items():
-        sms = stage_ms[name]
+    for name, (bound, amount, sms) in amounts.items():
         if bound == "hbm":
             ach, peak, unit, src = amount / (sms / 1e3) / 1e9, pk["hbm_gbs"], "GB/s", f"{pk['source']} HBM copy"
         elif bound == "tensor":
             ach, peak, unit = amount / (sms / 1e3) / 1e12, pk["bf16_tflops_sustained"], "TFLOP/s"
             src = f"{pk['source']} bf16 sustained (the kernels use mma.sync, not tcgen05)"
         else:
-            ach, peak, unit = amount / (sms / 1e3) / 1e12, fp32_peak, "TFLOP/s"
-            src = f"fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x {sm_mhz} MHz, {clk_src}"
+            ach, peak, unit = amount / (sms / 1e3) / 1e12, pk["bf16_tflops_sustained"] * 1.1 / 2.25, "TFLOP/s"
+            src = f"{pk['source']} bf16 sustained x 1.1 / 2.25 (tf32; mma.sync m16n8k8)"
         per[name] = {"bound": bound, "ms": sms, "share": sms / ms if ms else None, "achieved": ach, "peak": peak,
                      "unit": unit, "frac": (ach / peak) if peak else None, "peak_source": src,
                      ("bytes_per_step" if bound == "hbm" else "flops_per_step"): amount}
@@ -962,7 +956,7 @@ def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):
     return {"what": "nats_hybrid_bwd: gradients of q, k, v, g, beta, W_g, b_g and the RMSNorm weights at the "
                     "forward's selection, same workload as the forward",
             "value": job_throughput(B * L, world, ms), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
-            "launches_per_step": int(profs[0].launches),
+            "launches_per_step": int(profs[0].launches), "stages_ms": stage_ms,
             "stages": per, "clocks": clk,
             "roofline": {"kernel": top, **{k: per[top][k] for k in ("bound", "achieved", "peak", "unit", "frac",
                                                                    "peak_source")}}}

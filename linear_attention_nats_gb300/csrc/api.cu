@@ -340,7 +340,7 @@ nats_status nats_hybrid_fwd(const nats_dims* dims, const void* q, const void* k,
 
 size_t nats_bwd_workspace_size(const nats_dims* dims) {
   if (check_dims(dims) != NATS_OK) return 0;
-  return bwd_workspace_bytes(problem_of(dims));
+  return bwd_workspace_bytes(problem_of(dims), dims->dtype);
 }
 
 nats_status nats_hybrid_bwd(const nats_dims* dims, const void* q, const void* k, const void* v, const float* g,
@@ -375,7 +375,7 @@ nats_status nats_hybrid_bwd_profiled(const nats_dims* dims, const void* q, const
   const void* ptrs[] = {q, k, v, o_soft, o_lin, dout, dq, dk, dv, workspace};
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return NATS_ERR_ALIGN;
-  if (workspace_bytes < bwd_workspace_bytes(p)) return NATS_ERR_WORKSPACE;
+  if (workspace_bytes < bwd_workspace_bytes(p, dims->dtype)) return NATS_ERR_WORKSPACE;
   const nats_status r = cuda_status(launch_hybrid_bwd(
       p, dims->dtype, q, k, v, g, beta, w_g, b_g, norm_w_soft, norm_w_lin, sel, o_soft, o_lin, dout, dq, dk, dv, dg,
       dbeta, dw_g, db_g, dnorm_w_soft, dnorm_w_lin, workspace, (cudaStream_t)stream, prof ? prof->start : nullptr,

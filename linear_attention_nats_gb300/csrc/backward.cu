@@ -619,18 +619,69 @@ __global__ void __launch_bounds__(256) gdn_bwd_combine_kernel(
 
 }  // namespace
 
-size_t bwd_workspace_bytes(const Problem& p) {
-  auto al = [](size_t b) { return (b + 255) & ~(size_t)255; };
-  const size_t rows = (size_t)p.BH * p.L, dd = (size_t)p.d * p.d;
-  return 2 * al(rows * p.d * 4)            // d o_s, d o_l
-         + al(rows * p.d * 2)              // d o_s in bf16 (the operand of the tensor-core products)
-         + 2 * al(rows * 4)                // delta, lse
-         + al((size_t)p.BH * p.N * dd * 4)  // chunk-start states
-         + al((size_t)p.BH * kChunk * dd * 4)  // states inside the chunk being reversed
-         + al((size_t)p.BH * dd * 4)        // gradient held over a rolled-back chunk
-         + al((size_t)kRowSplit * rows * 2 * p.d * 4)  // the state halves' column sums per token
-         + al((size_t)kRowSplit * rows * 4 * 4);        // and their scalars
+// The backward workspace, carved in one order for the size query and the
+// launch (base == nullptr: sizes only).
+struct BwdLayout {
+  float *d_os, *d_ol, *delta, *lse;
+  __nv_bfloat16* d_os16;
+  // fp32 layers: the token-serial adjoint
+  float *Sc, *Tk, *dSx, *pcol, *psc;
+  // bf16 layers: the forward recompute of the chunk-start states, then the
+  // chunkwise adjoint
+  float *fG, *fgate;
+  void *fW, *fU, *fP, *fol16;
+  int* ferr;
+  GdnBwdScratch cw;
+};
+
+static size_t bwd_layout(const Problem& p, int dtype, uint8_t* base, BwdLayout* o) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> void* {
+    void* ptr = base ? base + off : nullptr;
+    off += (bytes + 255) & ~(size_t)255;
+    return ptr;
+  };
+  const size_t rows = (size_t)p.BH * p.L, dd = (size_t)p.d * p.d, chunks = (size_t)p.BH * p.N;
+  BwdLayout l{};
+  l.d_os = (float*)take(rows * p.d * 4);               // d o_s
+  l.d_ol = (float*)take(rows * p.d * 4);               // d o_l
+  l.d_os16 = (__nv_bfloat16*)take(rows * p.d * 2);     // d o_s in bf16 (the operand of the tensor-core products)
+  l.delta = (float*)take(rows * 4);
+  l.lse = (float*)take(rows * 4);
+  if (dtype != 0) {
+    l.Sc = (float*)take(chunks * dd * 4);                       // chunk-start states
+    l.Tk = (float*)take((size_t)p.BH * kChunk * dd * 4);        // states inside the chunk being reversed
+    l.dSx = (float*)take((size_t)p.BH * dd * 4);                // gradient held over a rolled-back chunk
+    l.pcol = (float*)take((size_t)kRowSplit * rows * 2 * p.d * 4);  // the state halves' column sums per token
+    l.psc = (float*)take((size_t)kRowSplit * rows * 4 * 4);     // and their scalars
+  } else {
+    l.fG = (float*)take(rows * 4);        // forward chunk factors (recomputed)
+    l.fW = take(rows * p.d * 2);
+    l.fU = take(rows * p.d * 2);
+    l.fP = take(rows * kChunk * 2);
+    l.fgate = (float*)take(rows * 4);
+    l.fol16 = take(rows * p.d * 2);       // the recompute's o_l (not used)
+    l.ferr = (int*)take(16);
+    GdnBwdScratch& w = l.cw;
+    w.S0 = (float*)take(chunks * dd * 4);
+    w.dSC = (float*)take(chunks * dd * 4);
+    w.G = (float*)take(rows * 4);
+    w.Li = (float*)take(rows * kChunk * 4);
+    w.P = (float*)take(rows * kChunk * 4);
+    w.W16 = (__nv_bfloat16*)take(rows * p.d * 2);
+    w.Qe16 = (__nv_bfloat16*)take(rows * p.d * 2);
+    w.Kt16 = (__nv_bfloat16*)take(rows * p.d * 2);
+    w.Vh = (float*)take(rows * p.d * 4);
+    w.U = (float*)take(rows * p.d * 4);
+    w.PtdO = (float*)take(rows * p.d * 4);
+    w.Y = (float*)take(rows * p.d * 4);
+    w.dG = (float*)take(rows * 4);
+  }
+  if (o) *o = l;
+  return off;
 }
+
+size_t bwd_workspace_bytes(const Problem& p, int dtype) { return bwd_layout(p, dtype, nullptr, nullptr); }
 
 cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const void* k, const void* v,
                               const float* g, const float* beta, const float* w_g, const float* b_g,
@@ -645,29 +696,19 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
   auto count = [&](int s, int n) {
     if (launches) launches[s] += n;
   };
-  auto al = [](size_t b) { return (b + 255) & ~(size_t)255; };
   const long long rows = (long long)p.BH * p.L;
-  const size_t dd = (size_t)p.d * p.d;
-  uint8_t* w = (uint8_t*)ws;
-  float* d_os = (float*)w;
-  w += al((size_t)rows * p.d * 4);
-  float* d_ol = (float*)w;
-  w += al((size_t)rows * p.d * 4);
-  __nv_bfloat16* d_os16 = (__nv_bfloat16*)w;
-  w += al((size_t)rows * p.d * 2);
-  float* delta = (float*)w;
-  w += al((size_t)rows * 4);
-  float* lse = (float*)w;
-  w += al((size_t)rows * 4);
-  float* Sc = (float*)w;
-  w += al((size_t)p.BH * p.N * dd * 4);
-  float* Tk = (float*)w;
-  w += al((size_t)p.BH * kChunk * dd * 4);
-  float* dSx = (float*)w;
-  w += al((size_t)p.BH * dd * 4);
-  float* pcol = (float*)w;
-  w += al((size_t)kRowSplit * rows * 2 * p.d * 4);
-  float* psc = (float*)w;
+  BwdLayout lay;
+  bwd_layout(p, dtype, (uint8_t*)ws, &lay);
+  float* d_os = lay.d_os;
+  float* d_ol = lay.d_ol;
+  __nv_bfloat16* d_os16 = lay.d_os16;
+  float* delta = lay.delta;
+  float* lse = lay.lse;
+  float* Sc = lay.Sc;
+  float* Tk = lay.Tk;
+  float* dSx = lay.dSx;
+  float* pcol = lay.pcol;
+  float* psc = lay.psc;
   // weight gradients are sums over the launch: zeroed first
   cudaError_t e = cudaSuccess;
   if (dw_g) e = cudaMemsetAsync(dw_g, 0, (size_t)p.H * p.d * 4, st);
@@ -701,19 +742,45 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
     }
     count(NATS_BWD_STAGE_SOFTMAX, 2);
     if ((e2 = mark(ev_stop, NATS_BWD_STAGE_SOFTMAX)) != cudaSuccess) return e2;
-    constexpr int smem = GdnBwd<D>::kBytes;
-    static const cudaError_t attr =
-        cudaFuncSetAttribute(gdn_bwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (attr != cudaSuccess) return attr;
     if ((e2 = mark(ev_start, NATS_BWD_STAGE_GDN)) != cudaSuccess) return e2;
-    gdn_bwd_kernel<T, D><<<(unsigned)(p.BH * kRowSplit), kGdnThreads, smem, st>>>(
-        qt, kt, vt, g, beta, sel, d_ol, p.L, p.N, p.scale, Sc, Tk, dSx, pcol, psc, dv);
-    count(NATS_BWD_STAGE_GDN, 1);
-    if ((e2 = mark(ev_stop, NATS_BWD_STAGE_GDN)) != cudaSuccess) return e2;
-    if ((e2 = mark(ev_start, NATS_BWD_STAGE_COMBINE)) != cudaSuccess) return e2;
-    gdn_bwd_combine_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(kt, g, beta, pcol, psc, rows, p.scale,
-                                                                            dq, dk, dg, dbeta);
-    count(NATS_BWD_STAGE_COMBINE, 1);
+    if constexpr (tc) {
+      // the chunk-start states, from the forward's chunk factors and scan
+      // (the same kernels as the forward; the selection is given)
+      if ((e2 = cudaMemsetAsync(lay.ferr, 0, 16, st)) != cudaSuccess) return e2;
+      if (D == 128)
+        e2 = launch_gdn_prep_tc(p, q, k, v, g, beta, w_g, b_g, lay.fG, lay.fW, lay.fU, lay.fP, lay.fgate, nullptr,
+                                nullptr, nullptr, lay.ferr, st);
+      else
+        e2 = launch_gdn_prep_mma(p, q, k, v, g, beta, w_g, b_g, lay.fG, lay.fW, lay.fU, lay.fP, lay.fgate, nullptr,
+                                 nullptr, nullptr, st);
+      if (e2 == cudaSuccess)
+        e2 = launch_gdn_scan_tc(p, q, k, sel, lay.fG, lay.fW, lay.fU, lay.fP, nullptr, lay.fol16, nullptr, lay.ferr,
+                                st, lay.cw.S0);
+      if (e2 != cudaSuccess) return e2;
+      count(NATS_BWD_STAGE_GDN, 2);
+      int32_t n4 = 0;
+      if ((e2 = launch_gdn_bwd_chunk(p, q, k, v, g, beta, sel, d_ol, lay.cw, dq, dk, dv, dg, dbeta, st, &n4)) !=
+          cudaSuccess)
+        return e2;
+      count(NATS_BWD_STAGE_GDN, n4);
+      if ((e2 = mark(ev_stop, NATS_BWD_STAGE_GDN)) != cudaSuccess) return e2;
+      if ((e2 = mark(ev_start, NATS_BWD_STAGE_COMBINE)) != cudaSuccess) return e2;
+      if ((e2 = launch_gdn_bwd_cc(p, q, k, beta, d_ol, lay.cw, dq, dk, dg, dbeta, st)) != cudaSuccess) return e2;
+      count(NATS_BWD_STAGE_COMBINE, 1);
+    } else {
+      constexpr int smem = GdnBwd<D>::kBytes;
+      static const cudaError_t attr =
+          cudaFuncSetAttribute(gdn_bwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (attr != cudaSuccess) return attr;
+      gdn_bwd_kernel<T, D><<<(unsigned)(p.BH * kRowSplit), kGdnThreads, smem, st>>>(
+          qt, kt, vt, g, beta, sel, d_ol, p.L, p.N, p.scale, Sc, Tk, dSx, pcol, psc, dv);
+      count(NATS_BWD_STAGE_GDN, 1);
+      if ((e2 = mark(ev_stop, NATS_BWD_STAGE_GDN)) != cudaSuccess) return e2;
+      if ((e2 = mark(ev_start, NATS_BWD_STAGE_COMBINE)) != cudaSuccess) return e2;
+      gdn_bwd_combine_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(kt, g, beta, pcol, psc, rows,
+                                                                              p.scale, dq, dk, dg, dbeta);
+      count(NATS_BWD_STAGE_COMBINE, 1);
+    }
     if ((e2 = mark(ev_stop, NATS_BWD_STAGE_COMBINE)) != cudaSuccess) return e2;
     return cudaGetLastError();
   };

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(448, 1)
                        const __grid_constant__ CUtensorMap tm_p, const uint8_t* __restrict__ sel,
                        const float* __restrict__ G, int L, int N, float scale, float* __restrict__ o_l,
                        __nv_bfloat16* __restrict__ o_l16,
-                       float* __restrict__ state_out, int* __restrict__ err) {
+                       float* __restrict__ state_out, float* __restrict__ s0_out, int* __restrict__ err) {
   using S = ScanSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -374,6 +374,21 @@ __global__ void __launch_bounds__(448, 1)
       }
       tc::fence_before();
       tc::mbar_arrive(&bars[SB_S0]);
+      // the state at the start of chunk c + 1 (after this chunk's update or
+      // rollback), fp32, when the caller keeps them (backward recompute);
+      // no product writes S before this thread's next Delta
+      if (s0_out && c + 1 < N && has_row) {
+#pragma unroll 1
+        for (int ch = 0; ch < SC / 32; ++ch) {
+          float v[32];
+          tc::tmem_ld32(tmem + kColS + lane_off + hf * SC + ch * 32, v);
+          tc::tmem_ld_wait();
+          float* dst = s0_out + ((bh * N + c + 1) * D + r) * (long long)D + hf * SC + ch * 32;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            ((float4*)dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+      }
       // the next chunk's MMA3 accumulates onto gamma_C S: scale now, off the
       // critical path (that MMA3 also waits for this thread's next Delta)
       if (lin_next && has_row) {
@@ -424,7 +439,7 @@ __global__ void __launch_bounds__(448, 1)
 template <int D>
 static cudaError_t launch_scan_tc_t(const Problem& p, const void* q, const void* k, const uint8_t* sel,
                                     const float* G, const void* W16, const void* UT16, const void* P16,
-                                    float* o_l, __nv_bfloat16* o_l16, float* state_out, int* err,
+                                    float* o_l, __nv_bfloat16* o_l16, float* state_out, float* s0_out, int* err,
                                     cudaStream_t st) {
   CUtensorMap mw, mq, mk, mu, mp;
   const long long rows = p.BH * p.L;  // = BH * N * 64
@@ -435,18 +450,23 @@ static cudaError_t launch_scan_tc_t(const Problem& p, const void* q, const void*
   const int smem = ScanSmem<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  if (s0_out) {  // chunk 0 starts from the zero state
+    e = cudaMemset2DAsync(s0_out, (size_t)p.N * D * D * sizeof(float), 0, (size_t)D * D * sizeof(float),
+                          (size_t)p.BH, st);
+    if (e != cudaSuccess) return e;
+  }
   kern<<<(unsigned)p.BH, 448, smem, st>>>(mw, mq, mk, mu, mp, sel, G, p.L, p.N, p.scale, o_l, o_l16, state_out,
-                                          err);
+                                          s0_out, err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gdn_scan_tc(const Problem& p, const void* q, const void* k, const uint8_t* sel, const float* G,
                                const void* W16, const void* UT16, const void* P16, float* o_l, void* o_l16,
-                               float* state_out, int* err, cudaStream_t st) {
+                               float* state_out, int* err, cudaStream_t st, float* s0_out) {
   if (p.BH == 0 || p.N == 0) return cudaSuccess;
   __nv_bfloat16* ol16 = (__nv_bfloat16*)o_l16;
-  return p.d == 64 ? launch_scan_tc_t<64>(p, q, k, sel, G, W16, UT16, P16, o_l, ol16, state_out, err, st)
-                   : launch_scan_tc_t<128>(p, q, k, sel, G, W16, UT16, P16, o_l, ol16, state_out, err, st);
+  return p.d == 64 ? launch_scan_tc_t<64>(p, q, k, sel, G, W16, UT16, P16, o_l, ol16, state_out, s0_out, err, st)
+                   : launch_scan_tc_t<128>(p, q, k, sel, G, W16, UT16, P16, o_l, ol16, state_out, s0_out, err, st);
 }
 
 }  // namespace nats

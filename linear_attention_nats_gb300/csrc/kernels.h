@@ -45,10 +45,11 @@ cudaError_t launch_gdn_prep_tc(const Problem& p, const void* q, const void* k, c
                                void* U16, void* P16, float* gate, const float* w_s, const float* b_s,
                                uint8_t* sel_out, int* err, cudaStream_t st);
 
-// bf16 chunk scan: o_l (fp32 [BH, L, dv]); state_out may be null.
+// bf16 chunk scan: o_l (fp32 [BH, L, dv]); state_out may be null; s0_out
+// (or null) receives every chunk's start state, fp32 [BH, N, dv, dk].
 cudaError_t launch_gdn_scan_tc(const Problem& p, const void* q, const void* k, const uint8_t* sel, const float* G,
                                const void* W16, const void* UT16, const void* P16, float* o_l, void* o_l16,
-                               float* state_out, int* err, cudaStream_t st);
+                               float* state_out, int* err, cudaStream_t st, float* s0_out = nullptr);
 
 // One decode step of the layer (dtype 0 = bf16, 1 = fp32), one CTA per (b, h).
 cudaError_t launch_decode_step(const Problem& p, int dtype, long long t, const void* q, const void* k,
@@ -62,7 +63,7 @@ cudaError_t launch_decode_step(const Problem& p, int dtype, long long t, const v
 // the launches (norm + merge, softmax dq and dk / dv, Gated DeltaNet adjoint,
 // per-token combine).  ev_start / ev_stop (NATS_BWD_STAGE_* ids, entries may
 // be NULL) are recorded around each stage, launches[stage] counts its kernels.
-size_t bwd_workspace_bytes(const Problem& p);
+size_t bwd_workspace_bytes(const Problem& p, int dtype);
 cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const void* k, const void* v,
                               const float* g, const float* beta, const float* w_g, const float* b_g,
                               const float* nws, const float* nwl, const uint8_t* sel, const float* o_s,
@@ -77,6 +78,34 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
 cudaError_t launch_score_bwd(const Problem& p, int dtype, const void* q, const void* k, const float* w_s,
                              const float* b_s, const uint8_t* sel, const void* out, const void* dout, float* dq,
                              float* dk, float* dw_s, float* db_s, cudaStream_t st);
+
+// Chunkwise Gated DeltaNet adjoint of bf16 layers (gdn_bwd_chunk.cu): its
+// scratch, carved from the backward workspace.
+struct GdnBwdScratch {
+  float* S0;    // [BH, N, dv, dk] chunk-start states (the forward recompute writes them)
+  float* dSC;   // [BH, N, dv, dk] gradient of each committed chunk's end state
+  float* G;     // [BH, L] in-chunk cumulative log-decay
+  float* Li;    // [BH, N, C, C] (I + diag(beta) A)^{-1}
+  float* P;     // [BH, N, C, C] lower(e^{G_i - G_j} scale q_i . k_j)
+  __nv_bfloat16* W16;   // [BH, L, dk] Linv diag(beta gamma) K
+  __nv_bfloat16* Qe16;  // [BH, L, dk] diag(gamma) Q~ - P W
+  __nv_bfloat16* Kt16;  // [BH, L, dk] diag(gamma_C / gamma) K
+  float* Vh;    // [BH, L, dv] V - diag(gamma) K S0^T
+  float* U;     // [BH, L, dv] Linv diag(beta) Vh
+  float* PtdO;  // [BH, L, dv] P^T dO
+  float* Y;     // [BH, L, dv] Linv^T dU
+  float* dG;    // [BH, L] gradient of G from the state products
+};
+// chunk factors, the reverse state-gradient scan and the state products
+// (four kernels; dq, dk, dv accumulate, dbeta is overwritten)
+cudaError_t launch_gdn_bwd_chunk(const Problem& p, const void* q, const void* k, const void* v, const float* g,
+                                 const float* beta, const uint8_t* sel, const float* dO, const GdnBwdScratch& w,
+                                 float* dq, float* dk, float* dv, float* dg, float* dbeta, cudaStream_t st,
+                                 int32_t* launches);
+// the C x C products and dg (one kernel; dq, dk, dbeta accumulate, dg is overwritten)
+cudaError_t launch_gdn_bwd_cc(const Problem& p, const void* q, const void* k, const float* beta, const float* dO,
+                              const GdnBwdScratch& w, float* dq, float* dk, float* dg, float* dbeta,
+                              cudaStream_t st);
 
 // Softmax branch of the backward pass on warp-level MMAs, bf16 layers
 // (backward_mma.cu): lse and dq (+=), then dk, dv (=).

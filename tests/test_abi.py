@@ -167,12 +167,21 @@ def test_backward_validation(nat):
     # the backward pass: argument checks before any launch
     dm = nat.dims(1, 2, 128, 64)
     need = nat.lib.nats_bwd_workspace_size(ctypes.byref(dm))
-    # d o_s, d o_l (fp32), d o_s (bf16), delta, lse, 2 chunk-start states, one chunk of states, one held
-    # gradient, then the two state halves' per-token column sums and scalars
-    rows, dd = 2 * 128, 64 * 64
+    rows, dd, chunks = 2 * 128, 64 * 64, 2 * 2
     al = lambda b: (b + 255) // 256 * 256
-    assert need == (2 * al(rows * 64 * 4) + al(rows * 64 * 2) + 2 * al(rows * 4) + al(2 * 2 * dd * 4)
-                    + al(2 * 64 * dd * 4) + al(2 * dd * 4) + al(2 * rows * 2 * 64 * 4) + al(2 * rows * 4 * 4))
+    common = 2 * al(rows * 64 * 4) + al(rows * 64 * 2) + 2 * al(rows * 4)  # d o_s, d o_l, d o_s bf16, delta, lse
+    # fp32 layers: 2 chunk-start states, one chunk of states, one held gradient, then the two state halves'
+    # per-token column sums and scalars
+    f32 = nat.lib.nats_bwd_workspace_size(ctypes.byref(nat.dims(1, 2, 128, 64, nat.NATS_F32)))
+    assert f32 == common + (al(chunks * dd * 4) + al(2 * 64 * dd * 4) + al(2 * dd * 4) + al(2 * rows * 2 * 64 * 4)
+                            + al(2 * rows * 4 * 4))
+    # bf16 layers: the forward's chunk factors (G, W, U^T, P, gate, o_l, error flag), then the chunkwise
+    # adjoint's chunk-start states and state gradients, G, Linv and P (fp32), W, Q_eff, K~ (bf16), Vh, U,
+    # P^T dO, Y (fp32) and dG
+    assert need == common + (al(rows * 4) + 2 * al(rows * 64 * 2) + al(rows * 64 * 2) + al(rows * 4)
+                             + al(rows * 64 * 2) + al(16)
+                             + 2 * al(chunks * dd * 4) + al(rows * 4) + 2 * al(rows * 64 * 4)
+                             + 3 * al(rows * 64 * 2) + 4 * al(rows * 64 * 4) + al(rows * 4))
     fake = ctypes.c_void_p(256)
     odd = ctypes.c_void_p(264)
     args = [fake] * 23  # q ... dnorm_w_lin, then the workspace

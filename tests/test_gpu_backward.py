@@ -92,11 +92,10 @@ def test_backward_after_cuda_forward(B, H, L, d, dtype, seed):
 
 
 def test_backward_profiled_stages():
-    # nats_hybrid_bwd_profiled: the same per-token gradients bit for bit as
-    # without events (the weight gradients are sums taken with atomics, in
-    # no fixed order: equal to rounding), every stage's events recorded in
-    # order, and the launch count (merge, softmax dq, softmax dk / dv,
-    # adjoint scan, combine)
+    # nats_hybrid_bwd_profiled: the same per-token gradients as without
+    # events (the weight gradients are sums taken with atomics, in no fixed
+    # order: equal to rounding), every stage's events recorded in order, and
+    # the launch count
     import linear_attention_nats_gb300 as nats
     from linear_attention_nats_gb300 import _native, build
 
@@ -118,12 +117,15 @@ def test_backward_profiled_stages():
         prof.start[i], prof.stop[i] = a.cuda_event, b.cuda_event
     timed = nats.hybrid_bwd(*args, **nw, profile=prof)
     torch.cuda.synchronize()
-    for n in GRADS[:5]:
-        assert torch.equal(plain[n], timed[n]), n
+    for n in GRADS[:5]:  # dg, dbeta and dq / dk gather shared-memory sums taken with atomics
+        assert torch.allclose(plain[n], timed[n], rtol=1e-5, atol=1e-6 * float(plain[n].abs().max())), n
     for n in GRADS[5:]:
         assert torch.allclose(plain[n], timed[n], rtol=1e-5, atol=1e-5 * float(plain[n].abs().max())), n
-    assert list(prof.stage_launches)[:len(_native.BWD_STAGES)] == [1, 2, 1, 1]
-    assert prof.launches == 5
+    # bf16: merge; softmax dq, dk / dv; the Gated DeltaNet stage (chunk
+    # factors and scan of the forward for the chunk-start states, the adjoint's
+    # chunk factors, reverse scan, S0 and dS_C products); the C x C products
+    assert list(prof.stage_launches)[:len(_native.BWD_STAGES)] == [1, 2, 6, 1]
+    assert prof.launches == 10
     ms = [a.elapsed_time(b) for a, b in ev]
     assert all(m > 0 for m in ms), ms
     for (_, b), (a, _) in zip(ev, ev[1:]):  # stage i ends before stage i + 1 starts
@@ -228,3 +230,31 @@ def test_score_layer_gradient(B, H, L, d, dtype, seed):
     print(f"[parity] score-layer surrogate {dtype}-{d}: " + " ".join(f"{n}={e:.1e}" for n, e in errs.items()))
     for n, e in errs.items():
         assert e <= TOL[dtype], (n, e)
+
+
+def test_backward_full_size_whole_head():
+    # the benchmark's workload through the CUDA forward and backward; one
+    # whole head (all 8192 tokens, every chunk's state gradient carried back
+    # through the reverse scan) against the oracle's backward of that head
+    import linear_attention_nats_gb300 as nats
+    from linear_attention_nats_gb300 import build
+
+    build.build()
+    inp = gen.make_inputs(name="l8192", **gen.CONFIGS["l8192"])
+    B, H, L, d = inp.B, inp.H, inp.L, inp.d
+    t = to_device(inp)
+    fwd = nats.hybrid_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_s"], t["b_s"], t["w_g"], t["b_g"],
+                          return_sel=True, return_branches=True, check_errors=True)
+    dout = gen.round_to_bf16(np.random.default_rng(49).standard_normal((B, H, L, d)).astype(np.float32))
+    got = nats.hybrid_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_g"], t["b_g"], fwd["sel"], fwd["o_soft"],
+                          fwd["o_lin"], _dev(dout, "bf16"))
+    torch.cuda.synchronize()
+    sel = fwd["sel"].cpu().numpy()
+    b, h = 2, 7
+    one = lambda a: a[b:b + 1, h:h + 1]
+    ref = ob.backward(one(inp.q), one(inp.k), one(inp.v), one(inp.g), one(inp.beta), inp.w_g[h:h + 1],
+                      inp.b_g[h:h + 1], sel[b:b + 1, h:h + 1], one(dout))
+    errs = {n: rel_err(got[n][b:b + 1, h:h + 1].cpu().numpy(), ref[n]) for n in ("dq", "dk", "dv", "dg", "dbeta")}
+    print("[parity] backward l8192 whole head: " + " ".join(f"{n}={e:.1e}" for n, e in errs.items()))
+    for n, e in errs.items():
+        assert e <= TOL["bf16"], (n, e)
