@@ -34,10 +34,16 @@
 //   gdn_bwd_s0_kernel    per chunk: Vh, U, P^T dO; dq += diag(gamma) dO S0
 //   gdn_bwd_ds_kernel    per chunk: dU, Y, dv; the U dS_C and dVh S0 terms
 //   gdn_bwd_cc_kernel    per chunk: the C x C products, dq, dk, dbeta, dg
-// Products run on warp-level tensor cores (mma.sync m16n8k8, tf32 operands,
-// fp32 accumulation); the triangular inverse is a forward substitution on
-// the CUDA cores.  Each CTA has 8 warps; a C x D output is split into 16-row
-// strips (warp w & 3) and column halves (warp w >> 2).
+// Products run on warp-level tensor cores with fp32 accumulation: the
+// per-chunk kernels take fp16 operand tiles through ldmatrix (m16n8k16),
+// each tile scaled by its own power of two so that its largest entry sits
+// below 2^15 (fp16 range is never exceeded, its 11-bit precision matches
+// tf32); the reverse scan keeps its fp32 state and uses tf32 (m16n8k8).
+// The triangular inverse is a forward substitution on the CUDA cores.  Each
+// CTA has 8 warps; a C x D output is split into 16-row strips (warp w & 3)
+// and column halves (warp w >> 2).
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -132,7 +138,6 @@ template <int D>
 struct Tiles {
   static constexpr int FS = D + 4;  // fp32 row stride of C x D and D x D tiles
   static constexpr int BS = D + 8;  // bf16 row stride of C x D tiles
-  static constexpr int NT = D / 16; // n8 tiles per warp of a C x D output
 };
 
 __device__ __forceinline__ void cp16(void* dst, const void* src) {
@@ -140,30 +145,6 @@ __device__ __forceinline__ void cp16(void* dst, const void* src) {
                "l"(src)
                : "memory");
 }
-// every asynchronous copy this thread issued has landed (then a block
-// barrier makes them visible to the other threads)
-__device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// cooperative asynchronous copies global -> shared (256 threads, 16 bytes each)
-template <int D>
-__device__ __forceinline__ void load_bf(bf16* dst, const bf16* src) {  // C x D
-  constexpr int V = C * D / 8;
-#pragma unroll
-  for (int x = threadIdx.x; x < V; x += 256) {
-    const int r = x / (D / 8), c8 = x % (D / 8);
-    cp16(dst + r * Tiles<D>::BS + 8 * c8, src + (size_t)r * D + 8 * c8);
-  }
-}
-template <int ROWS, int COLS, int LD>
-__device__ __forceinline__ void load_f(float* dst, const float* src) {  // ROWS x COLS, source row stride COLS
-  constexpr int V = ROWS * COLS / 4;
-#pragma unroll
-  for (int x = threadIdx.x; x < V; x += 256) {
-    const int r = x / (COLS / 4), c4 = x % (COLS / 4);
-    cp16(dst + r * LD + 4 * c4, src + (size_t)r * COLS + 4 * c4);
-  }
-}
-
 __device__ __forceinline__ float bf(const bf16* p) { return __bfloat162float(*p); }
 
 // the chunk's cumulative log-decay G (from Gb) and gamma, beta into shared memory
@@ -177,18 +158,202 @@ __device__ __forceinline__ void load_scalars(const float* Gb, const float* beta,
   }
 }
 
+// ---------------------------------------------------------- fp16 operands
+using half = __half;
+
+template <int COLS>
+struct H {
+  static constexpr int ld = COLS + 8;  // row stride (halves): 16-byte rows, ldmatrix without bank conflicts
+  static constexpr int bytes(int rows) { return rows * ld * 2; }
+};
+
+__device__ __forceinline__ void ldsm4(const half* p, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"((uint32_t)__cvta_generic_to_shared(p)));
+}
+__device__ __forceinline__ void ldsm4t(const half* p, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"((uint32_t)__cvta_generic_to_shared(p)));
+}
+__device__ __forceinline__ void mma16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// acc[j] (rows m0 .. m0 + 15, columns n0 + 8 j .. + 7) += sum_k A(i, k) B(k, n)
+// over fp16 tiles: A stored [m][k] (AT false) or [k][m] (AT true), B stored
+// [n][k] (BT false) or [k][n] (BT true); NT even, K a multiple of 16
+template <int NT, int K, bool AT, bool BT>
+__device__ __forceinline__ void hmm(float (&acc)[NT][4], int m0, int n0, const half* A, int lda, const half* B,
+                                    int ldb) {
+  static_assert(NT % 2 == 0, "pairs of n8 tiles");
+  const int lane = threadIdx.x & 31, mi = lane >> 3, r8 = lane & 7;
+#pragma unroll
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    uint32_t a[4];
+    if (!AT)
+      ldsm4(A + (m0 + (lane & 15)) * lda + k0 + 8 * (lane >> 4), a);
+    else
+      ldsm4t(A + (k0 + (mi >> 1) * 8 + r8) * lda + m0 + (mi & 1) * 8, a);
+#pragma unroll
+    for (int j = 0; j < NT; j += 2) {
+      uint32_t b[4];
+      if (!BT)
+        ldsm4(B + (n0 + 8 * j + (mi >> 1) * 8 + r8) * ldb + k0 + (mi & 1) * 8, b);
+      else
+        ldsm4t(B + (k0 + (mi & 1) * 8 + r8) * ldb + n0 + 8 * j + (mi >> 1) * 8, b);
+      mma16(acc[j], a, b[0], b[1]);
+      mma16(acc[j + 1], a, b[2], b[3]);
+    }
+  }
+}
+
+// A power of two s with m s < 2^15 (1 for m = 0 or not finite).
+__device__ __forceinline__ float pow2_scale(float m) {
+  if (!(m > 0.f) || !(m < INFINITY)) return 1.f;
+  int e = ((__float_as_int(m) >> 23) & 0xff) - 127;  // m in [2^e, 2^(e+1)) for normal m
+  e = min(max(e, -100), 100);
+  return __int_as_float((127 + 14 - e) << 23);
+}
+
+// The scale of a tile from every thread's partial max |x| (a block-wide
+// collective; red: 8 floats of shared memory).
+__device__ __forceinline__ float block_scale(float m, float* red) {
+  m = warp_max(m);
+  __syncthreads();  // red is free again
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) r = fmaxf(r, red[w]);
+  return pow2_scale(r);
+}
+
+__device__ __forceinline__ float max4(float4 v) {
+  return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+}
+__device__ __forceinline__ uint2 half4(float4 v, float s) {
+  const __half2 a = __floats2half2_rn(v.x * s, v.y * s), b = __floats2half2_rn(v.z * s, v.w * s);
+  return make_uint2(*(const uint32_t*)&a, *(const uint32_t*)&b);
+}
+
+// fp32 ROWS x COLS (row stride src_ld; global or shared) -> scaled fp16 tile;
+// returns the scale.  f(r, c, v) may rewrite each value first.
+template <int ROWS, int COLS, class F>
+__device__ __forceinline__ float tile_h(const float* src, int src_ld, half* dst, float* red, F f) {
+  constexpr int V = ROWS * COLS / 4 / 256;
+  static_assert(V >= 1 && ROWS * COLS % 1024 == 0, "tile");
+  float4 v[V];
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int x = threadIdx.x + 256 * i, r = x / (COLS / 4), c = 4 * (x % (COLS / 4));
+    v[i] = *(const float4*)(src + (size_t)r * src_ld + c);
+    v[i].x = f(r, c, v[i].x);
+    v[i].y = f(r, c + 1, v[i].y);
+    v[i].z = f(r, c + 2, v[i].z);
+    v[i].w = f(r, c + 3, v[i].w);
+    m = fmaxf(m, max4(v[i]));
+  }
+  const float s = block_scale(m, red);
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int x = threadIdx.x + 256 * i, r = x / (COLS / 4), c = 4 * (x % (COLS / 4));
+    *(uint2*)(dst + r * H<COLS>::ld + c) = half4(v[i], s);
+  }
+  return s;
+}
+template <int ROWS, int COLS>
+__device__ __forceinline__ float tile_h(const float* src, int src_ld, half* dst, float* red) {
+  return tile_h<ROWS, COLS>(src, src_ld, dst, red, [](int, int, float x) { return x; });
+}
+
+// bf16 C x D (global, row stride D) -> scaled fp16 tile
+template <int D>
+__device__ __forceinline__ float tile_h_bf(const bf16* src, half* dst, float* red) {
+  constexpr int V = C * D / 8 / 256;
+  uint4 v[V];
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int x = threadIdx.x + 256 * i, r = x / (D / 8), c = 8 * (x % (D / 8));
+    v[i] = *(const uint4*)(src + (size_t)r * D + c);
+    const __nv_bfloat162* h2 = (const __nv_bfloat162*)&v[i];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float2 f = __bfloat1622float2(h2[u]);
+      m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+  const float s = block_scale(m, red);
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int x = threadIdx.x + 256 * i, r = x / (D / 8), c = 8 * (x % (D / 8));
+    const __nv_bfloat162* h2 = (const __nv_bfloat162*)&v[i];
+    uint4 o;
+    uint32_t* o32 = (uint32_t*)&o;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float2 f = __bfloat1622float2(h2[u]);
+      const __half2 hh = __floats2half2_rn(f.x * s, f.y * s);
+      o32[u] = *(const uint32_t*)&hh;
+    }
+    *(uint4*)(dst + r * H<D>::ld + c) = o;
+  }
+  return s;
+}
+
+// accumulators (rows m0.., columns n0..) -> scaled fp16 tile (a block-wide
+// collective: every thread calls it); returns the scale
+template <int NT, int COLS>
+__device__ __forceinline__ float acc_h(const float (&acc)[NT][4], int m0, int n0, half* dst, float* red) {
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(acc[j][e]));
+  const float s = block_scale(m, red);
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const int c0 = n0 + 8 * j + 2 * t;
+    *(__half2*)(dst + (m0 + g) * H<COLS>::ld + c0) = __floats2half2_rn(acc[j][0] * s, acc[j][1] * s);
+    *(__half2*)(dst + (m0 + g + 8) * H<COLS>::ld + c0) = __floats2half2_rn(acc[j][2] * s, acc[j][3] * s);
+  }
+  return s;
+}
+
+template <int NT, class F>
+__device__ __forceinline__ void each_mut(float (&acc)[NT][4], int m0, int n0, F f) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const int c0 = n0 + 8 * j + 2 * t;
+    acc[j][0] = f(m0 + g, c0, acc[j][0], j, 0);
+    acc[j][1] = f(m0 + g, c0 + 1, acc[j][1], j, 1);
+    acc[j][2] = f(m0 + g + 8, c0, acc[j][2], j, 2);
+    acc[j][3] = f(m0 + g + 8, c0 + 1, acc[j][3], j, 3);
+  }
+}
+
 // ------------------------------------------------------------------ prep
 template <int D>
 struct PrepSm {
-  using T = Tiles<D>;
-  static constexpr int offQ = 0;
-  static constexpr int offK = offQ + C * T::BS * 2;
-  static constexpr int offA = offK + C * T::BS * 2;
-  static constexpr int offLi = offA + C * CS * 4;
-  static constexpr int offP = offLi + C * CS * 4;
-  static constexpr int offW = offP + C * CS * 4;
-  static constexpr int offV = offW + C * T::FS * 4;  // G, gamma, beta
-  static constexpr int kBytes = offV + 3 * C * 4;
+  static constexpr int offQ = 0;                              // fp16 [C][D + 8]
+  static constexpr int offK = offQ + H<D>::bytes(C);
+  static constexpr int offW = offK + H<D>::bytes(C);
+  static constexpr int offL = offW + H<D>::bytes(C);          // fp16 [C][C + 8]: Linv diag(beta gamma)
+  static constexpr int offPh = offL + H<C>::bytes(C);         // fp16 [C][C + 8]: P
+  static constexpr int offA = offPh + H<C>::bytes(C);         // fp32 [C][CS]: beta A
+  static constexpr int offLi = offA + C * CS * 4;             // fp32 [C][CS]: Linv
+  static constexpr int offP = offLi + C * CS * 4;             // fp32 [C][CS]: P
+  static constexpr int offV = offP + C * CS * 4;              // G, gamma, beta, reduction
+  static constexpr int kBytes = offV + 3 * C * 4 + 64;
 };
 
 template <int D>
@@ -198,25 +363,24 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
                                                            float* __restrict__ Gb, float* __restrict__ Li_out,
                                                            float* __restrict__ P_out, bf16* __restrict__ W16,
                                                            bf16* __restrict__ Qe16, bf16* __restrict__ Kt16) {
-  using T = Tiles<D>;
   using S = PrepSm<D>;
+  constexpr int NT = D / 16, LD = H<D>::ld, LC = H<C>::ld;
   extern __shared__ __align__(16) uint8_t sm[];
-  bf16* sQ = (bf16*)(sm + S::offQ);
-  bf16* sK = (bf16*)(sm + S::offK);
+  half* hQ = (half*)(sm + S::offQ);
+  half* hK = (half*)(sm + S::offK);
+  half* hW = (half*)(sm + S::offW);
+  half* hL = (half*)(sm + S::offL);
+  half* hP = (half*)(sm + S::offPh);
   float* sA = (float*)(sm + S::offA);
   float* sLi = (float*)(sm + S::offLi);
   float* sP = (float*)(sm + S::offP);
-  float* sW = (float*)(sm + S::offW);
   float* sG = (float*)(sm + S::offV);
   float* sGam = sG + C;
   float* sB = sGam + C;
+  float* red = sB + C;
   const long long chunk = blockIdx.x;
-  const long long bh = chunk / N;
-  const int c = (int)(chunk % N);
-  const size_t row0 = (size_t)bh * L + (size_t)c * C;
+  const size_t row0 = (size_t)(chunk / N) * L + (size_t)(chunk % N) * C;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  load_bf<D>(sQ, q + row0 * D);
-  load_bf<D>(sK, k + row0 * D);
   if (warp == 0) {  // in-chunk cumulative log-decay: two tokens per lane, then a warp scan
     const float x0 = g[row0 + 2 * lane], x1 = g[row0 + 2 * lane + 1];
     float s = x0 + x1;
@@ -233,7 +397,8 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
     Gb[row0 + 2 * lane + 1] = s;
   }
   if (tid < C) sB[tid] = beta[row0 + tid];
-  cp_wait_all();
+  const float sq = tile_h_bf<D>(q + row0 * D, hQ, red);  // (block collectives: they also publish sG, sB)
+  const float sk = tile_h_bf<D>(k + row0 * D, hK, red);
   __syncthreads();
   // beta A (strictly lower) and P (lower, diagonal included)
   {
@@ -241,15 +406,14 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
     float kk[4][4], qk[4][4];
     zero(kk);
     zero(qk);
-    wmm<4, D>(kk, m0, n0, [&](int i, int x) { return bf(sK + i * T::BS + x); },
-              [&](int x, int j) { return bf(sK + j * T::BS + x); });
-    wmm<4, D>(qk, m0, n0, [&](int i, int x) { return bf(sQ + i * T::BS + x); },
-              [&](int x, int j) { return bf(sK + j * T::BS + x); });
+    hmm<4, D, false, false>(kk, m0, n0, hK, LD, hK, LD);
+    hmm<4, D, false, false>(qk, m0, n0, hQ, LD, hK, LD);
+    const float ikk = 1.f / (sk * sk), iqk = scale / (sq * sk);
     each(kk, m0, n0, [&](int i, int j, float v, int, int) {
-      sA[i * CS + j] = j < i ? sB[i] * __expf(sG[i] - sG[j]) * v : 0.f;
+      sA[i * CS + j] = j < i ? sB[i] * __expf(sG[i] - sG[j]) * v * ikk : 0.f;
     });
     each(qk, m0, n0, [&](int i, int j, float v, int, int) {
-      sP[i * CS + j] = j <= i ? scale * __expf(sG[i] - sG[j]) * v : 0.f;
+      sP[i * CS + j] = j <= i ? __expf(sG[i] - sG[j]) * v * iqk : 0.f;
     });
   }
   __syncthreads();
@@ -273,29 +437,32 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
     for (int i = 0; i < C; ++i) sLi[i * CS + j] = x[i];
   }
   __syncthreads();
+  const float sl = tile_h<C, C>(sLi, CS, hL, red, [&](int, int m, float x) { return x * sB[m] * sGam[m]; });
+  const float sp = tile_h<C, C>(sP, CS, hP, red);
+  __syncthreads();
   const int m0 = 16 * (warp & 3), n0 = (warp >> 2) * (D / 2);
   // W = Linv diag(beta gamma) K
+  float acc[NT][4];
+  zero(acc);
+  hmm<NT, C, false, true>(acc, m0, n0, hL, LC, hK, LD);
   {
-    float acc[T::NT][4];
-    zero(acc);
-    wmm<T::NT, C>(acc, m0, n0, [&](int i, int m) { return sLi[i * CS + m] * sB[m] * sGam[m]; },
-                  [&](int m, int n) { return bf(sK + m * T::BS + n); });
-    each(acc, m0, n0, [&](int i, int n, float v, int, int) {
-      sW[i * T::FS + n] = v;
+    const float iw = 1.f / (sl * sk);
+    each_mut(acc, m0, n0, [&](int i, int n, float v, int, int) {
+      v *= iw;
       W16[(row0 + i) * D + n] = __float2bfloat16_rn(v);
+      return v;
     });
   }
+  const float sw = acc_h<NT, D>(acc, m0, n0, hW, red);
   __syncthreads();
   // Q_eff = diag(gamma) Q~ - P W, and K~ = diag(gamma_C / gamma) K
+  zero(acc);
+  hmm<NT, C, false, true>(acc, m0, n0, hP, LC, hW, LD);
   {
-    float acc[T::NT][4];
-    zero(acc);
-    wmm<T::NT, C>(acc, m0, n0, [&](int i, int m) { return sP[i * CS + m]; },
-                  [&](int m, int n) { return sW[m * T::FS + n]; });
-    const float gC = sGam[C - 1];
+    const float ipw = 1.f / (sp * sw), iq = scale / sq, ik = 1.f / sk, gC = sGam[C - 1];
     each(acc, m0, n0, [&](int i, int n, float v, int, int) {
-      Qe16[(row0 + i) * D + n] = __float2bfloat16_rn(sGam[i] * scale * bf(sQ + i * T::BS + n) - v);
-      Kt16[(row0 + i) * D + n] = __float2bfloat16_rn(gC / sGam[i] * bf(sK + i * T::BS + n));
+      Qe16[(row0 + i) * D + n] = __float2bfloat16_rn(sGam[i] * iq * __half2float(hQ[i * LD + n]) - v * ipw);
+      Kt16[(row0 + i) * D + n] = __float2bfloat16_rn(gC / sGam[i] * ik * __half2float(hK[i * LD + n]));
     });
   }
   // Linv and P for the per-chunk gradient kernels
@@ -406,19 +573,18 @@ __global__ void __launch_bounds__(256) gdn_bwd_scan_kernel(const bf16* __restric
   }
 }
 
+
 // -------------------------------------------------------- products with S0
 template <int D>
 struct S0Sm {
-  using T = Tiles<D>;
-  static constexpr int offS = 0;                          // fp32 [D][FS]
-  static constexpr int offK = offS + D * T::FS * 4;       // bf16 [C][BS]
-  static constexpr int offV = offK + C * T::BS * 2;
-  static constexpr int offO = offV + C * T::BS * 2;       // fp32 [C][FS]
-  static constexpr int offLi = offO + C * T::FS * 4;      // fp32 [C][CS]
-  static constexpr int offP = offLi + C * CS * 4;
-  static constexpr int offVh = offP + C * CS * 4;         // fp32 [C][FS]
-  static constexpr int offVec = offVh + C * T::FS * 4;    // G, gamma, beta, dG
-  static constexpr int kBytes = offVec + 4 * C * 4;
+  static constexpr int offS = 0;                          // fp16 [D][D + 8]: S0
+  static constexpr int offK = offS + H<D>::bytes(D);      // fp16 [C][D + 8]
+  static constexpr int offO = offK + H<D>::bytes(C);      // dO
+  static constexpr int offVh = offO + H<D>::bytes(C);     // Vh
+  static constexpr int offL = offVh + H<D>::bytes(C);     // fp16 [C][C + 8]: Linv diag(beta)
+  static constexpr int offP = offL + H<C>::bytes(C);      // P
+  static constexpr int offVec = offP + H<C>::bytes(C);    // G, gamma, beta, dG, reduction
+  static constexpr int kBytes = offVec + 4 * C * 4 + 64;
 };
 
 template <int D>
@@ -427,73 +593,75 @@ __global__ void __launch_bounds__(256) gdn_bwd_s0_kernel(
     const float* __restrict__ S0, const float* __restrict__ Li, const float* __restrict__ Pg,
     const float* __restrict__ Gb, const float* __restrict__ beta, int L, int N, float scale, float* __restrict__ Vh,
     float* __restrict__ Ug, float* __restrict__ PtdO, float* __restrict__ dq, float* __restrict__ dGs) {
-  using T = Tiles<D>;
   using S = S0Sm<D>;
+  constexpr int NT = D / 16, LD = H<D>::ld, LC = H<C>::ld;
   extern __shared__ __align__(16) uint8_t sm[];
-  float* sS = (float*)(sm + S::offS);
-  bf16* sK = (bf16*)(sm + S::offK);
-  bf16* sV = (bf16*)(sm + S::offV);
-  float* sO = (float*)(sm + S::offO);
-  float* sLi = (float*)(sm + S::offLi);
-  float* sP = (float*)(sm + S::offP);
-  float* sVh = (float*)(sm + S::offVh);
+  half* hS = (half*)(sm + S::offS);
+  half* hK = (half*)(sm + S::offK);
+  half* hO = (half*)(sm + S::offO);
+  half* hVh = (half*)(sm + S::offVh);
+  half* hL = (half*)(sm + S::offL);
+  half* hP = (half*)(sm + S::offP);
   float* sG = (float*)(sm + S::offVec);
   float* sGam = sG + C;
   float* sB = sGam + C;
   float* sdG = sB + C;
+  float* red = sdG + C;
   const long long chunk = blockIdx.x;
   const size_t row0 = (size_t)(chunk / N) * L + (size_t)(chunk % N) * C;
   const int tid = threadIdx.x, warp = tid >> 5;
-  load_f<D, D, T::FS>(sS, S0 + (size_t)chunk * D * D);
-  load_bf<D>(sK, k + row0 * D);
-  load_bf<D>(sV, v + row0 * D);
-  load_f<C, D, T::FS>(sO, dO + row0 * D);
-  load_f<C, C, CS>(sLi, Li + (size_t)chunk * C * C);
-  load_f<C, C, CS>(sP, Pg + (size_t)chunk * C * C);
   load_scalars(Gb, beta, row0, sG, sGam, sB);
   if (tid < C) sdG[tid] = 0.f;
-  cp_wait_all();
+  const float ss = tile_h<D, D>(S0 + (size_t)chunk * D * D, D, hS, red);
+  const float sk = tile_h_bf<D>(k + row0 * D, hK, red);
+  const float so = tile_h<C, D>(dO + row0 * D, D, hO, red);
+  const float sl = tile_h<C, C>(Li + (size_t)chunk * C * C, C, hL, red, [&](int, int m, float x) { return x * sB[m]; });
+  const float sp = tile_h<C, C>(Pg + (size_t)chunk * C * C, C, hP, red);
   __syncthreads();
   const int m0 = 16 * (warp & 3), n0 = (warp >> 2) * (D / 2);
-  {  // Vh = V - diag(gamma) K S0^T
-    float acc[T::NT][4];
-    zero(acc);
-    wmm<T::NT, D>(acc, m0, n0, [&](int i, int x) { return bf(sK + i * T::BS + x); },
-                  [&](int x, int n) { return sS[n * T::FS + x]; });
-    each(acc, m0, n0, [&](int i, int n, float val, int, int) {
-      const float vh = bf(sV + i * T::BS + n) - sGam[i] * val;
-      sVh[i * T::FS + n] = vh;
-      Vh[(row0 + i) * D + n] = vh;
+  float acc[NT][4];
+  // Vh = V - diag(gamma) K S0^T
+  zero(acc);
+  hmm<NT, D, false, false>(acc, m0, n0, hK, LD, hS, LD);
+  {
+    const float iks = 1.f / (sk * ss);
+    each_mut(acc, m0, n0, [&](int i, int n, float val, int, int) {
+      const size_t o = (row0 + i) * D + n;
+      const float vh = __bfloat162float(v[o]) - sGam[i] * val * iks;
+      Vh[o] = vh;
+      return vh;
     });
   }
-  {  // dO S0: dq += scale gamma_i (dO S0)_i; dG_i += gamma_i (dO S0)_i . q~_i
-    float acc[T::NT][4];
-    zero(acc);
-    wmm<T::NT, D>(acc, m0, n0, [&](int i, int a) { return sO[i * T::FS + a]; },
-                  [&](int a, int n) { return sS[a * T::FS + n]; });
+  const float svh = acc_h<NT, D>(acc, m0, n0, hVh, red);
+  // dO S0: dq += scale gamma_i (dO S0)_i; dG_i += gamma_i (dO S0)_i . q~_i
+  zero(acc);
+  hmm<NT, D, false, true>(acc, m0, n0, hO, LD, hS, LD);
+  {
+    const float ios = scale / (so * ss);
     float lo = 0.f, hi = 0.f;
     each(acc, m0, n0, [&](int i, int n, float val, int, int e) {
       const size_t o = (row0 + i) * D + n;
-      dq[o] += scale * sGam[i] * val;
-      const float d = scale * sGam[i] * val * __bfloat162float(q[o]);
-      if (e < 2) lo += d; else hi += d;
+      const float x = sGam[i] * val * ios;
+      dq[o] += x;
+      const float dd = x * __bfloat162float(q[o]);
+      if (e < 2) lo += dd; else hi += dd;
     });
     add_rows(lo, hi, m0, sdG);
   }
-  __syncthreads();
-  {  // U = Linv diag(beta) Vh
-    float acc[T::NT][4];
-    zero(acc);
-    wmm<T::NT, C>(acc, m0, n0, [&](int i, int m) { return sLi[i * CS + m] * sB[m]; },
-                  [&](int m, int n) { return sVh[m * T::FS + n]; });
-    each(acc, m0, n0, [&](int i, int n, float val, int, int) { Ug[(row0 + i) * D + n] = val; });
+  __syncthreads();  // hVh complete
+  // U = Linv diag(beta) Vh
+  zero(acc);
+  hmm<NT, C, false, true>(acc, m0, n0, hL, LC, hVh, LD);
+  {
+    const float iu = 1.f / (sl * svh);
+    each(acc, m0, n0, [&](int i, int n, float val, int, int) { Ug[(row0 + i) * D + n] = val * iu; });
   }
-  {  // P^T dO
-    float acc[T::NT][4];
-    zero(acc);
-    wmm<T::NT, C>(acc, m0, n0, [&](int i, int m) { return sP[m * CS + i]; },
-                  [&](int m, int n) { return sO[m * T::FS + n]; });
-    each(acc, m0, n0, [&](int i, int n, float val, int, int) { PtdO[(row0 + i) * D + n] = val; });
+  // P^T dO
+  zero(acc);
+  hmm<NT, C, true, true>(acc, m0, n0, hP, LC, hO, LD);
+  {
+    const float ipo = 1.f / (sp * so);
+    each(acc, m0, n0, [&](int i, int n, float val, int, int) { PtdO[(row0 + i) * D + n] = val * ipo; });
   }
   __syncthreads();
   if (tid < C) dGs[row0 + tid] = sdG[tid];
@@ -502,14 +670,13 @@ __global__ void __launch_bounds__(256) gdn_bwd_s0_kernel(
 // ----------------------------------------------------- products with dS_C
 template <int D>
 struct DsSm {
-  using T = Tiles<D>;
-  static constexpr int offS = 0;                          // fp32 [D][FS]: dS_C, then S0
-  static constexpr int offK = offS + D * T::FS * 4;       // bf16 [C][BS]
-  static constexpr int offU = offK + C * T::BS * 2;       // fp32 [C][FS]
-  static constexpr int offLi = offU + C * T::FS * 4;      // fp32 [C][CS]
-  static constexpr int offD = offLi + C * CS * 4;         // fp32 [C][FS]: dU, then Y
-  static constexpr int offVec = offD + C * T::FS * 4;     // G, gamma, beta, dG, dbeta, reduction
-  static constexpr int kBytes = offVec + 6 * C * 4;
+  static constexpr int offS = 0;                          // fp16 [D][D + 8]: dS_C, then S0
+  static constexpr int offK = offS + H<D>::bytes(D);      // fp16 [C][D + 8]
+  static constexpr int offU = offK + H<D>::bytes(C);
+  static constexpr int offD = offU + H<D>::bytes(C);      // dU, then diag(beta) Y
+  static constexpr int offL = offD + H<D>::bytes(C);      // fp16 [C][C + 8]: Linv
+  static constexpr int offVec = offL + H<C>::bytes(C);    // G, gamma, beta, dG, dbeta, reduction
+  static constexpr int kBytes = offVec + 5 * C * 4 + 64;
 };
 
 template <int D>
@@ -519,109 +686,107 @@ __global__ void __launch_bounds__(256) gdn_bwd_ds_kernel(
     const float* __restrict__ Vh, const float* __restrict__ Gb, const float* __restrict__ beta,
     const uint8_t* __restrict__ sel, int L, int N, float* __restrict__ Yg, float* __restrict__ dv,
     float* __restrict__ dk, float* __restrict__ dGs, float* __restrict__ dbeta) {
-  using T = Tiles<D>;
   using S = DsSm<D>;
+  constexpr int NT = D / 16, LD = H<D>::ld, LC = H<C>::ld;
   extern __shared__ __align__(16) uint8_t sm[];
-  float* sS = (float*)(sm + S::offS);
-  bf16* sK = (bf16*)(sm + S::offK);
-  float* sU = (float*)(sm + S::offU);
-  float* sLi = (float*)(sm + S::offLi);
-  float* sD = (float*)(sm + S::offD);
+  half* hS = (half*)(sm + S::offS);
+  half* hK = (half*)(sm + S::offK);
+  half* hU = (half*)(sm + S::offU);
+  half* hD = (half*)(sm + S::offD);
+  half* hL = (half*)(sm + S::offL);
   float* sG = (float*)(sm + S::offVec);
   float* sGam = sG + C;
   float* sB = sGam + C;
   float* sdG = sB + C;
   float* sdB = sdG + C;
-  float* sRed = sdB + C;
+  float* red = sdB + C;  // [0..7] tile maxima, [8] the last token's extra dG, [9] <dS_C, S0>
   const long long chunk = blockIdx.x;
   const int c = (int)(chunk % N);
   const size_t row0 = (size_t)(chunk / N) * L + (size_t)c * C;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool committed = sel[chunk] != 0 && c < N - 1;
-  load_bf<D>(sK, k + row0 * D);
-  load_f<C, D, T::FS>(sU, Ug + row0 * D);
-  load_f<C, C, CS>(sLi, Li + (size_t)chunk * C * C);
-  load_f<C, D, T::FS>(sD, PtdO + row0 * D);
-  if (committed) load_f<D, D, T::FS>(sS, dSC + (size_t)chunk * D * D);
   load_scalars(Gb, beta, row0, sG, sGam, sB);
   if (tid < C) sdG[tid] = sdB[tid] = 0.f;
-  if (tid == 0) sRed[0] = 0.f;
-  cp_wait_all();
-  __syncthreads();
-  const int m0 = 16 * (warp & 3), n0 = (warp >> 2) * (D / 2);
-  if (committed) {
-    const float gC = sGam[C - 1];
-    {  // dU += K~ dS_C^T
-      float acc[T::NT][4];
-      zero(acc);
-      wmm<T::NT, D>(acc, m0, n0, [&](int i, int x) { return gC / sGam[i] * bf(sK + i * T::BS + x); },
-                    [&](int x, int a) { return sS[a * T::FS + x]; });
-      each(acc, m0, n0, [&](int i, int a, float val, int, int) { sD[i * T::FS + a] += val; });
-    }
-    {  // U dS_C: dk += diag(gamma_C / gamma) (U dS_C); dG_j -= (U dS_C)_j . K~_j; the last token gains their sum
-      float acc[T::NT][4];
-      zero(acc);
-      wmm<T::NT, D>(acc, m0, n0, [&](int i, int a) { return sU[i * T::FS + a]; },
-                    [&](int a, int n) { return sS[a * T::FS + n]; });
-      float lo = 0.f, hi = 0.f;
-      each(acc, m0, n0, [&](int i, int n, float val, int, int e) {
-        const float f = gC / sGam[i];
-        dk[(row0 + i) * D + n] += f * val;
-        const float d = val * f * bf(sK + i * T::BS + n);
-        if (e < 2) lo -= d; else hi -= d;
-      });
-      float tot = -(lo + hi);
-      add_rows(lo, hi, m0, sdG);
-      tot = warp_sum(tot);
-      if (lane == 0) atomicAdd(sRed, tot);
-    }
-    {  // gamma_C <dS_C, S0> into the last token
-      const float* s0 = S0 + (size_t)chunk * D * D;
-      float acc = 0.f;
-      for (int x = tid; x < D * D / 4; x += 256) {
-        const int a = x / (D / 4), c4 = x % (D / 4);
-        const float4 u = *(const float4*)(sS + a * T::FS + 4 * c4);
-        const float4 w = *(const float4*)(s0 + (size_t)a * D + 4 * c4);
-        acc += u.x * w.x + u.y * w.y + u.z * w.z + u.w * w.w;
-      }
-      acc = warp_sum(acc);
-      if (lane == 0) atomicAdd(sRed, gC * acc);
-    }
+  if (tid < 2) red[8 + tid] = 0.f;
+  const float sk = tile_h_bf<D>(k + row0 * D, hK, red);
+  const float su = tile_h<C, D>(Ug + row0 * D, D, hU, red);
+  const float sl = tile_h<C, C>(Li + (size_t)chunk * C * C, C, hL, red);
+  float sd = 1.f;
+  if (committed) {  // dS_C, and <dS_C, S0> on the way
+    const float* s0 = S0 + (size_t)chunk * D * D;
+    float dot = 0.f;
+    sd = tile_h<D, D>(dSC + (size_t)chunk * D * D, D, hS, red, [&](int r, int cc, float x) {
+      dot += x * s0[(size_t)r * D + cc];
+      return x;
+    });
+    dot = warp_sum(dot);
+    if (lane == 0) atomicAdd(red + 9, dot);
   }
   __syncthreads();
-  if (tid == 0) sdG[C - 1] += sRed[0];
-  // Y = Linv^T dU; dv += diag(beta) Y; dbeta_i = Y_i . Vh_i
-  float accY[T::NT][4];
-  zero(accY);
-  wmm<T::NT, C>(accY, m0, n0, [&](int i, int m) { return sLi[m * CS + i]; },
-                [&](int m, int n) { return sD[m * T::FS + n]; });
-  __syncthreads();  // every read of dU is done
+  const int m0 = 16 * (warp & 3), n0 = (warp >> 2) * (D / 2);
+  const float gC = sGam[C - 1];
+  // dU = P^T dO + K~ dS_C^T (registers, fp32)
+  float dU[NT][4];
+  zero(dU);
+  if (committed) hmm<NT, D, false, false>(dU, m0, n0, hK, LD, hS, LD);
   {
+    const float ikd = 1.f / (sk * sd);
+    each_mut(dU, m0, n0, [&](int i, int a, float val, int, int) {
+      return PtdO[(row0 + i) * D + a] + gC / sGam[i] * val * ikd;
+    });
+  }
+  if (committed) {  // U dS_C: dk += diag(gamma_C / gamma) (U dS_C); dG_j -= (U dS_C)_j . K~_j; the last token gains their sum
+    float acc[NT][4];
+    zero(acc);
+    hmm<NT, D, false, true>(acc, m0, n0, hU, LD, hS, LD);
+    const float iud = 1.f / (su * sd), ik = 1.f / sk;
     float lo = 0.f, hi = 0.f;
-    each(accY, m0, n0, [&](int i, int n, float y, int, int e) {
+    each(acc, m0, n0, [&](int i, int n, float val, int, int e) {
+      const float f = gC / sGam[i];
+      const float x = f * val * iud;
+      dk[(row0 + i) * D + n] += x;
+      const float dd = x * ik * __half2float(hK[i * LD + n]);
+      if (e < 2) lo -= dd; else hi -= dd;
+    });
+    float tot = warp_sum(-(lo + hi));
+    add_rows(lo, hi, m0, sdG);
+    if (lane == 0) atomicAdd(red + 8, tot);
+  }
+  const float sdu = acc_h<NT, D>(dU, m0, n0, hD, red);  // (its barriers also order the reads of dS_C above)
+  __syncthreads();
+  if (tid == 0) sdG[C - 1] += red[8] + gC * red[9];
+  // Y = Linv^T dU; dv += diag(beta) Y; dbeta_i = Y_i . Vh_i
+  float acc[NT][4];
+  zero(acc);
+  hmm<NT, C, true, true>(acc, m0, n0, hL, LC, hD, LD);
+  {
+    const float iy = 1.f / (sl * sdu);
+    float lo = 0.f, hi = 0.f;
+    each_mut(acc, m0, n0, [&](int i, int n, float val, int, int e) {
       const size_t o = (row0 + i) * D + n;
-      sD[i * T::FS + n] = y;
+      const float y = val * iy;
       Yg[o] = y;
       dv[o] += sB[i] * y;
-      const float d = y * Vh[o];
-      if (e < 2) lo += d; else hi += d;
+      const float dd = y * Vh[o];
+      if (e < 2) lo += dd; else hi += dd;
+      return sB[i] * y;
     });
     add_rows(lo, hi, m0, sdB);
   }
-  // S0 for the dVh S0 term (every read of dS_C ended at the barrier above)
-  load_f<D, D, T::FS>(sS, S0 + (size_t)chunk * D * D);
-  cp_wait_all();
+  __syncthreads();  // every read of dU (and of dS_C) is done
+  const float sy = acc_h<NT, D>(acc, m0, n0, hD, red);
+  const float ss = tile_h<D, D>(S0 + (size_t)chunk * D * D, D, hS, red);
   __syncthreads();
   {  // dk -= diag(gamma) dVh S0; dG_i -= gamma_i (dVh S0)_i . k_i
-    float acc[T::NT][4];
     zero(acc);
-    wmm<T::NT, D>(acc, m0, n0, [&](int i, int a) { return sB[i] * sD[i * T::FS + a]; },
-                  [&](int a, int n) { return sS[a * T::FS + n]; });
+    hmm<NT, D, false, true>(acc, m0, n0, hD, LD, hS, LD);
+    const float iys = 1.f / (sy * ss), ik = 1.f / sk;
     float lo = 0.f, hi = 0.f;
     each(acc, m0, n0, [&](int i, int n, float val, int, int e) {
-      dk[(row0 + i) * D + n] -= sGam[i] * val;
-      const float d = sGam[i] * val * bf(sK + i * T::BS + n);
-      if (e < 2) lo -= d; else hi -= d;
+      const float x = sGam[i] * val * iys;
+      dk[(row0 + i) * D + n] -= x;
+      const float dd = x * ik * __half2float(hK[i * LD + n]);
+      if (e < 2) lo -= dd; else hi -= dd;
     });
     add_rows(lo, hi, m0, sdG);
   }
@@ -635,16 +800,15 @@ __global__ void __launch_bounds__(256) gdn_bwd_ds_kernel(
 // ---------------------------------------------------- C x C products, dg
 template <int D>
 struct CcSm {
-  using T = Tiles<D>;
-  static constexpr int offQ = 0;                          // bf16 [C][BS]
-  static constexpr int offK = offQ + C * T::BS * 2;
-  static constexpr int offO = offK + C * T::BS * 2;       // fp32 [C][FS]
-  static constexpr int offU = offO + C * T::FS * 4;
-  static constexpr int offY = offU + C * T::FS * 4;
-  static constexpr int offA = offY + C * T::FS * 4;       // fp32 [C][CS]: A~
-  static constexpr int offP = offA + C * CS * 4;          // fp32 [C][CS]: dP . R
-  static constexpr int offVec = offP + C * CS * 4;        // G, gamma, beta, dG, dbeta
-  static constexpr int kBytes = offVec + 5 * C * 4;
+  static constexpr int offQ = 0;                          // fp16 [C][D + 8]
+  static constexpr int offK = offQ + H<D>::bytes(C);
+  static constexpr int offO = offK + H<D>::bytes(C);
+  static constexpr int offU = offO + H<D>::bytes(C);
+  static constexpr int offY = offU + H<D>::bytes(C);
+  static constexpr int offA = offY + H<D>::bytes(C);      // fp16 [C][C + 8]: A~
+  static constexpr int offP = offA + H<C>::bytes(C);      // dP . R
+  static constexpr int offVec = offP + H<C>::bytes(C);    // G, gamma, beta, dG, dbeta, reduction
+  static constexpr int kBytes = offVec + 5 * C * 4 + 64;
 };
 
 template <int D>
@@ -653,33 +817,34 @@ __global__ void __launch_bounds__(256) gdn_bwd_cc_kernel(
     const float* __restrict__ Ug, const float* __restrict__ Yg, const float* __restrict__ Gb,
     const float* __restrict__ beta, int L, int N, float scale, float* __restrict__ dq, float* __restrict__ dk,
     const float* __restrict__ dGs, float* __restrict__ dbeta, float* __restrict__ dg) {
-  using T = Tiles<D>;
   using S = CcSm<D>;
+  constexpr int NT = D / 16, LD = H<D>::ld, LC = H<C>::ld;
   extern __shared__ __align__(16) uint8_t sm[];
-  bf16* sQ = (bf16*)(sm + S::offQ);
-  bf16* sK = (bf16*)(sm + S::offK);
-  float* sO = (float*)(sm + S::offO);
-  float* sU = (float*)(sm + S::offU);
-  float* sY = (float*)(sm + S::offY);
-  float* sA = (float*)(sm + S::offA);
-  float* sP = (float*)(sm + S::offP);
+  half* hQ = (half*)(sm + S::offQ);
+  half* hK = (half*)(sm + S::offK);
+  half* hO = (half*)(sm + S::offO);
+  half* hU = (half*)(sm + S::offU);
+  half* hY = (half*)(sm + S::offY);
+  half* hA = (half*)(sm + S::offA);
+  half* hPm = (half*)(sm + S::offP);
   float* sG = (float*)(sm + S::offVec);
   float* sGam = sG + C;
   float* sB = sGam + C;
   float* sdG = sB + C;
   float* sdB = sdG + C;
+  float* red = sdB + C;
   const long long chunk = blockIdx.x;
   const size_t row0 = (size_t)(chunk / N) * L + (size_t)(chunk % N) * C;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  load_bf<D>(sQ, q + row0 * D);
-  load_bf<D>(sK, k + row0 * D);
-  load_f<C, D, T::FS>(sO, dO + row0 * D);
-  load_f<C, D, T::FS>(sU, Ug + row0 * D);
-  load_f<C, D, T::FS>(sY, Yg + row0 * D);
   load_scalars(Gb, beta, row0, sG, sGam, sB);
   if (tid < C) sdG[tid] = sdB[tid] = 0.f;
-  cp_wait_all();
+  const float sq = tile_h_bf<D>(q + row0 * D, hQ, red);
+  const float sk = tile_h_bf<D>(k + row0 * D, hK, red);
+  const float so = tile_h<C, D>(dO + row0 * D, D, hO, red);
+  const float su = tile_h<C, D>(Ug + row0 * D, D, hU, red);
+  const float sy = tile_h<C, D>(Yg + row0 * D, D, hY, red);
   __syncthreads();
+  float sa, spm;
   {
     const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);
     // dL = -strict_lower(Y U^T), A = R . K K^T: dA = diag(beta) dL, A~ = dA . R,
@@ -688,77 +853,81 @@ __global__ void __launch_bounds__(256) gdn_bwd_cc_kernel(
       float yu[4][4], kk[4][4];
       zero(yu);
       zero(kk);
-      wmm<4, D>(yu, m0, n0, [&](int i, int a) { return sY[i * T::FS + a]; },
-                [&](int a, int j) { return sU[j * T::FS + a]; });
-      wmm<4, D>(kk, m0, n0, [&](int i, int x) { return bf(sK + i * T::BS + x); },
-                [&](int x, int j) { return bf(sK + j * T::BS + x); });
+      hmm<4, D, false, false>(yu, m0, n0, hY, LD, hU, LD);
+      hmm<4, D, false, false>(kk, m0, n0, hK, LD, hK, LD);
+      const float iyu = 1.f / (sy * su), ikk = 1.f / (sk * sk);
       float rlo = 0.f, rhi = 0.f, blo = 0.f, bhi = 0.f, col[4][2];
 #pragma unroll
       for (int j = 0; j < 4; ++j) col[j][0] = col[j][1] = 0.f;
-      each(yu, m0, n0, [&](int i, int jj, float val, int j, int e) {
+      each_mut(yu, m0, n0, [&](int i, int jj, float val, int j, int e) {
         float at = 0.f;
         if (jj < i) {
           const float r = __expf(sG[i] - sG[jj]);
-          const float A = r * kk[j][e];
-          const float dL = -val;
+          const float A = r * kk[j][e] * ikk;
+          const float dL = -val * iyu;
           const float dA = sB[i] * dL;
           const float x = dA * A;
           if (e < 2) rlo += x, blo += dL * A; else rhi += x, bhi += dL * A;
           col[j][e & 1] -= x;
           at = dA * r;
         }
-        sA[i * CS + jj] = at;
+        return at;
       });
       add_rows(rlo, rhi, m0, sdG);
       add_rows(blo, bhi, m0, sdB);
       add_cols<4>(col, n0, sdG);
+      sa = acc_h<4, C>(yu, m0, n0, hA, red);
     }
     // dP = lower(dO U^T), P = R . Q~ K^T: dPm = dP . R, dG += row sums - column sums of dP . P
     {
       float ou[4][4], qk[4][4];
       zero(ou);
       zero(qk);
-      wmm<4, D>(ou, m0, n0, [&](int i, int a) { return sO[i * T::FS + a]; },
-                [&](int a, int j) { return sU[j * T::FS + a]; });
-      wmm<4, D>(qk, m0, n0, [&](int i, int x) { return bf(sQ + i * T::BS + x); },
-                [&](int x, int j) { return bf(sK + j * T::BS + x); });
+      hmm<4, D, false, false>(ou, m0, n0, hO, LD, hU, LD);
+      hmm<4, D, false, false>(qk, m0, n0, hQ, LD, hK, LD);
+      const float iou = 1.f / (so * su), iqk = scale / (sq * sk);
       float rlo = 0.f, rhi = 0.f, col[4][2];
 #pragma unroll
       for (int j = 0; j < 4; ++j) col[j][0] = col[j][1] = 0.f;
-      each(ou, m0, n0, [&](int i, int jj, float val, int j, int e) {
+      each_mut(ou, m0, n0, [&](int i, int jj, float val, int j, int e) {
         float pm = 0.f;
         if (jj <= i) {
           const float r = __expf(sG[i] - sG[jj]);
-          const float P = r * scale * qk[j][e];
-          const float x = val * P;
+          const float P = r * qk[j][e] * iqk;
+          const float dP = val * iou;
+          const float x = dP * P;
           if (e < 2) rlo += x; else rhi += x;
           col[j][e & 1] -= x;
-          pm = val * r;
+          pm = dP * r;
         }
-        sP[i * CS + jj] = pm;
+        return pm;
       });
       add_rows(rlo, rhi, m0, sdG);
       add_cols<4>(col, n0, sdG);
+      spm = acc_h<4, C>(ou, m0, n0, hPm, red);
     }
   }
   __syncthreads();
   {
     const int m0 = 16 * (warp & 3), n0 = (warp >> 2) * (D / 2);
     {  // dq += scale (dP . R) K
-      float acc[T::NT][4];
+      float acc[NT][4];
       zero(acc);
-      wmm<T::NT, C>(acc, m0, n0, [&](int i, int j) { return sP[i * CS + j]; },
-                    [&](int j, int n) { return bf(sK + j * T::BS + n); });
-      each(acc, m0, n0, [&](int i, int n, float val, int, int) { dq[(row0 + i) * D + n] += scale * val; });
+      hmm<NT, C, false, true>(acc, m0, n0, hPm, LC, hK, LD);
+      const float f = scale / (spm * sk);
+      each(acc, m0, n0, [&](int i, int n, float val, int, int) { dq[(row0 + i) * D + n] += f * val; });
     }
     {  // dk += (dP . R)^T Q~ + (A~ + A~^T) K
-      float acc[T::NT][4];
-      zero(acc);
-      wmm<T::NT, C>(acc, m0, n0, [&](int i, int j) { return sP[j * CS + i]; },
-                    [&](int j, int n) { return scale * bf(sQ + j * T::BS + n); });
-      wmm<T::NT, C>(acc, m0, n0, [&](int i, int j) { return sA[i * CS + j] + sA[j * CS + i]; },
-                    [&](int j, int n) { return bf(sK + j * T::BS + n); });
-      each(acc, m0, n0, [&](int i, int n, float val, int, int) { dk[(row0 + i) * D + n] += val; });
+      float a1[NT][4], a2[NT][4];
+      zero(a1);
+      zero(a2);
+      hmm<NT, C, true, true>(a1, m0, n0, hPm, LC, hQ, LD);
+      hmm<NT, C, false, true>(a2, m0, n0, hA, LC, hK, LD);
+      hmm<NT, C, true, true>(a2, m0, n0, hA, LC, hK, LD);
+      const float f1 = scale / (spm * sq), f2 = 1.f / (sa * sk);
+      each(a1, m0, n0, [&](int i, int n, float val, int j, int e) {
+        dk[(row0 + i) * D + n] += f1 * val + f2 * a2[j][e];
+      });
     }
   }
   __syncthreads();
