@@ -351,8 +351,7 @@ struct PrepSm {
   static constexpr int offPh = offL + H<C>::bytes(C);         // fp16 [C][C + 8]: P
   static constexpr int offA = offPh + H<C>::bytes(C);         // fp32 [C][CS]: beta A
   static constexpr int offLi = offA + C * CS * 4;             // fp32 [C][CS]: Linv
-  static constexpr int offP = offLi + C * CS * 4;             // fp32 [C][CS]: P
-  static constexpr int offV = offP + C * CS * 4;              // G, gamma, beta, reduction
+  static constexpr int offV = offLi + C * CS * 4;             // G, gamma, beta, reduction
   static constexpr int kBytes = offV + 3 * C * 4 + 64;
 };
 
@@ -373,7 +372,6 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
   half* hP = (half*)(sm + S::offPh);
   float* sA = (float*)(sm + S::offA);
   float* sLi = (float*)(sm + S::offLi);
-  float* sP = (float*)(sm + S::offP);
   float* sG = (float*)(sm + S::offV);
   float* sGam = sG + C;
   float* sB = sGam + C;
@@ -401,6 +399,7 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
   const float sk = tile_h_bf<D>(k + row0 * D, hK, red);
   __syncthreads();
   // beta A (strictly lower) and P (lower, diagonal included)
+  float sp;
   {
     const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);
     float kk[4][4], qk[4][4];
@@ -412,9 +411,12 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
     each(kk, m0, n0, [&](int i, int j, float v, int, int) {
       sA[i * CS + j] = j < i ? sB[i] * __expf(sG[i] - sG[j]) * v * ikk : 0.f;
     });
-    each(qk, m0, n0, [&](int i, int j, float v, int, int) {
-      sP[i * CS + j] = j <= i ? __expf(sG[i] - sG[j]) * v * iqk : 0.f;
+    each_mut(qk, m0, n0, [&](int i, int j, float v, int, int) {
+      const float pv = j <= i ? __expf(sG[i] - sG[j]) * v * iqk : 0.f;
+      P_out[(size_t)chunk * C * C + i * C + j] = pv;
+      return pv;
     });
+    sp = acc_h<4, C>(qk, m0, n0, hP, red);
   }
   __syncthreads();
   // Linv = (I + beta A)^{-1} by forward substitution, one column per thread
@@ -438,7 +440,6 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
   }
   __syncthreads();
   const float sl = tile_h<C, C>(sLi, CS, hL, red, [&](int, int m, float x) { return x * sB[m] * sGam[m]; });
-  const float sp = tile_h<C, C>(sP, CS, hP, red);
   __syncthreads();
   const int m0 = 16 * (warp & 3), n0 = (warp >> 2) * (D / 2);
   // W = Linv diag(beta gamma) K
@@ -465,11 +466,10 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
       Kt16[(row0 + i) * D + n] = __float2bfloat16_rn(gC / sGam[i] * ik * __half2float(hK[i * LD + n]));
     });
   }
-  // Linv and P for the per-chunk gradient kernels
+  // Linv for the per-chunk gradient kernels (P was written above)
   for (int x = tid; x < C * C / 4; x += 256) {
     const int i = x / (C / 4), j4 = x % (C / 4);
     *(float4*)(Li_out + (size_t)chunk * C * C + i * C + 4 * j4) = *(const float4*)(sLi + i * CS + 4 * j4);
-    *(float4*)(P_out + (size_t)chunk * C * C + i * C + 4 * j4) = *(const float4*)(sP + i * CS + 4 * j4);
   }
 }
 
