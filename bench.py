@@ -869,8 +869,9 @@ def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):
       merge_bwd    HBM: per token it reads q, dout (bf16) and o_soft, o_lin
                    (fp32) and writes d o_soft (bf16), d o_lin, dq (fp32) and
                    delta: 22 d + 4 bytes;
-      softmax_bwd  bf16 tensor (warp-level MMAs): 10 d FLOP per visible
-                   (query, key) pair (scores recomputed, dP, dq, dk, dv);
+      softmax_bwd  bf16 tensor (tcgen05): 10 d FLOP per visible (query,
+                   key) pair (scores recomputed, dP, dq, dk, dv), plus the
+                   compaction of the softmax-chunk lists;
       gdn_bwd      the Gated DeltaNet stage and the per-chunk C x C stage
                    together, tf32 tensor (warp-level MMAs): per chunk the
                    forward's chunk factors and scan that recompute the chunk
@@ -945,7 +946,7 @@ def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):
             ach, peak, unit, src = amount / (sms / 1e3) / 1e9, pk["hbm_gbs"], "GB/s", f"{pk['source']} HBM copy"
         elif bound == "tensor":
             ach, peak, unit = amount / (sms / 1e3) / 1e12, pk["bf16_tflops_sustained"], "TFLOP/s"
-            src = f"{pk['source']} bf16 sustained (the kernels use mma.sync, not tcgen05)"
+            src = f"{pk['source']} bf16 sustained (tcgen05)"
         else:
             ach, peak, unit = amount / (sms / 1e3) / 1e12, pk["bf16_tflops_sustained"] * 1.1 / 2.25, "TFLOP/s"
             src = f"{pk['source']} bf16 sustained x 1.1 / 2.25 (tf32; mma.sync m16n8k8)"

@@ -628,6 +628,7 @@ struct BwdLayout {
   float *Sc, *Tk, *dSx, *pcol, *psc;
   // bf16 layers: the forward recompute of the chunk-start states, then the
   // chunkwise adjoint
+  int32_t *nprev, *sel_idx;
   float *fG, *fgate;
   void *fW, *fU, *fP, *fol16;
   int* ferr;
@@ -655,6 +656,8 @@ static size_t bwd_layout(const Problem& p, int dtype, uint8_t* base, BwdLayout* 
     l.pcol = (float*)take((size_t)kRowSplit * rows * 2 * p.d * 4);  // the state halves' column sums per token
     l.psc = (float*)take((size_t)kRowSplit * rows * 4 * 4);     // and their scalars
   } else {
+    l.nprev = (int32_t*)take(chunks * 4);    // compacted softmax-chunk lists
+    l.sel_idx = (int32_t*)take(chunks * 4);
     l.fG = (float*)take(rows * 4);        // forward chunk factors (recomputed)
     l.fW = take(rows * p.d * 2);
     l.fU = take(rows * p.d * 2);
@@ -715,6 +718,7 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
   if (e == cudaSuccess && db_g) e = cudaMemsetAsync(db_g, 0, (size_t)p.H * 4, st);
   if (e == cudaSuccess && dnws) e = cudaMemsetAsync(dnws, 0, (size_t)p.d * 4, st);
   if (e == cudaSuccess && dnwl) e = cudaMemsetAsync(dnwl, 0, (size_t)p.d * 4, st);
+  if (e == cudaSuccess && lay.ferr) e = cudaMemsetAsync(lay.ferr, 0, 16, st);  // bounded-wait flag of the tcgen05 kernels
   if (e != cudaSuccess) return e;
   auto run = [&](auto tag, auto dtag) -> cudaError_t {
     using T = decltype(tag);
@@ -732,8 +736,12 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
     if ((e2 = mark(ev_stop, NATS_BWD_STAGE_MERGE)) != cudaSuccess) return e2;
     if ((e2 = mark(ev_start, NATS_BWD_STAGE_SOFTMAX)) != cudaSuccess) return e2;
     if (tc) {
-      e2 = launch_softmax_bwd_mma(p, q, k, v, d_os16, delta, sel, lse, dq, dk, dv, st);
+      e2 = launch_compact(p, sel, lay.nprev, lay.sel_idx, nullptr, st);
+      if (e2 == cudaSuccess)
+        e2 = launch_softmax_bwd_tc(p, q, k, v, d_os16, delta, lay.nprev, lay.sel_idx, sel, lse, dq, dk, dv,
+                                   lay.ferr, st);
       if (e2 != cudaSuccess) return e2;
+      count(NATS_BWD_STAGE_SOFTMAX, 1);  // the compaction
     } else {
       softmax_bwd_rows_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(qt, kt, vt, sel, d_os, delta,
                                                                                rows, p.L, p.N, p.scale, lse, dq);
@@ -746,7 +754,6 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
     if constexpr (tc) {
       // the chunk-start states, from the forward's chunk factors and scan
       // (the same kernels as the forward; the selection is given)
-      if ((e2 = cudaMemsetAsync(lay.ferr, 0, 16, st)) != cudaSuccess) return e2;
       if (D == 128)
         e2 = launch_gdn_prep_tc(p, q, k, v, g, beta, w_g, b_g, lay.fG, lay.fW, lay.fU, lay.fP, lay.fgate, nullptr,
                                 nullptr, nullptr, lay.ferr, st);

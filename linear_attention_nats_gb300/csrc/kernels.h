@@ -107,6 +107,15 @@ cudaError_t launch_gdn_bwd_cc(const Problem& p, const void* q, const void* k, co
                               const GdnBwdScratch& w, float* dq, float* dk, float* dg, float* dbeta,
                               cudaStream_t st);
 
+// Softmax branch of the backward pass on tcgen05 (softmax_bwd_tc.cu), bf16
+// layers: lse (fp32 [BH, L], exp2 domain) and dq (+=), then dk, dv (=); the
+// compacted softmax-chunk lists (nprev, sel_idx) as the forward builds them;
+// err[0] is set if a bounded wait expires.
+cudaError_t launch_softmax_bwd_tc(const Problem& p, const void* q, const void* k, const void* v, const void* dos,
+                                  const float* delta, const int32_t* nprev, const int32_t* sel_idx,
+                                  const uint8_t* sel, float* lse, float* dq, float* dk, float* dv, int* err,
+                                  cudaStream_t st);
+
 // Softmax branch of the backward pass on warp-level MMAs, bf16 layers
 // (backward_mma.cu): lse and dq (+=), then dk, dv (=).
 cudaError_t launch_softmax_bwd_mma(const Problem& p, const void* q, const void* k, const void* v, const void* dos,

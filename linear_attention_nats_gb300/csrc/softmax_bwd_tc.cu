@@ -20,9 +20,11 @@
 //     second kernel); pass 2 recomputes S and forms dP = dO V^T, dS in place
 //     of S (bf16), dQ += dS K.  TMEM: two S buffers, dP, dQ.
 //   softmax_bwd_dkv_tc_kernel  key tile: query blocks = its own pair, then,
-//     when either key chunk chose softmax, every later pair.  S^T = K Q^T,
-//     dP^T = V dO^T; P^T and dS^T in place (bf16); dV += P^T dO,
-//     dK += dS^T Q.  TMEM: S^T, dP^T, dV, dK.
+//     when either key chunk chose softmax, every later pair, taken one
+//     64-query chunk at a time: S^T = K Q^T, dP^T = V dO^T (N = 64, issued
+//     one chunk ahead into the other TMEM half); P^T and dS^T in place
+//     (bf16); dV += P^T dO, dK += dS^T Q.  TMEM: S^T x 2, dP^T x 2 (64
+//     columns each), dV, dK.
 // Every wait is bounded (tc::kWaitLimitNs); on expiry a kernel records an
 // error, drains what it issued and exits.
 #include "common.cuh"
@@ -166,11 +168,12 @@ __global__ void __launch_bounds__(256, 1)
       };
       // K blocks of both passes through the K ring; the V block of a pass-2
       // block right after its K block
-      int nv = 0;
+      int nv = 0, nk = 0;
       for (int g = 0; g < 2 * nb && ok; ++g) {
         const int ks = g & 1;
         if (!(ok = tc::mbar_wait(&bars[DQ_KE + ks], ((g >> 1) & 1) ^ 1, err))) break;
         load_block(&tm_k, smem + S::offK + ks * S::kT, &bars[DQ_KF + ks], g < nb ? g : g - nb);
+        ++nk;
         if (g >= nb) {
           const int j = g - nb, vs = j & 1;
           if (!(ok = tc::mbar_wait(&bars[DQ_VE + vs], ((j >> 1) & 1) ^ 1, err))) break;
@@ -181,8 +184,8 @@ __global__ void __launch_bounds__(256, 1)
       // every copy issued has landed before the CTA may exit
       tc::mbar_wait(&bars[DQ_QF], 0, nullptr);
       for (int s = 0; s < 2; ++s) {
-        const int nk = 2 * nb > s ? (2 * nb - 1 - s) / 2 + 1 : 0;
-        if (nk > 0) tc::mbar_wait(&bars[DQ_KF + s], (nk - 1) & 1, nullptr);
+        const int nks = nk > s ? (nk - 1 - s) / 2 + 1 : 0;
+        if (nks > 0) tc::mbar_wait(&bars[DQ_KF + s], (nks - 1) & 1, nullptr);
         const int nvs = nv > s ? (nv - 1 - s) / 2 + 1 : 0;
         if (nvs > 0) tc::mbar_wait(&bars[DQ_VF + s], (nvs - 1) & 1, nullptr);
       }
@@ -369,11 +372,11 @@ struct DkvSm {
   static constexpr int offQ = offV + kT;          // 2 stages of [Q | dO]
   static constexpr int offVec = offQ + 4 * kT;    // 2 stages of [lse (128) | delta (128)] fp32
   static constexpr int offBar = offVec + 2 * 1024;
-  static constexpr int kNumBars = 12;
+  static constexpr int kNumBars = 14;
   static constexpr int offTmem = offBar + kNumBars * 8;
   static constexpr int kBytes = offTmem + 16 + 1024;
 };
-enum { KV_F = 0, KV_QF = 1, KV_QE = 3, KV_SF = 5, KV_PF = 6, KV_SR = 7, KV_DONE = 8, KV_DR = 9 };
+enum { KV_F = 0, KV_QF = 1, KV_QE = 3, KV_SF = 5, KV_PF = 7, KV_SR = 9, KV_DONE = 11, KV_DR = 12 };
 
 template <int D>
 __global__ void __launch_bounds__(256, 1)
@@ -403,9 +406,11 @@ __global__ void __launch_bounds__(256, 1)
       tc::mbar_init(&bars[KV_QF + s], 1);
       tc::mbar_init(&bars[KV_QE + s], 1);
     }
-    tc::mbar_init(&bars[KV_SF], 1);
-    tc::mbar_init(&bars[KV_PF], 1);
-    tc::mbar_init(&bars[KV_SR], 128);
+    for (int h = 0; h < 2; ++h) {
+      tc::mbar_init(&bars[KV_SF + h], 1);
+      tc::mbar_init(&bars[KV_PF + h], 1);
+      tc::mbar_init(&bars[KV_SR + h], 128);
+    }
     tc::mbar_init(&bars[KV_DONE], 1);
     tc::mbar_init(&bars[KV_DR], 1);
     tc::fence_barrier_init();
@@ -417,7 +422,8 @@ __global__ void __launch_bounds__(256, 1)
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  const uint32_t tmem = *tmem_slot;  // S^T | dP^T | dV | dK, 128 columns each
+  // S^T of query chunks h = 0, 1 (64 columns each) | dP^T likewise | dV | dK
+  const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
@@ -463,45 +469,59 @@ __global__ void __launch_bounds__(256, 1)
     }
   } else if (warp == 1) {
     // --------------------------------------------------------------- MMA
+    // One step per query chunk u (chunk 2r + h of query pair r = p + u / 2):
+    // its S^T and dP^T (N = 64) go to TMEM half h, and are issued one chunk
+    // ahead, so the tensor pipe works on chunk u + 1 while the elementwise
+    // warps turn chunk u into P^T and dS^T; then dV += P^T dO and
+    // dK += dS^T Q over the chunk's 64 queries.
     if (lane == 0) {
-      constexpr uint32_t id_qk = tc::idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t id_qk = tc::idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t id_pv = tc::idesc_bf16_f32(128, D, false, true);
       const uint64_t kd = tc::smem_desc_sw128(tc::smem_u32(smem + S::offK), 16, 1024);
       const uint64_t vd = tc::smem_desc_sw128(tc::smem_u32(smem + S::offV), 16, 1024);
       const uint32_t qb = tc::smem_u32(smem + S::offQ);
-      const uint32_t tS = tmem, tP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+      const uint32_t tdV = tmem + 256, tdK = tmem + 384;
+      const int nu = 2 * nq;
       bool ok = tc::mbar_wait(&bars[KV_F], 0, err);
-      for (int i = 0; i < nq && ok; ++i) {
-        const int s = i & 1;
-        if (!(ok = tc::mbar_wait(&bars[KV_QF + s], (i >> 1) & 1, err))) break;
+      auto issue_sp = [&](int u) -> bool {
+        const int i = u >> 1, h = u & 1, s = i & 1;
+        if (h == 0 && !tc::mbar_wait(&bars[KV_QF + s], (i >> 1) & 1, err)) return false;
+        tc::fence_after();
+        const uint32_t cb = qb + s * 2 * S::kT + h * (kHalf / 2);  // query chunk h of the stage
+        const uint64_t qk = tc::smem_desc_sw128(cb, 16, 1024), ok_ = tc::smem_desc_sw128(cb + S::kT, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          tc::mma_bf16(tmem + 64 * h, tc::desc_add(kd, off), tc::desc_add(qk, off), id_qk, kk > 0);
+        }
+        tc::mma_commit(&bars[KV_SF + h]);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          tc::mma_bf16(tmem + 128 + 64 * h, tc::desc_add(vd, off), tc::desc_add(ok_, off), id_qk, kk > 0);
+        }
+        tc::mma_commit(&bars[KV_PF + h]);
+        return true;
+      };
+      if (ok) ok = issue_sp(0);
+      for (int u = 0; u < nu && ok; ++u) {
+        const int i = u >> 1, h = u & 1, s = i & 1;
+        // the next chunk's buffers were last read by chunk u - 1's products,
+        // issued before (in order) once its P^T / dS^T were in place
+        if (u + 1 < nu && !(ok = issue_sp(u + 1))) break;
+        if (!(ok = tc::mbar_wait(&bars[KV_SR + h], (u >> 1) & 1, err))) break;
         tc::fence_after();
         const uint32_t sb = qb + s * 2 * S::kT;
-        const uint64_t qk = tc::smem_desc_sw128(sb, 16, 1024), ok_ = tc::smem_desc_sw128(sb + S::kT, 16, 1024);
         const uint64_t qn = tc::smem_desc_sw128(sb, kHalf, 1024), on = tc::smem_desc_sw128(sb + S::kT, kHalf, 1024);
-        // S^T = K Q^T and dP^T = V dO^T (the previous block's products that
-        // read these buffers were issued before: in order)
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          tc::mma_bf16(tS, tc::desc_add(kd, off), tc::desc_add(qk, off), id_qk, kk > 0);
-        }
-        tc::mma_commit(&bars[KV_SF]);
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_bf16_ts(tdV, tmem + 64 * h + kk * 8, tc::desc_add(on, h * (kHalf / 2) + kk * 2048), id_pv,
+                          (u > 0) || (kk > 0));
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          tc::mma_bf16(tP, tc::desc_add(vd, off), tc::desc_add(ok_, off), id_qk, kk > 0);
-        }
-        tc::mma_commit(&bars[KV_PF]);
-        // P^T and dS^T are in place: dV += P^T dO, dK += dS^T Q
-        if (!(ok = tc::mbar_wait(&bars[KV_SR], i & 1, err))) break;
-        tc::fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc::mma_bf16_ts(tdV, tS + kk * 8, tc::desc_add(on, kk * 2048), id_pv, (i > 0) || (kk > 0));
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc::mma_bf16_ts(tdK, tP + kk * 8, tc::desc_add(qn, kk * 2048), id_pv, (i > 0) || (kk > 0));
-        tc::mma_commit(&bars[KV_QE + s]);
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_bf16_ts(tdK, tmem + 128 + 64 * h + kk * 8, tc::desc_add(qn, h * (kHalf / 2) + kk * 2048), id_pv,
+                          (u > 0) || (kk > 0));
+        if (h == 1) tc::mma_commit(&bars[KV_QE + s]);
       }
       if (ok) tc::mma_commit(&bars[KV_DONE]);
       tc::mma_commit(&bars[KV_DR]);
@@ -516,43 +536,61 @@ __global__ void __launch_bounds__(256, 1)
     const bool soft_k = ks == 0 ? soft0 : soft1;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     bool ok = true;
-    for (int i = 0; i < nq && ok; ++i) {
-      const int s = i & 1, r = p + i;
-      if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[KV_SF], i & 1, err)))) break;
-      if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[KV_PF], i & 1, err)))) break;
+    for (int u = 0; u < 2 * nq && ok; ++u) {
+      const int i = u >> 1, h = u & 1, s = i & 1;
+      const int qc = 2 * (p + i) + h;  // the query chunk of this step
+      if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[KV_SF + h], (u >> 1) & 1, err)))) break;
+      if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[KV_PF + h], (u >> 1) & 1, err)))) break;
       tc::fence_after();
-      const float* ls = (const float*)(smem + S::offVec + s * 1024);
+      const float* ls = (const float*)(smem + S::offVec + s * 1024) + 64 * h;
       const float* dls = ls + 128;
+      int mode = kNone;  // whether this key row sees the chunk's queries
+      if (valid && qc < N) mode = qc == kc ? kCausal : ((soft_k && qc > kc) ? kFull : kNone);
+      const uint32_t ts = tmem + 64 * h + lane_off, tp = tmem + 128 + 64 * h + lane_off;
+      if (mode == kNone) {  // (warp-uniform: a warp's rows share a key chunk) nothing to read
+        uint32_t z[16];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        // query chunk of these 32 columns and whether this key row sees it
-        const int qc = 2 * r + (ch >> 1), q0 = (ch & 1) * 32;
-        int mode = kNone;
-        if (valid && qc < N) mode = qc == kc ? kCausal : ((soft_k && qc > kc) ? kFull : kNone);
-        float sv[32], pv[32];
-        tc::tmem_ld32(tmem + lane_off + 32 * ch, sv);
-        tc::tmem_ld32(tmem + 128 + lane_off + 32 * ch, pv);
-        tc::tmem_ld_wait();
-        uint32_t pp[16], pd[16];
+        for (int x = 0; x < 16; ++x) z[x] = 0u;
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          float e[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c = 32 * ch + 2 * x + u;
-            const bool vis = mode == kFull || (mode == kCausal && q0 + 2 * x + u >= ki);
-            e[u] = vis ? tc::fast_exp2(sv[2 * x + u] * sl2 - ls[c]) : 0.f;
-            pv[2 * x + u] = e[u] * (pv[2 * x + u] - dls[c]);
-          }
-          pp[x] = tc::pack_bf16x2(e[0], e[1]);
-          pd[x] = tc::pack_bf16x2(pv[2 * x], pv[2 * x + 1]);
+        for (int ch = 0; ch < 2; ++ch) {
+          tc::tmem_st16u(ts + 16 * ch, z);
+          tc::tmem_st16u(tp + 16 * ch, z);
         }
-        tc::tmem_st16u(tmem + lane_off + 16 * ch, pp);  // columns already read
-        tc::tmem_st16u(tmem + 128 + lane_off + 16 * ch, pd);
+      } else {
+        const float4* ls4 = (const float4*)ls;
+        const float4* dl4 = (const float4*)dls;
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          float sv[32], pv[32];
+          tc::tmem_ld32(ts + 32 * ch, sv);
+          tc::tmem_ld32(tp + 32 * ch, pv);
+          tc::tmem_ld_wait();
+          uint32_t pp[16], pd[16];
+#pragma unroll
+          for (int y = 0; y < 8; ++y) {
+            const float4 l = ls4[8 * ch + y], dd = dl4[8 * ch + y];
+            const float lv[4] = {l.x, l.y, l.z, l.w}, dv4[4] = {dd.x, dd.y, dd.z, dd.w};
+            float e[4], g4[4];
+#pragma unroll
+            for (int w4 = 0; w4 < 4; ++w4) {
+              const int c = 32 * ch + 4 * y + w4;  // query index within the chunk
+              const bool vis = mode == kFull || c >= ki;
+              // (queries that do not exist read stale lse / delta: selected away)
+              e[w4] = vis ? tc::fast_exp2(sv[4 * y + w4] * sl2 - lv[w4]) : 0.f;
+              g4[w4] = vis ? e[w4] * (pv[4 * y + w4] - dv4[w4]) : 0.f;
+            }
+            pp[2 * y] = tc::pack_bf16x2(e[0], e[1]);
+            pp[2 * y + 1] = tc::pack_bf16x2(e[2], e[3]);
+            pd[2 * y] = tc::pack_bf16x2(g4[0], g4[1]);
+            pd[2 * y + 1] = tc::pack_bf16x2(g4[2], g4[3]);
+          }
+          tc::tmem_st16u(ts + 16 * ch, pp);  // columns already read
+          tc::tmem_st16u(tp + 16 * ch, pd);
+        }
       }
       tc::tmem_st_wait();
       tc::fence_before();
-      tc::mbar_arrive(&bars[KV_SR]);
+      tc::mbar_arrive(&bars[KV_SR + h]);
     }
     // epilogue: dv = dV, dk = scale dK (every key row belongs to one tile)
     if (ok && (ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[KV_DONE], 0, err)))) {

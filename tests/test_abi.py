@@ -175,10 +175,11 @@ def test_backward_validation(nat):
     f32 = nat.lib.nats_bwd_workspace_size(ctypes.byref(nat.dims(1, 2, 128, 64, nat.NATS_F32)))
     assert f32 == common + (al(chunks * dd * 4) + al(2 * 64 * dd * 4) + al(2 * dd * 4) + al(2 * rows * 2 * 64 * 4)
                             + al(2 * rows * 4 * 4))
-    # bf16 layers: the forward's chunk factors (G, W, U^T, P, gate, o_l, error flag), then the chunkwise
-    # adjoint's chunk-start states and state gradients, G, Linv and P (fp32), W, Q_eff, K~ (bf16), Vh, U,
-    # P^T dO, Y (fp32) and dG
-    assert need == common + (al(rows * 4) + 2 * al(rows * 64 * 2) + al(rows * 64 * 2) + al(rows * 4)
+    # bf16 layers: the compacted softmax-chunk lists, the forward's chunk factors (G, W, U^T, P, gate, o_l,
+    # error flag), then the chunkwise adjoint's chunk-start states and state gradients, G, Linv and P (fp32),
+    # W, Q_eff, K~ (bf16), Vh, U, P^T dO, Y (fp32) and dG
+    assert need == common + (2 * al(chunks * 4) + al(rows * 4) + 2 * al(rows * 64 * 2) + al(rows * 64 * 2)
+                             + al(rows * 4)
                              + al(rows * 64 * 2) + al(16)
                              + 2 * al(chunks * dd * 4) + al(rows * 4) + 2 * al(rows * 64 * 4)
                              + 3 * al(rows * 64 * 2) + 4 * al(rows * 64 * 4) + al(rows * 4))
