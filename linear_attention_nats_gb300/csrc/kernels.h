@@ -116,12 +116,6 @@ cudaError_t launch_softmax_bwd_tc(const Problem& p, const void* q, const void* k
                                   const uint8_t* sel, float* lse, float* dq, float* dk, float* dv, int* err,
                                   cudaStream_t st);
 
-// Softmax branch of the backward pass on warp-level MMAs, bf16 layers
-// (backward_mma.cu): lse and dq (+=), then dk, dv (=).
-cudaError_t launch_softmax_bwd_mma(const Problem& p, const void* q, const void* k, const void* v, const void* dos,
-                                   const float* delta, const uint8_t* sel, float* lse, float* dq, float* dk,
-                                   float* dv, cudaStream_t st);
-
 // The projections around the layer on tcgen05 (gemm_tc.cu).  QKV: x W_qkv
 // into the layer's q, k (normalised per head), v [B, H, L, d] and x W_ab into
 // g, beta [B, H, L]; w_ab_pad is scratch of proj_gate_pad_bytes(H, hidden).

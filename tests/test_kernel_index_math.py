@@ -5,7 +5,7 @@ coverage arguments the kernels rely on are checked here by enumerating
 their index formulas over the shapes they run at: every element is touched
 exactly once where a kernel partitions work, and every address stays inside
 its buffer.  The formulas restate the kernels' own (decode.cu, backward.cu,
-backward_mma.cu); a change there has to be mirrored here.
+gdn_bwd_chunk.cu); a change there has to be mirrored here.
 """
 
 import itertools
@@ -99,31 +99,54 @@ def test_backward_partials_match_between_writer_and_combine():
             assert writer + 2 * D <= 2 * rows * 2 * D  # inside the buffer of both shares
 
 
-# ------------------------------------------- backward, tensor-core softmax
-def _frag_rows_cols(kind, lane, a, b):
-    # the (row, column) a lane's ldmatrix address points to, as in
-    # backward_mma.cu: frag_a (m0 = a, ks = b), frag_bt (jp = a, ks = b),
-    # frag_b (ks = a, np = b)
+# ------------------------------- backward, chunkwise Gated DeltaNet adjoint
+def _ldsm_rows_cols(kind, lane, m0, n0, j, k0):
+    # the (row, column) of the fp16 tile a lane's ldmatrix address points to,
+    # as in gdn_bwd_chunk.cu's hmm(): A stored [m][k] ("a") or [k][m] ("at"),
+    # B stored [n][k] ("b") or [k][n] ("bt"); j = the first of two n8 tiles
+    mi, r8 = lane >> 3, lane & 7
     if kind == "a":
-        return a + (lane & 7) + 8 * ((lane >> 3) & 1), 16 * b + 8 * (lane >> 4)
-    if kind == "bt":
-        return 16 * a + (lane & 7) + 8 * (lane >> 4), 16 * b + 8 * ((lane >> 3) & 1)
-    return 16 * a + (lane & 7) + 8 * ((lane >> 3) & 1), 16 * b + 8 * (lane >> 4)
+        return m0 + (lane & 15), k0 + 8 * (lane >> 4)
+    if kind == "at":
+        return k0 + (mi >> 1) * 8 + r8, m0 + (mi & 1) * 8
+    if kind == "b":
+        return n0 + 8 * j + (mi >> 1) * 8 + r8, k0 + (mi & 1) * 8
+    return k0 + (mi & 1) * 8 + r8, n0 + 8 * j + (mi >> 1) * 8
 
 
 @pytest.mark.parametrize("D", [64, 128])
-def test_backward_mma_fragments_stay_in_their_tiles(D):
-    rs = D + 8  # skewed row stride; a lane reads 8 bf16 (16 bytes) from its address
-    for lane in range(32):
-        for m0 in range(0, 64, 16):
-            for ks in range(D // 16):  # A over the feature dimension (Q, dO, K, V rows)
-                r, c = _frag_rows_cols("a", lane, m0, ks)
-                assert r < 64 and c + 8 <= D and (r * rs + c) * 2 % 16 == 0
-        for jp in range(4):
-            for ks in range(D // 16):  # K^T / V^T / Q^T / dO^T operands
-                r, c = _frag_rows_cols("bt", lane, jp, ks)
-                assert r < 64 and c + 8 <= D and (r * rs + c) * 2 % 16 == 0
-        for ks in range(4):
-            for np_ in range(D // 16):  # K / dO / Q as [k][n] operands
-                r, c = _frag_rows_cols("b", lane, ks, np_)
-                assert r < 64 and c + 8 <= D and (r * rs + c) * 2 % 16 == 0
+def test_chunk_adjoint_fragments_stay_in_their_tiles(D):
+    # every product of the per-chunk kernels: output C x D (NT = D / 16, n0 =
+    # (w >> 2) D / 2) or C x C (NT = 4, n0 = 32 (w >> 2)), m0 = 16 (w & 3),
+    # over tiles of C x D, D x D or C x C fp16 entries, row stride cols + 8
+    C = 64
+    shapes = {"CD": (C, D), "DD": (D, D), "CC": (C, C)}
+    products = [  # (output columns, K, A tile, A kind, B tile, B kind)
+        (C, D, "CD", "a", "CD", "b"),    # K K^T, Q K^T, Y U^T, dO U^T
+        (D, D, "CD", "a", "DD", "b"),    # K S0^T, K~ dS_C^T
+        (D, D, "CD", "a", "DD", "bt"),   # dO S0, U dS_C, dVh S0
+        (D, C, "CC", "a", "CD", "bt"),   # Linv diag(.) K, P W, Linv diag(beta) Vh, dPm K, A~ K
+        (D, C, "CC", "at", "CD", "bt"),  # P^T dO, Linv^T dU, dPm^T Q, A~^T K
+    ]
+    for ncols, K, ta, ka, tb, kb in products:
+        NT = ncols // 16 if ncols == D else 4
+        seen_a, seen_b = set(), set()
+        for w in range(8):
+            m0, n0 = 16 * (w & 3), (w >> 2) * (ncols // 2)
+            for k0 in range(0, K, 16):
+                for lane in range(32):
+                    r, c = _ldsm_rows_cols(ka, lane, m0, n0, 0, k0)
+                    rows, cols = shapes[ta]
+                    assert r < rows and c + 8 <= cols and (r * (cols + 8) + c) * 2 % 16 == 0
+                    seen_a.add((r, c))
+                    for j in range(0, NT, 2):
+                        r, c = _ldsm_rows_cols(kb, lane, m0, n0, j, k0)
+                        rows, cols = shapes[tb]
+                        assert r < rows and c + 8 <= cols and (r * (cols + 8) + c) * 2 % 16 == 0
+                        seen_b.add((r, c))
+        # the product reads exactly its operands' 8-element row segments:
+        # A over (C output rows) x K, B over K x (output columns)
+        def segs(kind, nrows, ncols_):
+            return {(r, c) for r in range(nrows) for c in range(0, ncols_, 8)}
+        assert seen_a == (segs(0, C, K) if ka == "a" else segs(0, K, C)), (ncols, K, ka)
+        assert seen_b == (segs(0, ncols, K) if kb == "b" else segs(0, K, ncols)), (ncols, K, kb)
