@@ -671,9 +671,10 @@ static size_t bwd_layout(const Problem& p, int dtype, uint8_t* base, BwdLayout* 
     w.G = (float*)take(rows * 4);
     w.Li = (float*)take(rows * kChunk * 4);
     w.P = (float*)take(rows * kChunk * 4);
-    w.W16 = (__nv_bfloat16*)take(rows * p.d * 2);
-    w.Qe16 = (__nv_bfloat16*)take(rows * p.d * 2);
-    w.Kt16 = (__nv_bfloat16*)take(rows * p.d * 2);
+    w.W16 = take(rows * p.d * 2);
+    w.Qe16 = take(rows * p.d * 2);
+    w.Kt16 = take(rows * p.d * 2);
+    w.sc = (float*)take(chunks * 4 * 4);
     w.Vh = (float*)take(rows * p.d * 4);
     w.U = (float*)take(rows * p.d * 4);
     w.PtdO = (float*)take(rows * p.d * 4);

@@ -28,17 +28,17 @@
 // chunk, dS_{c+1} + dO^T Q_eff for a rolled-back one.
 //
 // Kernels (after the forward scan has written every chunk's S0):
-//   gdn_bwd_prep_kernel  per chunk: G, Linv, P (fp32), W, Q_eff, K~ (bf16)
-//   gdn_bwd_scan_kernel  per (b, h, 32 state rows): the reverse scan, writing
+//   gdn_bwd_prep_kernel  per chunk: G, Linv, P (fp32), W, Q_eff, K~ (fp16, scaled)
+//   gdn_bwd_scan_kernel  per (b, h, 64 state rows): the reverse scan, writing
 //                        dS_C of every committed chunk (fp32)
 //   gdn_bwd_s0_kernel    per chunk: Vh, U, P^T dO; dq += diag(gamma) dO S0
 //   gdn_bwd_ds_kernel    per chunk: dU, Y, dv; the U dS_C and dVh S0 terms
 //   gdn_bwd_cc_kernel    per chunk: the C x C products, dq, dk, dbeta, dg
-// Products run on warp-level tensor cores with fp32 accumulation: the
-// per-chunk kernels take fp16 operand tiles through ldmatrix (m16n8k16),
-// each tile scaled by its own power of two so that its largest entry sits
-// below 2^15 (fp16 range is never exceeded, its 11-bit precision matches
-// tf32); the reverse scan keeps its fp32 state and uses tf32 (m16n8k8).
+// Products run on warp-level tensor cores with fp32 accumulation over fp16
+// operand tiles read through ldmatrix (m16n8k16), each tile scaled by its
+// own power of two so that its largest entry sits below 2^15 (fp16 range is
+// never exceeded, its 11-bit precision matches tf32); the reverse scan keeps
+// its state gradient in fp32 and converts it per step.
 // The triangular inverse is a forward substitution on the CUDA cores.  Each
 // CTA has 8 warps; a C x D output is split into 16-row strips (warp w & 3)
 // and column halves (warp w >> 2).
@@ -53,35 +53,6 @@ namespace {
 constexpr int C = kChunk;
 constexpr int CS = C + 4;  // fp32 row stride of C x C tiles
 using bf16 = __nv_bfloat16;
-
-__device__ __forceinline__ uint32_t tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
-
-__device__ __forceinline__ void mma8(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                                     uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// acc[j] (rows m0 .. m0 + 15, columns n0 + 8 j .. + 7) += sum_k A(i, k) B(k, n)
-template <int NT, int K, class FA, class FB>
-__device__ __forceinline__ void wmm(float (&acc)[NT][4], int m0, int n0, FA fa, FB fb) {
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-#pragma unroll 2
-  for (int k0 = 0; k0 < K; k0 += 8) {
-    const uint32_t a0 = tf32(fa(m0 + g, k0 + t)), a1 = tf32(fa(m0 + g + 8, k0 + t));
-    const uint32_t a2 = tf32(fa(m0 + g, k0 + t + 4)), a3 = tf32(fa(m0 + g + 8, k0 + t + 4));
-#pragma unroll
-    for (int j = 0; j < NT; ++j)
-      mma8(acc[j], a0, a1, a2, a3, tf32(fb(k0 + t, n0 + 8 * j + g)), tf32(fb(k0 + t + 4, n0 + 8 * j + g)));
-  }
-}
 
 template <int NT>
 __device__ __forceinline__ void zero(float (&acc)[NT][4]) {
@@ -145,7 +116,6 @@ __device__ __forceinline__ void cp16(void* dst, const void* src) {
                "l"(src)
                : "memory");
 }
-__device__ __forceinline__ float bf(const bf16* p) { return __bfloat162float(*p); }
 
 // the chunk's cumulative log-decay G (from Gb) and gamma, beta into shared memory
 __device__ __forceinline__ void load_scalars(const float* Gb, const float* beta, size_t row0, float* sG, float* sGam,
@@ -360,8 +330,9 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
                                                            const float* __restrict__ g,
                                                            const float* __restrict__ beta, int L, int N, float scale,
                                                            float* __restrict__ Gb, float* __restrict__ Li_out,
-                                                           float* __restrict__ P_out, bf16* __restrict__ W16,
-                                                           bf16* __restrict__ Qe16, bf16* __restrict__ Kt16) {
+                                                           float* __restrict__ P_out, half* __restrict__ W16,
+                                                           half* __restrict__ Qe16, half* __restrict__ Kt16,
+                                                           float* __restrict__ sc_out) {
   using S = PrepSm<D>;
   constexpr int NT = D / 16, LD = H<D>::ld, LC = H<C>::ld;
   extern __shared__ __align__(16) uint8_t sm[];
@@ -419,21 +390,25 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
     sp = acc_h<4, C>(qk, m0, n0, hP, red);
   }
   __syncthreads();
-  // Linv = (I + beta A)^{-1} by forward substitution, one column per thread
+  // Linv = (I + beta A)^{-1} by forward substitution, one column per thread;
+  // each row's sum runs in four independent partial sums (short chains)
   if (tid < C) {
     const int j = tid;
     float x[C];
 #pragma unroll
     for (int i = 0; i < C; ++i) {
-      float s = i == j ? 1.f : 0.f;
+      float s4[4] = {i == j ? 1.f : 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int m4 = 0; m4 < i / 4; ++m4) {
         const float4 a = *(const float4*)(sA + i * CS + 4 * m4);
-        s -= a.x * x[4 * m4] + a.y * x[4 * m4 + 1] + a.z * x[4 * m4 + 2] + a.w * x[4 * m4 + 3];
+        s4[0] = fmaf(-a.x, x[4 * m4], s4[0]);
+        s4[1] = fmaf(-a.y, x[4 * m4 + 1], s4[1]);
+        s4[2] = fmaf(-a.z, x[4 * m4 + 2], s4[2]);
+        s4[3] = fmaf(-a.w, x[4 * m4 + 3], s4[3]);
       }
 #pragma unroll
-      for (int m = (i / 4) * 4; m < i; ++m) s -= sA[i * CS + m] * x[m];
-      x[i] = s;
+      for (int m = (i / 4) * 4; m < i; ++m) s4[m & 3] = fmaf(-sA[i * CS + m], x[m], s4[m & 3]);
+      x[i] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
     }
 #pragma unroll
     for (int i = 0; i < C; ++i) sLi[i * CS + j] = x[i];
@@ -448,23 +423,48 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
   hmm<NT, C, false, true>(acc, m0, n0, hL, LC, hK, LD);
   {
     const float iw = 1.f / (sl * sk);
-    each_mut(acc, m0, n0, [&](int i, int n, float v, int, int) {
-      v *= iw;
-      W16[(row0 + i) * D + n] = __float2bfloat16_rn(v);
-      return v;
-    });
+    each_mut(acc, m0, n0, [&](int, int, float v, int, int) { return v * iw; });
   }
   const float sw = acc_h<NT, D>(acc, m0, n0, hW, red);
   __syncthreads();
-  // Q_eff = diag(gamma) Q~ - P W, and K~ = diag(gamma_C / gamma) K
+  // W and K~ for the reverse scan: fp16 rows as staged (K~ = the K tile
+  // times gamma_C / gamma <= 1, at the K tile's scale)
+  for (int x = tid; x < C * D / 8; x += 256) {
+    const int i = x / (D / 8), c8 = 8 * (x % (D / 8));
+    *(uint4*)(W16 + (row0 + i) * D + c8) = *(const uint4*)(hW + i * LD + c8);
+    const float f = sGam[C - 1] / sGam[i];
+    const __half2* k2 = (const __half2*)(hK + i * LD + c8);
+    uint4 o;
+    __half2* o2 = (__half2*)&o;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float2 kf = __half22float2(k2[u]);
+      o2[u] = __floats2half2_rn(kf.x * f, kf.y * f);
+    }
+    *(uint4*)(Kt16 + (row0 + i) * D + c8) = o;
+  }
+  // Q_eff = diag(gamma) Q~ - P W (fp16, at its own scale)
   zero(acc);
   hmm<NT, C, false, true>(acc, m0, n0, hP, LC, hW, LD);
   {
-    const float ipw = 1.f / (sp * sw), iq = scale / sq, ik = 1.f / sk, gC = sGam[C - 1];
-    each(acc, m0, n0, [&](int i, int n, float v, int, int) {
-      Qe16[(row0 + i) * D + n] = __float2bfloat16_rn(sGam[i] * iq * __half2float(hQ[i * LD + n]) - v * ipw);
-      Kt16[(row0 + i) * D + n] = __float2bfloat16_rn(gC / sGam[i] * ik * __half2float(hK[i * LD + n]));
+    const float ipw = 1.f / (sp * sw), iq = scale / sq;
+    each_mut(acc, m0, n0, [&](int i, int n, float v, int, int) {
+      return sGam[i] * iq * __half2float(hQ[i * LD + n]) - v * ipw;
     });
+    float mq = 0.f;
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) mq = fmaxf(mq, fabsf(acc[j][e]));
+    const float sqe = block_scale(mq, red);
+    each(acc, m0, n0, [&](int i, int n, float v, int j, int e) {  // pairs (n, n + 1)
+      if ((e & 1) == 0) *(__half2*)(Qe16 + (row0 + i) * D + n) = __floats2half2_rn(v * sqe, acc[j][e + 1] * sqe);
+    });
+    if (tid == 0) {
+      sc_out[chunk * 4 + 0] = sw;
+      sc_out[chunk * 4 + 1] = sqe;
+      sc_out[chunk * 4 + 2] = sk;
+    }
   }
   // Linv for the per-chunk gradient kernels (P was written above)
   for (int x = tid; x < C * C / 4; x += 256) {
@@ -474,50 +474,62 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
 }
 
 // ------------------------------------------------------------------ scan
-constexpr int RB = 32;  // state-gradient rows per CTA
+constexpr int RB = 64;  // state-gradient rows per CTA (BH x D / 64 CTAs: one wave at the layer's sizes)
 
 template <int D>
 struct ScanSm {
-  using T = Tiles<D>;
-  static constexpr int kTile = C * T::BS * 2;
-  static constexpr int kO = C * (RB + 4) * 4;
-  static constexpr int kStage = 3 * kTile + kO;
-  static constexpr int offS = 2 * kStage;          // fp32 [RB][FS]
-  static constexpr int offX = offS + RB * T::FS * 4; // fp32 [RB][CS]
-  static constexpr int kBytes = offX + RB * CS * 4;
+  static constexpr int kTile = H<D>::bytes(C);          // fp16 [C][D + 8]
+  static constexpr int kO = C * (RB + 4) * 4;            // fp32 [C][RB + 4]: dO columns of the CTA's rows
+  static constexpr int kStage = 3 * kTile + kO;          // K~, W, Q_eff, dO
+  static constexpr int offS = 2 * kStage;                // fp32 [RB][D + 4]: the state gradient
+  static constexpr int offSh = offS + RB * (D + 4) * 4;  // fp16 [RB][D + 8]: its scaled copy
+  static constexpr int offX = offSh + H<D>::bytes(RB);   // fp16 [RB][C + 8]: X = dS K~^T
+  static constexpr int offOh = offX + H<C>::bytes(RB);   // fp16 [C][RB + 8]: dO columns
+  static constexpr int offRed = offOh + H<RB>::bytes(C);
+  static constexpr int kBytes = offRed + 64;
 };
 
+
+// The state gradient, backwards over the chunks of one head, RB rows per
+// CTA (the rows are independent): dS_C of chunk c is the state gradient
+// before its step; then dS <- gamma_C dS - (dS K~^T) W + dO^T Q_eff for a
+// committed chunk, dS + dO^T Q_eff for a rolled-back one.  dS stays fp32 in
+// shared memory; each step's operands are fp16 tiles at their own scales.
 template <int D>
-__global__ void __launch_bounds__(256) gdn_bwd_scan_kernel(const bf16* __restrict__ Kt16,
-                                                           const bf16* __restrict__ W16,
-                                                           const bf16* __restrict__ Qe16,
+__global__ void __launch_bounds__(256) gdn_bwd_scan_kernel(const half* __restrict__ Kt16,
+                                                           const half* __restrict__ W16,
+                                                           const half* __restrict__ Qe16,
+                                                           const float* __restrict__ sc,
                                                            const float* __restrict__ dO, const float* __restrict__ Gb,
                                                            const uint8_t* __restrict__ sel, int L, int N,
                                                            float* __restrict__ dSC) {
-  using T = Tiles<D>;
   using S = ScanSm<D>;
+  constexpr int FS = D + 4, LD = H<D>::ld, LC = H<C>::ld, LR = H<RB>::ld;
   extern __shared__ __align__(16) uint8_t sm[];
   float* sdS = (float*)(sm + S::offS);
-  float* sX = (float*)(sm + S::offX);
+  half* hS = (half*)(sm + S::offSh);
+  half* hX = (half*)(sm + S::offX);
+  half* hO = (half*)(sm + S::offOh);
+  float* red = (float*)(sm + S::offRed);
   constexpr int splits = D / RB;
   const long long bh = blockIdx.x / splits;
   const int r0 = (blockIdx.x % splits) * RB;
   const int tid = threadIdx.x, warp = tid >> 5;
-  for (int x = tid; x < RB * T::FS; x += 256) sdS[x] = 0.f;
-  auto stage_ptr = [&](int s, int which) { return sm + s * S::kStage + which * S::kTile; };
+  for (int x = tid; x < RB * FS; x += 256) sdS[x] = 0.f;
+  auto stage_ptr = [&](int st, int which) { return sm + st * S::kStage + which * S::kTile; };
   auto prefetch = [&](int c) {
-    const int s = c & 1;
+    const int st = c & 1;
     const size_t row0 = (size_t)bh * L + (size_t)c * C;
-    const bf16* srcs[3] = {Kt16, W16, Qe16};
+    const half* srcs[3] = {Kt16, W16, Qe16};
 #pragma unroll
     for (int w3 = 0; w3 < 3; ++w3) {
-      bf16* dst = (bf16*)stage_ptr(s, w3);
+      half* dst = (half*)stage_ptr(st, w3);
       for (int x = tid; x < C * D / 8; x += 256) {
         const int r = x / (D / 8), c8 = x % (D / 8);
-        cp16(dst + r * T::BS + 8 * c8, srcs[w3] + (row0 + r) * D + 8 * c8);
+        cp16(dst + r * LD + 8 * c8, srcs[w3] + (row0 + r) * D + 8 * c8);
       }
     }
-    float* dO_s = (float*)stage_ptr(s, 3);
+    float* dO_s = (float*)stage_ptr(st, 3);
     for (int x = tid; x < C * RB / 4; x += 256) {
       const int r = x / (RB / 4), c4 = x % (RB / 4);
       cp16(dO_s + r * (RB + 4) + 4 * c4, dO + (row0 + r) * D + r0 + 4 * c4);
@@ -533,46 +545,54 @@ __global__ void __launch_bounds__(256) gdn_bwd_scan_kernel(const bf16* __restric
       asm volatile("cp.async.wait_group 0;" ::: "memory");
     }
     __syncthreads();
-    const int s = c & 1;
-    const bf16* sKt = (const bf16*)stage_ptr(s, 0);
-    const bf16* sW = (const bf16*)stage_ptr(s, 1);
-    const bf16* sQe = (const bf16*)stage_ptr(s, 2);
-    const float* sO = (const float*)stage_ptr(s, 3);
-    const bool lin = sel[bh * N + c] != 0;
+    const int st = c & 1;
+    const half* hKt = (const half*)stage_ptr(st, 0);
+    const half* hW = (const half*)stage_ptr(st, 1);
+    const half* hQe = (const half*)stage_ptr(st, 2);
+    const float* sO = (const float*)stage_ptr(st, 3);
+    const long long ch = bh * N + c;
+    const bool lin = sel[ch] != 0;
+    const float sw = sc[ch * 4], sqe = sc[ch * 4 + 1], skt = sc[ch * 4 + 2];
     // dS_C of a committed chunk (the last chunk's is zero and is not read)
     if (lin && c < N - 1) {
-      float* dst = dSC + (((size_t)bh * N + c) * D + r0) * D;
+      float* dst = dSC + (((size_t)ch) * D + r0) * D;
       for (int x = tid; x < RB * D / 4; x += 256) {
         const int i = x / (D / 4), c4 = x % (D / 4);
-        *(float4*)(dst + (size_t)i * D + 4 * c4) = *(const float4*)(sdS + i * T::FS + 4 * c4);
+        *(float4*)(dst + (size_t)i * D + 4 * c4) = *(const float4*)(sdS + i * FS + 4 * c4);
       }
     }
+    // the step's dO columns (fp16, scaled)
+    const float so = tile_h<C, RB>(sO, RB + 4, hO, red);
+    float sx = 1.f, sd = 1.f;
     if (lin) {  // X = dS K~^T (RB x C)
-      const int m0 = 16 * (warp & 1), n0 = 16 * (warp >> 1);
-      float acc[2][4];
-      zero(acc);
-      wmm<2, D>(acc, m0, n0, [&](int i, int x) { return sdS[i * T::FS + x]; },
-                [&](int x, int n) { return bf(sKt + n * T::BS + x); });
-      each(acc, m0, n0, [&](int i, int n, float v, int, int) { sX[i * CS + n] = v; });
+      sd = tile_h<RB, D>(sdS, FS, hS, red);
       __syncthreads();
-    }
-    {  // dS <- gamma_C dS - X W + dO^T Q_eff (committed), dS + dO^T Q_eff (rolled back)
-      constexpr int NT = D / 32;
-      const int m0 = 16 * (warp & 1), n0 = (warp >> 1) * (D / 4);
-      float acc[NT][4];
+      const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);
+      float acc[4][4];
       zero(acc);
-      if (lin)
-        wmm<NT, C>(acc, m0, n0, [&](int i, int m) { return -sX[i * CS + m]; },
-                   [&](int m, int n) { return bf(sW + m * T::BS + n); });
-      wmm<NT, C>(acc, m0, n0, [&](int i, int m) { return sO[m * (RB + 4) + i]; },
-                 [&](int m, int n) { return bf(sQe + m * T::BS + n); });
+      hmm<4, D, false, false>(acc, m0, n0, hS, LD, hKt, LD);
+      const float ix = 1.f / (sd * skt);
+      each_mut(acc, m0, n0, [&](int, int, float v, int, int) { return -v * ix; });
+      sx = acc_h<4, C>(acc, m0, n0, hX, red);
+    }
+    __syncthreads();
+    {  // dS <- gamma_C dS - X W + dO^T Q_eff (committed), dS + dO^T Q_eff (rolled back)
+      constexpr int NT = D / 16;
+      const int m0 = 16 * (warp & 3), n0 = (warp >> 2) * (D / 2);
+      float a1[NT][4], a2[NT][4];
+      zero(a1);
+      zero(a2);
+      if (lin) hmm<NT, C, false, true>(a1, m0, n0, hX, LC, hW, LD);
+      hmm<NT, C, true, true>(a2, m0, n0, hO, LR, hQe, LD);
       const float gC = lin ? __expf(Gb[(size_t)bh * L + (size_t)c * C + C - 1]) : 1.f;
-      each(acc, m0, n0, [&](int i, int n, float v, int, int) { sdS[i * T::FS + n] = gC * sdS[i * T::FS + n] + v; });
+      const float f1 = 1.f / (sx * sw), f2 = 1.f / (so * sqe);
+      each(a1, m0, n0, [&](int i, int n, float v, int j, int e) {
+        sdS[i * FS + n] = gC * sdS[i * FS + n] + v * f1 + a2[j][e] * f2;
+      });
     }
     __syncthreads();
   }
 }
-
 
 // -------------------------------------------------------- products with S0
 template <int D>
@@ -972,10 +992,10 @@ cudaError_t run(const Problem& p, const void* q, const void* k, const void* v, c
   const bf16* qb = (const bf16*)q;
   const bf16* kb = (const bf16*)k;
   const bf16* vb = (const bf16*)v;
-  gdn_bwd_prep_kernel<D><<<(unsigned)chunks, 256, PrepSm<D>::kBytes, st>>>(qb, kb, g, beta, p.L, p.N, p.scale, w.G,
-                                                                          w.Li, w.P, w.W16, w.Qe16, w.Kt16);
-  gdn_bwd_scan_kernel<D><<<(unsigned)(p.BH * (D / RB)), 256, ScanSm<D>::kBytes, st>>>(w.Kt16, w.W16, w.Qe16, dO,
-                                                                                      w.G, sel, p.L, p.N, w.dSC);
+  gdn_bwd_prep_kernel<D><<<(unsigned)chunks, 256, PrepSm<D>::kBytes, st>>>(
+      qb, kb, g, beta, p.L, p.N, p.scale, w.G, w.Li, w.P, (half*)w.W16, (half*)w.Qe16, (half*)w.Kt16, w.sc);
+  gdn_bwd_scan_kernel<D><<<(unsigned)(p.BH * (D / RB)), 256, ScanSm<D>::kBytes, st>>>(
+      (const half*)w.Kt16, (const half*)w.W16, (const half*)w.Qe16, w.sc, dO, w.G, sel, p.L, p.N, w.dSC);
   gdn_bwd_s0_kernel<D><<<(unsigned)chunks, 256, S0Sm<D>::kBytes, st>>>(qb, kb, vb, dO, w.S0, w.Li, w.P, w.G, beta,
                                                                       p.L, p.N, p.scale, w.Vh, w.U, w.PtdO, dq,
                                                                       w.dG);

@@ -87,9 +87,10 @@ struct GdnBwdScratch {
   float* G;     // [BH, L] in-chunk cumulative log-decay
   float* Li;    // [BH, N, C, C] (I + diag(beta) A)^{-1}
   float* P;     // [BH, N, C, C] lower(e^{G_i - G_j} scale q_i . k_j)
-  __nv_bfloat16* W16;   // [BH, L, dk] Linv diag(beta gamma) K
-  __nv_bfloat16* Qe16;  // [BH, L, dk] diag(gamma) Q~ - P W
-  __nv_bfloat16* Kt16;  // [BH, L, dk] diag(gamma_C / gamma) K
+  void* W16;    // [BH, L, dk] fp16: Linv diag(beta gamma) K  \  each times its chunk's
+  void* Qe16;   // [BH, L, dk] fp16: diag(gamma) Q~ - P W      >  power-of-two scale
+  void* Kt16;   // [BH, L, dk] fp16: diag(gamma_C / gamma) K  /   (sc)
+  float* sc;    // [BH, N, 4] the scales of W, Q_eff, K~
   float* Vh;    // [BH, L, dv] V - diag(gamma) K S0^T
   float* U;     // [BH, L, dv] Linv diag(beta) Vh
   float* PtdO;  // [BH, L, dv] P^T dO
