@@ -82,8 +82,9 @@ def select(q, k, w_s, b_s=None, *, scores: bool = False, stream=None):
 def hybrid_fwd(q, k, v, g, beta, w_s, b_s, w_g, b_g=None, *, norm_w_soft=None, norm_w_lin=None,
                sel_in=None, scale: float = 0.0, eps: float = 1e-6, out=None, workspace=None,
                return_sel: bool = False, return_state: bool = False,
-               return_branches: bool = False, check_errors: bool = False, stream=None):
-    """NAtS-L hybrid attention layer forward.
+               return_branches: bool = False, check_errors: bool = False, stream=None, profile=None):
+    """NAtS-L hybrid attention layer forward (nats_hybrid_fwd; with `profile`,
+    a _native.Profile, nats_hybrid_fwd_profiled).
 
     q, k, v: [B, H, L, d] bf16 or fp32 (same dtype); g, beta: fp32 [B, H, L];
     w_s: fp32 [H, 2, 2d]; b_s: fp32 [H, 2] or None; w_g: fp32 [H, d];
@@ -120,11 +121,13 @@ def hybrid_fwd(q, k, v, g, beta, w_s, b_s, w_g, b_g=None, *, norm_w_soft=None, n
     state = torch.empty((B, H, d, d), dtype=torch.float32, device=dev) if return_state else None
     o_soft = torch.empty((B, H, L, d), dtype=torch.float32, device=dev) if return_branches else None
     o_lin = torch.empty((B, H, L, d), dtype=torch.float32, device=dev) if return_branches else None
-    check(_native.lib.nats_hybrid_fwd(
-        ctypes.byref(dm), _p(q), _p(k), _p(v), _p(g), _p(beta), _p(w_s), _p(b_s), _p(w_g), _p(b_g),
-        _p(norm_w_soft), _p(norm_w_lin), _p(sel_in), _p(out), _p(sel), _p(state), _p(o_soft),
-        _p(o_lin), _p(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream)),
-        "nats_hybrid_fwd")
+    args = (ctypes.byref(dm), _p(q), _p(k), _p(v), _p(g), _p(beta), _p(w_s), _p(b_s), _p(w_g), _p(b_g),
+            _p(norm_w_soft), _p(norm_w_lin), _p(sel_in), _p(out), _p(sel), _p(state), _p(o_soft),
+            _p(o_lin), _p(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream))
+    if profile is None:
+        check(_native.lib.nats_hybrid_fwd(*args), "nats_hybrid_fwd")
+    else:
+        check(_native.lib.nats_hybrid_fwd_profiled(*args, ctypes.byref(profile)), "nats_hybrid_fwd_profiled")
     if check_errors:
         check_workspace(dm, workspace, stream)
     if not (return_sel or return_state or return_branches):
