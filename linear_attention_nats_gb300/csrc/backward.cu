@@ -58,6 +58,47 @@ __device__ __forceinline__ void row_load(const __nv_bfloat16* p, float (&o)[E]) 
 #pragma unroll
   for (int x = 0; x < E; ++x) o[x] = __bfloat162float(p[x]);
 }
+// E (2 or 4) consecutive elements at an E-aligned offset, one vector access
+template <int E>
+__device__ __forceinline__ void vec_load(const float* p, float (&o)[E]) {
+  if constexpr (E == 4) {
+    const float4 v = *(const float4*)p;
+    o[0] = v.x, o[1] = v.y, o[2] = v.z, o[3] = v.w;
+  } else {
+    const float2 v = *(const float2*)p;
+    o[0] = v.x, o[1] = v.y;
+  }
+}
+template <int E>
+__device__ __forceinline__ void vec_load(const __nv_bfloat16* p, float (&o)[E]) {
+  if constexpr (E == 4) {
+    const uint2 v = *(const uint2*)p;
+    const float2 a = __bfloat1622float2(*(const __nv_bfloat162*)&v.x), b = __bfloat1622float2(*(const __nv_bfloat162*)&v.y);
+    o[0] = a.x, o[1] = a.y, o[2] = b.x, o[3] = b.y;
+  } else {
+    const float2 a = __bfloat1622float2(*(const __nv_bfloat162*)p);
+    o[0] = a.x, o[1] = a.y;
+  }
+}
+template <int E>
+__device__ __forceinline__ void vec_store(float* p, const float (&o)[E]) {
+  if constexpr (E == 4)
+    *(float4*)p = make_float4(o[0], o[1], o[2], o[3]);
+  else
+    *(float2*)p = make_float2(o[0], o[1]);
+}
+template <int E>
+__device__ __forceinline__ void vec_store(__nv_bfloat16* p, const float (&o)[E]) {
+  if constexpr (E == 4) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(o[0], o[1]), b = __floats2bfloat162_rn(o[2], o[3]);
+    uint2 v;
+    v.x = *(const uint32_t*)&a;
+    v.y = *(const uint32_t*)&b;
+    *(uint2*)p = v;
+  } else {
+    *(__nv_bfloat162*)p = __floats2bfloat162_rn(o[0], o[1]);
+  }
+}
 
 // ------------------------------------------------------------ 1. merge
 template <typename T, int D>
@@ -91,10 +132,10 @@ __global__ void __launch_bounds__(256) merge_bwd_kernel(
   for (int r = warp; r < kMergeRows; r += 8) {
     const long long t = bh * L + row0 + r;
     float os[E], ol[E], R[E], qv[E];
-    row_load<E>(o_s + t * D + lane * E, os);
-    row_load<E>(o_l + t * D + lane * E, ol);
-    row_load<E>(dout + t * D + lane * E, R);
-    row_load<E>(q + t * D + lane * E, qv);
+    vec_load<E>(o_s + t * D + lane * E, os);
+    vec_load<E>(o_l + t * D + lane * E, ol);
+    vec_load<E>(dout + t * D + lane * E, R);
+    vec_load<E>(q + t * D + lane * E, qv);
     float ss = 0.f, sl = 0.f, z = 0.f;
 #pragma unroll
     for (int x = 0; x < E; ++x) {
@@ -118,20 +159,24 @@ __global__ void __launch_bounds__(256) merge_bwd_kernel(
     gs = warp_sum(gs);
     gl = warp_sum(gl);
     const float dz = dw * w * (1.f - w);
-    float dl = 0.f;
+    float dl = 0.f, g_s[E], g_l[E], gq[E];
 #pragma unroll
     for (int x = 0; x < E; ++x) {
-      const float g_s = rs * ws[x] * w * R[x] - os[x] * rs * rs * rs * gs / D;
-      const float g_l = rl * wl[x] * (1.f - w) * R[x] - ol[x] * rl * rl * rl * gl / D;
-      d_os[t * D + lane * E + x] = g_s;
-      if (d_os16) d_os16[t * D + lane * E + x] = __float2bfloat16_rn(g_s);
-      d_ol[t * D + lane * E + x] = g_l;
-      dq[t * D + lane * E + x] = dz * wg[x];
-      dl = fmaf(g_s, os[x], dl);
+      g_s[x] = rs * ws[x] * w * R[x] - os[x] * rs * rs * rs * gs / D;
+      g_l[x] = rl * wl[x] * (1.f - w) * R[x] - ol[x] * rl * rl * rl * gl / D;
+      gq[x] = dz * wg[x];
+      dl = fmaf(g_s[x], os[x], dl);
       a_wg[x] = fmaf(dz, qv[x], a_wg[x]);
       a_ns[x] = fmaf(w * R[x], os[x] * rs, a_ns[x]);
       a_nl[x] = fmaf((1.f - w) * R[x], ol[x] * rl, a_nl[x]);
     }
+    // d o_s in fp32 for the fp32 path, in bf16 for the tensor-core softmax backward
+    if (d_os16)
+      vec_store<E>(d_os16 + t * D + lane * E, g_s);
+    else
+      vec_store<E>(d_os + t * D + lane * E, g_s);
+    vec_store<E>(d_ol + t * D + lane * E, g_l);
+    vec_store<E>(dq + t * D + lane * E, gq);
     dl = warp_sum(dl);
     if (lane == 0) delta[t] = dl;
     a_bg += dz;
@@ -644,9 +689,11 @@ static size_t bwd_layout(const Problem& p, int dtype, uint8_t* base, BwdLayout* 
   };
   const size_t rows = (size_t)p.BH * p.L, dd = (size_t)p.d * p.d, chunks = (size_t)p.BH * p.N;
   BwdLayout l{};
-  l.d_os = (float*)take(rows * p.d * 4);               // d o_s
+  if (dtype != 0)
+    l.d_os = (float*)take(rows * p.d * 4);             // d o_s
+  else
+    l.d_os16 = (__nv_bfloat16*)take(rows * p.d * 2);   // d o_s in bf16 (the operand of the tensor-core products)
   l.d_ol = (float*)take(rows * p.d * 4);               // d o_l
-  l.d_os16 = (__nv_bfloat16*)take(rows * p.d * 2);     // d o_s in bf16 (the operand of the tensor-core products)
   l.delta = (float*)take(rows * 4);
   l.lse = (float*)take(rows * 4);
   if (dtype != 0) {

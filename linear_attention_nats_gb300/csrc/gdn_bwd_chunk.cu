@@ -700,7 +700,7 @@ struct DsSm {
 };
 
 template <int D>
-__global__ void __launch_bounds__(256) gdn_bwd_ds_kernel(
+__global__ void __launch_bounds__(256, 2) gdn_bwd_ds_kernel(
     const bf16* __restrict__ k, const float* __restrict__ S0, const float* __restrict__ dSC,
     const float* __restrict__ Ug, const float* __restrict__ Li, const float* __restrict__ PtdO,
     const float* __restrict__ Vh, const float* __restrict__ Gb, const float* __restrict__ beta,
@@ -755,18 +755,18 @@ __global__ void __launch_bounds__(256) gdn_bwd_ds_kernel(
       return PtdO[(row0 + i) * D + a] + gC / sGam[i] * val * ikd;
     });
   }
+  // this kernel's share of dk, written once at the end
+  float dka[NT][4];
+  zero(dka);
   if (committed) {  // U dS_C: dk += diag(gamma_C / gamma) (U dS_C); dG_j -= (U dS_C)_j . K~_j; the last token gains their sum
-    float acc[NT][4];
-    zero(acc);
-    hmm<NT, D, false, true>(acc, m0, n0, hU, LD, hS, LD);
+    hmm<NT, D, false, true>(dka, m0, n0, hU, LD, hS, LD);
     const float iud = 1.f / (su * sd), ik = 1.f / sk;
     float lo = 0.f, hi = 0.f;
-    each(acc, m0, n0, [&](int i, int n, float val, int, int e) {
-      const float f = gC / sGam[i];
-      const float x = f * val * iud;
-      dk[(row0 + i) * D + n] += x;
+    each_mut(dka, m0, n0, [&](int i, int n, float val, int, int e) {
+      const float x = gC / sGam[i] * val * iud;
       const float dd = x * ik * __half2float(hK[i * LD + n]);
       if (e < 2) lo -= dd; else hi -= dd;
+      return x;
     });
     float tot = warp_sum(-(lo + hi));
     add_rows(lo, hi, m0, sdG);
@@ -802,9 +802,9 @@ __global__ void __launch_bounds__(256) gdn_bwd_ds_kernel(
     hmm<NT, D, false, true>(acc, m0, n0, hD, LD, hS, LD);
     const float iys = 1.f / (sy * ss), ik = 1.f / sk;
     float lo = 0.f, hi = 0.f;
-    each(acc, m0, n0, [&](int i, int n, float val, int, int e) {
+    each(acc, m0, n0, [&](int i, int n, float val, int j, int e) {
       const float x = sGam[i] * val * iys;
-      dk[(row0 + i) * D + n] -= x;
+      dk[(row0 + i) * D + n] += dka[j][e] - x;
       const float dd = x * ik * __half2float(hK[i * LD + n]);
       if (e < 2) lo -= dd; else hi -= dd;
     });

@@ -169,11 +169,12 @@ def test_backward_validation(nat):
     need = nat.lib.nats_bwd_workspace_size(ctypes.byref(dm))
     rows, dd, chunks = 2 * 128, 64 * 64, 2 * 2
     al = lambda b: (b + 255) // 256 * 256
-    common = 2 * al(rows * 64 * 4) + al(rows * 64 * 2) + 2 * al(rows * 4)  # d o_s, d o_l, d o_s bf16, delta, lse
+    common = al(rows * 64 * 4) + 2 * al(rows * 4)  # d o_l, delta, lse; then d o_s (fp32 layers) or its bf16 copy
+    common_f32, common = common + al(rows * 64 * 4), common + al(rows * 64 * 2)
     # fp32 layers: 2 chunk-start states, one chunk of states, one held gradient, then the two state halves'
     # per-token column sums and scalars
     f32 = nat.lib.nats_bwd_workspace_size(ctypes.byref(nat.dims(1, 2, 128, 64, nat.NATS_F32)))
-    assert f32 == common + (al(chunks * dd * 4) + al(2 * 64 * dd * 4) + al(2 * dd * 4) + al(2 * rows * 2 * 64 * 4)
+    assert f32 == common_f32 + (al(chunks * dd * 4) + al(2 * 64 * dd * 4) + al(2 * dd * 4) + al(2 * rows * 2 * 64 * 4)
                             + al(2 * rows * 4 * 4))
     # bf16 layers: the compacted softmax-chunk lists, the forward's chunk factors (G, W, U^T, P, gate, o_l,
     # error flag), then the chunkwise adjoint's chunk-start states and state gradients, G, Linv and P (fp32),
