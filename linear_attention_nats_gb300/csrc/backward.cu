@@ -722,10 +722,11 @@ static size_t bwd_layout(const Problem& p, int dtype, uint8_t* base, BwdLayout* 
     w.Qe16 = take(rows * p.d * 2);
     w.Kt16 = take(rows * p.d * 2);
     w.sc = (float*)take(chunks * 4 * 4);
-    w.Vh = (float*)take(rows * p.d * 4);
-    w.U = (float*)take(rows * p.d * 4);
-    w.PtdO = (float*)take(rows * p.d * 4);
-    w.Y = (float*)take(rows * p.d * 4);
+    w.Vh = take(rows * p.d * 2);
+    w.U = take(rows * p.d * 2);
+    w.PtdO = take(rows * p.d * 2);
+    w.Y = take(rows * p.d * 2);
+    w.isc = (float*)take(chunks * 4 * 4);
     w.dG = (float*)take(rows * 4);
   }
   if (o) *o = l;

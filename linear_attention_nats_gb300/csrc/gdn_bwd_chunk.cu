@@ -298,6 +298,39 @@ __device__ __forceinline__ float acc_h(const float (&acc)[NT][4], int m0, int n0
   return s;
 }
 
+// fp16 C x D rows (global, row stride D) -> the padded tile, asynchronously
+template <int D>
+__device__ __forceinline__ void copy_h(half* dst, const half* src) {
+  for (int x = threadIdx.x; x < C * D / 8; x += 256) {
+    const int r = x / (D / 8), c8 = 8 * (x % (D / 8));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst + r * H<D>::ld + c8)),
+                 "l"(src + (size_t)r * D + c8)
+                 : "memory");
+  }
+}
+__device__ __forceinline__ void copy_wait() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// accumulators (rows m0.., columns n0..) -> fp16 rows in memory (row stride
+// D), scaled by a power of two taken over the block (a collective); returns
+// the scale
+template <int NT, int D>
+__device__ __forceinline__ float acc_store_h(const float (&acc)[NT][4], int m0, int n0, half* dst, float* red) {
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(acc[j][e]));
+  const float s = block_scale(m, red);
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const int c0 = n0 + 8 * j + 2 * t;
+    *(__half2*)(dst + (size_t)(m0 + g) * D + c0) = __floats2half2_rn(acc[j][0] * s, acc[j][1] * s);
+    *(__half2*)(dst + (size_t)(m0 + g + 8) * D + c0) = __floats2half2_rn(acc[j][2] * s, acc[j][3] * s);
+  }
+  return s;
+}
+
 template <int NT, class F>
 __device__ __forceinline__ void each_mut(float (&acc)[NT][4], int m0, int n0, F f) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -611,8 +644,9 @@ template <int D>
 __global__ void __launch_bounds__(256) gdn_bwd_s0_kernel(
     const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v, const float* __restrict__ dO,
     const float* __restrict__ S0, const float* __restrict__ Li, const float* __restrict__ Pg,
-    const float* __restrict__ Gb, const float* __restrict__ beta, int L, int N, float scale, float* __restrict__ Vh,
-    float* __restrict__ Ug, float* __restrict__ PtdO, float* __restrict__ dq, float* __restrict__ dGs) {
+    const float* __restrict__ Gb, const float* __restrict__ beta, int L, int N, float scale, half* __restrict__ Vh,
+    half* __restrict__ Ug, half* __restrict__ PtdO, float* __restrict__ isc, float* __restrict__ dq,
+    float* __restrict__ dGs) {
   using S = S0Sm<D>;
   constexpr int NT = D / 16, LD = H<D>::ld, LC = H<C>::ld;
   extern __shared__ __align__(16) uint8_t sm[];
@@ -646,10 +680,7 @@ __global__ void __launch_bounds__(256) gdn_bwd_s0_kernel(
   {
     const float iks = 1.f / (sk * ss);
     each_mut(acc, m0, n0, [&](int i, int n, float val, int, int) {
-      const size_t o = (row0 + i) * D + n;
-      const float vh = __bfloat162float(v[o]) - sGam[i] * val * iks;
-      Vh[o] = vh;
-      return vh;
+      return __bfloat162float(v[(row0 + i) * D + n]) - sGam[i] * val * iks;
     });
   }
   const float svh = acc_h<NT, D>(acc, m0, n0, hVh, red);
@@ -669,22 +700,34 @@ __global__ void __launch_bounds__(256) gdn_bwd_s0_kernel(
     add_rows(lo, hi, m0, sdG);
   }
   __syncthreads();  // hVh complete
+  // Vh as staged (fp16 at its scale), for the dbeta term of the next kernel
+  for (int x = tid; x < C * D / 8; x += 256) {
+    const int i = x / (D / 8), c8 = 8 * (x % (D / 8));
+    *(uint4*)(Vh + (row0 + i) * D + c8) = *(const uint4*)(hVh + i * LD + c8);
+  }
   // U = Linv diag(beta) Vh
   zero(acc);
   hmm<NT, C, false, true>(acc, m0, n0, hL, LC, hVh, LD);
   {
     const float iu = 1.f / (sl * svh);
-    each(acc, m0, n0, [&](int i, int n, float val, int, int) { Ug[(row0 + i) * D + n] = val * iu; });
+    each_mut(acc, m0, n0, [&](int, int, float val, int, int) { return val * iu; });
   }
+  const float su = acc_store_h<NT, D>(acc, m0, n0, Ug + row0 * D, red);
   // P^T dO
   zero(acc);
   hmm<NT, C, true, true>(acc, m0, n0, hP, LC, hO, LD);
   {
     const float ipo = 1.f / (sp * so);
-    each(acc, m0, n0, [&](int i, int n, float val, int, int) { PtdO[(row0 + i) * D + n] = val * ipo; });
+    each_mut(acc, m0, n0, [&](int, int, float val, int, int) { return val * ipo; });
   }
+  const float spo = acc_store_h<NT, D>(acc, m0, n0, PtdO + row0 * D, red);
   __syncthreads();
   if (tid < C) dGs[row0 + tid] = sdG[tid];
+  if (tid == 0) {
+    isc[chunk * 4 + 0] = svh;
+    isc[chunk * 4 + 1] = su;
+    isc[chunk * 4 + 2] = spo;
+  }
 }
 
 // ----------------------------------------------------- products with dS_C
@@ -702,9 +745,10 @@ struct DsSm {
 template <int D>
 __global__ void __launch_bounds__(256, 2) gdn_bwd_ds_kernel(
     const bf16* __restrict__ k, const float* __restrict__ S0, const float* __restrict__ dSC,
-    const float* __restrict__ Ug, const float* __restrict__ Li, const float* __restrict__ PtdO,
-    const float* __restrict__ Vh, const float* __restrict__ Gb, const float* __restrict__ beta,
-    const uint8_t* __restrict__ sel, int L, int N, float* __restrict__ Yg, float* __restrict__ dv,
+    const half* __restrict__ Ug, const float* __restrict__ Li, const half* __restrict__ PtdO,
+    const half* __restrict__ Vh, float* __restrict__ isc, const float* __restrict__ Gb,
+    const float* __restrict__ beta, const uint8_t* __restrict__ sel, int L, int N, half* __restrict__ Yg,
+    float* __restrict__ dv,
     float* __restrict__ dk, float* __restrict__ dGs, float* __restrict__ dbeta) {
   using S = DsSm<D>;
   constexpr int NT = D / 16, LD = H<D>::ld, LC = H<C>::ld;
@@ -729,7 +773,8 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_ds_kernel(
   if (tid < C) sdG[tid] = sdB[tid] = 0.f;
   if (tid < 2) red[8 + tid] = 0.f;
   const float sk = tile_h_bf<D>(k + row0 * D, hK, red);
-  const float su = tile_h<C, D>(Ug + row0 * D, D, hU, red);
+  copy_h<D>(hU, Ug + row0 * D);
+  const float svh = isc[chunk * 4 + 0], su = isc[chunk * 4 + 1], spo = isc[chunk * 4 + 2];
   const float sl = tile_h<C, C>(Li + (size_t)chunk * C * C, C, hL, red);
   float sd = 1.f;
   if (committed) {  // dS_C, and <dS_C, S0> on the way
@@ -742,6 +787,7 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_ds_kernel(
     dot = warp_sum(dot);
     if (lane == 0) atomicAdd(red + 9, dot);
   }
+  copy_wait();
   __syncthreads();
   const int m0 = 16 * (warp & 3), n0 = (warp >> 2) * (D / 2);
   const float gC = sGam[C - 1];
@@ -750,9 +796,9 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_ds_kernel(
   zero(dU);
   if (committed) hmm<NT, D, false, false>(dU, m0, n0, hK, LD, hS, LD);
   {
-    const float ikd = 1.f / (sk * sd);
+    const float ikd = 1.f / (sk * sd), ipo = 1.f / spo;
     each_mut(dU, m0, n0, [&](int i, int a, float val, int, int) {
-      return PtdO[(row0 + i) * D + a] + gC / sGam[i] * val * ikd;
+      return __half2float(PtdO[(row0 + i) * D + a]) * ipo + gC / sGam[i] * val * ikd;
     });
   }
   // this kernel's share of dk, written once at the end
@@ -780,14 +826,15 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_ds_kernel(
   zero(acc);
   hmm<NT, C, true, true>(acc, m0, n0, hL, LC, hD, LD);
   {
-    const float iy = 1.f / (sl * sdu);
+    const float iy = 1.f / (sl * sdu), ivh = 1.f / svh;
+    each_mut(acc, m0, n0, [&](int, int, float val, int, int) { return val * iy; });
+    const float sy = acc_store_h<NT, D>(acc, m0, n0, Yg + row0 * D, red);
+    if (tid == 0) isc[chunk * 4 + 3] = sy;
     float lo = 0.f, hi = 0.f;
-    each_mut(acc, m0, n0, [&](int i, int n, float val, int, int e) {
+    each_mut(acc, m0, n0, [&](int i, int n, float y, int, int e) {
       const size_t o = (row0 + i) * D + n;
-      const float y = val * iy;
-      Yg[o] = y;
       dv[o] += sB[i] * y;
-      const float dd = y * Vh[o];
+      const float dd = y * __half2float(Vh[o]) * ivh;
       if (e < 2) lo += dd; else hi += dd;
       return sB[i] * y;
     });
@@ -834,8 +881,9 @@ struct CcSm {
 template <int D>
 __global__ void __launch_bounds__(256) gdn_bwd_cc_kernel(
     const bf16* __restrict__ q, const bf16* __restrict__ k, const float* __restrict__ dO,
-    const float* __restrict__ Ug, const float* __restrict__ Yg, const float* __restrict__ Gb,
-    const float* __restrict__ beta, int L, int N, float scale, float* __restrict__ dq, float* __restrict__ dk,
+    const half* __restrict__ Ug, const half* __restrict__ Yg, const float* __restrict__ isc,
+    const float* __restrict__ Gb, const float* __restrict__ beta, int L, int N, float scale,
+    float* __restrict__ dq, float* __restrict__ dk,
     const float* __restrict__ dGs, float* __restrict__ dbeta, float* __restrict__ dg) {
   using S = CcSm<D>;
   constexpr int NT = D / 16, LD = H<D>::ld, LC = H<C>::ld;
@@ -861,8 +909,10 @@ __global__ void __launch_bounds__(256) gdn_bwd_cc_kernel(
   const float sq = tile_h_bf<D>(q + row0 * D, hQ, red);
   const float sk = tile_h_bf<D>(k + row0 * D, hK, red);
   const float so = tile_h<C, D>(dO + row0 * D, D, hO, red);
-  const float su = tile_h<C, D>(Ug + row0 * D, D, hU, red);
-  const float sy = tile_h<C, D>(Yg + row0 * D, D, hY, red);
+  copy_h<D>(hU, Ug + row0 * D);
+  copy_h<D>(hY, Yg + row0 * D);
+  const float su = isc[chunk * 4 + 1], sy = isc[chunk * 4 + 3];
+  copy_wait();
   __syncthreads();
   float sa, spm;
   {
@@ -996,12 +1046,12 @@ cudaError_t run(const Problem& p, const void* q, const void* k, const void* v, c
       qb, kb, g, beta, p.L, p.N, p.scale, w.G, w.Li, w.P, (half*)w.W16, (half*)w.Qe16, (half*)w.Kt16, w.sc);
   gdn_bwd_scan_kernel<D><<<(unsigned)(p.BH * (D / RB)), 256, ScanSm<D>::kBytes, st>>>(
       (const half*)w.Kt16, (const half*)w.W16, (const half*)w.Qe16, w.sc, dO, w.G, sel, p.L, p.N, w.dSC);
-  gdn_bwd_s0_kernel<D><<<(unsigned)chunks, 256, S0Sm<D>::kBytes, st>>>(qb, kb, vb, dO, w.S0, w.Li, w.P, w.G, beta,
-                                                                      p.L, p.N, p.scale, w.Vh, w.U, w.PtdO, dq,
-                                                                      w.dG);
-  gdn_bwd_ds_kernel<D><<<(unsigned)chunks, 256, DsSm<D>::kBytes, st>>>(kb, w.S0, w.dSC, w.U, w.Li, w.PtdO, w.Vh,
-                                                                      w.G, beta, sel, p.L, p.N, w.Y, dv, dk, w.dG,
-                                                                      dbeta);
+  gdn_bwd_s0_kernel<D><<<(unsigned)chunks, 256, S0Sm<D>::kBytes, st>>>(
+      qb, kb, vb, dO, w.S0, w.Li, w.P, w.G, beta, p.L, p.N, p.scale, (half*)w.Vh, (half*)w.U, (half*)w.PtdO, w.isc,
+      dq, w.dG);
+  gdn_bwd_ds_kernel<D><<<(unsigned)chunks, 256, DsSm<D>::kBytes, st>>>(
+      kb, w.S0, w.dSC, (const half*)w.U, w.Li, (const half*)w.PtdO, (const half*)w.Vh, w.isc, w.G, beta, sel, p.L,
+      p.N, (half*)w.Y, dv, dk, w.dG, dbeta);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (launches) *launches += 4;
   return cudaSuccess;
@@ -1011,7 +1061,8 @@ template <int D>
 cudaError_t run_cc(const Problem& p, const void* q, const void* k, const float* beta, const float* dO,
                    const GdnBwdScratch& w, float* dq, float* dk, float* dg, float* dbeta, cudaStream_t st) {
   gdn_bwd_cc_kernel<D><<<(unsigned)(p.BH * p.N), 256, CcSm<D>::kBytes, st>>>(
-      (const bf16*)q, (const bf16*)k, dO, w.U, w.Y, w.G, beta, p.L, p.N, p.scale, dq, dk, w.dG, dbeta, dg);
+      (const bf16*)q, (const bf16*)k, dO, (const half*)w.U, (const half*)w.Y, w.isc, w.G, beta, p.L, p.N, p.scale,
+      dq, dk, w.dG, dbeta, dg);
   return cudaGetLastError();
 }
 

@@ -91,10 +91,11 @@ struct GdnBwdScratch {
   void* Qe16;   // [BH, L, dk] fp16: diag(gamma) Q~ - P W      >  power-of-two scale
   void* Kt16;   // [BH, L, dk] fp16: diag(gamma_C / gamma) K  /   (sc)
   float* sc;    // [BH, N, 4] the scales of W, Q_eff, K~
-  float* Vh;    // [BH, L, dv] V - diag(gamma) K S0^T
-  float* U;     // [BH, L, dv] Linv diag(beta) Vh
-  float* PtdO;  // [BH, L, dv] P^T dO
-  float* Y;     // [BH, L, dv] Linv^T dU
+  void* Vh;     // [BH, L, dv] fp16: V - diag(gamma) K S0^T   \  each times its chunk's
+  void* U;      // [BH, L, dv] fp16: Linv diag(beta) Vh        |  power-of-two scale
+  void* PtdO;   // [BH, L, dv] fp16: P^T dO                    |  (isc)
+  void* Y;      // [BH, L, dv] fp16: Linv^T dU                 /
+  float* isc;   // [BH, N, 4] the scales of Vh, U, P^T dO, Y
   float* dG;    // [BH, L] gradient of G from the state products
 };
 // chunk factors, the reverse state-gradient scan and the state products
