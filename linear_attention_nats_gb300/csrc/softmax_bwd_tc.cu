@@ -19,8 +19,10 @@
 //     Pass 1 recomputes S = Q K^T for the row log-sum-exp (written out for the
 //     second kernel); pass 2 recomputes S and forms dP = dO V^T, dS in place
 //     of S (bf16), dQ += dS K.  TMEM: two S buffers, dP, dQ.
-//   softmax_bwd_dkv_tc_kernel  key tile: query blocks = its own pair, then,
-//     when either key chunk chose softmax, every later pair, taken one
+//   softmax_bwd_dkv_tc_kernel  key tiles, in two launches: the chunk pairs
+//     against their own query pair (each chunk's causal block), then pairs
+//     of the head's softmax chunks (the compacted list, no key row that
+//     later queries cannot see) against every later query pair; taken one
 //     64-query chunk at a time: S^T = K Q^T, dP^T = V dO^T (N = 64, issued
 //     one chunk ahead into the other TMEM half); P^T and dS^T in place
 //     (bf16); dV += P^T dO, dK += dS^T Q.  TMEM: S^T x 2, dP^T x 2 (64
@@ -382,22 +384,48 @@ template <int D>
 __global__ void __launch_bounds__(256, 1)
     softmax_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                              const uint8_t* __restrict__ sel, int L, int N, int T, long long BH, float scale,
-                              const float* __restrict__ lse, const float* __restrict__ delta,
-                              float* __restrict__ dk, float* __restrict__ dv, int* __restrict__ err) {
+                              const uint8_t* __restrict__ sel, const int32_t* __restrict__ nprev,
+                              const int32_t* __restrict__ sel_idx, int L, int N, int T, long long BH,
+                              float scale, int retained, const float* __restrict__ lse,
+                              const float* __restrict__ delta, float* __restrict__ dk, float* __restrict__ dv,
+                              int* __restrict__ err) {
   using S = DkvSm<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + S::offBar);
   uint32_t* tmem_slot = (uint32_t*)(smem + S::offTmem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int p = (int)(blockIdx.x / BH);  // heaviest first: early softmax chunks are seen by the most queries
+  // The key tile: two chunk slots.  Local tiles (retained = 0) are the
+  // chunk pairs (2p, 2p + 1) against their own query pair only: each
+  // chunk's causal block and, when 2p chose softmax, 2p + 1's queries on its
+  // keys; they write dk, dv.  Retained tiles (retained = 1) are pairs of the
+  // head's softmax chunks (its compacted list) against every later query
+  // chunk, and add into dk, dv.  Heaviest tiles first in both.
+  const int jt = (int)(blockIdx.x / BH);
   const long long bh = blockIdx.x % BH;
   const long long row0 = bh * (long long)L;
-  const int kc0 = 2 * p;
-  const bool has_k1 = kc0 + 1 < N;
-  const bool soft0 = sel[bh * N + kc0] == 0, soft1 = has_k1 && sel[bh * N + kc0 + 1] == 0;
-  const int nq = 1 + ((soft0 || soft1) ? T - 1 - p : 0);  // query pairs: the own one, then every later one
+  int kc0, kc1, r0, nq;
+  bool has_k1, soft0, soft1;
+  if (!retained) {
+    kc0 = 2 * jt;
+    has_k1 = kc0 + 1 < N;
+    kc1 = has_k1 ? kc0 + 1 : kc0;
+    soft0 = sel[bh * N + kc0] == 0;
+    soft1 = has_k1 && sel[bh * N + kc1] == 0;
+    r0 = jt;
+    nq = 1;
+  } else {
+    const int nsoft = nprev[bh * N + N - 1] + (sel[bh * N + N - 1] == 0 ? 1 : 0);
+    if (2 * jt >= nsoft) return;  // (uniform over the CTA, before any barrier)
+    kc0 = sel_idx[bh * N + 2 * jt];
+    has_k1 = 2 * jt + 1 < nsoft;
+    kc1 = has_k1 ? sel_idx[bh * N + 2 * jt + 1] : kc0;
+    soft0 = true;
+    soft1 = has_k1;
+    r0 = kc0 / 2 + 1;  // the first query pair after kc0's own (which the local tile covers)
+    nq = T - r0;
+    if (nq <= 0) return;
+  }
   const float sl2 = scale * 1.4426950408889634f;
 
   if (threadIdx.x == 0) {
@@ -434,7 +462,7 @@ __global__ void __launch_bounds__(256, 1)
       tc::prefetch_tensormap(&tm_do);
       tc::mbar_arrive_expect_tx(&bars[KV_F], 2 * S::kT);
       for (int slot = 0; slot < 2; ++slot) {
-        const int y = (int)(row0 + 64LL * (slot && has_k1 ? kc0 + 1 : kc0));
+        const int y = (int)(row0 + 64LL * (slot ? kc1 : kc0));
         for (int h = 0; h < D / 64; ++h) {
           tc::tma_load_2d(smem + S::offK + h * kHalf + slot * (kHalf / 2), &tm_k, 64 * h, y, &bars[KV_F]);
           tc::tma_load_2d(smem + S::offV + h * kHalf + slot * (kHalf / 2), &tm_v, 64 * h, y, &bars[KV_F]);
@@ -443,7 +471,7 @@ __global__ void __launch_bounds__(256, 1)
       bool ok = true;
       int issued = 0;
       for (int i = 0; i < nq && ok; ++i) {
-        const int s = i & 1, r = p + i;
+        const int s = i & 1, r = r0 + i;
         const bool has_q1 = 2 * r + 1 < N;
         const uint32_t vb = has_q1 ? 512 : 256;  // the rows' lse and delta that exist
         if (!(ok = tc::mbar_wait(&bars[KV_QE + s], ((i >> 1) & 1) ^ 1, err))) break;
@@ -531,21 +559,24 @@ __global__ void __launch_bounds__(256, 1)
     // -------------------------------------------------------- elementwise
     const int kr = threadIdx.x - 128;
     const int ks = kr >> 6, ki = kr & 63;
-    const int kc = kc0 + ks;
+    const int kc = ks ? kc1 : kc0;
     const bool valid = ks == 0 || has_k1;
     const bool soft_k = ks == 0 ? soft0 : soft1;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     bool ok = true;
     for (int u = 0; u < 2 * nq && ok; ++u) {
       const int i = u >> 1, h = u & 1, s = i & 1;
-      const int qc = 2 * (p + i) + h;  // the query chunk of this step
+      const int qc = 2 * (r0 + i) + h;  // the query chunk of this step
       if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[KV_SF + h], (u >> 1) & 1, err)))) break;
       if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[KV_PF + h], (u >> 1) & 1, err)))) break;
       tc::fence_after();
       const float* ls = (const float*)(smem + S::offVec + s * 1024) + 64 * h;
       const float* dls = ls + 128;
-      int mode = kNone;  // whether this key row sees the chunk's queries
-      if (valid && qc < N) mode = qc == kc ? kCausal : ((soft_k && qc > kc) ? kFull : kNone);
+      int mode = kNone;  // whether this key row sees the chunk's queries (its own chunk: local tiles only)
+      if (valid && qc < N) {
+        if (!retained) mode = qc == kc ? kCausal : ((soft_k && qc > kc) ? kFull : kNone);
+        else mode = (qc >> 1) > (kc >> 1) ? kFull : kNone;  // query pairs after the key chunk's own
+      }
       const uint32_t ts = tmem + 64 * h + lane_off, tp = tmem + 128 + 64 * h + lane_off;
       if (mode == kNone) {  // (warp-uniform: a warp's rows share a key chunk) nothing to read
         uint32_t z[16];
@@ -595,7 +626,7 @@ __global__ void __launch_bounds__(256, 1)
     // epilogue: dv = dV, dk = scale dK (every key row belongs to one tile)
     if (ok && (ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[KV_DONE], 0, err)))) {
       tc::fence_after();
-      const size_t row = (size_t)(row0 + 64LL * kc0 + kr);
+      const size_t row = (size_t)(row0 + 64LL * kc + ki);
 #pragma unroll 1
       for (int w2 = 0; w2 < 2; ++w2) {
 #pragma unroll 1
@@ -607,8 +638,14 @@ __global__ void __launch_bounds__(256, 1)
             const float f = w2 ? scale : 1.f;
             float4* dst = (float4*)((w2 ? dk : dv) + row * D + 32 * ch);
 #pragma unroll
-            for (int x = 0; x < 8; ++x)
-              dst[x] = make_float4(f * o[4 * x], f * o[4 * x + 1], f * o[4 * x + 2], f * o[4 * x + 3]);
+            for (int x = 0; x < 8; ++x) {
+              float4 a = make_float4(f * o[4 * x], f * o[4 * x + 1], f * o[4 * x + 2], f * o[4 * x + 3]);
+              if (retained) {  // add to the local tile's
+                const float4 b = dst[x];
+                a.x += b.x, a.y += b.y, a.z += b.z, a.w += b.w;
+              }
+              dst[x] = a;
+            }
           }
         }
       }
@@ -644,8 +681,10 @@ cudaError_t run(const Problem& p, const void* q, const void* k, const void* v, c
   const unsigned grid = (unsigned)(p.BH * T);
   softmax_bwd_dq_tc_kernel<D><<<grid, 256, DqSm<D>::kBytes, st>>>(mq, mk, mv, mo, nprev, sel_idx, sel, p.L, p.N, T,
                                                                   p.BH, p.scale, delta, lse, dq, err);
-  softmax_bwd_dkv_tc_kernel<D><<<grid, 256, DkvSm<D>::kBytes, st>>>(mq, mk, mv, mo, sel, p.L, p.N, T, p.BH, p.scale,
-                                                                    lse, delta, dk, dv, err);
+  for (int retained = 0; retained < 2; ++retained)
+    softmax_bwd_dkv_tc_kernel<D><<<grid, 256, DkvSm<D>::kBytes, st>>>(mq, mk, mv, mo, sel, nprev, sel_idx, p.L, p.N,
+                                                                      T, p.BH, p.scale, retained, lse, delta, dk,
+                                                                      dv, err);
   return cudaGetLastError();
 }
 
