@@ -873,12 +873,13 @@ def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):
                    key) pair (scores recomputed, dP, dq, dk, dv), plus the
                    compaction of the softmax-chunk lists;
       gdn_bwd      the Gated DeltaNet stage and the per-chunk C x C stage
-                   together, tf32 tensor (warp-level MMAs): per chunk the
-                   forward's chunk factors and scan that recompute the chunk
-                   start states (5 C^2 d + 6 C d^2 FLOP, the forward's count)
+                   together, fp16 / bf16 tensor: per chunk the forward's chunk
+                   factors and scan that recompute the chunk start states
+                   (5 C^2 d + 6 C d^2 FLOP, the forward's count, on tcgen05)
                    and the chunkwise adjoint's products, 2 (8 C d^2 + 15 C^2 d)
-                   FLOP (full tiles; rolled-back chunks skip some), against
-                   the bf16 peak x 1.1 / 2.25 (the nominal tf32 : bf16 ratio).
+                   FLOP (full tiles; rolled-back chunks skip some; fp16
+                   operands, fp32 accumulation, warp-level mma.sync m16n8k16),
+                   against the bf16 peak (the fp16 dense rate is the same).
     The headline roofline is the stage with the largest share of the time."""
     import torch
 
@@ -938,18 +939,16 @@ def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):
     chunks = B * H * (L // Cc)
     amounts = {"merge_bwd": ("hbm", (22 * d + 4) * tokens, stage_ms["merge_bwd"]),
                "softmax_bwd": ("tensor", 10 * d * pairs, stage_ms["softmax_bwd"]),
-               "gdn_bwd": ("tf32", chunks * (5 * Cc * Cc * d + 6 * Cc * d * d + 2 * (8 * Cc * d * d + 15 * Cc * Cc * d)),
+               "gdn_bwd": ("tensor", chunks * (5 * Cc * Cc * d + 6 * Cc * d * d + 2 * (8 * Cc * d * d + 15 * Cc * Cc * d)),
                            stage_ms["gdn_bwd"] + stage_ms["combine"])}
     per = {}
     for name, (bound, amount, sms) in amounts.items():
         if bound == "hbm":
             ach, peak, unit, src = amount / (sms / 1e3) / 1e9, pk["hbm_gbs"], "GB/s", f"{pk['source']} HBM copy"
-        elif bound == "tensor":
-            ach, peak, unit = amount / (sms / 1e3) / 1e12, pk["bf16_tflops_sustained"], "TFLOP/s"
-            src = f"{pk['source']} bf16 sustained (tcgen05)"
         else:
-            ach, peak, unit = amount / (sms / 1e3) / 1e12, pk["bf16_tflops_sustained"] * 1.1 / 2.25, "TFLOP/s"
-            src = f"{pk['source']} bf16 sustained x 1.1 / 2.25 (tf32; mma.sync m16n8k8)"
+            ach, peak, unit = amount / (sms / 1e3) / 1e12, pk["bf16_tflops_sustained"], "TFLOP/s"
+            src = f"{pk['source']} bf16 sustained" + (" (tcgen05)" if name == "softmax_bwd" else
+                                                      " (tcgen05 recompute; fp16 mma.sync adjoint)")
         per[name] = {"bound": bound, "ms": sms, "share": sms / ms if ms else None, "achieved": ach, "peak": peak,
                      "unit": unit, "frac": (ach / peak) if peak else None, "peak_source": src,
                      ("bytes_per_step" if bound == "hbm" else "flops_per_step"): amount}

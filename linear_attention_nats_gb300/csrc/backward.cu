@@ -790,14 +790,14 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
         e2 = launch_softmax_bwd_tc(p, q, k, v, d_os16, delta, lay.nprev, lay.sel_idx, sel, lse, dq, dk, dv,
                                    lay.ferr, st);
       if (e2 != cudaSuccess) return e2;
-      count(NATS_BWD_STAGE_SOFTMAX, 1);  // the compaction
+      count(NATS_BWD_STAGE_SOFTMAX, 4);  // compaction, query tiles, local and retained key tiles
     } else {
       softmax_bwd_rows_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(qt, kt, vt, sel, d_os, delta,
                                                                                rows, p.L, p.N, p.scale, lse, dq);
       softmax_bwd_keys_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
           qt, kt, vt, sel, d_os, delta, lse, rows, p.L, p.N, p.scale, dk, dv);
+      count(NATS_BWD_STAGE_SOFTMAX, 2);
     }
-    count(NATS_BWD_STAGE_SOFTMAX, 2);
     if ((e2 = mark(ev_stop, NATS_BWD_STAGE_SOFTMAX)) != cudaSuccess) return e2;
     if ((e2 = mark(ev_start, NATS_BWD_STAGE_GDN)) != cudaSuccess) return e2;
     if constexpr (tc) {

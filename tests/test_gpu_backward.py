@@ -121,11 +121,12 @@ def test_backward_profiled_stages():
         assert torch.allclose(plain[n], timed[n], rtol=1e-5, atol=1e-6 * float(plain[n].abs().max())), n
     for n in GRADS[5:]:
         assert torch.allclose(plain[n], timed[n], rtol=1e-5, atol=1e-5 * float(plain[n].abs().max())), n
-    # bf16: merge; the softmax-chunk lists, softmax dq, dk / dv; the Gated DeltaNet stage (chunk
+    # bf16: merge; the softmax-chunk lists, softmax dq, dk / dv (local and
+    # retained key tiles); the Gated DeltaNet stage (chunk
     # factors and scan of the forward for the chunk-start states, the adjoint's
     # chunk factors, reverse scan, S0 and dS_C products); the C x C products
-    assert list(prof.stage_launches)[:len(_native.BWD_STAGES)] == [1, 3, 6, 1]
-    assert prof.launches == 11
+    assert list(prof.stage_launches)[:len(_native.BWD_STAGES)] == [1, 4, 6, 1]
+    assert prof.launches == 12
     ms = [a.elapsed_time(b) for a, b in ev]
     assert all(m > 0 for m in ms), ms
     for (_, b), (a, _) in zip(ev, ev[1:]):  # stage i ends before stage i + 1 starts

@@ -188,4 +188,3 @@ def test_out_without_branch_outputs(name):
         err = rel_err(out[heads][:, rows], ref["out"][:, rows])
     print(f"[parity] {name} out only: out={err:.2e}")
     assert err <= TOL[inp.dtype]
-
