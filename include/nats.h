@@ -32,8 +32,10 @@
  *     it does hold is listed here.  Per device, created on first use and
  *     kept until the process exits: one side stream and two events (the
  *     layer forward runs its two branches concurrently on that stream,
- *     forked from and joined back into `stream`).  Per loaded library, on
- *     every GPU: the fixed scratch array of nats_hybrid_fwd_noalloc.
+ *     forked from and joined back into `stream`; nats_hybrid_fwd_streams
+ *     takes caller-owned ones instead, or runs both branches on `stream`).
+ *     Per loaded library, on every GPU: the fixed scratch array of
+ *     nats_hybrid_fwd_noalloc.
  *   - Arguments are validated on the host before anything is launched; a
  *     violation returns its status and leaves every output untouched.
  *   - Launch failures return NATS_ERR_CUDA (from cudaGetLastError).  Errors
@@ -223,6 +225,43 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
                                      uint8_t* sel_out, float* state_out, float* o_soft_out,
                                      float* o_lin_out, void* workspace, size_t workspace_bytes,
                                      nats_stream_t stream, nats_profile* prof);
+
+/* Caller-owned concurrency for the layer forward.  With bf16 inputs the
+ * forward runs its Gated DeltaNet scan on `stream` and the softmax branch on
+ * a second stream, forked from `stream` before the branches and joined back
+ * before the merge.  nats_hybrid_fwd and nats_hybrid_fwd_profiled take that
+ * second stream and the fork / join events from the library's per-device
+ * set; here the caller supplies them, and the call uses no library-held
+ * stream or event (and takes no lock):
+ *   side  the second stream (a cudaStream_t of the current device), or
+ *         NULL, or `stream` itself: then both branches run in order on
+ *         `stream` and fork / join are not used (may be NULL);
+ *   fork  a cudaEvent_t the call records on `stream` and makes `side` wait
+ *         for; join a cudaEvent_t it records on `side` and makes `stream`
+ *         wait for.  Any creation flags; the caller keeps them alive until
+ *         the call has been enqueued (they may be reused right after).
+ * Concurrent calls that share `side` or the events must be ordered by the
+ * caller. */
+typedef struct {
+  nats_stream_t side;
+  void* fork;
+  void* join;
+} nats_streams;
+
+/* nats_hybrid_fwd_profiled with caller-owned concurrency (streams may be
+ * NULL, which makes it identical to nats_hybrid_fwd_profiled).  Same
+ * arguments, errors and results; NATS_ERR_NULL when streams->side is a
+ * stream other than `stream` and fork or join is NULL; NATS_ERR_CUDA when
+ * recording or waiting on them fails. */
+nats_status nats_hybrid_fwd_streams(const nats_dims* dims, const void* q, const void* k,
+                                    const void* v, const float* g, const float* beta,
+                                    const float* w_s, const float* b_s, const float* w_g,
+                                    const float* b_g, const float* norm_w_soft,
+                                    const float* norm_w_lin, const uint8_t* sel_in, void* out,
+                                    uint8_t* sel_out, float* state_out, float* o_soft_out,
+                                    float* o_lin_out, void* workspace, size_t workspace_bytes,
+                                    nats_stream_t stream, const nats_streams* streams,
+                                    nats_profile* prof);
 
 /* ---- The projections around the layer ------------------------------------
  * The layer above takes Q, K, V and the gates; a model layer makes them

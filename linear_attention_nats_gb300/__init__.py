@@ -82,9 +82,15 @@ def select(q, k, w_s, b_s=None, *, scores: bool = False, stream=None):
 def hybrid_fwd(q, k, v, g, beta, w_s, b_s, w_g, b_g=None, *, norm_w_soft=None, norm_w_lin=None,
                sel_in=None, scale: float = 0.0, eps: float = 1e-6, out=None, workspace=None,
                return_sel: bool = False, return_state: bool = False,
-               return_branches: bool = False, check_errors: bool = False, stream=None, profile=None):
+               return_branches: bool = False, check_errors: bool = False, stream=None, profile=None,
+               side_stream=None):
     """NAtS-L hybrid attention layer forward (nats_hybrid_fwd; with `profile`,
-    a _native.Profile, nats_hybrid_fwd_profiled).
+    a _native.Profile, nats_hybrid_fwd_profiled; with `side_stream`,
+    nats_hybrid_fwd_streams).
+
+    side_stream: a torch.cuda.Stream for the softmax branch (fork / join
+    events are made here), or the string "serial" for both branches in order
+    on `stream`; None uses the library's per-device side stream.
 
     q, k, v: [B, H, L, d] bf16 or fp32 (same dtype); g, beta: fp32 [B, H, L];
     w_s: fp32 [H, 2, 2d]; b_s: fp32 [H, 2] or None; w_g: fp32 [H, d];
@@ -124,7 +130,16 @@ def hybrid_fwd(q, k, v, g, beta, w_s, b_s, w_g, b_g=None, *, norm_w_soft=None, n
     args = (ctypes.byref(dm), _p(q), _p(k), _p(v), _p(g), _p(beta), _p(w_s), _p(b_s), _p(w_g), _p(b_g),
             _p(norm_w_soft), _p(norm_w_lin), _p(sel_in), _p(out), _p(sel), _p(state), _p(o_soft),
             _p(o_lin), _p(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream))
-    if profile is None:
+    if side_stream is not None:
+        streams = _native.Streams()
+        if side_stream != "serial":
+            ev = [torch.cuda.Event(), torch.cuda.Event()]
+            for e in ev:  # materialise the event handles
+                e.record(side_stream)
+            streams.side, streams.fork, streams.join = side_stream.cuda_stream, ev[0].cuda_event, ev[1].cuda_event
+        prof = ctypes.byref(profile) if profile is not None else None
+        check(_native.lib.nats_hybrid_fwd_streams(*args, ctypes.byref(streams), prof), "nats_hybrid_fwd_streams")
+    elif profile is None:
         check(_native.lib.nats_hybrid_fwd(*args), "nats_hybrid_fwd")
     else:
         check(_native.lib.nats_hybrid_fwd_profiled(*args, ctypes.byref(profile)), "nats_hybrid_fwd_profiled")

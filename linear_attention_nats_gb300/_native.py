@@ -24,7 +24,8 @@ STATUS = {
 
 # Every symbol include/nats.h declares.
 EXPORTS = ("nats_status_string", "nats_last_cuda_error", "nats_workspace_size", "nats_workspace_check", "nats_select",
-           "nats_hybrid_fwd", "nats_hybrid_fwd_profiled", "nats_hybrid_fwd_noalloc", "nats_noalloc_check",
+           "nats_hybrid_fwd", "nats_hybrid_fwd_profiled", "nats_hybrid_fwd_streams", "nats_hybrid_fwd_noalloc",
+           "nats_noalloc_check",
            "nats_x_workspace_size", "nats_x_workspace_check",
            "nats_hybrid_fwd_x_profiled",
            "nats_hybrid_fwd_x", "nats_debug_fail_stage", "nats_debug_bounded_wait", "nats_decode_step",
@@ -42,6 +43,11 @@ BWD_STAGES = ("merge_bwd", "softmax_bwd", "gdn_bwd", "combine")
 class Profile(ctypes.Structure):
     _fields_ = [("start", ctypes.c_void_p * NUM_STAGES), ("stop", ctypes.c_void_p * NUM_STAGES),
                 ("launches", ctypes.c_int32), ("stage_launches", ctypes.c_int32 * NUM_STAGES)]
+
+
+class Streams(ctypes.Structure):
+    """nats_streams: the caller's second stream and fork / join events."""
+    _fields_ = [("side", ctypes.c_void_p), ("fork", ctypes.c_void_p), ("join", ctypes.c_void_p)]
 
 
 class DecodeState(ctypes.Structure):
@@ -99,6 +105,9 @@ def _load() -> ctypes.CDLL:
     lib.nats_hybrid_fwd_profiled.argtypes = [ctypes.POINTER(Dims)] + [P] * 18 + [
         ctypes.c_size_t, P, ctypes.POINTER(Profile)]
     lib.nats_hybrid_fwd_profiled.restype = ctypes.c_int
+    lib.nats_hybrid_fwd_streams.argtypes = [ctypes.POINTER(Dims)] + [P] * 18 + [
+        ctypes.c_size_t, P, ctypes.POINTER(Streams), ctypes.POINTER(Profile)]
+    lib.nats_hybrid_fwd_streams.restype = ctypes.c_int
     lib.nats_hybrid_fwd_noalloc.argtypes = [ctypes.POINTER(Dims)] + [P] * 17 + [P]
     lib.nats_hybrid_fwd_noalloc.restype = ctypes.c_int
     lib.nats_noalloc_check.argtypes = [ctypes.POINTER(Dims), P]

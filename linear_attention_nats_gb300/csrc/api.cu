@@ -228,17 +228,21 @@ nats_status nats_select(const nats_dims* dims, const void* q, const void* k, con
   return cuda_status(launch_score(p, dims->dtype, q, k, w_s, b_s, sel, scores, (cudaStream_t)stream));
 }
 
-nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const void* k,
-                                     const void* v, const float* g, const float* beta,
-                                     const float* w_s, const float* b_s, const float* w_g,
-                                     const float* b_g, const float* norm_w_soft,
-                                     const float* norm_w_lin, const uint8_t* sel_in, void* out,
-                                     uint8_t* sel_out, float* state_out, float* o_soft_out,
-                                     float* o_lin_out, void* workspace, size_t workspace_bytes,
-                                     nats_stream_t stream, nats_profile* prof) {
+nats_status nats_hybrid_fwd_streams(const nats_dims* dims, const void* q, const void* k,
+                                    const void* v, const float* g, const float* beta,
+                                    const float* w_s, const float* b_s, const float* w_g,
+                                    const float* b_g, const float* norm_w_soft,
+                                    const float* norm_w_lin, const uint8_t* sel_in, void* out,
+                                    uint8_t* sel_out, float* state_out, float* o_soft_out,
+                                    float* o_lin_out, void* workspace, size_t workspace_bytes,
+                                    nats_stream_t stream, const nats_streams* streams,
+                                    nats_profile* prof) {
   bool empty = false;
   nats_status s = check_fwd_args(dims, q, k, v, g, beta, w_s, w_g, sel_in, out, &empty);
   if (s != NATS_OK) return s;
+  // caller-owned concurrency: a second stream other than `stream` needs both events
+  const bool own_side = streams && streams->side && streams->side != stream;
+  if (own_side && (!streams->fork || !streams->join)) return NATS_ERR_NULL;
   const Problem p = problem_of(dims);
   if (prof) {
     prof->launches = 0;
@@ -290,23 +294,32 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
     // workspace (the merge reads half the bytes)
     float* o_l = o_lin_out;
     void* o_l16 = o_lin_out ? nullptr : (void*)ws.o_l;
-    Side* sd = side_of_current_device();
+    // (the caller's second stream and events, or the library's per-device
+    // ones, or none: in order on `stream`)
+    Side* sd = streams ? nullptr : side_of_current_device();
     {
       std::unique_lock<std::mutex> lk;
       cudaStream_t ss = st;
-      if (sd) {
+      cudaEvent_t fork = nullptr, join = nullptr;
+      if (own_side) {
+        ss = (cudaStream_t)streams->side;
+        fork = (cudaEvent_t)streams->fork;
+        join = (cudaEvent_t)streams->join;
+      } else if (sd) {
         lk = std::unique_lock<std::mutex>(sd->mu);
-        if (cudaEventRecord(sd->fork, st) != cudaSuccess || cudaStreamWaitEvent(sd->s, sd->fork, 0) != cudaSuccess)
-          return NATS_ERR_CUDA;
         ss = sd->s;
+        fork = sd->fork;
+        join = sd->join;
       }
+      if (ss != st && (cudaEventRecord(fork, st) != cudaSuccess || cudaStreamWaitEvent(ss, fork, 0) != cudaSuccess))
+        return NATS_ERR_CUDA;
       NATS_STAGE(stg, NATS_STAGE_GDN_SCAN, 1,
                  launch_gdn_scan_tc(p, q, k, sel, ws.G, ws.W, ws.U, ws.P, o_l, o_l16, state_out, ws.err, st));
       Stages stg_side{prof, ss};
       NATS_STAGE(stg_side, NATS_STAGE_SOFTMAX, 1,
                  launch_softmax_tc(p, q, k, v, ws.nprev, ws.sel_idx, sel, ws.gate, norm_w_soft, out, o_soft_out,
                                    ws.err, ss));
-      if (sd && (cudaEventRecord(sd->join, sd->s) != cudaSuccess || cudaStreamWaitEvent(st, sd->join, 0) != cudaSuccess))
+      if (ss != st && (cudaEventRecord(join, ss) != cudaSuccess || cudaStreamWaitEvent(st, join, 0) != cudaSuccess))
         return NATS_ERR_CUDA;
     }
     // 6. out += (1 - w) RMSNorm(o_l)
@@ -324,6 +337,19 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
                launch_norm_merge(p, dt, o_s, o_l, q, w_g, b_g, norm_w_soft, norm_w_lin, out, st));
   }
   return NATS_OK;
+}
+
+nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const void* k,
+                                     const void* v, const float* g, const float* beta,
+                                     const float* w_s, const float* b_s, const float* w_g,
+                                     const float* b_g, const float* norm_w_soft,
+                                     const float* norm_w_lin, const uint8_t* sel_in, void* out,
+                                     uint8_t* sel_out, float* state_out, float* o_soft_out,
+                                     float* o_lin_out, void* workspace, size_t workspace_bytes,
+                                     nats_stream_t stream, nats_profile* prof) {
+  return nats_hybrid_fwd_streams(dims, q, k, v, g, beta, w_s, b_s, w_g, b_g, norm_w_soft, norm_w_lin, sel_in, out,
+                                 sel_out, state_out, o_soft_out, o_lin_out, workspace, workspace_bytes, stream,
+                                 nullptr, prof);
 }
 
 nats_status nats_hybrid_fwd(const nats_dims* dims, const void* q, const void* k, const void* v,

@@ -276,3 +276,26 @@ def test_score_bwd_validation(nat):
         assert call(nat.dims(1, 2, 512, 128, 0), ok[:i] + [None] + ok[i + 1:]) == 1, i
     for i in (0, 1, 5, 6, 7, 8):  # q, k, out, dout, dq, dk 16-byte aligned
         assert call(nat.dims(1, 2, 512, 128, 0), ok[:i] + [P(0x10000004)] + ok[i + 1:]) == 4, i
+
+
+def test_streams_validation(nat):
+    # nats_hybrid_fwd_streams: a second stream other than `stream` needs both
+    # events (checked after the shape and pointer checks, before the workspace)
+    dm = nat.dims(1, 2, 256, 64)
+    names = ["q", "k", "v", "g", "beta", "w_s", "b_s", "w_g", "b_g", "nws", "nwl", "sel_in", "out",
+             "sel_out", "state", "o_soft", "o_lin", "ws"]
+
+    def call(dmx, streams, ws_bytes=1 << 40, **ptrs):
+        args = [None if ptrs.get(n) is None else ctypes.c_void_p(ptrs[n]) for n in names]
+        return nat.lib.nats_hybrid_fwd_streams(ctypes.byref(dmx), *args[:17], args[17], ctypes.c_size_t(ws_bytes),
+                                               None, ctypes.byref(streams) if streams is not None else None, None)
+
+    side = ctypes.c_void_p(0x7000).value
+    for fork, join in ((None, None), (A, None), (None, A)):
+        assert call(dm, nat.Streams(side, fork, join), **FULL) == 1
+    assert call(nat.dims(1, 2, 100, 64), nat.Streams(side, None, None), **FULL) == 2  # shapes first
+    need = nat.lib.nats_workspace_size(ctypes.byref(dm))
+    # no second stream (or the caller's own): events not needed, the workspace check comes next
+    for st in (nat.Streams(None, None, None), None):
+        assert call(dm, st, ws_bytes=need - 1, **FULL) == 5
+    assert call(dm, nat.Streams(side, A, A), ws_bytes=need - 1, **FULL) == 5
