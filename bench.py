@@ -66,6 +66,8 @@ def parse():
     ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass measurement")
     ap.add_argument("--no-nha", action="store_true", help="skip the Native Hybrid Attention measurement")
     ap.add_argument("--no-select", action="store_true", help="skip the score-layer (nats_select) measurement")
+    ap.add_argument("--decode-context", type=int, default=8192,
+                    help="context length before the timed decode steps (a multiple of 64)")
     ap.add_argument("--workload", default="l8192",
                     help="layer workload of the device-timed step (default: the 8192-token one); others, e.g. "
                          "'long' (1 x 32 x 65536, 12.5 %% softmax chunks), are extra data points")
@@ -963,9 +965,10 @@ def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):
 
 
 def run_decode(args, rank, dev, stream, dist):
-    """Times nats_decode_step after an 8192-token context (B = 4, H = 16,
-    d = 128, bf16, 25 % of the context's chunks retained: 2048 keys / values
-    per head): K steps at positions following the warm-up steps, captured in
+    """Times nats_decode_step after a T-token context (--decode-context,
+    default 8192; B = 4, H = 16, d = 128, bf16, 25 % of the context's chunks
+    retained: T / 4 keys / values per head): K steps at positions following
+    the warm-up steps, captured in
     a CUDA graph and replayed (device time, CUDA events, max over ranks), as
     a serving loop would run them; the same steps issued one call at a time
     from Python are reported beside it (host-bound).  The steps go through
@@ -977,7 +980,9 @@ def run_decode(args, rank, dev, stream, dist):
 
     import linear_attention_nats_gb300 as nats
 
-    B, H, d, t0, kept, NL = 4, 16, 128, 8192, 2048, 4
+    B, H, d, NL = 4, 16, 128, 4
+    t0 = args.decode_context
+    kept = t0 // 4
     g_ = torch.Generator(device="cpu").manual_seed(rank_seed(41, rank))
     nw = max(args.warmup, NL)
     K = max(args.steps, 32)  # steps per timed region: the graph's launch spread over enough of them
@@ -985,14 +990,18 @@ def run_decode(args, rank, dev, stream, dist):
     cap = 64 * ((t0 + steps_all // NL) // 64 + 1)
     rn = lambda *shape: torch.randn(*shape, generator=g_)
     states = []
+    # the retained keys / values are drawn once and copied into every layer's state
+    kv_k = torch.nn.functional.normalize(rn(B, H, kept, d), dim=-1).to(torch.bfloat16).to(dev)
+    kv_v = rn(B, H, kept, d).to(torch.bfloat16).to(dev)
     for _ in range(NL):
         st = nats.DecodeState(B, H, d, cap=cap, dtype=torch.bfloat16, device=dev)
         st.S.copy_(0.05 * rn(B, H, d, d))
         st.S0.copy_(st.S)
-        st.kv_k[:, :, :kept].copy_(torch.nn.functional.normalize(rn(B, H, kept, d), dim=-1).to(torch.bfloat16))
-        st.kv_v[:, :, :kept].copy_(rn(B, H, kept, d).to(torch.bfloat16))
+        st.kv_k[:, :, :kept].copy_(kv_k)
+        st.kv_v[:, :, :kept].copy_(kv_v)
         st.n_kv.fill_(kept)
         states.append(st)
+    del kv_k, kv_v
     q = rn(steps_all, B, H, d).to(torch.bfloat16).to(dev)
     k = torch.nn.functional.normalize(rn(steps_all, B, H, d), dim=-1).to(torch.bfloat16).to(dev)
     v = rn(steps_all, B, H, d).to(torch.bfloat16).to(dev)
@@ -1046,10 +1055,12 @@ def run_decode(args, rank, dev, stream, dist):
     nbytes = B * H * (2 * d * d * 4 + (kept + p_mean + 1) * d * 2 * 2 + 5 * d * 2)
     pk = peaks()
     gbs = nbytes / (ms / 1e3) / 1e9
-    return {"what": "nats_decode_step: one token per (b, h) after an 8192-token context, 25 % of its chunks "
-                    "retained (2048 keys / values per head)",
+    step_mb = B * H * (2 * d * d * 4 + (kept + 64) * d * 2 * 2) / 2**20
+    return {"what": f"nats_decode_step: one token per (b, h) after a {t0}-token context, 25 % of its chunks "
+                    f"retained ({kept} keys / values per head)",
             "config": {"B": B, "H": H, "d": d, "position": t0, "retained_per_head": kept, "layers_in_turn": NL,
-                       "l2": "four layers' states in turn: each step's 76 MB was evicted by the other three"},
+                       "l2": f"four layers' states in turn: each step's {step_mb:.0f} MB was evicted by the other "
+                             "three"},
             "value": job_throughput(B, world, ms), "unit": "tokens/s", "ms_per_step": ms, "steps": K,
             "host_loop_ms_per_step": host_ms,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",

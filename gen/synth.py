@@ -264,6 +264,10 @@ CONFIGS = {
     "sweep50": dict(B=1, H=16, L=32768, d=128, dtype="bf16", seed=3, pattern="random", frac=0.5),
     "sweep100": dict(B=1, H=16, L=32768, d=128, dtype="bf16", seed=3, pattern="all"),
     "long": dict(B=1, H=32, L=65536, d=128, dtype="bf16", seed=4, pattern="bursts", bursts=(4, 24, 32)),
+    # the 128k context at which the pages quote prefill and decode latency
+    "l128k": dict(B=1, H=4, L=131072, d=128, dtype="bf16", seed=6, pattern="random", frac=0.25),
+    # the same shape with every chunk softmax: full causal attention through the same kernels
+    "l128k_full": dict(B=1, H=4, L=131072, d=128, dtype="bf16", seed=6, pattern="all"),
 }
 
 

@@ -147,7 +147,7 @@ def _sample_rows(L, n, seed):
     return rows
 
 
-@pytest.mark.parametrize("name", ["l8192", "sweep0", "sweep12", "sweep50", "sweep100", "long"])
+@pytest.mark.parametrize("name", ["l8192", "sweep0", "sweep12", "sweep50", "sweep100", "long", "l128k"])
 def test_full_size_sampled(name):
     inp = gen.config_inputs(name)
     got = run_cuda(inp)

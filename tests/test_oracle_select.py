@@ -94,7 +94,7 @@ def test_workload_margins():
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["l8192", "sweep0", "sweep12", "sweep50", "sweep100", "long"])
+@pytest.mark.parametrize("name", ["l8192", "sweep0", "sweep12", "sweep50", "sweep100", "long", "l128k"])
 def test_large_workload_margins(name):
     """The full-size workloads too: every argmax margin >= 1e-3 on the rounded
     inputs (fp64 scores), and the score layer recovers the planted chunks
