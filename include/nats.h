@@ -50,8 +50,9 @@
  *     ordered by the caller.
  *   - Supported shapes: chunk = 64, L % 64 == 0, dk == dv in {64, 128},
  *     B, H, L >= 0 (any zero extent makes the call a no-op that returns
- *     NATS_OK).  Q, K, V, the output and the workspace must be 16-byte
- *     aligned.
+ *     NATS_OK), and B H L dk / 64 < 2^31 (tile coordinates are 32-bit;
+ *     else NATS_ERR_UNSUPPORTED).  Q, K, V, the output and the workspace
+ *     must be 16-byte aligned.
  */
 #ifndef NATS_H_
 #define NATS_H_

@@ -26,9 +26,11 @@ nats_status check_dims(const nats_dims* d) {
   if (d->dk != 64 && d->dk != 128) return NATS_ERR_UNSUPPORTED;
   if (!std::isfinite(d->scale) || d->scale < 0.f || !std::isfinite(d->eps) || d->eps < 0.f)
     return NATS_ERR_VALUE;
-  // every flat element offset must fit the int64 / int32 grid arithmetic used below
+  // every flat element offset must fit the int64 / int32 grid arithmetic,
+  // and every TMA row coordinate a 32-bit int: the largest is a line of the
+  // transposed chunk factor U^T, (B H N + c) d
   const long long BH = (long long)d->B * d->H;
-  if (BH > (1LL << 31) - 1 || BH * (d->L / kChunk) > (1LL << 31) - 1) return NATS_ERR_UNSUPPORTED;
+  if (BH > (1LL << 31) - 1 || BH * (d->L / kChunk) * d->dk > (1LL << 31) - 1) return NATS_ERR_UNSUPPORTED;
   return NATS_OK;
 }
 

@@ -50,6 +50,10 @@ def test_workspace_size(nat):
     assert ws(1, 1, 64, 64) > 0
     assert ws(1, 1, 100, 64) == 0  # L % 64 != 0
     assert ws(1, 1, 64, 96) == 0  # unsupported head size
+    # the largest TMA row coordinate, (B H N + c) d, must fit a 32-bit int
+    assert ws(1, 1 << 14, 1 << 16, 128) == 0
+    assert ws(1, 1 << 14, 1 << 16, 64) > 0
+    assert ws(1, (1 << 14) - 1, 1 << 16, 128) > 0
     assert ws(0, 4, 256, 64) >= 0
     small, big = ws(1, 2, 256, 64), ws(2, 2, 256, 64)
     assert big > small
