@@ -17,8 +17,8 @@
 //
 // One CTA per (b, h) walks the N chunks in order; the fp32 state S stays in
 // TMEM for the whole sequence, next to its bf16 copy S0.  Per chunk c:
-//   MMA1  [X | O] = S0 [W; Q~]^T  into TMEM buffer c % 2 (M = 128 lanes >= dv,
-//         N = 128: X = S0 W^T and the first term of O in one product, K = dk)
+//   MMA1  X = S0 W^T, then O = S0 Q~^T, into TMEM buffer c % 2 (M = 128
+//         lanes >= dv, N = 64 each, K = dk; X first, so Delta starts early)
 //   all   Delta^T = U^T - X -> TMEM (bf16)
 //   MMA3  S += Delta^T K~                (linear chunks only), then
 //   MMA2  O += Delta^T P^T
@@ -156,7 +156,6 @@ __global__ void __launch_bounds__(448, 1)
   } else if (warp == 9) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t id1 = tc::idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t id2 = tc::idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t id3 = tc::idesc_bf16_f32(128, D, false, true);
       // descriptors are built once per stage; each MMA only offsets them
@@ -175,17 +174,23 @@ __global__ void __launch_bounds__(448, 1)
         if (!(ok = tc::mbar_wait(&bars[SB_FULL + s], (c / S::kStages) & 1, err))) break;
         if (!(ok = tc::mbar_wait(&bars[SB_SCALED + s], (c / S::kStages) & 1, err))) break;
         if (!(ok = tc::mbar_wait(&bars[SB_S0], c & 1, err))) break;
-        if (c >= 2 && !(ok = tc::mbar_wait(&bars[SB_OFREE + (c & 1)], ((c - 2) / 2) & 1, err))) break;
         tc::fence_after();
-        // [S0 W^T | S0 Q~^T] in one N = 128 product over the stacked [W; Q~]
-        // tile (128 lines per 64-column half): X for Delta, and the first
-        // term of O, for the cost of one 64-wide product
+        // X = S0 W^T first (the W lines of the stacked [W; Q~] tile), so that
+        // Delta can start; then the first term of O, S0 Q~^T (the Q~ lines),
+        // once O buffer c % 2 has been read out
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t offb = (kk >> 2) * 16384 + (kk & 3) * 32;
-          tc::mma_bf16_ts(tX, tmem + kColS0 + kk * 8, tc::desc_add(wd, offb), id1, kk > 0);
+          tc::mma_bf16_ts(tX, tmem + kColS0 + kk * 8, tc::desc_add(wd, offb), id2, kk > 0);
         }
         tc::mma_commit(&bars[SB_Z]);
+        if (c >= 2 && !(ok = tc::mbar_wait(&bars[SB_OFREE + (c & 1)], ((c - 2) / 2) & 1, err))) break;
+        tc::fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t offb = (kk >> 2) * 16384 + (kk & 3) * 32 + 8192;
+          tc::mma_bf16_ts(tO, tmem + kColS0 + kk * 8, tc::desc_add(wd, offb), id2, kk > 0);
+        }
         if (!(ok = tc::mbar_wait(&bars[SB_DELTA], c & 1, err))) break;
         tc::fence_after();
         // the state update first (the next chunk waits for it), then O
