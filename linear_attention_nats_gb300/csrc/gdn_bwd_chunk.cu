@@ -27,7 +27,9 @@
 // over the chunks: dS_c = dS0 of chunk c with dS_C = dS_{c+1} for a committed
 // chunk, dS_{c+1} + dO^T Q_eff for a rolled-back one.
 //
-// Kernels (after the forward scan has written every chunk's S0):
+// Kernels (after the forward scan has written every chunk's S0; S0 and
+// dS_C are stored transposed, [dk][dv], so that both scans write them as
+// whole lines):
 //   gdn_bwd_prep_kernel  per chunk: G, Linv, P (fp32), W, Q_eff, K~ (fp16, scaled)
 //   gdn_bwd_scan_kernel  per (b, h, 64 state rows): the reverse scan, writing
 //                        dS_C of every committed chunk (fp32)
@@ -586,12 +588,14 @@ __global__ void __launch_bounds__(256) gdn_bwd_scan_kernel(const half* __restric
     const long long ch = bh * N + c;
     const bool lin = sel[ch] != 0;
     const float sw = sc[ch * 4], sqe = sc[ch * 4 + 1], skt = sc[ch * 4 + 2];
-    // dS_C of a committed chunk (the last chunk's is zero and is not read)
+    // dS_C of a committed chunk (the last chunk's is zero and is not read),
+    // stored transposed ([dk][dv]) like the chunk-start states: for each
+    // column the CTA's RB rows are contiguous
     if (lin && c < N - 1) {
-      float* dst = dSC + (((size_t)ch) * D + r0) * D;
-      for (int x = tid; x < RB * D / 4; x += 256) {
-        const int i = x / (D / 4), c4 = x % (D / 4);
-        *(float4*)(dst + (size_t)i * D + 4 * c4) = *(const float4*)(sdS + i * FS + 4 * c4);
+      float* dst = dSC + (size_t)ch * D * D + r0;
+      for (int x = tid; x < RB * D; x += 256) {
+        const int kc = x / RB, i = x % RB;
+        dst[(size_t)kc * D + i] = sdS[i * FS + kc];
       }
     }
     // the step's dO columns (fp16, scaled)
@@ -676,7 +680,7 @@ __global__ void __launch_bounds__(256) gdn_bwd_s0_kernel(
   float acc[NT][4];
   // Vh = V - diag(gamma) K S0^T
   zero(acc);
-  hmm<NT, D, false, false>(acc, m0, n0, hK, LD, hS, LD);
+  hmm<NT, D, false, true>(acc, m0, n0, hK, LD, hS, LD);
   {
     const float iks = 1.f / (sk * ss);
     each_mut(acc, m0, n0, [&](int i, int n, float val, int, int) {
@@ -686,7 +690,7 @@ __global__ void __launch_bounds__(256) gdn_bwd_s0_kernel(
   const float svh = acc_h<NT, D>(acc, m0, n0, hVh, red);
   // dO S0: dq += scale gamma_i (dO S0)_i; dG_i += gamma_i (dO S0)_i . q~_i
   zero(acc);
-  hmm<NT, D, false, true>(acc, m0, n0, hO, LD, hS, LD);
+  hmm<NT, D, false, false>(acc, m0, n0, hO, LD, hS, LD);
   {
     const float ios = scale / (so * ss);
     float lo = 0.f, hi = 0.f;
@@ -794,7 +798,7 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_ds_kernel(
   // dU = P^T dO + K~ dS_C^T (registers, fp32)
   float dU[NT][4];
   zero(dU);
-  if (committed) hmm<NT, D, false, false>(dU, m0, n0, hK, LD, hS, LD);
+  if (committed) hmm<NT, D, false, true>(dU, m0, n0, hK, LD, hS, LD);
   {
     const float ikd = 1.f / (sk * sd), ipo = 1.f / spo;
     each_mut(dU, m0, n0, [&](int i, int a, float val, int, int) {
@@ -805,7 +809,7 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_ds_kernel(
   float dka[NT][4];
   zero(dka);
   if (committed) {  // U dS_C: dk += diag(gamma_C / gamma) (U dS_C); dG_j -= (U dS_C)_j . K~_j; the last token gains their sum
-    hmm<NT, D, false, true>(dka, m0, n0, hU, LD, hS, LD);
+    hmm<NT, D, false, false>(dka, m0, n0, hU, LD, hS, LD);
     const float iud = 1.f / (su * sd), ik = 1.f / sk;
     float lo = 0.f, hi = 0.f;
     each_mut(dka, m0, n0, [&](int i, int n, float val, int, int e) {
@@ -846,7 +850,7 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_ds_kernel(
   __syncthreads();
   {  // dk -= diag(gamma) dVh S0; dG_i -= gamma_i (dVh S0)_i . k_i
     zero(acc);
-    hmm<NT, D, false, true>(acc, m0, n0, hD, LD, hS, LD);
+    hmm<NT, D, false, false>(acc, m0, n0, hD, LD, hS, LD);
     const float iys = 1.f / (sy * ss), ik = 1.f / sk;
     float lo = 0.f, hi = 0.f;
     each(acc, m0, n0, [&](int i, int n, float val, int j, int e) {

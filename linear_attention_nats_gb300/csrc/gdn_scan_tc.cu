@@ -380,18 +380,19 @@ __global__ void __launch_bounds__(448, 1)
       tc::fence_before();
       tc::mbar_arrive(&bars[SB_S0]);
       // the state at the start of chunk c + 1 (after this chunk's update or
-      // rollback), fp32, when the caller keeps them (backward recompute);
-      // no product writes S before this thread's next Delta
+      // rollback), fp32, when the caller keeps them (backward recompute),
+      // stored transposed ([dk][dv]): for each column the warp's 32 rows are
+      // 128 contiguous bytes; no product writes S before this thread's next
+      // Delta
       if (s0_out && c + 1 < N && has_row) {
 #pragma unroll 1
         for (int ch = 0; ch < SC / 32; ++ch) {
           float v[32];
           tc::tmem_ld32(tmem + kColS + lane_off + hf * SC + ch * 32, v);
           tc::tmem_ld_wait();
-          float* dst = s0_out + ((bh * N + c + 1) * D + r) * (long long)D + hf * SC + ch * 32;
+          float* dst = s0_out + ((bh * N + c + 1) * D + hf * SC + ch * 32) * (long long)D + r;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            ((float4*)dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          for (int i = 0; i < 32; ++i) dst[(size_t)i * D] = v[i];
         }
       }
       // the next chunk's MMA3 accumulates onto gamma_C S: scale now, off the

@@ -82,8 +82,8 @@ cudaError_t launch_score_bwd(const Problem& p, int dtype, const void* q, const v
 // Chunkwise Gated DeltaNet adjoint of bf16 layers (gdn_bwd_chunk.cu): its
 // scratch, carved from the backward workspace.
 struct GdnBwdScratch {
-  float* S0;    // [BH, N, dv, dk] chunk-start states (the forward recompute writes them)
-  float* dSC;   // [BH, N, dv, dk] gradient of each committed chunk's end state
+  float* S0;    // [BH, N, dk, dv] chunk-start states, transposed (the forward recompute writes them)
+  float* dSC;   // [BH, N, dk, dv] gradient of each committed chunk's end state, transposed
   float* G;     // [BH, L] in-chunk cumulative log-decay
   float* Li;    // [BH, N, C, C] (I + diag(beta) A)^{-1}
   float* P;     // [BH, N, C, C] lower(e^{G_i - G_j} scale q_i . k_j)
