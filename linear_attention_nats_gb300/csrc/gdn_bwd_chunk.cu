@@ -589,13 +589,16 @@ __global__ void __launch_bounds__(256) gdn_bwd_scan_kernel(const half* __restric
     const bool lin = sel[ch] != 0;
     const float sw = sc[ch * 4], sqe = sc[ch * 4 + 1], skt = sc[ch * 4 + 2];
     // dS_C of a committed chunk (the last chunk's is zero and is not read),
-    // stored transposed ([dk][dv]) like the chunk-start states: for each
-    // column the CTA's RB rows are contiguous
+    // stored transposed ([dk][dv]) like the chunk-start states: a thread
+    // gathers four consecutive rows of one column into a 16-byte store, a
+    // warp four whole 128-byte lines (32 rows of 4 columns)
     if (lin && c < N - 1) {
       float* dst = dSC + (size_t)ch * D * D + r0;
-      for (int x = tid; x < RB * D; x += 256) {
-        const int kc = x / RB, i = x % RB;
-        dst[(size_t)kc * D + i] = sdS[i * FS + kc];
+      for (int x = tid; x < RB * D / 4; x += 256) {
+        const int b = x >> 5, l = x & 31;
+        const int i = 32 * (b % (RB / 32)) + 4 * (l & 7), kc = 4 * (b / (RB / 32)) + (l >> 3);
+        const float* src = sdS + i * FS + kc;
+        *(float4*)(dst + (size_t)kc * D + i) = make_float4(src[0], src[FS], src[2 * FS], src[3 * FS]);
       }
     }
     // the step's dO columns (fp16, scaled)

@@ -123,8 +123,8 @@ def test_chunk_adjoint_fragments_stay_in_their_tiles(D):
     shapes = {"CD": (C, D), "DD": (D, D), "CC": (C, C)}
     products = [  # (output columns, K, A tile, A kind, B tile, B kind)
         (C, D, "CD", "a", "CD", "b"),    # K K^T, Q K^T, Y U^T, dO U^T
-        (D, D, "CD", "a", "DD", "b"),    # K S0^T, K~ dS_C^T
-        (D, D, "CD", "a", "DD", "bt"),   # dO S0, U dS_C, dVh S0
+        (D, D, "CD", "a", "DD", "b"),    # dO S0, U dS_C, dVh S0 (S0, dS_C stored [dk][dv])
+        (D, D, "CD", "a", "DD", "bt"),   # K S0^T, K~ dS_C^T
         (D, C, "CC", "a", "CD", "bt"),   # Linv diag(.) K, P W, Linv diag(beta) Vh, dPm K, A~ K
         (D, C, "CC", "at", "CD", "bt"),  # P^T dO, Linv^T dU, dPm^T Q, A~^T K
     ]
@@ -150,3 +150,31 @@ def test_chunk_adjoint_fragments_stay_in_their_tiles(D):
             return {(r, c) for r in range(nrows) for c in range(0, ncols_, 8)}
         assert seen_a == (segs(0, C, K) if ka == "a" else segs(0, K, C)), (ncols, K, ka)
         assert seen_b == (segs(0, ncols, K) if kb == "b" else segs(0, K, ncols)), (ncols, K, kb)
+
+
+def test_reverse_scan_transposed_store():
+    """gdn_bwd_scan_kernel stores each committed chunk's dS_C rows (RB = 64 of
+    them per CTA, fp32 shared rows of stride D + 4) transposed, four rows of
+    one column per 16-byte store: every (row, column) exactly once, inside
+    both buffers, 16-byte aligned, and each warp's stores four whole
+    128-byte lines."""
+    RB = 64
+    for D in (64, 128):
+        FS = D + 4
+        seen = set()
+        for w0 in range(0, RB * D // 4, 32):
+            lines = set()
+            for lane in range(32):
+                x = w0 + lane
+                b, l = x >> 5, x & 31
+                i = 32 * (b % (RB // 32)) + 4 * (l & 7)
+                kc = 4 * (b // (RB // 32)) + (l >> 3)
+                assert 0 <= i <= RB - 4 and 0 <= kc < D
+                assert ((i + 3) * FS + kc) < RB * FS
+                off = kc * D + i  # floats from a 64-row-aligned base
+                assert off % 4 == 0
+                for j in range(4):
+                    seen.add((i + j, kc))
+                lines.add(off * 4 // 128)
+            assert len(lines) == 4
+        assert len(seen) == RB * D
