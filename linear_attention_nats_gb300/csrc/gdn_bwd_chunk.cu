@@ -572,7 +572,26 @@ __global__ void __launch_bounds__(256) gdn_bwd_scan_kernel(const half* __restric
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
   if (N > 0) prefetch(N - 1);
+  // the step's selection, scales and end-of-chunk log-decay, read one step
+  // ahead (a global load on the chain costs as much as a product)
+  struct StepScalars {
+    bool lin;
+    float sw, sqe, skt, GC;
+  };
+  auto step_scalars = [&](int c) {
+    StepScalars t;
+    const long long ch = bh * N + c;
+    t.lin = sel[ch] != 0;
+    t.sw = sc[ch * 4];
+    t.sqe = sc[ch * 4 + 1];
+    t.skt = sc[ch * 4 + 2];
+    t.GC = Gb[(size_t)bh * L + (size_t)c * C + C - 1];
+    return t;
+  };
+  StepScalars nx = step_scalars(N > 0 ? N - 1 : 0);
   for (int c = N - 1; c >= 0; --c) {
+    const StepScalars cur = nx;
+    if (c > 0) nx = step_scalars(c - 1);
     if (c > 0) {
       prefetch(c - 1);
       asm volatile("cp.async.wait_group 1;" ::: "memory");
@@ -586,8 +605,8 @@ __global__ void __launch_bounds__(256) gdn_bwd_scan_kernel(const half* __restric
     const half* hQe = (const half*)stage_ptr(st, 2);
     const float* sO = (const float*)stage_ptr(st, 3);
     const long long ch = bh * N + c;
-    const bool lin = sel[ch] != 0;
-    const float sw = sc[ch * 4], sqe = sc[ch * 4 + 1], skt = sc[ch * 4 + 2];
+    const bool lin = cur.lin;
+    const float sw = cur.sw, sqe = cur.sqe, skt = cur.skt;
     // dS_C of a committed chunk (the last chunk's is zero and is not read),
     // stored transposed ([dk][dv]) like the chunk-start states: a thread
     // gathers four consecutive rows of one column into a 16-byte store, a
@@ -624,7 +643,7 @@ __global__ void __launch_bounds__(256) gdn_bwd_scan_kernel(const half* __restric
       zero(a2);
       if (lin) hmm<NT, C, false, true>(a1, m0, n0, hX, LC, hW, LD);
       hmm<NT, C, true, true>(a2, m0, n0, hO, LR, hQe, LD);
-      const float gC = lin ? __expf(Gb[(size_t)bh * L + (size_t)c * C + C - 1]) : 1.f;
+      const float gC = lin ? __expf(cur.GC) : 1.f;
       const float f1 = 1.f / (sx * sw), f2 = 1.f / (so * sqe);
       each(a1, m0, n0, [&](int i, int n, float v, int j, int e) {
         sdS[i * FS + n] = gC * sdS[i * FS + n] + v * f1 + a2[j][e] * f2;
