@@ -245,6 +245,66 @@ __device__ __forceinline__ float tile_h(const float* src, int src_ld, half* dst,
   return tile_h<ROWS, COLS>(src, src_ld, dst, red, [](int, int, float x) { return x; });
 }
 
+// A tile held in registers between its loads and its scaled store, so that
+// the loads of several tiles are in flight together and their scales come
+// from one block-wide reduction (block_scales2).
+template <int D>
+struct BF16Tile {  // bf16 C x D (row stride D) -> scaled fp16 tile
+  static constexpr int V = C * D / 8 / 256;
+  uint4 v[V];
+  float m;
+  __device__ __forceinline__ void load(const bf16* src) {
+    m = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int x = threadIdx.x + 256 * i, r = x / (D / 8), c = 8 * (x % (D / 8));
+      v[i] = *(const uint4*)(src + (size_t)r * D + c);
+    }
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const __nv_bfloat162* h2 = (const __nv_bfloat162*)&v[i];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 f = __bfloat1622float2(h2[u]);
+        m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+  }
+  __device__ __forceinline__ void store(half* dst, float s) const {
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int x = threadIdx.x + 256 * i, r = x / (D / 8), c = 8 * (x % (D / 8));
+      const __nv_bfloat162* h2 = (const __nv_bfloat162*)&v[i];
+      uint4 o;
+      uint32_t* o32 = (uint32_t*)&o;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 f = __bfloat1622float2(h2[u]);
+        const __half2 hh = __floats2half2_rn(f.x * s, f.y * s);
+        o32[u] = *(const uint32_t*)&hh;
+      }
+      *(uint4*)(dst + r * H<D>::ld + c) = o;
+    }
+  }
+};
+// The scales of two tiles from every thread's partial maxima (a block-wide
+// collective; red: 16 floats of shared memory).
+__device__ __forceinline__ void block_scales2(float m1, float m2, float* red, float& s1, float& s2) {
+  m1 = warp_max(m1);
+  m2 = warp_max(m2);
+  __syncthreads();  // red is free again
+  if ((threadIdx.x & 31) == 0) {
+    red[threadIdx.x >> 5] = m1;
+    red[8 + (threadIdx.x >> 5)] = m2;
+  }
+  __syncthreads();
+  float r1 = red[0], r2 = red[8];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) r1 = fmaxf(r1, red[w]), r2 = fmaxf(r2, red[8 + w]);
+  s1 = pow2_scale(r1);
+  s2 = pow2_scale(r2);
+}
+
 // bf16 C x D (global, row stride D) -> scaled fp16 tile
 template <int D>
 __device__ __forceinline__ float tile_h_bf(const bf16* src, half* dst, float* red) {
@@ -932,11 +992,18 @@ __global__ void __launch_bounds__(256) gdn_bwd_cc_kernel(
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   load_scalars(Gb, beta, row0, sG, sGam, sB);
   if (tid < C) sdG[tid] = sdB[tid] = 0.f;
-  const float sq = tile_h_bf<D>(q + row0 * D, hQ, red);
-  const float sk = tile_h_bf<D>(k + row0 * D, hK, red);
-  const float so = tile_h<C, D>(dO + row0 * D, D, hO, red);
   copy_h<D>(hU, Ug + row0 * D);
   copy_h<D>(hY, Yg + row0 * D);
+  float sq, sk;
+  {  // q and k: both tiles' loads in flight at once, one reduction
+    BF16Tile<D> tq, tk;
+    tq.load(q + row0 * D);
+    tk.load(k + row0 * D);
+    block_scales2(tq.m, tk.m, red, sq, sk);
+    tq.store(hQ, sq);
+    tk.store(hK, sk);
+  }
+  const float so = tile_h<C, D>(dO + row0 * D, D, hO, red);
   const float su = isc[chunk * 4 + 1], sy = isc[chunk * 4 + 3];
   copy_wait();
   __syncthreads();
