@@ -752,11 +752,14 @@ __global__ void __launch_bounds__(256) gdn_bwd_s0_kernel(
   const int tid = threadIdx.x, warp = tid >> 5;
   load_scalars(Gb, beta, row0, sG, sGam, sB);
   if (tid < C) sdG[tid] = 0.f;
+  // V (bf16) staged in the Vh tile, which it becomes
+  copy_h<D>(hVh, (const half*)(v + row0 * D));
   const float ss = tile_h<D, D>(S0 + (size_t)chunk * D * D, D, hS, red);
   const float sk = tile_h_bf<D>(k + row0 * D, hK, red);
   const float so = tile_h<C, D>(dO + row0 * D, D, hO, red);
   const float sl = tile_h<C, C>(Li + (size_t)chunk * C * C, C, hL, red, [&](int, int m, float x) { return x * sB[m]; });
   const float sp = tile_h<C, C>(Pg + (size_t)chunk * C * C, C, hP, red);
+  copy_wait();
   __syncthreads();
   const int m0 = 16 * (warp & 3), n0 = (warp >> 2) * (D / 2);
   float acc[NT][4];
@@ -765,8 +768,9 @@ __global__ void __launch_bounds__(256) gdn_bwd_s0_kernel(
   hmm<NT, D, false, true>(acc, m0, n0, hK, LD, hS, LD);
   {
     const float iks = 1.f / (sk * ss);
+    const bf16* vs = (const bf16*)hVh;
     each_mut(acc, m0, n0, [&](int i, int n, float val, int, int) {
-      return __bfloat162float(v[(row0 + i) * D + n]) - sGam[i] * val * iks;
+      return __bfloat162float(vs[i * LD + n]) - sGam[i] * val * iks;
     });
   }
   const float svh = acc_h<NT, D>(acc, m0, n0, hVh, red);
@@ -858,8 +862,9 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_ds_kernel(
   load_scalars(Gb, beta, row0, sG, sGam, sB);
   if (tid < C) sdG[tid] = sdB[tid] = 0.f;
   if (tid < 2) red[8 + tid] = 0.f;
-  const float sk = tile_h_bf<D>(k + row0 * D, hK, red);
   copy_h<D>(hU, Ug + row0 * D);
+  copy_h<D>(hD, PtdO + row0 * D);  // P^T dO staged in the dU tile, which it becomes part of
+  const float sk = tile_h_bf<D>(k + row0 * D, hK, red);
   const float svh = isc[chunk * 4 + 0], su = isc[chunk * 4 + 1], spo = isc[chunk * 4 + 2];
   const float sl = tile_h<C, C>(Li + (size_t)chunk * C * C, C, hL, red);
   float sd = 1.f;
@@ -884,7 +889,7 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_ds_kernel(
   {
     const float ikd = 1.f / (sk * sd), ipo = 1.f / spo;
     each_mut(dU, m0, n0, [&](int i, int a, float val, int, int) {
-      return __half2float(PtdO[(row0 + i) * D + a]) * ipo + gC / sGam[i] * val * ikd;
+      return __half2float(hD[i * LD + a]) * ipo + gC / sGam[i] * val * ikd;
     });
   }
   // this kernel's share of dk, written once at the end
@@ -906,6 +911,7 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_ds_kernel(
   }
   const float sdu = acc_h<NT, D>(dU, m0, n0, hD, red);  // (its barriers also order the reads of dS_C above)
   __syncthreads();
+  copy_h<D>(hU, Vh + row0 * D);  // U has been read: Vh staged in its tile
   if (tid == 0) sdG[C - 1] += red[8] + gC * red[9];
   // Y = Linv^T dU; dv += diag(beta) Y; dbeta_i = Y_i . Vh_i
   float acc[NT][4];
@@ -914,13 +920,14 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_ds_kernel(
   {
     const float iy = 1.f / (sl * sdu), ivh = 1.f / svh;
     each_mut(acc, m0, n0, [&](int, int, float val, int, int) { return val * iy; });
+    copy_wait();  // (the barriers of the next call make every thread's Vh copies visible)
     const float sy = acc_store_h<NT, D>(acc, m0, n0, Yg + row0 * D, red);
     if (tid == 0) isc[chunk * 4 + 3] = sy;
     float lo = 0.f, hi = 0.f;
     each_mut(acc, m0, n0, [&](int i, int n, float y, int, int e) {
       const size_t o = (row0 + i) * D + n;
       dv[o] += sB[i] * y;
-      const float dd = y * __half2float(Vh[o]) * ivh;
+      const float dd = y * __half2float(hU[i * LD + n]) * ivh;
       if (e < 2) lo += dd; else hi += dd;
       return sB[i] * y;
     });
