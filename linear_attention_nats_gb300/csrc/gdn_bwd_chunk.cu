@@ -63,6 +63,32 @@ __device__ __forceinline__ void zero(float (&acc)[NT][4]) {
 }
 
 // f(row, col, value, index into the tile) for every accumulator element
+// base[r][c] += acc (rows m0.., columns n0..; row stride D), two adjacent
+// columns per 8-byte access, the loads of four column groups issued before
+// their stores
+template <int NT, int D>
+__device__ __forceinline__ void acc_add_global(const float (&acc)[NT][4], int m0, int n0, float* base) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  constexpr int GJ = NT < 4 ? NT : 4;
+#pragma unroll
+  for (int j0 = 0; j0 < NT; j0 += GJ) {
+    float2 old[GJ][2];
+#pragma unroll
+    for (int j = 0; j < GJ; ++j) {
+      const int c0 = n0 + 8 * (j0 + j) + 2 * t;
+      old[j][0] = *(const float2*)(base + (size_t)(m0 + g) * D + c0);
+      old[j][1] = *(const float2*)(base + (size_t)(m0 + g + 8) * D + c0);
+    }
+#pragma unroll
+    for (int j = 0; j < GJ; ++j) {
+      const int c0 = n0 + 8 * (j0 + j) + 2 * t;
+      const float* a = acc[j0 + j];
+      *(float2*)(base + (size_t)(m0 + g) * D + c0) = make_float2(old[j][0].x + a[0], old[j][0].y + a[1]);
+      *(float2*)(base + (size_t)(m0 + g + 8) * D + c0) = make_float2(old[j][1].x + a[2], old[j][1].y + a[3]);
+    }
+  }
+}
+
 template <int NT, class F>
 __device__ __forceinline__ void each(const float (&acc)[NT][4], int m0, int n0, F f) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -774,19 +800,23 @@ __global__ void __launch_bounds__(256) gdn_bwd_s0_kernel(
     });
   }
   const float svh = acc_h<NT, D>(acc, m0, n0, hVh, red);
+  copy_h<D>(hK, (const half*)(q + row0 * D));  // K has been read: q (bf16) staged in its tile
   // dO S0: dq += scale gamma_i (dO S0)_i; dG_i += gamma_i (dO S0)_i . q~_i
   zero(acc);
   hmm<NT, D, false, false>(acc, m0, n0, hO, LD, hS, LD);
+  copy_wait();
+  __syncthreads();
   {
     const float ios = scale / (so * ss);
+    const bf16* qs = (const bf16*)hK;
     float lo = 0.f, hi = 0.f;
-    each(acc, m0, n0, [&](int i, int n, float val, int, int e) {
-      const size_t o = (row0 + i) * D + n;
+    each_mut(acc, m0, n0, [&](int i, int n, float val, int, int e) {
       const float x = sGam[i] * val * ios;
-      dq[o] += x;
-      const float dd = x * __bfloat162float(q[o]);
+      const float dd = x * __bfloat162float(qs[i * LD + n]);
       if (e < 2) lo += dd; else hi += dd;
+      return x;
     });
+    acc_add_global<NT, D>(acc, m0, n0, dq + row0 * D);
     add_rows(lo, hi, m0, sdG);
   }
   __syncthreads();  // hVh complete
@@ -925,12 +955,11 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_ds_kernel(
     if (tid == 0) isc[chunk * 4 + 3] = sy;
     float lo = 0.f, hi = 0.f;
     each_mut(acc, m0, n0, [&](int i, int n, float y, int, int e) {
-      const size_t o = (row0 + i) * D + n;
-      dv[o] += sB[i] * y;
       const float dd = y * __half2float(hU[i * LD + n]) * ivh;
       if (e < 2) lo += dd; else hi += dd;
       return sB[i] * y;
     });
+    acc_add_global<NT, D>(acc, m0, n0, dv + row0 * D);  // dv += diag(beta) Y
     add_rows(lo, hi, m0, sdB);
   }
   __syncthreads();  // every read of dU (and of dS_C) is done
@@ -944,10 +973,11 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_ds_kernel(
     float lo = 0.f, hi = 0.f;
     each(acc, m0, n0, [&](int i, int n, float val, int j, int e) {
       const float x = sGam[i] * val * iys;
-      dk[(row0 + i) * D + n] += dka[j][e] - x;
+      dka[j][e] -= x;
       const float dd = x * ik * __half2float(hK[i * LD + n]);
       if (e < 2) lo -= dd; else hi -= dd;
     });
+    acc_add_global<NT, D>(dka, m0, n0, dk + row0 * D);
     add_rows(lo, hi, m0, sdG);
   }
   __syncthreads();
@@ -1085,7 +1115,8 @@ __global__ void __launch_bounds__(256) gdn_bwd_cc_kernel(
       zero(acc);
       hmm<NT, C, false, true>(acc, m0, n0, hPm, LC, hK, LD);
       const float f = scale / (spm * sk);
-      each(acc, m0, n0, [&](int i, int n, float val, int, int) { dq[(row0 + i) * D + n] += f * val; });
+      each_mut(acc, m0, n0, [&](int, int, float val, int, int) { return f * val; });
+      acc_add_global<NT, D>(acc, m0, n0, dq + row0 * D);
     }
     {  // dk += (dP . R)^T Q~ + (A~ + A~^T) K
       float a1[NT][4], a2[NT][4];
@@ -1095,9 +1126,8 @@ __global__ void __launch_bounds__(256) gdn_bwd_cc_kernel(
       hmm<NT, C, false, true>(a2, m0, n0, hA, LC, hK, LD);
       hmm<NT, C, true, true>(a2, m0, n0, hA, LC, hK, LD);
       const float f1 = scale / (spm * sq), f2 = 1.f / (sa * sk);
-      each(a1, m0, n0, [&](int i, int n, float val, int j, int e) {
-        dk[(row0 + i) * D + n] += f1 * val + f2 * a2[j][e];
-      });
+      each_mut(a1, m0, n0, [&](int, int, float val, int j, int e) { return f1 * val + f2 * a2[j][e]; });
+      acc_add_global<NT, D>(a1, m0, n0, dk + row0 * D);
     }
   }
   __syncthreads();
