@@ -487,8 +487,15 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
     Gb[row0 + 2 * lane + 1] = s;
   }
   if (tid < C) sB[tid] = beta[row0 + tid];
-  const float sq = tile_h_bf<D>(q + row0 * D, hQ, red);  // (block collectives: they also publish sG, sB)
-  const float sk = tile_h_bf<D>(k + row0 * D, hK, red);
+  float sq, sk;
+  {  // q and k: both tiles' loads in flight at once, one reduction (its barriers also publish sG, sB)
+    BF16Tile<D> tq, tk;
+    tq.load(q + row0 * D);
+    tk.load(k + row0 * D);
+    block_scales2(tq.m, tk.m, red, sq, sk);
+    tq.store(hQ, sq);
+    tk.store(hK, sk);
+  }
   __syncthreads();
   // beta A (strictly lower) and P (lower, diagonal included)
   float sp;
@@ -504,10 +511,18 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
       sA[i * CS + j] = j < i ? sB[i] * __expf(sG[i] - sG[j]) * v * ikk : 0.f;
     });
     each_mut(qk, m0, n0, [&](int i, int j, float v, int, int) {
-      const float pv = j <= i ? __expf(sG[i] - sG[j]) * v * iqk : 0.f;
-      P_out[(size_t)chunk * C * C + i * C + j] = pv;
-      return pv;
+      return j <= i ? __expf(sG[i] - sG[j]) * v * iqk : 0.f;
     });
+    {  // P to memory, two columns per 8-byte store
+      const int g = lane >> 2, t = lane & 3;
+      float* pd = P_out + (size_t)chunk * C * C;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c0 = n0 + 8 * j + 2 * t;
+        *(float2*)(pd + (m0 + g) * C + c0) = make_float2(qk[j][0], qk[j][1]);
+        *(float2*)(pd + (m0 + g + 8) * C + c0) = make_float2(qk[j][2], qk[j][3]);
+      }
+    }
     sp = acc_h<4, C>(qk, m0, n0, hP, red);
   }
   __syncthreads();
