@@ -404,10 +404,16 @@ nats_status nats_hybrid_bwd_profiled(const nats_dims* dims, const void* q, const
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return NATS_ERR_ALIGN;
   if (workspace_bytes < bwd_workspace_bytes(p, dims->dtype)) return NATS_ERR_WORKSPACE;
+  // bf16 layers: the adjoint's chunk factors and reverse scan run on the
+  // per-device side stream (in order on `stream` if it could not be made)
+  Side* sd = dims->dtype == NATS_BF16 ? side_of_current_device() : nullptr;
+  std::unique_lock<std::mutex> lk;
+  if (sd) lk = std::unique_lock<std::mutex>(sd->mu);
   const nats_status r = cuda_status(launch_hybrid_bwd(
       p, dims->dtype, q, k, v, g, beta, w_g, b_g, norm_w_soft, norm_w_lin, sel, o_soft, o_lin, dout, dq, dk, dv, dg,
       dbeta, dw_g, db_g, dnorm_w_soft, dnorm_w_lin, workspace, (cudaStream_t)stream, prof ? prof->start : nullptr,
-      prof ? prof->stop : nullptr, prof ? prof->stage_launches : nullptr));
+      prof ? prof->stop : nullptr, prof ? prof->stage_launches : nullptr, sd ? sd->s : nullptr,
+      sd ? sd->fork : nullptr, sd ? sd->join : nullptr));
   if (prof)
     for (int i = 0; i < NATS_BWD_NUM_STAGES; ++i) prof->launches += prof->stage_launches[i];
   return r;

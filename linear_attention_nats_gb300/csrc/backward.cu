@@ -2,10 +2,10 @@
 // the gradient of <dout, out> with respect to q, k, v, g, beta, W_g, b_g and
 // the two RMSNorm weights ("Neural Attention Search Linear (NAtS-L)",
 // technical summary, "Kernmechanismen" items 3 and 4; item 5 says the
-// selection is learned end to end but gives no estimator for the argmax, so
-// the score layer gets no gradient here).
+// selection is learned end to end but gives no estimator for the argmax: the
+// score layer's surrogate gradient is a separate call, score_bwd.cu).
 //
-// Three stages on one stream, every result in fp32:
+// Stages, every result in fp32:
 //   1. norm + merge, one warp per token: with N_x = o_x r_x w_x,
 //      r_x = (mean(o_x^2) + eps)^(-1/2), out = w N_s + (1 - w) N_l and
 //      w = sigmoid(q . W_g + b_g):
@@ -14,15 +14,18 @@
 //      dq = dz W_g (the gate's share), and the weight gradients (dW_g,
 //      db_g, the norm weights) summed per CTA, then atomically;
 //   2. softmax branch, from the row log-sum-exp: P_tj = exp(s_tj - lse_t),
-//      dS_tj = P_tj (do_s,t . v_j - do_s,t . o_s,t); bf16 layers take it on
-//      warp-level tensor-core MMAs in 64 x 64 blocks (backward_mma.cu);
-//      fp32 layers here: a row pass (one warp per query) takes lse_t and
-//      dq_t += scale sum_j dS_tj k_j, a key pass (one warp per key)
-//      dk_j = scale sum_t dS_tj q_t and dv_j = sum_t P_tj do_s,t over the
-//      queries that see key j (the rest of its chunk, and every later query
-//      when its chunk chose softmax);
-//   3. Gated DeltaNet, one CTA per (b, h): the forward is replayed for the
-//      chunk-start states, then the adjoint runs backwards.  Per token, with
+//      dS_tj = P_tj (do_s,t . v_j - do_s,t . o_s,t); bf16 layers on tcgen05
+//      (softmax_bwd_tc.cu); fp32 layers here: a row pass (one warp per
+//      query) takes lse_t and dq_t += scale sum_j dS_tj k_j, a key pass (one
+//      warp per key) dk_j = scale sum_t dS_tj q_t and dv_j = sum_t P_tj do_s,t
+//      over the queries that see key j (the rest of its chunk, and every
+//      later query when its chunk chose softmax);
+//   3. Gated DeltaNet.  bf16 layers: the chunk-start states recomputed by the
+//      forward's own kernels, then the chunkwise adjoint (gdn_bwd_chunk.cu);
+//      the recompute and the adjoint's chunk factors and reverse scan run on
+//      a second stream beside stage 2.  fp32 layers, one CTA per (b, h): the
+//      forward is replayed for the chunk-start states, then the adjoint runs
+//      backwards token by token.  Per token, with
 //      u = S_{t-1} k, e = v - a u, S_t = a S_{t-1} + beta e k^T and
 //      o_t = S_t (scale q):
 //        dS_t += do_t (scale q)^T, dq += scale S_t^T do_t (formed as
@@ -740,11 +743,13 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
                               const float* nws, const float* nwl, const uint8_t* sel, const float* o_s,
                               const float* o_l, const void* dout, float* dq, float* dk, float* dv, float* dg,
                               float* dbeta, float* dw_g, float* db_g, float* dnws, float* dnwl, void* ws,
-                              cudaStream_t st, void* const* ev_start, void* const* ev_stop, int32_t* launches) {
+                              cudaStream_t st, void* const* ev_start, void* const* ev_stop, int32_t* launches,
+                              cudaStream_t side, cudaEvent_t fork, cudaEvent_t join) {
   if (p.BH == 0 || p.L == 0) return cudaSuccess;
-  auto mark = [&](void* const* ev, int s) -> cudaError_t {
-    return (ev && ev[s]) ? cudaEventRecord((cudaEvent_t)ev[s], st) : cudaSuccess;
+  auto mark_on = [&](void* const* ev, int s, cudaStream_t on) -> cudaError_t {
+    return (ev && ev[s]) ? cudaEventRecord((cudaEvent_t)ev[s], on) : cudaSuccess;
   };
+  auto mark = [&](void* const* ev, int s) -> cudaError_t { return mark_on(ev, s, st); };
   auto count = [&](int s, int n) {
     if (launches) launches[s] += n;
   };
@@ -783,47 +788,67 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
         delta, dq, dw_g, db_g, dnws, dnwl);
     count(NATS_BWD_STAGE_MERGE, 1);
     if ((e2 = mark(ev_stop, NATS_BWD_STAGE_MERGE)) != cudaSuccess) return e2;
-    if ((e2 = mark(ev_start, NATS_BWD_STAGE_SOFTMAX)) != cudaSuccess) return e2;
-    if (tc) {
-      e2 = launch_compact(p, sel, lay.nprev, lay.sel_idx, nullptr, st);
-      if (e2 == cudaSuccess)
-        e2 = launch_softmax_bwd_tc(p, q, k, v, d_os16, delta, lay.nprev, lay.sel_idx, sel, lse, dq, dk, dv,
-                                   lay.ferr, st);
-      if (e2 != cudaSuccess) return e2;
-      count(NATS_BWD_STAGE_SOFTMAX, 4);  // compaction, query tiles, local and retained key tiles
-    } else {
-      softmax_bwd_rows_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(qt, kt, vt, sel, d_os, delta,
-                                                                               rows, p.L, p.N, p.scale, lse, dq);
-      softmax_bwd_keys_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
-          qt, kt, vt, sel, d_os, delta, lse, rows, p.L, p.N, p.scale, dk, dv);
-      count(NATS_BWD_STAGE_SOFTMAX, 2);
-    }
-    if ((e2 = mark(ev_stop, NATS_BWD_STAGE_SOFTMAX)) != cudaSuccess) return e2;
-    if ((e2 = mark(ev_start, NATS_BWD_STAGE_GDN)) != cudaSuccess) return e2;
     if constexpr (tc) {
-      // the chunk-start states, from the forward's chunk factors and scan
-      // (the same kernels as the forward; the selection is given)
-      if (D == 128)
-        e2 = launch_gdn_prep_tc(p, q, k, v, g, beta, w_g, b_g, lay.fG, lay.fW, lay.fU, lay.fP, lay.fgate, nullptr,
-                                nullptr, nullptr, lay.ferr, st);
-      else
-        e2 = launch_gdn_prep_mma(p, q, k, v, g, beta, w_g, b_g, lay.fG, lay.fW, lay.fU, lay.fP, lay.fgate, nullptr,
-                                 nullptr, nullptr, st);
-      if (e2 == cudaSuccess)
-        e2 = launch_gdn_scan_tc(p, q, k, sel, lay.fG, lay.fW, lay.fU, lay.fP, nullptr, lay.fol16, nullptr, lay.ferr,
-                                st, lay.cw.S0);
-      if (e2 != cudaSuccess) return e2;
-      count(NATS_BWD_STAGE_GDN, 2);
-      int32_t n4 = 0;
-      if ((e2 = launch_gdn_bwd_chunk(p, q, k, v, g, beta, sel, d_ol, lay.cw, dq, dk, dv, dg, dbeta, st, &n4)) !=
-          cudaSuccess)
+      // The chunk-start states' recompute and the Gated DeltaNet adjoint's
+      // chunk factors and reverse scan read only the inputs, the selection
+      // and d o_l, and write only scratch: with a second stream they run
+      // beside the softmax branch, whose CTAs fill the SMs that the two scans
+      // (chains over the chunks: 1 and 2 CTAs per head) leave idle.  They are
+      // enqueued first so that the chains start first.
+      const bool two = side && side != st && fork && join;
+      const cudaStream_t ss = two ? side : st;
+      auto softmax_stage = [&]() -> cudaError_t {
+        cudaError_t e3 = mark(ev_start, NATS_BWD_STAGE_SOFTMAX);
+        if (e3 == cudaSuccess) e3 = launch_compact(p, sel, lay.nprev, lay.sel_idx, nullptr, st);
+        if (e3 == cudaSuccess)
+          e3 = launch_softmax_bwd_tc(p, q, k, v, d_os16, delta, lay.nprev, lay.sel_idx, sel, lse, dq, dk, dv,
+                                     lay.ferr, st);
+        if (e3 != cudaSuccess) return e3;
+        count(NATS_BWD_STAGE_SOFTMAX, 4);  // compaction, query tiles, local and retained key tiles
+        return mark(ev_stop, NATS_BWD_STAGE_SOFTMAX);
+      };
+      auto states_and_factors = [&]() -> cudaError_t {
+        cudaError_t e3 = mark_on(ev_start, NATS_BWD_STAGE_GDN, ss);
+        // the chunk-start states, from the forward's chunk factors and scan
+        // (the same kernels as the forward; the selection is given)
+        if (e3 == cudaSuccess)
+          e3 = D == 128 ? launch_gdn_prep_tc(p, q, k, v, g, beta, w_g, b_g, lay.fG, lay.fW, lay.fU, lay.fP,
+                                             lay.fgate, nullptr, nullptr, nullptr, lay.ferr, ss)
+                        : launch_gdn_prep_mma(p, q, k, v, g, beta, w_g, b_g, lay.fG, lay.fW, lay.fU, lay.fP,
+                                              lay.fgate, nullptr, nullptr, nullptr, ss);
+        if (e3 == cudaSuccess)
+          e3 = launch_gdn_scan_tc(p, q, k, sel, lay.fG, lay.fW, lay.fU, lay.fP, nullptr, lay.fol16, nullptr,
+                                  lay.ferr, ss, lay.cw.S0);
+        // the adjoint's chunk factors and reverse scan
+        if (e3 == cudaSuccess) e3 = launch_gdn_bwd_factors(p, q, k, g, beta, sel, d_ol, lay.cw, ss);
+        if (e3 == cudaSuccess) count(NATS_BWD_STAGE_GDN, 4);
+        return e3;
+      };
+      if (two) {
+        if ((e2 = cudaEventRecord(fork, st)) != cudaSuccess || (e2 = cudaStreamWaitEvent(ss, fork, 0)) != cudaSuccess ||
+            (e2 = states_and_factors()) != cudaSuccess || (e2 = softmax_stage()) != cudaSuccess)
+          return e2;
+      } else if ((e2 = softmax_stage()) != cudaSuccess || (e2 = states_and_factors()) != cudaSuccess) {
         return e2;
-      count(NATS_BWD_STAGE_GDN, n4);
+      }
+      if (two && ((e2 = cudaEventRecord(join, ss)) != cudaSuccess || (e2 = cudaStreamWaitEvent(st, join, 0)) != cudaSuccess))
+        return e2;
+      if ((e2 = launch_gdn_bwd_products(p, q, k, v, beta, sel, d_ol, lay.cw, dq, dk, dv, dbeta, st)) != cudaSuccess)
+        return e2;
+      count(NATS_BWD_STAGE_GDN, 2);
       if ((e2 = mark(ev_stop, NATS_BWD_STAGE_GDN)) != cudaSuccess) return e2;
       if ((e2 = mark(ev_start, NATS_BWD_STAGE_COMBINE)) != cudaSuccess) return e2;
       if ((e2 = launch_gdn_bwd_cc(p, q, k, beta, d_ol, lay.cw, dq, dk, dg, dbeta, st)) != cudaSuccess) return e2;
       count(NATS_BWD_STAGE_COMBINE, 1);
     } else {
+      if ((e2 = mark(ev_start, NATS_BWD_STAGE_SOFTMAX)) != cudaSuccess) return e2;
+      softmax_bwd_rows_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(qt, kt, vt, sel, d_os, delta,
+                                                                               rows, p.L, p.N, p.scale, lse, dq);
+      softmax_bwd_keys_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
+          qt, kt, vt, sel, d_os, delta, lse, rows, p.L, p.N, p.scale, dk, dv);
+      count(NATS_BWD_STAGE_SOFTMAX, 2);
+      if ((e2 = mark(ev_stop, NATS_BWD_STAGE_SOFTMAX)) != cudaSuccess) return e2;
+      if ((e2 = mark(ev_start, NATS_BWD_STAGE_GDN)) != cudaSuccess) return e2;
       constexpr int smem = GdnBwd<D>::kBytes;
       static const cudaError_t attr =
           cudaFuncSetAttribute(gdn_bwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

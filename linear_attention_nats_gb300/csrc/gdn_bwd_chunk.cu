@@ -1164,11 +1164,7 @@ __global__ void __launch_bounds__(256) gdn_bwd_cc_kernel(
 }
 
 template <int D>
-cudaError_t run(const Problem& p, const void* q, const void* k, const void* v, const float* g, const float* beta,
-                const uint8_t* sel, const float* dO, const GdnBwdScratch& w, float* dq, float* dk, float* dv,
-                float* dg, float* dbeta, cudaStream_t st, int32_t* launches) {
-  const long long chunks = p.BH * p.N;
-  cudaError_t e;
+cudaError_t set_attributes() {
   static const cudaError_t attr = [] {
     cudaError_t r = cudaFuncSetAttribute(gdn_bwd_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          PrepSm<D>::kBytes);
@@ -1183,23 +1179,37 @@ cudaError_t run(const Problem& p, const void* q, const void* k, const void* v, c
       r = cudaFuncSetAttribute(gdn_bwd_cc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, CcSm<D>::kBytes);
     return r;
   }();
-  if (attr != cudaSuccess) return attr;
-  const bf16* qb = (const bf16*)q;
-  const bf16* kb = (const bf16*)k;
-  const bf16* vb = (const bf16*)v;
-  gdn_bwd_prep_kernel<D><<<(unsigned)chunks, 256, PrepSm<D>::kBytes, st>>>(
-      qb, kb, g, beta, p.L, p.N, p.scale, w.G, w.Li, w.P, (half*)w.W16, (half*)w.Qe16, (half*)w.Kt16, w.sc);
+  return attr;
+}
+
+template <int D>
+cudaError_t run_factors(const Problem& p, const void* q, const void* k, const float* g, const float* beta,
+                        const uint8_t* sel, const float* dO, const GdnBwdScratch& w, cudaStream_t st) {
+  cudaError_t e = set_attributes<D>();
+  if (e != cudaSuccess) return e;
+  gdn_bwd_prep_kernel<D><<<(unsigned)(p.BH * p.N), 256, PrepSm<D>::kBytes, st>>>(
+      (const bf16*)q, (const bf16*)k, g, beta, p.L, p.N, p.scale, w.G, w.Li, w.P, (half*)w.W16, (half*)w.Qe16,
+      (half*)w.Kt16, w.sc);
   gdn_bwd_scan_kernel<D><<<(unsigned)(p.BH * (D / RB)), 256, ScanSm<D>::kBytes, st>>>(
       (const half*)w.Kt16, (const half*)w.W16, (const half*)w.Qe16, w.sc, dO, w.G, sel, p.L, p.N, w.dSC);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t run_products(const Problem& p, const void* q, const void* k, const void* v, const float* beta,
+                         const uint8_t* sel, const float* dO, const GdnBwdScratch& w, float* dq, float* dk,
+                         float* dv, float* dbeta, cudaStream_t st) {
+  cudaError_t e = set_attributes<D>();
+  if (e != cudaSuccess) return e;
+  const long long chunks = p.BH * p.N;
+  const bf16* kb = (const bf16*)k;
   gdn_bwd_s0_kernel<D><<<(unsigned)chunks, 256, S0Sm<D>::kBytes, st>>>(
-      qb, kb, vb, dO, w.S0, w.Li, w.P, w.G, beta, p.L, p.N, p.scale, (half*)w.Vh, (half*)w.U, (half*)w.PtdO, w.isc,
-      dq, w.dG);
+      (const bf16*)q, kb, (const bf16*)v, dO, w.S0, w.Li, w.P, w.G, beta, p.L, p.N, p.scale, (half*)w.Vh,
+      (half*)w.U, (half*)w.PtdO, w.isc, dq, w.dG);
   gdn_bwd_ds_kernel<D><<<(unsigned)chunks, 256, DsSm<D>::kBytes, st>>>(
       kb, w.S0, w.dSC, (const half*)w.U, w.Li, (const half*)w.PtdO, (const half*)w.Vh, w.isc, w.G, beta, sel, p.L,
       p.N, (half*)w.Y, dv, dk, w.dG, dbeta);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (launches) *launches += 4;
-  return cudaSuccess;
+  return cudaGetLastError();
 }
 
 template <int D>
@@ -1213,13 +1223,20 @@ cudaError_t run_cc(const Problem& p, const void* q, const void* k, const float* 
 
 }  // namespace
 
-cudaError_t launch_gdn_bwd_chunk(const Problem& p, const void* q, const void* k, const void* v, const float* g,
-                                 const float* beta, const uint8_t* sel, const float* dO, const GdnBwdScratch& w,
-                                 float* dq, float* dk, float* dv, float* dg, float* dbeta, cudaStream_t st,
-                                 int32_t* launches) {
+cudaError_t launch_gdn_bwd_factors(const Problem& p, const void* q, const void* k, const float* g,
+                                   const float* beta, const uint8_t* sel, const float* dO, const GdnBwdScratch& w,
+                                   cudaStream_t st) {
   if (p.BH == 0 || p.N == 0) return cudaSuccess;
-  return p.d == 64 ? run<64>(p, q, k, v, g, beta, sel, dO, w, dq, dk, dv, dg, dbeta, st, launches)
-                   : run<128>(p, q, k, v, g, beta, sel, dO, w, dq, dk, dv, dg, dbeta, st, launches);
+  return p.d == 64 ? run_factors<64>(p, q, k, g, beta, sel, dO, w, st)
+                   : run_factors<128>(p, q, k, g, beta, sel, dO, w, st);
+}
+
+cudaError_t launch_gdn_bwd_products(const Problem& p, const void* q, const void* k, const void* v,
+                                    const float* beta, const uint8_t* sel, const float* dO, const GdnBwdScratch& w,
+                                    float* dq, float* dk, float* dv, float* dbeta, cudaStream_t st) {
+  if (p.BH == 0 || p.N == 0) return cudaSuccess;
+  return p.d == 64 ? run_products<64>(p, q, k, v, beta, sel, dO, w, dq, dk, dv, dbeta, st)
+                   : run_products<128>(p, q, k, v, beta, sel, dO, w, dq, dk, dv, dbeta, st);
 }
 
 cudaError_t launch_gdn_bwd_cc(const Problem& p, const void* q, const void* k, const float* beta, const float* dO,

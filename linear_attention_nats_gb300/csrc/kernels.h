@@ -70,7 +70,8 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
                               const float* o_l, const void* dout, float* dq, float* dk, float* dv, float* dg,
                               float* dbeta, float* dw_g, float* db_g, float* dnws, float* dnwl, void* ws,
                               cudaStream_t st, void* const* ev_start = nullptr, void* const* ev_stop = nullptr,
-                              int32_t* launches = nullptr);
+                              int32_t* launches = nullptr, cudaStream_t side = nullptr, cudaEvent_t fork = nullptr,
+                              cudaEvent_t join = nullptr);
 
 // The score layer's gradient under the straight-through surrogate
 // (score_bwd.cu): zeroes dw_s, db_s, then sums into them and adds the score
@@ -98,12 +99,17 @@ struct GdnBwdScratch {
   float* isc;   // [BH, N, 4] the scales of Vh, U, P^T dO, Y
   float* dG;    // [BH, L] gradient of G from the state products
 };
-// chunk factors, the reverse state-gradient scan and the state products
-// (four kernels; dq, dk, dv accumulate, dbeta is overwritten)
-cudaError_t launch_gdn_bwd_chunk(const Problem& p, const void* q, const void* k, const void* v, const float* g,
-                                 const float* beta, const uint8_t* sel, const float* dO, const GdnBwdScratch& w,
-                                 float* dq, float* dk, float* dv, float* dg, float* dbeta, cudaStream_t st,
-                                 int32_t* launches);
+// the adjoint's chunk factors and the reverse state-gradient scan (two
+// kernels; they read q, k, g, beta, the selection and dO, and write only the
+// scratch: G, Linv, P, W, Q_eff, K~, their scales and dS_C)
+cudaError_t launch_gdn_bwd_factors(const Problem& p, const void* q, const void* k, const float* g,
+                                   const float* beta, const uint8_t* sel, const float* dO, const GdnBwdScratch& w,
+                                   cudaStream_t st);
+// the state products (two kernels, after the factors, the reverse scan and
+// the chunk-start states S0; dq, dk, dv accumulate, dbeta is overwritten)
+cudaError_t launch_gdn_bwd_products(const Problem& p, const void* q, const void* k, const void* v,
+                                    const float* beta, const uint8_t* sel, const float* dO, const GdnBwdScratch& w,
+                                    float* dq, float* dk, float* dv, float* dbeta, cudaStream_t st);
 // the C x C products and dg (one kernel; dq, dk, dbeta accumulate, dg is overwritten)
 cudaError_t launch_gdn_bwd_cc(const Problem& p, const void* q, const void* k, const float* beta, const float* dO,
                               const GdnBwdScratch& w, float* dq, float* dk, float* dg, float* dbeta,
