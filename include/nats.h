@@ -31,9 +31,11 @@
  *     legacy default stream).  It allocates no device memory per call; what
  *     it does hold is listed here.  Per device, created on first use and
  *     kept until the process exits: one side stream and two events (the
- *     layer forward runs its two branches concurrently on that stream,
- *     forked from and joined back into `stream`; nats_hybrid_fwd_streams
- *     takes caller-owned ones instead, or runs both branches on `stream`).
+ *     layer forward runs its two branches concurrently on that stream, and
+ *     the bf16 backward its Gated DeltaNet state work beside the softmax
+ *     branch, forked from and joined back into `stream`;
+ *     nats_hybrid_fwd_streams and nats_hybrid_bwd_streams take caller-owned
+ *     ones instead, or run everything on `stream`).
  *     Per loaded library, on every GPU: the fixed scratch array of
  *     nats_hybrid_fwd_noalloc.
  *   - Arguments are validated on the host before anything is launched; a
@@ -43,10 +45,10 @@
  *     caller's next synchronising call.
  *   - No C++ exception crosses this interface.  Calls from several host
  *     threads are safe: the per-device side stream and events are used
- *     under a lock.  Because all forward calls of a device
- *     share the one side stream, the softmax halves of concurrent calls
- *     made on different caller streams run one after the other on it
- *     (correct, but not concurrent).  Calls that share a workspace must be
+ *     under a lock.  Because all forward and backward calls of a device
+ *     share the one side stream, the side halves of concurrent calls made
+ *     on different caller streams run one after the other on it (correct,
+ *     but not concurrent).  Calls that share a workspace must be
  *     ordered by the caller.
  *   - Supported shapes: chunk = 64, L % 64 == 0, dk == dv in {64, 128},
  *     B, H, L >= 0 (any zero extent makes the call a no-op that returns
@@ -393,7 +395,7 @@ nats_status nats_decode_step(const nats_dims* dims, int64_t t, const void* q, co
  * Search Linear (NAtS-L)", technical summary, "Kernmechanismen" items 3 and
  * 4).  Item 5 says the choice of attention type is learned end to end, but
  * the pages give no estimator for the argmax; W_s and b_s get no gradient
- * here.  The forward's selection and its two branch outputs are the saved
+ * here (nats_score_bwd adds an opt-in surrogate).  The forward's selection and its two branch outputs are the saved
  * activations: call nats_hybrid_fwd with sel_out, o_soft_out and o_lin_out.
  *
  * dims as for nats_hybrid_fwd.  q, k, v, dout [B, H, L, d] (dtype); g, beta
@@ -406,7 +408,12 @@ nats_status nats_decode_step(const nats_dims* dims, int64_t t, const void* q, co
  * holds the per-token branch gradients, the row log-sum-exp of the softmax
  * branch, the Gated DeltaNet chunk-start states and the states of one chunk
  * per head (fp32).  All pointers device; q, k, v, o_soft, o_lin, dout, dq,
- * dk, dv and the workspace 16-byte aligned; asynchronous on `stream`.
+ * dk, dv and the workspace 16-byte aligned; asynchronous on `stream`.  With
+ * bf16 inputs the Gated DeltaNet chunk-start states' recompute and the
+ * adjoint's chunk factors and reverse scan (which write only the workspace)
+ * run on the library's per-device side stream, forked from `stream` after
+ * the merge stage and joined back before the first kernel that writes dq,
+ * dk or dv after the softmax branch.
  * Errors before any launch: NATS_ERR_NULL, NATS_ERR_SHAPE /
  * NATS_ERR_UNSUPPORTED / NATS_ERR_DTYPE / NATS_ERR_VALUE (dims),
  * NATS_ERR_ALIGN, NATS_ERR_WORKSPACE; NATS_ERR_CUDA on a failed launch. */
@@ -422,9 +429,12 @@ nats_status nats_hybrid_bwd(const nats_dims* dims, const void* q, const void* k,
  * of nats_profile). */
 typedef enum {
   NATS_BWD_STAGE_MERGE = 0,   /* RMSNorm + gated merge backward: branch output gradients, dW_g, db_g, dnorm_w */
-  NATS_BWD_STAGE_SOFTMAX = 1, /* softmax branch: dq, then dk / dv (bf16: warp-level tensor MMAs) */
-  NATS_BWD_STAGE_GDN = 2,     /* Gated DeltaNet adjoint scan, reverse over chunks (fp32 CUDA cores) */
-  NATS_BWD_STAGE_COMBINE = 3, /* per-token dq, dk, dg, dbeta from the adjoint's partial sums */
+  NATS_BWD_STAGE_SOFTMAX = 1, /* softmax branch: dq, then dk / dv (bf16: tcgen05) */
+  NATS_BWD_STAGE_GDN = 2,     /* Gated DeltaNet: bf16, the chunk-start states' recompute (on the
+                                 side stream, from its fork) and the chunkwise adjoint's factors,
+                                 reverse scan and state products; fp32, the token-serial adjoint */
+  NATS_BWD_STAGE_COMBINE = 3, /* bf16: the adjoint's C x C products, dq, dk, dg, dbeta; fp32: the
+                                 per-token sums of the adjoint's state halves */
   NATS_BWD_NUM_STAGES = 4
 } nats_bwd_stage;
 
@@ -438,6 +448,21 @@ nats_status nats_hybrid_bwd_profiled(const nats_dims* dims, const void* q, const
                                      float* dk, float* dv, float* dg, float* dbeta, float* dw_g, float* db_g,
                                      float* dnorm_w_soft, float* dnorm_w_lin, void* workspace,
                                      size_t workspace_bytes, nats_stream_t stream, nats_profile* prof);
+
+/* nats_hybrid_bwd_profiled with caller-owned concurrency, as
+ * nats_hybrid_fwd_streams: `streams` (or NULL: the library's per-device set)
+ * gives the second stream and the fork / join events of the bf16 backward;
+ * side NULL or equal to `stream` runs every kernel in order on `stream`.
+ * Same arguments, errors and results; NATS_ERR_NULL when streams->side is a
+ * stream other than `stream` and fork or join is NULL. */
+nats_status nats_hybrid_bwd_streams(const nats_dims* dims, const void* q, const void* k, const void* v,
+                                    const float* g, const float* beta, const float* w_g, const float* b_g,
+                                    const float* norm_w_soft, const float* norm_w_lin, const uint8_t* sel,
+                                    const float* o_soft, const float* o_lin, const void* dout, float* dq,
+                                    float* dk, float* dv, float* dg, float* dbeta, float* dw_g, float* db_g,
+                                    float* dnorm_w_soft, float* dnorm_w_lin, void* workspace,
+                                    size_t workspace_bytes, nats_stream_t stream, const nats_streams* streams,
+                                    nats_profile* prof);
 
 /* The score layer's gradient, opt-in ("Kernmechanismen" item 5: the score
  * layer is trained end to end; the pages name no estimator, and

@@ -79,6 +79,18 @@ def select(q, k, w_s, b_s=None, *, scores: bool = False, stream=None):
     return (sel, sc) if scores else sel
 
 
+def _streams_of(side_stream):
+    """nats_streams for a torch.cuda.Stream (fork / join events made here) or
+    "serial" (everything in order on the call's stream)."""
+    streams = _native.Streams()
+    if side_stream != "serial":
+        ev = [torch.cuda.Event(), torch.cuda.Event()]
+        for e in ev:  # materialise the event handles
+            e.record(side_stream)
+        streams.side, streams.fork, streams.join = side_stream.cuda_stream, ev[0].cuda_event, ev[1].cuda_event
+    return streams
+
+
 def hybrid_fwd(q, k, v, g, beta, w_s, b_s, w_g, b_g=None, *, norm_w_soft=None, norm_w_lin=None,
                sel_in=None, scale: float = 0.0, eps: float = 1e-6, out=None, workspace=None,
                return_sel: bool = False, return_state: bool = False,
@@ -131,12 +143,7 @@ def hybrid_fwd(q, k, v, g, beta, w_s, b_s, w_g, b_g=None, *, norm_w_soft=None, n
             _p(norm_w_soft), _p(norm_w_lin), _p(sel_in), _p(out), _p(sel), _p(state), _p(o_soft),
             _p(o_lin), _p(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream))
     if side_stream is not None:
-        streams = _native.Streams()
-        if side_stream != "serial":
-            ev = [torch.cuda.Event(), torch.cuda.Event()]
-            for e in ev:  # materialise the event handles
-                e.record(side_stream)
-            streams.side, streams.fork, streams.join = side_stream.cuda_stream, ev[0].cuda_event, ev[1].cuda_event
+        streams = _streams_of(side_stream)
         prof = ctypes.byref(profile) if profile is not None else None
         check(_native.lib.nats_hybrid_fwd_streams(*args, ctypes.byref(streams), prof), "nats_hybrid_fwd_streams")
     elif profile is None:
@@ -201,9 +208,14 @@ def hybrid_fwd_x(x, w_qkv, w_ab, w_s, b_s, w_g, b_g=None, *, heads: int, b_a=Non
 
 def hybrid_bwd(q, k, v, g, beta, w_g, b_g, sel, o_soft, o_lin, dout, *, norm_w_soft=None, norm_w_lin=None,
                scale: float = 0.0, eps: float = 1e-6, weight_grads: bool = True, workspace=None, stream=None,
-               profile=None):
-    """Backward pass of the layer at the forward's selection (nats_hybrid_bwd;
-    nats_hybrid_bwd_profiled when `profile`, a _native.Profile, is given).
+               profile=None, side_stream=None):
+    """Backward pass of the layer at the forward's selection
+    (nats_hybrid_bwd_streams; `profile`, a _native.Profile, or None).
+
+    side_stream: a torch.cuda.Stream for the Gated DeltaNet state work of a
+    bf16 layer (fork / join events are made here), or "serial" for every
+    kernel in order on `stream`; None uses the library's per-device side
+    stream.
 
     sel, o_soft, o_lin: the forward's selection and branch outputs
     (hybrid_fwd(..., return_sel=True, return_branches=True)); dout like q.
@@ -238,11 +250,13 @@ def hybrid_bwd(q, k, v, g, beta, w_g, b_g, sel, o_soft, o_lin, dout, *, norm_w_s
     if weight_grads:
         res.update(dw_g=torch.empty((H, d), **f32), db_g=torch.empty((H,), **f32),
                    dnorm_w_soft=torch.empty((d,), **f32), dnorm_w_lin=torch.empty((d,), **f32))
-    check(_native.lib.nats_hybrid_bwd_profiled(
+    streams = _streams_of(side_stream) if side_stream is not None else None
+    check(_native.lib.nats_hybrid_bwd_streams(
         ctypes.byref(dm), _p(q), _p(k), _p(v), _p(g), _p(beta), _p(w_g), _p(b_g), _p(norm_w_soft),
         _p(norm_w_lin), _p(sel), _p(o_soft), _p(o_lin), _p(dout), _p(res["dq"]), _p(res["dk"]), _p(res["dv"]),
         _p(res["dg"]), _p(res["dbeta"]), _p(res.get("dw_g")), _p(res.get("db_g")), _p(res.get("dnorm_w_soft")),
         _p(res.get("dnorm_w_lin")), _p(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream),
+        ctypes.byref(streams) if streams is not None else None,
         ctypes.byref(profile) if profile is not None else None), "nats_hybrid_bwd")
     return res
 

@@ -29,7 +29,8 @@ EXPORTS = ("nats_status_string", "nats_last_cuda_error", "nats_workspace_size", 
            "nats_x_workspace_size", "nats_x_workspace_check",
            "nats_hybrid_fwd_x_profiled",
            "nats_hybrid_fwd_x", "nats_debug_fail_stage", "nats_debug_bounded_wait", "nats_decode_step",
-           "nats_bwd_workspace_size", "nats_hybrid_bwd", "nats_hybrid_bwd_profiled", "nats_score_bwd",
+           "nats_bwd_workspace_size", "nats_hybrid_bwd", "nats_hybrid_bwd_profiled", "nats_hybrid_bwd_streams",
+           "nats_score_bwd",
            "nats_nha_workspace_size", "nats_nha_fwd",
            "nats_nha_workspace_check", "nats_nha_fwd_profiled")
 
@@ -135,6 +136,9 @@ def _load() -> ctypes.CDLL:
     lib.nats_hybrid_bwd_profiled.argtypes = [ctypes.POINTER(Dims)] + [P] * 23 + [ctypes.c_size_t, P,
                                                                                ctypes.POINTER(Profile)]
     lib.nats_hybrid_bwd_profiled.restype = ctypes.c_int
+    lib.nats_hybrid_bwd_streams.argtypes = [ctypes.POINTER(Dims)] + [P] * 23 + [
+        ctypes.c_size_t, P, ctypes.POINTER(Streams), ctypes.POINTER(Profile)]
+    lib.nats_hybrid_bwd_streams.restype = ctypes.c_int
     lib.nats_score_bwd.argtypes = [ctypes.POINTER(Dims)] + [P] * 11 + [P]
     lib.nats_score_bwd.restype = ctypes.c_int
     lib.nats_nha_workspace_size.argtypes = [ctypes.POINTER(NhaDims)]

@@ -389,6 +389,19 @@ nats_status nats_hybrid_bwd_profiled(const nats_dims* dims, const void* q, const
                                      float* dk, float* dv, float* dg, float* dbeta, float* dw_g, float* db_g,
                                      float* dnorm_w_soft, float* dnorm_w_lin, void* workspace,
                                      size_t workspace_bytes, nats_stream_t stream, nats_profile* prof) {
+  return nats_hybrid_bwd_streams(dims, q, k, v, g, beta, w_g, b_g, norm_w_soft, norm_w_lin, sel, o_soft, o_lin,
+                                 dout, dq, dk, dv, dg, dbeta, dw_g, db_g, dnorm_w_soft, dnorm_w_lin, workspace,
+                                 workspace_bytes, stream, nullptr, prof);
+}
+
+nats_status nats_hybrid_bwd_streams(const nats_dims* dims, const void* q, const void* k, const void* v,
+                                    const float* g, const float* beta, const float* w_g, const float* b_g,
+                                    const float* norm_w_soft, const float* norm_w_lin, const uint8_t* sel,
+                                    const float* o_soft, const float* o_lin, const void* dout, float* dq,
+                                    float* dk, float* dv, float* dg, float* dbeta, float* dw_g, float* db_g,
+                                    float* dnorm_w_soft, float* dnorm_w_lin, void* workspace,
+                                    size_t workspace_bytes, nats_stream_t stream, const nats_streams* streams,
+                                    nats_profile* prof) {
   if (prof) {
     prof->launches = 0;
     for (int i = 0; i < NATS_NUM_STAGES; ++i) prof->stage_launches[i] = 0;
@@ -403,17 +416,32 @@ nats_status nats_hybrid_bwd_profiled(const nats_dims* dims, const void* q, const
   const void* ptrs[] = {q, k, v, o_soft, o_lin, dout, dq, dk, dv, workspace};
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return NATS_ERR_ALIGN;
+  // caller-owned concurrency: a second stream other than `stream` needs both events
+  const bool own_side = streams && streams->side && streams->side != stream;
+  if (own_side && (!streams->fork || !streams->join)) return NATS_ERR_NULL;
   if (workspace_bytes < bwd_workspace_bytes(p, dims->dtype)) return NATS_ERR_WORKSPACE;
-  // bf16 layers: the adjoint's chunk factors and reverse scan run on the
-  // per-device side stream (in order on `stream` if it could not be made)
-  Side* sd = dims->dtype == NATS_BF16 ? side_of_current_device() : nullptr;
+  // bf16 layers: the Gated DeltaNet state work runs on a second stream (the
+  // caller's, or the library's per-device one; in order on `stream` if
+  // neither is given or the library's could not be made)
+  cudaStream_t ss = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
   std::unique_lock<std::mutex> lk;
-  if (sd) lk = std::unique_lock<std::mutex>(sd->mu);
+  if (own_side) {
+    ss = (cudaStream_t)streams->side;
+    fork = (cudaEvent_t)streams->fork;
+    join = (cudaEvent_t)streams->join;
+  } else if (!streams && dims->dtype == NATS_BF16) {
+    if (Side* sd = side_of_current_device()) {
+      lk = std::unique_lock<std::mutex>(sd->mu);
+      ss = sd->s;
+      fork = sd->fork;
+      join = sd->join;
+    }
+  }
   const nats_status r = cuda_status(launch_hybrid_bwd(
       p, dims->dtype, q, k, v, g, beta, w_g, b_g, norm_w_soft, norm_w_lin, sel, o_soft, o_lin, dout, dq, dk, dv, dg,
       dbeta, dw_g, db_g, dnorm_w_soft, dnorm_w_lin, workspace, (cudaStream_t)stream, prof ? prof->start : nullptr,
-      prof ? prof->stop : nullptr, prof ? prof->stage_launches : nullptr, sd ? sd->s : nullptr,
-      sd ? sd->fork : nullptr, sd ? sd->join : nullptr));
+      prof ? prof->stop : nullptr, prof ? prof->stage_launches : nullptr, ss, fork, join));
   if (prof)
     for (int i = 0; i < NATS_BWD_NUM_STAGES; ++i) prof->launches += prof->stage_launches[i];
   return r;

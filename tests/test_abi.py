@@ -210,6 +210,30 @@ def test_backward_validation(nat):
     assert nat.lib.nats_bwd_workspace_size(ctypes.byref(nat.dims(1, 2, 100, 64))) == 0
 
 
+def test_backward_streams_validation(nat):
+    # nats_hybrid_bwd_streams: a second stream other than `stream` needs both
+    # events (checked after the shape and pointer checks, before the workspace)
+    dm = nat.dims(1, 2, 128, 64)
+    need = nat.lib.nats_bwd_workspace_size(ctypes.byref(dm))
+    fake = ctypes.c_void_p(256)
+    args = [fake] * 23
+
+    def call(streams, d=dm, a=args, ws_bytes=1 << 40):
+        return nat.lib.nats_hybrid_bwd_streams(ctypes.byref(d), *a, ctypes.c_size_t(ws_bytes), None,
+                                               ctypes.byref(streams) if streams is not None else None, None)
+
+    side = ctypes.c_void_p(0x7000).value
+    for fork, join in ((None, None), (256, None), (None, 256)):
+        assert call(nat.Streams(side, fork, join)) == 1                      # NATS_ERR_NULL
+    assert call(nat.Streams(side, None, None), d=nat.dims(1, 2, 100, 64)) == 2  # shapes first
+    assert call(nat.Streams(side, None, None), a=[None] + args[1:]) == 1      # q NULL
+    # no second stream (or the caller's own): events not needed, the workspace check comes next
+    for st in (nat.Streams(None, None, None), None):
+        assert call(st, ws_bytes=need - 1) == 5
+    assert call(nat.Streams(side, 256, 256), ws_bytes=need - 1) == 5
+    assert call(nat.Streams(side, None, None), d=nat.dims(0, 2, 128, 64)) == 0  # nothing to do
+
+
 def test_debug_hook_validation(nat):
     # the bounded-wait hook checks its arguments before any launch
     assert nat.lib.nats_debug_bounded_wait(None, 1000, None) == 1           # NATS_ERR_NULL

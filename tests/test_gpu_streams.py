@@ -48,3 +48,31 @@ def test_side_stream_modes_agree(name):
         for n in ("out", "sel", "state", "o_soft", "o_lin"):
             assert torch.equal(got[n], ref[n]), (tag, n)
     assert prof.launches == 5  # chunk factors, compaction, scan, softmax, merge
+
+
+def test_backward_side_stream_modes_agree():
+    # nats_hybrid_bwd_streams: the library's side stream, a caller's second
+    # stream and every kernel in order on one stream give the same gradients
+    # (the per-token ones up to the order of their atomic sums)
+    import linear_attention_nats_gb300 as nats
+    from linear_attention_nats_gb300 import _native
+
+    inp = gen.config_inputs("small")
+    t = to_device(inp)
+    fwd = nats.hybrid_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_s"], t["b_s"], t["w_g"], t["b_g"],
+                          return_sel=True, return_branches=True)
+    dout = torch.randn(t["q"].shape, generator=torch.Generator().manual_seed(5)).to(t["q"].dtype).cuda()
+    args = (t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_g"], t["b_g"], fwd["sel"], fwd["o_soft"],
+            fwd["o_lin"], dout)
+    ref = nats.hybrid_bwd(*args)
+    side = torch.cuda.Stream()
+    prof = _native.Profile()
+    runs = {"caller side stream": nats.hybrid_bwd(*args, side_stream=side),
+            "one stream": nats.hybrid_bwd(*args, side_stream="serial"),
+            "caller side stream, profiled": nats.hybrid_bwd(*args, side_stream=side, profile=prof)}
+    torch.cuda.synchronize()
+    for tag, got in runs.items():
+        for n, x in ref.items():
+            tol = float(x.abs().max()) * (1e-6 if n in ("dq", "dk", "dv", "dg", "dbeta") else 1e-5)
+            assert torch.allclose(got[n], x, rtol=1e-5, atol=tol), (tag, n)
+    assert prof.launches == 12
