@@ -81,14 +81,16 @@ def select(q, k, w_s, b_s=None, *, scores: bool = False, stream=None):
 
 def _streams_of(side_stream):
     """nats_streams for a torch.cuda.Stream (fork / join events made here) or
-    "serial" (everything in order on the call's stream)."""
+    "serial" (everything in order on the call's stream), and the events,
+    which the caller keeps alive until the call has been enqueued."""
     streams = _native.Streams()
+    ev = []
     if side_stream != "serial":
         ev = [torch.cuda.Event(), torch.cuda.Event()]
         for e in ev:  # materialise the event handles
             e.record(side_stream)
         streams.side, streams.fork, streams.join = side_stream.cuda_stream, ev[0].cuda_event, ev[1].cuda_event
-    return streams
+    return streams, ev
 
 
 def hybrid_fwd(q, k, v, g, beta, w_s, b_s, w_g, b_g=None, *, norm_w_soft=None, norm_w_lin=None,
@@ -143,7 +145,7 @@ def hybrid_fwd(q, k, v, g, beta, w_s, b_s, w_g, b_g=None, *, norm_w_soft=None, n
             _p(norm_w_soft), _p(norm_w_lin), _p(sel_in), _p(out), _p(sel), _p(state), _p(o_soft),
             _p(o_lin), _p(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream))
     if side_stream is not None:
-        streams = _streams_of(side_stream)
+        streams, _events = _streams_of(side_stream)
         prof = ctypes.byref(profile) if profile is not None else None
         check(_native.lib.nats_hybrid_fwd_streams(*args, ctypes.byref(streams), prof), "nats_hybrid_fwd_streams")
     elif profile is None:
@@ -250,7 +252,7 @@ def hybrid_bwd(q, k, v, g, beta, w_g, b_g, sel, o_soft, o_lin, dout, *, norm_w_s
     if weight_grads:
         res.update(dw_g=torch.empty((H, d), **f32), db_g=torch.empty((H,), **f32),
                    dnorm_w_soft=torch.empty((d,), **f32), dnorm_w_lin=torch.empty((d,), **f32))
-    streams = _streams_of(side_stream) if side_stream is not None else None
+    streams, _events = _streams_of(side_stream) if side_stream is not None else (None, [])
     check(_native.lib.nats_hybrid_bwd_streams(
         ctypes.byref(dm), _p(q), _p(k), _p(v), _p(g), _p(beta), _p(w_g), _p(b_g), _p(norm_w_soft),
         _p(norm_w_lin), _p(sel), _p(o_soft), _p(o_lin), _p(dout), _p(res["dq"]), _p(res["dk"]), _p(res["dv"]),

@@ -821,8 +821,9 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
                                   lay.ferr, ss, lay.cw.S0);
         // the adjoint's chunk factors and reverse scan
         if (e3 == cudaSuccess) e3 = launch_gdn_bwd_factors(p, q, k, g, beta, sel, d_ol, lay.cw, ss);
-        if (e3 == cudaSuccess) count(NATS_BWD_STAGE_GDN, 4);
-        return e3;
+        if (e3 != cudaSuccess) return e3;
+        count(NATS_BWD_STAGE_GDN, 4);
+        return mark_on(ev_stop, NATS_BWD_STAGE_GDN, ss);
       };
       if (two) {
         if ((e2 = cudaEventRecord(fork, st)) != cudaSuccess || (e2 = cudaStreamWaitEvent(ss, fork, 0)) != cudaSuccess ||
@@ -833,12 +834,11 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
       }
       if (two && ((e2 = cudaEventRecord(join, ss)) != cudaSuccess || (e2 = cudaStreamWaitEvent(st, join, 0)) != cudaSuccess))
         return e2;
-      if ((e2 = launch_gdn_bwd_products(p, q, k, v, beta, sel, d_ol, lay.cw, dq, dk, dv, dbeta, st)) != cudaSuccess)
-        return e2;
-      count(NATS_BWD_STAGE_GDN, 2);
-      if ((e2 = mark(ev_stop, NATS_BWD_STAGE_GDN)) != cudaSuccess) return e2;
+      // every per-chunk product of the adjoint: dq, dk, dv, dg, dbeta
       if ((e2 = mark(ev_start, NATS_BWD_STAGE_COMBINE)) != cudaSuccess) return e2;
-      if ((e2 = launch_gdn_bwd_cc(p, q, k, beta, d_ol, lay.cw, dq, dk, dg, dbeta, st)) != cudaSuccess) return e2;
+      if ((e2 = launch_gdn_bwd_products(p, q, k, v, g, beta, sel, d_ol, lay.cw, dq, dk, dv, dg, dbeta, st)) !=
+          cudaSuccess)
+        return e2;
       count(NATS_BWD_STAGE_COMBINE, 1);
     } else {
       if ((e2 = mark(ev_start, NATS_BWD_STAGE_SOFTMAX)) != cudaSuccess) return e2;

@@ -219,17 +219,35 @@ __device__ __forceinline__ float pow2_scale(float m) {
   return __int_as_float((127 + 14 - e) << 23);
 }
 
-// The scale of a tile from every thread's partial max |x| (a block-wide
-// collective; red: 8 floats of shared memory).
-__device__ __forceinline__ float block_scale(float m, float* red) {
-  m = warp_max(m);
-  __syncthreads();  // red is free again
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-  __syncthreads();
-  float r = red[0];
+// The scales of NS tiles from every thread's partial maxima m[u] of |x| (a
+// block-wide collective over NTH threads; red: NS x NTH / 32 floats of
+// shared memory).
+template <int NS, int NTH>
+__device__ __forceinline__ void block_scalesN(float (&m)[NS], float* red, float (&s)[NS]) {
+  constexpr int NW = NTH / 32;
 #pragma unroll
-  for (int w = 1; w < 8; ++w) r = fmaxf(r, red[w]);
-  return pow2_scale(r);
+  for (int u = 0; u < NS; ++u) m[u] = warp_max(m[u]);
+  __syncthreads();  // red is free again
+  if ((threadIdx.x & 31) == 0)
+#pragma unroll
+    for (int u = 0; u < NS; ++u) red[u * NW + (threadIdx.x >> 5)] = m[u];
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < NS; ++u) {
+    float r = red[u * NW];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) r = fmaxf(r, red[u * NW + w]);
+    s[u] = pow2_scale(r);
+  }
+}
+
+// The scale of a tile from every thread's partial max |x| (a block-wide
+// collective; red: NTH / 32 floats of shared memory).
+template <int NTH = 256>
+__device__ __forceinline__ float block_scale(float m, float* red) {
+  float mm[1] = {m}, s[1];
+  block_scalesN<1, NTH>(mm, red, s);
+  return s[0];
 }
 
 __device__ __forceinline__ float max4(float4 v) {
@@ -242,15 +260,15 @@ __device__ __forceinline__ uint2 half4(float4 v, float s) {
 
 // fp32 ROWS x COLS (row stride src_ld; global or shared) -> scaled fp16 tile;
 // returns the scale.  f(r, c, v) may rewrite each value first.
-template <int ROWS, int COLS, class F>
+template <int ROWS, int COLS, int NTH = 256, class F>
 __device__ __forceinline__ float tile_h(const float* src, int src_ld, half* dst, float* red, F f) {
-  constexpr int V = ROWS * COLS / 4 / 256;
-  static_assert(V >= 1 && ROWS * COLS % 1024 == 0, "tile");
+  constexpr int V = ROWS * COLS / 4 / NTH;
+  static_assert(V >= 1 && ROWS * COLS % (4 * NTH) == 0, "tile");
   float4 v[V];
   float m = 0.f;
 #pragma unroll
   for (int i = 0; i < V; ++i) {
-    const int x = threadIdx.x + 256 * i, r = x / (COLS / 4), c = 4 * (x % (COLS / 4));
+    const int x = threadIdx.x + NTH * i, r = x / (COLS / 4), c = 4 * (x % (COLS / 4));
     v[i] = *(const float4*)(src + (size_t)r * src_ld + c);
     v[i].x = f(r, c, v[i].x);
     v[i].y = f(r, c + 1, v[i].y);
@@ -258,32 +276,32 @@ __device__ __forceinline__ float tile_h(const float* src, int src_ld, half* dst,
     v[i].w = f(r, c + 3, v[i].w);
     m = fmaxf(m, max4(v[i]));
   }
-  const float s = block_scale(m, red);
+  const float s = block_scale<NTH>(m, red);
 #pragma unroll
   for (int i = 0; i < V; ++i) {
-    const int x = threadIdx.x + 256 * i, r = x / (COLS / 4), c = 4 * (x % (COLS / 4));
+    const int x = threadIdx.x + NTH * i, r = x / (COLS / 4), c = 4 * (x % (COLS / 4));
     *(uint2*)(dst + r * H<COLS>::ld + c) = half4(v[i], s);
   }
   return s;
 }
-template <int ROWS, int COLS>
+template <int ROWS, int COLS, int NTH = 256>
 __device__ __forceinline__ float tile_h(const float* src, int src_ld, half* dst, float* red) {
-  return tile_h<ROWS, COLS>(src, src_ld, dst, red, [](int, int, float x) { return x; });
+  return tile_h<ROWS, COLS, NTH>(src, src_ld, dst, red, [](int, int, float x) { return x; });
 }
 
 // A tile held in registers between its loads and its scaled store, so that
 // the loads of several tiles are in flight together and their scales come
 // from one block-wide reduction (block_scales2).
-template <int D>
+template <int D, int NTH = 256>
 struct BF16Tile {  // bf16 C x D (row stride D) -> scaled fp16 tile
-  static constexpr int V = C * D / 8 / 256;
+  static constexpr int V = C * D / 8 / NTH;
   uint4 v[V];
   float m;
   __device__ __forceinline__ void load(const bf16* src) {
     m = 0.f;
 #pragma unroll
     for (int i = 0; i < V; ++i) {
-      const int x = threadIdx.x + 256 * i, r = x / (D / 8), c = 8 * (x % (D / 8));
+      const int x = threadIdx.x + NTH * i, r = x / (D / 8), c = 8 * (x % (D / 8));
       v[i] = *(const uint4*)(src + (size_t)r * D + c);
     }
 #pragma unroll
@@ -299,7 +317,7 @@ struct BF16Tile {  // bf16 C x D (row stride D) -> scaled fp16 tile
   __device__ __forceinline__ void store(half* dst, float s) const {
 #pragma unroll
     for (int i = 0; i < V; ++i) {
-      const int x = threadIdx.x + 256 * i, r = x / (D / 8), c = 8 * (x % (D / 8));
+      const int x = threadIdx.x + NTH * i, r = x / (D / 8), c = 8 * (x % (D / 8));
       const __nv_bfloat162* h2 = (const __nv_bfloat162*)&v[i];
       uint4 o;
       uint32_t* o32 = (uint32_t*)&o;
@@ -368,14 +386,14 @@ __device__ __forceinline__ float tile_h_bf(const bf16* src, half* dst, float* re
 
 // accumulators (rows m0.., columns n0..) -> scaled fp16 tile (a block-wide
 // collective: every thread calls it); returns the scale
-template <int NT, int COLS>
+template <int NT, int COLS, int NTH = 256>
 __device__ __forceinline__ float acc_h(const float (&acc)[NT][4], int m0, int n0, half* dst, float* red) {
   float m = 0.f;
 #pragma unroll
   for (int j = 0; j < NT; ++j)
 #pragma unroll
     for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(acc[j][e]));
-  const float s = block_scale(m, red);
+  const float s = block_scale<NTH>(m, red);
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
@@ -387,9 +405,9 @@ __device__ __forceinline__ float acc_h(const float (&acc)[NT][4], int m0, int n0
 }
 
 // fp16 C x D rows (global, row stride D) -> the padded tile, asynchronously
-template <int D>
+template <int D, int NTH = 256>
 __device__ __forceinline__ void copy_h(half* dst, const half* src) {
-  for (int x = threadIdx.x; x < C * D / 8; x += 256) {
+  for (int x = threadIdx.x; x < C * D / 8; x += NTH) {
     const int r = x / (D / 8), c8 = 8 * (x % (D / 8));
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst + r * H<D>::ld + c8)),
                  "l"(src + (size_t)r * D + c8)
@@ -1163,6 +1181,352 @@ __global__ void __launch_bounds__(256) gdn_bwd_cc_kernel(
   if (tid < C) dbeta[row0 + tid] += sdB[tid];
 }
 
+// ------------------------------------------ every per-chunk product, fused
+// One CTA of 16 warps per chunk holds all of the chunk's operand tiles in
+// shared memory (fp16, each at its own power-of-two scale) and takes every
+// product of the adjoint in turn, so that dq, dk and dv are each updated
+// once, dbeta and dg written once, and no per-chunk intermediate goes
+// through global memory.  A C x D output is split into 16-row strips
+// (warp w & 3) and column quarters (warp w >> 2); a C x C output likewise.
+template <int D>
+struct FusedSm {
+  static constexpr int offS = 0;                        // fp16 [D][D + 8]: S0 ([dk][dv])
+  static constexpr int offT = offS + H<D>::bytes(D);    // dS_C ([dk][dv])
+  static constexpr int offQ = offT + H<D>::bytes(D);    // fp16 [C][D + 8]: q
+  static constexpr int offK = offQ + H<D>::bytes(C);    // k
+  static constexpr int offV = offK + H<D>::bytes(C);    // v (bf16 as loaded), then Vh
+  static constexpr int offO = offV + H<D>::bytes(C);    // dO
+  static constexpr int offU = offO + H<D>::bytes(C);    // U
+  static constexpr int offD = offU + H<D>::bytes(C);    // dU, then Y
+  static constexpr int offL = offD + H<D>::bytes(C);    // fp16 [C][C + 8]: Linv
+  static constexpr int offLb = offL + H<C>::bytes(C);   // Linv diag(beta)
+  static constexpr int offP = offLb + H<C>::bytes(C);   // P, then dP . R
+  static constexpr int offA = offP + H<C>::bytes(C);    // A~
+  static constexpr int offVec = offA + H<C>::bytes(C);  // G, gamma, beta, dG, dbeta
+  static constexpr int offRed = offVec + 5 * C * 4;     // partial maxima; [126]: extra dG of the last token; [127]: <dS_C, S0>
+  static constexpr int kBytes = offRed + 128 * 4;
+};
+
+template <int D>
+__global__ void __launch_bounds__(512, 1) gdn_bwd_fused_kernel(
+    const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v, const float* __restrict__ dO,
+    const float* __restrict__ S0, const float* __restrict__ dSC, const float* __restrict__ Li,
+    const float* __restrict__ Pg, const float* __restrict__ Gb, const float* __restrict__ beta,
+    const uint8_t* __restrict__ sel, int L, int N, float scale, float* __restrict__ dq, float* __restrict__ dk,
+    float* __restrict__ dv, float* __restrict__ dg, float* __restrict__ dbeta) {
+  using S = FusedSm<D>;
+  constexpr int NTH = 512, NTD = D / 32, LD = H<D>::ld, LC = H<C>::ld;
+  extern __shared__ __align__(16) uint8_t sm[];
+  half* hS = (half*)(sm + S::offS);
+  half* hT = (half*)(sm + S::offT);
+  half* hQ = (half*)(sm + S::offQ);
+  half* hK = (half*)(sm + S::offK);
+  half* hV = (half*)(sm + S::offV);
+  half* hO = (half*)(sm + S::offO);
+  half* hU = (half*)(sm + S::offU);
+  half* hD = (half*)(sm + S::offD);
+  half* hL = (half*)(sm + S::offL);
+  half* hLb = (half*)(sm + S::offLb);
+  half* hP = (half*)(sm + S::offP);
+  half* hA = (half*)(sm + S::offA);
+  float* sG = (float*)(sm + S::offVec);
+  float* sGam = sG + C;
+  float* sB = sGam + C;
+  float* sdG = sB + C;
+  float* sdB = sdG + C;
+  float* red = (float*)(sm + S::offRed);
+  const long long chunk = blockIdx.x;
+  const int c = (int)(chunk % N);
+  const size_t row0 = (size_t)(chunk / N) * L + (size_t)c * C;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool committed = sel[chunk] != 0 && c < N - 1;
+  load_scalars(Gb, beta, row0, sG, sGam, sB);
+  if (tid < C) sdG[tid] = sdB[tid] = 0.f;
+  if (tid < 2) red[126 + tid] = 0.f;
+  copy_h<D, NTH>(hV, (const half*)(v + row0 * D));  // v (bf16) staged where Vh will be formed
+  // S0 and dS_C (a committed chunk's; zero otherwise), read in the same
+  // order so that <dS_C, S0> is taken in fp32 on the way
+  float ss, sd;
+  {
+    constexpr int V = D * D / 4 / NTH;
+    const float* s0 = S0 + (size_t)chunk * D * D;
+    const float* ds = dSC + (size_t)chunk * D * D;
+    float4 a[V], b[V];
+    float m[2] = {0.f, 0.f}, sc2[2], dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int x = tid + NTH * i, r = x / (D / 4), cc = 4 * (x % (D / 4));
+      a[i] = *(const float4*)(s0 + (size_t)r * D + cc);
+      m[0] = fmaxf(m[0], max4(a[i]));
+    }
+    if (committed) {
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const int x = tid + NTH * i, r = x / (D / 4), cc = 4 * (x % (D / 4));
+        b[i] = *(const float4*)(ds + (size_t)r * D + cc);
+        m[1] = fmaxf(m[1], max4(b[i]));
+        dot += a[i].x * b[i].x + a[i].y * b[i].y + a[i].z * b[i].z + a[i].w * b[i].w;
+      }
+    }
+    block_scalesN<2, NTH>(m, red, sc2);
+    ss = sc2[0];
+    sd = sc2[1];
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int x = tid + NTH * i, r = x / (D / 4), cc = 4 * (x % (D / 4));
+      *(uint2*)(hS + r * LD + cc) = half4(a[i], ss);
+      if (committed) *(uint2*)(hT + r * LD + cc) = half4(b[i], sd);
+    }
+    if (committed) {
+      dot = warp_sum(dot);
+      if (lane == 0) atomicAdd(red + 127, dot);
+    }
+  }
+  // q, k, dO, Linv (plain and with its columns scaled by beta) and P: every
+  // load in flight together, one reduction for the six scales
+  float sq, sk, so, sl, slb, sp;
+  {
+    constexpr int VO = C * D / 4 / NTH, VC = C * C / 4 / NTH;
+    BF16Tile<D, NTH> tq, tk;
+    tq.load(q + row0 * D);
+    tk.load(k + row0 * D);
+    float4 o[VO], l[VC], pp[VC];
+    float m[6] = {tq.m, tk.m, 0.f, 0.f, 0.f, 0.f}, s6[6];
+    const float* lsrc = Li + (size_t)chunk * C * C;
+    const float* psrc = Pg + (size_t)chunk * C * C;
+#pragma unroll
+    for (int i = 0; i < VO; ++i) {
+      const int x = tid + NTH * i, r = x / (D / 4), cc = 4 * (x % (D / 4));
+      o[i] = *(const float4*)(dO + (row0 + r) * D + cc);
+      m[2] = fmaxf(m[2], max4(o[i]));
+    }
+#pragma unroll
+    for (int i = 0; i < VC; ++i) {
+      const int x = tid + NTH * i, r = x / (C / 4), cc = 4 * (x % (C / 4));
+      l[i] = *(const float4*)(lsrc + r * C + cc);
+      pp[i] = *(const float4*)(psrc + r * C + cc);
+    }
+#pragma unroll
+    for (int i = 0; i < VC; ++i) {
+      const int x = tid + NTH * i, cc = 4 * (x % (C / 4));
+      m[3] = fmaxf(m[3], max4(l[i]));
+      const float4 lb = make_float4(l[i].x * sB[cc], l[i].y * sB[cc + 1], l[i].z * sB[cc + 2], l[i].w * sB[cc + 3]);
+      m[4] = fmaxf(m[4], max4(lb));
+      m[5] = fmaxf(m[5], max4(pp[i]));
+    }
+    block_scalesN<6, NTH>(m, red, s6);
+    sq = s6[0], sk = s6[1], so = s6[2], sl = s6[3], slb = s6[4], sp = s6[5];
+    tq.store(hQ, sq);
+    tk.store(hK, sk);
+#pragma unroll
+    for (int i = 0; i < VO; ++i) {
+      const int x = tid + NTH * i, r = x / (D / 4), cc = 4 * (x % (D / 4));
+      *(uint2*)(hO + r * LD + cc) = half4(o[i], so);
+    }
+#pragma unroll
+    for (int i = 0; i < VC; ++i) {
+      const int x = tid + NTH * i, r = x / (C / 4), cc = 4 * (x % (C / 4));
+      const float4 lb = make_float4(l[i].x * sB[cc], l[i].y * sB[cc + 1], l[i].z * sB[cc + 2], l[i].w * sB[cc + 3]);
+      *(uint2*)(hL + r * LC + cc) = half4(l[i], sl);
+      *(uint2*)(hLb + r * LC + cc) = half4(lb, slb);
+      *(uint2*)(hP + r * LC + cc) = half4(pp[i], sp);
+    }
+  }
+  copy_wait();
+  __syncthreads();
+  const int m0 = 16 * (warp & 3), nD = (warp >> 2) * (D / 4), nC = (warp >> 2) * (C / 4);
+  const float gC = sGam[C - 1];
+  float acc[NTD][4], acc2[NTD][4];
+  // Vh = V - diag(gamma) K S0^T
+  zero(acc);
+  hmm<NTD, D, false, true>(acc, m0, nD, hK, LD, hS, LD);
+  {
+    const float iks = 1.f / (sk * ss);
+    const bf16* vs = (const bf16*)hV;
+    each_mut(acc, m0, nD, [&](int i, int n, float val, int, int) {
+      return __bfloat162float(vs[i * LD + n]) - sGam[i] * val * iks;
+    });
+  }
+  const float svh = acc_h<NTD, D, NTH>(acc, m0, nD, hV, red);  // (every read of v precedes its barriers)
+  __syncthreads();
+  // U = Linv diag(beta) Vh
+  zero(acc);
+  hmm<NTD, C, false, true>(acc, m0, nD, hLb, LC, hV, LD);
+  {
+    const float iu = 1.f / (slb * svh);
+    each_mut(acc, m0, nD, [&](int, int, float val, int, int) { return val * iu; });
+  }
+  const float su = acc_h<NTD, D, NTH>(acc, m0, nD, hU, red);
+  __syncthreads();
+  // dU = P^T dO + K~ dS_C^T
+  zero(acc);
+  zero(acc2);
+  hmm<NTD, C, true, true>(acc, m0, nD, hP, LC, hO, LD);
+  if (committed) hmm<NTD, D, false, true>(acc2, m0, nD, hK, LD, hT, LD);
+  {
+    const float ipo = 1.f / (sp * so), ikd = 1.f / (sk * sd);
+    each_mut(acc, m0, nD, [&](int i, int, float val, int j, int e) {
+      return val * ipo + gC / sGam[i] * acc2[j][e] * ikd;
+    });
+  }
+  const float sdu = acc_h<NTD, D, NTH>(acc, m0, nD, hD, red);
+  // dP = lower(dO U^T), P = R . Q~ K^T (the chunk factor, fp32): dP . R
+  // replaces P; dG += row sums - column sums of dP . P
+  float spm;
+  {
+    float ou[2][4];
+    zero(ou);
+    hmm<2, D, false, false>(ou, m0, nC, hO, LD, hU, LD);
+    const float iou = 1.f / (so * su);
+    const float* pg = Pg + (size_t)chunk * C * C;
+    float rlo = 0.f, rhi = 0.f, col[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    each_mut(ou, m0, nC, [&](int i, int jj, float val, int j, int e) {
+      float pm = 0.f;
+      if (jj <= i) {
+        const float r = __expf(sG[i] - sG[jj]);
+        const float dP = val * iou;
+        const float x = dP * pg[i * C + jj];
+        if (e < 2) rlo += x; else rhi += x;
+        col[j][e & 1] -= x;
+        pm = dP * r;
+      }
+      return pm;
+    });
+    add_rows(rlo, rhi, m0, sdG);
+    add_cols<2>(col, nC, sdG);
+    spm = acc_h<2, C, NTH>(ou, m0, nC, hP, red);  // (every read of P precedes its barriers)
+  }
+  __syncthreads();
+  // dq += scale diag(gamma) dO S0 + scale (dP . R) K (one accumulator: the
+  // first product is brought to the second's scale before it is added);
+  // dG_i += gamma_i (dO S0)_i . q~_i
+  {
+    zero(acc);
+    hmm<NTD, D, false, false>(acc, m0, nD, hO, LD, hS, LD);
+    const float ios = scale / (so * ss), f2 = scale / (spm * sk), if2 = (spm * sk) / scale, iq = 1.f / sq;
+    float lo = 0.f, hi = 0.f;
+    each_mut(acc, m0, nD, [&](int i, int n, float val, int, int e) {
+      const float x = sGam[i] * val * ios;
+      const float dd = x * __half2float(hQ[i * LD + n]) * iq;
+      if (e < 2) lo += dd; else hi += dd;
+      return x * if2;
+    });
+    add_rows(lo, hi, m0, sdG);
+    hmm<NTD, C, false, true>(acc, m0, nD, hP, LC, hK, LD);
+    each_mut(acc, m0, nD, [&](int, int, float val, int, int) { return val * f2; });
+    acc_add_global<NTD, D>(acc, m0, nD, dq + row0 * D);
+  }
+  // Y = Linv^T dU (replaces dU); dv += diag(beta) Y; dbeta_i = Y_i . Vh_i
+  float sy;
+  {
+    zero(acc);
+    hmm<NTD, C, true, true>(acc, m0, nD, hL, LC, hD, LD);
+    const float iy = 1.f / (sl * sdu), ivh = 1.f / svh;
+    float lo = 0.f, hi = 0.f;
+    each_mut(acc, m0, nD, [&](int i, int n, float val, int, int e) {
+      const float y = val * iy;
+      const float dd = y * __half2float(hV[i * LD + n]) * ivh;
+      if (e < 2) lo += dd; else hi += dd;
+      return y;
+    });
+    add_rows(lo, hi, m0, sdB);
+    sy = acc_h<NTD, D, NTH>(acc, m0, nD, hD, red);  // (every read of dU precedes its barriers)
+    each_mut(acc, m0, nD, [&](int i, int, float y, int, int) { return sB[i] * y; });
+    acc_add_global<NTD, D>(acc, m0, nD, dv + row0 * D);
+  }
+  __syncthreads();
+  // dL = -strict_lower(Y U^T), A = R . K K^T: dA = diag(beta) dL, A~ = dA . R,
+  // dbeta_i += sum_j dL_ij A_ij, dG += row sums - column sums of dA . A
+  float sa;
+  {
+    float yu[2][4], kk[2][4];
+    zero(yu);
+    zero(kk);
+    hmm<2, D, false, false>(yu, m0, nC, hD, LD, hU, LD);
+    hmm<2, D, false, false>(kk, m0, nC, hK, LD, hK, LD);
+    const float iyu = 1.f / (sy * su), ikk = 1.f / (sk * sk);
+    float rlo = 0.f, rhi = 0.f, blo = 0.f, bhi = 0.f, col[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    each_mut(yu, m0, nC, [&](int i, int jj, float val, int j, int e) {
+      float at = 0.f;
+      if (jj < i) {
+        const float r = __expf(sG[i] - sG[jj]);
+        const float A = r * kk[j][e] * ikk;
+        const float dL = -val * iyu;
+        const float dA = sB[i] * dL;
+        const float x = dA * A;
+        if (e < 2) rlo += x, blo += dL * A; else rhi += x, bhi += dL * A;
+        col[j][e & 1] -= x;
+        at = dA * r;
+      }
+      return at;
+    });
+    add_rows(rlo, rhi, m0, sdG);
+    add_rows(blo, bhi, m0, sdB);
+    add_cols<2>(col, nC, sdG);
+    sa = acc_h<2, C, NTH>(yu, m0, nC, hA, red);
+  }
+  __syncthreads();
+  // dk += diag(gamma_C / gamma) U dS_C - diag(gamma beta) Y S0 + (dP . R)^T Q~
+  //       + (A~ + A~^T) K
+  {
+    float dkp[NTD][4];
+    zero(dkp);
+    const float ik = 1.f / sk;
+    if (committed) {  // dG_j -= (U dS_C)_j . K~_j; the last token gains their sum
+      hmm<NTD, D, false, false>(dkp, m0, nD, hU, LD, hT, LD);
+      const float iud = 1.f / (su * sd);
+      float lo = 0.f, hi = 0.f;
+      each_mut(dkp, m0, nD, [&](int i, int n, float val, int, int e) {
+        const float x = gC / sGam[i] * val * iud;
+        const float dd = x * ik * __half2float(hK[i * LD + n]);
+        if (e < 2) lo -= dd; else hi -= dd;
+        return x;
+      });
+      const float tot = warp_sum(-(lo + hi));
+      add_rows(lo, hi, m0, sdG);
+      if (lane == 0) atomicAdd(red + 126, tot);
+    }
+    {  // dG_i -= gamma_i beta_i (Y S0)_i . k_i
+      zero(acc);
+      hmm<NTD, D, false, false>(acc, m0, nD, hD, LD, hS, LD);
+      const float iys = 1.f / (sy * ss);
+      float lo = 0.f, hi = 0.f;
+      each(acc, m0, nD, [&](int i, int n, float val, int j, int e) {
+        const float x = sGam[i] * sB[i] * val * iys;
+        dkp[j][e] -= x;
+        const float dd = x * ik * __half2float(hK[i * LD + n]);
+        if (e < 2) lo -= dd; else hi -= dd;
+      });
+      add_rows(lo, hi, m0, sdG);
+    }
+    zero(acc);
+    zero(acc2);
+    hmm<NTD, C, true, true>(acc, m0, nD, hP, LC, hQ, LD);
+    hmm<NTD, C, false, true>(acc2, m0, nD, hA, LC, hK, LD);
+    hmm<NTD, C, true, true>(acc2, m0, nD, hA, LC, hK, LD);
+    const float f1 = scale / (spm * sq), fa = 1.f / (sa * sk);
+    each(acc, m0, nD, [&](int, int, float val, int j, int e) { dkp[j][e] += f1 * val + fa * acc2[j][e]; });
+    acc_add_global<NTD, D>(dkp, m0, nD, dk + row0 * D);
+  }
+  __syncthreads();
+  if (tid == 0) sdG[C - 1] += red[126] + gC * red[127];
+  __syncthreads();
+  if (warp == 0) {  // dg = reverse cumulative sum of dG over the chunk
+    const float a0 = sdG[2 * lane], a1 = sdG[2 * lane + 1];
+    float s = a0 + a1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_down_sync(0xffffffffu, s, o);
+      if (lane + o < 32) s += y;
+    }
+    // s = sum over lanes >= this one
+    const float after = s - a0 - a1;
+    dg[row0 + 2 * lane + 1] = a1 + after;
+    dg[row0 + 2 * lane] = a0 + a1 + after;
+  }
+  if (tid < C) dbeta[row0 + tid] = sdB[tid];
+}
+
 template <int D>
 cudaError_t set_attributes() {
   static const cudaError_t attr = [] {
@@ -1172,11 +1536,8 @@ cudaError_t set_attributes() {
       r = cudaFuncSetAttribute(gdn_bwd_scan_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                ScanSm<D>::kBytes);
     if (r == cudaSuccess)
-      r = cudaFuncSetAttribute(gdn_bwd_s0_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, S0Sm<D>::kBytes);
-    if (r == cudaSuccess)
-      r = cudaFuncSetAttribute(gdn_bwd_ds_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DsSm<D>::kBytes);
-    if (r == cudaSuccess)
-      r = cudaFuncSetAttribute(gdn_bwd_cc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, CcSm<D>::kBytes);
+      r = cudaFuncSetAttribute(gdn_bwd_fused_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               FusedSm<D>::kBytes);
     return r;
   }();
   return attr;
@@ -1196,28 +1557,14 @@ cudaError_t run_factors(const Problem& p, const void* q, const void* k, const fl
 }
 
 template <int D>
-cudaError_t run_products(const Problem& p, const void* q, const void* k, const void* v, const float* beta,
-                         const uint8_t* sel, const float* dO, const GdnBwdScratch& w, float* dq, float* dk,
-                         float* dv, float* dbeta, cudaStream_t st) {
+cudaError_t run_products(const Problem& p, const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const uint8_t* sel, const float* dO, const GdnBwdScratch& w, float* dq,
+                         float* dk, float* dv, float* dg, float* dbeta, cudaStream_t st) {
   cudaError_t e = set_attributes<D>();
   if (e != cudaSuccess) return e;
-  const long long chunks = p.BH * p.N;
-  const bf16* kb = (const bf16*)k;
-  gdn_bwd_s0_kernel<D><<<(unsigned)chunks, 256, S0Sm<D>::kBytes, st>>>(
-      (const bf16*)q, kb, (const bf16*)v, dO, w.S0, w.Li, w.P, w.G, beta, p.L, p.N, p.scale, (half*)w.Vh,
-      (half*)w.U, (half*)w.PtdO, w.isc, dq, w.dG);
-  gdn_bwd_ds_kernel<D><<<(unsigned)chunks, 256, DsSm<D>::kBytes, st>>>(
-      kb, w.S0, w.dSC, (const half*)w.U, w.Li, (const half*)w.PtdO, (const half*)w.Vh, w.isc, w.G, beta, sel, p.L,
-      p.N, (half*)w.Y, dv, dk, w.dG, dbeta);
-  return cudaGetLastError();
-}
-
-template <int D>
-cudaError_t run_cc(const Problem& p, const void* q, const void* k, const float* beta, const float* dO,
-                   const GdnBwdScratch& w, float* dq, float* dk, float* dg, float* dbeta, cudaStream_t st) {
-  gdn_bwd_cc_kernel<D><<<(unsigned)(p.BH * p.N), 256, CcSm<D>::kBytes, st>>>(
-      (const bf16*)q, (const bf16*)k, dO, (const half*)w.U, (const half*)w.Y, w.isc, w.G, beta, p.L, p.N, p.scale,
-      dq, dk, w.dG, dbeta, dg);
+  gdn_bwd_fused_kernel<D><<<(unsigned)(p.BH * p.N), 512, FusedSm<D>::kBytes, st>>>(
+      (const bf16*)q, (const bf16*)k, (const bf16*)v, dO, w.S0, w.dSC, w.Li, w.P, w.G, beta, sel, p.L, p.N, p.scale,
+      dq, dk, dv, dg, dbeta);
   return cudaGetLastError();
 }
 
@@ -1231,20 +1578,12 @@ cudaError_t launch_gdn_bwd_factors(const Problem& p, const void* q, const void* 
                    : run_factors<128>(p, q, k, g, beta, sel, dO, w, st);
 }
 
-cudaError_t launch_gdn_bwd_products(const Problem& p, const void* q, const void* k, const void* v,
+cudaError_t launch_gdn_bwd_products(const Problem& p, const void* q, const void* k, const void* v, const float* g,
                                     const float* beta, const uint8_t* sel, const float* dO, const GdnBwdScratch& w,
-                                    float* dq, float* dk, float* dv, float* dbeta, cudaStream_t st) {
+                                    float* dq, float* dk, float* dv, float* dg, float* dbeta, cudaStream_t st) {
   if (p.BH == 0 || p.N == 0) return cudaSuccess;
-  return p.d == 64 ? run_products<64>(p, q, k, v, beta, sel, dO, w, dq, dk, dv, dbeta, st)
-                   : run_products<128>(p, q, k, v, beta, sel, dO, w, dq, dk, dv, dbeta, st);
-}
-
-cudaError_t launch_gdn_bwd_cc(const Problem& p, const void* q, const void* k, const float* beta, const float* dO,
-                              const GdnBwdScratch& w, float* dq, float* dk, float* dg, float* dbeta,
-                              cudaStream_t st) {
-  if (p.BH == 0 || p.N == 0) return cudaSuccess;
-  return p.d == 64 ? run_cc<64>(p, q, k, beta, dO, w, dq, dk, dg, dbeta, st)
-                   : run_cc<128>(p, q, k, beta, dO, w, dq, dk, dg, dbeta, st);
+  return p.d == 64 ? run_products<64>(p, q, k, v, g, beta, sel, dO, w, dq, dk, dv, dg, dbeta, st)
+                   : run_products<128>(p, q, k, v, g, beta, sel, dO, w, dq, dk, dv, dg, dbeta, st);
 }
 
 }  // namespace nats

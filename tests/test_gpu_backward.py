@@ -122,19 +122,18 @@ def test_backward_profiled_stages():
     for n in GRADS[5:]:
         assert torch.allclose(plain[n], timed[n], rtol=1e-5, atol=1e-5 * float(plain[n].abs().max())), n
     # bf16: merge; the softmax-chunk lists, softmax dq, dk / dv (local and
-    # retained key tiles); the Gated DeltaNet stage (chunk
-    # factors and scan of the forward for the chunk-start states, the adjoint's
-    # chunk factors, reverse scan, S0 and dS_C products); the C x C products
-    assert list(prof.stage_launches)[:len(_native.BWD_STAGES)] == [1, 4, 6, 1]
-    assert prof.launches == 12
+    # retained key tiles); the Gated DeltaNet stage (chunk factors and scan of
+    # the forward for the chunk-start states, the adjoint's chunk factors and
+    # reverse scan); the adjoint's per-chunk products
+    assert list(prof.stage_launches)[:len(_native.BWD_STAGES)] == [1, 4, 4, 1]
+    assert prof.launches == 10
     ms = [a.elapsed_time(b) for a, b in ev]
     assert all(m > 0 for m in ms), ms
     # the softmax stage and the Gated DeltaNet stage both start after the
-    # merge; the adjoint's chunk factors and reverse scan may run beside the
-    # softmax stage on a second stream, so the Gated DeltaNet stage ends after
-    # the softmax stage, and the C x C stage starts after both
+    # merge and may run side by side on two streams; the per-chunk products
+    # start after both
     merge, soft, gdn, comb = ev
-    for a, b in ((merge[1], soft[0]), (merge[1], gdn[0]), (soft[1], gdn[1]), (gdn[1], comb[0])):
+    for a, b in ((merge[1], soft[0]), (merge[1], gdn[0]), (soft[1], comb[0]), (gdn[1], comb[0])):
         assert a.elapsed_time(b) >= 0
 
 
