@@ -725,12 +725,6 @@ static size_t bwd_layout(const Problem& p, int dtype, uint8_t* base, BwdLayout* 
     w.Qe16 = take(rows * p.d * 2);
     w.Kt16 = take(rows * p.d * 2);
     w.sc = (float*)take(chunks * 4 * 4);
-    w.Vh = take(rows * p.d * 2);
-    w.U = take(rows * p.d * 2);
-    w.PtdO = take(rows * p.d * 2);
-    w.Y = take(rows * p.d * 2);
-    w.isc = (float*)take(chunks * 4 * 4);
-    w.dG = (float*)take(rows * 4);
   }
   if (o) *o = l;
   return off;

@@ -30,20 +30,21 @@
 // Kernels (after the forward scan has written every chunk's S0; S0 and
 // dS_C are stored transposed, [dk][dv], so that both scans write them as
 // whole lines):
-//   gdn_bwd_prep_kernel  per chunk: G, Linv, P (fp32), W, Q_eff, K~ (fp16, scaled)
-//   gdn_bwd_scan_kernel  per (b, h, 64 state rows): the reverse scan, writing
-//                        dS_C of every committed chunk (fp32)
-//   gdn_bwd_s0_kernel    per chunk: Vh, U, P^T dO; dq += diag(gamma) dO S0
-//   gdn_bwd_ds_kernel    per chunk: dU, Y, dv; the U dS_C and dVh S0 terms
-//   gdn_bwd_cc_kernel    per chunk: the C x C products, dq, dk, dbeta, dg
+//   gdn_bwd_prep_kernel   per chunk: G, Linv, P (fp32), W, Q_eff, K~ (fp16, scaled)
+//   gdn_bwd_scan_kernel   per (b, h, 64 state rows): the reverse scan, writing
+//                         dS_C of every committed chunk (fp32)
+//   gdn_bwd_fused_kernel  per chunk, every product above: Vh, U, dU, Y, the
+//                         C x C products; dq, dk, dv updated once each, dbeta
+//                         and dg written
 // Products run on warp-level tensor cores with fp32 accumulation over fp16
 // operand tiles read through ldmatrix (m16n8k16), each tile scaled by its
 // own power of two so that its largest entry sits below 2^15 (fp16 range is
 // never exceeded, its 11-bit precision matches tf32); the reverse scan keeps
 // its state gradient in fp32 and converts it per step.
-// The triangular inverse is a forward substitution on the CUDA cores.  Each
-// CTA has 8 warps; a C x D output is split into 16-row strips (warp w & 3)
-// and column halves (warp w >> 2).
+// The triangular inverse is a forward substitution on the CUDA cores.  The
+// chunk-factor and scan kernels have 8 warps, the fused kernel 16; a C x D
+// output is split into 16-row strips (warp w & 3) and column halves (8
+// warps) or quarters (16 warps) (warp w >> 2).
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -349,41 +350,6 @@ __device__ __forceinline__ void block_scales2(float m1, float m2, float* red, fl
   s2 = pow2_scale(r2);
 }
 
-// bf16 C x D (global, row stride D) -> scaled fp16 tile
-template <int D>
-__device__ __forceinline__ float tile_h_bf(const bf16* src, half* dst, float* red) {
-  constexpr int V = C * D / 8 / 256;
-  uint4 v[V];
-  float m = 0.f;
-#pragma unroll
-  for (int i = 0; i < V; ++i) {
-    const int x = threadIdx.x + 256 * i, r = x / (D / 8), c = 8 * (x % (D / 8));
-    v[i] = *(const uint4*)(src + (size_t)r * D + c);
-    const __nv_bfloat162* h2 = (const __nv_bfloat162*)&v[i];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float2 f = __bfloat1622float2(h2[u]);
-      m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
-    }
-  }
-  const float s = block_scale(m, red);
-#pragma unroll
-  for (int i = 0; i < V; ++i) {
-    const int x = threadIdx.x + 256 * i, r = x / (D / 8), c = 8 * (x % (D / 8));
-    const __nv_bfloat162* h2 = (const __nv_bfloat162*)&v[i];
-    uint4 o;
-    uint32_t* o32 = (uint32_t*)&o;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float2 f = __bfloat1622float2(h2[u]);
-      const __half2 hh = __floats2half2_rn(f.x * s, f.y * s);
-      o32[u] = *(const uint32_t*)&hh;
-    }
-    *(uint4*)(dst + r * H<D>::ld + c) = o;
-  }
-  return s;
-}
-
 // accumulators (rows m0.., columns n0..) -> scaled fp16 tile (a block-wide
 // collective: every thread calls it); returns the scale
 template <int NT, int COLS, int NTH = 256>
@@ -415,27 +381,6 @@ __device__ __forceinline__ void copy_h(half* dst, const half* src) {
   }
 }
 __device__ __forceinline__ void copy_wait() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// accumulators (rows m0.., columns n0..) -> fp16 rows in memory (row stride
-// D), scaled by a power of two taken over the block (a collective); returns
-// the scale
-template <int NT, int D>
-__device__ __forceinline__ float acc_store_h(const float (&acc)[NT][4], int m0, int n0, half* dst, float* red) {
-  float m = 0.f;
-#pragma unroll
-  for (int j = 0; j < NT; ++j)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(acc[j][e]));
-  const float s = block_scale(m, red);
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-#pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    const int c0 = n0 + 8 * j + 2 * t;
-    *(__half2*)(dst + (size_t)(m0 + g) * D + c0) = __floats2half2_rn(acc[j][0] * s, acc[j][1] * s);
-    *(__half2*)(dst + (size_t)(m0 + g + 8) * D + c0) = __floats2half2_rn(acc[j][2] * s, acc[j][3] * s);
-  }
-  return s;
-}
 
 template <int NT, class F>
 __device__ __forceinline__ void each_mut(float (&acc)[NT][4], int m0, int n0, F f) {
@@ -770,415 +715,6 @@ __global__ void __launch_bounds__(256) gdn_bwd_scan_kernel(const half* __restric
     }
     __syncthreads();
   }
-}
-
-// -------------------------------------------------------- products with S0
-template <int D>
-struct S0Sm {
-  static constexpr int offS = 0;                          // fp16 [D][D + 8]: S0
-  static constexpr int offK = offS + H<D>::bytes(D);      // fp16 [C][D + 8]
-  static constexpr int offO = offK + H<D>::bytes(C);      // dO
-  static constexpr int offVh = offO + H<D>::bytes(C);     // Vh
-  static constexpr int offL = offVh + H<D>::bytes(C);     // fp16 [C][C + 8]: Linv diag(beta)
-  static constexpr int offP = offL + H<C>::bytes(C);      // P
-  static constexpr int offVec = offP + H<C>::bytes(C);    // G, gamma, beta, dG, reduction
-  static constexpr int kBytes = offVec + 4 * C * 4 + 64;
-};
-
-template <int D>
-__global__ void __launch_bounds__(256) gdn_bwd_s0_kernel(
-    const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v, const float* __restrict__ dO,
-    const float* __restrict__ S0, const float* __restrict__ Li, const float* __restrict__ Pg,
-    const float* __restrict__ Gb, const float* __restrict__ beta, int L, int N, float scale, half* __restrict__ Vh,
-    half* __restrict__ Ug, half* __restrict__ PtdO, float* __restrict__ isc, float* __restrict__ dq,
-    float* __restrict__ dGs) {
-  using S = S0Sm<D>;
-  constexpr int NT = D / 16, LD = H<D>::ld, LC = H<C>::ld;
-  extern __shared__ __align__(16) uint8_t sm[];
-  half* hS = (half*)(sm + S::offS);
-  half* hK = (half*)(sm + S::offK);
-  half* hO = (half*)(sm + S::offO);
-  half* hVh = (half*)(sm + S::offVh);
-  half* hL = (half*)(sm + S::offL);
-  half* hP = (half*)(sm + S::offP);
-  float* sG = (float*)(sm + S::offVec);
-  float* sGam = sG + C;
-  float* sB = sGam + C;
-  float* sdG = sB + C;
-  float* red = sdG + C;
-  const long long chunk = blockIdx.x;
-  const size_t row0 = (size_t)(chunk / N) * L + (size_t)(chunk % N) * C;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  load_scalars(Gb, beta, row0, sG, sGam, sB);
-  if (tid < C) sdG[tid] = 0.f;
-  // V (bf16) staged in the Vh tile, which it becomes
-  copy_h<D>(hVh, (const half*)(v + row0 * D));
-  const float ss = tile_h<D, D>(S0 + (size_t)chunk * D * D, D, hS, red);
-  const float sk = tile_h_bf<D>(k + row0 * D, hK, red);
-  const float so = tile_h<C, D>(dO + row0 * D, D, hO, red);
-  const float sl = tile_h<C, C>(Li + (size_t)chunk * C * C, C, hL, red, [&](int, int m, float x) { return x * sB[m]; });
-  const float sp = tile_h<C, C>(Pg + (size_t)chunk * C * C, C, hP, red);
-  copy_wait();
-  __syncthreads();
-  const int m0 = 16 * (warp & 3), n0 = (warp >> 2) * (D / 2);
-  float acc[NT][4];
-  // Vh = V - diag(gamma) K S0^T
-  zero(acc);
-  hmm<NT, D, false, true>(acc, m0, n0, hK, LD, hS, LD);
-  {
-    const float iks = 1.f / (sk * ss);
-    const bf16* vs = (const bf16*)hVh;
-    each_mut(acc, m0, n0, [&](int i, int n, float val, int, int) {
-      return __bfloat162float(vs[i * LD + n]) - sGam[i] * val * iks;
-    });
-  }
-  const float svh = acc_h<NT, D>(acc, m0, n0, hVh, red);
-  copy_h<D>(hK, (const half*)(q + row0 * D));  // K has been read: q (bf16) staged in its tile
-  // dO S0: dq += scale gamma_i (dO S0)_i; dG_i += gamma_i (dO S0)_i . q~_i
-  zero(acc);
-  hmm<NT, D, false, false>(acc, m0, n0, hO, LD, hS, LD);
-  copy_wait();
-  __syncthreads();
-  {
-    const float ios = scale / (so * ss);
-    const bf16* qs = (const bf16*)hK;
-    float lo = 0.f, hi = 0.f;
-    each_mut(acc, m0, n0, [&](int i, int n, float val, int, int e) {
-      const float x = sGam[i] * val * ios;
-      const float dd = x * __bfloat162float(qs[i * LD + n]);
-      if (e < 2) lo += dd; else hi += dd;
-      return x;
-    });
-    acc_add_global<NT, D>(acc, m0, n0, dq + row0 * D);
-    add_rows(lo, hi, m0, sdG);
-  }
-  __syncthreads();  // hVh complete
-  // Vh as staged (fp16 at its scale), for the dbeta term of the next kernel
-  for (int x = tid; x < C * D / 8; x += 256) {
-    const int i = x / (D / 8), c8 = 8 * (x % (D / 8));
-    *(uint4*)(Vh + (row0 + i) * D + c8) = *(const uint4*)(hVh + i * LD + c8);
-  }
-  // U = Linv diag(beta) Vh
-  zero(acc);
-  hmm<NT, C, false, true>(acc, m0, n0, hL, LC, hVh, LD);
-  {
-    const float iu = 1.f / (sl * svh);
-    each_mut(acc, m0, n0, [&](int, int, float val, int, int) { return val * iu; });
-  }
-  const float su = acc_store_h<NT, D>(acc, m0, n0, Ug + row0 * D, red);
-  // P^T dO
-  zero(acc);
-  hmm<NT, C, true, true>(acc, m0, n0, hP, LC, hO, LD);
-  {
-    const float ipo = 1.f / (sp * so);
-    each_mut(acc, m0, n0, [&](int, int, float val, int, int) { return val * ipo; });
-  }
-  const float spo = acc_store_h<NT, D>(acc, m0, n0, PtdO + row0 * D, red);
-  __syncthreads();
-  if (tid < C) dGs[row0 + tid] = sdG[tid];
-  if (tid == 0) {
-    isc[chunk * 4 + 0] = svh;
-    isc[chunk * 4 + 1] = su;
-    isc[chunk * 4 + 2] = spo;
-  }
-}
-
-// ----------------------------------------------------- products with dS_C
-template <int D>
-struct DsSm {
-  static constexpr int offS = 0;                          // fp16 [D][D + 8]: dS_C, then S0
-  static constexpr int offK = offS + H<D>::bytes(D);      // fp16 [C][D + 8]
-  static constexpr int offU = offK + H<D>::bytes(C);
-  static constexpr int offD = offU + H<D>::bytes(C);      // dU, then diag(beta) Y
-  static constexpr int offL = offD + H<D>::bytes(C);      // fp16 [C][C + 8]: Linv
-  static constexpr int offVec = offL + H<C>::bytes(C);    // G, gamma, beta, dG, dbeta, reduction
-  static constexpr int kBytes = offVec + 5 * C * 4 + 64;
-};
-
-template <int D>
-__global__ void __launch_bounds__(256, 2) gdn_bwd_ds_kernel(
-    const bf16* __restrict__ k, const float* __restrict__ S0, const float* __restrict__ dSC,
-    const half* __restrict__ Ug, const float* __restrict__ Li, const half* __restrict__ PtdO,
-    const half* __restrict__ Vh, float* __restrict__ isc, const float* __restrict__ Gb,
-    const float* __restrict__ beta, const uint8_t* __restrict__ sel, int L, int N, half* __restrict__ Yg,
-    float* __restrict__ dv,
-    float* __restrict__ dk, float* __restrict__ dGs, float* __restrict__ dbeta) {
-  using S = DsSm<D>;
-  constexpr int NT = D / 16, LD = H<D>::ld, LC = H<C>::ld;
-  extern __shared__ __align__(16) uint8_t sm[];
-  half* hS = (half*)(sm + S::offS);
-  half* hK = (half*)(sm + S::offK);
-  half* hU = (half*)(sm + S::offU);
-  half* hD = (half*)(sm + S::offD);
-  half* hL = (half*)(sm + S::offL);
-  float* sG = (float*)(sm + S::offVec);
-  float* sGam = sG + C;
-  float* sB = sGam + C;
-  float* sdG = sB + C;
-  float* sdB = sdG + C;
-  float* red = sdB + C;  // [0..7] tile maxima, [8] the last token's extra dG, [9] <dS_C, S0>
-  const long long chunk = blockIdx.x;
-  const int c = (int)(chunk % N);
-  const size_t row0 = (size_t)(chunk / N) * L + (size_t)c * C;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool committed = sel[chunk] != 0 && c < N - 1;
-  load_scalars(Gb, beta, row0, sG, sGam, sB);
-  if (tid < C) sdG[tid] = sdB[tid] = 0.f;
-  if (tid < 2) red[8 + tid] = 0.f;
-  copy_h<D>(hU, Ug + row0 * D);
-  copy_h<D>(hD, PtdO + row0 * D);  // P^T dO staged in the dU tile, which it becomes part of
-  const float sk = tile_h_bf<D>(k + row0 * D, hK, red);
-  const float svh = isc[chunk * 4 + 0], su = isc[chunk * 4 + 1], spo = isc[chunk * 4 + 2];
-  const float sl = tile_h<C, C>(Li + (size_t)chunk * C * C, C, hL, red);
-  float sd = 1.f;
-  if (committed) {  // dS_C, and <dS_C, S0> on the way
-    const float* s0 = S0 + (size_t)chunk * D * D;
-    float dot = 0.f;
-    sd = tile_h<D, D>(dSC + (size_t)chunk * D * D, D, hS, red, [&](int r, int cc, float x) {
-      dot += x * s0[(size_t)r * D + cc];
-      return x;
-    });
-    dot = warp_sum(dot);
-    if (lane == 0) atomicAdd(red + 9, dot);
-  }
-  copy_wait();
-  __syncthreads();
-  const int m0 = 16 * (warp & 3), n0 = (warp >> 2) * (D / 2);
-  const float gC = sGam[C - 1];
-  // dU = P^T dO + K~ dS_C^T (registers, fp32)
-  float dU[NT][4];
-  zero(dU);
-  if (committed) hmm<NT, D, false, true>(dU, m0, n0, hK, LD, hS, LD);
-  {
-    const float ikd = 1.f / (sk * sd), ipo = 1.f / spo;
-    each_mut(dU, m0, n0, [&](int i, int a, float val, int, int) {
-      return __half2float(hD[i * LD + a]) * ipo + gC / sGam[i] * val * ikd;
-    });
-  }
-  // this kernel's share of dk, written once at the end
-  float dka[NT][4];
-  zero(dka);
-  if (committed) {  // U dS_C: dk += diag(gamma_C / gamma) (U dS_C); dG_j -= (U dS_C)_j . K~_j; the last token gains their sum
-    hmm<NT, D, false, false>(dka, m0, n0, hU, LD, hS, LD);
-    const float iud = 1.f / (su * sd), ik = 1.f / sk;
-    float lo = 0.f, hi = 0.f;
-    each_mut(dka, m0, n0, [&](int i, int n, float val, int, int e) {
-      const float x = gC / sGam[i] * val * iud;
-      const float dd = x * ik * __half2float(hK[i * LD + n]);
-      if (e < 2) lo -= dd; else hi -= dd;
-      return x;
-    });
-    float tot = warp_sum(-(lo + hi));
-    add_rows(lo, hi, m0, sdG);
-    if (lane == 0) atomicAdd(red + 8, tot);
-  }
-  const float sdu = acc_h<NT, D>(dU, m0, n0, hD, red);  // (its barriers also order the reads of dS_C above)
-  __syncthreads();
-  copy_h<D>(hU, Vh + row0 * D);  // U has been read: Vh staged in its tile
-  if (tid == 0) sdG[C - 1] += red[8] + gC * red[9];
-  // Y = Linv^T dU; dv += diag(beta) Y; dbeta_i = Y_i . Vh_i
-  float acc[NT][4];
-  zero(acc);
-  hmm<NT, C, true, true>(acc, m0, n0, hL, LC, hD, LD);
-  {
-    const float iy = 1.f / (sl * sdu), ivh = 1.f / svh;
-    each_mut(acc, m0, n0, [&](int, int, float val, int, int) { return val * iy; });
-    copy_wait();  // (the barriers of the next call make every thread's Vh copies visible)
-    const float sy = acc_store_h<NT, D>(acc, m0, n0, Yg + row0 * D, red);
-    if (tid == 0) isc[chunk * 4 + 3] = sy;
-    float lo = 0.f, hi = 0.f;
-    each_mut(acc, m0, n0, [&](int i, int n, float y, int, int e) {
-      const float dd = y * __half2float(hU[i * LD + n]) * ivh;
-      if (e < 2) lo += dd; else hi += dd;
-      return sB[i] * y;
-    });
-    acc_add_global<NT, D>(acc, m0, n0, dv + row0 * D);  // dv += diag(beta) Y
-    add_rows(lo, hi, m0, sdB);
-  }
-  __syncthreads();  // every read of dU (and of dS_C) is done
-  const float sy = acc_h<NT, D>(acc, m0, n0, hD, red);
-  const float ss = tile_h<D, D>(S0 + (size_t)chunk * D * D, D, hS, red);
-  __syncthreads();
-  {  // dk -= diag(gamma) dVh S0; dG_i -= gamma_i (dVh S0)_i . k_i
-    zero(acc);
-    hmm<NT, D, false, false>(acc, m0, n0, hD, LD, hS, LD);
-    const float iys = 1.f / (sy * ss), ik = 1.f / sk;
-    float lo = 0.f, hi = 0.f;
-    each(acc, m0, n0, [&](int i, int n, float val, int j, int e) {
-      const float x = sGam[i] * val * iys;
-      dka[j][e] -= x;
-      const float dd = x * ik * __half2float(hK[i * LD + n]);
-      if (e < 2) lo -= dd; else hi -= dd;
-    });
-    acc_add_global<NT, D>(dka, m0, n0, dk + row0 * D);
-    add_rows(lo, hi, m0, sdG);
-  }
-  __syncthreads();
-  if (tid < C) {
-    dGs[row0 + tid] += sdG[tid];
-    dbeta[row0 + tid] = sdB[tid];
-  }
-}
-
-// ---------------------------------------------------- C x C products, dg
-template <int D>
-struct CcSm {
-  static constexpr int offQ = 0;                          // fp16 [C][D + 8]
-  static constexpr int offK = offQ + H<D>::bytes(C);
-  static constexpr int offO = offK + H<D>::bytes(C);
-  static constexpr int offU = offO + H<D>::bytes(C);
-  static constexpr int offY = offU + H<D>::bytes(C);
-  static constexpr int offA = offY + H<D>::bytes(C);      // fp16 [C][C + 8]: A~
-  static constexpr int offP = offA + H<C>::bytes(C);      // dP . R
-  static constexpr int offVec = offP + H<C>::bytes(C);    // G, gamma, beta, dG, dbeta, reduction
-  static constexpr int kBytes = offVec + 5 * C * 4 + 64;
-};
-
-template <int D>
-__global__ void __launch_bounds__(256) gdn_bwd_cc_kernel(
-    const bf16* __restrict__ q, const bf16* __restrict__ k, const float* __restrict__ dO,
-    const half* __restrict__ Ug, const half* __restrict__ Yg, const float* __restrict__ isc,
-    const float* __restrict__ Gb, const float* __restrict__ beta, int L, int N, float scale,
-    float* __restrict__ dq, float* __restrict__ dk,
-    const float* __restrict__ dGs, float* __restrict__ dbeta, float* __restrict__ dg) {
-  using S = CcSm<D>;
-  constexpr int NT = D / 16, LD = H<D>::ld, LC = H<C>::ld;
-  extern __shared__ __align__(16) uint8_t sm[];
-  half* hQ = (half*)(sm + S::offQ);
-  half* hK = (half*)(sm + S::offK);
-  half* hO = (half*)(sm + S::offO);
-  half* hU = (half*)(sm + S::offU);
-  half* hY = (half*)(sm + S::offY);
-  half* hA = (half*)(sm + S::offA);
-  half* hPm = (half*)(sm + S::offP);
-  float* sG = (float*)(sm + S::offVec);
-  float* sGam = sG + C;
-  float* sB = sGam + C;
-  float* sdG = sB + C;
-  float* sdB = sdG + C;
-  float* red = sdB + C;
-  const long long chunk = blockIdx.x;
-  const size_t row0 = (size_t)(chunk / N) * L + (size_t)(chunk % N) * C;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  load_scalars(Gb, beta, row0, sG, sGam, sB);
-  if (tid < C) sdG[tid] = sdB[tid] = 0.f;
-  copy_h<D>(hU, Ug + row0 * D);
-  copy_h<D>(hY, Yg + row0 * D);
-  float sq, sk;
-  {  // q and k: both tiles' loads in flight at once, one reduction
-    BF16Tile<D> tq, tk;
-    tq.load(q + row0 * D);
-    tk.load(k + row0 * D);
-    block_scales2(tq.m, tk.m, red, sq, sk);
-    tq.store(hQ, sq);
-    tk.store(hK, sk);
-  }
-  const float so = tile_h<C, D>(dO + row0 * D, D, hO, red);
-  const float su = isc[chunk * 4 + 1], sy = isc[chunk * 4 + 3];
-  copy_wait();
-  __syncthreads();
-  float sa, spm;
-  {
-    const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);
-    // dL = -strict_lower(Y U^T), A = R . K K^T: dA = diag(beta) dL, A~ = dA . R,
-    // dbeta_i += sum_j dL_ij A_ij, dG += row sums - column sums of dA . A
-    {
-      float yu[4][4], kk[4][4];
-      zero(yu);
-      zero(kk);
-      hmm<4, D, false, false>(yu, m0, n0, hY, LD, hU, LD);
-      hmm<4, D, false, false>(kk, m0, n0, hK, LD, hK, LD);
-      const float iyu = 1.f / (sy * su), ikk = 1.f / (sk * sk);
-      float rlo = 0.f, rhi = 0.f, blo = 0.f, bhi = 0.f, col[4][2];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) col[j][0] = col[j][1] = 0.f;
-      each_mut(yu, m0, n0, [&](int i, int jj, float val, int j, int e) {
-        float at = 0.f;
-        if (jj < i) {
-          const float r = __expf(sG[i] - sG[jj]);
-          const float A = r * kk[j][e] * ikk;
-          const float dL = -val * iyu;
-          const float dA = sB[i] * dL;
-          const float x = dA * A;
-          if (e < 2) rlo += x, blo += dL * A; else rhi += x, bhi += dL * A;
-          col[j][e & 1] -= x;
-          at = dA * r;
-        }
-        return at;
-      });
-      add_rows(rlo, rhi, m0, sdG);
-      add_rows(blo, bhi, m0, sdB);
-      add_cols<4>(col, n0, sdG);
-      sa = acc_h<4, C>(yu, m0, n0, hA, red);
-    }
-    // dP = lower(dO U^T), P = R . Q~ K^T: dPm = dP . R, dG += row sums - column sums of dP . P
-    {
-      float ou[4][4], qk[4][4];
-      zero(ou);
-      zero(qk);
-      hmm<4, D, false, false>(ou, m0, n0, hO, LD, hU, LD);
-      hmm<4, D, false, false>(qk, m0, n0, hQ, LD, hK, LD);
-      const float iou = 1.f / (so * su), iqk = scale / (sq * sk);
-      float rlo = 0.f, rhi = 0.f, col[4][2];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) col[j][0] = col[j][1] = 0.f;
-      each_mut(ou, m0, n0, [&](int i, int jj, float val, int j, int e) {
-        float pm = 0.f;
-        if (jj <= i) {
-          const float r = __expf(sG[i] - sG[jj]);
-          const float P = r * qk[j][e] * iqk;
-          const float dP = val * iou;
-          const float x = dP * P;
-          if (e < 2) rlo += x; else rhi += x;
-          col[j][e & 1] -= x;
-          pm = dP * r;
-        }
-        return pm;
-      });
-      add_rows(rlo, rhi, m0, sdG);
-      add_cols<4>(col, n0, sdG);
-      spm = acc_h<4, C>(ou, m0, n0, hPm, red);
-    }
-  }
-  __syncthreads();
-  {
-    const int m0 = 16 * (warp & 3), n0 = (warp >> 2) * (D / 2);
-    {  // dq += scale (dP . R) K
-      float acc[NT][4];
-      zero(acc);
-      hmm<NT, C, false, true>(acc, m0, n0, hPm, LC, hK, LD);
-      const float f = scale / (spm * sk);
-      each_mut(acc, m0, n0, [&](int, int, float val, int, int) { return f * val; });
-      acc_add_global<NT, D>(acc, m0, n0, dq + row0 * D);
-    }
-    {  // dk += (dP . R)^T Q~ + (A~ + A~^T) K
-      float a1[NT][4], a2[NT][4];
-      zero(a1);
-      zero(a2);
-      hmm<NT, C, true, true>(a1, m0, n0, hPm, LC, hQ, LD);
-      hmm<NT, C, false, true>(a2, m0, n0, hA, LC, hK, LD);
-      hmm<NT, C, true, true>(a2, m0, n0, hA, LC, hK, LD);
-      const float f1 = scale / (spm * sq), f2 = 1.f / (sa * sk);
-      each_mut(a1, m0, n0, [&](int, int, float val, int j, int e) { return f1 * val + f2 * a2[j][e]; });
-      acc_add_global<NT, D>(a1, m0, n0, dk + row0 * D);
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {  // dg = reverse cumulative sum of dG over the chunk
-    const float a0 = sdG[2 * lane] + dGs[row0 + 2 * lane];
-    const float a1 = sdG[2 * lane + 1] + dGs[row0 + 2 * lane + 1];
-    float s = a0 + a1;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_down_sync(0xffffffffu, s, o);
-      if (lane + o < 32) s += y;
-    }
-    // s = sum over lanes >= this one
-    const float after = s - a0 - a1;
-    dg[row0 + 2 * lane + 1] = a1 + after;
-    dg[row0 + 2 * lane] = a0 + a1 + after;
-  }
-  if (tid < C) dbeta[row0 + tid] += sdB[tid];
 }
 
 // ------------------------------------------ every per-chunk product, fused

@@ -92,12 +92,6 @@ struct GdnBwdScratch {
   void* Qe16;   // [BH, L, dk] fp16: diag(gamma) Q~ - P W      >  power-of-two scale
   void* Kt16;   // [BH, L, dk] fp16: diag(gamma_C / gamma) K  /   (sc)
   float* sc;    // [BH, N, 4] the scales of W, Q_eff, K~
-  void* Vh;     // [BH, L, dv] fp16: V - diag(gamma) K S0^T   \  each times its chunk's
-  void* U;      // [BH, L, dv] fp16: Linv diag(beta) Vh        |  power-of-two scale
-  void* PtdO;   // [BH, L, dv] fp16: P^T dO                    |  (isc)
-  void* Y;      // [BH, L, dv] fp16: Linv^T dU                 /
-  float* isc;   // [BH, N, 4] the scales of Vh, U, P^T dO, Y
-  float* dG;    // [BH, L] gradient of G from the state products
 };
 // the adjoint's chunk factors and the reverse state-gradient scan (two
 // kernels; they read q, k, g, beta, the selection and dO, and write only the

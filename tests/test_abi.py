@@ -182,13 +182,12 @@ def test_backward_validation(nat):
                             + al(2 * rows * 4 * 4))
     # bf16 layers: the compacted softmax-chunk lists, the forward's chunk factors (G, W, U^T, P, gate, o_l,
     # error flag), then the chunkwise adjoint's chunk-start states and state gradients, G, Linv and P (fp32),
-    # W, Q_eff, K~ (fp16) and their scales, Vh, U, P^T dO, Y (fp16) and their scales, and dG
+    # W, Q_eff, K~ (fp16) and their scales
     assert need == common + (2 * al(chunks * 4) + al(rows * 4) + 2 * al(rows * 64 * 2) + al(rows * 64 * 2)
                              + al(rows * 4)
                              + al(rows * 64 * 2) + al(16)
                              + 2 * al(chunks * dd * 4) + al(rows * 4) + 2 * al(rows * 64 * 4)
-                             + 3 * al(rows * 64 * 2) + al(chunks * 16) + 4 * al(rows * 64 * 2) + al(chunks * 16)
-                             + al(rows * 4))
+                             + 3 * al(rows * 64 * 2) + al(chunks * 16))
     fake = ctypes.c_void_p(256)
     odd = ctypes.c_void_p(264)
     args = [fake] * 23  # q ... dnorm_w_lin, then the workspace
