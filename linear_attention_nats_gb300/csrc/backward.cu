@@ -830,8 +830,8 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
         return e2;
       // every per-chunk product of the adjoint: dq, dk, dv, dg, dbeta
       if ((e2 = mark(ev_start, NATS_BWD_STAGE_COMBINE)) != cudaSuccess) return e2;
-      if ((e2 = launch_gdn_bwd_products(p, q, k, v, g, beta, sel, d_ol, lay.cw, dq, dk, dv, dg, dbeta, st)) !=
-          cudaSuccess)
+      if ((e2 = launch_gdn_bwd_products(p, q, k, v, g, beta, sel, d_ol, lay.cw, dq, dk, dv, dg, dbeta, lay.ferr,
+                                        st)) != cudaSuccess)
         return e2;
       count(NATS_BWD_STAGE_COMBINE, 1);
     } else {

@@ -49,6 +49,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
 
 namespace nats {
 namespace {
@@ -139,6 +140,11 @@ struct Tiles {
   static constexpr int FS = D + 4;  // fp32 row stride of C x D and D x D tiles
   static constexpr int BS = D + 8;  // bf16 row stride of C x D tiles
 };
+
+// a hint: bring `bytes` (a multiple of 16, 16-byte aligned) at p into L2
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 __device__ __forceinline__ void cp16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
@@ -1063,6 +1069,554 @@ __global__ void __launch_bounds__(512, 1) gdn_bwd_fused_kernel(
   if (tid < C) dbeta[row0 + tid] = sdB[tid];
 }
 
+// ------------------------------------------ the per-chunk products on tcgen05
+// (d = 128).  The products of gdn_bwd_fused_kernel on the 5th-generation
+// tensor cores: every C x D product is taken transposed (TMEM lane = feature
+// dv or dk, column = token; M = 128, N = 64), the C x C ones as
+// [Y; dO] U^T and [K; Q] K^T (rows of Y and K in lanes 0-63, of dO and Q in
+// lanes 64-127, so that each lane quarter holds the rows its epilogue
+// pairs).  Operand tiles are fp16 at their own power-of-two scales in
+// 128-byte-swizzled lines; thread 0 issues each phase's MMAs, and warp w
+// reads TMEM lanes 32 (w & 3) .. + 31, columns 16 (w >> 2) .. + 15.
+namespace tcb {
+constexpr int D = 128, NTH = 512;
+constexpr int kBlk = 16384;     // distance between the 64-column blocks of a 128-column tile
+constexpr int offS = 0;         // S0   [dk][dv]  (128 lines x 128 columns)
+constexpr int offT = 32768;     // dS_C [dk][dv]
+constexpr int offYO = 65536;    // [Y; dO] [128][dv]: Y lines 0-63, dO lines 64-127
+constexpr int offKQ = 98304;    // [K; Q]  [128][dk]: K lines 0-63, Q lines 64-127
+constexpr int offVh = 131072;   // Vh^T [dv][64]
+constexpr int offU = 147456;    // U^T  [dv][64]
+constexpr int offDU = 163840;   // dU^T [dv][64]
+constexpr int offL = 180224;    // Linv [64][64]
+constexpr int offLb = 188416;   // Linv diag(beta)
+constexpr int offP = 196608;    // P, then dP . R
+constexpr int offA = 204800;    // A~
+constexpr int offVec = 212992;  // G, gamma, beta, dG, dbeta (fp32 [64] each)
+constexpr int offRed = offVec + 5 * C * 4;  // 128 floats: partial maxima; [126] extra dG of the last token; [127] <dS_C, S0>
+constexpr int offBar = offRed + 128 * 4;    // 6 mbarriers, one per phase
+constexpr int offFlag = offBar + 6 * 8;     // a wait ran out (the rest of the CTA's waits are skipped)
+constexpr int offTmem = offFlag + 8;
+constexpr int kBytes = offTmem + 8 + 1024;  // + alignment slack of the dynamic base
+static_assert(offVec == offA + 8192 && offA % 1024 == 0, "tiles");
+// TMEM columns (64 fp32 each); the last phase reuses those read before it
+constexpr uint32_t cVh = 0, cDqA = 64, cDub = 128, cKQ = 192, cU = 256, cDua = 320, cY = 384, cYO = 448;
+constexpr uint32_t cDqB = 0, cDka = 256, cDkb = 320, cDkc = 384, cDkd = 128;
+constexpr uint32_t ID_KK = tc::idesc_f16_f32(128, 64, false, false), ID_MK = tc::idesc_f16_f32(128, 64, true, false),
+                   ID_KM = tc::idesc_f16_f32(128, 64, false, true), ID_MM = tc::idesc_f16_f32(128, 64, true, true);
+
+// byte offset of element (r, c) of a swizzled tile
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return (uint32_t)((c >> 6) * kBlk + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + (c & 7) * 2);
+}
+// K-major operand at shared address t, lines r0 .., k = 16 kk .. + 15
+__device__ __forceinline__ uint64_t kmaj(uint32_t t, int r0, int kk) {
+  return tc::smem_desc_sw128(t + r0 * 128 + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024);
+}
+// MN-major operand at shared address t (lines = k), k = 16 kk .. + 15
+__device__ __forceinline__ uint64_t mnmaj(uint32_t t, int kk) {
+  return tc::smem_desc_sw128(t + kk * 2048, kBlk, 1024);
+}
+__device__ __forceinline__ void st4(uint8_t* tile, int r, int c, float4 v, float s) {
+  *(uint2*)(tile + swz(r, c)) = half4(v, s);
+}
+__device__ __forceinline__ void st_bf8(uint8_t* tile, int r, int c, uint4 raw, float s) {
+  const __nv_bfloat162* h2 = (const __nv_bfloat162*)&raw;
+  uint4 o;
+  uint32_t* o32 = (uint32_t*)&o;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float2 x = __bfloat1622float2(h2[u]);
+    const __half2 hh = __floats2half2_rn(x.x * s, x.y * s);
+    o32[u] = *(const uint32_t*)&hh;
+  }
+  *(uint4*)(tile + swz(r, c)) = o;
+}
+__device__ __forceinline__ float bf8_max(uint4 raw) {
+  const __nv_bfloat162* h2 = (const __nv_bfloat162*)&raw;
+  float m = 0.f;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float2 x = __bfloat1622float2(h2[u]);
+    m = fmaxf(m, fmaxf(fabsf(x.x), fabsf(x.y)));
+  }
+  return m;
+}
+// line r, columns c0 .. c0 + 15 (two 16-byte granules) of a swizzled tile
+__device__ __forceinline__ void st_row16(uint8_t* tile, int r, int c0, const float (&v)[16], float s) {
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    uint4 o;
+    uint32_t* o32 = (uint32_t*)&o;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const __half2 hh = __floats2half2_rn(v[8 * g + 2 * u] * s, v[8 * g + 2 * u + 1] * s);
+      o32[u] = *(const uint32_t*)&hh;
+    }
+    *(uint4*)(tile + swz(r, c0 + 8 * g)) = o;
+  }
+}
+__device__ __forceinline__ void ld_row16(const uint8_t* tile, int r, int c0, float (&v)[16]) {
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    const uint4 o = *(const uint4*)(tile + swz(r, c0 + 8 * g));
+    const __half2* h2 = (const __half2*)&o;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float2 x = __half22float2(h2[u]);
+      v[8 * g + 2 * u] = x.x;
+      v[8 * g + 2 * u + 1] = x.y;
+    }
+  }
+}
+__device__ __forceinline__ float elem(const uint8_t* tile, int r, int c) {
+  return __half2float(*(const half*)(tile + swz(r, c)));
+}
+// p[t] (token t0 + t) summed over the warp's 32 lanes and added into
+// dst[t0 + t]: a halving exchange leaves lanes 2u and 2u + 1 with token u
+__device__ __forceinline__ void add_tokens(const float (&p)[16], float* dst, int t0) {
+  const int lane = threadIdx.x & 31;
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+  float w8[8], w4[4], w2[2];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    w8[i] = (b4 ? p[i + 8] : p[i]) + __shfl_xor_sync(0xffffffffu, b4 ? p[i] : p[i + 8], 16);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w4[i] = (b3 ? w8[i + 4] : w8[i]) + __shfl_xor_sync(0xffffffffu, b3 ? w8[i] : w8[i + 4], 8);
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    w2[i] = (b2 ? w4[i + 2] : w4[i]) + __shfl_xor_sync(0xffffffffu, b2 ? w4[i] : w4[i + 2], 4);
+  float w1 = (b1 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? w2[0] : w2[1], 2);
+  w1 += __shfl_xor_sync(0xffffffffu, w1, 1);
+  if (!(lane & 1)) atomicAdd(dst + t0 + ((lane >> 1) & 15), w1);
+}
+}  // namespace tcb
+
+__global__ void __launch_bounds__(tcb::NTH, 1) gdn_bwd_tc_kernel(
+    const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v, const float* __restrict__ dO,
+    const float* __restrict__ S0, const float* __restrict__ dSC, const float* __restrict__ Li,
+    const float* __restrict__ Pg, const float* __restrict__ Gb, const float* __restrict__ beta,
+    const uint8_t* __restrict__ sel, int L, int N, float scale, float* __restrict__ dq, float* __restrict__ dk,
+    float* __restrict__ dv, float* __restrict__ dg, float* __restrict__ dbeta, int* __restrict__ err) {
+  using namespace tcb;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const uint32_t sb = tc::smem_u32(sm);
+  float* sG = (float*)(sm + offVec);
+  float* sGam = sG + C;
+  float* sB = sGam + C;
+  float* sdG = sB + C;
+  float* sdB = sdG + C;
+  float* red = (float*)(sm + offRed);
+  uint64_t* bars = (uint64_t*)(sm + offBar);
+  volatile int* fail = (volatile int*)(sm + offFlag);
+  uint32_t* tslot = (uint32_t*)(sm + offTmem);
+  const long long chunk = blockIdx.x;
+  const int c = (int)(chunk % N);
+  const size_t row0 = (size_t)(chunk / N) * L + (size_t)c * C;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int f = 32 * (warp & 3) + lane;  // this thread's TMEM lane
+  const int t0 = 16 * (warp >> 2);       // and its first column
+  const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+  const bool committed = sel[chunk] != 0 && c < N - 1;
+  // the rows the epilogues read late (v, and dq, dk, dv before their
+  // updates) start towards L2 while the operand tiles load
+  if (tid == 64) prefetch_l2(v + row0 * D, C * D * 2);
+  if (tid == 96) prefetch_l2(dv + row0 * D, C * D * 4);
+  if (tid == 128) prefetch_l2(dq + row0 * D, C * D * 4);
+  if (tid == 160) prefetch_l2(dk + row0 * D, C * D * 4);
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, 512);
+    tc::tmem_relinquish();
+    tc::fence_before();
+  }
+  if (tid == 32) {
+    for (int i = 0; i < 6; ++i) tc::mbar_init(&bars[i], 1);
+    tc::fence_barrier_init();
+    *fail = 0;
+  }
+  load_scalars(Gb, beta, row0, sG, sGam, sB);
+  if (tid < C) sdG[tid] = sdB[tid] = 0.f;
+  if (tid < 2) red[126 + tid] = 0.f;
+  // S0 and dS_C (a committed chunk's; zero otherwise), read in the same
+  // order so that <dS_C, S0> is taken in fp32 on the way
+  float ss, sd;
+  {
+    constexpr int V = D * D / 4 / NTH;
+    const float* s0 = S0 + (size_t)chunk * D * D;
+    const float* ds = dSC + (size_t)chunk * D * D;
+    float4 a[V], b[V];
+    float m[2] = {0.f, 0.f}, sc2[2], dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int x = tid + NTH * i;
+      a[i] = *(const float4*)(s0 + (size_t)(x / (D / 4)) * D + 4 * (x % (D / 4)));
+      m[0] = fmaxf(m[0], max4(a[i]));
+    }
+    if (committed) {
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const int x = tid + NTH * i;
+        b[i] = *(const float4*)(ds + (size_t)(x / (D / 4)) * D + 4 * (x % (D / 4)));
+        m[1] = fmaxf(m[1], max4(b[i]));
+        dot += a[i].x * b[i].x + a[i].y * b[i].y + a[i].z * b[i].z + a[i].w * b[i].w;
+      }
+    }
+    block_scalesN<2, NTH>(m, red, sc2);
+    ss = sc2[0];
+    sd = sc2[1];
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int x = tid + NTH * i, r = x / (D / 4), cc = 4 * (x % (D / 4));
+      st4(sm + offS, r, cc, a[i], ss);
+      if (committed) st4(sm + offT, r, cc, b[i], sd);
+    }
+    if (committed) {
+      dot = warp_sum(dot);
+      if (lane == 0) atomicAdd(red + 127, dot);
+    }
+  }
+  // k, q, dO, Linv (plain and with its columns scaled by beta) and P: every
+  // load in flight together, one reduction for the six scales
+  float sq, sk, so, sl, slb, sp;
+  {
+    constexpr int VB = C * D / 8 / NTH, VO = C * D / 4 / NTH, VC = C * C / 4 / NTH;
+    uint4 kr[VB], qr[VB];
+    float4 o[VO], l[VC], pp[VC];
+    float m[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, s6[6];
+    const float* lsrc = Li + (size_t)chunk * C * C;
+    const float* psrc = Pg + (size_t)chunk * C * C;
+#pragma unroll
+    for (int i = 0; i < VB; ++i) {
+      const int x = tid + NTH * i, r = x / (D / 8), cc = 8 * (x % (D / 8));
+      kr[i] = *(const uint4*)(k + (row0 + r) * D + cc);
+      qr[i] = *(const uint4*)(q + (row0 + r) * D + cc);
+    }
+#pragma unroll
+    for (int i = 0; i < VO; ++i) {
+      const int x = tid + NTH * i;
+      o[i] = *(const float4*)(dO + (row0 + x / (D / 4)) * D + 4 * (x % (D / 4)));
+    }
+#pragma unroll
+    for (int i = 0; i < VC; ++i) {
+      const int x = tid + NTH * i;
+      l[i] = *(const float4*)(lsrc + (x / (C / 4)) * C + 4 * (x % (C / 4)));
+      pp[i] = *(const float4*)(psrc + (x / (C / 4)) * C + 4 * (x % (C / 4)));
+    }
+#pragma unroll
+    for (int i = 0; i < VB; ++i) m[0] = fmaxf(m[0], bf8_max(kr[i])), m[1] = fmaxf(m[1], bf8_max(qr[i]));
+#pragma unroll
+    for (int i = 0; i < VO; ++i) m[2] = fmaxf(m[2], max4(o[i]));
+#pragma unroll
+    for (int i = 0; i < VC; ++i) {
+      const int cc = 4 * ((tid + NTH * i) % (C / 4));
+      m[3] = fmaxf(m[3], max4(l[i]));
+      m[4] = fmaxf(m[4], max4(make_float4(l[i].x * sB[cc], l[i].y * sB[cc + 1], l[i].z * sB[cc + 2],
+                                          l[i].w * sB[cc + 3])));
+      m[5] = fmaxf(m[5], max4(pp[i]));
+    }
+    block_scalesN<6, NTH>(m, red, s6);
+    sk = s6[0], sq = s6[1], so = s6[2], sl = s6[3], slb = s6[4], sp = s6[5];
+#pragma unroll
+    for (int i = 0; i < VB; ++i) {
+      const int x = tid + NTH * i, r = x / (D / 8), cc = 8 * (x % (D / 8));
+      st_bf8(sm + offKQ, r, cc, kr[i], sk);
+      st_bf8(sm + offKQ, C + r, cc, qr[i], sq);
+    }
+#pragma unroll
+    for (int i = 0; i < VO; ++i) {
+      const int x = tid + NTH * i;
+      st4(sm + offYO, C + x / (D / 4), 4 * (x % (D / 4)), o[i], so);
+    }
+#pragma unroll
+    for (int i = 0; i < VC; ++i) {
+      const int x = tid + NTH * i, r = x / (C / 4), cc = 4 * (x % (C / 4));
+      st4(sm + offL, r, cc, l[i], sl);
+      st4(sm + offLb, r, cc,
+          make_float4(l[i].x * sB[cc], l[i].y * sB[cc + 1], l[i].z * sB[cc + 2], l[i].w * sB[cc + 3]), slb);
+      st4(sm + offP, r, cc, pp[i], sp);
+    }
+  }
+  // V of this thread's feature f and tokens t0 .., for the Vh epilogue
+  float vv[16];
+#pragma unroll
+  for (int t = 0; t < 16; ++t) vv[t] = __bfloat162float(v[(row0 + t0 + t) * D + f]);
+  tc::fence_proxy_async_smem();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tm = *tslot;
+  const uint32_t sS = sb + offS, sT = sb + offT, sYO = sb + offYO, sKQ = sb + offKQ, sVh = sb + offVh,
+                 sU = sb + offU, sDU = sb + offDU, sL = sb + offL, sLb = sb + offLb, sP = sb + offP, sA = sb + offA;
+  // a phase's products, issued by one thread; every thread then waits for them
+  auto issue = [&](int bar, auto body) {
+    if (tid == 0 && !*fail) {
+      tc::fence_after();
+      body();
+      tc::mma_commit(&bars[bar]);
+    }
+  };
+  auto wait = [&](int bar) {
+    if (!*fail && !tc::mbar_wait(&bars[bar], 0, err)) *fail = 1;
+    tc::fence_after();
+  };
+  auto ld = [&](uint32_t col, float (&x)[16]) {
+    tc::tmem_ld16(tm + col + t0 + lane_off, x);
+    tc::tmem_ld_wait();
+  };
+  // the end of an epilogue: its tile writes visible to the MMAs, its TMEM
+  // reads done before the next phase may overwrite their columns
+  auto phase_end = [&]() {
+    tc::fence_proxy_async_smem();
+    tc::fence_before();
+    __syncthreads();
+  };
+  const float gC = sGam[C - 1];
+  // products that need only the loaded tiles: Vh^T = (K S0^T)^T, (dO S0)^T,
+  // (K dS_C^T)^T, [K; Q] K^T
+  issue(0, [&] {
+    for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tm + cVh, mnmaj(sS, kk), kmaj(sKQ, 0, kk), ID_MK, kk > 0);
+    for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tm + cDqA, kmaj(sS, 0, kk), kmaj(sYO, C, kk), ID_KK, kk > 0);
+    if (committed)
+      for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tm + cDub, mnmaj(sT, kk), kmaj(sKQ, 0, kk), ID_MK, kk > 0);
+    for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tm + cKQ, kmaj(sKQ, 0, kk), kmaj(sKQ, 0, kk), ID_KK, kk > 0);
+  });
+  wait(0);
+  float svh;
+  {  // Vh = V - diag(gamma) K S0^T; dG_i += gamma_i (dO S0)_i . q~_i
+    float a[16], b[16], part[16];
+    ld(cVh, a);
+    ld(cDqA, b);
+    const float iks = 1.f / (sk * ss), ios = scale / (so * ss), iq = 1.f / sq;
+    float mx = 0.f;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      a[t] = vv[t] - sGam[t0 + t] * a[t] * iks;
+      mx = fmaxf(mx, fabsf(a[t]));
+      part[t] = sGam[t0 + t] * b[t] * ios * elem(sm + offKQ, C + t0 + t, f) * iq;
+    }
+    add_tokens(part, sdG, t0);
+    svh = block_scale<NTH>(mx, red);
+    st_row16(sm + offVh, f, t0, a, svh);
+  }
+  phase_end();
+  // U^T = (Linv diag(beta) Vh)^T
+  issue(1, [&] {
+    for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(tm + cU, kmaj(sVh, 0, kk), kmaj(sLb, 0, kk), ID_KK, kk > 0);
+  });
+  wait(1);
+  float su;
+  {
+    float a[16];
+    ld(cU, a);
+    const float iu = 1.f / (slb * svh);
+    float mx = 0.f;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) a[t] *= iu, mx = fmaxf(mx, fabsf(a[t]));
+    su = block_scale<NTH>(mx, red);
+    st_row16(sm + offU, f, t0, a, su);
+  }
+  phase_end();
+  // dU^T = (P^T dO + K~ dS_C^T)^T
+  issue(2, [&] {
+    for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(tm + cDua, mnmaj(sYO + C * 128, kk), mnmaj(sP, kk), ID_MM, kk > 0);
+  });
+  wait(2);
+  float sdu;
+  {
+    float a[16], b[16];
+    ld(cDua, a);
+    if (committed) ld(cDub, b);
+    const float ipo = 1.f / (sp * so), ikd = 1.f / (sk * sd);
+    float mx = 0.f;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      a[t] = a[t] * ipo + (committed ? gC / sGam[t0 + t] * b[t] * ikd : 0.f);
+      mx = fmaxf(mx, fabsf(a[t]));
+    }
+    sdu = block_scale<NTH>(mx, red);
+    st_row16(sm + offDU, f, t0, a, sdu);
+  }
+  phase_end();
+  // Y^T = (Linv^T dU)^T; dv += diag(beta) Y; dbeta_j = Y_j . Vh_j
+  issue(3, [&] {
+    for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(tm + cY, kmaj(sDU, 0, kk), mnmaj(sL, kk), ID_KM, kk > 0);
+  });
+  wait(3);
+  float sy;
+  {
+    float y[16], vh[16], part[16];
+    ld(cY, y);
+    ld_row16(sm + offVh, f, t0, vh);
+    const float iy = 1.f / (sl * sdu), ivh = 1.f / svh;
+    float mx = 0.f, old[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) old[t] = dv[(row0 + t0 + t) * D + f];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      y[t] *= iy;
+      mx = fmaxf(mx, fabsf(y[t]));
+      part[t] = y[t] * vh[t] * ivh;
+      dv[(row0 + t0 + t) * D + f] = old[t] + sB[t0 + t] * y[t];
+    }
+    add_tokens(part, sdB, t0);
+    sy = block_scale<NTH>(mx, red);
+#pragma unroll
+    for (int t = 0; t < 16; ++t) *(half*)(sm + offYO + swz(t0 + t, f)) = __float2half_rn(y[t] * sy);
+  }
+  phase_end();
+  // [Y; dO] U^T: lanes 0-63 Y U^T (with K K^T from the first phase), lanes
+  // 64-127 dP = dO U^T (with Q K^T)
+  issue(4, [&] {
+    for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tm + cYO, kmaj(sYO, 0, kk), mnmaj(sU, kk), ID_KM, kk > 0);
+  });
+  wait(4);
+  float sa, spm;
+  {
+    float x1[16], x2[16], cs[16], o[16];
+    ld(cYO, x1);
+    ld(cKQ, x2);
+    float rs = 0.f, bs = 0.f, mx = 0.f;
+    if (f < C) {  // row j = f: dL = -strict_lower(Y U^T), A = R . K K^T, dA = diag(beta) dL, A~ = dA . R
+      const int j = f;
+      const float iyu = 1.f / (sy * su), ikk = 1.f / (sk * sk);
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const int jj = t0 + t;
+        cs[t] = 0.f;
+        o[t] = 0.f;
+        if (jj < j) {
+          const float r = __expf(sG[j] - sG[jj]);
+          const float A = r * x2[t] * ikk;
+          const float dL = -x1[t] * iyu;
+          const float dA = sB[j] * dL;
+          const float x = dA * A;
+          rs += x;
+          bs += dL * A;
+          cs[t] = -x;
+          o[t] = dA * r;
+        }
+        mx = fmaxf(mx, fabsf(o[t]));
+      }
+      atomicAdd(sdB + j, bs);
+    } else {  // row i = f - 64: dP = lower(dO U^T), P = R . Q~ K^T: dP . R; dG from dP . P
+      const int i = f - C;
+      const float iou = 1.f / (so * su), iqk = scale / (sq * sk);
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const int jj = t0 + t;
+        cs[t] = 0.f;
+        o[t] = 0.f;
+        if (jj <= i) {
+          const float r = __expf(sG[i] - sG[jj]);
+          const float dP = x1[t] * iou;
+          const float x = dP * (r * x2[t] * iqk);
+          rs += x;
+          cs[t] = -x;
+          o[t] = dP * r;
+        }
+        mx = fmaxf(mx, fabsf(o[t]));
+      }
+    }
+    atomicAdd(sdG + (f & (C - 1)), rs);
+    add_tokens(cs, sdG, t0);
+    float m2[2] = {f < C ? mx : 0.f, f < C ? 0.f : mx}, s2[2];
+    block_scalesN<2, NTH>(m2, red, s2);
+    sa = s2[0];
+    spm = s2[1];
+    if (f < C)
+      st_row16(sm + offA, f, t0, o, sa);
+    else
+      st_row16(sm + offP, f - C, t0, o, spm);  // P was last read by the dU products
+  }
+  phase_end();
+  // dq^T: (dP . R) K;  dk^T: U dS_C, Y S0, (dP . R)^T Q~, (A~ + A~^T) K
+  issue(5, [&] {
+    for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(tm + cDqB, mnmaj(sKQ, kk), kmaj(sP, 0, kk), ID_MK, kk > 0);
+    if (committed)
+      for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tm + cDka, kmaj(sT, 0, kk), mnmaj(sU, kk), ID_KM, kk > 0);
+    for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tm + cDkb, kmaj(sS, 0, kk), kmaj(sYO, 0, kk), ID_KK, kk > 0);
+    for (int kk = 0; kk < 4; ++kk)
+      tc::mma_bf16(tm + cDkc, mnmaj(sKQ + C * 128, kk), mnmaj(sP, kk), ID_MM, kk > 0);
+    for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(tm + cDkd, mnmaj(sKQ, kk), kmaj(sA, 0, kk), ID_MK, kk > 0);
+    for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(tm + cDkd, mnmaj(sKQ, kk), mnmaj(sA, kk), ID_MM, 1);
+  });
+  wait(5);
+  {  // dq += scale diag(gamma) dO S0 + scale (dP . R) K
+    float a[16], b[16], old[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) old[t] = dq[(row0 + t0 + t) * D + f];
+    ld(cDqA, a);
+    ld(cDqB, b);
+    const float ios = scale / (so * ss), f2 = scale / (spm * sk);
+#pragma unroll
+    for (int t = 0; t < 16; ++t) dq[(row0 + t0 + t) * D + f] = old[t] + sGam[t0 + t] * a[t] * ios + b[t] * f2;
+  }
+  {  // dk; dG_j -= (U dS_C)_j . K~_j and gamma_j beta_j (Y S0)_j . k_j; the
+     // last token gains sum_j (U dS_C)_j . K~_j
+    float acc[16], x[16], part[16], old[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) old[t] = dk[(row0 + t0 + t) * D + f];
+    const float ik = 1.f / sk;
+    float kf[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) kf[t] = elem(sm + offKQ, t0 + t, f) * ik, part[t] = 0.f;
+    float tot = 0.f;
+    if (committed) {
+      ld(cDka, x);
+      const float iud = 1.f / (su * sd);
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const float xa = gC / sGam[t0 + t] * x[t] * iud;
+        acc[t] = xa;
+        part[t] -= xa * kf[t];
+        tot += xa * kf[t];
+      }
+    } else {
+#pragma unroll
+      for (int t = 0; t < 16; ++t) acc[t] = 0.f;
+    }
+    ld(cDkb, x);
+    const float iys = 1.f / (sy * ss);
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      const float xb = sGam[t0 + t] * sB[t0 + t] * x[t] * iys;
+      acc[t] -= xb;
+      part[t] -= xb * kf[t];
+    }
+    ld(cDkc, x);
+    const float f1 = scale / (spm * sq);
+#pragma unroll
+    for (int t = 0; t < 16; ++t) acc[t] += f1 * x[t];
+    ld(cDkd, x);
+    const float fa = 1.f / (sa * sk);
+#pragma unroll
+    for (int t = 0; t < 16; ++t) dk[(row0 + t0 + t) * D + f] = old[t] + acc[t] + fa * x[t];
+    add_tokens(part, sdG, t0);
+    tot = warp_sum(tot);
+    if (lane == 0) atomicAdd(red + 126, tot);
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (tid == 0) sdG[C - 1] += red[126] + gC * red[127];
+  __syncthreads();
+  if (warp == 0) {  // dg = reverse cumulative sum of dG over the chunk
+    const float a0 = sdG[2 * lane], a1 = sdG[2 * lane + 1];
+    float s = a0 + a1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_down_sync(0xffffffffu, s, o);
+      if (lane + o < 32) s += y;
+    }
+    const float after = s - a0 - a1;  // s: the sum over lanes >= this one
+    dg[row0 + 2 * lane + 1] = a1 + after;
+    dg[row0 + 2 * lane] = a0 + a1 + after;
+    tc::fence_after();
+    tc::tmem_dealloc(tm, 512);
+  }
+  if (tid < C) dbeta[row0 + tid] = sdB[tid];
+}
+
 template <int D>
 cudaError_t set_attributes() {
   static const cudaError_t attr = [] {
@@ -1074,6 +1628,8 @@ cudaError_t set_attributes() {
     if (r == cudaSuccess)
       r = cudaFuncSetAttribute(gdn_bwd_fused_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                FusedSm<D>::kBytes);
+    if (r == cudaSuccess && D == 128)
+      r = cudaFuncSetAttribute(gdn_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tcb::kBytes);
     return r;
   }();
   return attr;
@@ -1095,9 +1651,15 @@ cudaError_t run_factors(const Problem& p, const void* q, const void* k, const fl
 template <int D>
 cudaError_t run_products(const Problem& p, const void* q, const void* k, const void* v, const float* g,
                          const float* beta, const uint8_t* sel, const float* dO, const GdnBwdScratch& w, float* dq,
-                         float* dk, float* dv, float* dg, float* dbeta, cudaStream_t st) {
+                         float* dk, float* dv, float* dg, float* dbeta, int* err, cudaStream_t st) {
   cudaError_t e = set_attributes<D>();
   if (e != cudaSuccess) return e;
+  if constexpr (D == 128) {  // on tcgen05
+    gdn_bwd_tc_kernel<<<(unsigned)(p.BH * p.N), tcb::NTH, tcb::kBytes, st>>>(
+        (const bf16*)q, (const bf16*)k, (const bf16*)v, dO, w.S0, w.dSC, w.Li, w.P, w.G, beta, sel, p.L, p.N,
+        p.scale, dq, dk, dv, dg, dbeta, err);
+    return cudaGetLastError();
+  }
   gdn_bwd_fused_kernel<D><<<(unsigned)(p.BH * p.N), 512, FusedSm<D>::kBytes, st>>>(
       (const bf16*)q, (const bf16*)k, (const bf16*)v, dO, w.S0, w.dSC, w.Li, w.P, w.G, beta, sel, p.L, p.N, p.scale,
       dq, dk, dv, dg, dbeta);
@@ -1116,10 +1678,11 @@ cudaError_t launch_gdn_bwd_factors(const Problem& p, const void* q, const void* 
 
 cudaError_t launch_gdn_bwd_products(const Problem& p, const void* q, const void* k, const void* v, const float* g,
                                     const float* beta, const uint8_t* sel, const float* dO, const GdnBwdScratch& w,
-                                    float* dq, float* dk, float* dv, float* dg, float* dbeta, cudaStream_t st) {
+                                    float* dq, float* dk, float* dv, float* dg, float* dbeta, int* err,
+                                    cudaStream_t st) {
   if (p.BH == 0 || p.N == 0) return cudaSuccess;
-  return p.d == 64 ? run_products<64>(p, q, k, v, g, beta, sel, dO, w, dq, dk, dv, dg, dbeta, st)
-                   : run_products<128>(p, q, k, v, g, beta, sel, dO, w, dq, dk, dv, dg, dbeta, st);
+  return p.d == 64 ? run_products<64>(p, q, k, v, g, beta, sel, dO, w, dq, dk, dv, dg, dbeta, err, st)
+                   : run_products<128>(p, q, k, v, g, beta, sel, dO, w, dq, dk, dv, dg, dbeta, err, st);
 }
 
 }  // namespace nats

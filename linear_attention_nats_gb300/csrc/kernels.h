@@ -100,11 +100,13 @@ cudaError_t launch_gdn_bwd_factors(const Problem& p, const void* q, const void* 
                                    const float* beta, const uint8_t* sel, const float* dO, const GdnBwdScratch& w,
                                    cudaStream_t st);
 // every per-chunk product of the adjoint, after the factors, the reverse
-// scan and the chunk-start states S0 (one kernel; dq, dk, dv accumulate, dg
-// and dbeta are overwritten)
+// scan and the chunk-start states S0 (one kernel, on tcgen05 for d = 128;
+// dq, dk, dv accumulate, dg and dbeta are overwritten; err[0] is set if a
+// bounded wait expires)
 cudaError_t launch_gdn_bwd_products(const Problem& p, const void* q, const void* k, const void* v, const float* g,
                                     const float* beta, const uint8_t* sel, const float* dO, const GdnBwdScratch& w,
-                                    float* dq, float* dk, float* dv, float* dg, float* dbeta, cudaStream_t st);
+                                    float* dq, float* dk, float* dv, float* dg, float* dbeta, int* err,
+                                    cudaStream_t st);
 
 // Softmax branch of the backward pass on tcgen05 (softmax_bwd_tc.cu), bf16
 // layers: lse (fp32 [BH, L], exp2 domain) and dq (+=), then dk, dv (=); the
