@@ -1198,7 +1198,8 @@ __global__ void __launch_bounds__(tcb::NTH, 1) gdn_bwd_tc_kernel(
     const float* __restrict__ S0, const float* __restrict__ dSC, const float* __restrict__ Li,
     const float* __restrict__ Pg, const float* __restrict__ Gb, const float* __restrict__ beta,
     const uint8_t* __restrict__ sel, int L, int N, float scale, float* __restrict__ dq, float* __restrict__ dk,
-    float* __restrict__ dv, float* __restrict__ dg, float* __restrict__ dbeta, int* __restrict__ err) {
+    float* __restrict__ dv, float* __restrict__ dg, float* __restrict__ dbeta, int* __restrict__ err,
+    long long nchunks, int ahead) {
   using namespace tcb;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -1226,6 +1227,11 @@ __global__ void __launch_bounds__(tcb::NTH, 1) gdn_bwd_tc_kernel(
   if (tid == 96) prefetch_l2(dv + row0 * D, C * D * 4);
   if (tid == 128) prefetch_l2(dq + row0 * D, C * D * 4);
   if (tid == 160) prefetch_l2(dk + row0 * D, C * D * 4);
+  // and the states of the chunk `ahead` CTAs later (about one SM count: the
+  // CTA that starts when one of the running ones ends)
+  if (tid == 192 && chunk + ahead < nchunks) prefetch_l2(S0 + (size_t)(chunk + ahead) * D * D, D * D * 4);
+  if (tid == 224 && chunk + ahead < nchunks && sel[chunk + ahead] != 0 && (chunk + ahead) % N < N - 1)
+    prefetch_l2(dSC + (size_t)(chunk + ahead) * D * D, D * D * 4);
   if (warp == 0) {
     tc::tmem_alloc(tslot, 512);
     tc::tmem_relinquish();
@@ -1655,9 +1661,12 @@ cudaError_t run_products(const Problem& p, const void* q, const void* k, const v
   cudaError_t e = set_attributes<D>();
   if (e != cudaSuccess) return e;
   if constexpr (D == 128) {  // on tcgen05
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     gdn_bwd_tc_kernel<<<(unsigned)(p.BH * p.N), tcb::NTH, tcb::kBytes, st>>>(
         (const bf16*)q, (const bf16*)k, (const bf16*)v, dO, w.S0, w.dSC, w.Li, w.P, w.G, beta, sel, p.L, p.N,
-        p.scale, dq, dk, dv, dg, dbeta, err);
+        p.scale, dq, dk, dv, dg, dbeta, err, p.BH * p.N, sms);
     return cudaGetLastError();
   }
   gdn_bwd_fused_kernel<D><<<(unsigned)(p.BH * p.N), 512, FusedSm<D>::kBytes, st>>>(
