@@ -866,22 +866,27 @@ def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):
     """Times nats_hybrid_bwd on the layer workload: the gradients of a seeded
     dout at the forward's selection, from the activations the CUDA forward
     saved (one forward outside the timed region).  Its stages are timed with
-    the library's own stage events and set against the roofline of their
-    own kind of work:
-      merge_bwd    HBM: per token it reads q, dout (bf16) and o_soft, o_lin
-                   (fp32) and writes d o_soft (bf16), d o_lin, dq (fp32) and
-                   delta: 22 d + 4 bytes;
-      softmax_bwd  bf16 tensor (tcgen05): 10 d FLOP per visible (query,
-                   key) pair (scores recomputed, dP, dq, dk, dv), plus the
-                   compaction of the softmax-chunk lists;
-      gdn_bwd      the Gated DeltaNet stage and the per-chunk C x C stage
-                   together, fp16 / bf16 tensor: per chunk the forward's chunk
-                   factors and scan that recompute the chunk start states
-                   (5 C^2 d + 6 C d^2 FLOP, the forward's count, on tcgen05)
-                   and the chunkwise adjoint's products, 2 (8 C d^2 + 15 C^2 d)
-                   FLOP (full tiles; rolled-back chunks skip some; fp16
-                   operands, fp32 accumulation, warp-level mma.sync m16n8k16),
-                   against the bf16 peak (the fp16 dense rate is the same).
+    the library's own stage events (softmax_bwd on the caller's stream and
+    gdn_bwd on the library's second stream run side by side, so their times
+    overlap and the shares add up to more than one) and set against the
+    roofline of their own kind of work:
+      merge_bwd     HBM: per token it reads q, dout (bf16) and o_soft, o_lin
+                    (fp32) and writes d o_soft (bf16), d o_lin, dq (fp32) and
+                    delta: 22 d + 4 bytes;
+      softmax_bwd   bf16 tensor (tcgen05): 10 d FLOP per visible (query,
+                    key) pair (scores recomputed, dP, dq, dk, dv), plus the
+                    compaction of the softmax-chunk lists;
+      gdn_bwd       bf16 / fp16 tensor: per chunk the forward's chunk factors
+                    and scan that recompute the chunk start states (5 C^2 d +
+                    6 C d^2 FLOP, the forward's count, on tcgen05), the
+                    adjoint's chunk factors (2 x 4 C^2 d) and reverse scan
+                    (2 x 3 C d^2; warp-level mma.sync, fp16 operands);
+      gdn_products  HBM: the adjoint's per-chunk products in one kernel (on
+                    tcgen05 for d = 128) read S0 and dS_C (fp32 d x d each),
+                    q, k, v (bf16), dO (fp32), Linv and P (fp32 C x C),
+                    update dq, dk, dv (fp32) and write dg, dbeta: 8 d^2 +
+                    34 C d + 8 C^2 + 8 C bytes per chunk (its 2 (5 C d^2 +
+                    10 C^2 d) FLOP are a few percent of the tensor peak).
     The headline roofline is the stage with the largest share of the time."""
     import torch
 
@@ -941,8 +946,10 @@ def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):
     chunks = B * H * (L // Cc)
     amounts = {"merge_bwd": ("hbm", (22 * d + 4) * tokens, stage_ms["merge_bwd"]),
                "softmax_bwd": ("tensor", 10 * d * pairs, stage_ms["softmax_bwd"]),
-               "gdn_bwd": ("tensor", chunks * (5 * Cc * Cc * d + 6 * Cc * d * d + 2 * (8 * Cc * d * d + 15 * Cc * Cc * d)),
-                           stage_ms["gdn_bwd"] + stage_ms["combine"])}
+               "gdn_bwd": ("tensor", chunks * (5 * Cc * Cc * d + 6 * Cc * d * d + 2 * (4 * Cc * Cc * d + 3 * Cc * d * d)),
+                           stage_ms["gdn_bwd"]),
+               "gdn_products": ("hbm", chunks * (8 * d * d + 34 * Cc * d + 8 * Cc * Cc + 8 * Cc),
+                                stage_ms["gdn_products"])}
     per = {}
     for name, (bound, amount, sms) in amounts.items():
         if bound == "hbm":
@@ -950,7 +957,7 @@ def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):
         else:
             ach, peak, unit = amount / (sms / 1e3) / 1e12, pk["bf16_tflops_sustained"], "TFLOP/s"
             src = f"{pk['source']} bf16 sustained" + (" (tcgen05)" if name == "softmax_bwd" else
-                                                      " (tcgen05 recompute; fp16 mma.sync adjoint)")
+                                                      " (tcgen05 recompute; fp16 mma.sync adjoint factors and scan)")
         per[name] = {"bound": bound, "ms": sms, "share": sms / ms if ms else None, "achieved": ach, "peak": peak,
                      "unit": unit, "frac": (ach / peak) if peak else None, "peak_source": src,
                      ("bytes_per_step" if bound == "hbm" else "flops_per_step"): amount}
@@ -959,6 +966,7 @@ def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):
                     "forward's selection, same workload as the forward",
             "value": job_throughput(B * L, world, ms), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
             "launches_per_step": int(profs[0].launches), "stages_ms": stage_ms,
+            "stages_overlap": "softmax_bwd (caller's stream) and gdn_bwd (second stream) run side by side",
             "stages": per, "clocks": clk,
             "roofline": {"kernel": top, **{k: per[top][k] for k in ("bound", "achieved", "peak", "unit", "frac",
                                                                    "peak_source")}}}

@@ -430,11 +430,12 @@ nats_status nats_hybrid_bwd(const nats_dims* dims, const void* q, const void* k,
 typedef enum {
   NATS_BWD_STAGE_MERGE = 0,   /* RMSNorm + gated merge backward: branch output gradients, dW_g, db_g, dnorm_w */
   NATS_BWD_STAGE_SOFTMAX = 1, /* softmax branch: dq, then dk / dv (bf16: tcgen05) */
-  NATS_BWD_STAGE_GDN = 2,     /* Gated DeltaNet: bf16, the chunk-start states' recompute (on the
-                                 side stream, from its fork) and the chunkwise adjoint's factors,
-                                 reverse scan and state products; fp32, the token-serial adjoint */
-  NATS_BWD_STAGE_COMBINE = 3, /* bf16: the adjoint's C x C products, dq, dk, dg, dbeta; fp32: the
-                                 per-token sums of the adjoint's state halves */
+  NATS_BWD_STAGE_GDN = 2,     /* Gated DeltaNet: bf16, the chunk-start states' recompute and the
+                                 chunkwise adjoint's factors and reverse scan (on the side stream,
+                                 beside the softmax stage); fp32, the token-serial adjoint */
+  NATS_BWD_STAGE_COMBINE = 3, /* bf16: every per-chunk product of the adjoint (one kernel: dq, dk,
+                                 dv, dg, dbeta); fp32: the per-token sums of the adjoint's state
+                                 halves */
   NATS_BWD_NUM_STAGES = 4
 } nats_bwd_stage;
 

@@ -38,7 +38,7 @@ NOALLOC_SCRATCH_BYTES = 64 << 20
 
 NUM_STAGES = 8
 STAGES = ("score", "compact", "softmax", "gdn_prep", "gdn_scan", "merge", "proj_in", "proj_out")
-BWD_STAGES = ("merge_bwd", "softmax_bwd", "gdn_bwd", "combine")
+BWD_STAGES = ("merge_bwd", "softmax_bwd", "gdn_bwd", "gdn_products")
 
 
 class Profile(ctypes.Structure):
