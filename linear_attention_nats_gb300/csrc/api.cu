@@ -278,11 +278,11 @@ nats_status nats_hybrid_fwd_streams(const nats_dims* dims, const void* q, const 
     if (p.d == 128)
       NATS_STAGE(stg, NATS_STAGE_GDN_PREP, 1,
                  launch_gdn_prep_tc(p, q, k, v, g, beta, w_g, b_g, ws.G, ws.W, ws.U, ws.P, ws.gate, w_s, b_s,
-                                    score_dst, ws.err, st));
+                                    score_dst, ws.err, nullptr, st));
     else
       NATS_STAGE(stg, NATS_STAGE_GDN_PREP, 1,
                  launch_gdn_prep_mma(p, q, k, v, g, beta, w_g, b_g, ws.G, ws.W, ws.U, ws.P, ws.gate, w_s, b_s,
-                                     score_dst, st));
+                                     score_dst, nullptr, st));
   }
   // 3. compacted softmax-chunk lists (mirrors an overridden selection to sel_out)
   NATS_STAGE(stg, NATS_STAGE_COMPACT, 1,

@@ -804,12 +804,13 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
       auto states_and_factors = [&]() -> cudaError_t {
         cudaError_t e3 = mark_on(ev_start, NATS_BWD_STAGE_GDN, ss);
         // the chunk-start states, from the forward's chunk factors and scan
-        // (the same kernels as the forward; the selection is given)
+        // (the same kernels as the forward; the selection is given), and
+        // every chunk's Linv = (I + diag(beta) A)^{-1} in fp32 on the way
         if (e3 == cudaSuccess)
           e3 = D == 128 ? launch_gdn_prep_tc(p, q, k, v, g, beta, w_g, b_g, lay.fG, lay.fW, lay.fU, lay.fP,
-                                             lay.fgate, nullptr, nullptr, nullptr, lay.ferr, ss)
+                                             lay.fgate, nullptr, nullptr, nullptr, lay.ferr, lay.cw.Li, ss)
                         : launch_gdn_prep_mma(p, q, k, v, g, beta, w_g, b_g, lay.fG, lay.fW, lay.fU, lay.fP,
-                                              lay.fgate, nullptr, nullptr, nullptr, ss);
+                                              lay.fgate, nullptr, nullptr, nullptr, lay.cw.Li, ss);
         if (e3 == cudaSuccess)
           e3 = launch_gdn_scan_tc(p, q, k, sel, lay.fG, lay.fW, lay.fU, lay.fP, nullptr, lay.fol16, nullptr,
                                   lay.ferr, ss, lay.cw.S0);

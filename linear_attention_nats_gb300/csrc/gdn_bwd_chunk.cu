@@ -30,7 +30,8 @@
 // Kernels (after the forward scan has written every chunk's S0; S0 and
 // dS_C are stored transposed, [dk][dv], so that both scans write them as
 // whole lines):
-//   gdn_bwd_prep_kernel   per chunk: G, Linv, P (fp32), W, Q_eff, K~ (fp16, scaled)
+//   gdn_bwd_prep_kernel   per chunk: G, P (fp32), W, Q_eff, K~ (fp16, scaled), from
+//                         Linv as the forward's chunk-factor kernel stores it
 //   gdn_bwd_scan_kernel   per (b, h, 64 state rows): the reverse scan, writing
 //                         dS_C of every committed chunk (fp32)
 //   gdn_bwd_fused_kernel  per chunk, every product above: Vh, U, dU, Y, the
@@ -41,8 +42,7 @@
 // own power of two so that its largest entry sits below 2^15 (fp16 range is
 // never exceeded, its 11-bit precision matches tf32); the reverse scan keeps
 // its state gradient in fp32 and converts it per step.
-// The triangular inverse is a forward substitution on the CUDA cores.  The
-// chunk-factor and scan kernels have 8 warps, the fused kernel 16; a C x D
+// The chunk-factor and scan kernels have 8 warps, the fused kernel 16; a C x D
 // output is split into 16-row strips (warp w & 3) and column halves (8
 // warps) or quarters (16 warps) (warp w >> 2).
 #include <cuda_fp16.h>
@@ -55,7 +55,6 @@ namespace nats {
 namespace {
 
 constexpr int C = kChunk;
-constexpr int CS = C + 4;  // fp32 row stride of C x C tiles
 using bf16 = __nv_bfloat16;
 
 template <int NT>
@@ -409,17 +408,17 @@ struct PrepSm {
   static constexpr int offW = offK + H<D>::bytes(C);
   static constexpr int offL = offW + H<D>::bytes(C);          // fp16 [C][C + 8]: Linv diag(beta gamma)
   static constexpr int offPh = offL + H<C>::bytes(C);         // fp16 [C][C + 8]: P
-  static constexpr int offA = offPh + H<C>::bytes(C);         // fp32 [C][CS]: beta A
-  static constexpr int offLi = offA + C * CS * 4;             // fp32 [C][CS]: Linv
-  static constexpr int offV = offLi + C * CS * 4;             // G, gamma, beta, reduction
+  static constexpr int offV = offPh + H<C>::bytes(C);         // G, gamma, beta, reduction
   static constexpr int kBytes = offV + 3 * C * 4 + 64;
 };
 
+// Linv comes from the forward's chunk-factor kernel (rerun for the
+// chunk-start states), which forms it by its blocked inverse.
 template <int D>
 __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k,
                                                            const float* __restrict__ g,
                                                            const float* __restrict__ beta, int L, int N, float scale,
-                                                           float* __restrict__ Gb, float* __restrict__ Li_out,
+                                                           float* __restrict__ Gb, const float* __restrict__ Li,
                                                            float* __restrict__ P_out, half* __restrict__ W16,
                                                            half* __restrict__ Qe16, half* __restrict__ Kt16,
                                                            float* __restrict__ sc_out) {
@@ -431,8 +430,6 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
   half* hW = (half*)(sm + S::offW);
   half* hL = (half*)(sm + S::offL);
   half* hP = (half*)(sm + S::offPh);
-  float* sA = (float*)(sm + S::offA);
-  float* sLi = (float*)(sm + S::offLi);
   float* sG = (float*)(sm + S::offV);
   float* sGam = sG + C;
   float* sB = sGam + C;
@@ -465,20 +462,18 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
     tq.store(hQ, sq);
     tk.store(hK, sk);
   }
+  // Linv diag(beta gamma) (the W product's operand)
+  const float sl = tile_h<C, C>(Li + (size_t)chunk * C * C, C, hL, red,
+                                [&](int, int m, float x) { return x * sB[m] * sGam[m]; });
   __syncthreads();
-  // beta A (strictly lower) and P (lower, diagonal included)
+  // P (lower, diagonal included)
   float sp;
   {
     const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);
-    float kk[4][4], qk[4][4];
-    zero(kk);
+    float qk[4][4];
     zero(qk);
-    hmm<4, D, false, false>(kk, m0, n0, hK, LD, hK, LD);
     hmm<4, D, false, false>(qk, m0, n0, hQ, LD, hK, LD);
-    const float ikk = 1.f / (sk * sk), iqk = scale / (sq * sk);
-    each(kk, m0, n0, [&](int i, int j, float v, int, int) {
-      sA[i * CS + j] = j < i ? sB[i] * __expf(sG[i] - sG[j]) * v * ikk : 0.f;
-    });
+    const float iqk = scale / (sq * sk);
     each_mut(qk, m0, n0, [&](int i, int j, float v, int, int) {
       return j <= i ? __expf(sG[i] - sG[j]) * v * iqk : 0.f;
     });
@@ -494,32 +489,6 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
     }
     sp = acc_h<4, C>(qk, m0, n0, hP, red);
   }
-  __syncthreads();
-  // Linv = (I + beta A)^{-1} by forward substitution, one column per thread;
-  // each row's sum runs in four independent partial sums (short chains)
-  if (tid < C) {
-    const int j = tid;
-    float x[C];
-#pragma unroll
-    for (int i = 0; i < C; ++i) {
-      float s4[4] = {i == j ? 1.f : 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int m4 = 0; m4 < i / 4; ++m4) {
-        const float4 a = *(const float4*)(sA + i * CS + 4 * m4);
-        s4[0] = fmaf(-a.x, x[4 * m4], s4[0]);
-        s4[1] = fmaf(-a.y, x[4 * m4 + 1], s4[1]);
-        s4[2] = fmaf(-a.z, x[4 * m4 + 2], s4[2]);
-        s4[3] = fmaf(-a.w, x[4 * m4 + 3], s4[3]);
-      }
-#pragma unroll
-      for (int m = (i / 4) * 4; m < i; ++m) s4[m & 3] = fmaf(-sA[i * CS + m], x[m], s4[m & 3]);
-      x[i] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-    }
-#pragma unroll
-    for (int i = 0; i < C; ++i) sLi[i * CS + j] = x[i];
-  }
-  __syncthreads();
-  const float sl = tile_h<C, C>(sLi, CS, hL, red, [&](int, int m, float x) { return x * sB[m] * sGam[m]; });
   __syncthreads();
   const int m0 = 16 * (warp & 3), n0 = (warp >> 2) * (D / 2);
   // W = Linv diag(beta gamma) K
@@ -570,11 +539,6 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
       sc_out[chunk * 4 + 1] = sqe;
       sc_out[chunk * 4 + 2] = sk;
     }
-  }
-  // Linv for the per-chunk gradient kernels (P was written above)
-  for (int x = tid; x < C * C / 4; x += 256) {
-    const int i = x / (C / 4), j4 = x % (C / 4);
-    *(float4*)(Li_out + (size_t)chunk * C * C + i * C + 4 * j4) = *(const float4*)(sLi + i * CS + 4 * j4);
   }
 }
 

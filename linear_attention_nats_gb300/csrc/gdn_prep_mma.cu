@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(256, 2) gdn_prep_mma_kernel(
     int N, float scale, float* __restrict__ Gout, __nv_bfloat16* __restrict__ Wout,
     __nv_bfloat16* __restrict__ Uout, __nv_bfloat16* __restrict__ Pout, const float* __restrict__ w_g, const float* __restrict__ b_g, int H,
     float* __restrict__ gate_out, const float* __restrict__ w_s, const float* __restrict__ b_s,
-    uint8_t* __restrict__ sel_out) {
+    uint8_t* __restrict__ sel_out, float* __restrict__ T_out) {
   using S = PrepSmem<D>;
   constexpr int RS = S::RS, TS = S::TS, FS = S::FS;
   constexpr int NT = 256;
@@ -408,6 +408,11 @@ __global__ void __launch_bounds__(256, 2) gdn_prep_mma_kernel(
       for (int x = 0; x < 4; ++x)
         o32[x] = pack2(j0 + 2 * x <= t ? v8[2 * x] : 0.f, j0 + 2 * x + 1 <= t ? v8[2 * x + 1] : 0.f);
       *(uint4*)(Tb + t * TS + j0) = o;
+      if (T_out) {  // T in fp32 for the backward pass
+        float* dst = T_out + (size_t)blk * C * C + t * C + j0;
+#pragma unroll
+        for (int x = 0; x < 8; ++x) dst[x] = j0 + x <= t ? v8[x] : 0.f;
+      }
     }
   }
   __syncthreads();
@@ -482,7 +487,7 @@ __global__ void __launch_bounds__(256, 2) gdn_prep_mma_kernel(
 cudaError_t launch_gdn_prep_mma(const Problem& p, const void* q, const void* k, const void* v, const float* g,
                                 const float* beta, const float* w_g, const float* b_g, float* G, void* W16,
                                 void* U16, void* P16, float* gate, const float* w_s, const float* b_s,
-                                uint8_t* sel_out, cudaStream_t st) {
+                                uint8_t* sel_out, float* T_out, cudaStream_t st) {
   if (p.BH == 0 || p.N == 0) return cudaSuccess;
   auto run = [&](auto kern, int smem) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -490,7 +495,7 @@ cudaError_t launch_gdn_prep_mma(const Problem& p, const void* q, const void* k, 
     kern<<<(unsigned)(p.BH * p.N), 256, smem, st>>>(
         (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, g, beta, p.L, p.N, p.scale,
         G, (__nv_bfloat16*)W16, (__nv_bfloat16*)U16, (__nv_bfloat16*)P16, w_g, b_g, p.H, gate, w_s, b_s,
-        sel_out);
+        sel_out, T_out);
     return cudaGetLastError();
   };
   // d = 128 takes the tcgen05 pipeline (gdn_prep_tc.cu)

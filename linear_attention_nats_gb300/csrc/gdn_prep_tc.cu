@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const float* __restrict__ g, const float* __restrict__ beta, int L, int N, int H,
                        long long nchunks, float scale, float* __restrict__ Gout, const float* __restrict__ w_g, const float* __restrict__ b_g, float* __restrict__ gate_out,
                        const float* __restrict__ w_s, const float* __restrict__ b_s, uint8_t* __restrict__ sel_out,
-                       int* __restrict__ err) {
+                       int* __restrict__ err, float* __restrict__ T_out) {
   using S = PrepTcSmem;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -549,6 +549,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bars[B_TBF + j]);
+      if (T_out) {  // T in fp32 for the backward pass (zero above the diagonal blocks)
+        named_barrier(kBarInv, 128);
+        float* dst = T_out + (size_t)(blockIdx.x + i * stride) * C * C;
+        for (int e4 = gi; e4 < C * C / 4; e4 += 128) {
+          const int t = e4 / (C / 4), c4 = 4 * (e4 % (C / 4));
+          const float4 x = c4 < 16 * (t / 16 + 1) ? *(const float4*)(Ts + t * FS + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          *(float4*)(dst + t * C + c4) = x;
+        }
+      }
     }
   } else if (warp >= kWarpEpi) {
     // ----------------------------- A (fp32, shared) and P (bf16) from TMEM
@@ -734,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_gdn_prep_tc(const Problem& p, const void* q, const void* k, const void* v, const float* g,
                                const float* beta, const float* w_g, const float* b_g, float* G, void* W16,
                                void* U16, void* P16, float* gate, const float* w_s, const float* b_s,
-                               uint8_t* sel_out, int* err, cudaStream_t st) {
+                               uint8_t* sel_out, int* err, float* T_out, cudaStream_t st) {
   if (p.BH == 0 || p.N == 0) return cudaSuccess;
   if (p.d != D) return cudaErrorInvalidValue;
   CUtensorMap mk, mq, mv, mw, mu, mp;
@@ -752,7 +761,7 @@ cudaError_t launch_gdn_prep_tc(const Problem& p, const void* q, const void* k, c
   const long long nchunks = p.BH * p.N;
   const unsigned grid = (unsigned)(nchunks < sms ? nchunks : sms);
   gdn_prep_tc_kernel<<<grid, kThreads, smem, st>>>(mk, mq, mv, mw, mu, mp, g, beta, p.L, p.N, p.H, nchunks,
-                                                   p.scale, G, w_g, b_g, gate, w_s, b_s, sel_out, err);
+                                                   p.scale, G, w_g, b_g, gate, w_s, b_s, sel_out, err, T_out);
   return cudaGetLastError();
 }
 

@@ -32,18 +32,20 @@ cudaError_t launch_gdn_scan_simt(const Problem& p, int dtype, const void* q, con
                                  const uint8_t* sel, const Workspace& ws, float* o_l,
                                  float* state_out, cudaStream_t st);
 
-// bf16 chunk factors of the Gated DeltaNet branch plus the per-token merge gate.
+// bf16 chunk factors of the Gated DeltaNet branch plus the per-token merge
+// gate; T_out (or null) receives T = (I + A)^{-1} of every chunk, fp32
+// [BH, N, C, C], zero above the diagonal.
 cudaError_t launch_gdn_prep_mma(const Problem& p, const void* q, const void* k, const void* v, const float* g,
                                 const float* beta, const float* w_g, const float* b_g, float* G, void* W16,
                                 void* U16, void* P16, float* gate, const float* w_s, const float* b_s,
-                                uint8_t* sel_out, cudaStream_t st);
+                                uint8_t* sel_out, float* T_out, cudaStream_t st);
 
 // The same factors (d = 128) from the persistent tcgen05 pipeline; err[0] is
 // set if one of its bounded waits expires.
 cudaError_t launch_gdn_prep_tc(const Problem& p, const void* q, const void* k, const void* v, const float* g,
                                const float* beta, const float* w_g, const float* b_g, float* G, void* W16,
                                void* U16, void* P16, float* gate, const float* w_s, const float* b_s,
-                               uint8_t* sel_out, int* err, cudaStream_t st);
+                               uint8_t* sel_out, int* err, float* T_out, cudaStream_t st);
 
 // bf16 chunk scan: o_l (fp32 [BH, L, dv]); state_out may be null; s0_out
 // (or null) receives every chunk's start state, fp32 [BH, N, dv, dk].
@@ -86,7 +88,7 @@ struct GdnBwdScratch {
   float* S0;    // [BH, N, dk, dv] chunk-start states, transposed (the forward recompute writes them)
   float* dSC;   // [BH, N, dk, dv] gradient of each committed chunk's end state, transposed
   float* G;     // [BH, L] in-chunk cumulative log-decay
-  float* Li;    // [BH, N, C, C] (I + diag(beta) A)^{-1}
+  float* Li;    // [BH, N, C, C] (I + diag(beta) A)^{-1} (the forward's chunk-factor kernel stores it)
   float* P;     // [BH, N, C, C] lower(e^{G_i - G_j} scale q_i . k_j)
   void* W16;    // [BH, L, dk] fp16: Linv diag(beta gamma) K  \  each times its chunk's
   void* Qe16;   // [BH, L, dk] fp16: diag(gamma) Q~ - P W      >  power-of-two scale
@@ -94,8 +96,8 @@ struct GdnBwdScratch {
   float* sc;    // [BH, N, 4] the scales of W, Q_eff, K~
 };
 // the adjoint's chunk factors and the reverse state-gradient scan (two
-// kernels; they read q, k, g, beta, the selection and dO, and write only the
-// scratch: G, Linv, P, W, Q_eff, K~, their scales and dS_C)
+// kernels; they read q, k, g, beta, the selection, dO and Linv, and write
+// only the scratch: G, P, W, Q_eff, K~, their scales and dS_C)
 cudaError_t launch_gdn_bwd_factors(const Problem& p, const void* q, const void* k, const float* g,
                                    const float* beta, const uint8_t* sel, const float* dO, const GdnBwdScratch& w,
                                    cudaStream_t st);
