@@ -865,7 +865,8 @@ def run_nha(args, rank, dev, stream, dist):
 def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):
     """Times nats_hybrid_bwd on the layer workload: the gradients of a seeded
     dout at the forward's selection, from the activations the CUDA forward
-    saved (one forward outside the timed region).  Its stages are timed with
+    saved (one forward outside the timed region, which also saves the softmax
+    rows' log-sum-exp for a bf16 layer).  Its stages are timed with
     the library's own stage events (softmax_bwd on the caller's stream and
     gdn_bwd on the library's second stream run side by side, so their times
     overlap and the shares add up to more than one) and set against the
@@ -874,8 +875,9 @@ def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):
                     (fp32) and writes d o_soft (bf16), d o_lin, dq (fp32) and
                     delta: 22 d + 4 bytes;
       softmax_bwd   bf16 tensor (tcgen05): 10 d FLOP per visible (query,
-                    key) pair (scores recomputed, dP, dq, dk, dv), plus the
-                    compaction of the softmax-chunk lists;
+                    key) pair (scores recomputed, dP, dq, dk, dv; the row
+                    log-sum-exp comes from the forward), plus the compaction
+                    of the softmax-chunk lists;
       gdn_bwd       bf16 / fp16 tensor: per chunk the forward's chunk factors
                     and scan that recompute the chunk start states (5 C^2 d +
                     6 C d^2 FLOP, the forward's count, on tcgen05), the
@@ -894,8 +896,9 @@ def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):
     from linear_attention_nats_gb300 import _native
 
     t = dv
+    tc_layer = t["q"].dtype == torch.bfloat16
     fwd = nats.hybrid_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_s"], t["b_s"], t["w_g"], t["b_g"],
-                          return_sel=True, return_branches=True, stream=stream)
+                          return_sel=True, return_branches=True, return_lse=tc_layer, stream=stream)
     gen_ = torch.Generator(device="cpu").manual_seed(43)
     dout = torch.randn((B, H, L, d), generator=gen_).to(t["q"].dtype).to(dev)
     dm = nats.dims(B, H, L, d, 0 if t["q"].dtype == torch.bfloat16 else 1)
@@ -904,7 +907,8 @@ def run_backward(args, dev, stream, dist, dv, B, H, L, d, work):
 
     def step(prof=None):
         return nats.hybrid_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_g"], t["b_g"], fwd["sel"],
-                               fwd["o_soft"], fwd["o_lin"], dout, workspace=ws, stream=stream, profile=prof)
+                               fwd["o_soft"], fwd["o_lin"], dout, workspace=ws, stream=stream, profile=prof,
+                               lse=fwd.get("lse"))
 
     steps = max(1, min(args.steps, 3))
     with torch.cuda.stream(stream):

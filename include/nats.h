@@ -252,17 +252,21 @@ typedef struct {
 } nats_streams;
 
 /* nats_hybrid_fwd_profiled with caller-owned concurrency (streams may be
- * NULL, which makes it identical to nats_hybrid_fwd_profiled).  Same
- * arguments, errors and results; NATS_ERR_NULL when streams->side is a
- * stream other than `stream` and fork or join is NULL; NATS_ERR_CUDA when
- * recording or waiting on them fails. */
+ * NULL, which makes it identical to nats_hybrid_fwd_profiled) and one more
+ * saved activation for training: lse_out (or NULL), fp32 [B, H, L], each
+ * token's log2 of the sum of 2^(s scale log2 e) over the keys its softmax
+ * branch sees (s the scores q . k), written for bf16 layers (NATS_ERR_DTYPE
+ * for fp32 ones); nats_hybrid_bwd_streams takes it to skip recomputing it.
+ * Same arguments, errors and results otherwise; NATS_ERR_NULL when
+ * streams->side is a stream other than `stream` and fork or join is NULL;
+ * NATS_ERR_CUDA when recording or waiting on them fails. */
 nats_status nats_hybrid_fwd_streams(const nats_dims* dims, const void* q, const void* k,
                                     const void* v, const float* g, const float* beta,
                                     const float* w_s, const float* b_s, const float* w_g,
                                     const float* b_g, const float* norm_w_soft,
                                     const float* norm_w_lin, const uint8_t* sel_in, void* out,
                                     uint8_t* sel_out, float* state_out, float* o_soft_out,
-                                    float* o_lin_out, void* workspace, size_t workspace_bytes,
+                                    float* o_lin_out, float* lse_out, void* workspace, size_t workspace_bytes,
                                     nats_stream_t stream, const nats_streams* streams,
                                     nats_profile* prof);
 
@@ -454,14 +458,17 @@ nats_status nats_hybrid_bwd_profiled(const nats_dims* dims, const void* q, const
  * nats_hybrid_fwd_streams: `streams` (or NULL: the library's per-device set)
  * gives the second stream and the fork / join events of the bf16 backward;
  * side NULL or equal to `stream` runs every kernel in order on `stream`.
- * Same arguments, errors and results; NATS_ERR_NULL when streams->side is a
- * stream other than `stream` and fork or join is NULL. */
+ * lse (or NULL; device, 16-byte aligned) is the forward's lse_out for the
+ * same inputs and selection: with it, a bf16 backward reads each token's row
+ * statistic instead of recomputing it from the scores (fp32 layers ignore
+ * it).  Same arguments, errors and results otherwise; NATS_ERR_NULL when
+ * streams->side is a stream other than `stream` and fork or join is NULL. */
 nats_status nats_hybrid_bwd_streams(const nats_dims* dims, const void* q, const void* k, const void* v,
                                     const float* g, const float* beta, const float* w_g, const float* b_g,
                                     const float* norm_w_soft, const float* norm_w_lin, const uint8_t* sel,
-                                    const float* o_soft, const float* o_lin, const void* dout, float* dq,
-                                    float* dk, float* dv, float* dg, float* dbeta, float* dw_g, float* db_g,
-                                    float* dnorm_w_soft, float* dnorm_w_lin, void* workspace,
+                                    const float* o_soft, const float* o_lin, const float* lse, const void* dout,
+                                    float* dq, float* dk, float* dv, float* dg, float* dbeta, float* dw_g,
+                                    float* db_g, float* dnorm_w_soft, float* dnorm_w_lin, void* workspace,
                                     size_t workspace_bytes, nats_stream_t stream, const nats_streams* streams,
                                     nats_profile* prof);
 

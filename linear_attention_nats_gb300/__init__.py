@@ -96,15 +96,17 @@ def _streams_of(side_stream):
 def hybrid_fwd(q, k, v, g, beta, w_s, b_s, w_g, b_g=None, *, norm_w_soft=None, norm_w_lin=None,
                sel_in=None, scale: float = 0.0, eps: float = 1e-6, out=None, workspace=None,
                return_sel: bool = False, return_state: bool = False,
-               return_branches: bool = False, check_errors: bool = False, stream=None, profile=None,
-               side_stream=None):
+               return_branches: bool = False, return_lse: bool = False, check_errors: bool = False,
+               stream=None, profile=None, side_stream=None):
     """NAtS-L hybrid attention layer forward (nats_hybrid_fwd; with `profile`,
-    a _native.Profile, nats_hybrid_fwd_profiled; with `side_stream`,
-    nats_hybrid_fwd_streams).
+    a _native.Profile, nats_hybrid_fwd_profiled; with `side_stream` or
+    `return_lse`, nats_hybrid_fwd_streams).
 
     side_stream: a torch.cuda.Stream for the softmax branch (fork / join
     events are made here), or the string "serial" for both branches in order
     on `stream`; None uses the library's per-device side stream.
+    return_lse (bf16 layers): also return "lse" ([B, H, L] fp32), the softmax
+    branch's row statistic that hybrid_bwd(lse=...) reuses.
 
     q, k, v: [B, H, L, d] bf16 or fp32 (same dtype); g, beta: fp32 [B, H, L];
     w_s: fp32 [H, 2, 2d]; b_s: fp32 [H, 2] or None; w_g: fp32 [H, d];
@@ -141,22 +143,28 @@ def hybrid_fwd(q, k, v, g, beta, w_s, b_s, w_g, b_g=None, *, norm_w_soft=None, n
     state = torch.empty((B, H, d, d), dtype=torch.float32, device=dev) if return_state else None
     o_soft = torch.empty((B, H, L, d), dtype=torch.float32, device=dev) if return_branches else None
     o_lin = torch.empty((B, H, L, d), dtype=torch.float32, device=dev) if return_branches else None
+    lse = torch.empty((B, H, L), dtype=torch.float32, device=dev) if return_lse else None
     args = (ctypes.byref(dm), _p(q), _p(k), _p(v), _p(g), _p(beta), _p(w_s), _p(b_s), _p(w_g), _p(b_g),
             _p(norm_w_soft), _p(norm_w_lin), _p(sel_in), _p(out), _p(sel), _p(state), _p(o_soft),
-            _p(o_lin), _p(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream))
-    if side_stream is not None:
-        streams, _events = _streams_of(side_stream)
+            _p(o_lin))
+    tail = (_p(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream))
+    if side_stream is not None or return_lse:
+        streams, _events = _streams_of(side_stream) if side_stream is not None else (None, [])
         prof = ctypes.byref(profile) if profile is not None else None
-        check(_native.lib.nats_hybrid_fwd_streams(*args, ctypes.byref(streams), prof), "nats_hybrid_fwd_streams")
+        check(_native.lib.nats_hybrid_fwd_streams(*args, _p(lse), *tail,
+                                                  ctypes.byref(streams) if streams is not None else None, prof),
+              "nats_hybrid_fwd_streams")
     elif profile is None:
-        check(_native.lib.nats_hybrid_fwd(*args), "nats_hybrid_fwd")
+        check(_native.lib.nats_hybrid_fwd(*args, *tail), "nats_hybrid_fwd")
     else:
-        check(_native.lib.nats_hybrid_fwd_profiled(*args, ctypes.byref(profile)), "nats_hybrid_fwd_profiled")
+        check(_native.lib.nats_hybrid_fwd_profiled(*args, *tail, ctypes.byref(profile)), "nats_hybrid_fwd_profiled")
     if check_errors:
         check_workspace(dm, workspace, stream)
-    if not (return_sel or return_state or return_branches):
+    if not (return_sel or return_state or return_branches or return_lse):
         return out
     res = {"out": out}
+    if return_lse:
+        res["lse"] = lse
     if return_sel:
         res["sel"] = sel
     if return_state:
@@ -210,7 +218,7 @@ def hybrid_fwd_x(x, w_qkv, w_ab, w_s, b_s, w_g, b_g=None, *, heads: int, b_a=Non
 
 def hybrid_bwd(q, k, v, g, beta, w_g, b_g, sel, o_soft, o_lin, dout, *, norm_w_soft=None, norm_w_lin=None,
                scale: float = 0.0, eps: float = 1e-6, weight_grads: bool = True, workspace=None, stream=None,
-               profile=None, side_stream=None):
+               profile=None, side_stream=None, lse=None):
     """Backward pass of the layer at the forward's selection
     (nats_hybrid_bwd_streams; `profile`, a _native.Profile, or None).
 
@@ -218,6 +226,9 @@ def hybrid_bwd(q, k, v, g, beta, w_g, b_g, sel, o_soft, o_lin, dout, *, norm_w_s
     bf16 layer (fork / join events are made here), or "serial" for every
     kernel in order on `stream`; None uses the library's per-device side
     stream.
+    lse: the forward's "lse" (hybrid_fwd(..., return_lse=True)) for the same
+    inputs; a bf16 backward then reads the softmax row statistic instead of
+    recomputing it.
 
     sel, o_soft, o_lin: the forward's selection and branch outputs
     (hybrid_fwd(..., return_sel=True, return_branches=True)); dout like q.
@@ -240,6 +251,7 @@ def hybrid_bwd(q, k, v, g, beta, w_g, b_g, sel, o_soft, o_lin, dout, *, norm_w_s
     _req(sel, "sel", torch.uint8, (B, H, N))
     _req(o_soft, "o_soft", torch.float32, (B, H, L, d))
     _req(o_lin, "o_lin", torch.float32, (B, H, L, d))
+    _req(lse, "lse", torch.float32, (B, H, L))
     dm = dims(B, H, L, d, _dtype_code(q), scale, eps)
     need = int(_native.lib.nats_bwd_workspace_size(ctypes.byref(dm)))
     if workspace is None:
@@ -255,7 +267,7 @@ def hybrid_bwd(q, k, v, g, beta, w_g, b_g, sel, o_soft, o_lin, dout, *, norm_w_s
     streams, _events = _streams_of(side_stream) if side_stream is not None else (None, [])
     check(_native.lib.nats_hybrid_bwd_streams(
         ctypes.byref(dm), _p(q), _p(k), _p(v), _p(g), _p(beta), _p(w_g), _p(b_g), _p(norm_w_soft),
-        _p(norm_w_lin), _p(sel), _p(o_soft), _p(o_lin), _p(dout), _p(res["dq"]), _p(res["dk"]), _p(res["dv"]),
+        _p(norm_w_lin), _p(sel), _p(o_soft), _p(o_lin), _p(lse), _p(dout), _p(res["dq"]), _p(res["dk"]), _p(res["dv"]),
         _p(res["dg"]), _p(res["dbeta"]), _p(res.get("dw_g")), _p(res.get("db_g")), _p(res.get("dnorm_w_soft")),
         _p(res.get("dnorm_w_lin")), _p(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream),
         ctypes.byref(streams) if streams is not None else None,

@@ -106,7 +106,7 @@ def _load() -> ctypes.CDLL:
     lib.nats_hybrid_fwd_profiled.argtypes = [ctypes.POINTER(Dims)] + [P] * 18 + [
         ctypes.c_size_t, P, ctypes.POINTER(Profile)]
     lib.nats_hybrid_fwd_profiled.restype = ctypes.c_int
-    lib.nats_hybrid_fwd_streams.argtypes = [ctypes.POINTER(Dims)] + [P] * 18 + [
+    lib.nats_hybrid_fwd_streams.argtypes = [ctypes.POINTER(Dims)] + [P] * 19 + [
         ctypes.c_size_t, P, ctypes.POINTER(Streams), ctypes.POINTER(Profile)]
     lib.nats_hybrid_fwd_streams.restype = ctypes.c_int
     lib.nats_hybrid_fwd_noalloc.argtypes = [ctypes.POINTER(Dims)] + [P] * 17 + [P]
@@ -136,7 +136,7 @@ def _load() -> ctypes.CDLL:
     lib.nats_hybrid_bwd_profiled.argtypes = [ctypes.POINTER(Dims)] + [P] * 23 + [ctypes.c_size_t, P,
                                                                                ctypes.POINTER(Profile)]
     lib.nats_hybrid_bwd_profiled.restype = ctypes.c_int
-    lib.nats_hybrid_bwd_streams.argtypes = [ctypes.POINTER(Dims)] + [P] * 23 + [
+    lib.nats_hybrid_bwd_streams.argtypes = [ctypes.POINTER(Dims)] + [P] * 24 + [
         ctypes.c_size_t, P, ctypes.POINTER(Streams), ctypes.POINTER(Profile)]
     lib.nats_hybrid_bwd_streams.restype = ctypes.c_int
     lib.nats_score_bwd.argtypes = [ctypes.POINTER(Dims)] + [P] * 11 + [P]

@@ -236,12 +236,13 @@ nats_status nats_hybrid_fwd_streams(const nats_dims* dims, const void* q, const 
                                     const float* b_g, const float* norm_w_soft,
                                     const float* norm_w_lin, const uint8_t* sel_in, void* out,
                                     uint8_t* sel_out, float* state_out, float* o_soft_out,
-                                    float* o_lin_out, void* workspace, size_t workspace_bytes,
+                                    float* o_lin_out, float* lse_out, void* workspace, size_t workspace_bytes,
                                     nats_stream_t stream, const nats_streams* streams,
                                     nats_profile* prof) {
   bool empty = false;
   nats_status s = check_fwd_args(dims, q, k, v, g, beta, w_s, w_g, sel_in, out, &empty);
   if (s != NATS_OK) return s;
+  if (lse_out && dims->dtype != NATS_BF16) return NATS_ERR_DTYPE;  // the row statistic of the bf16 path
   // caller-owned concurrency: a second stream other than `stream` needs both events
   const bool own_side = streams && streams->side && streams->side != stream;
   if (own_side && (!streams->fork || !streams->join)) return NATS_ERR_NULL;
@@ -320,7 +321,7 @@ nats_status nats_hybrid_fwd_streams(const nats_dims* dims, const void* q, const 
       Stages stg_side{prof, ss};
       NATS_STAGE(stg_side, NATS_STAGE_SOFTMAX, 1,
                  launch_softmax_tc(p, q, k, v, ws.nprev, ws.sel_idx, sel, ws.gate, norm_w_soft, out, o_soft_out,
-                                   ws.err, ss));
+                                   lse_out, ws.err, ss));
       if (ss != st && (cudaEventRecord(join, ss) != cudaSuccess || cudaStreamWaitEvent(st, join, 0) != cudaSuccess))
         return NATS_ERR_CUDA;
     }
@@ -350,8 +351,8 @@ nats_status nats_hybrid_fwd_profiled(const nats_dims* dims, const void* q, const
                                      float* o_lin_out, void* workspace, size_t workspace_bytes,
                                      nats_stream_t stream, nats_profile* prof) {
   return nats_hybrid_fwd_streams(dims, q, k, v, g, beta, w_s, b_s, w_g, b_g, norm_w_soft, norm_w_lin, sel_in, out,
-                                 sel_out, state_out, o_soft_out, o_lin_out, workspace, workspace_bytes, stream,
-                                 nullptr, prof);
+                                 sel_out, state_out, o_soft_out, o_lin_out, nullptr, workspace, workspace_bytes,
+                                 stream, nullptr, prof);
 }
 
 nats_status nats_hybrid_fwd(const nats_dims* dims, const void* q, const void* k, const void* v,
@@ -390,14 +391,15 @@ nats_status nats_hybrid_bwd_profiled(const nats_dims* dims, const void* q, const
                                      float* dnorm_w_soft, float* dnorm_w_lin, void* workspace,
                                      size_t workspace_bytes, nats_stream_t stream, nats_profile* prof) {
   return nats_hybrid_bwd_streams(dims, q, k, v, g, beta, w_g, b_g, norm_w_soft, norm_w_lin, sel, o_soft, o_lin,
-                                 dout, dq, dk, dv, dg, dbeta, dw_g, db_g, dnorm_w_soft, dnorm_w_lin, workspace,
-                                 workspace_bytes, stream, nullptr, prof);
+                                 nullptr, dout, dq, dk, dv, dg, dbeta, dw_g, db_g, dnorm_w_soft, dnorm_w_lin,
+                                 workspace, workspace_bytes, stream, nullptr, prof);
 }
 
 nats_status nats_hybrid_bwd_streams(const nats_dims* dims, const void* q, const void* k, const void* v,
                                     const float* g, const float* beta, const float* w_g, const float* b_g,
                                     const float* norm_w_soft, const float* norm_w_lin, const uint8_t* sel,
-                                    const float* o_soft, const float* o_lin, const void* dout, float* dq,
+                                    const float* o_soft, const float* o_lin, const float* lse, const void* dout,
+                                    float* dq,
                                     float* dk, float* dv, float* dg, float* dbeta, float* dw_g, float* db_g,
                                     float* dnorm_w_soft, float* dnorm_w_lin, void* workspace,
                                     size_t workspace_bytes, nats_stream_t stream, const nats_streams* streams,
@@ -416,6 +418,7 @@ nats_status nats_hybrid_bwd_streams(const nats_dims* dims, const void* q, const 
   const void* ptrs[] = {q, k, v, o_soft, o_lin, dout, dq, dk, dv, workspace};
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return NATS_ERR_ALIGN;
+  if (lse && !aligned16(lse)) return NATS_ERR_ALIGN;
   // caller-owned concurrency: a second stream other than `stream` needs both events
   const bool own_side = streams && streams->side && streams->side != stream;
   if (own_side && (!streams->fork || !streams->join)) return NATS_ERR_NULL;
@@ -441,7 +444,8 @@ nats_status nats_hybrid_bwd_streams(const nats_dims* dims, const void* q, const 
   const nats_status r = cuda_status(launch_hybrid_bwd(
       p, dims->dtype, q, k, v, g, beta, w_g, b_g, norm_w_soft, norm_w_lin, sel, o_soft, o_lin, dout, dq, dk, dv, dg,
       dbeta, dw_g, db_g, dnorm_w_soft, dnorm_w_lin, workspace, (cudaStream_t)stream, prof ? prof->start : nullptr,
-      prof ? prof->stop : nullptr, prof ? prof->stage_launches : nullptr, ss, fork, join));
+      prof ? prof->stop : nullptr, prof ? prof->stage_launches : nullptr, ss, fork, join,
+      dims->dtype == NATS_BF16 ? lse : nullptr));
   if (prof)
     for (int i = 0; i < NATS_BWD_NUM_STAGES; ++i) prof->launches += prof->stage_launches[i];
   return r;

@@ -738,7 +738,7 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
                               const float* o_l, const void* dout, float* dq, float* dk, float* dv, float* dg,
                               float* dbeta, float* dw_g, float* db_g, float* dnws, float* dnwl, void* ws,
                               cudaStream_t st, void* const* ev_start, void* const* ev_stop, int32_t* launches,
-                              cudaStream_t side, cudaEvent_t fork, cudaEvent_t join) {
+                              cudaStream_t side, cudaEvent_t fork, cudaEvent_t join, const float* lse_in) {
   if (p.BH == 0 || p.L == 0) return cudaSuccess;
   auto mark_on = [&](void* const* ev, int s, cudaStream_t on) -> cudaError_t {
     return (ev && ev[s]) ? cudaEventRecord((cudaEvent_t)ev[s], on) : cudaSuccess;
@@ -795,8 +795,8 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
         cudaError_t e3 = mark(ev_start, NATS_BWD_STAGE_SOFTMAX);
         if (e3 == cudaSuccess) e3 = launch_compact(p, sel, lay.nprev, lay.sel_idx, nullptr, st);
         if (e3 == cudaSuccess)
-          e3 = launch_softmax_bwd_tc(p, q, k, v, d_os16, delta, lay.nprev, lay.sel_idx, sel, lse, dq, dk, dv,
-                                     lay.ferr, st);
+          e3 = launch_softmax_bwd_tc(p, q, k, v, d_os16, delta, lay.nprev, lay.sel_idx, sel, lse, lse_in, dq, dk,
+                                     dv, lay.ferr, st);
         if (e3 != cudaSuccess) return e3;
         count(NATS_BWD_STAGE_SOFTMAX, 4);  // compaction, query tiles, local and retained key tiles
         return mark(ev_stop, NATS_BWD_STAGE_SOFTMAX);

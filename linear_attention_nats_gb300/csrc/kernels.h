@@ -14,11 +14,13 @@ cudaError_t launch_compact(const Problem& p, const uint8_t* sel, int32_t* nprev,
                            uint8_t* sel_copy, cudaStream_t st);
 
 // bf16 softmax branch; its epilogue writes out = w RMSNorm(o_s) (bf16) with
-// the per-token gate w; o_s (fp32 diagnostics) may be null.
+// the per-token gate w; o_s (fp32 diagnostics) may be null, and so may
+// lse_out (fp32 [BH, L]: each row's log2-sum-exp2 of its scores times
+// scale log2 e, the backward pass's row statistic).
 cudaError_t launch_softmax_tc(const Problem& p, const void* q, const void* k, const void* v,
                               const int32_t* nprev, const int32_t* sel_idx, const uint8_t* sel,
-                              const float* gate, const float* nw_s, void* out, float* o_s, int* err,
-                              cudaStream_t st);
+                              const float* gate, const float* nw_s, void* out, float* o_s, float* lse_out,
+                              int* err, cudaStream_t st);
 
 cudaError_t launch_softmax_simt(const Problem& p, int dtype, const void* q, const void* k,
                                 const void* v, const int32_t* nprev, const int32_t* sel_idx,
@@ -73,7 +75,7 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
                               float* dbeta, float* dw_g, float* db_g, float* dnws, float* dnwl, void* ws,
                               cudaStream_t st, void* const* ev_start = nullptr, void* const* ev_stop = nullptr,
                               int32_t* launches = nullptr, cudaStream_t side = nullptr, cudaEvent_t fork = nullptr,
-                              cudaEvent_t join = nullptr);
+                              cudaEvent_t join = nullptr, const float* lse_in = nullptr);
 
 // The score layer's gradient under the straight-through surrogate
 // (score_bwd.cu): zeroes dw_s, db_s, then sums into them and adds the score
@@ -113,11 +115,13 @@ cudaError_t launch_gdn_bwd_products(const Problem& p, const void* q, const void*
 // Softmax branch of the backward pass on tcgen05 (softmax_bwd_tc.cu), bf16
 // layers: lse (fp32 [BH, L], exp2 domain) and dq (+=), then dk, dv (=); the
 // compacted softmax-chunk lists (nprev, sel_idx) as the forward builds them;
-// err[0] is set if a bounded wait expires.
+// lse_in (or null) is the forward's row statistic, which then replaces the
+// query-tile kernel's first pass (lse is not written); err[0] is set if a
+// bounded wait expires.
 cudaError_t launch_softmax_bwd_tc(const Problem& p, const void* q, const void* k, const void* v, const void* dos,
                                   const float* delta, const int32_t* nprev, const int32_t* sel_idx,
-                                  const uint8_t* sel, float* lse, float* dq, float* dk, float* dv, int* err,
-                                  cudaStream_t st);
+                                  const uint8_t* sel, float* lse, const float* lse_in, float* dq, float* dk,
+                                  float* dv, int* err, cudaStream_t st);
 
 // The projections around the layer on tcgen05 (gemm_tc.cu).  QKV: x W_qkv
 // into the layer's q, k (normalised per head), v [B, H, L, d] and x W_ab into

@@ -96,8 +96,8 @@ __global__ void __launch_bounds__(256, 1)
                              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                              const int32_t* __restrict__ nprev, const int32_t* __restrict__ sel_idx,
                              const uint8_t* __restrict__ sel, int L, int N, int T, long long BH, float scale,
-                             const float* __restrict__ delta, float* __restrict__ lse, float* __restrict__ dq,
-                             int* __restrict__ err) {
+                             const float* __restrict__ delta, float* __restrict__ lse,
+                             const float* __restrict__ lse_in, float* __restrict__ dq, int* __restrict__ err) {
   using S = DqSm<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(256, 1)
   const QTile ti = q_tile(blockIdx.x, BH, T, N, nprev, sel);
   const long long row0 = ti.bh * (long long)L;
   const int nb = ti.nb;
+  const int gp = lse_in ? 0 : nb;  // blocks of pass 1 (none when the forward's row statistic is given)
   const float sl2 = scale * 1.4426950408889634f;
 
   if (threadIdx.x == 0) {
@@ -171,13 +172,13 @@ __global__ void __launch_bounds__(256, 1)
       // K blocks of both passes through the K ring; the V block of a pass-2
       // block right after its K block
       int nv = 0, nk = 0;
-      for (int g = 0; g < 2 * nb && ok; ++g) {
+      for (int g = 0; g < gp + nb && ok; ++g) {
         const int ks = g & 1;
         if (!(ok = tc::mbar_wait(&bars[DQ_KE + ks], ((g >> 1) & 1) ^ 1, err))) break;
-        load_block(&tm_k, smem + S::offK + ks * S::kT, &bars[DQ_KF + ks], g < nb ? g : g - nb);
+        load_block(&tm_k, smem + S::offK + ks * S::kT, &bars[DQ_KF + ks], g < gp ? g : g - gp);
         ++nk;
-        if (g >= nb) {
-          const int j = g - nb, vs = j & 1;
+        if (g >= gp) {
+          const int j = g - gp, vs = j & 1;
           if (!(ok = tc::mbar_wait(&bars[DQ_VE + vs], ((j >> 1) & 1) ^ 1, err))) break;
           load_block(&tm_v, smem + S::offV + vs * S::kT, &bars[DQ_VF + vs], j);
           ++nv;
@@ -221,14 +222,14 @@ __global__ void __launch_bounds__(256, 1)
         return true;
       };
       // pass 1: S only, for the row statistics
-      for (int g = 0; g < nb && ok; ++g) {
+      for (int g = 0; g < gp && ok; ++g) {
         if (!(ok = issue_s(g))) break;
         tc::mma_commit(&bars[DQ_KE + (g & 1)]);
       }
       // pass 2: S (one block ahead), dP = dO V^T, then dQ += dS K
-      if (ok) ok = issue_s(nb);
+      if (ok) ok = issue_s(gp);
       for (int j = 0; j < nb && ok; ++j) {
-        const int g = nb + j, b = g & 1, vs = j & 1;
+        const int g = gp + j, b = g & 1, vs = j & 1;
         if (!(ok = tc::mbar_wait(&bars[DQ_VF + vs], (j >> 1) & 1, err))) break;
         // the dP buffer: the elementwise warps are done with the previous block
         if (j > 0 && !(ok = tc::mbar_wait(&bars[DQ_SR + ((g - 1) & 1)], ((g - 1) >> 1) & 1, err))) break;
@@ -278,7 +279,7 @@ __global__ void __launch_bounds__(256, 1)
     bool ok = true;
     // pass 1: running max and sum in the exp2 domain
     float m = -INFINITY, l = 0.f;
-    for (int g = 0; g < nb && ok; ++g) {
+    for (int g = 0; g < gp && ok; ++g) {
       const int b = g & 1;
       if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[DQ_SF + b], (g >> 1) & 1, err)))) break;
       tc::fence_after();
@@ -304,11 +305,11 @@ __global__ void __launch_bounds__(256, 1)
       tc::fence_before();
       tc::mbar_arrive(&bars[DQ_SR + b]);
     }
-    const float lse2 = m + __log2f(l);
-    if (ok && valid) lse[row] = lse2;
+    const float lse2 = lse_in ? (valid ? lse_in[row] : 0.f) : m + __log2f(l);
+    if (ok && valid && !lse_in) lse[row] = lse2;
     // pass 2: dS = P (dP - delta) in place of S
     for (int j = 0; j < nb && ok; ++j) {
-      const int g = nb + j, b = g & 1;
+      const int g = gp + j, b = g & 1;
       if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[DQ_SF + b], (g >> 1) & 1, err)))) break;
       if (!(ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars[DQ_PF], j & 1, err)))) break;
       tc::fence_after();
@@ -662,7 +663,7 @@ __global__ void __launch_bounds__(256, 1)
 template <int D>
 cudaError_t run(const Problem& p, const void* q, const void* k, const void* v, const void* dos,
                 const float* delta, const int32_t* nprev, const int32_t* sel_idx, const uint8_t* sel, float* lse,
-                float* dq, float* dk, float* dv, int* err, cudaStream_t st) {
+                const float* lse_in, float* dq, float* dk, float* dv, int* err, cudaStream_t st) {
   CUtensorMap mq, mk, mv, mo;
   const long long rows = p.BH * p.L;
   if (!make_tile_map(&mq, q, rows, D) || !make_tile_map(&mk, k, rows, D) || !make_tile_map(&mv, v, rows, D) ||
@@ -680,11 +681,11 @@ cudaError_t run(const Problem& p, const void* q, const void* k, const void* v, c
   const int T = (p.N + 1) / 2;
   const unsigned grid = (unsigned)(p.BH * T);
   softmax_bwd_dq_tc_kernel<D><<<grid, 256, DqSm<D>::kBytes, st>>>(mq, mk, mv, mo, nprev, sel_idx, sel, p.L, p.N, T,
-                                                                  p.BH, p.scale, delta, lse, dq, err);
+                                                                  p.BH, p.scale, delta, lse, lse_in, dq, err);
   for (int retained = 0; retained < 2; ++retained)
     softmax_bwd_dkv_tc_kernel<D><<<grid, 256, DkvSm<D>::kBytes, st>>>(mq, mk, mv, mo, sel, nprev, sel_idx, p.L, p.N,
-                                                                      T, p.BH, p.scale, retained, lse, delta, dk,
-                                                                      dv, err);
+                                                                      T, p.BH, p.scale, retained,
+                                                                      lse_in ? lse_in : lse, delta, dk, dv, err);
   return cudaGetLastError();
 }
 
@@ -692,11 +693,11 @@ cudaError_t run(const Problem& p, const void* q, const void* k, const void* v, c
 
 cudaError_t launch_softmax_bwd_tc(const Problem& p, const void* q, const void* k, const void* v, const void* dos,
                                   const float* delta, const int32_t* nprev, const int32_t* sel_idx,
-                                  const uint8_t* sel, float* lse, float* dq, float* dk, float* dv, int* err,
-                                  cudaStream_t st) {
+                                  const uint8_t* sel, float* lse, const float* lse_in, float* dq, float* dk,
+                                  float* dv, int* err, cudaStream_t st) {
   if (p.BH == 0 || p.N == 0) return cudaSuccess;
-  return p.d == 64 ? run<64>(p, q, k, v, dos, delta, nprev, sel_idx, sel, lse, dq, dk, dv, err, st)
-                   : run<128>(p, q, k, v, dos, delta, nprev, sel_idx, sel, lse, dq, dk, dv, err, st);
+  return p.d == 64 ? run<64>(p, q, k, v, dos, delta, nprev, sel_idx, sel, lse, lse_in, dq, dk, dv, err, st)
+                   : run<128>(p, q, k, v, dos, delta, nprev, sel_idx, sel, lse, lse_in, dq, dk, dv, err, st);
 }
 
 }  // namespace nats

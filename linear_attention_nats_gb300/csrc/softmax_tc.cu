@@ -124,7 +124,8 @@ __global__ void __launch_bounds__(256, 1)
                       const int32_t* __restrict__ sel_idx, const uint8_t* __restrict__ sel, int L, int N,
                       int T, long long BH, float sl2, const float* __restrict__ gate,
                       const float* __restrict__ nw_s, float eps, __nv_bfloat16* __restrict__ out,
-                      float* __restrict__ o_s, int* __restrict__ err, int* __restrict__ tile_ctr) {
+                      float* __restrict__ o_s, float* __restrict__ lse_out, int* __restrict__ err,
+                      int* __restrict__ tile_ctr) {
   using S = SoftmaxSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -478,6 +479,8 @@ __global__ void __launch_bounds__(256, 1)
         // the scaled row packed to bf16
         const float inv = 1.f / l;
         const size_t row = (size_t)(ti.bh * (long long)L + 128LL * ti.p + r);
+        // the row's log-sum-exp of its scaled scores, base 2 (saved for the backward pass)
+        if (lse_out) lse_out[row] = m_used + __log2f(l);
         float o[D];
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) tc::tmem_ld32(o_addr + ch * 32, *reinterpret_cast<float(*)[32]>(&o[32 * ch]));
@@ -569,8 +572,8 @@ bool make_tile_map(CUtensorMap* map, const void* base, long long rows, int D) {
 template <int D>
 static cudaError_t launch_tc_t(const Problem& p, const void* q, const void* k, const void* v,
                                const int32_t* nprev, const int32_t* sel_idx, const uint8_t* sel,
-                               const float* gate, const float* nw_s, void* out, float* o_s, int* err,
-                               cudaStream_t st) {
+                               const float* gate, const float* nw_s, void* out, float* o_s, float* lse_out,
+                               int* err, cudaStream_t st) {
   CUtensorMap mq, mk, mv, mo;
   const long long rows = p.BH * p.L;
   if (!make_tile_map(&mq, q, rows, D) || !make_tile_map(&mk, k, rows, D) || !make_tile_map(&mv, v, rows, D) ||
@@ -588,17 +591,17 @@ static cudaError_t launch_tc_t(const Problem& p, const void* q, const void* k, c
   const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
   kern<<<grid, 256, smem, st>>>(mq, mk, mv, mo, nprev, sel_idx, sel, p.L, p.N, T, p.BH,
                                 p.scale * 1.4426950408889634f, gate, nw_s, p.eps, (__nv_bfloat16*)out, o_s,
-                                err, err + 1);
+                                lse_out, err, err + 1);
   return cudaGetLastError();
 }
 
 cudaError_t launch_softmax_tc(const Problem& p, const void* q, const void* k, const void* v,
                               const int32_t* nprev, const int32_t* sel_idx, const uint8_t* sel,
-                              const float* gate, const float* nw_s, void* out, float* o_s, int* err,
-                              cudaStream_t st) {
+                              const float* gate, const float* nw_s, void* out, float* o_s, float* lse_out,
+                              int* err, cudaStream_t st) {
   if (p.BH == 0 || p.N == 0) return cudaSuccess;
-  return p.d == 64 ? launch_tc_t<64>(p, q, k, v, nprev, sel_idx, sel, gate, nw_s, out, o_s, err, st)
-                   : launch_tc_t<128>(p, q, k, v, nprev, sel_idx, sel, gate, nw_s, out, o_s, err, st);
+  return p.d == 64 ? launch_tc_t<64>(p, q, k, v, nprev, sel_idx, sel, gate, nw_s, out, o_s, lse_out, err, st)
+                   : launch_tc_t<128>(p, q, k, v, nprev, sel_idx, sel, gate, nw_s, out, o_s, lse_out, err, st);
 }
 
 }  // namespace nats

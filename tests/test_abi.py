@@ -215,7 +215,7 @@ def test_backward_streams_validation(nat):
     dm = nat.dims(1, 2, 128, 64)
     need = nat.lib.nats_bwd_workspace_size(ctypes.byref(dm))
     fake = ctypes.c_void_p(256)
-    args = [fake] * 23
+    args = [fake] * 24  # q ... o_lin, lse, dout ... dnorm_w_lin, the workspace
 
     def call(streams, d=dm, a=args, ws_bytes=1 << 40):
         return nat.lib.nats_hybrid_bwd_streams(ctypes.byref(d), *a, ctypes.c_size_t(ws_bytes), None,
@@ -231,6 +231,9 @@ def test_backward_streams_validation(nat):
         assert call(st, ws_bytes=need - 1) == 5
     assert call(nat.Streams(side, 256, 256), ws_bytes=need - 1) == 5
     assert call(nat.Streams(side, None, None), d=nat.dims(0, 2, 128, 64)) == 0  # nothing to do
+    # the forward's row statistic: optional, 16-byte aligned
+    assert call(None, a=args[:12] + [None] + args[13:], ws_bytes=need - 1) == 5
+    assert call(None, a=args[:12] + [ctypes.c_void_p(264)] + args[13:]) == 4
 
 
 def test_debug_hook_validation(nat):
@@ -312,10 +315,11 @@ def test_streams_validation(nat):
     names = ["q", "k", "v", "g", "beta", "w_s", "b_s", "w_g", "b_g", "nws", "nwl", "sel_in", "out",
              "sel_out", "state", "o_soft", "o_lin", "ws"]
 
-    def call(dmx, streams, ws_bytes=1 << 40, **ptrs):
+    def call(dmx, streams, ws_bytes=1 << 40, lse=None, **ptrs):
         args = [None if ptrs.get(n) is None else ctypes.c_void_p(ptrs[n]) for n in names]
-        return nat.lib.nats_hybrid_fwd_streams(ctypes.byref(dmx), *args[:17], args[17], ctypes.c_size_t(ws_bytes),
-                                               None, ctypes.byref(streams) if streams is not None else None, None)
+        return nat.lib.nats_hybrid_fwd_streams(ctypes.byref(dmx), *args[:17], lse, args[17],
+                                               ctypes.c_size_t(ws_bytes), None,
+                                               ctypes.byref(streams) if streams is not None else None, None)
 
     side = ctypes.c_void_p(0x7000).value
     for fork, join in ((None, None), (A, None), (None, A)):
@@ -326,3 +330,7 @@ def test_streams_validation(nat):
     for st in (nat.Streams(None, None, None), None):
         assert call(dm, st, ws_bytes=need - 1, **FULL) == 5
     assert call(dm, nat.Streams(side, A, A), ws_bytes=need - 1, **FULL) == 5
+    # the saved row statistic exists for bf16 layers only
+    f32 = nat.dims(1, 2, 256, 64, nat.NATS_F32)
+    assert call(f32, None, lse=ctypes.c_void_p(A), **FULL) == 3
+    assert call(dm, None, ws_bytes=need - 1, lse=ctypes.c_void_p(A), **FULL) == 5

@@ -263,3 +263,36 @@ def test_backward_full_size_whole_head():
     print("[parity] backward l8192 whole head: " + " ".join(f"{n}={e:.1e}" for n, e in errs.items()))
     for n, e in errs.items():
         assert e <= TOL["bf16"], (n, e)
+
+
+@pytest.mark.parametrize("B,H,L,d,seed", [(2, 2, 320, 128, 47), (1, 3, 448, 64, 48)])
+def test_backward_with_the_forward_row_statistic(B, H, L, d, seed):
+    # hybrid_fwd(return_lse=True) saves the softmax rows' log-sum-exp;
+    # hybrid_bwd(lse=...) then skips recomputing it: the same gradients as
+    # without it (the statistic differs only by rounding order), and, for
+    # d = 128, within the oracle's bar end to end
+    import linear_attention_nats_gb300 as nats
+    from linear_attention_nats_gb300 import build
+
+    build.build()
+    inp, nws, nwl, dout = _case(B, H, L, d, "bf16", seed)
+    t = to_device(inp)
+    nw = {"norm_w_soft": _dev(nws, "f32"), "norm_w_lin": _dev(nwl, "f32")}
+    fwd = nats.hybrid_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_s"], t["b_s"], t["w_g"], t["b_g"],
+                          return_sel=True, return_branches=True, return_lse=True, check_errors=True, **nw)
+    plain = nats.hybrid_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_s"], t["b_s"], t["w_g"], t["b_g"],
+                            return_sel=True, return_branches=True, **nw)
+    torch.cuda.synchronize()
+    for n in ("out", "sel", "o_soft", "o_lin"):  # the statistic's store changes nothing else
+        assert torch.equal(plain[n], fwd[n]), n
+    args = (t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_g"], t["b_g"], fwd["sel"], fwd["o_soft"],
+            fwd["o_lin"], _dev(dout, "bf16"))
+    ref = nats.hybrid_bwd(*args, **nw)
+    got = nats.hybrid_bwd(*args, lse=fwd["lse"], **nw)
+    torch.cuda.synchronize()
+    for n in GRADS:
+        scale = float(ref[n].abs().max())
+        assert torch.allclose(got[n], ref[n], rtol=1e-3, atol=1e-4 * scale), n
+    if d == 128:  # the end-to-end bar, as after the CUDA forward above
+        sel_ref = oracle.select_inputs(inp)[0].reshape(B, H, L // 64)
+        _compare(got, _oracle(inp, nws, nwl, dout, sel_ref), TOL["bf16"], f"bf16-{d} (forward's row statistic)")
