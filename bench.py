@@ -631,6 +631,7 @@ def run_x_path(args, rank, dev, stream, dist):
     t = dict(x=bf(xi.x), w_qkv=bf(xi.w_qkv), w_ab=bf(xi.w_ab), w_o=bf(xi.w_o), b_a=f(xi.b_a),
              a_scale=f(xi.a_scale), b_b=f(xi.b_b), w_s=f(xi.w_s), b_s=f(xi.b_s), w_g=f(xi.w_g), b_g=f(xi.b_g))
     y = torch.empty((B, L, hidden), dtype=torch.bfloat16, device=dev)
+    sel = torch.empty((B, H, L // 64), dtype=torch.uint8, device=dev)  # the chunks the score layer chose
     dm = nats.dims(B, H, L, d, nats.NATS_BF16)
     wsb = int(_native.lib.nats_x_workspace_size(ctypes.byref(dm), hidden))
     ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
@@ -639,7 +640,7 @@ def run_x_path(args, rank, dev, stream, dist):
     def call(prof=None):
         code = _native.lib.nats_hybrid_fwd_x_profiled(
             ctypes.byref(dm), hidden, P(t["x"]), P(t["w_qkv"]), P(t["w_ab"]), P(t["b_a"]), P(t["a_scale"]),
-            P(t["b_b"]), P(t["w_s"]), P(t["b_s"]), P(t["w_g"]), P(t["b_g"]), P(t["w_o"]), P(y), None, P(ws),
+            P(t["b_b"]), P(t["w_s"]), P(t["b_s"]), P(t["w_g"]), P(t["b_g"]), P(t["w_o"]), P(y), P(sel), P(ws),
             ctypes.c_size_t(wsb), ctypes.c_void_p(stream.cuda_stream),
             ctypes.byref(prof) if prof is not None else None)
         if code != 0:
@@ -693,7 +694,10 @@ def run_x_path(args, rank, dev, stream, dist):
     dom = max(gemms, key=lambda k: gemms[k]["ms_per_launch"]) if gemms else None
     return {"what": "nats_hybrid_fwd_x: x -> q, k, v, g, beta (tcgen05 GEMM, head split + key norm + gates in "
                     "its epilogue), the layer, output projection (the same GEMM kernel)",
-            "config": {"B": B, "H": H, "L": L, "d": d, "hidden": hidden},
+            "config": {"B": B, "H": H, "L": L, "d": d, "hidden": hidden,
+                       # random projections and score weights with zero bias: the score layer's own
+                       # choice, near half the chunks (the layer leg fixes 25 % by its inputs)
+                       "softmax_chunk_frac": float((sel == 0).float().mean().item())},
             "value": job_throughput(B * L, world, ms), "unit": "tokens/s", "ms_per_step": ms,
             "stages_ms": stage_ms, "projection_gemm_flops_per_step": f_in + f_out,
             "roofline": gemms.get(dom), "gemm_rooflines": gemms}
