@@ -41,3 +41,34 @@ def test_x_path_parity(name):
     err = rel_err(r["y"].float().cpu().numpy(), ref["y"])
     print(f"[parity] {name} x path: y={err:.2e}")
     assert err <= TOL["bf16"]
+
+
+def test_x_path_full_size_composition():
+    # x_l8192, the shapes the bench times (4 x 8192 tokens, hidden 2048, 16
+    # heads): the output equals its parts composed, a property that holds at
+    # any size: the projections in fp64 (oracle.project, rounded as the layer
+    # holds them), the layer (its own parity is tested apart) at the x path's
+    # own selection, and the output projection in fp64, compared on sampled
+    # tokens (every head of each)
+    import linear_attention_nats_gb300 as nats
+    from linear_attention_nats_gb300 import build
+
+    build.build()
+    inp = gen.x_config_inputs("x_l8192")
+    B, H, L, d = inp.B, inp.H, inp.L, inp.d
+    r = nats.hybrid_fwd_x(_bf16(inp.x), _bf16(inp.w_qkv), _bf16(inp.w_ab), _f32(inp.w_s), _f32(inp.b_s),
+                          _f32(inp.w_g), _f32(inp.b_g), heads=H, b_a=_f32(inp.b_a), a_scale=_f32(inp.a_scale),
+                          b_b=_f32(inp.b_b), w_o=_bf16(inp.w_o), return_sel=True, check_errors=True)
+    torch.cuda.synchronize()
+    q, k, v, g, beta = oracle.project(inp.x, inp.w_qkv, inp.w_ab, H, b_a=inp.b_a, a_scale=inp.a_scale, b_b=inp.b_b)
+    o = nats.hybrid_fwd(_bf16(q), _bf16(k), _bf16(v), _f32(g), _f32(beta), _f32(inp.w_s), _f32(inp.b_s),
+                        _f32(inp.w_g), _f32(inp.b_g), sel_in=r["sel"], check_errors=True)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(29)
+    tok = np.sort(rng.choice(B * L, size=256, replace=False))
+    of = o.float().cpu().numpy().transpose(0, 2, 1, 3).reshape(B * L, H * d)[tok]
+    y_ref = of.astype(np.float64) @ np.asarray(inp.w_o, np.float64)
+    y = r["y"].float().cpu().numpy().reshape(B * L, -1)[tok]
+    err = rel_err(y, y_ref)
+    print(f"[parity] x_l8192 x path (composition, 256 tokens): y={err:.2e}")
+    assert err <= TOL["bf16"]
