@@ -775,34 +775,18 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
     const T* kt = (const T*)k;
     const T* vt = (const T*)v;
     constexpr bool tc = std::is_same<T, __nv_bfloat16>::value;  // bf16: the softmax branch on tensor cores
-    cudaError_t e2 = mark(ev_start, NATS_BWD_STAGE_MERGE);
-    if (e2 != cudaSuccess) return e2;
-    merge_bwd_kernel<T, D><<<(unsigned)(rows / kMergeRows), 256, 0, st>>>(
-        qt, (const T*)dout, o_s, o_l, w_g, b_g, nws, nwl, p.H, p.L, p.eps, d_os, tc ? d_os16 : nullptr, d_ol,
-        delta, dq, dw_g, db_g, dnws, dnwl);
-    count(NATS_BWD_STAGE_MERGE, 1);
-    if ((e2 = mark(ev_stop, NATS_BWD_STAGE_MERGE)) != cudaSuccess) return e2;
-    if constexpr (tc) {
-      // The chunk-start states' recompute and the Gated DeltaNet adjoint's
-      // chunk factors and reverse scan read only the inputs, the selection
-      // and d o_l, and write only scratch: with a second stream they run
-      // beside the softmax branch, whose CTAs fill the SMs that the two scans
-      // (chains over the chunks: 1 and 2 CTAs per head) leave idle.  They are
-      // enqueued first so that the chains start first.
-      const bool two = side && side != st && fork && join;
-      const cudaStream_t ss = two ? side : st;
-      auto softmax_stage = [&]() -> cudaError_t {
-        cudaError_t e3 = mark(ev_start, NATS_BWD_STAGE_SOFTMAX);
-        if (e3 == cudaSuccess) e3 = launch_compact(p, sel, lay.nprev, lay.sel_idx, nullptr, st);
-        if (e3 == cudaSuccess)
-          e3 = launch_softmax_bwd_tc(p, q, k, v, d_os16, delta, lay.nprev, lay.sel_idx, sel, lse, lse_in, dq, dk,
-                                     dv, lay.ferr, st);
-        if (e3 != cudaSuccess) return e3;
-        count(NATS_BWD_STAGE_SOFTMAX, 4);  // compaction, query tiles, local and retained key tiles
-        return mark(ev_stop, NATS_BWD_STAGE_SOFTMAX);
-      };
-      auto states_and_factors = [&]() -> cudaError_t {
-        cudaError_t e3 = mark_on(ev_start, NATS_BWD_STAGE_GDN, ss);
+    // bf16 layers with a second stream: the chunk-start states' recompute
+    // and the adjoint's chunk factors need only the inputs and the selection
+    // and write only scratch, so they start on the second stream before the
+    // merge stage; the reverse scan (it reads d o_l) waits for the merge.
+    // That stream's work is the longer of the two branches', and the softmax
+    // branch's CTAs fill the SMs its scans (chains over the chunks: 1 and 2
+    // CTAs per head) leave idle.
+    const bool two = tc && side && side != st && fork && join;
+    const cudaStream_t ss = two ? side : st;
+    auto state_work = [&]() -> cudaError_t {
+      cudaError_t e3 = mark_on(ev_start, NATS_BWD_STAGE_GDN, ss);
+      if constexpr (tc) {
         // the chunk-start states, from the forward's chunk factors and scan
         // (the same kernels as the forward; the selection is given), and
         // every chunk's Linv = (I + diag(beta) A)^{-1} in fp32 on the way
@@ -814,21 +798,50 @@ cudaError_t launch_hybrid_bwd(const Problem& p, int dtype, const void* q, const 
         if (e3 == cudaSuccess)
           e3 = launch_gdn_scan_tc(p, q, k, sel, lay.fG, lay.fW, lay.fU, lay.fP, nullptr, lay.fol16, nullptr,
                                   lay.ferr, ss, lay.cw.S0);
-        // the adjoint's chunk factors and reverse scan
-        if (e3 == cudaSuccess) e3 = launch_gdn_bwd_factors(p, q, k, g, beta, sel, d_ol, lay.cw, ss);
+        // the adjoint's chunk factors
+        if (e3 == cudaSuccess) e3 = launch_gdn_bwd_factors(p, q, k, g, beta, lay.cw, ss);
+        if (e3 == cudaSuccess) count(NATS_BWD_STAGE_GDN, 3);
+      }
+      return e3;
+    };
+    cudaError_t e2 = cudaSuccess;
+    if (two && ((e2 = cudaEventRecord(fork, st)) != cudaSuccess || (e2 = cudaStreamWaitEvent(ss, fork, 0)) != cudaSuccess ||
+                (e2 = state_work()) != cudaSuccess))
+      return e2;
+    if ((e2 = mark(ev_start, NATS_BWD_STAGE_MERGE)) != cudaSuccess) return e2;
+    merge_bwd_kernel<T, D><<<(unsigned)(rows / kMergeRows), 256, 0, st>>>(
+        qt, (const T*)dout, o_s, o_l, w_g, b_g, nws, nwl, p.H, p.L, p.eps, d_os, tc ? d_os16 : nullptr, d_ol,
+        delta, dq, dw_g, db_g, dnws, dnwl);
+    count(NATS_BWD_STAGE_MERGE, 1);
+    if ((e2 = mark(ev_stop, NATS_BWD_STAGE_MERGE)) != cudaSuccess) return e2;
+    if constexpr (tc) {
+      auto softmax_stage = [&]() -> cudaError_t {
+        cudaError_t e3 = mark(ev_start, NATS_BWD_STAGE_SOFTMAX);
+        if (e3 == cudaSuccess) e3 = launch_compact(p, sel, lay.nprev, lay.sel_idx, nullptr, st);
+        if (e3 == cudaSuccess)
+          e3 = launch_softmax_bwd_tc(p, q, k, v, d_os16, delta, lay.nprev, lay.sel_idx, sel, lse, lse_in, dq, dk,
+                                     dv, lay.ferr, st);
         if (e3 != cudaSuccess) return e3;
-        count(NATS_BWD_STAGE_GDN, 4);
+        count(NATS_BWD_STAGE_SOFTMAX, 4);  // compaction, query tiles, local and retained key tiles
+        return mark(ev_stop, NATS_BWD_STAGE_SOFTMAX);
+      };
+      auto reverse_scan = [&]() -> cudaError_t {
+        cudaError_t e3 = launch_gdn_bwd_reverse_scan(p, sel, d_ol, lay.cw, ss);
+        if (e3 != cudaSuccess) return e3;
+        count(NATS_BWD_STAGE_GDN, 1);
         return mark_on(ev_stop, NATS_BWD_STAGE_GDN, ss);
       };
       if (two) {
+        // the reverse scan after the merge (the fork event is recorded again:
+        // a wait takes the event's latest record)
         if ((e2 = cudaEventRecord(fork, st)) != cudaSuccess || (e2 = cudaStreamWaitEvent(ss, fork, 0)) != cudaSuccess ||
-            (e2 = states_and_factors()) != cudaSuccess || (e2 = softmax_stage()) != cudaSuccess)
+            (e2 = reverse_scan()) != cudaSuccess || (e2 = softmax_stage()) != cudaSuccess ||
+            (e2 = cudaEventRecord(join, ss)) != cudaSuccess || (e2 = cudaStreamWaitEvent(st, join, 0)) != cudaSuccess)
           return e2;
-      } else if ((e2 = softmax_stage()) != cudaSuccess || (e2 = states_and_factors()) != cudaSuccess) {
+      } else if ((e2 = softmax_stage()) != cudaSuccess || (e2 = state_work()) != cudaSuccess ||
+                 (e2 = reverse_scan()) != cudaSuccess) {
         return e2;
       }
-      if (two && ((e2 = cudaEventRecord(join, ss)) != cudaSuccess || (e2 = cudaStreamWaitEvent(st, join, 0)) != cudaSuccess))
-        return e2;
       // every per-chunk product of the adjoint: dq, dk, dv, dg, dbeta
       if ((e2 = mark(ev_start, NATS_BWD_STAGE_COMBINE)) != cudaSuccess) return e2;
       if ((e2 = launch_gdn_bwd_products(p, q, k, v, g, beta, sel, d_ol, lay.cw, dq, dk, dv, dg, dbeta, lay.ferr,

@@ -1607,12 +1607,20 @@ cudaError_t set_attributes() {
 
 template <int D>
 cudaError_t run_factors(const Problem& p, const void* q, const void* k, const float* g, const float* beta,
-                        const uint8_t* sel, const float* dO, const GdnBwdScratch& w, cudaStream_t st) {
+                        const GdnBwdScratch& w, cudaStream_t st) {
   cudaError_t e = set_attributes<D>();
   if (e != cudaSuccess) return e;
   gdn_bwd_prep_kernel<D><<<(unsigned)(p.BH * p.N), 256, PrepSm<D>::kBytes, st>>>(
       (const bf16*)q, (const bf16*)k, g, beta, p.L, p.N, p.scale, w.G, w.Li, w.P, (half*)w.W16, (half*)w.Qe16,
       (half*)w.Kt16, w.sc);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t run_reverse_scan(const Problem& p, const uint8_t* sel, const float* dO, const GdnBwdScratch& w,
+                             cudaStream_t st) {
+  cudaError_t e = set_attributes<D>();
+  if (e != cudaSuccess) return e;
   gdn_bwd_scan_kernel<D><<<(unsigned)(p.BH * (D / RB)), 256, ScanSm<D>::kBytes, st>>>(
       (const half*)w.Kt16, (const half*)w.W16, (const half*)w.Qe16, w.sc, dO, w.G, sel, p.L, p.N, w.dSC);
   return cudaGetLastError();
@@ -1642,11 +1650,15 @@ cudaError_t run_products(const Problem& p, const void* q, const void* k, const v
 }  // namespace
 
 cudaError_t launch_gdn_bwd_factors(const Problem& p, const void* q, const void* k, const float* g,
-                                   const float* beta, const uint8_t* sel, const float* dO, const GdnBwdScratch& w,
-                                   cudaStream_t st) {
+                                   const float* beta, const GdnBwdScratch& w, cudaStream_t st) {
   if (p.BH == 0 || p.N == 0) return cudaSuccess;
-  return p.d == 64 ? run_factors<64>(p, q, k, g, beta, sel, dO, w, st)
-                   : run_factors<128>(p, q, k, g, beta, sel, dO, w, st);
+  return p.d == 64 ? run_factors<64>(p, q, k, g, beta, w, st) : run_factors<128>(p, q, k, g, beta, w, st);
+}
+
+cudaError_t launch_gdn_bwd_reverse_scan(const Problem& p, const uint8_t* sel, const float* dO,
+                                        const GdnBwdScratch& w, cudaStream_t st) {
+  if (p.BH == 0 || p.N == 0) return cudaSuccess;
+  return p.d == 64 ? run_reverse_scan<64>(p, sel, dO, w, st) : run_reverse_scan<128>(p, sel, dO, w, st);
 }
 
 cudaError_t launch_gdn_bwd_products(const Problem& p, const void* q, const void* k, const void* v, const float* g,

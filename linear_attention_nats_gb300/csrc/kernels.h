@@ -97,12 +97,14 @@ struct GdnBwdScratch {
   void* Kt16;   // [BH, L, dk] fp16: diag(gamma_C / gamma) K  /   (sc)
   float* sc;    // [BH, N, 4] the scales of W, Q_eff, K~
 };
-// the adjoint's chunk factors and the reverse state-gradient scan (two
-// kernels; they read q, k, g, beta, the selection, dO and Linv, and write
-// only the scratch: G, P, W, Q_eff, K~, their scales and dS_C)
+// the adjoint's chunk factors (one kernel; it reads q, k, g, beta and Linv
+// and writes only the scratch: G, P, W, Q_eff, K~ and their scales)
 cudaError_t launch_gdn_bwd_factors(const Problem& p, const void* q, const void* k, const float* g,
-                                   const float* beta, const uint8_t* sel, const float* dO, const GdnBwdScratch& w,
-                                   cudaStream_t st);
+                                   const float* beta, const GdnBwdScratch& w, cudaStream_t st);
+// the reverse state-gradient scan (one kernel, after the factors; it reads
+// them, the selection and dO, and writes dS_C of every committed chunk)
+cudaError_t launch_gdn_bwd_reverse_scan(const Problem& p, const uint8_t* sel, const float* dO,
+                                        const GdnBwdScratch& w, cudaStream_t st);
 // every per-chunk product of the adjoint, after the factors, the reverse
 // scan and the chunk-start states S0 (one kernel, on tcgen05 for d = 128;
 // dq, dk, dv accumulate, dg and dbeta are overwritten; err[0] is set if a

@@ -129,11 +129,12 @@ def test_backward_profiled_stages():
     assert prof.launches == 10
     ms = [a.elapsed_time(b) for a, b in ev]
     assert all(m > 0 for m in ms), ms
-    # the softmax stage and the Gated DeltaNet stage both start after the
-    # merge and may run side by side on two streams; the per-chunk products
+    # the softmax stage starts after the merge; the Gated DeltaNet stage's
+    # state work needs no merge output and may start before it on a second
+    # stream, beside the merge and the softmax stage; the per-chunk products
     # start after both
     merge, soft, gdn, comb = ev
-    for a, b in ((merge[1], soft[0]), (merge[1], gdn[0]), (soft[1], comb[0]), (gdn[1], comb[0])):
+    for a, b in ((merge[1], soft[0]), (soft[1], comb[0]), (gdn[1], comb[0])):
         assert a.elapsed_time(b) >= 0
 
 
