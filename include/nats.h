@@ -415,9 +415,10 @@ nats_status nats_decode_step(const nats_dims* dims, int64_t t, const void* q, co
  * dk, dv and the workspace 16-byte aligned; asynchronous on `stream`.  With
  * bf16 inputs the Gated DeltaNet chunk-start states' recompute and the
  * adjoint's chunk factors and reverse scan (which write only the workspace)
- * run on the library's per-device side stream, forked from `stream` after
- * the merge stage and joined back before the first kernel that writes dq,
- * dk or dv after the softmax branch.
+ * run on the library's per-device side stream, forked from `stream` at the
+ * call's start (the reverse scan waits for the merge stage, whose output it
+ * reads) and joined back before the first kernel that writes dq, dk or dv
+ * after the softmax branch.
  * Errors before any launch: NATS_ERR_NULL, NATS_ERR_SHAPE /
  * NATS_ERR_UNSUPPORTED / NATS_ERR_DTYPE / NATS_ERR_VALUE (dims),
  * NATS_ERR_ALIGN, NATS_ERR_WORKSPACE; NATS_ERR_CUDA on a failed launch. */
