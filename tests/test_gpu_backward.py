@@ -239,9 +239,12 @@ def test_score_layer_gradient(B, H, L, d, dtype, seed):
 
 
 def test_backward_full_size_whole_head():
-    # the benchmark's workload through the CUDA forward and backward; one
-    # whole head (all 8192 tokens, every chunk's state gradient carried back
-    # through the reverse scan) against the oracle's backward of that head
+    # the benchmark's workload through the CUDA forward and backward as
+    # bench.py runs them (the forward saves the row log-sum-exp, the backward
+    # takes it); one whole head (all 8192 tokens, every chunk's state
+    # gradient carried back through the reverse scan) against the oracle's
+    # backward of that head, and every gradient against the backward that
+    # recomputes the statistic
     import linear_attention_nats_gb300 as nats
     from linear_attention_nats_gb300 import build
 
@@ -250,11 +253,18 @@ def test_backward_full_size_whole_head():
     B, H, L, d = inp.B, inp.H, inp.L, inp.d
     t = to_device(inp)
     fwd = nats.hybrid_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_s"], t["b_s"], t["w_g"], t["b_g"],
-                          return_sel=True, return_branches=True, check_errors=True)
+                          return_sel=True, return_branches=True, return_lse=True, check_errors=True)
     dout = gen.round_to_bf16(np.random.default_rng(49).standard_normal((B, H, L, d)).astype(np.float32))
-    got = nats.hybrid_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_g"], t["b_g"], fwd["sel"], fwd["o_soft"],
-                          fwd["o_lin"], _dev(dout, "bf16"))
+    args = (t["q"], t["k"], t["v"], t["g"], t["beta"], t["w_g"], t["b_g"], fwd["sel"], fwd["o_soft"], fwd["o_lin"],
+            _dev(dout, "bf16"))
+    got = nats.hybrid_bwd(*args, lse=fwd["lse"])
+    plain = nats.hybrid_bwd(*args)
     torch.cuda.synchronize()
+    # the statistic differs from the recomputed one in its last bits, which
+    # flips the bf16 rounding of a few P entries (dv sums P directly: up to
+    # ~1e-4 of its max at this size)
+    for n in GRADS:
+        assert torch.allclose(got[n], plain[n], rtol=1e-3, atol=1e-3 * float(plain[n].abs().max())), n
     sel = fwd["sel"].cpu().numpy()
     b, h = 2, 7
     one = lambda a: a[b:b + 1, h:h + 1]
@@ -291,9 +301,9 @@ def test_backward_with_the_forward_row_statistic(B, H, L, d, seed):
     ref = nats.hybrid_bwd(*args, **nw)
     got = nats.hybrid_bwd(*args, lse=fwd["lse"], **nw)
     torch.cuda.synchronize()
-    for n in GRADS:
+    for n in GRADS:  # (rounding flips of P in bf16, as in the full-size test)
         scale = float(ref[n].abs().max())
-        assert torch.allclose(got[n], ref[n], rtol=1e-3, atol=1e-4 * scale), n
+        assert torch.allclose(got[n], ref[n], rtol=1e-3, atol=1e-3 * scale), n
     if d == 128:  # the end-to-end bar, as after the CUDA forward above
         sel_ref = oracle.select_inputs(inp)[0].reshape(B, H, L // 64)
         _compare(got, _oracle(inp, nws, nwl, dout, sel_ref), TOL["bf16"], f"bf16-{d} (forward's row statistic)")
