@@ -1412,16 +1412,17 @@ __global__ void __launch_bounds__(tcb::NTH, 1) gdn_bwd_tc_kernel(
   issue(3, [&] {
     for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(tm + cY, kmaj(sDU, 0, kk), mnmaj(sL, kk), ID_KM, kk > 0);
   });
-  wait(3);
   float sy;
   {
+    float old[16];  // dv before its update, read while the product runs
+#pragma unroll
+    for (int t = 0; t < 16; ++t) old[t] = dv[(row0 + t0 + t) * D + f];
+    wait(3);
     float y[16], vh[16], part[16];
     ld(cY, y);
     ld_row16(sm + offVh, f, t0, vh);
     const float iy = 1.f / (sl * sdu), ivh = 1.f / svh;
-    float mx = 0.f, old[16];
-#pragma unroll
-    for (int t = 0; t < 16; ++t) old[t] = dv[(row0 + t0 + t) * D + f];
+    float mx = 0.f;
 #pragma unroll
     for (int t = 0; t < 16; ++t) {
       y[t] *= iy;
@@ -1511,11 +1512,14 @@ __global__ void __launch_bounds__(tcb::NTH, 1) gdn_bwd_tc_kernel(
     for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(tm + cDkd, mnmaj(sKQ, kk), kmaj(sA, 0, kk), ID_MK, kk > 0);
     for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(tm + cDkd, mnmaj(sKQ, kk), mnmaj(sA, kk), ID_MM, 1);
   });
+  // dq and dk before their updates, read while the products run
+  float oldq[16], oldk[16];
+#pragma unroll
+  for (int t = 0; t < 16; ++t) oldq[t] = dq[(row0 + t0 + t) * D + f], oldk[t] = dk[(row0 + t0 + t) * D + f];
   wait(5);
   {  // dq += scale diag(gamma) dO S0 + scale (dP . R) K
-    float a[16], b[16], old[16];
-#pragma unroll
-    for (int t = 0; t < 16; ++t) old[t] = dq[(row0 + t0 + t) * D + f];
+    float a[16], b[16];
+    float (&old)[16] = oldq;
     ld(cDqA, a);
     ld(cDqB, b);
     const float ios = scale / (so * ss), f2 = scale / (spm * sk);
@@ -1524,9 +1528,8 @@ __global__ void __launch_bounds__(tcb::NTH, 1) gdn_bwd_tc_kernel(
   }
   {  // dk; dG_j -= (U dS_C)_j . K~_j and gamma_j beta_j (Y S0)_j . k_j; the
      // last token gains sum_j (U dS_C)_j . K~_j
-    float acc[16], x[16], part[16], old[16];
-#pragma unroll
-    for (int t = 0; t < 16; ++t) old[t] = dk[(row0 + t0 + t) * D + f];
+    float acc[16], x[16], part[16];
+    float (&old)[16] = oldk;
     const float ik = 1.f / sk;
     float kf[16];
 #pragma unroll
