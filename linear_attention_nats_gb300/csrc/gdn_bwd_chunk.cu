@@ -1191,6 +1191,12 @@ __global__ void __launch_bounds__(tcb::NTH, 1) gdn_bwd_tc_kernel(
   if (tid == 96) prefetch_l2(dv + row0 * D, C * D * 4);
   if (tid == 128) prefetch_l2(dq + row0 * D, C * D * 4);
   if (tid == 160) prefetch_l2(dk + row0 * D, C * D * 4);
+  // and the second group of operand tiles, read after the states' reduction
+  if (tid == 256) prefetch_l2(k + row0 * D, C * D * 2);
+  if (tid == 288) prefetch_l2(q + row0 * D, C * D * 2);
+  if (tid == 320) prefetch_l2(dO + row0 * D, C * D * 4);
+  if (tid == 352) prefetch_l2(Li + (size_t)chunk * C * C, C * C * 4);
+  if (tid == 384) prefetch_l2(Pg + (size_t)chunk * C * C, C * C * 4);
   // and the states of the chunk `ahead` CTAs later (about one SM count: the
   // CTA that starts when one of the running ones ends)
   if (tid == 192 && chunk + ahead < nchunks) prefetch_l2(S0 + (size_t)(chunk + ahead) * D * D, D * D * 4);
