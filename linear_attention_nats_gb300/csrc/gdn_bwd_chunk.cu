@@ -41,7 +41,9 @@
 // operand tiles read through ldmatrix (m16n8k16), each tile scaled by its
 // own power of two so that its largest entry sits below 2^15 (fp16 range is
 // never exceeded, its 11-bit precision matches tf32); the reverse scan keeps
-// its state gradient in fp32 and converts it per step.
+// its state gradient in fp32 and feeds it, X = dS K~^T and dO to the
+// products as fp16 rows, each at its own power-of-two scale (taken within a
+// quad of threads: no block-wide reduction on the chain).
 // The chunk-factor and scan kernels have 8 warps, the fused kernel 16; a C x D
 // output is split into 16-row strips (warp w & 3) and column halves (8
 // warps) or quarters (16 warps) (warp w >> 2).
@@ -545,17 +547,90 @@ __global__ void __launch_bounds__(256) gdn_bwd_prep_kernel(const bf16* __restric
 // ------------------------------------------------------------------ scan
 constexpr int RB = 64;  // state-gradient rows per CTA (BH x D / 64 CTAs: one wave at the layer's sizes)
 
+// acc[j] (rows m0 .. m0 + 15, columns n0 + 8 j .. + 7) += sum_k A(i, k) B(k, n)
+// with A fp32 in shared memory, [m][k] (AT false; row stride = 8 mod 32
+// words: conflict-free 8-byte loads) or [k][m] (AT true; row stride = 4 mod
+// 16 words), and B fp16 as in hmm.  Each row of A enters as fp16 at its own
+// power-of-two scale (the four threads of a quad hold the whole row, so the
+// scale takes two shuffles, no barrier); u_lo and u_hi return the inverse
+// scales of the thread's rows m0 + g and m0 + g + 8, by which the caller
+// multiplies the accumulator rows.
+template <int NT, int K, bool AT, bool BT>
+__device__ __forceinline__ void rmm(float (&acc)[NT][4], float& u_lo, float& u_hi, int m0, int n0, const float* A,
+                                    int lda, const half* B, int ldb) {
+  static_assert(NT % 2 == 0 && K % 16 == 0, "pairs of n8 tiles, k16 blocks");
+  constexpr int KB = K / 16;
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3, mi = lane >> 3, r8 = lane & 7;
+  // x[kb]: row g at k = 2t, 2t + 1, 2t + 8, 2t + 9 of block kb, then row g + 8
+  float x[KB][8];
+  float mlo = 0.f, mhi = 0.f;
+#pragma unroll
+  for (int kb = 0; kb < KB; ++kb) {
+    const int k = 16 * kb + 2 * t;
+    if (!AT) {
+      const float* r_lo = A + (m0 + g) * lda + k;
+      const float* r_hi = A + (m0 + g + 8) * lda + k;
+      const float2 p0 = *(const float2*)r_lo, p1 = *(const float2*)(r_lo + 8);
+      const float2 q0 = *(const float2*)r_hi, q1 = *(const float2*)(r_hi + 8);
+      x[kb][0] = p0.x, x[kb][1] = p0.y, x[kb][2] = p1.x, x[kb][3] = p1.y;
+      x[kb][4] = q0.x, x[kb][5] = q0.y, x[kb][6] = q1.x, x[kb][7] = q1.y;
+    } else {
+      const int kk[4] = {k, k + 1, k + 8, k + 9};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x[kb][e] = A[kk[e] * lda + m0 + g];
+        x[kb][4 + e] = A[kk[e] * lda + m0 + g + 8];
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      mlo = fmaxf(mlo, fabsf(x[kb][e]));
+      mhi = fmaxf(mhi, fabsf(x[kb][4 + e]));
+    }
+  }
+  mlo = fmaxf(mlo, __shfl_xor_sync(0xffffffffu, mlo, 1));
+  mlo = fmaxf(mlo, __shfl_xor_sync(0xffffffffu, mlo, 2));
+  mhi = fmaxf(mhi, __shfl_xor_sync(0xffffffffu, mhi, 1));
+  mhi = fmaxf(mhi, __shfl_xor_sync(0xffffffffu, mhi, 2));
+  const float slo = pow2_scale(mlo), shi = pow2_scale(mhi);
+  u_lo = 1.f / slo;
+  u_hi = 1.f / shi;
+  auto pack = [](float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  };
+#pragma unroll
+  for (int kb = 0; kb < KB; ++kb) {
+    const int k0 = 16 * kb;
+    uint32_t a[4];
+    a[0] = pack(x[kb][0] * slo, x[kb][1] * slo);
+    a[1] = pack(x[kb][4] * shi, x[kb][5] * shi);
+    a[2] = pack(x[kb][2] * slo, x[kb][3] * slo);
+    a[3] = pack(x[kb][6] * shi, x[kb][7] * shi);
+#pragma unroll
+    for (int j = 0; j < NT; j += 2) {
+      uint32_t b[4];
+      if (!BT)
+        ldsm4(B + (n0 + 8 * j + (mi >> 1) * 8 + r8) * ldb + k0 + (mi & 1) * 8, b);
+      else
+        ldsm4t(B + (k0 + (mi & 1) * 8 + r8) * ldb + n0 + 8 * j + (mi >> 1) * 8, b);
+      mma16(acc[j], a, b[0], b[1]);
+      mma16(acc[j + 1], a, b[2], b[3]);
+    }
+  }
+}
+
 template <int D>
 struct ScanSm {
-  static constexpr int kTile = H<D>::bytes(C);          // fp16 [C][D + 8]
-  static constexpr int kO = C * (RB + 4) * 4;            // fp32 [C][RB + 4]: dO columns of the CTA's rows
-  static constexpr int kStage = 3 * kTile + kO;          // K~, W, Q_eff, dO
-  static constexpr int offS = 2 * kStage;                // fp32 [RB][D + 4]: the state gradient
-  static constexpr int offSh = offS + RB * (D + 4) * 4;  // fp16 [RB][D + 8]: its scaled copy
-  static constexpr int offX = offSh + H<D>::bytes(RB);   // fp16 [RB][C + 8]: X = dS K~^T
-  static constexpr int offOh = offX + H<C>::bytes(RB);   // fp16 [C][RB + 8]: dO columns
-  static constexpr int offRed = offOh + H<RB>::bytes(C);
-  static constexpr int kBytes = offRed + 64;
+  static constexpr int kTile = H<D>::bytes(C);   // fp16 [C][D + 8]
+  static constexpr int OL = RB + 4;              // fp32 [C][RB + 4]: dO columns of the CTA's rows
+  static constexpr int kO = C * OL * 4;
+  static constexpr int kStage = 3 * kTile + kO;  // K~, W, Q_eff, dO
+  static constexpr int FS = D + 8;               // fp32 [RB][D + 8]: the state gradient
+  static constexpr int XS = C + 8;               // fp32 [RB][C + 8]: X = -dS K~^T
+  static constexpr int offS = 2 * kStage;
+  static constexpr int offX = offS + RB * FS * 4;
+  static constexpr int kBytes = offX + RB * XS * 4;
 };
 
 
@@ -563,7 +638,13 @@ struct ScanSm {
 // CTA (the rows are independent): dS_C of chunk c is the state gradient
 // before its step; then dS <- gamma_C dS - (dS K~^T) W + dO^T Q_eff for a
 // committed chunk, dS + dO^T Q_eff for a rolled-back one.  dS stays fp32 in
-// shared memory; each step's operands are fp16 tiles at their own scales.
+// shared memory and enters the products as fp16 rows at their own scales, as
+// do X and dO^T; K~, W and Q_eff are the chunk-factor kernel's fp16 tiles at
+// their stored scales.
+// Two barriers a step: the step's stage is complete and the last update
+// visible (then the next stage's copies start: every read of the stage they
+// overwrite is behind that barrier), and X complete.  The update writes the
+// next chunk's dS_C (when it is committed) from registers.
 template <int D>
 __global__ void __launch_bounds__(256) gdn_bwd_scan_kernel(const half* __restrict__ Kt16,
                                                            const half* __restrict__ W16,
@@ -573,17 +654,15 @@ __global__ void __launch_bounds__(256) gdn_bwd_scan_kernel(const half* __restric
                                                            const uint8_t* __restrict__ sel, int L, int N,
                                                            float* __restrict__ dSC) {
   using S = ScanSm<D>;
-  constexpr int FS = D + 4, LD = H<D>::ld, LC = H<C>::ld, LR = H<RB>::ld;
+  constexpr int FS = S::FS, XS = S::XS, OL = S::OL, LD = H<D>::ld;
   extern __shared__ __align__(16) uint8_t sm[];
   float* sdS = (float*)(sm + S::offS);
-  half* hS = (half*)(sm + S::offSh);
-  half* hX = (half*)(sm + S::offX);
-  half* hO = (half*)(sm + S::offOh);
-  float* red = (float*)(sm + S::offRed);
+  float* sX = (float*)(sm + S::offX);
   constexpr int splits = D / RB;
   const long long bh = blockIdx.x / splits;
   const int r0 = (blockIdx.x % splits) * RB;
   const int tid = threadIdx.x, warp = tid >> 5;
+  const int lane = tid & 31, g = lane >> 2, t = lane & 3;
   for (int x = tid; x < RB * FS; x += 256) sdS[x] = 0.f;
   auto stage_ptr = [&](int st, int which) { return sm + st * S::kStage + which * S::kTile; };
   auto prefetch = [&](int c) {
@@ -601,7 +680,7 @@ __global__ void __launch_bounds__(256) gdn_bwd_scan_kernel(const half* __restric
     float* dO_s = (float*)stage_ptr(st, 3);
     for (int x = tid; x < C * RB / 4; x += 256) {
       const int r = x / (RB / 4), c4 = x % (RB / 4);
-      cp16(dO_s + r * (RB + 4) + 4 * c4, dO + (row0 + r) * D + r0 + 4 * c4);
+      cp16(dO_s + r * OL + 4 * c4, dO + (row0 + r) * D + r0 + 4 * c4);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
@@ -613,77 +692,76 @@ __global__ void __launch_bounds__(256) gdn_bwd_scan_kernel(const half* __restric
     float sw, sqe, skt, GC;
   };
   auto step_scalars = [&](int c) {
-    StepScalars t;
+    StepScalars s;
     const long long ch = bh * N + c;
-    t.lin = sel[ch] != 0;
-    t.sw = sc[ch * 4];
-    t.sqe = sc[ch * 4 + 1];
-    t.skt = sc[ch * 4 + 2];
-    t.GC = Gb[(size_t)bh * L + (size_t)c * C + C - 1];
-    return t;
+    s.lin = sel[ch] != 0;
+    s.sw = sc[ch * 4];
+    s.sqe = sc[ch * 4 + 1];
+    s.skt = sc[ch * 4 + 2];
+    s.GC = Gb[(size_t)bh * L + (size_t)c * C + C - 1];
+    return s;
   };
   StepScalars nx = step_scalars(N > 0 ? N - 1 : 0);
   for (int c = N - 1; c >= 0; --c) {
     const StepScalars cur = nx;
     if (c > 0) nx = step_scalars(c - 1);
-    if (c > 0) {
-      prefetch(c - 1);
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
-    } else {
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
+    if (c > 0) prefetch(c - 1);
     const int st = c & 1;
     const half* hKt = (const half*)stage_ptr(st, 0);
     const half* hW = (const half*)stage_ptr(st, 1);
     const half* hQe = (const half*)stage_ptr(st, 2);
     const float* sO = (const float*)stage_ptr(st, 3);
-    const long long ch = bh * N + c;
     const bool lin = cur.lin;
-    const float sw = cur.sw, sqe = cur.sqe, skt = cur.skt;
-    // dS_C of a committed chunk (the last chunk's is zero and is not read),
-    // stored transposed ([dk][dv]) like the chunk-start states: a thread
-    // gathers four consecutive rows of one column into a 16-byte store, a
-    // warp four whole 128-byte lines (32 rows of 4 columns)
-    if (lin && c < N - 1) {
-      float* dst = dSC + (size_t)ch * D * D + r0;
-      for (int x = tid; x < RB * D / 4; x += 256) {
-        const int b = x >> 5, l = x & 31;
-        const int i = 32 * (b % (RB / 32)) + 4 * (l & 7), kc = 4 * (b / (RB / 32)) + (l >> 3);
-        const float* src = sdS + i * FS + kc;
-        *(float4*)(dst + (size_t)kc * D + i) = make_float4(src[0], src[FS], src[2 * FS], src[3 * FS]);
-      }
-    }
-    // the step's dO columns (fp16, scaled)
-    const float so = tile_h<C, RB>(sO, RB + 4, hO, red);
-    float sx = 1.f, sd = 1.f;
-    if (lin) {  // X = dS K~^T (RB x C)
-      sd = tile_h<RB, D>(sdS, FS, hS, red);
-      __syncthreads();
+    if (lin) {  // X = -dS K~^T (RB x C)
       const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);
       float acc[4][4];
       zero(acc);
-      hmm<4, D, false, false>(acc, m0, n0, hS, LD, hKt, LD);
-      const float ix = 1.f / (sd * skt);
-      each_mut(acc, m0, n0, [&](int, int, float v, int, int) { return -v * ix; });
-      sx = acc_h<4, C>(acc, m0, n0, hX, red);
+      float ulo, uhi;
+      rmm<4, D, false, false>(acc, ulo, uhi, m0, n0, sdS, FS, hKt, LD);
+      const float ilo = -ulo / cur.skt, ihi = -uhi / cur.skt;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c0 = n0 + 8 * j + 2 * t;
+        *(float2*)(sX + (m0 + g) * XS + c0) = make_float2(acc[j][0] * ilo, acc[j][1] * ilo);
+        *(float2*)(sX + (m0 + g + 8) * XS + c0) = make_float2(acc[j][2] * ihi, acc[j][3] * ihi);
+      }
     }
     __syncthreads();
-    {  // dS <- gamma_C dS - X W + dO^T Q_eff (committed), dS + dO^T Q_eff (rolled back)
+    {  // dS <- gamma_C dS + X W + dO^T Q_eff (committed), dS + dO^T Q_eff (rolled back)
       constexpr int NT = D / 16;
       const int m0 = 16 * (warp & 3), n0 = (warp >> 2) * (D / 2);
       float a1[NT][4], a2[NT][4];
       zero(a1);
       zero(a2);
-      if (lin) hmm<NT, C, false, true>(a1, m0, n0, hX, LC, hW, LD);
-      hmm<NT, C, true, true>(a2, m0, n0, hO, LR, hQe, LD);
+      float u1[2] = {0.f, 0.f}, u2[2];
+      if (lin) rmm<NT, C, false, true>(a1, u1[0], u1[1], m0, n0, sX, XS, hW, LD);
+      rmm<NT, C, true, true>(a2, u2[0], u2[1], m0, n0, sO, OL, hQe, LD);
       const float gC = lin ? __expf(cur.GC) : 1.f;
-      const float f1 = 1.f / (sx * sw), f2 = 1.f / (so * sqe);
-      each(a1, m0, n0, [&](int i, int n, float v, int j, int e) {
-        sdS[i * FS + n] = gC * sdS[i * FS + n] + v * f1 + a2[j][e] * f2;
-      });
+      const float f1[2] = {u1[0] / cur.sw, u1[1] / cur.sw}, f2[2] = {u2[0] / cur.sqe, u2[1] / cur.sqe};
+      // dS_C of chunk c - 1 (when committed), stored transposed ([dk][dv])
+      // like the chunk-start states: 8 consecutive rows of a column make one
+      // whole 32-byte sector
+      float* dst = (c > 0 && nx.lin) ? dSC + (size_t)(bh * N + c - 1) * D * D + r0 : nullptr;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const int c0 = n0 + 8 * j + 2 * t;
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int i = m0 + g + 8 * hr;
+          float2* p = (float2*)(sdS + i * FS + c0);
+          const float2 o = *p;
+          const float2 v = make_float2(gC * o.x + a1[j][2 * hr] * f1[hr] + a2[j][2 * hr] * f2[hr],
+                                       gC * o.y + a1[j][2 * hr + 1] * f1[hr] + a2[j][2 * hr + 1] * f2[hr]);
+          *p = v;
+          if (dst) {
+            dst[(size_t)c0 * D + i] = v.x;
+            dst[(size_t)(c0 + 1) * D + i] = v.y;
+          }
+        }
+      }
     }
-    __syncthreads();
   }
 }
 
